@@ -1,0 +1,158 @@
+"""CPU fp64 oracle for the paged-KV decode step.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+benchmark's ``cpu_baseline`` / ``--impl reference`` legs may import this
+package.  The product path (``paged_kv_cache_xs_gb300``) never imports it and
+shares no code with it.
+
+The arithmetic lives in ``paged_oracle.c`` (plain C, fp64, OpenMP over
+(sequence, query head)); this module only compiles it with gcc and marshals
+arguments.  Each function follows the definition cited in the C source:
+
+* ``slot_mapping``  - slot resolution of the token a decode step writes
+  ("xserv compare phase10...cf1e9e4", attention.rs,
+  ``reshape_and_cache_batched_bf16``: kv_lens = index of the just-written
+  token + 1).
+* ``kv_append``     - byte copy of each new K/V row into its pool slot (same
+  page, ``reshape_and_cache_bf16`` pool layout).
+* ``paged_decode``  - softmax(scale * q K^T) V over every cached token of the
+  sequence, keys and values gathered through the block table, GQA head map
+  h -> h / (Hq/Hkv) ("xserv compare phase8...phase13", qwen3.rs ``repeat_kv``;
+  "xserv compare phase5...phase9", docs/09-kv-cache.md "After (with cache)").
+
+Parity pins (tests/test_oracle_pins.py) tie these to closed forms,
+hand-derived golden values, an independent dense formulation and
+invariants.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "paged_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
+
+F32 = 0
+BF16 = 1
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False, src: str = _SRC, out: str = _LIB_PATH) -> str:
+    """Compile the oracle C source with gcc (OpenMP, -O2, no -ffast-math)."""
+    if not force and os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(src):
+        return out
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    tmp = out + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared", "-o", tmp, src, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def load(path: str | None = None):
+    """Load (building first if needed) the oracle shared library."""
+    global _lib
+    if path is not None:
+        return _bind(ctypes.CDLL(path))
+    with _lock:
+        if _lib is None:
+            _lib = _bind(ctypes.CDLL(build()))
+    return _lib
+
+
+def _bind(lib):
+    P, I, L, D = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_double
+    lib.oracle_slot_mapping.argtypes = [P, I, P, I, I, L, P]
+    lib.oracle_kv_append.argtypes = [P, P, P, P, P, I, I, I, I, L, I]
+    lib.oracle_paged_decode.argtypes = [P, P, P, P, I, P, I, I, I, I, I, L, D, I, P, I]
+    lib.oracle_max_threads.argtypes = []
+    for f in (lib.oracle_slot_mapping, lib.oracle_kv_append, lib.oracle_paged_decode,
+              lib.oracle_max_threads):
+        f.restype = ctypes.c_int
+    return lib
+
+
+class OracleError(RuntimeError):
+    pass
+
+
+def _check(status: int, what: str) -> None:
+    if status != 0:
+        raise OracleError(f"{what}: oracle status {status}")
+
+
+def _cpu(t: torch.Tensor, dtype=None) -> torch.Tensor:
+    if not isinstance(t, torch.Tensor):
+        t = torch.as_tensor(np.asarray(t))
+    if dtype is not None:
+        t = t.to(dtype)
+    return t.detach().to("cpu").contiguous()
+
+
+def _code(dtype: torch.dtype) -> int:
+    if dtype == torch.float32:
+        return F32
+    if dtype == torch.bfloat16:
+        return BF16
+    raise ValueError(f"oracle supports float32 and bfloat16, not {dtype}")
+
+
+def default_threads() -> int:
+    return len(os.sched_getaffinity(0))
+
+
+def slot_mapping(block_tables, context_lens, block_size: int, num_blocks: int,
+                 lib=None) -> torch.Tensor:
+    """int64 [B] slots of the token each sequence writes this step (-1: none)."""
+    lib = lib or load()
+    bt = _cpu(block_tables, torch.int32)
+    cl = _cpu(context_lens, torch.int32)
+    B = cl.numel()
+    out = torch.empty(B, dtype=torch.int64)
+    st = lib.oracle_slot_mapping(bt.data_ptr(), bt.shape[1] if bt.dim() == 2 else 0,
+                                 cl.data_ptr(), B, block_size, num_blocks, out.data_ptr())
+    _check(st, "slot_mapping")
+    return out
+
+
+def kv_append(k_new, v_new, k_cache, v_cache, slot_mapping, lib=None):
+    """Return copies of (k_cache, v_cache) with the new rows written in."""
+    lib = lib or load()
+    kn, vn = _cpu(k_new), _cpu(v_new)
+    kc, vc = _cpu(k_cache).clone(), _cpu(v_cache).clone()
+    sm = _cpu(slot_mapping, torch.int64)
+    T, Hkv, D = kn.shape
+    num_blocks, _, bs, _ = kc.shape
+    st = lib.oracle_kv_append(kn.data_ptr(), vn.data_ptr(), kc.data_ptr(), vc.data_ptr(),
+                              sm.data_ptr(), T, Hkv, D, bs, num_blocks, _code(kn.dtype))
+    _check(st, "kv_append")
+    return kc, vc
+
+
+def paged_decode(q, k_cache, v_cache, block_tables, context_lens, scale: float,
+                 nthreads: int | None = None, lib=None) -> torch.Tensor:
+    """fp64 [B, Hq, D] attention output of one decode step."""
+    lib = lib or load()
+    qq, kc, vc = _cpu(q), _cpu(k_cache), _cpu(v_cache)
+    bt = _cpu(block_tables, torch.int32)
+    cl = _cpu(context_lens, torch.int32)
+    B, Hq, D = qq.shape
+    num_blocks, Hkv, bs, D2 = kc.shape
+    if D2 != D or kc.dtype != qq.dtype or vc.dtype != qq.dtype:
+        raise ValueError("q and pools must share head_dim and dtype")
+    out = torch.empty(B, Hq, D, dtype=torch.float64)
+    st = lib.oracle_paged_decode(qq.data_ptr(), kc.data_ptr(), vc.data_ptr(), bt.data_ptr(),
+                                 bt.shape[1], cl.data_ptr(), B, Hq, Hkv, D, bs, num_blocks,
+                                 float(scale), _code(qq.dtype), out.data_ptr(),
+                                 nthreads or default_threads())
+    _check(st, "paged_decode")
+    return out

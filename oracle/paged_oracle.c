@@ -1,0 +1,200 @@
+/*
+ * Paged-KV decode oracle: plain, slow, obviously correct CPU code in fp64.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path links, loads or
+ * calls this file; only the tests, the package's smoke check and the
+ * benchmark's CPU-baseline leg do.  It shares no code, header or constant
+ * with the CUDA library: it takes the same raw arrays (pools, block tables,
+ * context lengths, slot mapping, q) and computes the textbook definition.
+ *
+ * Sources (the xserv compare pages):
+ *  - "xserv compare phase10...cf1e9e4", crates/xserv-kernels/src/attention.rs,
+ *    doc comments of `reshape_and_cache_bf16`, `reshape_and_cache_batched_bf16`
+ *    and `paged_decode_attention`: the pool layout
+ *    [num_blocks_total, num_kv_heads, block_size, head_dim], the block table
+ *    [batch, max_blocks_per_seq] (int32), context lengths [batch] (int32) that
+ *    count the just-written token, scale = 1/sqrt(head_dim), output
+ *    [batch, num_q_heads, 1, head_dim].
+ *  - "xserv compare phase5...phase9", docs/09-kv-cache.md, section
+ *    "After (with cache)": a decode step appends the new K/V to the cache and
+ *    attends with one query over all S+1 cached tokens (softmax(q K^T) V).
+ *  - "xserv compare phase8...phase13", crates/xserv-model/src/qwen3.rs,
+ *    `repeat_kv`: query head h reads KV head h / (num_q_heads/num_kv_heads).
+ *
+ * Precision: inputs are widened exactly (bf16 -> fp32 -> fp64 by bit shift);
+ * every sum, the max, exp and the division run in fp64.  Output is fp64.
+ *
+ * Functions return 0 on success and a negative code on invalid input; the
+ * oracle never clamps anything.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORACLE_F32 0
+#define ORACLE_BF16 1
+
+#define ORACLE_OK 0
+#define ORACLE_EINVAL -1
+#define ORACLE_ETABLE -2 /* a position beyond the block table's width   */
+#define ORACLE_EBLOCK -3 /* a physical block id outside [0, num_blocks)  */
+#define ORACLE_ENOMEM -4
+
+/* Exact widening of element idx of a bf16 or fp32 array to double. */
+static double widen(const void *base, int64_t idx, int dtype) {
+    if (dtype == ORACLE_F32) return (double)((const float *)base)[idx];
+    uint32_t bits = (uint32_t)((const uint16_t *)base)[idx] << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+}
+
+static int elem_bytes(int dtype) {
+    if (dtype == ORACLE_F32) return 4;
+    if (dtype == ORACLE_BF16) return 2;
+    return 0;
+}
+
+/*
+ * Slot resolution for one decode step.  context_lens[b] counts the token
+ * being written ("current seq_len + 1 - i.e. the index of the just-written
+ * token + 1", reshape_and_cache_batched_bf16), so the new token's logical
+ * position is p = context_lens[b] - 1 and it lives at
+ *     slot = block_tables[b][p / block_size] * block_size + p % block_size.
+ * A sequence with context_lens[b] <= 0 writes nothing: slot -1.
+ */
+int oracle_slot_mapping(const int32_t *block_tables, int max_blocks_per_seq,
+                        const int32_t *context_lens, int B, int block_size,
+                        int64_t num_blocks, int64_t *slot_mapping) {
+    if (B < 0 || block_size <= 0 || max_blocks_per_seq < 0) return ORACLE_EINVAL;
+    for (int b = 0; b < B; ++b) {
+        int32_t n = context_lens[b];
+        if (n <= 0) {
+            slot_mapping[b] = -1;
+            continue;
+        }
+        int64_t p = (int64_t)n - 1;
+        int64_t logical_block = p / block_size;
+        if (logical_block >= max_blocks_per_seq) return ORACLE_ETABLE;
+        int32_t blk = block_tables[(int64_t)b * max_blocks_per_seq + logical_block];
+        if (blk < 0 || blk >= num_blocks) return ORACLE_EBLOCK;
+        slot_mapping[b] = (int64_t)blk * block_size + p % block_size;
+    }
+    return ORACLE_OK;
+}
+
+/*
+ * KV append: for every token t with slot s = slot_mapping[t] >= 0, copy the
+ * head_dim elements of k_new[t, h, :] into k_cache[s / bs, h, s % bs, :]
+ * (same for V), for every KV head h.  A pure byte copy.
+ * k_new, v_new: [T, Hkv, D]; pools: [num_blocks, Hkv, bs, D].
+ */
+int oracle_kv_append(const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                     const int64_t *slot_mapping, int T, int Hkv, int D, int block_size,
+                     int64_t num_blocks, int dtype) {
+    int eb = elem_bytes(dtype);
+    if (!eb || T < 0 || Hkv <= 0 || D <= 0 || block_size <= 0) return ORACLE_EINVAL;
+    size_t row = (size_t)D * eb;
+    for (int t = 0; t < T; ++t) {
+        int64_t s = slot_mapping[t];
+        if (s < 0) continue;
+        int64_t blk = s / block_size, off = s % block_size;
+        if (blk >= num_blocks) return ORACLE_EBLOCK;
+        for (int h = 0; h < Hkv; ++h) {
+            size_t dst = (size_t)(((blk * Hkv + h) * block_size + off) * D) * eb;
+            size_t src = (size_t)(((int64_t)t * Hkv + h) * D) * eb;
+            memcpy((char *)k_cache + dst, (const char *)k_new + src, row);
+            memcpy((char *)v_cache + dst, (const char *)v_new + src, row);
+        }
+    }
+    return ORACLE_OK;
+}
+
+/*
+ * Paged decode attention, one query token per sequence.
+ *
+ * For sequence b, query head h, KV head g = h / (Hq / Hkv) and each token
+ * t < N = context_lens[b], the key row is found through the block table:
+ *     blk = block_tables[b][t / bs],  K_t = k_cache[blk, g, t % bs, :].
+ * logit_t = scale * sum_d q[b, h, d] * K_t[d]
+ * w_t     = exp(logit_t - max_t' logit_t')
+ * out[b, h, :] = sum_t w_t V_t / sum_t w_t
+ * A sequence with N <= 0 attends to nothing and its output is zero.
+ * q: [B, Hq, D]; out: [B, Hq, D] fp64.
+ */
+int oracle_paged_decode(const void *q, const void *k_cache, const void *v_cache,
+                        const int32_t *block_tables, int max_blocks_per_seq,
+                        const int32_t *context_lens, int B, int Hq, int Hkv, int D,
+                        int block_size, int64_t num_blocks, double scale, int dtype,
+                        double *out, int nthreads) {
+    if (!elem_bytes(dtype) || B < 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || block_size <= 0)
+        return ORACLE_EINVAL;
+    if (Hq % Hkv != 0) return ORACLE_EINVAL;
+    const int group = Hq / Hkv;
+
+    /* Validate every block id that will be read before doing any work. */
+    for (int b = 0; b < B; ++b) {
+        int32_t n = context_lens[b];
+        if (n <= 0) continue;
+        int64_t nblk = ((int64_t)n + block_size - 1) / block_size;
+        if (nblk > max_blocks_per_seq) return ORACLE_ETABLE;
+        for (int64_t i = 0; i < nblk; ++i) {
+            int32_t blk = block_tables[(int64_t)b * max_blocks_per_seq + i];
+            if (blk < 0 || blk >= num_blocks) return ORACLE_EBLOCK;
+        }
+    }
+
+    int status = ORACLE_OK;
+    if (nthreads <= 0) nthreads = 1;
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)
+    for (int64_t bh = 0; bh < (int64_t)B * Hq; ++bh) {
+        int b = (int)(bh / Hq), h = (int)(bh % Hq);
+        int g = h / group;
+        int32_t n = context_lens[b];
+        double *o = out + bh * D;
+        for (int d = 0; d < D; ++d) o[d] = 0.0;
+        if (n <= 0) continue;
+        double *logit = (double *)malloc(sizeof(double) * (size_t)n);
+        if (!logit) {
+#pragma omp atomic write
+            status = ORACLE_ENOMEM;
+            continue;
+        }
+        const int64_t qbase = bh * D;
+        for (int32_t t = 0; t < n; ++t) {
+            int64_t blk = block_tables[(int64_t)b * max_blocks_per_seq + t / block_size];
+            int64_t kbase = ((blk * Hkv + g) * block_size + t % block_size) * D;
+            double dot = 0.0;
+            for (int d = 0; d < D; ++d)
+                dot += widen(q, qbase + d, dtype) * widen(k_cache, kbase + d, dtype);
+            logit[t] = scale * dot;
+        }
+        double mx = logit[0];
+        for (int32_t t = 1; t < n; ++t)
+            if (logit[t] > mx) mx = logit[t];
+        double den = 0.0;
+        for (int32_t t = 0; t < n; ++t) {
+            double w = exp(logit[t] - mx);
+            den += w;
+            int64_t blk = block_tables[(int64_t)b * max_blocks_per_seq + t / block_size];
+            int64_t vbase = ((blk * Hkv + g) * block_size + t % block_size) * D;
+            for (int d = 0; d < D; ++d) o[d] += w * widen(v_cache, vbase + d, dtype);
+        }
+        for (int d = 0; d < D; ++d) o[d] /= den;
+        free(logit);
+    }
+    return status;
+}
+
+/* Number of threads an OpenMP parallel region would use (1 without OpenMP). */
+int oracle_max_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

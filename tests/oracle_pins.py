@@ -1,0 +1,311 @@
+"""Pins that tie the CPU oracle to something other than itself.
+
+Each ``pin_*`` takes a loaded oracle library (the real one, or a deliberately
+broken copy built by test_oracle_mutants.py) and raises AssertionError if the
+oracle disagrees with:
+
+* hand-derived closed forms (tests/golden/hand_worked_cases.txt);
+* an independent dense formulation: pages gathered to a contiguous copy with
+  tensor indexing, K/V repeated over the GQA group (the repeat_kv equivalence
+  of "xserv compare phase8...phase13", qwen3.rs), then torch.softmax and
+  matmul in float64;
+* brute force in pure Python on tiny inputs;
+* invariants: physical-block permutation, constant V, zero query, one
+  dominant key, linearity in V, exact bf16 widening, and the pages' own
+  "cache == recompute" invariant ("xserv compare phase5...phase9",
+  docs/benchmarks/phase9-kv-cache.md, Correctness table).
+"""
+from __future__ import annotations
+
+import math
+import random
+
+import torch
+
+import oracle
+from paged_kv_cache_xs_gb300 import workloads as wl
+from tests import golden_cases as gc
+
+TOL = 1e-12
+
+
+def _close(a: torch.Tensor, b: torch.Tensor, tol: float = TOL, what: str = "") -> None:
+    a = a.to(torch.float64)
+    b = b.to(torch.float64)
+    assert a.shape == b.shape, f"{what}: shape {tuple(a.shape)} vs {tuple(b.shape)}"
+    assert torch.isfinite(a).all(), f"{what}: non-finite oracle output"
+    err = (a - b).abs().max().item() if a.numel() else 0.0
+    assert err <= tol, f"{what}: max-abs error {err:.3e} > {tol:.1e}"
+
+
+def _layer(w: wl.DecodeWorkload, layer: int = 0):
+    return (w.q[layer], w.k_cache[layer], w.v_cache[layer], w.k_new[layer], w.v_new[layer])
+
+
+def dense_reference(q, k_cache, v_cache, block_tables, context_lens, scale) -> torch.Tensor:
+    """softmax(scale * q K^T) V per sequence on a contiguous float64 copy."""
+    B, Hq, D = q.shape
+    _, Hkv, bs, _ = k_cache.shape
+    rep = Hq // Hkv
+    out = torch.zeros(B, Hq, D, dtype=torch.float64)
+    for b in range(B):
+        n = int(context_lens[b])
+        if n <= 0:
+            continue
+        pages = block_tables[b, : (n + bs - 1) // bs].long()
+        K = k_cache[pages].to(torch.float64).permute(0, 2, 1, 3).reshape(-1, Hkv, D)[:n]
+        V = v_cache[pages].to(torch.float64).permute(0, 2, 1, 3).reshape(-1, Hkv, D)[:n]
+        K = K.transpose(0, 1).repeat_interleave(rep, dim=0)      # [Hq, n, D]
+        V = V.transpose(0, 1).repeat_interleave(rep, dim=0)
+        logits = torch.matmul(q[b].to(torch.float64).unsqueeze(1), K.transpose(1, 2)) * scale
+        out[b] = torch.matmul(torch.softmax(logits, dim=-1), V).squeeze(1)
+    return out
+
+
+# ----------------------------------------------------------------- closed forms
+
+def pin_slots_by_hand(lib):
+    c = gc.load_cases()["slots_by_hand"]
+    got = oracle.slot_mapping(torch.tensor(c["block_tables"]), torch.tensor(c["context_lens"]),
+                              c["block_size"], c["num_blocks"], lib=lib)
+    assert got.tolist() == c["expected_slots"], f"slots {got.tolist()}"
+
+
+def _golden_attention(lib, name):
+    c = gc.load_cases()[name]
+    q = torch.tensor(c["q"], dtype=torch.float32)
+    kc, vc = gc.pool_tensor(c, "k_cache"), gc.pool_tensor(c, "v_cache")
+    out = oracle.paged_decode(q, kc, vc, torch.tensor(c["block_tables"]),
+                              torch.tensor(c["context_lens"]), gc.scale_of(c), lib=lib)
+    _close(out, gc.expected_of(c), 1e-14, name)
+
+
+def pin_gqa_paged_by_hand(lib):
+    _golden_attention(lib, "gqa_paged_by_hand")
+
+
+def pin_single_token(lib):
+    _golden_attention(lib, "single_token_is_v_row")
+
+
+# ------------------------------------------------------- independent formulation
+
+def _small_workloads():
+    yield wl.make_workload(0)                                   # fp32 MHA, 8-block pool
+    yield wl.make_workload(wl.custom_config(3, 8, 2, 16, torch.bfloat16, history=("uniform", (0, 70)),
+                                            pool=("factor", 2.0), seed=11))
+    yield wl.make_workload(wl.custom_config(4, 6, 3, 8, torch.float32, history=("uniform", (0, 40)),
+                                            pool=("factor", 1.0), values="uniform", seed=12))
+
+
+def pin_dense_equivalence(lib):
+    for w in _small_workloads():
+        q, kc, vc, _, _ = _layer(w)
+        got = oracle.paged_decode(q, kc, vc, w.block_tables, w.context_lens, w.scale, lib=lib)
+        ref = dense_reference(q, kc, vc, w.block_tables, w.context_lens, w.scale)
+        _close(got, ref, TOL, f"dense {w.cfg.name}")
+
+
+def pin_brute_force_python(lib):
+    rng = random.Random(5)
+    for trial in range(6):
+        B = rng.randint(1, 3)
+        Hkv = rng.choice([1, 2])
+        Hq = Hkv * rng.choice([1, 2])
+        D = rng.choice([4, 8])
+        bs = rng.choice([2, 4, 16])
+        lens = [rng.randint(1, 40) for _ in range(B)]
+        pages = [(n + bs - 1) // bs for n in lens]
+        nblk = sum(pages) + 2
+        perm = list(range(nblk))
+        rng.shuffle(perm)
+        table, pos = [], 0
+        for p in pages:
+            table.append(perm[pos:pos + p] + [-1] * (max(pages) - p))
+            pos += p
+        # Store K/V as a dict keyed by (block, head, offset) in pure Python.
+        kd = {(blk, h, o): [rng.uniform(-2, 2) for _ in range(D)]
+              for blk in range(nblk) for h in range(Hkv) for o in range(bs)}
+        vd = {key: [rng.uniform(-2, 2) for _ in range(D)] for key in kd}
+        qv = [[[rng.uniform(-2, 2) for _ in range(D)] for _ in range(Hq)] for _ in range(B)]
+        scale = 1.0 / math.sqrt(D)
+        kc = torch.zeros(nblk, Hkv, bs, D, dtype=torch.float32)
+        vc = torch.zeros_like(kc)
+        for (blk, h, o), row in kd.items():
+            kc[blk, h, o] = torch.tensor(row)
+        for (blk, h, o), row in vd.items():
+            vc[blk, h, o] = torch.tensor(row)
+        # The Python side used the same fp32-rounded values the oracle sees.
+        for key in kd:
+            kd[key] = kc[key].double().tolist()
+            vd[key] = vc[key].double().tolist()
+        q = torch.tensor(qv, dtype=torch.float32)
+        qv = q.double().tolist()
+        expect = []
+        for b in range(B):
+            rows = []
+            for h in range(Hq):
+                g = h // (Hq // Hkv)
+                keys = [(table[b][t // bs], g, t % bs) for t in range(lens[b])]
+                logits = [scale * sum(a * c for a, c in zip(qv[b][h], kd[key])) for key in keys]
+                top = max(logits)
+                ws = [math.exp(x - top) for x in logits]
+                tot = math.fsum(ws)
+                rows.append([math.fsum(w * vd[key][d] for w, key in zip(ws, keys)) / tot
+                             for d in range(D)])
+            expect.append(rows)
+        got = oracle.paged_decode(q, kc, vc, torch.tensor(table, dtype=torch.int32),
+                                  torch.tensor(lens, dtype=torch.int32), scale, lib=lib)
+        _close(got, torch.tensor(expect, dtype=torch.float64), TOL, f"brute force trial {trial}")
+
+
+# ------------------------------------------------------------------- invariants
+
+def pin_permutation_invariance(lib):
+    w = wl.make_workload(wl.custom_config(3, 8, 4, 32, torch.bfloat16, history=("uniform", (5, 90)),
+                                          pool=("factor", 2.0), seed=21))
+    q, kc, vc, _, _ = _layer(w)
+    base = oracle.paged_decode(q, kc, vc, w.block_tables, w.context_lens, w.scale, lib=lib)
+    g = torch.Generator().manual_seed(3)
+    perm = torch.randperm(w.num_blocks, generator=g)          # new position of each block
+    kc2 = torch.empty_like(kc)
+    vc2 = torch.empty_like(vc)
+    kc2[perm] = kc
+    vc2[perm] = vc
+    bt2 = w.block_tables.clone()
+    used = bt2 >= 0
+    bt2[used] = perm[bt2[used].long()].to(torch.int32)
+    moved = oracle.paged_decode(q, kc2, vc2, bt2, w.context_lens, w.scale, lib=lib)
+    assert torch.equal(base, moved), "permuting physical blocks changed the output"
+
+
+def pin_constant_v(lib):
+    w = wl.make_workload(wl.custom_config(2, 4, 2, 16, torch.float32, history=("uniform", (0, 50)),
+                                          seed=22))
+    q, kc, vc, _, _ = _layer(w)
+    c = torch.linspace(-3, 3, 16)
+    vc = c.expand_as(vc).contiguous()
+    out = oracle.paged_decode(q, kc, vc, w.block_tables, w.context_lens, w.scale, lib=lib)
+    _close(out, c.double().expand_as(out), TOL, "constant V")
+
+
+def _mean_v(vc, block_tables, context_lens, Hq):
+    _, Hkv, bs, D = vc.shape
+    B = context_lens.numel()
+    out = torch.zeros(B, Hq, D, dtype=torch.float64)
+    for b in range(B):
+        n = int(context_lens[b])
+        for h in range(Hq):
+            g = h // (Hq // Hkv)
+            rows = [vc[int(block_tables[b, t // bs]), g, t % bs].double() for t in range(n)]
+            out[b, h] = torch.stack(rows).mean(0)
+    return out
+
+
+def pin_zero_query_mean(lib):
+    w = wl.make_workload(wl.custom_config(3, 6, 2, 8, torch.float32, history=("uniform", (0, 45)),
+                                          seed=23))
+    _, kc, vc, _, _ = _layer(w)
+    q = torch.zeros(w.cfg.B, w.cfg.Hq, w.cfg.D)
+    out = oracle.paged_decode(q, kc, vc, w.block_tables, w.context_lens, w.scale, lib=lib)
+    _close(out, _mean_v(vc, w.block_tables, w.context_lens, w.cfg.Hq), TOL, "q=0 mean")
+    out0 = oracle.paged_decode(w.q[0], kc, vc, w.block_tables, w.context_lens, 0.0, lib=lib)
+    _close(out0, _mean_v(vc, w.block_tables, w.context_lens, w.cfg.Hq), TOL, "scale=0 mean")
+
+
+def pin_dominant_key(lib):
+    # One key gets a logit near 1000 (exp would overflow without the max
+    # subtraction); every other weight is below e^-900, so the output is that
+    # token's V row to double precision.
+    w = wl.make_workload(wl.custom_config(2, 4, 4, 8, torch.float32, history=("fixed", (30,)),
+                                          seed=24))
+    q, kc, vc, _, _ = _layer(w)
+    q = torch.zeros_like(q)
+    q[..., 0] = 1.0
+    kc = kc.clone()
+    kc[..., 0] = 0.0
+    t_star = 17
+    bs = w.cfg.block_size
+    expect = torch.zeros(w.cfg.B, w.cfg.Hq, w.cfg.D, dtype=torch.float64)
+    for b in range(w.cfg.B):
+        blk = int(w.block_tables[b, t_star // bs])
+        kc[blk, :, t_star % bs, 0] = 1000.0
+        expect[b] = vc[blk, :, t_star % bs].double()
+    out = oracle.paged_decode(q, kc, vc, w.block_tables, w.context_lens, 1.0, lib=lib)
+    _close(out, expect, TOL, "dominant key")
+
+
+def pin_linearity_in_v(lib):
+    w = wl.make_workload(wl.custom_config(2, 4, 2, 8, torch.float32, history=("uniform", (3, 60)),
+                                          seed=25))
+    q, kc, vc, _, _ = _layer(w)
+    # Values on a 2^-10 grid in [-2, 2]: every sum below is exact in fp32.
+    vc = torch.round(vc * 1024) / 1024
+    v2 = torch.round(torch.roll(vc, 1, dims=-1) * 512) / 1024
+    a = oracle.paged_decode(q, kc, vc, w.block_tables, w.context_lens, w.scale, lib=lib)
+    b = oracle.paged_decode(q, kc, v2, w.block_tables, w.context_lens, w.scale, lib=lib)
+    s = oracle.paged_decode(q, kc, vc + v2, w.block_tables, w.context_lens, w.scale, lib=lib)
+    _close(s, a + b, 1e-11, "linearity in V")
+
+
+def pin_bf16_widening(lib):
+    w = wl.make_workload(wl.custom_config(2, 4, 2, 16, torch.bfloat16, history=("uniform", (1, 40)),
+                                          seed=26))
+    q, kc, vc, _, _ = _layer(w)
+    a = oracle.paged_decode(q, kc, vc, w.block_tables, w.context_lens, w.scale, lib=lib)
+    b = oracle.paged_decode(q.float(), kc.float(), vc.float(), w.block_tables, w.context_lens,
+                            w.scale, lib=lib)
+    assert torch.equal(a, b), "bf16 widening is not exact"
+
+
+def pin_append_bytes(lib):
+    for dtype in (torch.float32, torch.bfloat16):
+        w = wl.make_workload(wl.custom_config(5, 4, 2, 16, dtype, history=("uniform", (0, 40)),
+                                              pool=("factor", 2.0), seed=27), pool_fill="canary")
+        _, kc, vc, kn, vn = _layer(w)
+        slots = oracle.slot_mapping(w.block_tables, w.context_lens, w.cfg.block_size, w.num_blocks,
+                                    lib=lib)
+        kc2, vc2 = oracle.kv_append(kn, vn, kc, vc, slots, lib=lib)
+        itype = torch.int16 if dtype == torch.bfloat16 else torch.int32
+        bs = w.cfg.block_size
+        ek, ev = kc.clone(), vc.clone()
+        for b in range(w.cfg.B):
+            p = int(w.context_lens[b]) - 1
+            blk = int(w.block_tables[b, p // bs])
+            ek[blk, :, p % bs] = kn[b]
+            ev[blk, :, p % bs] = vn[b]
+        assert torch.equal(kc2.view(itype), ek.view(itype)), "K append bytes differ"
+        assert torch.equal(vc2.view(itype), ev.view(itype)), "V append bytes differ"
+    # Skipped tokens (slot < 0) write nothing.
+    kc3, vc3 = oracle.kv_append(kn, vn, kc, vc, torch.full_like(slots, -1), lib=lib)
+    assert torch.equal(kc3.view(itype), kc.view(itype)) and torch.equal(vc3.view(itype), vc.view(itype))
+
+
+def pin_cache_equals_recompute(lib):
+    w = wl.make_workload(wl.custom_config(4, 8, 2, 32, torch.bfloat16, history=("uniform", (0, 100)),
+                                          pool=("factor", 1.5), seed=28))
+    q, kc, vc, kn, vn = _layer(w)
+    slots = oracle.slot_mapping(w.block_tables, w.context_lens, w.cfg.block_size, w.num_blocks, lib=lib)
+    kc2, vc2 = oracle.kv_append(kn, vn, kc, vc, slots, lib=lib)
+    cached = oracle.paged_decode(q, kc2, vc2, w.block_tables, w.context_lens, w.scale, lib=lib)
+    # Recompute: history gathered from the untouched pool, the new row
+    # appended from k_new/v_new, dense attention on the result.
+    bs, Hkv, D = w.cfg.block_size, w.cfg.Hkv, w.cfg.D
+    rep = w.cfg.Hq // Hkv
+    for b in range(w.cfg.B):
+        hist = int(w.history_lens[b])
+        pages = w.block_tables[b, : (hist + bs - 1) // bs].long()
+        K = kc[pages].double().permute(0, 2, 1, 3).reshape(-1, Hkv, D)[:hist]
+        V = vc[pages].double().permute(0, 2, 1, 3).reshape(-1, Hkv, D)[:hist]
+        K = torch.cat([K, kn[b].double().unsqueeze(0)]).transpose(0, 1).repeat_interleave(rep, 0)
+        V = torch.cat([V, vn[b].double().unsqueeze(0)]).transpose(0, 1).repeat_interleave(rep, 0)
+        att = torch.softmax(torch.matmul(q[b].double().unsqueeze(1), K.transpose(1, 2)) * w.scale, -1)
+        _close(cached[b], torch.matmul(att, V).squeeze(1), TOL, f"cache==recompute seq {b}")
+
+
+ALL_PINS = [
+    pin_slots_by_hand, pin_gqa_paged_by_hand, pin_single_token, pin_dense_equivalence,
+    pin_brute_force_python, pin_permutation_invariance, pin_constant_v, pin_zero_query_mean,
+    pin_dominant_key, pin_linearity_in_v, pin_bf16_widening, pin_append_bytes,
+    pin_cache_equals_recompute,
+]

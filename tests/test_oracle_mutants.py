@@ -1,0 +1,58 @@
+"""Plant plausible mistakes in a copy of the oracle source and check that the
+pin suite catches every one.  The mutants are built in a temporary directory;
+the committed oracle source is never modified."""
+import os
+import tempfile
+
+import pytest
+
+import oracle
+from tests import oracle_pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "paged_oracle.c")
+
+# (name, text to replace, replacement): each is a single plausible bug.
+MUTANTS = [
+    ("gqa_map_modulo", "int g = h / group;", "int g = h % Hkv;"),
+    ("scale_dropped", "logit[t] = scale * dot;", "logit[t] = dot;"),
+    ("last_token_dropped_qk", "for (int32_t t = 0; t < n; ++t) {\n            int64_t blk",
+     "for (int32_t t = 0; t < n - 1; ++t) {\n            int64_t blk"),
+    ("page_index_swapped", "int64_t kbase = ((blk * Hkv + g) * block_size + t % block_size) * D;",
+     "int64_t kbase = ((blk * Hkv + g) * block_size + t / block_size % block_size) * D;"),
+    ("layout_head_block_swapped", "int64_t vbase = ((blk * Hkv + g) * block_size + t % block_size) * D;",
+     "int64_t vbase = ((g * num_blocks + blk) * block_size + t % block_size) * D;"),
+    ("no_max_subtraction", "double w = exp(logit[t] - mx);", "double w = exp(logit[t]);"),
+    ("no_normalisation", "for (int d = 0; d < D; ++d) o[d] /= den;", ""),
+    ("v_read_from_k", "o[d] += w * widen(v_cache, vbase + d, dtype);",
+     "o[d] += w * widen(k_cache, vbase + d, dtype);"),
+    ("bf16_widen_shift", "<< 16;", "<< 15;"),
+    ("slot_position_off_by_one", "int64_t p = (int64_t)n - 1;", "int64_t p = (int64_t)n;"),
+    ("append_rows_swapped", "memcpy((char *)v_cache + dst, (const char *)v_new + src, row);",
+     "memcpy((char *)v_cache + dst, (const char *)k_new + src, row);"),
+    ("append_offset_in_block", "int64_t blk = s / block_size, off = s % block_size;",
+     "int64_t blk = s / block_size, off = 0;"),
+    ("q_head_index", "const int64_t qbase = bh * D;", "const int64_t qbase = (int64_t)b * D;"),
+]
+
+
+def _build_mutant(name, old, new, workdir):
+    text = open(SRC).read()
+    assert text.count(old) >= 1, f"mutation anchor for {name} not found"
+    path = os.path.join(workdir, f"{name}.c")
+    with open(path, "w") as f:
+        f.write(text.replace(old, new))
+    return oracle.load(oracle.build(force=True, src=path, out=os.path.join(workdir, f"lib{name}.so")))
+
+
+@pytest.mark.parametrize("mutant", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_mutant(mutant):
+    name, old, new = mutant
+    with tempfile.TemporaryDirectory() as d:
+        lib = _build_mutant(name, old, new, d)
+        caught = []
+        for pin in oracle_pins.ALL_PINS:
+            try:
+                pin(lib)
+            except Exception:          # an assertion, or an oracle error status
+                caught.append(pin.__name__)
+        assert caught, f"mutant {name} passed every pin"
