@@ -1,0 +1,458 @@
+#!/usr/bin/env python
+"""Decode-step benchmark: KV append + paged decode attention (+ split-K reduce).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config I] [--impl ours|reference]
+
+Prints ONE JSON line (rank 0).  A step is one pass of the whole hot path over
+one batch: for every layer, the paged KV append of the new token of each
+sequence, the split-K paged decode attention and the split-K reduce.  The
+default workload is the large-batch long-context one (128 sequences, contexts
+U[4097, 32769], Qwen3-8B attention shape, bf16, ~17 GB pool): it reads ~9.7 GB
+per step, far more than the 126 MB L2, so no flush is needed between steps.
+
+``--impl reference`` times the CPU fp64 oracle instead (the baseline arm), on
+a bounded sample of the same workload, on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from paged_kv_cache_xs_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "paged decode-attn KV GB/s & % of GB300 HBM peak; sequence-steps/s"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SRC = os.path.join(ROOT, "paged_kv_cache_xs_gb300", "csrc", "paged_decode.cu")
+
+
+# ------------------------------------------------------------------ byte accounting
+
+def step_bytes(cfg: wl.DecodeConfig, context_lens: torch.Tensor) -> dict:
+    """Algorithmic bytes of one layer of the decode step (per the cost model:
+    K and V read once per KV head, not per query head)."""
+    s = torch.tensor([], dtype=cfg.dtype).element_size()
+    n = context_lens.to(torch.int64).clamp(min=0)
+    kv = int(n.sum()) * cfg.Hkv * cfg.D * 2 * s
+    q = cfg.B * cfg.Hq * cfg.D * s
+    out = cfg.B * cfg.Hq * cfg.D * s
+    append = 2 * cfg.B * cfg.Hkv * cfg.D * s * 2
+    tables = int(((n + cfg.block_size - 1) // cfg.block_size).sum()) * 4 + 4 * cfg.B
+    attn = kv + q + tables
+    return {"kv": kv, "attn": attn, "step": attn + out + append}
+
+
+def hbm_peak() -> tuple[float, str]:
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_traffic(workload: str) -> int | None:
+    """Per-launch DRAM bytes of the attention kernel from the committed ncu
+    summary, if it was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", f"paged_decode_attn_{workload}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    sha = hashlib.sha256(open(KERNEL_SRC, "rb").read()).hexdigest()[:16]
+    m_sha = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
+    m_tr = re.search(r"dram_bytes_per_full_launch:\s*([0-9]+)", text)
+    if not m_sha or not m_tr or m_sha.group(1) != sha:
+        return None
+    return int(m_tr.group(1))
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu_index = gpu_index
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+        self.marks = []
+
+    def mark(self):
+        self.marks.append(time.time())
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append({"sm": float(parts[1]), "max": float(parts[2]),
+                             "power": float(parts[3]) if parts[3] not in ("[N/A]", "") else None,
+                             "hw": parts[5], "hw_th": parts[6], "sw_th": parts[7],
+                             "pcap": parts[8]})
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        load = [r for r in rows if r["power"] is None or r["power"] > 0] or rows
+        reasons = set()
+        for r in load:
+            if r["hw"] == "Active":
+                reasons.add("hw_slowdown")
+            if r["hw_th"] == "Active":
+                reasons.add("hw_thermal_slowdown")
+            if r["sw_th"] == "Active":
+                reasons.add("sw_thermal_slowdown")
+            if r["pcap"] == "Active":
+                reasons.add("sw_power_cap")
+        return {"sm_mhz": statistics.median(r["sm"] for r in load),
+                "sm_max_mhz": max(r["max"] for r in load), "reasons": sorted(reasons),
+                "samples": len(load),
+                "power_w_max": max((r["power"] for r in load if r["power"] is not None),
+                                   default=None)}
+
+
+# ------------------------------------------------------------------ distributed
+
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+        return rank, world, local, dist
+    return rank, world, local, None
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def max_over_ranks(x: float, dist) -> float:
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ CPU oracle leg
+
+def oracle_sample(w: wl.DecodeWorkload, seqs: list[int], layer: int = 0):
+    """CPU inputs for the oracle on a subset of sequences: the pre-append
+    pages those sequences use (renumbered), their q and new rows."""
+    bt = w.block_tables[seqs].cpu()
+    lens = w.context_lens[seqs].cpu()
+    ids, rows = [], []
+    for i in range(len(seqs)):
+        p = (int(lens[i]) + 15) // 16
+        rows.append(list(range(len(ids), len(ids) + p)))
+        ids.extend(bt[i, :p].tolist())
+    nbt = torch.full((len(seqs), max(len(r) for r in rows)), -1, dtype=torch.int32)
+    for i, r in enumerate(rows):
+        nbt[i, :len(r)] = torch.tensor(r, dtype=torch.int32)
+    idx = torch.tensor(ids, dtype=torch.long, device=w.k_cache.device)
+    sel = torch.tensor(seqs, dtype=torch.long, device=w.q.device)
+    return dict(q=w.q[layer].index_select(0, sel).cpu(),
+                k_new=w.k_new[layer].index_select(0, sel).cpu(),
+                v_new=w.v_new[layer].index_select(0, sel).cpu(),
+                k_cache=w.k_cache[layer].index_select(0, idx).cpu(),
+                v_cache=w.v_cache[layer].index_select(0, idx).cpu(),
+                block_tables=nbt, context_lens=lens, scale=w.scale)
+
+
+def oracle_step(sample: dict, threads: int):
+    import oracle
+    slots = oracle.slot_mapping(sample["block_tables"], sample["context_lens"], 16,
+                                sample["k_cache"].shape[0])
+    kc, vc = oracle.kv_append(sample["k_new"], sample["v_new"], sample["k_cache"],
+                              sample["v_cache"], slots)
+    return oracle.paged_decode(sample["q"], kc, vc, sample["block_tables"],
+                               sample["context_lens"], sample["scale"], nthreads=threads)
+
+
+def sample_bytes(cfg, sample) -> int:
+    sub = wl.DecodeConfig(**{**cfg.__dict__, "B": len(sample["context_lens"])})
+    return step_bytes(sub, sample["context_lens"])["step"]
+
+
+def pick_sample(w: wl.DecodeWorkload, target_s: float, threads: int, seed: int = 0):
+    """Choose a seeded subset of sequences whose oracle step takes about
+    target_s seconds on `threads` cores (calibrated on two sequences)."""
+    g = torch.Generator().manual_seed(seed)
+    order = torch.randperm(w.cfg.B, generator=g).tolist()
+    cal = oracle_sample(w, order[:min(2, w.cfg.B)])
+    t0 = time.perf_counter()
+    oracle_step(cal, threads)
+    dt = max(time.perf_counter() - t0, 1e-3)
+    tokens_cal = int(cal["context_lens"].sum())
+    lens = w.context_lens.cpu()
+    chosen, tok = [], 0
+    budget = target_s / dt * tokens_cal
+    for b in order:
+        if chosen and tok + int(lens[b]) > budget:
+            break
+        chosen.append(b)
+        tok += int(lens[b])
+    return sorted(chosen)
+
+
+def cpu_baseline(w: wl.DecodeWorkload, target_s: float) -> dict:
+    threads = len(os.sched_getaffinity(0))
+    seqs = pick_sample(w, target_s, threads)
+    sample = oracle_sample(w, seqs)
+    t0 = time.perf_counter()
+    oracle_step(sample, threads)
+    dt = time.perf_counter() - t0
+    gbs = sample_bytes(w.cfg, sample) / dt / 1e9
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "seconds": round(dt, 3),
+            "sample": f"{len(seqs)} of {w.cfg.B} sequences (seeded), all {w.cfg.Hq} query heads, "
+                      f"1 layer: append + fp64 attention over {int(sample['context_lens'].sum())} "
+                      f"tokens"}
+
+
+# ------------------------------------------------------------------ arms
+
+def run_reference(args, rank, world, dist):
+    """The oracle as the baseline arm: each step is the fp64 CPU oracle on a
+    bounded sample of the workload."""
+    if rank != 0:
+        return
+    cfg = wl.CONFIGS[args.config]
+    dev = torch.device("cuda:0") if torch.cuda.is_available() else torch.device("cpu")
+    w = wl.make_workload(cfg, device=dev, layers=1)
+    threads = len(os.sched_getaffinity(0))
+    seqs = pick_sample(w, args.ref_step_seconds, threads)
+    sample = oracle_sample(w, seqs)
+    del w
+    for _ in range(args.warmup):
+        oracle_step(sample, threads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(sample, threads)
+    dt = (time.perf_counter() - t0) / args.steps
+    gbs = sample_bytes(cfg, sample) / dt / 1e9
+    sample_desc = (f"{len(seqs)} of {cfg.B} sequences (seeded) per step, all {cfg.Hq} query heads, "
+                   f"1 layer")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+        "config": {"workload": cfg.name, "B": cfg.B, "Hq": cfg.Hq, "Hkv": cfg.Hkv, "D": cfg.D,
+                   "block_size": cfg.block_size, "layers": cfg.layers, "sample": sample_desc},
+        "seq_steps_per_s": round(len(seqs) / dt, 3),
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": threads,
+                         "kind": "oracle", "sample": sample_desc},
+        "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, rank, world, local, dist):
+    from paged_kv_cache_xs_gb300 import build as xsbuild
+    from paged_kv_cache_xs_gb300 import ops
+    from paged_kv_cache_xs_gb300.step import PagedDecodeStep
+
+    xsbuild.build()
+    ops.load()
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    cfg = wl.CONFIGS[args.config]
+    # Weak scaling: every rank runs its own independent batch of the same shape.
+    w = wl.make_workload(cfg, device=dev, seed=cfg.seed + 7919 * rank)
+    L = cfg.layers
+    step = PagedDecodeStep(cfg.B, cfg.Hq, cfg.Hkv, cfg.D, w.max_blocks_per_seq, cfg.dtype, dev,
+                           total_context_tokens=w.total_context_tokens,
+                           max_context_len=w.max_context_len)
+    out = torch.empty(cfg.B, cfg.Hq, cfg.D, dtype=cfg.dtype, device=dev)
+    stream = torch.cuda.current_stream()
+    by = step_bytes(cfg, w.context_lens.cpu())
+    bytes_per_step = by["step"] * L
+
+    def one_step(ev=None):
+        for layer in range(L):
+            step.append(w.k_new[layer], w.v_new[layer], w.k_cache[layer], w.v_cache[layer],
+                        w.block_tables, w.context_lens)
+            if ev is not None:
+                ev[layer][0].record(stream)
+            step.attend(out, w.q[layer], w.k_cache[layer], w.v_cache[layer], w.block_tables,
+                        w.context_lens, w.scale)
+            if ev is not None:
+                ev[layer][1].record(stream)
+            step.reduce(out, w.context_lens)
+
+    clocks = ClockSampler(local)
+    # Warm-up, then keep the GPU loaded for >= ~1 s so the clock sampler sees it.
+    for _ in range(args.warmup):
+        one_step()
+    torch.cuda.synchronize()
+    t_load = time.time()
+    while time.time() - t_load < args.load_seconds:
+        for _ in range(4):
+            one_step()
+        torch.cuda.synchronize()
+
+    # ---- timed region: exactly K steps
+    attn_ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(L)]
+               for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(dist)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for k in range(args.steps):
+        one_step(attn_ev[k])
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(dist)
+    elapsed_ms = start.elapsed_time(end)
+    attn_ms = [e[0].elapsed_time(e[1]) for ev in attn_ev for e in ev]
+    clock_info = clocks.stop()
+    assert step.error_flags() == 0, f"device error flags {step.error_flags()}"
+
+    max_ms = max_over_ranks(elapsed_ms, dist)
+    ms_per_step = max_ms / args.steps
+    value = world * bytes_per_step / (ms_per_step * 1e-3) / 1e9
+    seq_steps = world * cfg.B * L / (ms_per_step * 1e-3)
+
+    # ---- e2e: through the public API from pinned host buffers, H2D/D2H every step
+    hq = w.q[0].cpu().pin_memory()
+    hk = w.k_new[0].cpu().pin_memory()
+    hv = w.v_new[0].cpu().pin_memory()
+    hbt = w.block_tables.cpu().pin_memory()
+    hcl = w.context_lens.cpu().pin_memory()
+    hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hbt, hcl)) * L
+    d2h = hout.numel() * hout.element_size() * L
+
+    def e2e_step():
+        for layer in range(L):
+            step.run_from_host(hout, hq, hk, hv, hbt, hcl, w.k_cache[layer], w.v_cache[layer],
+                               w.scale)
+
+    for _ in range(2):
+        e2e_step()
+    barrier(dist)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        e2e_step()
+    e2e_s = max_over_ranks(time.perf_counter() - t0, dist) / args.steps
+    e2e_value = world * bytes_per_step / e2e_s / 1e9
+
+    if rank != 0:
+        return
+    peak, peak_kind = hbm_peak()
+    attn_avg_ms = statistics.mean(attn_ms)
+    attn_gbs = by["attn"] / (attn_avg_ms * 1e-3) / 1e9
+    traffic = kernel_traffic(cfg.name)
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if cfg.dtype == torch.bfloat16 else "f32",
+        "data": "synthetic (seeded; lengths, shuffled block order and N(0,1) values drawn "
+                "per the workload recipe)",
+        "config": {"workload": cfg.name, "B": cfg.B, "Hq": cfg.Hq, "Hkv": cfg.Hkv, "D": cfg.D,
+                   "block_size": cfg.block_size, "layers": L, "pool_blocks": w.num_blocks,
+                   "context_tokens": w.total_context_tokens,
+                   "max_context_len": w.max_context_len,
+                   "partition_tokens": step.partition_tokens,
+                   "max_partitions": step.max_partitions,
+                   "l2": f"inputs larger than L2 ({bytes_per_step / 1e9:.2f} GB read per step)",
+                   "parallelism": f"replicas x{world} (independent batches, no collective)"},
+        "seq_steps_per_s": round(seq_steps, 1),
+        "pct_of_hbm_peak": {"of_measured": round(100 * value / world / peak, 2),
+                            "of_nominal_8TBps": round(100 * value / world / NOMINAL_HBM_GBS, 2),
+                            "peak_kind": peak_kind},
+        "roofline": {"kernel": "paged_decode_kernel", "bound": "hbm",
+                     "achieved": round(attn_gbs, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(attn_gbs / peak, 4), "peak_kind": peak_kind,
+                     "traffic": traffic,
+                     "algorithmic_bytes_per_launch": by["attn"],
+                     "avg_launch_ms": round(attn_avg_ms, 4)},
+        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_s * 1e3, 4)},
+        "gpu_launches": args.steps * L * step.launches_per_step,
+        "clocks": clock_info,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", type=int, default=4,
+                    help="workload index (0-4); default: the large-batch long-context one")
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="target duration of the CPU oracle baseline sample")
+    ap.add_argument("--ref-step-seconds", type=float, default=2.0,
+                    help="target duration of one reference-arm step")
+    ap.add_argument("--load-seconds", type=float, default=1.0,
+                    help="untimed load before the timed region (clock sampling)")
+    args = ap.parse_args(argv)
+    args.warmup = max(args.warmup, 3)  # at least 3 untimed warm-up steps
+    rank, world, local, dist = dist_setup(args.gpus)
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world, dist)
+        else:
+            run_ours(args, rank, world, local, dist)
+    finally:
+        if dist is not None:
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

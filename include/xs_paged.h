@@ -1,0 +1,238 @@
+/*
+ * xs_paged.h - C ABI of libxs_paged, the GB300 (sm_103a) decode step over a
+ * paged KV cache: write each running sequence's new K/V token into its page,
+ * then attend with that sequence's single query token over all of its pages.
+ *
+ * The operations follow the xserv inference engine's description of its
+ * paged KV cache ("xserv compare phase10...cf1e9e4",
+ * crates/xserv-kernels/src/attention.rs, the doc comments and extern
+ * signatures of reshape_and_cache_bf16, reshape_and_cache_batched_bf16 and
+ * paged_decode_attention) and of decode attention over a cache
+ * ("xserv compare phase5...phase9", docs/09-kv-cache.md, "After (with
+ * cache)").
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every array argument is a DEVICE pointer owned by the caller.  The
+ *    library never allocates, frees or retains memory; scratch space
+ *    (split-K partials) is passed in by the caller.
+ *  - Work is enqueued asynchronously on the caller's stream; a call returns
+ *    once the launch is queued.  Nothing synchronises the device.
+ *  - Return value: XS_OK (0) or a negative XS_E* code.  Host-visible
+ *    argument errors are detected before anything is launched.  A launch
+ *    failure reports XS_ELAUNCH (the CUDA error is left for
+ *    cudaGetLastError/cudaPeekAtLastError to inspect).
+ *  - Device-side problems (a block id outside the pool, a context length
+ *    beyond the block table) are never trapped: the kernel redirects the
+ *    access to a valid address or skips it, and ORs an XS_FLAG_* bit into
+ *    *err_flag when err_flag is not NULL.  Results are then unspecified for
+ *    the affected sequence only.
+ *  - Layouts (all row-major, contiguous):
+ *      KV pool      [num_blocks, Hkv, block_size, D]   element (blk,h,o,d) at
+ *                   ((blk*Hkv + h)*block_size + o)*D + d
+ *      block_tables int32 [B, max_blocks_per_seq]; row b lists sequence b's
+ *                   physical blocks in logical order; entries past the last
+ *                   page the sequence uses are never read
+ *      context_lens int32 [B]; number of tokens of sequence b INCLUDING the
+ *                   token written this step (the pages' kv_lens: "current
+ *                   seq_len + 1 - i.e., the index of the just-written token
+ *                   + 1")
+ *      q, out       [B, Hq, D] (the pages' [batch, num_q_heads, 1, head_dim])
+ *      k_new, v_new [T, Hkv, D], one row per written token
+ *  - Query head h reads KV head h / (Hq/Hkv) ("xserv compare
+ *    phase8...phase13", crates/xserv-model/src/qwen3.rs, repeat_kv).
+ *  - dtype: XS_F32 or XS_BF16; q, k_new, v_new, pools and out share it.
+ *    Arithmetic is fp32; bf16 outputs are rounded to nearest-even.
+ *  - Supported: block_size 16, D in {64, 128}, Hq/Hkv in {1, 2, 4, 8}.
+ *    Pointers to pools, q, k_new, v_new, out and partials must be 16-byte
+ *    aligned.
+ */
+#ifndef XS_PAGED_H
+#define XS_PAGED_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* dtype codes */
+#define XS_F32 0
+#define XS_BF16 1
+
+/* return codes */
+#define XS_OK 0
+#define XS_ENULL -1        /* a required pointer is NULL                      */
+#define XS_ESHAPE -2       /* a size is negative, zero where it must not be,
+                              Hq % Hkv != 0, or sizes are inconsistent        */
+#define XS_EDTYPE -3       /* dtype is not XS_F32 / XS_BF16                   */
+#define XS_EALIGN -4       /* a pointer is not 16-byte aligned                */
+#define XS_EUNSUPPORTED -5 /* block_size != 16, D not in {64,128},
+                              Hq/Hkv not in {1,2,4,8}                         */
+#define XS_EWORKSPACE -6   /* partials missing or too small for the split    */
+#define XS_ELAUNCH -7      /* a kernel launch failed                          */
+#define XS_EDEVICE -8      /* querying the current device failed              */
+
+/* bits ORed into *err_flag by the kernels */
+#define XS_FLAG_BAD_BLOCK 1 /* a block id outside [0, num_blocks) was met;
+                               block 0 was read instead / the write skipped  */
+#define XS_FLAG_BAD_LEN 2   /* context_lens[b] > max_blocks_per_seq*block_size;
+                               the length was clamped to that bound          */
+#define XS_FLAG_BAD_SLOT 4  /* slot_mapping[t] beyond the pool; write skipped */
+#define XS_FLAG_TIMEOUT 8   /* a bounded wait for staged data gave up; the
+                               kernel drained its copies and returned        */
+
+/*
+ * xs_slot_mapping - where each sequence's new token goes (one decode step).
+ *
+ * For every b with n = context_lens[b] > 0 the new token's logical position
+ * is p = n - 1 and its slot is
+ *     slot_mapping[b] = block_tables[b][p / block_size] * block_size
+ *                       + p % block_size;
+ * sequences with n <= 0 get -1 (nothing to write).  The pages pass
+ * block_tables + kv_lens to their batched append
+ * ("xserv compare phase10...cf1e9e4", attention.rs,
+ * reshape_and_cache_batched_bf16); this call exposes that address step.
+ *
+ * block_tables int32 [B, max_blocks_per_seq]; context_lens int32 [B];
+ * slot_mapping int64 [B] (output).  A position beyond the table width sets
+ * XS_FLAG_BAD_LEN and a block id outside [0, num_blocks) sets
+ * XS_FLAG_BAD_BLOCK; both write slot -1.
+ */
+int xs_slot_mapping(const int32_t *block_tables, int max_blocks_per_seq,
+                    const int32_t *context_lens, int B, int block_size, int64_t num_blocks,
+                    int64_t *slot_mapping, int *err_flag, cudaStream_t stream);
+
+/*
+ * xs_kv_append - scatter T new K/V rows into their pool slots.
+ *
+ *     k_cache[s / bs, h, s % bs, :] = k_new[t, h, :]   (same for V)
+ * for every t < T with s = slot_mapping[t] >= 0 and every KV head h; the
+ * copy is bit-exact.  Follows the pool layout and scatter of
+ * reshape_and_cache_bf16 / reshape_and_cache_batched_bf16
+ * ("xserv compare phase10...cf1e9e4", attention.rs); here the destination
+ * comes from a precomputed slot_mapping so one call serves any token mix.
+ *
+ * k_new, v_new [T, Hkv, D]; k_cache, v_cache [num_blocks, Hkv, bs, D];
+ * slot_mapping int64 [T].  Slots at or beyond num_blocks*bs set
+ * XS_FLAG_BAD_SLOT and are skipped.  Tokens must have distinct slots.
+ */
+int xs_kv_append(const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                 const int64_t *slot_mapping, int T, int Hkv, int D, int block_size,
+                 int64_t num_blocks, int dtype, int *err_flag, cudaStream_t stream);
+
+/*
+ * xs_kv_append_paged - the decode-step append with slot resolution fused in:
+ * writes k_new[b] / v_new[b] ([B, Hkv, D]) at position context_lens[b] - 1
+ * of sequence b, located through block_tables exactly as xs_slot_mapping
+ * does.  This is the pages' reshape_and_cache_batched_bf16 ("xserv compare
+ * phase10...cf1e9e4", attention.rs: "same buffer the paged-attention kernel
+ * reads").  Errors as xs_slot_mapping; bad entries are skipped.
+ */
+int xs_kv_append_paged(const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                       const int32_t *block_tables, int max_blocks_per_seq,
+                       const int32_t *context_lens, int B, int Hkv, int D, int block_size,
+                       int64_t num_blocks, int dtype, int *err_flag, cudaStream_t stream);
+
+/*
+ * xs_paged_decode_partition_tokens - host-only heuristic for the split-K
+ * partition size (tokens, a multiple of 16) of xs_paged_decode_attn.
+ *
+ * Each sequence's context is cut into partitions of this many tokens; one
+ * work item is (sequence, KV head, partition).  The size is the largest
+ * power of two in [16, 2048] that still gives at least ~6 work items per
+ * resident CTA on num_sms SMs, so a persistent grid stays busy to the end.
+ * total_context_tokens = sum of context_lens (pass <= 0 if unknown:
+ * B * max_context_len is used).  Returns the partition size (>= 16), or a
+ * negative XS_E* code.
+ */
+int xs_paged_decode_partition_tokens(int B, int Hkv, int64_t total_context_tokens,
+                                     int max_context_len, int num_sms);
+
+/*
+ * xs_paged_decode_max_partitions - partitions a sequence can need: the
+ * ceiling of max_blocks_per_seq*block_size / partition_tokens.
+ */
+int xs_paged_decode_max_partitions(int max_blocks_per_seq, int block_size, int partition_tokens);
+
+/*
+ * xs_paged_decode_workspace_bytes - bytes of fp32 partials for the split:
+ * part_o [B, Hq, max_partitions, D], part_m and part_l [B, Hq,
+ * max_partitions], each rounded up to 256 bytes (the caller may carve one
+ * buffer: part_o at 0, part_m and part_l after it).
+ */
+size_t xs_paged_decode_workspace_bytes(int B, int Hq, int D, int max_partitions);
+
+/*
+ * xs_paged_decode_attn - paged decode attention, split-K partition pass.
+ *
+ * For sequence b, query head h, KV head g = h / (Hq/Hkv), tokens
+ * t < N = context_lens[b] gathered through the page table
+ * (K_t = k_cache[block_tables[b][t / bs], g, t % bs, :]):
+ *     out[b, h, :] = sum_t softmax_t(scale * q[b, h, :] . K_t) V_t
+ * ("xserv compare phase10...cf1e9e4", attention.rs, paged_decode_attention
+ * and its launch_paged_decode_attention_bf16 signature; the softmax over all
+ * cached tokens from "xserv compare phase5...phase9", docs/09-kv-cache.md).
+ *
+ * Work split: every (b, g, partition p) covers tokens
+ * [p*P, min(N, (p+1)*P)) with P = partition_tokens (a multiple of 16) and
+ * computes all Hq/Hkv query heads of group g from one read of each page.
+ *  - A sequence with one partition (N <= P) gets its final out[b] written
+ *    here.
+ *  - A sequence with more partitions gets fp32 partials instead:
+ *      part_o[b, h, p, :] = sum_t w_t V_t / l,  part_l[b, h, p] = l = sum_t w_t,
+ *      part_m[b, h, p] = max_t logit_t * log2(e)  (w_t = 2^(logit_t*log2 e - m));
+ *    xs_paged_decode_reduce then writes out[b].
+ *  - A sequence with N <= 0 gets out[b] = 0.
+ * max_partitions must be >= xs_paged_decode_max_partitions(...); part_* may
+ * be NULL only when max_partitions == 1.
+ *
+ * q [B, Hq, D]; out [B, Hq, D]; k_cache, v_cache [num_blocks, Hkv, bs, D];
+ * block_tables int32 [B, max_blocks_per_seq]; context_lens int32 [B].
+ * Device-side errors: XS_FLAG_BAD_BLOCK, XS_FLAG_BAD_LEN, XS_FLAG_TIMEOUT.
+ */
+int xs_paged_decode_attn(void *out, float *part_o, float *part_m, float *part_l,
+                         const void *q, const void *k_cache, const void *v_cache,
+                         const int32_t *block_tables, int max_blocks_per_seq,
+                         const int32_t *context_lens, int B, int Hq, int Hkv, int D,
+                         int block_size, int64_t num_blocks, float scale,
+                         int partition_tokens, int max_partitions, int dtype, int *err_flag,
+                         cudaStream_t stream);
+
+/*
+ * xs_paged_decode_reduce - split-K combine.  For every sequence with more
+ * than one partition and every query head, merges the partials by their
+ * log-sum-exp weights:
+ *     M = max_i m_i,  L = sum_i l_i 2^(m_i - M),
+ *     out = sum_i l_i 2^(m_i - M) o_i / L
+ * and writes out[b, h, :] in dtype.  Sequences with one partition or none
+ * are left as xs_paged_decode_attn wrote them.  Arguments as in
+ * xs_paged_decode_attn; partials are read only.
+ */
+int xs_paged_decode_reduce(void *out, const float *part_o, const float *part_m,
+                           const float *part_l, const int32_t *context_lens, int B, int Hq,
+                           int D, int partition_tokens, int max_partitions, int dtype,
+                           cudaStream_t stream);
+
+/*
+ * xs_paged_decode - xs_paged_decode_attn followed, when max_partitions > 1,
+ * by xs_paged_decode_reduce on the same stream.
+ */
+int xs_paged_decode(void *out, float *part_o, float *part_m, float *part_l, const void *q,
+                    const void *k_cache, const void *v_cache, const int32_t *block_tables,
+                    int max_blocks_per_seq, const int32_t *context_lens, int B, int Hq, int Hkv,
+                    int D, int block_size, int64_t num_blocks, float scale, int partition_tokens,
+                    int max_partitions, int dtype, int *err_flag, cudaStream_t stream);
+
+/*
+ * xs_version - library version as MAJOR*10000 + MINOR*100 + PATCH.
+ */
+int xs_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* XS_PAGED_H */

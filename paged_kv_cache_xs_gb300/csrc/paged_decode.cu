@@ -1,0 +1,722 @@
+// Paged decode attention for GB300 (sm_103a): one query token per sequence
+// attends over all of that sequence's K/V pages, gathered through its block
+// table; query heads of a GQA group share every page read.
+//
+// Definition ("xserv compare phase10...cf1e9e4", crates/xserv-kernels/src/
+// attention.rs, paged_decode_attention; "xserv compare phase5...phase9",
+// docs/09-kv-cache.md, "After (with cache)"):
+//     out[b,h,:] = sum_t softmax_t(scale * q[b,h,:] . K[b,t]) V[b,t]
+// with K[b,t] = k_cache[block_tables[b][t/16], h/(Hq/Hkv), t%16, :].
+//
+// Design (flash-decoding, persistent, warp-specialised):
+//  * Work item = (sequence b, KV head g, partition p of P tokens).  Items are
+//    numbered by a per-CTA prefix sum over context_lens and dealt to a
+//    persistent grid round-robin; all items have the same size except a
+//    sequence's last one, so the grid drains evenly.
+//  * Warp 0 is the producer: it reads block ids (32 at a time, coalesced) and
+//    streams each page pair (K page + V page of head g, 16 tokens x D, one
+//    contiguous run per the pool layout) into an S-stage shared-memory ring
+//    with 1-D bulk copies (cp.async.bulk) completing on mbarriers.  It also
+//    stages the G query rows of each item into a double-buffered q slot.
+//  * Warps 1..4 are consumers.  Consumer c takes ring pages c, c+4, ... and
+//    keeps its own online-softmax state (running max m, sum l, output o) for
+//    all G heads.  QK: 8 lanes per token x 4 tokens per pass, each lane a
+//    D/8 slice of the row, reduce-scatter over the 8 lanes so each lane ends
+//    with one head's score.  PV: each lane owns D/32 output dims for all G
+//    heads; weights are broadcast through a per-warp shared buffer.
+//  * At the end of an item the four consumer states are merged in shared
+//    memory; the item writes the final bf16/fp32 output (single-partition
+//    sequence) or fp32 partials (o, m, l) for the split-K reduce.
+//  * Logits are kept in base-2 units (q is pre-scaled by scale*log2(e)) so
+//    exponentials are single ex2 instructions.
+#include <algorithm>
+#include <mutex>
+
+#include "xs_common.cuh"
+
+namespace xs {
+namespace attn {
+
+constexpr int kBlock = 16;          // tokens per page
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = 32 * (kConsumerWarps + 1);
+constexpr int kStages = 8;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s per bounded wait
+constexpr int kMaxBatch = 16384;                  // prefix sums live in shared memory
+
+template <typename T, int D, int G>
+struct Cfg {
+    static constexpr int kRowBytes = D * static_cast<int>(sizeof(T));
+    static constexpr int kPageBytes = kBlock * kRowBytes;
+    static constexpr int kChunksPerRow = kRowBytes / 16;
+    static constexpr int kChunksPerLane = kChunksPerRow / 8;   // QK: 8 lanes per token
+    static constexpr int kElemsPerChunk = 16 / static_cast<int>(sizeof(T));
+    static constexpr int kQkDims = kChunksPerLane * kElemsPerChunk;  // = D / 8
+    static constexpr int kPvDims = D / 32;                           // PV dims per lane
+    static constexpr int kPvBytes = kPvDims * static_cast<int>(sizeof(T));
+    static constexpr int kQBytes = G * kRowBytes;
+    static constexpr int kLogG = G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : 3;
+    static constexpr int kHeadShift = 3 - kLogG;  // lane j of a token group owns head j >> shift
+    // Shared memory carve-up (bytes).
+    static constexpr int kRingBytes = kStages * 2 * kPageBytes;
+    static constexpr int kQSlotOff = kRingBytes;
+    static constexpr int kWOff = kQSlotOff + 2 * kQBytes;
+    static constexpr int kWBytes = kConsumerWarps * kBlock * G * 4;
+    static constexpr int kCombOff = kWOff + kWBytes;
+    static constexpr int kCombBytes = kConsumerWarps * G * (D + 2) * 4;
+    static constexpr int kBarOff = (kCombOff + kCombBytes + 7) / 8 * 8;
+    static constexpr int kBarBytes = (2 * kStages + 4) * 8;
+    static constexpr int kPrefixOff = kBarOff + kBarBytes;
+    static __host__ __device__ constexpr int smem_bytes(int B) { return kPrefixOff + 4 * (B + 1); }
+    static_assert(kChunksPerLane >= 1 && kChunksPerRow % 8 == 0, "row must split over 8 lanes");
+    static_assert(D % 32 == 0, "D must split over 32 lanes");
+};
+
+struct Params {
+    void *out;
+    float *part_o, *part_m, *part_l;
+    const void *q, *k_cache, *v_cache;
+    const int32_t *block_tables, *context_lens;
+    int max_blocks, B, Hq, Hkv, P, max_parts;
+    int64_t num_blocks;
+    float qscale;  // scale * log2(e)
+    int *err_flag;
+};
+
+// Number of tokens sequence b attends to, clamped to the table's reach.
+__device__ __forceinline__ int seq_len(const Params &p, int b, bool report) {
+    int n = p.context_lens[b];
+    const int cap = p.max_blocks * kBlock;
+    if (n > cap) {
+        if (report) raise_flag(p.err_flag, XS_FLAG_BAD_LEN);
+        n = cap;
+    }
+    return n;
+}
+
+struct Item {
+    int b, g, part, n, tok0, tok1, pg0, pg1;
+};
+
+__device__ __forceinline__ Item decode_item(const Params &p, const int *prefix, int item) {
+    // Largest b with prefix[b] <= item.
+    int lo = 0, hi = p.B - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (prefix[mid] <= item) lo = mid; else hi = mid - 1;
+    }
+    Item it;
+    it.b = lo;
+    const int r = item - prefix[lo];
+    const int nparts = (prefix[lo + 1] - prefix[lo]) / p.Hkv;
+    it.g = r / nparts;
+    it.part = r - it.g * nparts;
+    it.n = seq_len(p, lo, false);
+    it.tok0 = it.part * p.P;
+    it.tok1 = min(it.n, it.tok0 + p.P);
+    it.pg0 = it.tok0 / kBlock;
+    it.pg1 = (it.tok1 + kBlock - 1) / kBlock;
+    return it;
+}
+
+template <typename T, int D, int G>
+__global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const Params p) {
+    using C = Cfg<T, D, G>;
+    extern __shared__ __align__(128) unsigned char smem[];
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::kBarOff);
+    uint64_t *empty = full + kStages;
+    uint64_t *qfull = empty + kStages;
+    uint64_t *qempty = qfull + 2;
+    int *prefix = reinterpret_cast<int *>(smem + C::kPrefixOff);
+    __shared__ int s_abort, s_stop;
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+
+    // ---- prologue: barriers, item prefix sums, zero outputs of empty sequences
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&qfull[s], 1);
+            mbar_init(&qempty[s], kConsumerWarps);
+        }
+        mbar_fence_init();
+        s_abort = 0;
+        s_stop = 0;
+    }
+    {
+        // Items of sequence b: ceil(n/P) partitions x Hkv heads.  Chunked scan.
+        const int per = (p.B + kThreads - 1) / kThreads;
+        const int b0 = min(p.B, tid * per), b1 = min(p.B, b0 + per);
+        int local = 0;
+        for (int b = b0; b < b1; ++b) {
+            const int n = seq_len(p, b, blockIdx.x == 0);
+            local += (n > 0 ? (n + p.P - 1) / p.P : 0) * p.Hkv;
+        }
+        // Inclusive scan of `local` over the block (warp shuffles + one pass over warps).
+        int x = local;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        __shared__ int warp_tot[kThreads / 32];
+        if (lane == 31) warp_tot[warp] = x;
+        __syncthreads();
+        int base = 0;
+        for (int w = 0; w < warp; ++w) base += warp_tot[w];
+        int run = base + x - local;  // exclusive prefix of this thread's range
+        for (int b = b0; b < b1; ++b) {
+            prefix[b] = run;
+            const int n = seq_len(p, b, false);
+            run += (n > 0 ? (n + p.P - 1) / p.P : 0) * p.Hkv;
+        }
+        if (tid == kThreads - 1) prefix[p.B] = base + x;
+    }
+    // Sequences with no tokens produce zeros.
+    for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
+        if (p.context_lens[b] > 0) continue;
+        T *o = static_cast<T *>(p.out) + static_cast<int64_t>(b) * p.Hq * D;
+        for (int i = tid; i < p.Hq * D; i += kThreads) o[i] = Elem<T>::from_f32(0.f);
+    }
+    __syncthreads();
+    const int total_items = prefix[p.B];
+
+    if (warp == 0) {
+        // ================================================================ producer
+        const uint64_t pol = policy_evict_first();
+        const unsigned char *kbase = static_cast<const unsigned char *>(p.k_cache);
+        const unsigned char *vbase = static_cast<const unsigned char *>(p.v_cache);
+        const unsigned char *qbase = static_cast<const unsigned char *>(p.q);
+        uint32_t page_ctr = 0, item_ctr = 0;
+        bool ok = true;
+        for (int item = blockIdx.x; ok && item < total_items; item += gridDim.x, ++item_ctr) {
+            const Item it = decode_item(p, prefix, item);
+            if (lane == 0) {
+                const uint32_t slot = item_ctr & 1, k = item_ctr >> 1;
+                ok = mbar_wait_bounded(&qempty[slot], (k & 1) ^ 1, kWaitLimitNs);
+                if (ok) {
+                    unsigned char *dst = smem + C::kQSlotOff + slot * C::kQBytes;
+                    const int64_t qoff =
+                        (static_cast<int64_t>(it.b) * p.Hq + static_cast<int64_t>(it.g) * G) *
+                        C::kRowBytes;
+                    mbar_arrive_expect_tx(&qfull[slot], C::kQBytes);
+                    bulk_g2s(dst, qbase + qoff, C::kQBytes, &qfull[slot]);
+                }
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            const int32_t *row = p.block_tables + static_cast<int64_t>(it.b) * p.max_blocks;
+            for (int base = it.pg0; ok && base < it.pg1; base += 32) {
+                int32_t blk = 0;
+                const int pg = base + lane;
+                if (pg < it.pg1) {
+                    blk = row[pg];
+                    if (blk < 0 || blk >= p.num_blocks) {
+                        raise_flag(p.err_flag, XS_FLAG_BAD_BLOCK);
+                        blk = 0;
+                    }
+                }
+                const int cnt = min(32, it.pg1 - base);
+                for (int i = 0; i < cnt; ++i) {
+                    const int32_t bi = __shfl_sync(0xffffffffu, blk, i);
+                    if (lane == 0) {
+                        const uint32_t s = page_ctr % kStages, k = page_ctr / kStages;
+                        ok = mbar_wait_bounded(&empty[s], (k & 1) ^ 1, kWaitLimitNs);
+                        if (ok) {
+                            unsigned char *dk = smem + s * 2 * C::kPageBytes;
+                            const int64_t off =
+                                (static_cast<int64_t>(bi) * p.Hkv + it.g) * C::kPageBytes;
+                            mbar_arrive_expect_tx(&full[s], 2 * C::kPageBytes);
+                            bulk_g2s(dk, kbase + off, C::kPageBytes, &full[s], pol);
+                            bulk_g2s(dk + C::kPageBytes, vbase + off, C::kPageBytes, &full[s], pol);
+                        }
+                    }
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    if (!ok) break;
+                    ++page_ctr;  // pages issued so far
+                }
+            }
+        }
+        if (!ok && lane == 0) {
+            raise_flag(p.err_flag, XS_FLAG_TIMEOUT);
+            atomicExch(&s_abort, 1);
+            // Drain: let every copy this CTA issued land before the CTA exits.
+            const uint32_t first = page_ctr > kStages ? page_ctr - kStages : 0;
+            for (uint32_t c = first; c < page_ctr; ++c)
+                mbar_wait_bounded(&full[c % kStages], (c / kStages) & 1, kWaitLimitNs);
+        }
+        return;
+    }
+
+    // ==================================================================== consumers
+    const int cw = warp - 1;
+    const int tg = lane >> 3, j = lane & 7;
+    const int own_head = j >> C::kHeadShift;
+    float *Wbuf = reinterpret_cast<float *>(smem + C::kWOff) + cw * kBlock * G;
+    float *cM = reinterpret_cast<float *>(smem + C::kCombOff);
+    float *cL = cM + kConsumerWarps * G;
+    float *cO = cL + kConsumerWarps * G;
+    const int ctid = tid - 32;
+    uint32_t page_ctr = 0, item_ctr = 0;
+
+    for (int item = blockIdx.x; item < total_items; item += gridDim.x, ++item_ctr) {
+        const Item it = decode_item(p, prefix, item);
+        // ---- q rows of the group (scaled into base-2 logits)
+        // A failed wait marks the item bad: the warp skips its pages but still
+        // takes part in both merge barriers, so no consumer is left waiting.
+        bool bad = false;
+        float qf[G][C::kQkDims];
+        {
+            const uint32_t slot = item_ctr & 1, k = item_ctr >> 1;
+            bad = !__all_sync(0xffffffffu, mbar_wait_bounded(&qfull[slot], k & 1, kWaitLimitNs));
+            const unsigned char *qs = smem + C::kQSlotOff + slot * C::kQBytes;
+#pragma unroll
+            for (int h = 0; h < G; ++h)
+#pragma unroll
+                for (int c = 0; c < C::kChunksPerLane; ++c) {
+                    const uint4 raw = *reinterpret_cast<const uint4 *>(
+                        qs + h * C::kRowBytes + (j + 8 * c) * 16);
+                    float f[C::kElemsPerChunk];
+                    unpack16(raw, f, static_cast<T *>(nullptr));
+#pragma unroll
+                    for (int e = 0; e < C::kElemsPerChunk; ++e)
+                        qf[h][c * C::kElemsPerChunk + e] = f[e] * p.qscale;
+                }
+            __syncwarp();
+            if (lane == 0 && !bad) mbar_arrive(&qempty[slot]);
+        }
+
+        float m_own = -INFINITY, l_own = 0.f;
+        float o[G][C::kPvDims];
+#pragma unroll
+        for (int h = 0; h < G; ++h)
+#pragma unroll
+            for (int d = 0; d < C::kPvDims; ++d) o[h][d] = 0.f;
+
+        for (int pg = it.pg0; pg < it.pg1 && !bad; ++pg, ++page_ctr) {
+            if ((page_ctr % kConsumerWarps) != static_cast<uint32_t>(cw)) continue;
+            const uint32_t s = page_ctr % kStages, k = page_ctr / kStages;
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(&full[s], k & 1, kWaitLimitNs)) ||
+                *static_cast<volatile int *>(&s_abort)) {
+                bad = true;
+                break;
+            }
+            const unsigned char *Ks = smem + s * 2 * C::kPageBytes;
+            const unsigned char *Vs = Ks + C::kPageBytes;
+            const int n_valid = min(kBlock, it.tok1 - pg * kBlock);
+
+            // ---- QK: 4 passes x 4 tokens; lane (tg, j) covers dims of chunks j, j+8, ...
+            float sc[4];
+#pragma unroll
+            for (int pass = 0; pass < 4; ++pass) {
+                const int t = pass * 4 + tg;
+                float2 acc[G];
+#pragma unroll
+                for (int h = 0; h < G; ++h) acc[h] = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int c = 0; c < C::kChunksPerLane; ++c) {
+                    const uint4 raw =
+                        *reinterpret_cast<const uint4 *>(Ks + t * C::kRowBytes + (j + 8 * c) * 16);
+                    float f[C::kElemsPerChunk];
+                    unpack16(raw, f, static_cast<T *>(nullptr));
+#pragma unroll
+                    for (int e = 0; e < C::kElemsPerChunk; e += 2) {
+                        const float2 kv = make_float2(f[e], f[e + 1]);
+#pragma unroll
+                        for (int h = 0; h < G; ++h) {
+                            const float2 qv = make_float2(qf[h][c * C::kElemsPerChunk + e],
+                                                          qf[h][c * C::kElemsPerChunk + e + 1]);
+                            acc[h] = __ffma2_rn(qv, kv, acc[h]);
+                        }
+                    }
+                }
+                float v[G];
+#pragma unroll
+                for (int h = 0; h < G; ++h) v[h] = acc[h].x + acc[h].y;
+                // Reduce-scatter over the 8 lanes of the token group.
+                int cnt = G;
+#pragma unroll
+                for (int mask = 4; mask >= 1; mask >>= 1) {
+                    if (cnt > 1) {
+                        const int half = cnt >> 1;
+                        const bool upper = (lane & mask) != 0;
+#pragma unroll
+                        for (int i = 0; i < G / 2; ++i) {
+                            if (i < half) {
+                                const float send = upper ? v[i] : v[i + half];
+                                const float keep = upper ? v[i + half] : v[i];
+                                v[i] = keep + __shfl_xor_sync(0xffffffffu, send, mask);
+                            }
+                        }
+                        cnt = half;
+                    } else {
+                        v[0] += __shfl_xor_sync(0xffffffffu, v[0], mask);
+                    }
+                }
+                sc[pass] = (t < n_valid) ? v[0] : -INFINITY;
+            }
+
+            // ---- online softmax for head own_head (lanes sharing j agree)
+            float pm = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
+            pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 8));
+            pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 16));
+            const float m_new = fmaxf(m_own, pm);
+            const float corr_own = fast_exp2(m_own - m_new);
+            m_own = m_new;
+            float w[4], ps = 0.f;
+#pragma unroll
+            for (int pass = 0; pass < 4; ++pass) {
+                w[pass] = fast_exp2(sc[pass] - m_new);
+                ps += w[pass];
+            }
+            ps += __shfl_xor_sync(0xffffffffu, ps, 8);
+            ps += __shfl_xor_sync(0xffffffffu, ps, 16);
+            l_own = l_own * corr_own + ps;
+            if ((j & ((1 << C::kHeadShift) - 1)) == 0) {
+#pragma unroll
+                for (int pass = 0; pass < 4; ++pass) Wbuf[(pass * 4 + tg) * G + own_head] = w[pass];
+            }
+            float corr[G];
+#pragma unroll
+            for (int h = 0; h < G; ++h)
+                corr[h] = __shfl_sync(0xffffffffu, corr_own, h << C::kHeadShift);
+            __syncwarp();
+
+            // ---- PV: lane owns dims [lane*kPvDims, +kPvDims) of every head
+#pragma unroll
+            for (int h = 0; h < G; ++h)
+#pragma unroll
+                for (int d = 0; d < C::kPvDims; ++d) o[h][d] *= corr[h];
+            for (int t = 0; t < n_valid; ++t) {
+                float vf[C::kPvDims];
+                const unsigned char *src = Vs + t * C::kRowBytes + lane * C::kPvBytes;
+                if constexpr (C::kPvBytes == 4) {
+                    const uint32_t raw = *reinterpret_cast<const uint32_t *>(src);
+                    if constexpr (sizeof(T) == 2) {
+                        vf[0] = __uint_as_float(raw << 16);
+                        vf[1] = __uint_as_float(raw & 0xffff0000u);
+                    } else {
+                        vf[0] = __uint_as_float(raw);
+                    }
+                } else if constexpr (C::kPvBytes == 8) {
+                    const uint2 raw = *reinterpret_cast<const uint2 *>(src);
+                    if constexpr (sizeof(T) == 2) {
+                        vf[0] = __uint_as_float(raw.x << 16);
+                        vf[1] = __uint_as_float(raw.x & 0xffff0000u);
+                        vf[2] = __uint_as_float(raw.y << 16);
+                        vf[3] = __uint_as_float(raw.y & 0xffff0000u);
+                    } else {
+                        vf[0] = __uint_as_float(raw.x);
+                        vf[1] = __uint_as_float(raw.y);
+                    }
+                } else {
+                    const uint4 raw = *reinterpret_cast<const uint4 *>(src);
+                    unpack16(raw, vf, static_cast<T *>(nullptr));
+                }
+                float wt[G];
+#pragma unroll
+                for (int h = 0; h < G; ++h) wt[h] = Wbuf[t * G + h];
+#pragma unroll
+                for (int h = 0; h < G; ++h)
+#pragma unroll
+                    for (int d = 0; d < C::kPvDims; d += 2) {
+                        if constexpr (C::kPvDims >= 2) {
+                            float2 acc = make_float2(o[h][d], o[h][d + 1]);
+                            acc = __ffma2_rn(make_float2(wt[h], wt[h]),
+                                             make_float2(vf[d], vf[d + 1]), acc);
+                            o[h][d] = acc.x;
+                            o[h][d + 1] = acc.y;
+                        }
+                    }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+        }
+        if (bad && lane == 0) {
+            raise_flag(p.err_flag, XS_FLAG_TIMEOUT);
+            atomicExch(&s_abort, 1);
+        }
+
+        // ---- merge the four consumer states of this item
+#pragma unroll
+        for (int h = 0; h < G; ++h)
+#pragma unroll
+            for (int d = 0; d < C::kPvDims; ++d)
+                cO[(cw * G + h) * D + lane * C::kPvDims + d] = o[h][d];
+        if (tg == 0 && (j & ((1 << C::kHeadShift) - 1)) == 0) {
+            cM[cw * G + own_head] = m_own;
+            cL[cw * G + own_head] = l_own;
+        }
+        named_barrier_sync(1, 32 * kConsumerWarps);
+        if (ctid == 0) s_stop = s_abort;
+        const bool single = (it.n + p.P - 1) / p.P == 1;
+        const int64_t head0 = static_cast<int64_t>(it.b) * p.Hq + static_cast<int64_t>(it.g) * G;
+        for (int idx = ctid; idx < G * D; idx += 32 * kConsumerWarps) {
+            const int h = idx / D, d = idx - (idx / D) * D;
+            float mx = -INFINITY;
+#pragma unroll
+            for (int w2 = 0; w2 < kConsumerWarps; ++w2) mx = fmaxf(mx, cM[w2 * G + h]);
+            float lt = 0.f, ot = 0.f;
+#pragma unroll
+            for (int w2 = 0; w2 < kConsumerWarps; ++w2) {
+                const float f = fast_exp2(cM[w2 * G + h] - mx);
+                lt += f * cL[w2 * G + h];
+                ot += f * cO[(w2 * G + h) * D + d];
+            }
+            if (single) {
+                static_cast<T *>(p.out)[(head0 + h) * D + d] = Elem<T>::from_f32(ot / lt);
+            } else {
+                const int64_t pi = (head0 + h) * p.max_parts + it.part;
+                p.part_o[pi * D + d] = ot / lt;
+                if (d == 0) {
+                    p.part_m[pi] = mx;
+                    p.part_l[pi] = lt;
+                }
+            }
+        }
+        named_barrier_sync(1, 32 * kConsumerWarps);
+        if (s_stop) break;  // one value for every consumer (written before the barrier)
+    }
+}
+
+// Split-K combine: one CTA of D threads per (sequence, query head).
+template <typename T>
+__global__ void paged_decode_reduce_kernel(T *__restrict__ out, const float *__restrict__ part_o,
+                                           const float *__restrict__ part_m,
+                                           const float *__restrict__ part_l,
+                                           const int32_t *__restrict__ lens, int Hq, int D, int P,
+                                           int max_parts) {
+    const int bh = blockIdx.x;
+    const int b = bh / Hq;
+    const int n = lens[b];
+    int np = n > 0 ? (n + P - 1) / P : 0;
+    np = min(np, max_parts);
+    if (np <= 1) return;
+    const int64_t base = static_cast<int64_t>(bh) * max_parts;
+    float mx = -INFINITY;
+    for (int i = 0; i < np; ++i) mx = fmaxf(mx, part_m[base + i]);
+    const int d = threadIdx.x;
+    float lt = 0.f, acc = 0.f;
+    for (int i = 0; i < np; ++i) {
+        const float f = fast_exp2(part_m[base + i] - mx) * part_l[base + i];
+        lt += f;
+        if (d < D) acc += f * part_o[(base + i) * D + d];
+    }
+    if (d < D) out[static_cast<int64_t>(bh) * D + d] = Elem<T>::from_f32(acc / lt);
+}
+
+// ------------------------------------------------------------------ host side
+
+using KernelFn = void (*)(Params);
+
+template <typename T, int D, int G>
+KernelFn kernel_for() {
+    return paged_decode_kernel<T, D, G>;
+}
+
+KernelFn pick_kernel(int dtype, int D, int G, int *smem_base_fn_B0) {
+#define XS_PICK(TT, DD, GG)                                                          \
+    if (D == DD && G == GG) {                                                        \
+        *smem_base_fn_B0 = Cfg<TT, DD, GG>::smem_bytes(0);                           \
+        return kernel_for<TT, DD, GG>();                                             \
+    }
+    if (dtype == XS_BF16) {
+        XS_PICK(__nv_bfloat16, 64, 1) XS_PICK(__nv_bfloat16, 64, 2)
+        XS_PICK(__nv_bfloat16, 64, 4) XS_PICK(__nv_bfloat16, 64, 8)
+        XS_PICK(__nv_bfloat16, 128, 1) XS_PICK(__nv_bfloat16, 128, 2)
+        XS_PICK(__nv_bfloat16, 128, 4) XS_PICK(__nv_bfloat16, 128, 8)
+    } else if (dtype == XS_F32) {
+        XS_PICK(float, 64, 1) XS_PICK(float, 64, 2) XS_PICK(float, 64, 4) XS_PICK(float, 64, 8)
+        XS_PICK(float, 128, 1) XS_PICK(float, 128, 2) XS_PICK(float, 128, 4)
+        XS_PICK(float, 128, 8)
+    }
+#undef XS_PICK
+    return nullptr;
+}
+
+struct DeviceInfo {
+    int sms = 0;
+    int max_smem_optin = 0;
+};
+
+int device_info(DeviceInfo *info) {
+    static std::mutex mu;
+    static DeviceInfo cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return XS_EDEVICE;
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache[dev].sms == 0) {
+        DeviceInfo d;
+        if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin,
+                                   dev) != cudaSuccess)
+            return XS_EDEVICE;
+        cache[dev] = d;
+    }
+    *info = cache[dev];
+    return XS_OK;
+}
+
+// Resident CTAs per SM for a kernel at a given dynamic smem size (raises the
+// kernel's smem limit first).
+int occupancy(KernelFn fn, int smem, int *per_sm) {
+    if (cudaFuncSetAttribute(reinterpret_cast<const void *>(fn),
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+        return XS_ELAUNCH;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, reinterpret_cast<const void *>(fn),
+                                                      kThreads, smem) != cudaSuccess)
+        return XS_ELAUNCH;
+    *per_sm = n > 0 ? n : 1;
+    return XS_OK;
+}
+
+}  // namespace attn
+}  // namespace xs
+
+using namespace xs;
+
+extern "C" int xs_version(void) { return 100; }
+
+extern "C" int xs_paged_decode_partition_tokens(int B, int Hkv, int64_t total_context_tokens,
+                                                int max_context_len, int num_sms) {
+    if (B < 0 || Hkv <= 0 || max_context_len < 0 || num_sms <= 0) return XS_ESHAPE;
+    int64_t tokens = total_context_tokens > 0
+                         ? total_context_tokens
+                         : static_cast<int64_t>(B) * std::max(max_context_len, 1);
+    // Aim for >= 6 items per resident CTA (2 CTAs per SM assumed).
+    const int64_t want_items = static_cast<int64_t>(num_sms) * 2 * 6;
+    int P = 2048;
+    while (P > attn::kBlock) {
+        const int64_t items = (tokens / P + B) * Hkv;  // each sequence adds at most one ragged tail
+        if (items >= want_items) break;
+        P >>= 1;
+    }
+    return P;
+}
+
+extern "C" int xs_paged_decode_max_partitions(int max_blocks_per_seq, int block_size,
+                                              int partition_tokens) {
+    if (max_blocks_per_seq < 0 || block_size <= 0 || partition_tokens <= 0) return XS_ESHAPE;
+    const int64_t cap = static_cast<int64_t>(max_blocks_per_seq) * block_size;
+    return static_cast<int>(std::max<int64_t>(1, (cap + partition_tokens - 1) / partition_tokens));
+}
+
+extern "C" size_t xs_paged_decode_workspace_bytes(int B, int Hq, int D, int max_partitions) {
+    if (B <= 0 || Hq <= 0 || D <= 0 || max_partitions <= 0) return 0;
+    auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+    const size_t n = static_cast<size_t>(B) * Hq * max_partitions;
+    return up(n * D * 4) + 2 * up(n * 4);
+}
+
+static int check_attn_args(const void *out, const float *po, const float *pm, const float *pl,
+                           const void *q, const void *kc, const void *vc, const int32_t *bt,
+                           int max_blocks, const int32_t *lens, int B, int Hq, int Hkv, int D,
+                           int bs, int64_t num_blocks, int P, int max_parts, int dtype) {
+    if (!out || !q || !kc || !vc || !bt || !lens) return XS_ENULL;
+    if (!elem_bytes(dtype)) return XS_EDTYPE;
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || max_blocks < 0 || num_blocks < 0) return XS_ESHAPE;
+    if (Hq % Hkv != 0) return XS_ESHAPE;
+    const int G = Hq / Hkv;
+    if (bs != attn::kBlock || (D != 64 && D != 128) || (G != 1 && G != 2 && G != 4 && G != 8))
+        return XS_EUNSUPPORTED;
+    if (B > attn::kMaxBatch) return XS_EUNSUPPORTED;
+    if (P < attn::kBlock || P % attn::kBlock != 0) return XS_ESHAPE;
+    if (max_parts < xs_paged_decode_max_partitions(max_blocks, bs, P)) return XS_EWORKSPACE;
+    if (max_parts > 1 && (!po || !pm || !pl)) return XS_EWORKSPACE;
+    if (!aligned16(out) || !aligned16(q) || !aligned16(kc) || !aligned16(vc)) return XS_EALIGN;
+    if (max_parts > 1 && (!aligned16(po) || !aligned16(pm) || !aligned16(pl))) return XS_EALIGN;
+    return XS_OK;
+}
+
+extern "C" int xs_paged_decode_attn(void *out, float *part_o, float *part_m, float *part_l,
+                                    const void *q, const void *k_cache, const void *v_cache,
+                                    const int32_t *block_tables, int max_blocks_per_seq,
+                                    const int32_t *context_lens, int B, int Hq, int Hkv, int D,
+                                    int block_size, int64_t num_blocks, float scale,
+                                    int partition_tokens, int max_partitions, int dtype,
+                                    int *err_flag, cudaStream_t stream) {
+    int st = check_attn_args(out, part_o, part_m, part_l, q, k_cache, v_cache, block_tables,
+                             max_blocks_per_seq, context_lens, B, Hq, Hkv, D, block_size,
+                             num_blocks, partition_tokens, max_partitions, dtype);
+    if (st != XS_OK) return st;
+    if (B == 0) return XS_OK;
+    attn::DeviceInfo dev;
+    if ((st = attn::device_info(&dev)) != XS_OK) return st;
+    int smem0 = 0;
+    attn::KernelFn fn = attn::pick_kernel(dtype, D, Hq / Hkv, &smem0);
+    if (!fn) return XS_EUNSUPPORTED;
+    const int smem = smem0 + 4 * (B + 1);
+    if (smem > dev.max_smem_optin) return XS_EUNSUPPORTED;
+    int per_sm = 1;
+    if ((st = attn::occupancy(fn, smem, &per_sm)) != XS_OK) return st;
+    const int64_t max_items = static_cast<int64_t>(B) * Hkv * max_partitions;
+    const int64_t resident = static_cast<int64_t>(dev.sms) * per_sm;
+    const int grid = static_cast<int>(std::max<int64_t>(1, std::min(max_items, resident)));
+    attn::Params p;
+    p.out = out;
+    p.part_o = part_o;
+    p.part_m = part_m;
+    p.part_l = part_l;
+    p.q = q;
+    p.k_cache = k_cache;
+    p.v_cache = v_cache;
+    p.block_tables = block_tables;
+    p.context_lens = context_lens;
+    p.max_blocks = max_blocks_per_seq;
+    p.B = B;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.P = partition_tokens;
+    p.max_parts = max_partitions;
+    p.num_blocks = num_blocks;
+    p.qscale = scale * attn::kLog2e;
+    p.err_flag = err_flag;
+    fn<<<grid, attn::kThreads, smem, stream>>>(p);
+    return launch_status();
+}
+
+extern "C" int xs_paged_decode_reduce(void *out, const float *part_o, const float *part_m,
+                                      const float *part_l, const int32_t *context_lens, int B,
+                                      int Hq, int D, int partition_tokens, int max_partitions,
+                                      int dtype, cudaStream_t stream) {
+    if (!out || !context_lens) return XS_ENULL;
+    if (!elem_bytes(dtype)) return XS_EDTYPE;
+    if (B < 0 || Hq <= 0 || D <= 0 || D > 1024 || partition_tokens <= 0 || max_partitions <= 0)
+        return XS_ESHAPE;
+    if (B == 0 || max_partitions == 1) return XS_OK;
+    if (!part_o || !part_m || !part_l) return XS_EWORKSPACE;
+    const int64_t blocks = static_cast<int64_t>(B) * Hq;
+    if (blocks > 0x7fffffff) return XS_ESHAPE;
+    const int threads = (D + 31) / 32 * 32;
+    if (dtype == XS_BF16)
+        attn::paged_decode_reduce_kernel<__nv_bfloat16><<<static_cast<int>(blocks), threads, 0,
+                                                          stream>>>(
+            static_cast<__nv_bfloat16 *>(out), part_o, part_m, part_l, context_lens, Hq, D,
+            partition_tokens, max_partitions);
+    else
+        attn::paged_decode_reduce_kernel<float><<<static_cast<int>(blocks), threads, 0, stream>>>(
+            static_cast<float *>(out), part_o, part_m, part_l, context_lens, Hq, D,
+            partition_tokens, max_partitions);
+    return launch_status();
+}
+
+extern "C" int xs_paged_decode(void *out, float *part_o, float *part_m, float *part_l,
+                               const void *q, const void *k_cache, const void *v_cache,
+                               const int32_t *block_tables, int max_blocks_per_seq,
+                               const int32_t *context_lens, int B, int Hq, int Hkv, int D,
+                               int block_size, int64_t num_blocks, float scale,
+                               int partition_tokens, int max_partitions, int dtype, int *err_flag,
+                               cudaStream_t stream) {
+    int st = xs_paged_decode_attn(out, part_o, part_m, part_l, q, k_cache, v_cache, block_tables,
+                                  max_blocks_per_seq, context_lens, B, Hq, Hkv, D, block_size,
+                                  num_blocks, scale, partition_tokens, max_partitions, dtype,
+                                  err_flag, stream);
+    if (st != XS_OK || max_partitions <= 1) return st;
+    return xs_paged_decode_reduce(out, part_o, part_m, part_l, context_lens, B, Hq, D,
+                                  partition_tokens, max_partitions, dtype, stream);
+}

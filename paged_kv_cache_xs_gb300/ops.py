@@ -1,0 +1,221 @@
+"""Python binding of libxs_paged (argument marshalling only).
+
+Each ``xs_*`` function here calls the C entry point of the same name in
+``include/xs_paged.h`` with ``tensor.data_ptr()`` values and the current
+PyTorch CUDA stream; every step of the decode path runs in the library's
+kernels.  PyTorch supplies device memory and streams.  There is no fallback:
+if the shared library is missing or a call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+XS_F32 = 0
+XS_BF16 = 1
+BLOCK_SIZE = 16
+
+STATUS = {
+    0: "XS_OK", -1: "XS_ENULL", -2: "XS_ESHAPE", -3: "XS_EDTYPE", -4: "XS_EALIGN",
+    -5: "XS_EUNSUPPORTED", -6: "XS_EWORKSPACE", -7: "XS_ELAUNCH", -8: "XS_EDEVICE",
+}
+FLAG_BAD_BLOCK, FLAG_BAD_LEN, FLAG_BAD_SLOT, FLAG_TIMEOUT = 1, 2, 4, 8
+
+# name -> (restype, argtypes)
+_P, _I, _L, _F, _S = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float,
+                      ctypes.c_size_t)
+SIGNATURES = {
+    "xs_slot_mapping": (_I, [_P, _I, _P, _I, _I, _L, _P, _P, _P]),
+    "xs_kv_append": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _L, _I, _P, _P]),
+    "xs_kv_append_paged": (_I, [_P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _L, _I, _P, _P]),
+    "xs_paged_decode_partition_tokens": (_I, [_I, _I, _L, _I, _I]),
+    "xs_paged_decode_max_partitions": (_I, [_I, _I, _I]),
+    "xs_paged_decode_workspace_bytes": (_S, [_I, _I, _I, _I]),
+    "xs_paged_decode_attn": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I,
+                                  _L, _F, _I, _I, _I, _P, _P]),
+    "xs_paged_decode_reduce": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
+    "xs_paged_decode": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _L, _F,
+                             _I, _I, _I, _P, _P]),
+    "xs_version": (_I, []),
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class XsError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn} failed: {STATUS.get(code, code)} ({code})")
+        self.code = code
+
+
+def lib_path() -> str:
+    return _build.LIB_PATH
+
+
+def load(path: str | None = None):
+    """Load libxs_paged.so (built in-tree by ``build.build()``)."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or _build.LIB_PATH
+        if not os.path.exists(p):
+            raise ImportError(f"{p} is missing: build it with paged_kv_cache_xs_gb300.build.build()")
+        lib = ctypes.CDLL(p)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def _call(name: str, *args) -> int:
+    code = getattr(load(), name)(*args)
+    if code != 0:
+        raise XsError(name, code)
+    return code
+
+
+def dtype_code(dt: torch.dtype) -> int:
+    if dt == torch.float32:
+        return XS_F32
+    if dt == torch.bfloat16:
+        return XS_BF16
+    raise ValueError(f"unsupported dtype {dt}")
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to libxs_paged must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+# ---------------------------------------------------------------- entry points
+
+def xs_slot_mapping(block_tables, context_lens, block_size, num_blocks, slot_mapping=None,
+                    err_flag=None, stream=None) -> torch.Tensor:
+    B = context_lens.numel()
+    if slot_mapping is None:
+        slot_mapping = torch.empty(B, dtype=torch.int64, device=context_lens.device)
+    _call("xs_slot_mapping", _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), B,
+          block_size, num_blocks, _ptr(slot_mapping), _ptr(err_flag), _stream(stream))
+    return slot_mapping
+
+
+def xs_kv_append(k_new, v_new, k_cache, v_cache, slot_mapping, err_flag=None, stream=None):
+    T, Hkv, D = k_new.shape
+    num_blocks, _, bs, _ = k_cache.shape
+    _call("xs_kv_append", _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+          _ptr(slot_mapping), T, Hkv, D, bs, num_blocks, dtype_code(k_new.dtype), _ptr(err_flag),
+          _stream(stream))
+
+
+def xs_kv_append_paged(k_new, v_new, k_cache, v_cache, block_tables, context_lens, err_flag=None,
+                       stream=None):
+    B, Hkv, D = k_new.shape
+    num_blocks, _, bs, _ = k_cache.shape
+    _call("xs_kv_append_paged", _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+          _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), B, Hkv, D, bs,
+          num_blocks, dtype_code(k_new.dtype), _ptr(err_flag), _stream(stream))
+
+
+def xs_paged_decode_partition_tokens(B, Hkv, total_context_tokens, max_context_len, num_sms) -> int:
+    r = load().xs_paged_decode_partition_tokens(B, Hkv, total_context_tokens, max_context_len,
+                                                num_sms)
+    if r < 0:
+        raise XsError("xs_paged_decode_partition_tokens", r)
+    return r
+
+
+def xs_paged_decode_max_partitions(max_blocks_per_seq, block_size, partition_tokens) -> int:
+    r = load().xs_paged_decode_max_partitions(max_blocks_per_seq, block_size, partition_tokens)
+    if r < 0:
+        raise XsError("xs_paged_decode_max_partitions", r)
+    return r
+
+
+def xs_paged_decode_workspace_bytes(B, Hq, D, max_partitions) -> int:
+    return int(load().xs_paged_decode_workspace_bytes(B, Hq, D, max_partitions))
+
+
+def xs_paged_decode_attn(out, part_o, part_m, part_l, q, k_cache, v_cache, block_tables,
+                         context_lens, scale, partition_tokens, max_partitions, err_flag=None,
+                         stream=None):
+    B, Hq, D = q.shape
+    num_blocks, Hkv, bs, _ = k_cache.shape
+    _call("xs_paged_decode_attn", _ptr(out), _ptr(part_o), _ptr(part_m), _ptr(part_l), _ptr(q),
+          _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1],
+          _ptr(context_lens), B, Hq, Hkv, D, bs, num_blocks, float(scale), partition_tokens,
+          max_partitions, dtype_code(q.dtype), _ptr(err_flag), _stream(stream))
+
+
+def xs_paged_decode_reduce(out, part_o, part_m, part_l, context_lens, partition_tokens,
+                           max_partitions, stream=None):
+    B, Hq, D = out.shape
+    _call("xs_paged_decode_reduce", _ptr(out), _ptr(part_o), _ptr(part_m), _ptr(part_l),
+          _ptr(context_lens), B, Hq, D, partition_tokens, max_partitions, dtype_code(out.dtype),
+          _stream(stream))
+
+
+def xs_paged_decode(out, part_o, part_m, part_l, q, k_cache, v_cache, block_tables, context_lens,
+                    scale, partition_tokens, max_partitions, err_flag=None, stream=None):
+    B, Hq, D = q.shape
+    num_blocks, Hkv, bs, _ = k_cache.shape
+    _call("xs_paged_decode", _ptr(out), _ptr(part_o), _ptr(part_m), _ptr(part_l), _ptr(q),
+          _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1],
+          _ptr(context_lens), B, Hq, Hkv, D, bs, num_blocks, float(scale), partition_tokens,
+          max_partitions, dtype_code(q.dtype), _ptr(err_flag), _stream(stream))
+
+
+def xs_version() -> int:
+    return load().xs_version()
+
+
+# ---------------------------------------------------------------- workspace holder
+
+class DecodeWorkspace:
+    """Split-K partials sized for a batch shape, allocated once through PyTorch.
+
+    ``partition_tokens`` comes from the library's heuristic unless given."""
+
+    def __init__(self, B: int, Hq: int, Hkv: int, D: int, max_blocks_per_seq: int,
+                 device, total_context_tokens: int = 0, max_context_len: int | None = None,
+                 partition_tokens: int | None = None, num_sms: int | None = None):
+        device = torch.device(device)
+        if num_sms is None:
+            num_sms = torch.cuda.get_device_properties(device).multi_processor_count
+        if max_context_len is None:
+            max_context_len = max_blocks_per_seq * BLOCK_SIZE
+        self.partition_tokens = partition_tokens or xs_paged_decode_partition_tokens(
+            B, Hkv, total_context_tokens, max_context_len, num_sms)
+        self.max_partitions = xs_paged_decode_max_partitions(max_blocks_per_seq, BLOCK_SIZE,
+                                                             self.partition_tokens)
+        n = B * Hq * self.max_partitions
+        if self.max_partitions > 1:
+            self.part_o = torch.empty(n * D, dtype=torch.float32, device=device)
+            self.part_m = torch.empty(n, dtype=torch.float32, device=device)
+            self.part_l = torch.empty(n, dtype=torch.float32, device=device)
+        else:
+            self.part_o = self.part_m = self.part_l = None
+
+    @property
+    def partial_bytes(self) -> int:
+        if self.part_o is None:
+            return 0
+        return 4 * (self.part_o.numel() + self.part_m.numel() + self.part_l.numel())

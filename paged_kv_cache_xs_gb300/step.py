@@ -1,0 +1,93 @@
+"""One continuous-batching decode step over a paged KV cache.
+
+``PagedDecodeStep`` owns nothing but the split-K workspace; the KV pools,
+block tables and lengths belong to the caller.  ``run`` enqueues, on the
+current stream:
+
+1. ``xs_kv_append_paged``  - slot resolution + KV append (the pages'
+   reshape_and_cache_batched_bf16, "xserv compare phase10...cf1e9e4",
+   attention.rs);
+2. ``xs_paged_decode_attn`` - paged decode attention, split-K partitions;
+3. ``xs_paged_decode_reduce`` - split-K combine (only when a sequence can
+   span several partitions).
+
+``run_from_host`` is the same step fed from pinned host buffers: it copies
+the step's inputs to the device, runs the step and copies the output back.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import ops
+
+
+class PagedDecodeStep:
+    def __init__(self, B: int, Hq: int, Hkv: int, D: int, max_blocks_per_seq: int, dtype,
+                 device, total_context_tokens: int = 0, max_context_len: int | None = None,
+                 partition_tokens: int | None = None):
+        self.B, self.Hq, self.Hkv, self.D = B, Hq, Hkv, D
+        self.dtype = dtype
+        self.device = torch.device(device)
+        self.max_blocks_per_seq = max_blocks_per_seq
+        self.ws = ops.DecodeWorkspace(B, Hq, Hkv, D, max_blocks_per_seq, self.device,
+                                      total_context_tokens=total_context_tokens,
+                                      max_context_len=max_context_len,
+                                      partition_tokens=partition_tokens)
+        self.err_flag = torch.zeros(1, dtype=torch.int32, device=self.device)
+        self._dev_inputs = None
+
+    @property
+    def partition_tokens(self) -> int:
+        return self.ws.partition_tokens
+
+    @property
+    def max_partitions(self) -> int:
+        return self.ws.max_partitions
+
+    @property
+    def launches_per_step(self) -> int:
+        return 3 if self.ws.max_partitions > 1 else 2
+
+    def append(self, k_new, v_new, k_cache, v_cache, block_tables, context_lens):
+        ops.xs_kv_append_paged(k_new, v_new, k_cache, v_cache, block_tables, context_lens,
+                               err_flag=self.err_flag)
+
+    def attend(self, out, q, k_cache, v_cache, block_tables, context_lens, scale):
+        ws = self.ws
+        ops.xs_paged_decode_attn(out, ws.part_o, ws.part_m, ws.part_l, q, k_cache, v_cache,
+                                 block_tables, context_lens, scale, ws.partition_tokens,
+                                 ws.max_partitions, err_flag=self.err_flag)
+
+    def reduce(self, out, context_lens):
+        ws = self.ws
+        if ws.max_partitions > 1:
+            ops.xs_paged_decode_reduce(out, ws.part_o, ws.part_m, ws.part_l, context_lens,
+                                       ws.partition_tokens, ws.max_partitions)
+
+    def run(self, out, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, scale):
+        """Append this step's K/V, then attend; all tensors on the device."""
+        self.append(k_new, v_new, k_cache, v_cache, block_tables, context_lens)
+        self.attend(out, q, k_cache, v_cache, block_tables, context_lens, scale)
+        self.reduce(out, context_lens)
+        return out
+
+    def run_from_host(self, out_host, q, k_new, v_new, block_tables, context_lens, k_cache,
+                      v_cache, scale):
+        """Step fed from (pinned) host tensors q, k_new, v_new, block_tables and
+        context_lens; the pools stay on the device.  Writes out_host and waits
+        for it."""
+        if self._dev_inputs is None or self._dev_inputs[0].shape != q.shape \
+                or self._dev_inputs[3].shape != block_tables.shape:
+            self._dev_inputs = tuple(torch.empty(t.shape, dtype=t.dtype, device=self.device)
+                                     for t in (q, k_new, v_new, block_tables, context_lens))
+            self._dev_out = torch.empty(q.shape, dtype=q.dtype, device=self.device)
+        dq, dk, dv, dbt, dcl = self._dev_inputs
+        for d, h in zip(self._dev_inputs, (q, k_new, v_new, block_tables, context_lens)):
+            d.copy_(h, non_blocking=True)
+        self.run(self._dev_out, dq, dk, dv, k_cache, v_cache, dbt, dcl, scale)
+        out_host.copy_(self._dev_out, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+        return out_host
+
+    def error_flags(self) -> int:
+        return int(self.err_flag.item())

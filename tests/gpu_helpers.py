@@ -1,0 +1,100 @@
+"""Shared helpers for the GPU parity tests (CUDA path vs the CPU oracle)."""
+from __future__ import annotations
+
+import torch
+
+import oracle
+from paged_kv_cache_xs_gb300 import build as xsbuild
+from paged_kv_cache_xs_gb300 import ops
+
+BS = 16
+# Attention tolerances (max-abs against the fp64 oracle).
+TOL = {torch.float32: 1e-5, torch.bfloat16: 1e-2}
+
+
+def device() -> torch.device:
+    xsbuild.build()
+    ops.load()
+    return torch.device("cuda:0")
+
+
+def int_view(t: torch.Tensor) -> torch.Tensor:
+    return t.view(torch.int16 if t.element_size() == 2 else torch.int32)
+
+
+def compact_pages(block_tables, context_lens, seqs, k_pool, v_pool):
+    """CPU copies of the pages the sequences `seqs` read, renumbered 0..n-1,
+    with a matching block table.  (The oracle's output does not depend on
+    where pages sit, which its permutation pin checks.)"""
+    bt = block_tables[seqs].cpu()
+    lens = context_lens[seqs].cpu()
+    ids, rows = [], []
+    for i in range(len(seqs)):
+        n = max(int(lens[i]), 0)
+        p = (n + BS - 1) // BS
+        rows.append(list(range(len(ids), len(ids) + p)))
+        ids.extend(bt[i, :p].tolist())
+    width = max([1] + [len(r) for r in rows])
+    new_bt = torch.full((len(seqs), width), -1, dtype=torch.int32)
+    for i, r in enumerate(rows):
+        if r:
+            new_bt[i, :len(r)] = torch.tensor(r, dtype=torch.int32)
+    idx = torch.tensor(ids, dtype=torch.long, device=k_pool.device)
+    return k_pool.index_select(0, idx).cpu(), v_pool.index_select(0, idx).cpu(), new_bt, lens
+
+
+def changed_rows(before: torch.Tensor, after: torch.Tensor) -> set:
+    """(block, head, offset) of every pool row whose bytes differ."""
+    diff = (int_view(before) != int_view(after)).any(dim=-1)
+    return {tuple(x) for x in diff.nonzero().tolist()}
+
+
+def expected_rows(block_tables, context_lens, num_blocks, Hkv) -> set:
+    slots = oracle.slot_mapping(block_tables.cpu(), context_lens.cpu(), BS, num_blocks)
+    return {(s // BS, h, s % BS) for s in slots.tolist() if s >= 0 for h in range(Hkv)}
+
+
+def max_abs(out: torch.Tensor, ref: torch.Tensor) -> float:
+    if out.numel() == 0:
+        return 0.0
+    return (out.detach().cpu().double() - ref).abs().max().item()
+
+
+def check_step(w, layer, step, seqs=None, check_unchanged=True):
+    """Run one decode step (append + attention) of layer `layer` through the
+    CUDA path and compare it with the oracle on the sequences `seqs`.
+    Returns the attention max-abs error."""
+    cfg = w.cfg
+    seqs = list(range(cfg.B)) if seqs is None else list(seqs)
+    kc, vc = w.k_cache[layer], w.v_cache[layer]
+    kb, vb, bt_c, lens_c = compact_pages(w.block_tables, w.context_lens, seqs, kc, vc)
+    before_k = kc.clone() if check_unchanged else None
+    before_v = vc.clone() if check_unchanged else None
+    out = torch.empty(cfg.B, cfg.Hq, cfg.D, dtype=cfg.dtype, device=kc.device)
+    step.err_flag.zero_()
+    step.run(out, w.q[layer], w.k_new[layer], w.v_new[layer], kc, vc, w.block_tables,
+             w.context_lens, w.scale)
+    torch.cuda.synchronize()
+    assert step.error_flags() == 0, f"device error flag {step.error_flags()}"
+
+    # Append: bit-exact against the oracle's append of the same pre-state.
+    sel = torch.tensor(seqs, dtype=torch.long, device=kc.device)
+    kn = w.k_new[layer].index_select(0, sel).cpu()
+    vn = w.v_new[layer].index_select(0, sel).cpu()
+    slots = oracle.slot_mapping(bt_c, lens_c, BS, kb.shape[0])
+    ek, ev = oracle.kv_append(kn, vn, kb, vb, slots)
+    ka, va, _, _ = compact_pages(w.block_tables, w.context_lens, seqs, kc, vc)
+    assert torch.equal(int_view(ka), int_view(ek)), "K pages differ from the oracle append"
+    assert torch.equal(int_view(va), int_view(ev)), "V pages differ from the oracle append"
+    if check_unchanged:
+        want = expected_rows(w.block_tables, w.context_lens, w.num_blocks, cfg.Hkv)
+        assert changed_rows(before_k, kc) <= want, "append wrote outside the new slots"
+        assert changed_rows(before_v, vc) <= want, "append wrote outside the new slots"
+        del before_k, before_v
+
+    # Attention over the appended cache.
+    q = w.q[layer].index_select(0, sel).cpu()
+    ref = oracle.paged_decode(q, ek, ev, bt_c, lens_c, w.scale)
+    err = max_abs(out.index_select(0, sel), ref)
+    assert err <= TOL[cfg.dtype], f"{cfg.name} layer {layer}: max-abs {err:.3e}"
+    return err

@@ -1,0 +1,132 @@
+"""libxs_paged without a GPU: it builds, loads, exports every entry point the
+header declares, and its host-side logic (split heuristic, workspace sizes,
+argument validation) behaves as documented.  Validation errors return before
+any CUDA call, so these run on a machine with no GPU."""
+import glob
+import os
+import re
+
+import pytest
+
+from paged_kv_cache_xs_gb300 import build as xsbuild
+from paged_kv_cache_xs_gb300 import ops
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    xsbuild.build()
+    return ops.load()
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        names.update(re.findall(r"^(?:int|size_t|void)\s+(xs_\w+)\s*\(", text, flags=re.M))
+    return sorted(names)
+
+
+def test_header_declares_entry_points():
+    names = declared_functions()
+    for required in ("xs_kv_append", "xs_paged_decode_attn", "xs_paged_decode_reduce",
+                     "xs_slot_mapping"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, f"not exported: {missing}"
+
+
+def test_binding_covers_every_declared_symbol():
+    assert set(declared_functions()) <= set(ops.SIGNATURES), \
+        set(declared_functions()) - set(ops.SIGNATURES)
+
+
+def test_version(lib):
+    assert lib.xs_version() >= 100
+
+
+def test_partition_heuristic(lib):
+    for B, Hkv, total, mx in [(128, 8, 128 * 18433, 32769), (1, 8, 4097, 4097),
+                              (64, 8, 64 * 1300, 8193), (8, 12, 8 * 600, 1025), (2, 12, 29, 21)]:
+        P = ops.xs_paged_decode_partition_tokens(B, Hkv, total, mx, 152)
+        assert 16 <= P <= 2048 and P % 16 == 0 and (P & (P - 1)) == 0
+        items = (total // P + B) * Hkv
+        assert items >= 152 * 2 * 6 or P == 16
+    # More SMs never asks for bigger partitions.
+    a = ops.xs_paged_decode_partition_tokens(64, 8, 64 * 1300, 8193, 76)
+    b = ops.xs_paged_decode_partition_tokens(64, 8, 64 * 1300, 8193, 152)
+    assert b <= a
+    assert ops.load().xs_paged_decode_partition_tokens(-1, 8, 0, 0, 152) == -2
+
+
+def test_max_partitions_and_workspace(lib):
+    assert ops.xs_paged_decode_max_partitions(2049, 16, 1024) == 33
+    assert ops.xs_paged_decode_max_partitions(1, 16, 1024) == 1
+    assert ops.xs_paged_decode_max_partitions(0, 16, 64) == 1
+    n = 128 * 32 * 33
+    up = lambda x: (x + 255) // 256 * 256
+    assert ops.xs_paged_decode_workspace_bytes(128, 32, 128, 33) == up(n * 128 * 4) + 2 * up(n * 4)
+    assert ops.xs_paged_decode_workspace_bytes(0, 32, 128, 33) == 0
+
+
+# Fake, non-null, 16-byte-aligned "device" addresses: every call below is
+# rejected by host-side validation before anything touches CUDA.
+A = 1 << 20
+
+
+def _attn(lib, **kw):
+    args = dict(out=A, po=A, pm=A, pl=A, q=A, k=A, v=A, bt=A, maxb=4, lens=A, B=2, Hq=8, Hkv=2,
+                D=128, bs=16, nb=10, scale=0.1, P=16, maxp=4, dtype=1, err=None, stream=None)
+    args.update(kw)
+    return lib.xs_paged_decode_attn(args["out"], args["po"], args["pm"], args["pl"], args["q"],
+                                    args["k"], args["v"], args["bt"], args["maxb"], args["lens"],
+                                    args["B"], args["Hq"], args["Hkv"], args["D"], args["bs"],
+                                    args["nb"], args["scale"], args["P"], args["maxp"],
+                                    args["dtype"], args["err"], args["stream"])
+
+
+def test_attn_argument_validation(lib):
+    assert _attn(lib, B=0) == 0                     # nothing to do, nothing launched
+    assert _attn(lib, q=None) == -1
+    assert _attn(lib, bt=None) == -1
+    assert _attn(lib, dtype=7) == -3
+    assert _attn(lib, Hq=6, Hkv=4) == -2            # Hq % Hkv != 0
+    assert _attn(lib, B=-1) == -2
+    assert _attn(lib, D=96) == -5
+    assert _attn(lib, bs=32) == -5
+    assert _attn(lib, Hq=24, Hkv=2) == -5           # group of 12
+    assert _attn(lib, P=24) == -2                   # not a multiple of 16
+    assert _attn(lib, maxp=3) == -6                 # 4 blocks * 16 / 16 = 4 partitions needed
+    assert _attn(lib, po=None) == -6
+    assert _attn(lib, k=A + 8) == -4
+    assert _attn(lib, out=A + 2) == -4
+    assert _attn(lib, B=20000) == -5                # beyond the per-launch batch limit
+
+
+def test_append_argument_validation(lib):
+    f = lib.xs_kv_append
+    assert f(A, A, A, A, A, 0, 8, 128, 16, 10, 1, None, None) == 0   # T == 0
+    assert f(None, A, A, A, A, 3, 8, 128, 16, 10, 1, None, None) == -1
+    assert f(A, A, A, A, None, 3, 8, 128, 16, 10, 1, None, None) == -1
+    assert f(A, A, A, A, A, 3, 8, 128, 16, 10, 5, None, None) == -3
+    assert f(A, A, A, A, A, 3, 0, 128, 16, 10, 1, None, None) == -2
+    assert f(A, A, A, A, A, 3, 8, 4, 16, 10, 1, None, None) == -5     # 8-byte rows
+    assert f(A, A, A + 4, A, A, 3, 8, 128, 16, 10, 1, None, None) == -4
+    g = lib.xs_kv_append_paged
+    assert g(A, A, A, A, None, 4, A, 3, 8, 128, 16, 10, 1, None, None) == -1
+    assert g(A, A, A, A, A, 4, A, 0, 8, 128, 16, 10, 1, None, None) == 0
+    assert lib.xs_slot_mapping(None, 4, A, 3, 16, 10, A, None, None) == -1
+    assert lib.xs_slot_mapping(A, 4, A, 0, 16, 10, A, None, None) == 0
+    assert lib.xs_paged_decode_reduce(A, A, A, A, A, 2, 8, 128, 16, 1, 1, None) == 0
+    assert lib.xs_paged_decode_reduce(A, None, A, A, A, 2, 8, 128, 16, 4, 1, None) == -6
+    assert lib.xs_paged_decode_reduce(A, A, A, A, A, 2, 8, 128, 16, 4, 9, None) == -3
+
+
+def test_binding_raises_on_error_code(lib):
+    with pytest.raises(ops.XsError) as e:
+        ops._call("xs_slot_mapping", None, 4, A, 3, 16, 10, A, None, None)
+    assert e.value.code == -1

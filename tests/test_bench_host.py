@@ -1,0 +1,66 @@
+"""Host-side pieces of bench.py: byte accounting, the reference (oracle) arm
+on the tiny workload, and the max-over-ranks timing across two gloo ranks."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+from paged_kv_cache_xs_gb300 import workloads as wl  # noqa: E402
+
+
+def test_step_bytes_tiny_config():
+    cfg = wl.CONFIGS[0]
+    lens = torch.tensor([8, 21], dtype=torch.int32)
+    by = bench.step_bytes(cfg, lens)
+    s = 4
+    kv = (8 + 21) * 12 * 64 * 2 * s
+    assert by["kv"] == kv
+    tables = (1 + 2) * 4 + 4 * 2
+    assert by["attn"] == kv + 2 * 12 * 64 * s + tables
+    assert by["step"] == by["attn"] + 2 * 12 * 64 * s + 2 * 2 * 12 * 64 * s * 2
+
+
+def test_reference_arm_tiny_config():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--config", "0", "--steps", "2", "--warmup", "3",
+                        "--ref-step-seconds", "0.05"],
+                       capture_output=True, text=True, timeout=300,
+                       env={**os.environ, "CUDA_VISIBLE_DEVICES": ""})
+    assert r.returncode == 0, r.stderr
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["unit"] == "GB/s" and line["value"] > 0
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
+
+
+def _rank_main(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    import torch.distributed as dist
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    bench.barrier(dist)
+    got = bench.max_over_ranks(1.5 + rank, dist)
+    dist.destroy_process_group()
+    q.put((rank, got))
+
+
+def test_max_over_ranks_gloo_two_ranks():
+    import multiprocessing as mp
+    import socket
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = dict(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+    assert res == {0: 2.5, 1: 2.5}
