@@ -51,8 +51,7 @@ def test_variants_split_and_single(dtype, D, G):
     for P in (16, 48, 128, 512):
         out = _attend(w, 0, P)
         torch.cuda.synchronize()
-        err = gh.max_abs(out, ref)
-        assert err <= gh.TOL[dtype], f"P={P}: max-abs {err:.3e}"
+        gh.assert_close(out, ref, dtype, what=f"P={P}")
 
 
 def test_full_step_ragged_with_empty_sequences():
@@ -63,15 +62,14 @@ def test_full_step_ragged_with_empty_sequences():
     w = wl.make_workload(cfg, device=dev, history=hist)
     step = PagedDecodeStep(cfg.B, cfg.Hq, cfg.Hkv, cfg.D, w.max_blocks_per_seq, cfg.dtype, dev,
                            partition_tokens=256)
-    gh.check_step(w, 0, step)
+    gh.check_step(w, 0, step, strict=False)
     # Sequences with nothing to attend to (context length 0) give zeros and write nothing.
     w.context_lens[2] = 0
     w.context_lens[5] = 0
     out = _attend(w, 0, 64)
     torch.cuda.synchronize()
     assert torch.count_nonzero(out[2]).item() == 0 and torch.count_nonzero(out[5]).item() == 0
-    ref = _oracle(w, 0)
-    assert gh.max_abs(out, ref) <= 1e-2
+    gh.assert_close(out, _oracle(w, 0), torch.bfloat16)
 
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
@@ -109,7 +107,7 @@ def test_physical_permutation_is_bit_identical():
     b = _attend(w, 0, 128, kc=kc2, vc=vc2, bt=bt2)
     torch.cuda.synchronize()
     assert torch.equal(gh.int_view(a), gh.int_view(b))
-    assert gh.max_abs(a, _oracle(w, 0)) <= 1e-2
+    gh.assert_close(a, _oracle(w, 0), torch.bfloat16)
 
 
 def test_constant_v_gives_constant_output():
@@ -133,7 +131,7 @@ def test_many_sequences_prefix_scan():
     w = wl.make_workload(cfg, device=dev)
     step = PagedDecodeStep(cfg.B, cfg.Hq, cfg.Hkv, cfg.D, w.max_blocks_per_seq, cfg.dtype, dev,
                            partition_tokens=16)
-    gh.check_step(w, 0, step)
+    gh.check_step(w, 0, step, strict=False)
 
 
 def test_one_long_sequence_many_partitions():
@@ -146,11 +144,11 @@ def test_one_long_sequence_many_partitions():
                                partition_tokens=P)
         # re-draw the appended slot's pre-state each time: run append only once
         if P == 16:
-            gh.check_step(w, 0, step)
+            gh.check_step(w, 0, step, strict=False)
         else:
             out = _attend(w, 0, P)
             torch.cuda.synchronize()
-            assert gh.max_abs(out, _oracle(w, 0)) <= 1e-2
+            gh.assert_close(out, _oracle(w, 0), torch.bfloat16)
 
 
 def test_side_stream():
@@ -163,7 +161,7 @@ def test_side_stream():
     with torch.cuda.stream(s):
         out = _attend(w, 0, 64)
     s.synchronize()
-    assert gh.max_abs(out, _oracle(w, 0)) <= 1e-2
+    gh.assert_close(out, _oracle(w, 0), torch.bfloat16)
 
 
 def test_slot_mapping_matches_oracle():
@@ -213,7 +211,7 @@ def test_device_errors_are_flagged_not_trapped():
     torch.cuda.synchronize()
     assert int(err.item()) & ops.FLAG_BAD_BLOCK
     keep = [0, 2, 3]
-    assert gh.max_abs(out[keep], ref[keep]) <= 1e-2
+    gh.assert_close(out[keep], ref[keep], torch.bfloat16)
     # (b) a context length beyond the table: flagged and clamped.
     err.zero_()
     lens = w.context_lens.clone()
