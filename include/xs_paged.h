@@ -14,8 +14,10 @@
  * Conventions shared by every entry point
  * ---------------------------------------
  *  - Every array argument is a DEVICE pointer owned by the caller.  The
- *    library never allocates, frees or retains memory; scratch space
- *    (split-K partials) is passed in by the caller.
+ *    library never allocates or frees memory; scratch space (split-K
+ *    partials) is passed in by the caller, except for
+ *    xs_paged_decode_noalloc, which uses one fixed array the library
+ *    reserves on each device when it is loaded.
  *  - Work is enqueued asynchronously on the caller's stream; a call returns
  *    once the launch is queued.  Nothing synchronises the device.
  *  - Return value: XS_OK (0) or a negative XS_E* code.  Host-visible
@@ -34,9 +36,8 @@
  *                   physical blocks in logical order; entries past the last
  *                   page the sequence uses are never read
  *      context_lens int32 [B]; number of tokens of sequence b INCLUDING the
- *                   token written this step (the pages' kv_lens: "current
- *                   seq_len + 1 - i.e., the index of the just-written token
- *                   + 1")
+ *                   token written this step (the same meaning as the
+ *                   per-sequence lengths of the pages' batched append)
  *      q, out       [B, Hq, D] (the pages' [batch, num_q_heads, 1, head_dim])
  *      k_new, v_new [T, Hkv, D], one row per written token
  *  - Query head h reads KV head h / (Hq/Hkv) ("xserv compare
@@ -74,6 +75,8 @@ extern "C" {
 #define XS_EWORKSPACE -6   /* partials missing or too small for the split    */
 #define XS_ELAUNCH -7      /* a kernel launch failed                          */
 #define XS_EDEVICE -8      /* querying the current device failed              */
+#define XS_ESCRATCH -9     /* the split needs more than the library's fixed
+                              scratch array holds (xs_paged_decode_noalloc)   */
 
 /* bits ORed into *err_flag by the kernels */
 #define XS_FLAG_BAD_BLOCK 1 /* a block id outside [0, num_blocks) was met;
@@ -128,8 +131,8 @@ int xs_kv_append(const void *k_new, const void *v_new, void *k_cache, void *v_ca
  * writes k_new[b] / v_new[b] ([B, Hkv, D]) at position context_lens[b] - 1
  * of sequence b, located through block_tables exactly as xs_slot_mapping
  * does.  This is the pages' reshape_and_cache_batched_bf16 ("xserv compare
- * phase10...cf1e9e4", attention.rs: "same buffer the paged-attention kernel
- * reads").  Errors as xs_slot_mapping; bad entries are skipped.
+ * phase10...cf1e9e4", attention.rs), which reads the very block table the
+ * attention call reads.  Errors as xs_slot_mapping; bad entries are skipped.
  */
 int xs_kv_append_paged(const void *k_new, const void *v_new, void *k_cache, void *v_cache,
                        const int32_t *block_tables, int max_blocks_per_seq,
@@ -225,6 +228,52 @@ int xs_paged_decode(void *out, float *part_o, float *part_m, float *part_l, cons
                     int max_blocks_per_seq, const int32_t *context_lens, int B, int Hq, int Hkv,
                     int D, int block_size, int64_t num_blocks, float scale, int partition_tokens,
                     int max_partitions, int dtype, int *err_flag, cudaStream_t stream);
+
+/*
+ * xs_paged_decode_noalloc - xs_paged_decode for callers that cannot allocate
+ * device memory.  The paper has no counterpart of this entry point: it is a
+ * service of this library.
+ *
+ * Who needs it: code that must not call cudaMalloc/cudaFree (or any
+ * allocating library routine) on its decode path - for example an engine
+ * that has already handed all free device memory to its own KV pool, a
+ * plugin whose host application owns every allocation, or a serving loop
+ * where an allocation could stall the device (cudaFree synchronises) or fail
+ * under memory pressure in the middle of a step.  Such callers still pass
+ * q, the pools, the tables and out, but not the split-K partials.
+ *
+ * The partials live in one array that the library defines at file scope in
+ * device memory, XS_NOALLOC_SCRATCH_BYTES (64 MiB) in size.  Every GPU that
+ * loads the library reserves that array until the process exits.  The call
+ * allocates nothing: it looks the array's device address up with
+ * cudaGetSymbolAddress the first time it runs on a device (with that device
+ * current) and caches it, so make that first call on each device before any
+ * stream capture.
+ *
+ * Arguments as xs_paged_decode, without part_o/part_m/part_l and
+ * max_partitions (derived as xs_paged_decode_max_partitions(
+ * max_blocks_per_seq, block_size, partition_tokens)).  partition_tokens <= 0
+ * picks the size with xs_paged_decode_partition_tokens for the current
+ * device, taking B * max_blocks_per_seq * block_size as the token count.
+ * Returns XS_ESCRATCH, before launching anything, when
+ * xs_paged_decode_workspace_bytes(B, Hq, D, max_partitions) exceeds
+ * XS_NOALLOC_SCRATCH_BYTES (choose a larger partition_tokens or a smaller
+ * batch).
+ *
+ * All calls share the one array and it keeps whatever the last call left
+ * there.  Nothing in it needs clearing: every partial the reduce reads is
+ * written by the attention pass of the same call first.  Two calls whose
+ * work overlaps on the GPU (different streams, or different host threads)
+ * race on the array and corrupt each other's results; order them on one
+ * stream or serialise them.
+ */
+#define XS_NOALLOC_SCRATCH_BYTES (64ull << 20)
+int xs_paged_decode_noalloc(void *out, const void *q, const void *k_cache, const void *v_cache,
+                            const int32_t *block_tables, int max_blocks_per_seq,
+                            const int32_t *context_lens, int B, int Hq, int Hkv, int D,
+                            int block_size, int64_t num_blocks, float scale,
+                            int partition_tokens, int dtype, int *err_flag,
+                            cudaStream_t stream);
 
 /*
  * xs_version - library version as MAJOR*10000 + MINOR*100 + PATCH.

@@ -720,3 +720,77 @@ extern "C" int xs_paged_decode(void *out, float *part_o, float *part_m, float *p
     return xs_paged_decode_reduce(out, part_o, part_m, part_l, context_lens, B, Hq, D,
                                   partition_tokens, max_partitions, dtype, stream);
 }
+
+// ---------------------------------------------------------------- no-allocation variant
+//
+// Split-K partials for callers that cannot allocate device memory: a fixed
+// array of XS_NOALLOC_SCRATCH_BYTES at file scope, reserved on every device
+// that loads this library.  Host code must not use the symbol itself as a
+// pointer (in host code it names a host-side stand-in), so its device
+// address is looked up once per device with cudaGetSymbolAddress and cached.
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[XS_NOALLOC_SCRATCH_BYTES];
+
+static int noalloc_scratch(unsigned char **out) {
+    static std::mutex mu;
+    static unsigned char *cache[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return XS_EDEVICE;
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache[dev] == nullptr) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+            return XS_EDEVICE;
+        cache[dev] = static_cast<unsigned char *>(p);
+    }
+    *out = cache[dev];
+    return XS_OK;
+}
+
+extern "C" int xs_paged_decode_noalloc(void *out, const void *q, const void *k_cache,
+                                       const void *v_cache, const int32_t *block_tables,
+                                       int max_blocks_per_seq, const int32_t *context_lens,
+                                       int B, int Hq, int Hkv, int D, int block_size,
+                                       int64_t num_blocks, float scale, int partition_tokens,
+                                       int dtype, int *err_flag, cudaStream_t stream) {
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || max_blocks_per_seq < 0 || block_size <= 0)
+        return XS_ESHAPE;
+    if (partition_tokens <= 0) {
+        attn::DeviceInfo dev;
+        const int st = attn::device_info(&dev);
+        if (st != XS_OK) return st;
+        partition_tokens = xs_paged_decode_partition_tokens(
+            B, Hkv, static_cast<int64_t>(B) * max_blocks_per_seq * block_size,
+            max_blocks_per_seq * block_size, dev.sms);
+        if (partition_tokens < 0) return partition_tokens;
+    }
+    const int max_parts =
+        xs_paged_decode_max_partitions(max_blocks_per_seq, block_size, partition_tokens);
+    if (max_parts < 0) return max_parts;
+    float *po = nullptr, *pm = nullptr, *pl = nullptr;
+    if (max_parts > 1 && B > 0) {
+        const size_t need = xs_paged_decode_workspace_bytes(B, Hq, D, max_parts);
+        if (need == 0) return XS_ESHAPE;
+        if (need > XS_NOALLOC_SCRATCH_BYTES) return XS_ESCRATCH;
+        // Validate everything else before touching the device.
+        const int st = check_attn_args(out, reinterpret_cast<float *>(256),
+                                       reinterpret_cast<float *>(256),
+                                       reinterpret_cast<float *>(256), q, k_cache, v_cache,
+                                       block_tables, max_blocks_per_seq, context_lens, B, Hq, Hkv,
+                                       D, block_size, num_blocks, partition_tokens, max_parts,
+                                       dtype);
+        if (st != XS_OK) return st;
+        unsigned char *base = nullptr;
+        const int sst = noalloc_scratch(&base);
+        if (sst != XS_OK) return sst;
+        const size_t n = static_cast<size_t>(B) * Hq * max_parts;
+        const size_t o_bytes = (n * D * 4 + 255) / 256 * 256;
+        const size_t ml_bytes = (n * 4 + 255) / 256 * 256;
+        po = reinterpret_cast<float *>(base);
+        pm = reinterpret_cast<float *>(base + o_bytes);
+        pl = reinterpret_cast<float *>(base + o_bytes + ml_bytes);
+    }
+    return xs_paged_decode(out, po, pm, pl, q, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                           context_lens, B, Hq, Hkv, D, block_size, num_blocks, scale,
+                           partition_tokens, max_parts, dtype, err_flag, stream);
+}

@@ -23,7 +23,9 @@ BLOCK_SIZE = 16
 STATUS = {
     0: "XS_OK", -1: "XS_ENULL", -2: "XS_ESHAPE", -3: "XS_EDTYPE", -4: "XS_EALIGN",
     -5: "XS_EUNSUPPORTED", -6: "XS_EWORKSPACE", -7: "XS_ELAUNCH", -8: "XS_EDEVICE",
+    -9: "XS_ESCRATCH",
 }
+NOALLOC_SCRATCH_BYTES = 64 << 20
 FLAG_BAD_BLOCK, FLAG_BAD_LEN, FLAG_BAD_SLOT, FLAG_TIMEOUT = 1, 2, 4, 8
 
 # name -> (restype, argtypes)
@@ -41,6 +43,8 @@ SIGNATURES = {
     "xs_paged_decode_reduce": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
     "xs_paged_decode": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _L, _F,
                              _I, _I, _I, _P, _P]),
+    "xs_paged_decode_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _L, _F,
+                                     _I, _I, _P, _P]),
     "xs_version": (_I, []),
 }
 
@@ -181,6 +185,19 @@ def xs_paged_decode(out, part_o, part_m, part_l, q, k_cache, v_cache, block_tabl
           _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1],
           _ptr(context_lens), B, Hq, Hkv, D, bs, num_blocks, float(scale), partition_tokens,
           max_partitions, dtype_code(q.dtype), _ptr(err_flag), _stream(stream))
+
+
+def xs_paged_decode_noalloc(out, q, k_cache, v_cache, block_tables, context_lens, scale,
+                            partition_tokens=0, err_flag=None, stream=None):
+    """xs_paged_decode without caller-provided partials: for callers that may
+    not allocate device memory; the split-K partials live in the library's
+    fixed 64 MiB device array (see include/xs_paged.h)."""
+    B, Hq, D = q.shape
+    num_blocks, Hkv, bs, _ = k_cache.shape
+    _call("xs_paged_decode_noalloc", _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+          _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), B, Hq, Hkv, D, bs,
+          num_blocks, float(scale), int(partition_tokens), dtype_code(q.dtype), _ptr(err_flag),
+          _stream(stream))
 
 
 def xs_version() -> int:
