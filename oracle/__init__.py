@@ -11,8 +11,8 @@ arguments.  Each function follows the definition cited in the C source:
 
 * ``slot_mapping``  - slot resolution of the token a decode step writes
   ("xserv compare phase10...cf1e9e4", attention.rs,
-  ``reshape_and_cache_batched_bf16``: kv_lens = index of the just-written
-  token + 1).
+  ``reshape_and_cache_batched_bf16``: the per-sequence length passed to the
+  append already counts the token being written).
 * ``kv_append``     - byte copy of each new K/V row into its pool slot (same
   page, ``reshape_and_cache_bf16`` pool layout).
 * ``paged_decode``  - softmax(scale * q K^T) V over every cached token of the

@@ -13,7 +13,7 @@
  *    and `paged_decode_attention`: the pool layout
  *    [num_blocks_total, num_kv_heads, block_size, head_dim], the block table
  *    [batch, max_blocks_per_seq] (int32), context lengths [batch] (int32) that
- *    count the just-written token, scale = 1/sqrt(head_dim), output
+ *    count the token written in this step, scale = 1/sqrt(head_dim), output
  *    [batch, num_q_heads, 1, head_dim].
  *  - "xserv compare phase5...phase9", docs/09-kv-cache.md, section
  *    "After (with cache)": a decode step appends the new K/V to the cache and
@@ -60,10 +60,10 @@ static int elem_bytes(int dtype) {
 }
 
 /*
- * Slot resolution for one decode step.  context_lens[b] counts the token
- * being written ("current seq_len + 1 - i.e. the index of the just-written
- * token + 1", reshape_and_cache_batched_bf16), so the new token's logical
- * position is p = context_lens[b] - 1 and it lives at
+ * Slot resolution for one decode step.  context_lens[b] already counts the
+ * token being written (the batched append of reshape_and_cache_batched_bf16
+ * takes the length after the step), so the new token's logical position is
+ * p = context_lens[b] - 1 and it lives at
  *     slot = block_tables[b][p / block_size] * block_size + p % block_size.
  * A sequence with context_lens[b] <= 0 writes nothing: slot -1.
  */

@@ -2,7 +2,7 @@
 // vectorised scatter of new K/V rows into their pool pages.
 //
 // Pool layout [num_blocks, Hkv, block_size, D] and the meaning of the
-// lengths ("index of the just-written token + 1") follow the xserv pages
+// lengths (they already count the token written in this step) follow the xserv pages
 // ("xserv compare phase10...cf1e9e4", crates/xserv-kernels/src/attention.rs,
 // reshape_and_cache_bf16 / reshape_and_cache_batched_bf16).
 #include "xs_common.cuh"
