@@ -144,12 +144,13 @@ int xs_kv_append_paged(const void *k_new, const void *v_new, void *k_cache, void
  * partition size (tokens, a multiple of 16) of xs_paged_decode_attn.
  *
  * Each sequence's context is cut into partitions of this many tokens; one
- * work item is (sequence, KV head, partition).  The size is the largest
- * power of two in [16, 2048] that still gives at least ~6 work items per
- * resident CTA on num_sms SMs, so a persistent grid stays busy to the end.
- * total_context_tokens = sum of context_lens (pass <= 0 if unknown:
- * B * max_context_len is used).  Returns the partition size (>= 16), or a
- * negative XS_E* code.
+ * work item is (sequence, KV head, partition).  The heuristic picks the
+ * power of two in [64, 2048] that minimises a simple cost model: items per
+ * resident CTA (2 per SM) plus one, times the time of one item (its pages
+ * spread over 4 consumer warps plus a fixed per-item cost for staging q,
+ * merging and the partials).  total_context_tokens = sum of context_lens
+ * (pass <= 0 if unknown: B * max_context_len is used).  Returns the
+ * partition size, or a negative XS_E* code.
  */
 int xs_paged_decode_partition_tokens(int B, int Hkv, int64_t total_context_tokens,
                                      int max_context_len, int num_sms);
@@ -192,6 +193,15 @@ size_t xs_paged_decode_workspace_bytes(int B, int Hq, int D, int max_partitions)
  * max_partitions must be >= xs_paged_decode_max_partitions(...); part_* may
  * be NULL only when max_partitions == 1.
  *
+ * Scheduling: a persistent grid (resident CTAs on every SM) takes the work
+ * items.  With work_counters == NULL, CTA c takes items c, c + grid, ...
+ * With work_counters (2 ints on the device, zero before the first launch
+ * that uses them), CTAs take the next item from work_counters[0] as they
+ * finish, which balances ragged batches; the last CTA of every launch sets
+ * both ints back to zero.  Launches sharing one work_counters buffer must be
+ * ordered (one stream); if a launch is abandoned, zero the buffer before the
+ * next one.
+ *
  * q [B, Hq, D]; out [B, Hq, D]; k_cache, v_cache [num_blocks, Hkv, bs, D];
  * block_tables int32 [B, max_blocks_per_seq]; context_lens int32 [B].
  * Device-side errors: XS_FLAG_BAD_BLOCK, XS_FLAG_BAD_LEN, XS_FLAG_TIMEOUT.
@@ -202,7 +212,7 @@ int xs_paged_decode_attn(void *out, float *part_o, float *part_m, float *part_l,
                          const int32_t *context_lens, int B, int Hq, int Hkv, int D,
                          int block_size, int64_t num_blocks, float scale,
                          int partition_tokens, int max_partitions, int dtype, int *err_flag,
-                         cudaStream_t stream);
+                         int *work_counters, cudaStream_t stream);
 
 /*
  * xs_paged_decode_reduce - split-K combine.  For every sequence with more
@@ -227,7 +237,8 @@ int xs_paged_decode(void *out, float *part_o, float *part_m, float *part_l, cons
                     const void *k_cache, const void *v_cache, const int32_t *block_tables,
                     int max_blocks_per_seq, const int32_t *context_lens, int B, int Hq, int Hkv,
                     int D, int block_size, int64_t num_blocks, float scale, int partition_tokens,
-                    int max_partitions, int dtype, int *err_flag, cudaStream_t stream);
+                    int max_partitions, int dtype, int *err_flag, int *work_counters,
+                    cudaStream_t stream);
 
 /*
  * xs_paged_decode_noalloc - xs_paged_decode for callers that cannot allocate

@@ -30,6 +30,7 @@
 //  * Logits are kept in base-2 units (q is pre-scaled by scale*log2(e)) so
 //    exponentials are single ex2 instructions.
 #include <algorithm>
+#include <cmath>
 #include <mutex>
 
 #include "xs_common.cuh"
@@ -40,7 +41,6 @@ namespace attn {
 constexpr int kBlock = 16;          // tokens per page
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = 32 * (kConsumerWarps + 1);
-constexpr int kStages = 8;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s per bounded wait
 constexpr int kMaxBatch = 16384;                  // prefix sums live in shared memory
@@ -49,6 +49,12 @@ template <typename T, int D, int G>
 struct Cfg {
     static constexpr int kRowBytes = D * static_cast<int>(sizeof(T));
     static constexpr int kPageBytes = kBlock * kRowBytes;
+    // Ring of page pairs.  Page c goes to stage c % kStages and to consumer
+    // warp c % kConsumerWarps; kStages must be a multiple of kConsumerWarps so
+    // every stage is only ever used by one warp.  Otherwise a warp could wait
+    // for phase k of a stage whose phase k-1 (another warp's page) has not
+    // completed yet, and a parity wait cannot tell phase k from phase k-2.
+    static constexpr int kStages = 2 * kConsumerWarps;
     static constexpr int kChunksPerRow = kRowBytes / 16;
     static constexpr int kChunksPerLane = kChunksPerRow / 8;   // QK: 8 lanes per token
     static constexpr int kElemsPerChunk = 16 / static_cast<int>(sizeof(T));
@@ -58,19 +64,23 @@ struct Cfg {
     static constexpr int kQBytes = G * kRowBytes;
     static constexpr int kLogG = G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : 3;
     static constexpr int kHeadShift = 3 - kLogG;  // lane j of a token group owns head j >> shift
+    // Resident CTAs per SM the register budget is sized for.
+    static constexpr int kMinBlocks = G == 8 ? 1 : ((2 * kPageBytes <= 4096) ? 3 : 2);
     // Shared memory carve-up (bytes).
     static constexpr int kRingBytes = kStages * 2 * kPageBytes;
     static constexpr int kQSlotOff = kRingBytes;
     static constexpr int kWOff = kQSlotOff + 2 * kQBytes;
-    static constexpr int kWBytes = kConsumerWarps * kBlock * G * 4;
+    static constexpr int kWBytes = kConsumerWarps * kBlock * G * 8;   // (w, w) pairs
     static constexpr int kCombOff = kWOff + kWBytes;
     static constexpr int kCombBytes = kConsumerWarps * G * (D + 2) * 4;
     static constexpr int kBarOff = (kCombOff + kCombBytes + 7) / 8 * 8;
     static constexpr int kBarBytes = (2 * kStages + 4) * 8;
-    static constexpr int kPrefixOff = kBarOff + kBarBytes;
+    static constexpr int kItemOff = kBarOff + kBarBytes;             // 2 published items
+    static constexpr int kPrefixOff = kItemOff + 2 * 32;
     static __host__ __device__ constexpr int smem_bytes(int B) { return kPrefixOff + 4 * (B + 1); }
+    static_assert(kStages % kConsumerWarps == 0, "each ring stage must belong to one consumer");
     static_assert(kChunksPerLane >= 1 && kChunksPerRow % 8 == 0, "row must split over 8 lanes");
-    static_assert(D % 32 == 0, "D must split over 32 lanes");
+    static_assert(D % 64 == 0, "PV works on dim pairs: D must split over 32 lanes x 2");
 };
 
 struct Params {
@@ -82,6 +92,7 @@ struct Params {
     int64_t num_blocks;
     float qscale;  // scale * log2(e)
     int *err_flag;
+    int *work;     // [2] item counter + finished-CTA counter (zero between launches), or null
 };
 
 // Number of tokens sequence b attends to, clamped to the table's reach.
@@ -98,6 +109,7 @@ __device__ __forceinline__ int seq_len(const Params &p, int b, bool report) {
 struct Item {
     int b, g, part, n, tok0, tok1, pg0, pg1;
 };
+static_assert(sizeof(Item) == 32, "item slots are 32 bytes");
 
 __device__ __forceinline__ Item decode_item(const Params &p, const int *prefix, int item) {
     // Largest b with prefix[b] <= item.
@@ -120,16 +132,164 @@ __device__ __forceinline__ Item decode_item(const Params &p, const int *prefix, 
     return it;
 }
 
-template <typename T, int D, int G>
-__global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const Params p) {
+// Load kPvDims consecutive elements of a V row (one lane's share) as fp32.
+template <typename T, int kPvDims>
+__device__ __forceinline__ void load_v(const unsigned char *src, float *vf) {
+    if constexpr (sizeof(T) == 2 && kPvDims == 2) {
+        const uint32_t raw = *reinterpret_cast<const uint32_t *>(src);
+        vf[0] = __uint_as_float(raw << 16);
+        vf[1] = __uint_as_float(raw & 0xffff0000u);
+    } else if constexpr (sizeof(T) == 2 && kPvDims == 4) {
+        const uint2 raw = *reinterpret_cast<const uint2 *>(src);
+        vf[0] = __uint_as_float(raw.x << 16);
+        vf[1] = __uint_as_float(raw.x & 0xffff0000u);
+        vf[2] = __uint_as_float(raw.y << 16);
+        vf[3] = __uint_as_float(raw.y & 0xffff0000u);
+    } else if constexpr (sizeof(T) == 4 && kPvDims == 2) {
+        const float2 raw = *reinterpret_cast<const float2 *>(src);
+        vf[0] = raw.x;
+        vf[1] = raw.y;
+    } else {
+        static_assert(sizeof(T) == 4 && kPvDims == 4, "unsupported V row split");
+        const float4 raw = *reinterpret_cast<const float4 *>(src);
+        vf[0] = raw.x;
+        vf[1] = raw.y;
+        vf[2] = raw.z;
+        vf[3] = raw.w;
+    }
+}
+
+// One consumer warp folds one page (16 tokens of one KV head) into its
+// online-softmax state.  kFull: all 16 tokens are valid (every page but a
+// sequence's last), which lets the PV loop unroll completely.
+template <typename T, int D, int G, bool kFull>
+__device__ __forceinline__ void consume_page(const unsigned char *Ks, const unsigned char *Vs,
+                                             int n_valid, const float (&qf)[G][D / 8],
+                                             float &m_own, float &l_own,
+                                             float2 (&o)[G][D / 64], float2 *W2, int lane) {
     using C = Cfg<T, D, G>;
+    const int tg = lane >> 3, j = lane & 7;
+    const int own_head = j >> C::kHeadShift;
+
+    // ---- QK: 4 passes x 4 tokens; lane (tg, j) covers dims of chunks j, j+8, ...
+    float sc[4];
+#pragma unroll
+    for (int pass = 0; pass < 4; ++pass) {
+        const int t = pass * 4 + tg;
+        float2 acc[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h) acc[h] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int c = 0; c < C::kChunksPerLane; ++c) {
+            const uint4 raw =
+                *reinterpret_cast<const uint4 *>(Ks + t * C::kRowBytes + (j + 8 * c) * 16);
+            float f[C::kElemsPerChunk];
+            unpack16(raw, f, static_cast<T *>(nullptr));
+#pragma unroll
+            for (int e = 0; e < C::kElemsPerChunk; e += 2) {
+                const float2 kv = make_float2(f[e], f[e + 1]);
+#pragma unroll
+                for (int h = 0; h < G; ++h)
+                    acc[h] = __ffma2_rn(make_float2(qf[h][c * C::kElemsPerChunk + e],
+                                                    qf[h][c * C::kElemsPerChunk + e + 1]),
+                                        kv, acc[h]);
+            }
+        }
+        float v[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h) v[h] = acc[h].x + acc[h].y;
+        // Reduce-scatter over the 8 lanes of the token group: lane j keeps head j >> shift.
+        int cnt = G;
+#pragma unroll
+        for (int mask = 4; mask >= 1; mask >>= 1) {
+            if (cnt > 1) {
+                const int half = cnt >> 1;
+                const bool upper = (lane & mask) != 0;
+#pragma unroll
+                for (int i = 0; i < (G > 1 ? G / 2 : 1); ++i) {
+                    if (i < half) {
+                        const float send = upper ? v[i] : v[i + half];
+                        const float keep = upper ? v[i + half] : v[i];
+                        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, mask);
+                    }
+                }
+                cnt = half;
+            } else {
+                v[0] += __shfl_xor_sync(0xffffffffu, v[0], mask);
+            }
+        }
+        sc[pass] = (kFull || t < n_valid) ? v[0] : -INFINITY;
+    }
+
+    // ---- online softmax for head own_head (lanes sharing j agree)
+    float pm = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
+    pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 8));
+    pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 16));
+    const float m_new = fmaxf(m_own, pm);
+    const float corr_own = fast_exp2(m_own - m_new);
+    m_own = m_new;
+    float w[4], ps = 0.f;
+#pragma unroll
+    for (int pass = 0; pass < 4; ++pass) {
+        w[pass] = fast_exp2(sc[pass] - m_new);
+        ps += w[pass];
+    }
+    ps += __shfl_xor_sync(0xffffffffu, ps, 8);
+    ps += __shfl_xor_sync(0xffffffffu, ps, 16);
+    l_own = l_own * corr_own + ps;
+    if ((j & ((1 << C::kHeadShift) - 1)) == 0) {
+#pragma unroll
+        for (int pass = 0; pass < 4; ++pass)
+            W2[(pass * 4 + tg) * G + own_head] = make_float2(w[pass], w[pass]);
+    }
+    float2 corr[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+        const float c = __shfl_sync(0xffffffffu, corr_own, h << C::kHeadShift);
+        corr[h] = make_float2(c, c);
+    }
+    __syncwarp();
+
+    // ---- PV: lane owns dims [lane*kPvDims, +kPvDims) of every head
+#pragma unroll
+    for (int h = 0; h < G; ++h)
+#pragma unroll
+        for (int d = 0; d < C::kPvDims / 2; ++d) o[h][d] = __fmul2_rn(o[h][d], corr[h]);
+    const unsigned char *vrow = Vs + lane * C::kPvBytes;
+    auto pv_token = [&](int t) {
+        float vf[C::kPvDims];
+        load_v<T, C::kPvDims>(vrow + t * C::kRowBytes, vf);
+        const float2 *wt = W2 + t * G;
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            const float2 wh = wt[h];
+#pragma unroll
+            for (int d = 0; d < C::kPvDims / 2; ++d)
+                o[h][d] = __ffma2_rn(wh, make_float2(vf[2 * d], vf[2 * d + 1]), o[h][d]);
+        }
+    };
+    if constexpr (kFull) {
+#pragma unroll
+        for (int t = 0; t < kBlock; ++t) pv_token(t);
+    } else {
+        for (int t = 0; t < n_valid; ++t) pv_token(t);
+    }
+    __syncwarp();
+}
+
+template <typename T, int D, int G>
+__global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
+    paged_decode_kernel(const Params p) {
+    using C = Cfg<T, D, G>;
+    constexpr int kStages = C::kStages;
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::kBarOff);
     uint64_t *empty = full + kStages;
     uint64_t *qfull = empty + kStages;
     uint64_t *qempty = qfull + 2;
+    Item *item_slot = reinterpret_cast<Item *>(smem + C::kItemOff);
     int *prefix = reinterpret_cast<int *>(smem + C::kPrefixOff);
-    __shared__ int s_abort, s_stop;
+    __shared__ int s_abort, s_stop, s_done;
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
@@ -147,6 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const Params 
         mbar_fence_init();
         s_abort = 0;
         s_stop = 0;
+        s_done = 0;
     }
     {
         // Items of sequence b: ceil(n/P) partitions x Hkv heads.  Chunked scan.
@@ -188,27 +349,52 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const Params 
 
     if (warp == 0) {
         // ================================================================ producer
+        // Takes items (from the shared work counter, or blockIdx.x + k*gridDim.x
+        // without one), publishes each item's ranges and q rows in a
+        // double-buffered slot, then streams its pages into the ring.  An item
+        // with b < 0 tells the consumers to stop.
         const uint64_t pol = policy_evict_first();
         const unsigned char *kbase = static_cast<const unsigned char *>(p.k_cache);
         const unsigned char *vbase = static_cast<const unsigned char *>(p.v_cache);
         const unsigned char *qbase = static_cast<const unsigned char *>(p.q);
         uint32_t page_ctr = 0, item_ctr = 0;
+        int static_next = blockIdx.x;
         bool ok = true;
-        for (int item = blockIdx.x; ok && item < total_items; item += gridDim.x, ++item_ctr) {
-            const Item it = decode_item(p, prefix, item);
+        while (ok) {
+            int item = 0;
+            if (lane == 0) {
+                item = p.work ? atomicAdd(&p.work[0], 1) : static_next;
+                static_next += gridDim.x;
+            }
+            item = __shfl_sync(0xffffffffu, item, 0);
+            const bool last = item >= total_items;
+            Item it;
+            if (!last) {
+                it = decode_item(p, prefix, item);
+            } else {
+                it.b = -1;
+                it.pg0 = it.pg1 = 0;
+            }
             if (lane == 0) {
                 const uint32_t slot = item_ctr & 1, k = item_ctr >> 1;
                 ok = mbar_wait_bounded(&qempty[slot], (k & 1) ^ 1, kWaitLimitNs);
                 if (ok) {
-                    unsigned char *dst = smem + C::kQSlotOff + slot * C::kQBytes;
-                    const int64_t qoff =
-                        (static_cast<int64_t>(it.b) * p.Hq + static_cast<int64_t>(it.g) * G) *
-                        C::kRowBytes;
-                    mbar_arrive_expect_tx(&qfull[slot], C::kQBytes);
-                    bulk_g2s(dst, qbase + qoff, C::kQBytes, &qfull[slot]);
+                    item_slot[slot] = it;
+                    if (last) {
+                        mbar_arrive(&qfull[slot]);
+                    } else {
+                        unsigned char *dst = smem + C::kQSlotOff + slot * C::kQBytes;
+                        const int64_t qoff = (static_cast<int64_t>(it.b) * p.Hq +
+                                              static_cast<int64_t>(it.g) * G) *
+                                             C::kRowBytes;
+                        mbar_arrive_expect_tx(&qfull[slot], C::kQBytes);
+                        bulk_g2s(dst, qbase + qoff, C::kQBytes, &qfull[slot]);
+                    }
                 }
             }
             ok = __shfl_sync(0xffffffffu, ok, 0);
+            ++item_ctr;
+            if (last) break;
             const int32_t *row = p.block_tables + static_cast<int64_t>(it.b) * p.max_blocks;
             for (int base = it.pg0; ok && base < it.pg1; base += 32) {
                 int32_t blk = 0;
@@ -241,38 +427,51 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const Params 
                 }
             }
         }
-        if (!ok && lane == 0) {
-            raise_flag(p.err_flag, XS_FLAG_TIMEOUT);
-            atomicExch(&s_abort, 1);
-            // Drain: let every copy this CTA issued land before the CTA exits.
-            const uint32_t first = page_ctr > kStages ? page_ctr - kStages : 0;
-            for (uint32_t c = first; c < page_ctr; ++c)
-                mbar_wait_bounded(&full[c % kStages], (c / kStages) & 1, kWaitLimitNs);
+        if (lane == 0) {
+            if (!ok) {
+                raise_flag(p.err_flag, XS_FLAG_TIMEOUT);
+                atomicExch(&s_abort, 1);
+                // Drain: let every copy this CTA issued land before the CTA exits.
+                const uint32_t first = page_ctr > kStages ? page_ctr - kStages : 0;
+                for (uint32_t c = first; c < page_ctr; ++c)
+                    mbar_wait_bounded(&full[c % kStages], (c / kStages) & 1, kWaitLimitNs);
+            }
+            if (p.work) {
+                // The last CTA to stop taking items resets the counters for the
+                // next launch on this workspace.
+                __threadfence();
+                if (atomicAdd(&p.work[1], 1) == static_cast<int>(gridDim.x) - 1) {
+                    atomicExch(&p.work[0], 0);
+                    atomicExch(&p.work[1], 0);
+                }
+            }
         }
         return;
     }
 
     // ==================================================================== consumers
     const int cw = warp - 1;
-    const int tg = lane >> 3, j = lane & 7;
-    const int own_head = j >> C::kHeadShift;
-    float *Wbuf = reinterpret_cast<float *>(smem + C::kWOff) + cw * kBlock * G;
+    const int j = lane & 7;
+    float2 *W2 = reinterpret_cast<float2 *>(smem + C::kWOff) + cw * kBlock * G;
     float *cM = reinterpret_cast<float *>(smem + C::kCombOff);
     float *cL = cM + kConsumerWarps * G;
     float *cO = cL + kConsumerWarps * G;
     const int ctid = tid - 32;
     uint32_t page_ctr = 0, item_ctr = 0;
 
-    for (int item = blockIdx.x; item < total_items; item += gridDim.x, ++item_ctr) {
-        const Item it = decode_item(p, prefix, item);
-        // ---- q rows of the group (scaled into base-2 logits)
-        // A failed wait marks the item bad: the warp skips its pages but still
-        // takes part in both merge barriers, so no consumer is left waiting.
-        bool bad = false;
+    for (;; ++item_ctr) {
+        // A failed wait marks the item bad, and the producer's end marker
+        // (b < 0) marks it done: either way the warp skips the pages but still
+        // takes part in both merge barriers, and all consumers leave the loop
+        // together after the second one, so none is left waiting.
+        const uint32_t slot = item_ctr & 1;
+        bool bad = !__all_sync(0xffffffffu,
+                               mbar_wait_bounded(&qfull[slot], (item_ctr >> 1) & 1, kWaitLimitNs));
+        Item it = item_slot[slot];
+        const bool done = !bad && it.b < 0;
+        if (done && lane == 0) *static_cast<volatile int *>(&s_done) = 1;
         float qf[G][C::kQkDims];
         {
-            const uint32_t slot = item_ctr & 1, k = item_ctr >> 1;
-            bad = !__all_sync(0xffffffffu, mbar_wait_bounded(&qfull[slot], k & 1, kWaitLimitNs));
             const unsigned char *qs = smem + C::kQSlotOff + slot * C::kQBytes;
 #pragma unroll
             for (int h = 0; h < G; ++h)
@@ -287,19 +486,27 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const Params 
                         qf[h][c * C::kElemsPerChunk + e] = f[e] * p.qscale;
                 }
             __syncwarp();
-            if (lane == 0 && !bad) mbar_arrive(&qempty[slot]);
+            if (lane == 0 && !bad && !done) mbar_arrive(&qempty[slot]);
+        }
+        if (bad || done) {
+            it.b = -1;
+            it.pg0 = it.pg1 = 0;
         }
 
         float m_own = -INFINITY, l_own = 0.f;
-        float o[G][C::kPvDims];
+        float2 o[G][C::kPvDims / 2];
 #pragma unroll
         for (int h = 0; h < G; ++h)
 #pragma unroll
-            for (int d = 0; d < C::kPvDims; ++d) o[h][d] = 0.f;
+            for (int d = 0; d < C::kPvDims / 2; ++d) o[h][d] = make_float2(0.f, 0.f);
 
-        for (int pg = it.pg0; pg < it.pg1 && !bad; ++pg, ++page_ctr) {
-            if ((page_ctr % kConsumerWarps) != static_cast<uint32_t>(cw)) continue;
-            const uint32_t s = page_ctr % kStages, k = page_ctr / kStages;
+        // Pages of this item for this warp: page_ctr advances over every page of
+        // the item; this warp takes those with page_ctr % kConsumerWarps == cw.
+        const int first = (cw - static_cast<int>(page_ctr % kConsumerWarps) + kConsumerWarps) %
+                          kConsumerWarps;
+        for (int pg = it.pg0 + first; pg < it.pg1; pg += kConsumerWarps) {
+            const uint32_t c = page_ctr + (pg - it.pg0);
+            const uint32_t s = c % kStages, k = c / kStages;
             if (!__all_sync(0xffffffffu, mbar_wait_bounded(&full[s], k & 1, kWaitLimitNs)) ||
                 *static_cast<volatile int *>(&s_abort)) {
                 bad = true;
@@ -308,134 +515,13 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const Params 
             const unsigned char *Ks = smem + s * 2 * C::kPageBytes;
             const unsigned char *Vs = Ks + C::kPageBytes;
             const int n_valid = min(kBlock, it.tok1 - pg * kBlock);
-
-            // ---- QK: 4 passes x 4 tokens; lane (tg, j) covers dims of chunks j, j+8, ...
-            float sc[4];
-#pragma unroll
-            for (int pass = 0; pass < 4; ++pass) {
-                const int t = pass * 4 + tg;
-                float2 acc[G];
-#pragma unroll
-                for (int h = 0; h < G; ++h) acc[h] = make_float2(0.f, 0.f);
-#pragma unroll
-                for (int c = 0; c < C::kChunksPerLane; ++c) {
-                    const uint4 raw =
-                        *reinterpret_cast<const uint4 *>(Ks + t * C::kRowBytes + (j + 8 * c) * 16);
-                    float f[C::kElemsPerChunk];
-                    unpack16(raw, f, static_cast<T *>(nullptr));
-#pragma unroll
-                    for (int e = 0; e < C::kElemsPerChunk; e += 2) {
-                        const float2 kv = make_float2(f[e], f[e + 1]);
-#pragma unroll
-                        for (int h = 0; h < G; ++h) {
-                            const float2 qv = make_float2(qf[h][c * C::kElemsPerChunk + e],
-                                                          qf[h][c * C::kElemsPerChunk + e + 1]);
-                            acc[h] = __ffma2_rn(qv, kv, acc[h]);
-                        }
-                    }
-                }
-                float v[G];
-#pragma unroll
-                for (int h = 0; h < G; ++h) v[h] = acc[h].x + acc[h].y;
-                // Reduce-scatter over the 8 lanes of the token group.
-                int cnt = G;
-#pragma unroll
-                for (int mask = 4; mask >= 1; mask >>= 1) {
-                    if (cnt > 1) {
-                        const int half = cnt >> 1;
-                        const bool upper = (lane & mask) != 0;
-#pragma unroll
-                        for (int i = 0; i < G / 2; ++i) {
-                            if (i < half) {
-                                const float send = upper ? v[i] : v[i + half];
-                                const float keep = upper ? v[i + half] : v[i];
-                                v[i] = keep + __shfl_xor_sync(0xffffffffu, send, mask);
-                            }
-                        }
-                        cnt = half;
-                    } else {
-                        v[0] += __shfl_xor_sync(0xffffffffu, v[0], mask);
-                    }
-                }
-                sc[pass] = (t < n_valid) ? v[0] : -INFINITY;
-            }
-
-            // ---- online softmax for head own_head (lanes sharing j agree)
-            float pm = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
-            pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 8));
-            pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 16));
-            const float m_new = fmaxf(m_own, pm);
-            const float corr_own = fast_exp2(m_own - m_new);
-            m_own = m_new;
-            float w[4], ps = 0.f;
-#pragma unroll
-            for (int pass = 0; pass < 4; ++pass) {
-                w[pass] = fast_exp2(sc[pass] - m_new);
-                ps += w[pass];
-            }
-            ps += __shfl_xor_sync(0xffffffffu, ps, 8);
-            ps += __shfl_xor_sync(0xffffffffu, ps, 16);
-            l_own = l_own * corr_own + ps;
-            if ((j & ((1 << C::kHeadShift) - 1)) == 0) {
-#pragma unroll
-                for (int pass = 0; pass < 4; ++pass) Wbuf[(pass * 4 + tg) * G + own_head] = w[pass];
-            }
-            float corr[G];
-#pragma unroll
-            for (int h = 0; h < G; ++h)
-                corr[h] = __shfl_sync(0xffffffffu, corr_own, h << C::kHeadShift);
-            __syncwarp();
-
-            // ---- PV: lane owns dims [lane*kPvDims, +kPvDims) of every head
-#pragma unroll
-            for (int h = 0; h < G; ++h)
-#pragma unroll
-                for (int d = 0; d < C::kPvDims; ++d) o[h][d] *= corr[h];
-            for (int t = 0; t < n_valid; ++t) {
-                float vf[C::kPvDims];
-                const unsigned char *src = Vs + t * C::kRowBytes + lane * C::kPvBytes;
-                if constexpr (C::kPvBytes == 4) {
-                    const uint32_t raw = *reinterpret_cast<const uint32_t *>(src);
-                    if constexpr (sizeof(T) == 2) {
-                        vf[0] = __uint_as_float(raw << 16);
-                        vf[1] = __uint_as_float(raw & 0xffff0000u);
-                    } else {
-                        vf[0] = __uint_as_float(raw);
-                    }
-                } else if constexpr (C::kPvBytes == 8) {
-                    const uint2 raw = *reinterpret_cast<const uint2 *>(src);
-                    if constexpr (sizeof(T) == 2) {
-                        vf[0] = __uint_as_float(raw.x << 16);
-                        vf[1] = __uint_as_float(raw.x & 0xffff0000u);
-                        vf[2] = __uint_as_float(raw.y << 16);
-                        vf[3] = __uint_as_float(raw.y & 0xffff0000u);
-                    } else {
-                        vf[0] = __uint_as_float(raw.x);
-                        vf[1] = __uint_as_float(raw.y);
-                    }
-                } else {
-                    const uint4 raw = *reinterpret_cast<const uint4 *>(src);
-                    unpack16(raw, vf, static_cast<T *>(nullptr));
-                }
-                float wt[G];
-#pragma unroll
-                for (int h = 0; h < G; ++h) wt[h] = Wbuf[t * G + h];
-#pragma unroll
-                for (int h = 0; h < G; ++h)
-#pragma unroll
-                    for (int d = 0; d < C::kPvDims; d += 2) {
-                        if constexpr (C::kPvDims >= 2) {
-                            float2 acc = make_float2(o[h][d], o[h][d + 1]);
-                            acc = __ffma2_rn(make_float2(wt[h], wt[h]),
-                                             make_float2(vf[d], vf[d + 1]), acc);
-                            o[h][d] = acc.x;
-                            o[h][d + 1] = acc.y;
-                        }
-                    }
-            }
-            __syncwarp();
+            if (n_valid == kBlock)
+                consume_page<T, D, G, true>(Ks, Vs, kBlock, qf, m_own, l_own, o, W2, lane);
+            else
+                consume_page<T, D, G, false>(Ks, Vs, n_valid, qf, m_own, l_own, o, W2, lane);
             if (lane == 0) mbar_arrive(&empty[s]);
         }
+        page_ctr += static_cast<uint32_t>(it.pg1 - it.pg0);
         if (bad && lane == 0) {
             raise_flag(p.err_flag, XS_FLAG_TIMEOUT);
             atomicExch(&s_abort, 1);
@@ -445,17 +531,22 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const Params 
 #pragma unroll
         for (int h = 0; h < G; ++h)
 #pragma unroll
-            for (int d = 0; d < C::kPvDims; ++d)
-                cO[(cw * G + h) * D + lane * C::kPvDims + d] = o[h][d];
-        if (tg == 0 && (j & ((1 << C::kHeadShift) - 1)) == 0) {
+            for (int d = 0; d < C::kPvDims / 2; ++d)
+                *reinterpret_cast<float2 *>(&cO[(cw * G + h) * D + lane * C::kPvDims + 2 * d]) =
+                    o[h][d];
+        if (lane < 8 && (j & ((1 << C::kHeadShift) - 1)) == 0) {
+            const int own_head = j >> C::kHeadShift;
             cM[cw * G + own_head] = m_own;
             cL[cw * G + own_head] = l_own;
         }
         named_barrier_sync(1, 32 * kConsumerWarps);
-        if (ctid == 0) s_stop = s_abort;
+        if (ctid == 0) s_stop = s_abort | s_done;
+        const bool valid = it.b >= 0 && it.b < p.B && it.g >= 0 && it.g < p.Hkv &&
+                           it.part >= 0 && it.part < p.max_parts &&
+                           !*static_cast<volatile int *>(&s_abort);
         const bool single = (it.n + p.P - 1) / p.P == 1;
         const int64_t head0 = static_cast<int64_t>(it.b) * p.Hq + static_cast<int64_t>(it.g) * G;
-        for (int idx = ctid; idx < G * D; idx += 32 * kConsumerWarps) {
+        for (int idx = ctid; valid && idx < G * D; idx += 32 * kConsumerWarps) {
             const int h = idx / D, d = idx - (idx / D) * D;
             float mx = -INFINITY;
 #pragma unroll
@@ -498,9 +589,11 @@ __global__ void paged_decode_reduce_kernel(T *__restrict__ out, const float *__r
     if (np <= 1) return;
     const int64_t base = static_cast<int64_t>(bh) * max_parts;
     float mx = -INFINITY;
+#pragma unroll 8
     for (int i = 0; i < np; ++i) mx = fmaxf(mx, part_m[base + i]);
     const int d = threadIdx.x;
     float lt = 0.f, acc = 0.f;
+#pragma unroll 8
     for (int i = 0; i < np; ++i) {
         const float f = fast_exp2(part_m[base + i] - mx) * part_l[base + i];
         lt += f;
@@ -562,16 +655,51 @@ int device_info(DeviceInfo *info) {
 }
 
 // Resident CTAs per SM for a kernel at a given dynamic smem size (raises the
-// kernel's smem limit first).
+// kernel's smem limit first).  Cached per (kernel, device, smem size).
 int occupancy(KernelFn fn, int smem, int *per_sm) {
-    if (cudaFuncSetAttribute(reinterpret_cast<const void *>(fn),
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-        return XS_ELAUNCH;
+    struct Entry {
+        KernelFn fn;
+        int dev, smem, per_sm;
+    };
+    static std::mutex mu;
+    static Entry cache[64];
+    static int n_cached = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return XS_EDEVICE;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < n_cached; ++i)
+        if (cache[i].fn == fn && cache[i].dev == dev && cache[i].smem == smem) {
+            *per_sm = cache[i].per_sm;
+            return XS_OK;
+        }
+    // Allow the kernel the device's whole opt-in shared memory once; the
+    // attribute is never lowered, so any cached size stays launchable.
+    bool raised = false;
+    for (int i = 0; i < n_cached; ++i) raised |= cache[i].fn == fn && cache[i].dev == dev;
+    if (!raised) {
+        // Opt-in maximum minus the kernel's own static shared memory.
+        int max_optin = 0;
+        cudaFuncAttributes fa;
+        if (cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+                cudaSuccess ||
+            cudaFuncGetAttributes(&fa, reinterpret_cast<const void *>(fn)) != cudaSuccess ||
+            cudaFuncSetAttribute(reinterpret_cast<const void *>(fn),
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 max_optin - static_cast<int>(fa.sharedSizeBytes)) !=
+                cudaSuccess) {
+            cudaGetLastError();  // do not leave the failure for an unrelated later check
+            return XS_ELAUNCH;
+        }
+    }
     int n = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, reinterpret_cast<const void *>(fn),
-                                                      kThreads, smem) != cudaSuccess)
+                                                      kThreads, smem) != cudaSuccess) {
+        cudaGetLastError();
         return XS_ELAUNCH;
+    }
     *per_sm = n > 0 ? n : 1;
+    Entry e{fn, dev, smem, *per_sm};
+    if (n_cached < 64) cache[n_cached++] = e;  // a full cache just stops caching
     return XS_OK;
 }
 
@@ -585,18 +713,30 @@ extern "C" int xs_version(void) { return 100; }
 extern "C" int xs_paged_decode_partition_tokens(int B, int Hkv, int64_t total_context_tokens,
                                                 int max_context_len, int num_sms) {
     if (B < 0 || Hkv <= 0 || max_context_len < 0 || num_sms <= 0) return XS_ESHAPE;
-    int64_t tokens = total_context_tokens > 0
-                         ? total_context_tokens
-                         : static_cast<int64_t>(B) * std::max(max_context_len, 1);
-    // Aim for >= 6 items per resident CTA (2 CTAs per SM assumed).
-    const int64_t want_items = static_cast<int64_t>(num_sms) * 2 * 6;
-    int P = 2048;
-    while (P > attn::kBlock) {
-        const int64_t items = (tokens / P + B) * Hkv;  // each sequence adds at most one ragged tail
-        if (items >= want_items) break;
-        P >>= 1;
+    if (B == 0) return 64;
+    const double tokens = total_context_tokens > 0
+                              ? static_cast<double>(total_context_tokens)
+                              : static_cast<double>(B) * std::max(max_context_len, 1);
+    // Cost model, in units of "one page per consumer warp": an item of P
+    // tokens costs P/16/4 + kItemCost (q staging, the four-warp merge and the
+    // partials it writes and the reduce reads back); items are taken by
+    // 2 resident CTAs per SM, so the step takes about items / CTAs + 1 item
+    // times (the last round is ragged).  Each sequence adds about half a
+    // partition of ragged tail.  At
+    // least 4 pages per item, so every consumer warp has a page.
+    constexpr double kItemCost = 1.5;
+    const double ctas = 2.0 * num_sms;
+    int best = 64;
+    double best_cost = 1e300;
+    for (int P = 64; P <= 2048; P *= 2) {
+        const double items = std::max((tokens / P + 0.5 * B) * Hkv, static_cast<double>(B) * Hkv);
+        const double cost = (items / ctas + 1.0) * (P / 64.0 + kItemCost);
+        if (cost <= best_cost * (1.0 + 1e-9)) {  // ties go to the larger partition
+            best_cost = cost;
+            best = P;
+        }
     }
-    return P;
+    return best;
 }
 
 extern "C" int xs_paged_decode_max_partitions(int max_blocks_per_seq, int block_size,
@@ -639,7 +779,7 @@ extern "C" int xs_paged_decode_attn(void *out, float *part_o, float *part_m, flo
                                     const int32_t *context_lens, int B, int Hq, int Hkv, int D,
                                     int block_size, int64_t num_blocks, float scale,
                                     int partition_tokens, int max_partitions, int dtype,
-                                    int *err_flag, cudaStream_t stream) {
+                                    int *err_flag, int *work_counters, cudaStream_t stream) {
     int st = check_attn_args(out, part_o, part_m, part_l, q, k_cache, v_cache, block_tables,
                              max_blocks_per_seq, context_lens, B, Hq, Hkv, D, block_size,
                              num_blocks, partition_tokens, max_partitions, dtype);
@@ -651,7 +791,7 @@ extern "C" int xs_paged_decode_attn(void *out, float *part_o, float *part_m, flo
     attn::KernelFn fn = attn::pick_kernel(dtype, D, Hq / Hkv, &smem0);
     if (!fn) return XS_EUNSUPPORTED;
     const int smem = smem0 + 4 * (B + 1);
-    if (smem > dev.max_smem_optin) return XS_EUNSUPPORTED;
+    if (smem + 1024 > dev.max_smem_optin) return XS_EUNSUPPORTED;  // room for static smem
     int per_sm = 1;
     if ((st = attn::occupancy(fn, smem, &per_sm)) != XS_OK) return st;
     const int64_t max_items = static_cast<int64_t>(B) * Hkv * max_partitions;
@@ -676,6 +816,7 @@ extern "C" int xs_paged_decode_attn(void *out, float *part_o, float *part_m, flo
     p.num_blocks = num_blocks;
     p.qscale = scale * attn::kLog2e;
     p.err_flag = err_flag;
+    p.work = work_counters;
     fn<<<grid, attn::kThreads, smem, stream>>>(p);
     return launch_status();
 }
@@ -711,11 +852,11 @@ extern "C" int xs_paged_decode(void *out, float *part_o, float *part_m, float *p
                                const int32_t *context_lens, int B, int Hq, int Hkv, int D,
                                int block_size, int64_t num_blocks, float scale,
                                int partition_tokens, int max_partitions, int dtype, int *err_flag,
-                               cudaStream_t stream) {
+                               int *work_counters, cudaStream_t stream) {
     int st = xs_paged_decode_attn(out, part_o, part_m, part_l, q, k_cache, v_cache, block_tables,
                                   max_blocks_per_seq, context_lens, B, Hq, Hkv, D, block_size,
                                   num_blocks, scale, partition_tokens, max_partitions, dtype,
-                                  err_flag, stream);
+                                  err_flag, work_counters, stream);
     if (st != XS_OK || max_partitions <= 1) return st;
     return xs_paged_decode_reduce(out, part_o, part_m, part_l, context_lens, B, Hq, D,
                                   partition_tokens, max_partitions, dtype, stream);
@@ -792,5 +933,5 @@ extern "C" int xs_paged_decode_noalloc(void *out, const void *q, const void *k_c
     }
     return xs_paged_decode(out, po, pm, pl, q, k_cache, v_cache, block_tables, max_blocks_per_seq,
                            context_lens, B, Hq, Hkv, D, block_size, num_blocks, scale,
-                           partition_tokens, max_parts, dtype, err_flag, stream);
+                           partition_tokens, max_parts, dtype, err_flag, nullptr, stream);
 }

@@ -39,10 +39,10 @@ SIGNATURES = {
     "xs_paged_decode_max_partitions": (_I, [_I, _I, _I]),
     "xs_paged_decode_workspace_bytes": (_S, [_I, _I, _I, _I]),
     "xs_paged_decode_attn": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I,
-                                  _L, _F, _I, _I, _I, _P, _P]),
+                                  _L, _F, _I, _I, _I, _P, _P, _P]),
     "xs_paged_decode_reduce": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
     "xs_paged_decode": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _L, _F,
-                             _I, _I, _I, _P, _P]),
+                             _I, _I, _I, _P, _P, _P]),
     "xs_paged_decode_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _L, _F,
                                      _I, _I, _P, _P]),
     "xs_version": (_I, []),
@@ -160,13 +160,14 @@ def xs_paged_decode_workspace_bytes(B, Hq, D, max_partitions) -> int:
 
 def xs_paged_decode_attn(out, part_o, part_m, part_l, q, k_cache, v_cache, block_tables,
                          context_lens, scale, partition_tokens, max_partitions, err_flag=None,
-                         stream=None):
+                         work_counters=None, stream=None):
     B, Hq, D = q.shape
     num_blocks, Hkv, bs, _ = k_cache.shape
     _call("xs_paged_decode_attn", _ptr(out), _ptr(part_o), _ptr(part_m), _ptr(part_l), _ptr(q),
           _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1],
           _ptr(context_lens), B, Hq, Hkv, D, bs, num_blocks, float(scale), partition_tokens,
-          max_partitions, dtype_code(q.dtype), _ptr(err_flag), _stream(stream))
+          max_partitions, dtype_code(q.dtype), _ptr(err_flag), _ptr(work_counters),
+          _stream(stream))
 
 
 def xs_paged_decode_reduce(out, part_o, part_m, part_l, context_lens, partition_tokens,
@@ -178,13 +179,15 @@ def xs_paged_decode_reduce(out, part_o, part_m, part_l, context_lens, partition_
 
 
 def xs_paged_decode(out, part_o, part_m, part_l, q, k_cache, v_cache, block_tables, context_lens,
-                    scale, partition_tokens, max_partitions, err_flag=None, stream=None):
+                    scale, partition_tokens, max_partitions, err_flag=None, work_counters=None,
+                    stream=None):
     B, Hq, D = q.shape
     num_blocks, Hkv, bs, _ = k_cache.shape
     _call("xs_paged_decode", _ptr(out), _ptr(part_o), _ptr(part_m), _ptr(part_l), _ptr(q),
           _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1],
           _ptr(context_lens), B, Hq, Hkv, D, bs, num_blocks, float(scale), partition_tokens,
-          max_partitions, dtype_code(q.dtype), _ptr(err_flag), _stream(stream))
+          max_partitions, dtype_code(q.dtype), _ptr(err_flag), _ptr(work_counters),
+          _stream(stream))
 
 
 def xs_paged_decode_noalloc(out, q, k_cache, v_cache, block_tables, context_lens, scale,
@@ -224,6 +227,8 @@ class DecodeWorkspace:
         self.max_partitions = xs_paged_decode_max_partitions(max_blocks_per_seq, BLOCK_SIZE,
                                                              self.partition_tokens)
         n = B * Hq * self.max_partitions
+        # Work counters for the dynamic item scheduler (zero between launches).
+        self.work = torch.zeros(2, dtype=torch.int32, device=device)
         if self.max_partitions > 1:
             self.part_o = torch.empty(n * D, dtype=torch.float32, device=device)
             self.part_m = torch.empty(n, dtype=torch.float32, device=device)

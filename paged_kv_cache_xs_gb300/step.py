@@ -56,7 +56,8 @@ class PagedDecodeStep:
         ws = self.ws
         ops.xs_paged_decode_attn(out, ws.part_o, ws.part_m, ws.part_l, q, k_cache, v_cache,
                                  block_tables, context_lens, scale, ws.partition_tokens,
-                                 ws.max_partitions, err_flag=self.err_flag)
+                                 ws.max_partitions, err_flag=self.err_flag,
+                                 work_counters=ws.work)
 
     def reduce(self, out, context_lens):
         ws = self.ws

@@ -53,9 +53,10 @@ def test_partition_heuristic(lib):
     for B, Hkv, total, mx in [(128, 8, 128 * 18433, 32769), (1, 8, 4097, 4097),
                               (64, 8, 64 * 1300, 8193), (8, 12, 8 * 600, 1025), (2, 12, 29, 21)]:
         P = ops.xs_paged_decode_partition_tokens(B, Hkv, total, mx, 152)
-        assert 16 <= P <= 2048 and P % 16 == 0 and (P & (P - 1)) == 0
-        items = (total // P + B) * Hkv
-        assert items >= 152 * 2 * 6 or P == 16
+        assert 64 <= P <= 2048 and (P & (P - 1)) == 0
+    # Large batches get long partitions; a single stream gets short ones.
+    assert ops.xs_paged_decode_partition_tokens(128, 8, 128 * 18433, 32769, 152) >= 1024
+    assert ops.xs_paged_decode_partition_tokens(1, 8, 4097, 4097, 152) == 128
     # More SMs never asks for bigger partitions.
     a = ops.xs_paged_decode_partition_tokens(64, 8, 64 * 1300, 8193, 76)
     b = ops.xs_paged_decode_partition_tokens(64, 8, 64 * 1300, 8193, 152)
@@ -80,13 +81,14 @@ A = 1 << 20
 
 def _attn(lib, **kw):
     args = dict(out=A, po=A, pm=A, pl=A, q=A, k=A, v=A, bt=A, maxb=4, lens=A, B=2, Hq=8, Hkv=2,
-                D=128, bs=16, nb=10, scale=0.1, P=16, maxp=4, dtype=1, err=None, stream=None)
+                D=128, bs=16, nb=10, scale=0.1, P=16, maxp=4, dtype=1, err=None, work=None,
+                stream=None)
     args.update(kw)
     return lib.xs_paged_decode_attn(args["out"], args["po"], args["pm"], args["pl"], args["q"],
                                     args["k"], args["v"], args["bt"], args["maxb"], args["lens"],
                                     args["B"], args["Hq"], args["Hkv"], args["D"], args["bs"],
                                     args["nb"], args["scale"], args["P"], args["maxp"],
-                                    args["dtype"], args["err"], args["stream"])
+                                    args["dtype"], args["err"], args["work"], args["stream"])
 
 
 def test_attn_argument_validation(lib):

@@ -13,18 +13,19 @@ from tests import gpu_helpers as gh
 pytestmark = pytest.mark.gpu
 
 
-def _attend(w, layer, P, out=None, kc=None, vc=None, bt=None, err=None):
+def _attend(w, layer, P, out=None, kc=None, vc=None, bt=None, err=None, dynamic=False,
+            ws=None):
     cfg = w.cfg
     kc = w.k_cache[layer] if kc is None else kc
     vc = w.v_cache[layer] if vc is None else vc
     bt = w.block_tables if bt is None else bt
-    ws = ops.DecodeWorkspace(cfg.B, cfg.Hq, cfg.Hkv, cfg.D, bt.shape[1], kc.device,
-                             partition_tokens=P)
+    ws = ws or ops.DecodeWorkspace(cfg.B, cfg.Hq, cfg.Hkv, cfg.D, bt.shape[1], kc.device,
+                                   partition_tokens=P)
     out = torch.full((cfg.B, cfg.Hq, cfg.D), float("nan"), dtype=cfg.dtype, device=kc.device) \
         if out is None else out
     ops.xs_paged_decode(out, ws.part_o, ws.part_m, ws.part_l, w.q[layer], kc, vc, bt,
                         w.context_lens, w.scale, ws.partition_tokens, ws.max_partitions,
-                        err_flag=err)
+                        err_flag=err, work_counters=ws.work if dynamic else None)
     return out
 
 
@@ -49,9 +50,30 @@ def test_variants_split_and_single(dtype, D, G):
     w = wl.make_workload(cfg, device=dev)
     ref = _oracle(w, 0)
     for P in (16, 48, 128, 512):
-        out = _attend(w, 0, P)
-        torch.cuda.synchronize()
-        gh.assert_close(out, ref, dtype, what=f"P={P}")
+        for dynamic in (False, True):
+            out = _attend(w, 0, P, dynamic=dynamic)
+            torch.cuda.synchronize()
+            gh.assert_close(out, ref, dtype, what=f"P={P} dynamic={dynamic}")
+
+
+def test_dynamic_scheduler_counters_reset():
+    # Several launches share one pair of work counters: each must see them at
+    # zero (the previous launch's last CTA resets them) and produce the same,
+    # correct output.
+    dev = gh.device()
+    cfg = wl.custom_config(23, 32, 8, 128, torch.bfloat16, history=("loguniform", (16, 6000)),
+                           pool=("factor", 1.5), seed=121)
+    w = wl.make_workload(cfg, device=dev)
+    ref = _oracle(w, 0)
+    ws = ops.DecodeWorkspace(cfg.B, cfg.Hq, cfg.Hkv, cfg.D, w.max_blocks_per_seq, dev,
+                             partition_tokens=128)
+    outs = []
+    for _ in range(4):
+        outs.append(_attend(w, 0, 128, dynamic=True, ws=ws))
+    torch.cuda.synchronize()
+    assert ws.work.tolist() == [0, 0]
+    for out in outs:
+        gh.assert_close(out, ref, torch.bfloat16)
 
 
 def test_full_step_ragged_with_empty_sequences():
