@@ -302,7 +302,8 @@ def run_ours(args, rank, world, local, dist):
     L = cfg.layers
     step = PagedDecodeStep(cfg.B, cfg.Hq, cfg.Hkv, cfg.D, w.max_blocks_per_seq, cfg.dtype, dev,
                            total_context_tokens=w.total_context_tokens,
-                           max_context_len=w.max_context_len)
+                           max_context_len=w.max_context_len,
+                           partition_tokens=args.partition_tokens or None)
     out = torch.empty(cfg.B, cfg.Hq, cfg.D, dtype=cfg.dtype, device=dev)
     stream = torch.cuda.current_stream()
     by = step_bytes(cfg, w.context_lens.cpu())
@@ -435,6 +436,8 @@ def main(argv=None):
                     help="workload index (0-4); default: the large-batch long-context one")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--partition-tokens", type=int, default=0,
+                    help="split-K partition size (multiple of 16); 0 = the library's heuristic")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target duration of the CPU oracle baseline sample")
     ap.add_argument("--ref-step-seconds", type=float, default=2.0,

@@ -86,6 +86,8 @@ extern "C" {
 #define XS_FLAG_BAD_SLOT 4  /* slot_mapping[t] beyond the pool; write skipped */
 #define XS_FLAG_TIMEOUT 8   /* a bounded wait for staged data gave up; the
                                kernel drained its copies and returned        */
+#define XS_FLAG_CONFIG 16   /* internal: a launch got less shared memory than
+                               its batch needs; the kernel did nothing       */
 
 /*
  * xs_slot_mapping - where each sequence's new token goes (one decode step).

@@ -40,10 +40,14 @@ namespace attn {
 
 constexpr int kBlock = 16;          // tokens per page
 constexpr int kConsumerWarps = 4;
-constexpr int kThreads = 32 * (kConsumerWarps + 1);
+constexpr int kThreads = 32 * (kConsumerWarps + 2);  // producer, consumers, merger
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s per bounded wait
-constexpr int kMaxBatch = 16384;                  // prefix sums live in shared memory
+constexpr int kMaxBatch = 8192;                   // per-sequence tables live in shared memory
+
+// Per-sequence tables a CTA keeps in shared memory: pfull[B + 1], ptail[B + 1]
+// (item numbering) and nlen[B] (clamped context lengths).
+__host__ __device__ constexpr int table_bytes(int B) { return 4 * (3 * B + 2); }
 
 template <typename T, int D, int G>
 struct Cfg {
@@ -72,15 +76,19 @@ struct Cfg {
     static constexpr int kWOff = kQSlotOff + 2 * kQBytes;
     static constexpr int kWBytes = kConsumerWarps * kBlock * G * 8;   // (w, w) pairs
     static constexpr int kCombOff = kWOff + kWBytes;
-    static constexpr int kCombBytes = kConsumerWarps * G * (D + 2) * 4;
-    static constexpr int kBarOff = (kCombOff + kCombBytes + 7) / 8 * 8;
-    static constexpr int kBarBytes = (2 * kStages + 4) * 8;
+    // A merge buffer: the item (32 B), then m[4][G], l[4][G], o[4][G][D] (fp32).
+    static constexpr int kCombBytes = 32 + kConsumerWarps * G * (D + 2) * 4;  // one of 2
+    static constexpr int kBarOff = (kCombOff + 2 * kCombBytes + 7) / 8 * 8;
+    static constexpr int kBarBytes = (2 * kStages + 8) * 8;
     static constexpr int kItemOff = kBarOff + kBarBytes;             // 2 published items
     static constexpr int kPrefixOff = kItemOff + 2 * 32;
-    static __host__ __device__ constexpr int smem_bytes(int B) { return kPrefixOff + 4 * (B + 1); }
+    // The host sizes every launch with this same function.
+    static __host__ __device__ constexpr int smem_bytes(int B) { return kPrefixOff + table_bytes(B); }
     static_assert(kStages % kConsumerWarps == 0, "each ring stage must belong to one consumer");
     static_assert(kChunksPerLane >= 1 && kChunksPerRow % 8 == 0, "row must split over 8 lanes");
     static_assert(D % 64 == 0, "PV works on dim pairs: D must split over 32 lanes x 2");
+    static_assert(kCombOff % 16 == 0 && kCombBytes % 16 == 0 && (kConsumerWarps * G * 4) % 16 == 0,
+                  "merge buffers are read as float4");
 };
 
 struct Params {
@@ -109,22 +117,41 @@ __device__ __forceinline__ int seq_len(const Params &p, int b, bool report) {
 struct Item {
     int b, g, part, n, tok0, tok1, pg0, pg1;
 };
-static_assert(sizeof(Item) == 32, "item slots are 32 bytes");
+static_assert(sizeof(Item) == 32, "item slots and merge-buffer headers are 32 bytes");
 
-__device__ __forceinline__ Item decode_item(const Params &p, const int *prefix, int item) {
-    // Largest b with prefix[b] <= item.
-    int lo = 0, hi = p.B - 1;
+// Largest b in [0, B) with table[b] <= x (table is non-decreasing).
+__device__ __forceinline__ int upper_index(const int *table, int B, int x) {
+    int lo = 0, hi = B - 1;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (prefix[mid] <= item) lo = mid; else hi = mid - 1;
+        if (table[mid] <= x) lo = mid; else hi = mid - 1;
     }
+    return lo;
+}
+
+// Item numbering: first every full partition (P tokens) of every sequence and
+// KV head, in sequence order, then the ragged last partitions (and short
+// sequences) - so the end of a launch is made of small items that balance
+// the grid.  pfull/ptail are the exclusive prefix sums of those counts.
+__device__ __forceinline__ Item decode_item(const Params &p, const int *pfull, const int *ptail,
+                                            const int *nlen, int item) {
     Item it;
-    it.b = lo;
-    const int r = item - prefix[lo];
-    const int nparts = (prefix[lo + 1] - prefix[lo]) / p.Hkv;
-    it.g = r / nparts;
-    it.part = r - it.g * nparts;
-    it.n = seq_len(p, lo, false);
+    const int n_full = pfull[p.B];
+    int b;
+    if (item < n_full) {
+        b = upper_index(pfull, p.B, item);
+        const int r = item - pfull[b];
+        const int nf = (pfull[b + 1] - pfull[b]) / p.Hkv;
+        it.g = r / nf;
+        it.part = r - it.g * nf;
+    } else {
+        const int r2 = item - n_full;
+        b = upper_index(ptail, p.B, r2);
+        it.g = r2 - ptail[b];
+        it.part = nlen[b] / p.P;
+    }
+    it.b = b;
+    it.n = nlen[b];
     it.tok0 = it.part * p.P;
     it.tok1 = min(it.n, it.tok0 + p.P);
     it.pg0 = it.tok0 / kBlock;
@@ -287,12 +314,23 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
     uint64_t *empty = full + kStages;
     uint64_t *qfull = empty + kStages;
     uint64_t *qempty = qfull + 2;
+    uint64_t *merged = qempty + 2;  // per merge buffer: the four consumer states are in
+    uint64_t *freed = merged + 2;   // per merge buffer: the merger has read it
     Item *item_slot = reinterpret_cast<Item *>(smem + C::kItemOff);
-    int *prefix = reinterpret_cast<int *>(smem + C::kPrefixOff);
-    __shared__ int s_abort, s_stop, s_done;
+    int *pfull = reinterpret_cast<int *>(smem + C::kPrefixOff);
+    int *ptail = pfull + p.B + 1;
+    int *nlen = ptail + p.B + 1;
+    __shared__ int s_abort;
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
+
+    // The launch must provide the shared memory this B needs; refuse (flag,
+    // return before touching shared memory) if it does not.
+    if (dynamic_smem_bytes() < static_cast<uint32_t>(C::smem_bytes(p.B))) {
+        if (tid == 0) raise_flag(p.err_flag, XS_FLAG_CONFIG);
+        return;
+    }
 
     // ---- prologue: barriers, item prefix sums, zero outputs of empty sequences
     if (tid == 0) {
@@ -303,40 +341,57 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
         for (int s = 0; s < 2; ++s) {
             mbar_init(&qfull[s], 1);
             mbar_init(&qempty[s], kConsumerWarps);
+            mbar_init(&merged[s], kConsumerWarps);
+            mbar_init(&freed[s], 1);
         }
         mbar_fence_init();
         s_abort = 0;
-        s_stop = 0;
-        s_done = 0;
     }
     {
-        // Items of sequence b: ceil(n/P) partitions x Hkv heads.  Chunked scan.
+        // Per sequence: n/P full partitions and (n % P != 0) ragged one, each
+        // x Hkv heads.  Chunked scan of both counts over the block.
         const int per = (p.B + kThreads - 1) / kThreads;
         const int b0 = min(p.B, tid * per), b1 = min(p.B, b0 + per);
-        int local = 0;
+        int lf = 0, lt = 0;
         for (int b = b0; b < b1; ++b) {
-            const int n = seq_len(p, b, blockIdx.x == 0);
-            local += (n > 0 ? (n + p.P - 1) / p.P : 0) * p.Hkv;
+            const int n = max(seq_len(p, b, blockIdx.x == 0), 0);
+            lf += (n / p.P) * p.Hkv;
+            lt += (n % p.P != 0) * p.Hkv;
         }
-        // Inclusive scan of `local` over the block (warp shuffles + one pass over warps).
-        int x = local;
+        int xf = lf, xt = lt;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, x, o);
-            if (lane >= o) x += y;
+            const int yf = __shfl_up_sync(0xffffffffu, xf, o);
+            const int yt = __shfl_up_sync(0xffffffffu, xt, o);
+            if (lane >= o) {
+                xf += yf;
+                xt += yt;
+            }
         }
-        __shared__ int warp_tot[kThreads / 32];
-        if (lane == 31) warp_tot[warp] = x;
+        __shared__ int warp_tot[2][kThreads / 32];
+        if (lane == 31) {
+            warp_tot[0][warp] = xf;
+            warp_tot[1][warp] = xt;
+        }
         __syncthreads();
-        int base = 0;
-        for (int w = 0; w < warp; ++w) base += warp_tot[w];
-        int run = base + x - local;  // exclusive prefix of this thread's range
-        for (int b = b0; b < b1; ++b) {
-            prefix[b] = run;
-            const int n = seq_len(p, b, false);
-            run += (n > 0 ? (n + p.P - 1) / p.P : 0) * p.Hkv;
+        int basef = 0, baset = 0;
+        for (int w = 0; w < warp; ++w) {
+            basef += warp_tot[0][w];
+            baset += warp_tot[1][w];
         }
-        if (tid == kThreads - 1) prefix[p.B] = base + x;
+        int runf = basef + xf - lf, runt = baset + xt - lt;  // exclusive prefixes
+        for (int b = b0; b < b1; ++b) {
+            const int n = max(seq_len(p, b, false), 0);
+            pfull[b] = runf;
+            ptail[b] = runt;
+            nlen[b] = n;
+            runf += (n / p.P) * p.Hkv;
+            runt += (n % p.P != 0) * p.Hkv;
+        }
+        if (tid == kThreads - 1) {
+            pfull[p.B] = basef + xf;
+            ptail[p.B] = baset + xt;
+        }
     }
     // Sequences with no tokens produce zeros.
     for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
@@ -345,42 +400,68 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
         for (int i = tid; i < p.Hq * D; i += kThreads) o[i] = Elem<T>::from_f32(0.f);
     }
     __syncthreads();
-    const int total_items = prefix[p.B];
+    const int total_items = pfull[p.B] + ptail[p.B];
 
     if (warp == 0) {
         // ================================================================ producer
         // Takes items (from the shared work counter, or blockIdx.x + k*gridDim.x
         // without one), publishes each item's ranges and q rows in a
         // double-buffered slot, then streams its pages into the ring.  An item
-        // with b < 0 tells the consumers to stop.
+        // with b < 0 tells the consumers to stop.  The producer runs one item
+        // ahead: while it issues item A's pages, item B is decoded with its
+        // first block ids loading, and the counter fetch for the item after
+        // B is in flight.
         const uint64_t pol = policy_evict_first();
         const unsigned char *kbase = static_cast<const unsigned char *>(p.k_cache);
         const unsigned char *vbase = static_cast<const unsigned char *>(p.v_cache);
         const unsigned char *qbase = static_cast<const unsigned char *>(p.q);
         uint32_t page_ctr = 0, item_ctr = 0;
         int static_next = blockIdx.x;
-        bool ok = true;
-        while (ok) {
-            int item = 0;
-            if (lane == 0) {
-                item = p.work ? atomicAdd(&p.work[0], 1) : static_next;
-                static_next += gridDim.x;
-            }
-            item = __shfl_sync(0xffffffffu, item, 0);
-            const bool last = item >= total_items;
+        int grabs = 0;
+        // The first two items of CTA c are c and c + gridDim.x (no atomic on
+        // the start-up path); later ones come from the shared counter (items
+        // 2*gridDim.x, 2*gridDim.x + 1, ...) or, without one, from
+        // c + k * gridDim.x.  Lane 0's value is the item: read it with a shuffle.
+        auto grab = [&]() {
+            int v = static_next;
+            if (p.work && grabs >= 2 && lane == 0)
+                v = 2 * static_cast<int>(gridDim.x) + atomicAdd(&p.work[0], 1);
+            ++grabs;
+            static_next += gridDim.x;
+            return v;
+        };
+        auto decode = [&](int item) {
             Item it;
-            if (!last) {
-                it = decode_item(p, prefix, item);
+            if (item < total_items) {
+                it = decode_item(p, pfull, ptail, nlen, item);
             } else {
                 it.b = -1;
-                it.pg0 = it.pg1 = 0;
+                it.g = it.part = it.n = it.tok0 = it.tok1 = it.pg0 = it.pg1 = 0;
             }
+            return it;
+        };
+        // Block ids of pages [base, base + 32) of an item, one per lane (0 past the end).
+        auto load_ids = [&](const Item &it, int base) {
+            int32_t blk = 0;
+            const int pg = base + lane;
+            if (it.b >= 0 && pg < it.pg1) {
+                blk = p.block_tables[static_cast<int64_t>(it.b) * p.max_blocks + pg];
+                if (blk < 0 || blk >= p.num_blocks) {
+                    raise_flag(p.err_flag, XS_FLAG_BAD_BLOCK);
+                    blk = 0;
+                }
+            }
+            return blk;
+        };
+        // Publish an item (or the end marker) in the next q slot.
+        auto publish = [&](const Item &it) {
+            bool ok = true;
             if (lane == 0) {
                 const uint32_t slot = item_ctr & 1, k = item_ctr >> 1;
                 ok = mbar_wait_bounded(&qempty[slot], (k & 1) ^ 1, kWaitLimitNs);
                 if (ok) {
                     item_slot[slot] = it;
-                    if (last) {
+                    if (it.b < 0) {
                         mbar_arrive(&qfull[slot]);
                     } else {
                         unsigned char *dst = smem + C::kQSlotOff + slot * C::kQBytes;
@@ -392,30 +473,35 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
                     }
                 }
             }
-            ok = __shfl_sync(0xffffffffu, ok, 0);
             ++item_ctr;
-            if (last) break;
-            const int32_t *row = p.block_tables + static_cast<int64_t>(it.b) * p.max_blocks;
-            for (int base = it.pg0; ok && base < it.pg1; base += 32) {
-                int32_t blk = 0;
-                const int pg = base + lane;
-                if (pg < it.pg1) {
-                    blk = row[pg];
-                    if (blk < 0 || blk >= p.num_blocks) {
-                        raise_flag(p.err_flag, XS_FLAG_BAD_BLOCK);
-                        blk = 0;
-                    }
-                }
-                const int cnt = min(32, it.pg1 - base);
+            return __shfl_sync(0xffffffffu, ok, 0);
+        };
+        // Item B is published (q rows copied in) before item A's pages are
+        // issued, so consumers finishing A find B's q already in place.
+        Item A = decode(__shfl_sync(0xffffffffu, grab(), 0));
+        int32_t idsA = load_ids(A, A.pg0);
+        int nextB = grab();
+        bool ok = publish(A);
+        while (ok && A.b >= 0) {
+            Item Bt = decode(__shfl_sync(0xffffffffu, nextB, 0));
+            const int32_t idsB = load_ids(Bt, Bt.pg0);
+            if (Bt.b >= 0) nextB = grab();
+            ok = publish(Bt);
+            if (!ok) break;
+            // Stream A's pages, 32 block ids at a time (the next 32 load meanwhile).
+            int32_t ids = idsA;
+            for (int base = A.pg0; ok && base < A.pg1; base += 32) {
+                const int32_t ids_next = (base + 32 < A.pg1) ? load_ids(A, base + 32) : 0;
+                const int cnt = min(32, A.pg1 - base);
                 for (int i = 0; i < cnt; ++i) {
-                    const int32_t bi = __shfl_sync(0xffffffffu, blk, i);
+                    const int32_t bi = __shfl_sync(0xffffffffu, ids, i);
                     if (lane == 0) {
                         const uint32_t s = page_ctr % kStages, k = page_ctr / kStages;
                         ok = mbar_wait_bounded(&empty[s], (k & 1) ^ 1, kWaitLimitNs);
                         if (ok) {
                             unsigned char *dk = smem + s * 2 * C::kPageBytes;
                             const int64_t off =
-                                (static_cast<int64_t>(bi) * p.Hkv + it.g) * C::kPageBytes;
+                                (static_cast<int64_t>(bi) * p.Hkv + A.g) * C::kPageBytes;
                             mbar_arrive_expect_tx(&full[s], 2 * C::kPageBytes);
                             bulk_g2s(dk, kbase + off, C::kPageBytes, &full[s], pol);
                             bulk_g2s(dk + C::kPageBytes, vbase + off, C::kPageBytes, &full[s], pol);
@@ -425,7 +511,10 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
                     if (!ok) break;
                     ++page_ctr;  // pages issued so far
                 }
+                ids = ids_next;
             }
+            A = Bt;
+            idsA = idsB;
         }
         if (lane == 0) {
             if (!ok) {
@@ -449,29 +538,95 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
         return;
     }
 
+    if (warp == kConsumerWarps + 1) {
+        // ================================================================ merger
+        // Waits for the four consumer states of each item, merges them (each
+        // lane 4 consecutive dims of one head at a time) and writes the final
+        // output or the split-K partials, then frees the buffer.
+        for (uint32_t item_ctr = 0;; ++item_ctr) {
+            const int buf = item_ctr & 1;
+            unsigned char *mb = smem + C::kCombOff + buf * C::kCombBytes;
+            if (!mbar_wait_bounded(&merged[buf], (item_ctr >> 1) & 1, kWaitLimitNs)) {
+                if (lane == 0) {
+                    raise_flag(p.err_flag, XS_FLAG_TIMEOUT);
+                    atomicExch(&s_abort, 1);
+                }
+                break;
+            }
+            const Item it = *reinterpret_cast<const Item *>(mb);
+            if (it.b < 0) break;  // the consumers have no more items
+            const float *cM = reinterpret_cast<const float *>(mb + 32);
+            const float *cL = cM + kConsumerWarps * G;
+            const float *cO = cL + kConsumerWarps * G;
+            const bool valid = it.b < p.B && it.g >= 0 && it.g < p.Hkv && it.part >= 0 &&
+                               it.part < p.max_parts && !*static_cast<volatile int *>(&s_abort);
+            const bool single = (it.n + p.P - 1) / p.P == 1;
+            const int64_t head0 =
+                static_cast<int64_t>(it.b) * p.Hq + static_cast<int64_t>(it.g) * G;
+            for (int ch = lane; valid && ch < G * D / 4; ch += 32) {
+                const int h = ch / (D / 4), d = (ch - h * (D / 4)) * 4;
+                float mw[kConsumerWarps], mx = -INFINITY;
+#pragma unroll
+                for (int w2 = 0; w2 < kConsumerWarps; ++w2) {
+                    mw[w2] = cM[w2 * G + h];
+                    mx = fmaxf(mx, mw[w2]);
+                }
+                float lt = 0.f;
+                float4 ot = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int w2 = 0; w2 < kConsumerWarps; ++w2) {
+                    const float f = fast_exp2(mw[w2] - mx);
+                    lt += f * cL[w2 * G + h];
+                    const float4 v = *reinterpret_cast<const float4 *>(&cO[(w2 * G + h) * D + d]);
+                    ot.x += f * v.x;
+                    ot.y += f * v.y;
+                    ot.z += f * v.z;
+                    ot.w += f * v.w;
+                }
+                const float inv = 1.f / lt;
+                ot.x *= inv;
+                ot.y *= inv;
+                ot.z *= inv;
+                ot.w *= inv;
+                if (single) {
+                    T *dst = static_cast<T *>(p.out) + (head0 + h) * D + d;
+                    dst[0] = Elem<T>::from_f32(ot.x);
+                    dst[1] = Elem<T>::from_f32(ot.y);
+                    dst[2] = Elem<T>::from_f32(ot.z);
+                    dst[3] = Elem<T>::from_f32(ot.w);
+                } else {
+                    const int64_t pi = (head0 + h) * p.max_parts + it.part;
+                    *reinterpret_cast<float4 *>(&p.part_o[pi * D + d]) = ot;
+                    if (d == 0) {
+                        p.part_m[pi] = mx;
+                        p.part_l[pi] = lt;
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&freed[buf]);
+        }
+        return;
+    }
+
     // ==================================================================== consumers
     const int cw = warp - 1;
     const int j = lane & 7;
     float2 *W2 = reinterpret_cast<float2 *>(smem + C::kWOff) + cw * kBlock * G;
-    float *cM = reinterpret_cast<float *>(smem + C::kCombOff);
-    float *cL = cM + kConsumerWarps * G;
-    float *cO = cL + kConsumerWarps * G;
-    const int ctid = tid - 32;
-    uint32_t page_ctr = 0, item_ctr = 0;
+    uint32_t page_ctr = 0;
 
-    for (;; ++item_ctr) {
-        // A failed wait marks the item bad, and the producer's end marker
-        // (b < 0) marks it done: either way the warp skips the pages but still
-        // takes part in both merge barriers, and all consumers leave the loop
-        // together after the second one, so none is left waiting.
+    for (uint32_t item_ctr = 0;; ++item_ctr) {
+        // Every consumer sees the producer's end marker (b < 0) in the same
+        // slot and leaves; warp 0 passes the marker on to the merger.  A
+        // failed (timed-out) wait marks the item bad: the warp skips its pages.
+        // All waits in the CTA are bounded, so no warp can wait forever.
         const uint32_t slot = item_ctr & 1;
         bool bad = !__all_sync(0xffffffffu,
                                mbar_wait_bounded(&qfull[slot], (item_ctr >> 1) & 1, kWaitLimitNs));
         Item it = item_slot[slot];
         const bool done = !bad && it.b < 0;
-        if (done && lane == 0) *static_cast<volatile int *>(&s_done) = 1;
         float qf[G][C::kQkDims];
-        {
+        if (!done) {
             const unsigned char *qs = smem + C::kQSlotOff + slot * C::kQBytes;
 #pragma unroll
             for (int h = 0; h < G; ++h)
@@ -486,7 +641,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
                         qf[h][c * C::kElemsPerChunk + e] = f[e] * p.qscale;
                 }
             __syncwarp();
-            if (lane == 0 && !bad && !done) mbar_arrive(&qempty[slot]);
+            if (lane == 0 && !bad) mbar_arrive(&qempty[slot]);
         }
         if (bad || done) {
             it.b = -1;
@@ -527,50 +682,41 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
             atomicExch(&s_abort, 1);
         }
 
-        // ---- merge the four consumer states of this item
-#pragma unroll
-        for (int h = 0; h < G; ++h)
-#pragma unroll
-            for (int d = 0; d < C::kPvDims / 2; ++d)
-                *reinterpret_cast<float2 *>(&cO[(cw * G + h) * D + lane * C::kPvDims + 2 * d]) =
-                    o[h][d];
-        if (lane < 8 && (j & ((1 << C::kHeadShift) - 1)) == 0) {
-            const int own_head = j >> C::kHeadShift;
-            cM[cw * G + own_head] = m_own;
-            cL[cw * G + own_head] = l_own;
-        }
-        named_barrier_sync(1, 32 * kConsumerWarps);
-        if (ctid == 0) s_stop = s_abort | s_done;
-        const bool valid = it.b >= 0 && it.b < p.B && it.g >= 0 && it.g < p.Hkv &&
-                           it.part >= 0 && it.part < p.max_parts &&
-                           !*static_cast<volatile int *>(&s_abort);
-        const bool single = (it.n + p.P - 1) / p.P == 1;
-        const int64_t head0 = static_cast<int64_t>(it.b) * p.Hq + static_cast<int64_t>(it.g) * G;
-        for (int idx = ctid; valid && idx < G * D; idx += 32 * kConsumerWarps) {
-            const int h = idx / D, d = idx - (idx / D) * D;
-            float mx = -INFINITY;
-#pragma unroll
-            for (int w2 = 0; w2 < kConsumerWarps; ++w2) mx = fmaxf(mx, cM[w2 * G + h]);
-            float lt = 0.f, ot = 0.f;
-#pragma unroll
-            for (int w2 = 0; w2 < kConsumerWarps; ++w2) {
-                const float f = fast_exp2(cM[w2 * G + h] - mx);
-                lt += f * cL[w2 * G + h];
-                ot += f * cO[(w2 * G + h) * D + d];
+        // ---- hand this warp's state to the merger (double-buffered by item
+        // parity; a buffer is reused once the merger has freed it).
+        const int buf = item_ctr & 1;
+        unsigned char *mb = smem + C::kCombOff + buf * C::kCombBytes;
+        if (!__all_sync(0xffffffffu,
+                        mbar_wait_bounded(&freed[buf], ((item_ctr >> 1) & 1) ^ 1, kWaitLimitNs))) {
+            if (lane == 0) {
+                raise_flag(p.err_flag, XS_FLAG_TIMEOUT);
+                atomicExch(&s_abort, 1);
             }
-            if (single) {
-                static_cast<T *>(p.out)[(head0 + h) * D + d] = Elem<T>::from_f32(ot / lt);
-            } else {
-                const int64_t pi = (head0 + h) * p.max_parts + it.part;
-                p.part_o[pi * D + d] = ot / lt;
-                if (d == 0) {
-                    p.part_m[pi] = mx;
-                    p.part_l[pi] = lt;
-                }
+            break;
+        }
+        float *cM = reinterpret_cast<float *>(mb + 32);
+        float *cL = cM + kConsumerWarps * G;
+        float *cO = cL + kConsumerWarps * G;
+        if (cw == 0 && lane == 0) *reinterpret_cast<Item *>(mb) = it;
+        if (!done) {
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                float *dst = &cO[(cw * G + h) * D + lane * C::kPvDims];
+                if constexpr (C::kPvDims == 4)
+                    *reinterpret_cast<float4 *>(dst) =
+                        make_float4(o[h][0].x, o[h][0].y, o[h][1].x, o[h][1].y);
+                else
+                    *reinterpret_cast<float2 *>(dst) = o[h][0];
+            }
+            if (lane < 8 && (j & ((1 << C::kHeadShift) - 1)) == 0) {
+                const int own_head = j >> C::kHeadShift;
+                cM[cw * G + own_head] = m_own;
+                cL[cw * G + own_head] = l_own;
             }
         }
-        named_barrier_sync(1, 32 * kConsumerWarps);
-        if (s_stop) break;  // one value for every consumer (written before the barrier)
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&merged[buf]);
+        if (done || *static_cast<volatile int *>(&s_abort)) break;
     }
 }
 
@@ -614,7 +760,7 @@ KernelFn kernel_for() {
 KernelFn pick_kernel(int dtype, int D, int G, int *smem_base_fn_B0) {
 #define XS_PICK(TT, DD, GG)                                                          \
     if (D == DD && G == GG) {                                                        \
-        *smem_base_fn_B0 = Cfg<TT, DD, GG>::smem_bytes(0);                           \
+        *smem_base_fn_B0 = Cfg<TT, DD, GG>::kPrefixOff;                              \
         return kernel_for<TT, DD, GG>();                                             \
     }
     if (dtype == XS_BF16) {
@@ -790,7 +936,7 @@ extern "C" int xs_paged_decode_attn(void *out, float *part_o, float *part_m, flo
     int smem0 = 0;
     attn::KernelFn fn = attn::pick_kernel(dtype, D, Hq / Hkv, &smem0);
     if (!fn) return XS_EUNSUPPORTED;
-    const int smem = smem0 + 4 * (B + 1);
+    const int smem = smem0 + attn::table_bytes(B);  // = Cfg<...>::smem_bytes(B)
     if (smem + 1024 > dev.max_smem_optin) return XS_EUNSUPPORTED;  // room for static smem
     int per_sm = 1;
     if ((st = attn::occupancy(fn, smem, &per_sm)) != XS_OK) return st;

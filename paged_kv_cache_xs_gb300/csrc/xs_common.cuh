@@ -129,6 +129,13 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
     return p;
 }
 
+// Dynamic shared memory the running launch was given (bytes).
+__device__ __forceinline__ uint32_t dynamic_smem_bytes() {
+    uint32_t n;
+    asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(n));
+    return n;
+}
+
 __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }

@@ -26,7 +26,7 @@ STATUS = {
     -9: "XS_ESCRATCH",
 }
 NOALLOC_SCRATCH_BYTES = 64 << 20
-FLAG_BAD_BLOCK, FLAG_BAD_LEN, FLAG_BAD_SLOT, FLAG_TIMEOUT = 1, 2, 4, 8
+FLAG_BAD_BLOCK, FLAG_BAD_LEN, FLAG_BAD_SLOT, FLAG_TIMEOUT, FLAG_CONFIG = 1, 2, 4, 8, 16
 
 # name -> (restype, argtypes)
 _P, _I, _L, _F, _S = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float,
