@@ -290,7 +290,7 @@ def run_reference(args, rank, world, dist):
 def run_ours(args, rank, world, local, dist):
     from paged_kv_cache_xs_gb300 import build as xsbuild
     from paged_kv_cache_xs_gb300 import ops
-    from paged_kv_cache_xs_gb300.step import PagedDecodeStep
+    from paged_kv_cache_xs_gb300.step import CapturedStep, PagedDecodeStep
 
     xsbuild.build()
     ops.load()
@@ -304,48 +304,74 @@ def run_ours(args, rank, world, local, dist):
                            total_context_tokens=w.total_context_tokens,
                            max_context_len=w.max_context_len,
                            partition_tokens=args.partition_tokens or None)
-    out = torch.empty(cfg.B, cfg.Hq, cfg.D, dtype=cfg.dtype, device=dev)
+    out = torch.empty(L, cfg.B, cfg.Hq, cfg.D, dtype=cfg.dtype, device=dev)  # every layer's output
     stream = torch.cuda.current_stream()
     by = step_bytes(cfg, w.context_lens.cpu())
     bytes_per_step = by["step"] * L
 
     def one_step(ev=None):
+        cur = torch.cuda.current_stream()
         for layer in range(L):
             step.append(w.k_new[layer], w.v_new[layer], w.k_cache[layer], w.v_cache[layer],
                         w.block_tables, w.context_lens)
             if ev is not None:
-                ev[layer][0].record(stream)
-            step.attend(out, w.q[layer], w.k_cache[layer], w.v_cache[layer], w.block_tables,
-                        w.context_lens, w.scale)
+                ev[layer][0].record(cur)
+            step.attend(out[layer], w.q[layer], w.k_cache[layer], w.v_cache[layer],
+                        w.block_tables, w.context_lens, w.scale)
             if ev is not None:
-                ev[layer][1].record(stream)
-            step.reduce(out, w.context_lens)
+                ev[layer][1].record(cur)
+            step.reduce(out[layer], w.context_lens)
+
+    use_graph = args.graph == "on" or (args.graph == "auto" and L > 1)
+    graph = None
+    graph_ev = None
+    if use_graph:
+        # One CUDA graph per step (all layers); attention launches are
+        # bracketed by event-record nodes so their device time is measured.
+        try:
+            graph_ev = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)]
+                        for _ in range(L)]
+        except TypeError:  # a torch without external events: time the graph only
+            graph_ev = None
+        graph = CapturedStep(lambda: one_step(graph_ev))
+
+    def run_step(ev=None):
+        if graph is not None:
+            graph.replay()
+        else:
+            one_step(ev)
 
     clocks = ClockSampler(local)
     # Warm-up, then keep the GPU loaded for >= ~1 s so the clock sampler sees it.
     for _ in range(args.warmup):
-        one_step()
+        run_step()
     torch.cuda.synchronize()
     t_load = time.time()
     while time.time() - t_load < args.load_seconds:
         for _ in range(4):
-            one_step()
+            run_step()
         torch.cuda.synchronize()
 
     # ---- timed region: exactly K steps
-    attn_ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(L)]
-               for _ in range(args.steps)]
+    attn_ev = None if graph is not None else [
+        [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(L)]
+        for _ in range(args.steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(dist)
     torch.cuda.synchronize()
     start.record(stream)
     for k in range(args.steps):
-        one_step(attn_ev[k])
+        run_step(None if attn_ev is None else attn_ev[k])
     end.record(stream)
     torch.cuda.synchronize()
     barrier(dist)
     elapsed_ms = start.elapsed_time(end)
-    attn_ms = [e[0].elapsed_time(e[1]) for ev in attn_ev for e in ev]
+    if attn_ev is not None:
+        attn_ms = [e[0].elapsed_time(e[1]) for ev in attn_ev for e in ev]
+    elif graph_ev is not None:  # the last replay's attention launches
+        attn_ms = [e[0].elapsed_time(e[1]) for e in graph_ev]
+    else:
+        attn_ms = [elapsed_ms / (args.steps * L)]
     clock_info = clocks.stop()
     assert step.error_flags() == 0, f"device error flags {step.error_flags()}"
 
@@ -354,20 +380,22 @@ def run_ours(args, rank, world, local, dist):
     value = world * bytes_per_step / (ms_per_step * 1e-3) / 1e9
     seq_steps = world * cfg.B * L / (ms_per_step * 1e-3)
 
-    # ---- e2e: through the public API from pinned host buffers, H2D/D2H every step
-    hq = w.q[0].cpu().pin_memory()
-    hk = w.k_new[0].cpu().pin_memory()
-    hv = w.v_new[0].cpu().pin_memory()
-    hbt = w.block_tables.cpu().pin_memory()
-    hcl = w.context_lens.cpu().pin_memory()
+    # ---- e2e: the same step fed from pinned host buffers: every step copies that
+    # step's inputs (all layers' q and new K/V rows, block tables, lengths) to the
+    # device, runs the step (the same graph or launches), and reads every layer's
+    # output back.  The KV pools are device-resident state.
+    dev_in = (w.q, w.k_new, w.v_new, w.block_tables, w.context_lens)
+    host_in = tuple(t.cpu().pin_memory() for t in dev_in)
     hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hbt, hcl)) * L
-    d2h = hout.numel() * hout.element_size() * L
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = hout.numel() * hout.element_size()
 
     def e2e_step():
-        for layer in range(L):
-            step.run_from_host(hout, hq, hk, hv, hbt, hcl, w.k_cache[layer], w.v_cache[layer],
-                               w.scale)
+        for d, h in zip(dev_in, host_in):
+            d.copy_(h, non_blocking=True)
+        run_step()
+        hout.copy_(out, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
 
     for _ in range(2):
         e2e_step()
@@ -420,6 +448,7 @@ def run_ours(args, rank, world, local, dist):
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_s * 1e3, 4)},
         "gpu_launches": args.steps * L * step.launches_per_step,
+        "cuda_graph": graph is not None,
         "clocks": clock_info,
     }
     if not args.no_cpu_baseline:
@@ -436,6 +465,9 @@ def main(argv=None):
                     help="workload index (0-4); default: the large-batch long-context one")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--graph", choices=["auto", "on", "off"], default="auto",
+                    help="replay each step as one CUDA graph (auto: when the workload has "
+                         "more than one layer)")
     ap.add_argument("--partition-tokens", type=int, default=0,
                     help="split-K partition size (multiple of 16); 0 = the library's heuristic")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,

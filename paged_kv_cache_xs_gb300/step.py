@@ -92,3 +92,30 @@ class PagedDecodeStep:
 
     def error_flags(self) -> int:
         return int(self.err_flag.item())
+
+
+class CapturedStep:
+    """A decode step (any sequence of library calls, e.g. every layer's
+    append + attention + reduce) captured once into a CUDA graph and
+    replayed.
+
+    Every kernel of the path reads its per-step data (lengths, block tables,
+    q, the new K/V rows) from device memory and takes only fixed sizes from
+    the host, so a replay sees whatever the caller has written into the same
+    buffers since the last one.  The split-K work counters reset themselves
+    at the end of every launch, so replays need no host action."""
+
+    def __init__(self, fn, warmup: int = 1):
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            for _ in range(warmup):  # fills the library's per-kernel caches
+                fn()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            fn()
+
+    def replay(self):
+        self.graph.replay()
