@@ -15,6 +15,8 @@ arguments.  Each function follows the definition cited in the C source:
   append already counts the token being written).
 * ``kv_append``     - byte copy of each new K/V row into its pool slot (same
   page, ``reshape_and_cache_bf16`` pool layout).
+* ``paged_decode_sinks`` - the gpt-oss variant: per-head sink logits in the
+  softmax denominator and a sliding window (same page, paged_decode_attention_sinks).
 * ``paged_decode``  - softmax(scale * q K^T) V over every cached token of the
   sequence, keys and values gathered through the block table, GQA head map
   h -> h / (Hq/Hkv) ("xserv compare phase8...phase13", qwen3.rs ``repeat_kv``;
@@ -74,9 +76,10 @@ def _bind(lib):
     lib.oracle_slot_mapping.argtypes = [P, I, P, I, I, L, P]
     lib.oracle_kv_append.argtypes = [P, P, P, P, P, I, I, I, I, L, I]
     lib.oracle_paged_decode.argtypes = [P, P, P, P, I, P, I, I, I, I, I, L, D, I, P, I]
+    lib.oracle_paged_decode_sinks.argtypes = [P, P, P, P, I, P, I, I, I, I, I, L, D, P, I, I, P, I]
     lib.oracle_max_threads.argtypes = []
     for f in (lib.oracle_slot_mapping, lib.oracle_kv_append, lib.oracle_paged_decode,
-              lib.oracle_max_threads):
+              lib.oracle_paged_decode_sinks, lib.oracle_max_threads):
         f.restype = ctypes.c_int
     return lib
 
@@ -155,4 +158,26 @@ def paged_decode(q, k_cache, v_cache, block_tables, context_lens, scale: float,
                                  float(scale), _code(qq.dtype), out.data_ptr(),
                                  nthreads or default_threads())
     _check(st, "paged_decode")
+    return out
+
+
+def paged_decode_sinks(q, k_cache, v_cache, block_tables, context_lens, scale: float,
+                       sinks=None, window: int = 0, nthreads: int | None = None,
+                       lib=None) -> torch.Tensor:
+    """fp64 [B, Hq, D]: decode attention with per-head sinks ([Hq], q's dtype,
+    or None) and a sliding window of the last ``window`` tokens (0 = all)."""
+    lib = lib or load()
+    qq, kc, vc = _cpu(q), _cpu(k_cache), _cpu(v_cache)
+    bt = _cpu(block_tables, torch.int32)
+    cl = _cpu(context_lens, torch.int32)
+    B, Hq, D = qq.shape
+    num_blocks, Hkv, bs, _ = kc.shape
+    sk = None if sinks is None else _cpu(sinks, qq.dtype)
+    out = torch.empty(B, Hq, D, dtype=torch.float64)
+    st = lib.oracle_paged_decode_sinks(qq.data_ptr(), kc.data_ptr(), vc.data_ptr(), bt.data_ptr(),
+                                       bt.shape[1], cl.data_ptr(), B, Hq, Hkv, D, bs, num_blocks,
+                                       float(scale), None if sk is None else sk.data_ptr(),
+                                       int(window), _code(qq.dtype), out.data_ptr(),
+                                       nthreads or default_threads())
+    _check(st, "paged_decode_sinks")
     return out

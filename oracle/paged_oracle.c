@@ -190,6 +190,90 @@ int oracle_paged_decode(const void *q, const void *k_cache, const void *v_cache,
     return status;
 }
 
+/*
+ * Paged decode attention with attention sinks and a sliding window (the
+ * gpt-oss variant: "xserv compare phase10...cf1e9e4",
+ * crates/xserv-kernels/src/attention.rs, paged_decode_attention_sinks and
+ * flash_attention_sinks doc comments: a per-query-head sink value folded
+ * into the softmax denominator; window_size 0 = full attention, > 0 =
+ * sliding window).
+ *
+ * Readings: the sink s_h is one more logit, in the same units as
+ * scale * q.K, that has no value row; a window W > 0 keeps the W most
+ * recent tokens, t in [max(0, N - W), N).  sinks may be NULL (no sink);
+ * otherwise it holds Hq values of the q dtype.
+ *     m   = max(max_t logit_t, s_h)
+ *     den = sum_t exp(logit_t - m) + exp(s_h - m)
+ *     out[b, h, :] = sum_t exp(logit_t - m) V_t / den
+ */
+int oracle_paged_decode_sinks(const void *q, const void *k_cache, const void *v_cache,
+                              const int32_t *block_tables, int max_blocks_per_seq,
+                              const int32_t *context_lens, int B, int Hq, int Hkv, int D,
+                              int block_size, int64_t num_blocks, double scale,
+                              const void *sinks, int window, int dtype, double *out,
+                              int nthreads) {
+    if (!elem_bytes(dtype) || B < 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || block_size <= 0 ||
+        window < 0)
+        return ORACLE_EINVAL;
+    if (Hq % Hkv != 0) return ORACLE_EINVAL;
+    const int group = Hq / Hkv;
+    for (int b = 0; b < B; ++b) {
+        int32_t n = context_lens[b];
+        if (n <= 0) continue;
+        int64_t nblk = ((int64_t)n + block_size - 1) / block_size;
+        if (nblk > max_blocks_per_seq) return ORACLE_ETABLE;
+        for (int64_t i = 0; i < nblk; ++i) {
+            int32_t blk = block_tables[(int64_t)b * max_blocks_per_seq + i];
+            if (blk < 0 || blk >= num_blocks) return ORACLE_EBLOCK;
+        }
+    }
+    int status = ORACLE_OK;
+    if (nthreads <= 0) nthreads = 1;
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)
+    for (int64_t bh = 0; bh < (int64_t)B * Hq; ++bh) {
+        int b = (int)(bh / Hq), h = (int)(bh % Hq);
+        int kv_head = h / group;
+        int32_t n = context_lens[b];
+        double *o = out + bh * D;
+        for (int d = 0; d < D; ++d) o[d] = 0.0;
+        if (n <= 0) continue;
+        int32_t first = (window > 0 && n > window) ? n - window : 0;
+        double *lg = (double *)malloc(sizeof(double) * (size_t)(n - first));
+        if (!lg) {
+#pragma omp atomic write
+            status = ORACLE_ENOMEM;
+            continue;
+        }
+        for (int32_t t = first; t < n; ++t) {
+            int64_t blk = block_tables[(int64_t)b * max_blocks_per_seq + t / block_size];
+            int64_t krow = ((blk * Hkv + kv_head) * block_size + t % block_size) * D;
+            double dot = 0.0;
+            for (int d = 0; d < D; ++d)
+                dot += widen(q, bh * D + d, dtype) * widen(k_cache, krow + d, dtype);
+            lg[t - first] = scale * dot;
+        }
+        double top = lg[0];
+        for (int32_t i = 1; i < n - first; ++i)
+            if (lg[i] > top) top = lg[i];
+        double sink = 0.0;
+        if (sinks) {
+            sink = widen(sinks, h, dtype);
+            if (sink > top) top = sink;
+        }
+        double den = sinks ? exp(sink - top) : 0.0;
+        for (int32_t t = first; t < n; ++t) {
+            double wt = exp(lg[t - first] - top);
+            den += wt;
+            int64_t blk = block_tables[(int64_t)b * max_blocks_per_seq + t / block_size];
+            int64_t vrow = ((blk * Hkv + kv_head) * block_size + t % block_size) * D;
+            for (int d = 0; d < D; ++d) o[d] += wt * widen(v_cache, vrow + d, dtype);
+        }
+        for (int d = 0; d < D; ++d) o[d] /= den;
+        free(lg);
+    }
+    return status;
+}
+
 /* Number of threads an OpenMP parallel region would use (1 without OpenMP). */
 int oracle_max_threads(void) {
 #ifdef _OPENMP

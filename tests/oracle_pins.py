@@ -303,9 +303,83 @@ def pin_cache_equals_recompute(lib):
         _close(cached[b], torch.matmul(att, V).squeeze(1), TOL, f"cache==recompute seq {b}")
 
 
+# ------------------------------------------------------- sinks + sliding window
+
+def pin_sink_window_by_hand(lib):
+    c = gc.load_cases()["sink_window_by_hand"]
+    q = torch.tensor(c["q"], dtype=torch.float32)
+    kc, vc = gc.pool_tensor(c, "k_cache"), gc.pool_tensor(c, "v_cache")
+    out = oracle.paged_decode_sinks(q, kc, vc, torch.tensor(c["block_tables"]),
+                                    torch.tensor(c["context_lens"]), gc.scale_of(c),
+                                    sinks=torch.tensor(c["sinks"], dtype=torch.float32),
+                                    window=c["window"], lib=lib)
+    _close(out, gc.expected_of(c), 1e-14, "sink_window_by_hand")
+
+
+def dense_sinks_window(q, k_cache, v_cache, block_tables, context_lens, scale, sinks, window):
+    """Dense float64 formulation: the last `window` tokens gathered to a
+    contiguous copy, the sink appended as one more key column whose value row
+    is zero, then torch.softmax and matmul."""
+    B, Hq, D = q.shape
+    _, Hkv, bs, _ = k_cache.shape
+    rep = Hq // Hkv
+    out = torch.zeros(B, Hq, D, dtype=torch.float64)
+    for b in range(B):
+        n = int(context_lens[b])
+        if n <= 0:
+            continue
+        pages = block_tables[b, : (n + bs - 1) // bs].long()
+        K = k_cache[pages].double().permute(0, 2, 1, 3).reshape(-1, Hkv, D)[:n]
+        V = v_cache[pages].double().permute(0, 2, 1, 3).reshape(-1, Hkv, D)[:n]
+        if window > 0:
+            K, V = K[-window:], V[-window:]
+        K = K.transpose(0, 1).repeat_interleave(rep, dim=0)
+        V = V.transpose(0, 1).repeat_interleave(rep, dim=0)
+        logits = torch.matmul(q[b].double().unsqueeze(1), K.transpose(1, 2)).squeeze(1) * scale
+        if sinks is not None:
+            logits = torch.cat([logits, sinks.double().unsqueeze(1)], dim=1)
+            V = torch.cat([V, torch.zeros(Hq, 1, D, dtype=torch.float64)], dim=1)
+        out[b] = torch.matmul(torch.softmax(logits, dim=-1).unsqueeze(1), V).squeeze(1)
+    return out
+
+
+def pin_sinks_window_dense(lib):
+    for dtype, G, window in ((torch.float32, 2, 5), (torch.bfloat16, 4, 33), (torch.float32, 1, 0)):
+        w = wl.make_workload(wl.custom_config(4, 4 * G, 4, 16, dtype, history=("uniform", (0, 90)),
+                                              pool=("factor", 1.5), seed=41 + G))
+        q, kc, vc, _, _ = _layer(w)
+        g = torch.Generator().manual_seed(G)
+        sinks = (torch.randn(w.cfg.Hq, generator=g) * 2).to(dtype)
+        got = oracle.paged_decode_sinks(q, kc, vc, w.block_tables, w.context_lens, w.scale,
+                                        sinks=sinks, window=window, lib=lib)
+        ref = dense_sinks_window(q, kc, vc, w.block_tables, w.context_lens, w.scale, sinks, window)
+        _close(got, ref, TOL, f"sinks+window dense {dtype} G={G} W={window}")
+
+
+def pin_sinks_window_reduce_to_plain(lib):
+    w = wl.make_workload(wl.custom_config(3, 8, 2, 16, torch.bfloat16, history=("uniform", (1, 70)),
+                                          pool=("factor", 2.0), seed=44))
+    q, kc, vc, _, _ = _layer(w)
+    plain = oracle.paged_decode(q, kc, vc, w.block_tables, w.context_lens, w.scale, lib=lib)
+    # No sink and no window, or a window as long as every context: the plain oracle.
+    a = oracle.paged_decode_sinks(q, kc, vc, w.block_tables, w.context_lens, w.scale, lib=lib)
+    b = oracle.paged_decode_sinks(q, kc, vc, w.block_tables, w.context_lens, w.scale,
+                                  window=int(w.context_lens.max()), lib=lib)
+    _close(a, plain, TOL, "no sink, no window")
+    _close(b, plain, TOL, "window >= context")
+    # A sink far below every logit changes nothing; one far above sends the output to 0.
+    low = oracle.paged_decode_sinks(q, kc, vc, w.block_tables, w.context_lens, w.scale,
+                                    sinks=torch.full((w.cfg.Hq,), -1e4), lib=lib)
+    high = oracle.paged_decode_sinks(q, kc, vc, w.block_tables, w.context_lens, w.scale,
+                                     sinks=torch.full((w.cfg.Hq,), 1e4), lib=lib)
+    _close(low, plain, TOL, "sink -> -inf")
+    _close(high, torch.zeros_like(plain), TOL, "sink -> +inf")
+
+
 ALL_PINS = [
     pin_slots_by_hand, pin_gqa_paged_by_hand, pin_single_token, pin_dense_equivalence,
     pin_brute_force_python, pin_permutation_invariance, pin_constant_v, pin_zero_query_mean,
     pin_dominant_key, pin_linearity_in_v, pin_bf16_widening, pin_append_bytes,
-    pin_cache_equals_recompute,
+    pin_cache_equals_recompute, pin_sink_window_by_hand, pin_sinks_window_dense,
+    pin_sinks_window_reduce_to_plain,
 ]

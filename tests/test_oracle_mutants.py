@@ -32,6 +32,12 @@ MUTANTS = [
     ("append_offset_in_block", "int64_t blk = s / block_size, off = s % block_size;",
      "int64_t blk = s / block_size, off = 0;"),
     ("q_head_index", "const int64_t qbase = bh * D;", "const int64_t qbase = (int64_t)b * D;"),
+    ("sink_dropped", "double den = sinks ? exp(sink - top) : 0.0;", "double den = 0.0;"),
+    ("sink_scaled", "sink = widen(sinks, h, dtype);", "sink = scale * widen(sinks, h, dtype);"),
+    ("window_one_short", "(window > 0 && n > window) ? n - window : 0;",
+     "(window > 0 && n > window) ? n - window + 1 : 0;"),
+    ("window_one_long", "(window > 0 && n > window) ? n - window : 0;",
+     "(window > 0 && n > window) ? n - window - 1 : 0;"),
 ]
 
 
