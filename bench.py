@@ -41,11 +41,14 @@ KERNEL_SRC = os.path.join(ROOT, "paged_kv_cache_xs_gb300", "csrc", "paged_decode
 
 # ------------------------------------------------------------------ byte accounting
 
-def step_bytes(cfg: wl.DecodeConfig, context_lens: torch.Tensor) -> dict:
+def step_bytes(cfg: wl.DecodeConfig, context_lens: torch.Tensor, window: int = 0) -> dict:
     """Algorithmic bytes of one layer of the decode step (per the cost model:
-    K and V read once per KV head, not per query head)."""
+    K and V read once per KV head, not per query head; with a sliding window
+    only the tokens inside it)."""
     s = torch.tensor([], dtype=cfg.dtype).element_size()
     n = context_lens.to(torch.int64).clamp(min=0)
+    if window > 0:
+        n = n.clamp(max=window)
     kv = int(n.sum()) * cfg.Hkv * cfg.D * 2 * s
     q = cfg.B * cfg.Hq * cfg.D * s
     out = cfg.B * cfg.Hq * cfg.D * s
@@ -300,13 +303,21 @@ def run_ours(args, rank, world, local, dist):
     # Weak scaling: every rank runs its own independent batch of the same shape.
     w = wl.make_workload(cfg, device=dev, seed=cfg.seed + 7919 * rank)
     L = cfg.layers
+    sinks = None
+    if args.sinks:
+        g = torch.Generator(device=dev).manual_seed(cfg.seed + 17)
+        sinks = torch.randn(cfg.Hq, generator=g, device=dev).to(cfg.dtype)
+    lens_cpu = w.context_lens.cpu()
+    win_tokens = int(lens_cpu.clamp(max=args.window).sum()) if args.window > 0 \
+        else w.total_context_tokens
     step = PagedDecodeStep(cfg.B, cfg.Hq, cfg.Hkv, cfg.D, w.max_blocks_per_seq, cfg.dtype, dev,
-                           total_context_tokens=w.total_context_tokens,
-                           max_context_len=w.max_context_len,
-                           partition_tokens=args.partition_tokens or None)
+                           total_context_tokens=win_tokens,
+                           max_context_len=min(w.max_context_len, args.window or 1 << 30),
+                           partition_tokens=args.partition_tokens or None,
+                           sinks=sinks, window=args.window)
     out = torch.empty(L, cfg.B, cfg.Hq, cfg.D, dtype=cfg.dtype, device=dev)  # every layer's output
     stream = torch.cuda.current_stream()
-    by = step_bytes(cfg, w.context_lens.cpu())
+    by = step_bytes(cfg, lens_cpu, args.window)
     bytes_per_step = by["step"] * L
 
     def one_step(ev=None):
@@ -432,6 +443,7 @@ def run_ours(args, rank, world, local, dist):
                    "context_tokens": w.total_context_tokens,
                    "max_context_len": w.max_context_len,
                    "partition_tokens": step.partition_tokens,
+                   "sinks": bool(args.sinks), "window": args.window,
                    "max_partitions": step.max_partitions,
                    "l2": f"inputs larger than L2 ({bytes_per_step / 1e9:.2f} GB read per step)",
                    "parallelism": f"replicas x{world} (independent batches, no collective)"},
@@ -465,6 +477,10 @@ def main(argv=None):
                     help="workload index (0-4); default: the large-batch long-context one")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sinks", action="store_true",
+                    help="gpt-oss variant: random per-head sink logits in the softmax")
+    ap.add_argument("--window", type=int, default=0,
+                    help="gpt-oss variant: sliding window of the last W tokens (0 = all)")
     ap.add_argument("--graph", choices=["auto", "on", "off"], default="auto",
                     help="replay each step as one CUDA graph (auto: when the workload has "
                          "more than one layer)")

@@ -243,6 +243,41 @@ int xs_paged_decode(void *out, float *part_o, float *part_m, float *part_l, cons
                     cudaStream_t stream);
 
 /*
+ * xs_paged_decode_attn_sinks / xs_paged_decode_reduce_sinks /
+ * xs_paged_decode_sinks - the gpt-oss variant of the three calls above
+ * ("xserv compare phase10...cf1e9e4", attention.rs,
+ * paged_decode_attention_sinks and launch_paged_decode_attention_sinks_bf16):
+ *  - sinks: NULL or [Hq] values of the q dtype, one per query head.  A sink
+ *    is one more logit, in the same units as scale * q.K, with no value row:
+ *    it only adds exp(sink - max) to the softmax denominator.
+ *  - window: 0 = attend to every cached token; W > 0 = a sliding window,
+ *    only the W most recent tokens [max(0, N - W), N) of each sequence.
+ * The split covers the windowed range; the reduce must get the same sinks
+ * and window as the attention pass.  Arguments and errors otherwise as
+ * xs_paged_decode_attn / xs_paged_decode_reduce / xs_paged_decode; a
+ * negative window is XS_ESHAPE.
+ */
+int xs_paged_decode_attn_sinks(void *out, float *part_o, float *part_m, float *part_l,
+                               const void *q, const void *k_cache, const void *v_cache,
+                               const int32_t *block_tables, int max_blocks_per_seq,
+                               const int32_t *context_lens, const void *sinks, int window, int B,
+                               int Hq, int Hkv, int D, int block_size, int64_t num_blocks,
+                               float scale, int partition_tokens, int max_partitions, int dtype,
+                               int *err_flag, int *work_counters, cudaStream_t stream);
+int xs_paged_decode_reduce_sinks(void *out, const float *part_o, const float *part_m,
+                                 const float *part_l, const int32_t *context_lens,
+                                 const void *sinks, int window, int B, int Hq, int D,
+                                 int partition_tokens, int max_partitions, int dtype,
+                                 cudaStream_t stream);
+int xs_paged_decode_sinks(void *out, float *part_o, float *part_m, float *part_l, const void *q,
+                          const void *k_cache, const void *v_cache, const int32_t *block_tables,
+                          int max_blocks_per_seq, const int32_t *context_lens, const void *sinks,
+                          int window, int B, int Hq, int Hkv, int D, int block_size,
+                          int64_t num_blocks, float scale, int partition_tokens,
+                          int max_partitions, int dtype, int *err_flag, int *work_counters,
+                          cudaStream_t stream);
+
+/*
  * xs_paged_decode_noalloc - xs_paged_decode for callers that cannot allocate
  * device memory.  The paper has no counterpart of this entry point: it is a
  * service of this library.

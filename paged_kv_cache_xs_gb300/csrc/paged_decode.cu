@@ -99,6 +99,8 @@ struct Params {
     int max_blocks, B, Hq, Hkv, P, max_parts;
     int64_t num_blocks;
     float qscale;  // scale * log2(e)
+    const void *sinks;  // [Hq] sink logits (q's dtype), or null
+    int window;         // > 0: attend to the last `window` tokens only
     int *err_flag;
     int *work;     // [2] item counter + finished-CTA counter (zero between launches), or null
 };
@@ -115,9 +117,15 @@ __device__ __forceinline__ int seq_len(const Params &p, int b, bool report) {
 }
 
 struct Item {
-    int b, g, part, n, tok0, tok1, pg0, pg1;
+    int b, g, part, nparts, tok0, tok1, pg0, pg1;
 };
 static_assert(sizeof(Item) == 32, "item slots and merge-buffer headers are 32 bytes");
+
+// First token a sequence of n tokens attends to: the sliding window keeps
+// the last p.window tokens (all of them when p.window is 0).
+__device__ __forceinline__ int first_token(const Params &p, int n) {
+    return (p.window > 0 && n > p.window) ? n - p.window : 0;
+}
 
 // Largest b in [0, B) with table[b] <= x (table is non-decreasing).
 __device__ __forceinline__ int upper_index(const int *table, int B, int x) {
@@ -148,12 +156,13 @@ __device__ __forceinline__ Item decode_item(const Params &p, const int *pfull, c
         const int r2 = item - n_full;
         b = upper_index(ptail, p.B, r2);
         it.g = r2 - ptail[b];
-        it.part = nlen[b] / p.P;
+        it.part = (nlen[b] - first_token(p, nlen[b])) / p.P;
     }
     it.b = b;
-    it.n = nlen[b];
-    it.tok0 = it.part * p.P;
-    it.tok1 = min(it.n, it.tok0 + p.P);
+    const int n = nlen[b], t0 = first_token(p, n);
+    it.nparts = (n - t0 + p.P - 1) / p.P;
+    it.tok0 = t0 + it.part * p.P;
+    it.tok1 = min(n, it.tok0 + p.P);
     it.pg0 = it.tok0 / kBlock;
     it.pg1 = (it.tok1 + kBlock - 1) / kBlock;
     return it;
@@ -187,11 +196,12 @@ __device__ __forceinline__ void load_v(const unsigned char *src, float *vf) {
 }
 
 // One consumer warp folds one page (16 tokens of one KV head) into its
-// online-softmax state.  kFull: all 16 tokens are valid (every page but a
-// sequence's last), which lets the PV loop unroll completely.
+// online-softmax state; only tokens [t_lo, t_hi) of the page count.  kFull:
+// all 16 are valid (every page but the first and last of a windowed or
+// ragged range), which lets the PV loop unroll completely.
 template <typename T, int D, int G, bool kFull>
 __device__ __forceinline__ void consume_page(const unsigned char *Ks, const unsigned char *Vs,
-                                             int n_valid, const float (&qf)[G][D / 8],
+                                             int t_lo, int t_hi, const float (&qf)[G][D / 8],
                                              float &m_own, float &l_own,
                                              float2 (&o)[G][D / 64], float2 *W2, int lane) {
     using C = Cfg<T, D, G>;
@@ -245,7 +255,7 @@ __device__ __forceinline__ void consume_page(const unsigned char *Ks, const unsi
                 v[0] += __shfl_xor_sync(0xffffffffu, v[0], mask);
             }
         }
-        sc[pass] = (kFull || t < n_valid) ? v[0] : -INFINITY;
+        sc[pass] = (kFull || (t >= t_lo && t < t_hi)) ? v[0] : -INFINITY;
     }
 
     // ---- online softmax for head own_head (lanes sharing j agree)
@@ -299,7 +309,7 @@ __device__ __forceinline__ void consume_page(const unsigned char *Ks, const unsi
 #pragma unroll
         for (int t = 0; t < kBlock; ++t) pv_token(t);
     } else {
-        for (int t = 0; t < n_valid; ++t) pv_token(t);
+        for (int t = t_lo; t < t_hi; ++t) pv_token(t);
     }
     __syncwarp();
 }
@@ -348,15 +358,17 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
         s_abort = 0;
     }
     {
-        // Per sequence: n/P full partitions and (n % P != 0) ragged one, each
-        // x Hkv heads.  Chunked scan of both counts over the block.
+        // Per sequence: nw/P full partitions and (nw % P != 0) ragged one, each
+        // x Hkv heads (nw = tokens inside the window).  Chunked scan of both
+        // counts over the block.
         const int per = (p.B + kThreads - 1) / kThreads;
         const int b0 = min(p.B, tid * per), b1 = min(p.B, b0 + per);
         int lf = 0, lt = 0;
         for (int b = b0; b < b1; ++b) {
             const int n = max(seq_len(p, b, blockIdx.x == 0), 0);
-            lf += (n / p.P) * p.Hkv;
-            lt += (n % p.P != 0) * p.Hkv;
+            const int nw = n - first_token(p, n);  // tokens inside the window
+            lf += (nw / p.P) * p.Hkv;
+            lt += (nw % p.P != 0) * p.Hkv;
         }
         int xf = lf, xt = lt;
 #pragma unroll
@@ -382,11 +394,12 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
         int runf = basef + xf - lf, runt = baset + xt - lt;  // exclusive prefixes
         for (int b = b0; b < b1; ++b) {
             const int n = max(seq_len(p, b, false), 0);
+            const int nw = n - first_token(p, n);
             pfull[b] = runf;
             ptail[b] = runt;
             nlen[b] = n;
-            runf += (n / p.P) * p.Hkv;
-            runt += (n % p.P != 0) * p.Hkv;
+            runf += (nw / p.P) * p.Hkv;
+            runt += (nw % p.P != 0) * p.Hkv;
         }
         if (tid == kThreads - 1) {
             pfull[p.B] = basef + xf;
@@ -436,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
                 it = decode_item(p, pfull, ptail, nlen, item);
             } else {
                 it.b = -1;
-                it.g = it.part = it.n = it.tok0 = it.tok1 = it.pg0 = it.pg1 = 0;
+                it.g = it.part = it.nparts = it.tok0 = it.tok1 = it.pg0 = it.pg1 = 0;
             }
             return it;
         };
@@ -560,7 +573,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
             const float *cO = cL + kConsumerWarps * G;
             const bool valid = it.b < p.B && it.g >= 0 && it.g < p.Hkv && it.part >= 0 &&
                                it.part < p.max_parts && !*static_cast<volatile int *>(&s_abort);
-            const bool single = (it.n + p.P - 1) / p.P == 1;
+            const bool single = it.nparts == 1;
             const int64_t head0 =
                 static_cast<int64_t>(it.b) * p.Hq + static_cast<int64_t>(it.g) * G;
             for (int ch = lane; valid && ch < G * D / 4; ch += 32) {
@@ -583,7 +596,14 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
                     ot.z += f * v.z;
                     ot.w += f * v.w;
                 }
-                const float inv = 1.f / lt;
+                // A sink is one more logit with no value row: it only adds to
+                // the final denominator (partials leave it to the reduce).
+                float den = lt;
+                if (single && p.sinks)
+                    den += fast_exp2(Elem<T>::to_f32(static_cast<const T *>(p.sinks)[it.g * G + h]) *
+                                         kLog2e -
+                                     mx);
+                const float inv = 1.f / (single ? den : lt);
                 ot.x *= inv;
                 ot.y *= inv;
                 ot.z *= inv;
@@ -669,11 +689,12 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
             }
             const unsigned char *Ks = smem + s * 2 * C::kPageBytes;
             const unsigned char *Vs = Ks + C::kPageBytes;
-            const int n_valid = min(kBlock, it.tok1 - pg * kBlock);
-            if (n_valid == kBlock)
-                consume_page<T, D, G, true>(Ks, Vs, kBlock, qf, m_own, l_own, o, W2, lane);
+            const int t_lo = max(0, it.tok0 - pg * kBlock);
+            const int t_hi = min(kBlock, it.tok1 - pg * kBlock);
+            if (t_lo == 0 && t_hi == kBlock)
+                consume_page<T, D, G, true>(Ks, Vs, 0, kBlock, qf, m_own, l_own, o, W2, lane);
             else
-                consume_page<T, D, G, false>(Ks, Vs, n_valid, qf, m_own, l_own, o, W2, lane);
+                consume_page<T, D, G, false>(Ks, Vs, t_lo, t_hi, qf, m_own, l_own, o, W2, lane);
             if (lane == 0) mbar_arrive(&empty[s]);
         }
         page_ctr += static_cast<uint32_t>(it.pg1 - it.pg0);
@@ -721,15 +742,19 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
 }
 
 // Split-K combine: one CTA of D threads per (sequence, query head).
+// With sinks, a sink is one more logit (no value row) in the denominator;
+// with a window, only the last `window` tokens were split into partitions.
 template <typename T>
 __global__ void paged_decode_reduce_kernel(T *__restrict__ out, const float *__restrict__ part_o,
                                            const float *__restrict__ part_m,
                                            const float *__restrict__ part_l,
                                            const int32_t *__restrict__ lens, int Hq, int D, int P,
-                                           int max_parts) {
+                                           int max_parts, const T *__restrict__ sinks,
+                                           int window) {
     const int bh = blockIdx.x;
     const int b = bh / Hq;
-    const int n = lens[b];
+    int n = lens[b];
+    if (window > 0 && n > window) n = window;
     int np = n > 0 ? (n + P - 1) / P : 0;
     np = min(np, max_parts);
     if (np <= 1) return;
@@ -745,6 +770,7 @@ __global__ void paged_decode_reduce_kernel(T *__restrict__ out, const float *__r
         lt += f;
         if (d < D) acc += f * part_o[(base + i) * D + d];
     }
+    if (sinks) lt += fast_exp2(Elem<T>::to_f32(sinks[bh % Hq]) * kLog2e - mx);
     if (d < D) out[static_cast<int64_t>(bh) * D + d] = Elem<T>::from_f32(acc / lt);
 }
 
@@ -919,13 +945,13 @@ static int check_attn_args(const void *out, const float *po, const float *pm, co
     return XS_OK;
 }
 
-extern "C" int xs_paged_decode_attn(void *out, float *part_o, float *part_m, float *part_l,
-                                    const void *q, const void *k_cache, const void *v_cache,
-                                    const int32_t *block_tables, int max_blocks_per_seq,
-                                    const int32_t *context_lens, int B, int Hq, int Hkv, int D,
-                                    int block_size, int64_t num_blocks, float scale,
-                                    int partition_tokens, int max_partitions, int dtype,
-                                    int *err_flag, int *work_counters, cudaStream_t stream) {
+static int launch_attn(void *out, float *part_o, float *part_m, float *part_l, const void *q,
+                       const void *k_cache, const void *v_cache, const int32_t *block_tables,
+                       int max_blocks_per_seq, const int32_t *context_lens, int B, int Hq,
+                       int Hkv, int D, int block_size, int64_t num_blocks, float scale,
+                       const void *sinks, int window, int partition_tokens, int max_partitions,
+                       int dtype, int *err_flag, int *work_counters, cudaStream_t stream) {
+    if (window < 0) return XS_ESHAPE;
     int st = check_attn_args(out, part_o, part_m, part_l, q, k_cache, v_cache, block_tables,
                              max_blocks_per_seq, context_lens, B, Hq, Hkv, D, block_size,
                              num_blocks, partition_tokens, max_partitions, dtype);
@@ -961,17 +987,48 @@ extern "C" int xs_paged_decode_attn(void *out, float *part_o, float *part_m, flo
     p.max_parts = max_partitions;
     p.num_blocks = num_blocks;
     p.qscale = scale * attn::kLog2e;
+    p.sinks = sinks;
+    p.window = window;
     p.err_flag = err_flag;
     p.work = work_counters;
     fn<<<grid, attn::kThreads, smem, stream>>>(p);
     return launch_status();
 }
 
-extern "C" int xs_paged_decode_reduce(void *out, const float *part_o, const float *part_m,
-                                      const float *part_l, const int32_t *context_lens, int B,
-                                      int Hq, int D, int partition_tokens, int max_partitions,
-                                      int dtype, cudaStream_t stream) {
+extern "C" int xs_paged_decode_attn(void *out, float *part_o, float *part_m, float *part_l,
+                                    const void *q, const void *k_cache, const void *v_cache,
+                                    const int32_t *block_tables, int max_blocks_per_seq,
+                                    const int32_t *context_lens, int B, int Hq, int Hkv, int D,
+                                    int block_size, int64_t num_blocks, float scale,
+                                    int partition_tokens, int max_partitions, int dtype,
+                                    int *err_flag, int *work_counters, cudaStream_t stream) {
+    return launch_attn(out, part_o, part_m, part_l, q, k_cache, v_cache, block_tables,
+                       max_blocks_per_seq, context_lens, B, Hq, Hkv, D, block_size, num_blocks,
+                       scale, nullptr, 0, partition_tokens, max_partitions, dtype, err_flag,
+                       work_counters, stream);
+}
+
+extern "C" int xs_paged_decode_attn_sinks(void *out, float *part_o, float *part_m, float *part_l,
+                                          const void *q, const void *k_cache, const void *v_cache,
+                                          const int32_t *block_tables, int max_blocks_per_seq,
+                                          const int32_t *context_lens, const void *sinks,
+                                          int window, int B, int Hq, int Hkv, int D,
+                                          int block_size, int64_t num_blocks, float scale,
+                                          int partition_tokens, int max_partitions, int dtype,
+                                          int *err_flag, int *work_counters,
+                                          cudaStream_t stream) {
+    return launch_attn(out, part_o, part_m, part_l, q, k_cache, v_cache, block_tables,
+                       max_blocks_per_seq, context_lens, B, Hq, Hkv, D, block_size, num_blocks,
+                       scale, sinks, window, partition_tokens, max_partitions, dtype, err_flag,
+                       work_counters, stream);
+}
+
+static int launch_reduce(void *out, const float *part_o, const float *part_m,
+                         const float *part_l, const int32_t *context_lens, const void *sinks,
+                         int window, int B, int Hq, int D, int partition_tokens,
+                         int max_partitions, int dtype, cudaStream_t stream) {
     if (!out || !context_lens) return XS_ENULL;
+    if (window < 0) return XS_ESHAPE;
     if (!elem_bytes(dtype)) return XS_EDTYPE;
     if (B < 0 || Hq <= 0 || D <= 0 || D > 1024 || partition_tokens <= 0 || max_partitions <= 0)
         return XS_ESHAPE;
@@ -984,12 +1041,29 @@ extern "C" int xs_paged_decode_reduce(void *out, const float *part_o, const floa
         attn::paged_decode_reduce_kernel<__nv_bfloat16><<<static_cast<int>(blocks), threads, 0,
                                                           stream>>>(
             static_cast<__nv_bfloat16 *>(out), part_o, part_m, part_l, context_lens, Hq, D,
-            partition_tokens, max_partitions);
+            partition_tokens, max_partitions, static_cast<const __nv_bfloat16 *>(sinks), window);
     else
         attn::paged_decode_reduce_kernel<float><<<static_cast<int>(blocks), threads, 0, stream>>>(
             static_cast<float *>(out), part_o, part_m, part_l, context_lens, Hq, D,
-            partition_tokens, max_partitions);
+            partition_tokens, max_partitions, static_cast<const float *>(sinks), window);
     return launch_status();
+}
+
+extern "C" int xs_paged_decode_reduce(void *out, const float *part_o, const float *part_m,
+                                      const float *part_l, const int32_t *context_lens, int B,
+                                      int Hq, int D, int partition_tokens, int max_partitions,
+                                      int dtype, cudaStream_t stream) {
+    return launch_reduce(out, part_o, part_m, part_l, context_lens, nullptr, 0, B, Hq, D,
+                         partition_tokens, max_partitions, dtype, stream);
+}
+
+extern "C" int xs_paged_decode_reduce_sinks(void *out, const float *part_o, const float *part_m,
+                                            const float *part_l, const int32_t *context_lens,
+                                            const void *sinks, int window, int B, int Hq, int D,
+                                            int partition_tokens, int max_partitions, int dtype,
+                                            cudaStream_t stream) {
+    return launch_reduce(out, part_o, part_m, part_l, context_lens, sinks, window, B, Hq, D,
+                         partition_tokens, max_partitions, dtype, stream);
 }
 
 extern "C" int xs_paged_decode(void *out, float *part_o, float *part_m, float *part_l,
@@ -1006,6 +1080,24 @@ extern "C" int xs_paged_decode(void *out, float *part_o, float *part_m, float *p
     if (st != XS_OK || max_partitions <= 1) return st;
     return xs_paged_decode_reduce(out, part_o, part_m, part_l, context_lens, B, Hq, D,
                                   partition_tokens, max_partitions, dtype, stream);
+}
+
+extern "C" int xs_paged_decode_sinks(void *out, float *part_o, float *part_m, float *part_l,
+                                     const void *q, const void *k_cache, const void *v_cache,
+                                     const int32_t *block_tables, int max_blocks_per_seq,
+                                     const int32_t *context_lens, const void *sinks, int window,
+                                     int B, int Hq, int Hkv, int D, int block_size,
+                                     int64_t num_blocks, float scale, int partition_tokens,
+                                     int max_partitions, int dtype, int *err_flag,
+                                     int *work_counters, cudaStream_t stream) {
+    int st = xs_paged_decode_attn_sinks(out, part_o, part_m, part_l, q, k_cache, v_cache,
+                                        block_tables, max_blocks_per_seq, context_lens, sinks,
+                                        window, B, Hq, Hkv, D, block_size, num_blocks, scale,
+                                        partition_tokens, max_partitions, dtype, err_flag,
+                                        work_counters, stream);
+    if (st != XS_OK || max_partitions <= 1) return st;
+    return xs_paged_decode_reduce_sinks(out, part_o, part_m, part_l, context_lens, sinks, window,
+                                        B, Hq, D, partition_tokens, max_partitions, dtype, stream);
 }
 
 // ---------------------------------------------------------------- no-allocation variant

@@ -45,6 +45,12 @@ SIGNATURES = {
                              _I, _I, _I, _P, _P, _P]),
     "xs_paged_decode_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _L, _F,
                                      _I, _I, _P, _P]),
+    "xs_paged_decode_attn_sinks": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I,
+                                        _I, _I, _I, _L, _F, _I, _I, _I, _P, _P, _P]),
+    "xs_paged_decode_reduce_sinks": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I,
+                                          _P]),
+    "xs_paged_decode_sinks": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I,
+                                   _I, _I, _L, _F, _I, _I, _I, _P, _P, _P]),
     "xs_version": (_I, []),
 }
 
@@ -201,6 +207,40 @@ def xs_paged_decode_noalloc(out, q, k_cache, v_cache, block_tables, context_lens
           _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), B, Hq, Hkv, D, bs,
           num_blocks, float(scale), int(partition_tokens), dtype_code(q.dtype), _ptr(err_flag),
           _stream(stream))
+
+
+def xs_paged_decode_sinks(out, part_o, part_m, part_l, q, k_cache, v_cache, block_tables,
+                          context_lens, scale, partition_tokens, max_partitions, sinks=None,
+                          window=0, err_flag=None, work_counters=None, stream=None):
+    """Decode attention with per-head sinks ([Hq], q's dtype, or None) and a
+    sliding window of the last ``window`` tokens (0 = all): attn + reduce."""
+    B, Hq, D = q.shape
+    num_blocks, Hkv, bs, _ = k_cache.shape
+    _call("xs_paged_decode_sinks", _ptr(out), _ptr(part_o), _ptr(part_m), _ptr(part_l), _ptr(q),
+          _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1],
+          _ptr(context_lens), _ptr(sinks), int(window), B, Hq, Hkv, D, bs, num_blocks,
+          float(scale), partition_tokens, max_partitions, dtype_code(q.dtype), _ptr(err_flag),
+          _ptr(work_counters), _stream(stream))
+
+
+def xs_paged_decode_attn_sinks(out, part_o, part_m, part_l, q, k_cache, v_cache, block_tables,
+                               context_lens, scale, partition_tokens, max_partitions, sinks=None,
+                               window=0, err_flag=None, work_counters=None, stream=None):
+    B, Hq, D = q.shape
+    num_blocks, Hkv, bs, _ = k_cache.shape
+    _call("xs_paged_decode_attn_sinks", _ptr(out), _ptr(part_o), _ptr(part_m), _ptr(part_l),
+          _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1],
+          _ptr(context_lens), _ptr(sinks), int(window), B, Hq, Hkv, D, bs, num_blocks,
+          float(scale), partition_tokens, max_partitions, dtype_code(q.dtype), _ptr(err_flag),
+          _ptr(work_counters), _stream(stream))
+
+
+def xs_paged_decode_reduce_sinks(out, part_o, part_m, part_l, context_lens, partition_tokens,
+                                 max_partitions, sinks=None, window=0, stream=None):
+    B, Hq, D = out.shape
+    _call("xs_paged_decode_reduce_sinks", _ptr(out), _ptr(part_o), _ptr(part_m), _ptr(part_l),
+          _ptr(context_lens), _ptr(sinks), int(window), B, Hq, D, partition_tokens,
+          max_partitions, dtype_code(out.dtype), _stream(stream))
 
 
 def xs_version() -> int:

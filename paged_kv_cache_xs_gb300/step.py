@@ -22,10 +22,14 @@ from . import ops
 
 
 class PagedDecodeStep:
+    """sinks ([Hq] tensor of q's dtype, or None) and window (0 = all tokens)
+    select the gpt-oss variant: per-head sink logits and a sliding window."""
+
     def __init__(self, B: int, Hq: int, Hkv: int, D: int, max_blocks_per_seq: int, dtype,
                  device, total_context_tokens: int = 0, max_context_len: int | None = None,
-                 partition_tokens: int | None = None):
+                 partition_tokens: int | None = None, sinks=None, window: int = 0):
         self.B, self.Hq, self.Hkv, self.D = B, Hq, Hkv, D
+        self.sinks, self.window = sinks, int(window)
         self.dtype = dtype
         self.device = torch.device(device)
         self.max_blocks_per_seq = max_blocks_per_seq
@@ -54,16 +58,29 @@ class PagedDecodeStep:
 
     def attend(self, out, q, k_cache, v_cache, block_tables, context_lens, scale):
         ws = self.ws
-        ops.xs_paged_decode_attn(out, ws.part_o, ws.part_m, ws.part_l, q, k_cache, v_cache,
-                                 block_tables, context_lens, scale, ws.partition_tokens,
-                                 ws.max_partitions, err_flag=self.err_flag,
-                                 work_counters=ws.work)
+        if self.sinks is None and self.window == 0:
+            ops.xs_paged_decode_attn(out, ws.part_o, ws.part_m, ws.part_l, q, k_cache, v_cache,
+                                     block_tables, context_lens, scale, ws.partition_tokens,
+                                     ws.max_partitions, err_flag=self.err_flag,
+                                     work_counters=ws.work)
+        else:
+            ops.xs_paged_decode_attn_sinks(out, ws.part_o, ws.part_m, ws.part_l, q, k_cache,
+                                           v_cache, block_tables, context_lens, scale,
+                                           ws.partition_tokens, ws.max_partitions,
+                                           sinks=self.sinks, window=self.window,
+                                           err_flag=self.err_flag, work_counters=ws.work)
 
     def reduce(self, out, context_lens):
         ws = self.ws
-        if ws.max_partitions > 1:
+        if ws.max_partitions <= 1:
+            return
+        if self.sinks is None and self.window == 0:
             ops.xs_paged_decode_reduce(out, ws.part_o, ws.part_m, ws.part_l, context_lens,
                                        ws.partition_tokens, ws.max_partitions)
+        else:
+            ops.xs_paged_decode_reduce_sinks(out, ws.part_o, ws.part_m, ws.part_l, context_lens,
+                                             ws.partition_tokens, ws.max_partitions,
+                                             sinks=self.sinks, window=self.window)
 
     def run(self, out, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, scale):
         """Append this step's K/V, then attend; all tensors on the device."""
