@@ -15,6 +15,8 @@ arguments.  Each function follows the definition cited in the C source:
   append already counts the token being written).
 * ``kv_append``     - byte copy of each new K/V row into its pool slot (same
   page, ``reshape_and_cache_bf16`` pool layout).
+* ``kv_swap``       - whole-block copies between a device pool and a host
+  swap pool (the README's CPU swap-out/in of KV blocks).
 * ``paged_decode_sinks`` - the gpt-oss variant: per-head sink logits in the
   softmax denominator and a sliding window (same page, paged_decode_attention_sinks).
 * ``paged_decode``  - softmax(scale * q K^T) V over every cached token of the
@@ -77,9 +79,10 @@ def _bind(lib):
     lib.oracle_kv_append.argtypes = [P, P, P, P, P, I, I, I, I, L, I]
     lib.oracle_paged_decode.argtypes = [P, P, P, P, I, P, I, I, I, I, I, L, D, I, P, I]
     lib.oracle_paged_decode_sinks.argtypes = [P, P, P, P, I, P, I, I, I, I, I, L, D, P, I, I, P, I]
+    lib.oracle_kv_swap.argtypes = [P, P, P, P, P, I, L, L, L]
     lib.oracle_max_threads.argtypes = []
     for f in (lib.oracle_slot_mapping, lib.oracle_kv_append, lib.oracle_paged_decode,
-              lib.oracle_paged_decode_sinks, lib.oracle_max_threads):
+              lib.oracle_paged_decode_sinks, lib.oracle_kv_swap, lib.oracle_max_threads):
         f.restype = ctypes.c_int
     return lib
 
@@ -181,3 +184,19 @@ def paged_decode_sinks(q, k_cache, v_cache, block_tables, context_lens, scale: f
                                        nthreads or default_threads())
     _check(st, "paged_decode_sinks")
     return out
+
+
+def kv_swap(src_k, src_v, dst_k, dst_v, mapping, lib=None):
+    """Return copies of (dst_k, dst_v) with the mapped blocks of the source
+    pools copied in; mapping is int64 [n, 2] of (source block, destination
+    block), pools are [blocks, ...] tensors of one dtype."""
+    lib = lib or load()
+    sk, sv = _cpu(src_k), _cpu(src_v)
+    dk, dv = _cpu(dst_k).clone(), _cpu(dst_v).clone()
+    mp = _cpu(mapping, torch.int64).reshape(-1, 2).contiguous()
+    block_bytes = sk[0].numel() * sk.element_size() if sk.shape[0] else \
+        dk[0].numel() * dk.element_size()
+    st = lib.oracle_kv_swap(sk.data_ptr(), sv.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                            mp.data_ptr(), mp.shape[0], block_bytes, sk.shape[0], dk.shape[0])
+    _check(st, "kv_swap")
+    return dk, dv

@@ -274,6 +274,32 @@ int oracle_paged_decode_sinks(const void *q, const void *k_cache, const void *v_
     return status;
 }
 
+/*
+ * KV swap: copy whole KV blocks between two pools (the pages' CPU swap-out /
+ * swap-in of paged KV blocks to pinned host memory: "xserv compare
+ * phase10...cf1e9e4", README, --swap-space-gb).  For every pair
+ * i < n of mapping ([n][2] int64: source block, destination block) with both
+ * ids >= 0, the block_bytes bytes of source block s in src_k (and src_v) are
+ * copied to destination block d of dst_k (and dst_v).  A pair with a
+ * negative id is skipped; an id at or past its pool's size is an error.
+ * Destinations are expected to be distinct.
+ */
+int oracle_kv_swap(const void *src_k, const void *src_v, void *dst_k, void *dst_v,
+                   const int64_t *mapping, int n, int64_t block_bytes, int64_t src_blocks,
+                   int64_t dst_blocks) {
+    if (n < 0 || block_bytes <= 0) return ORACLE_EINVAL;
+    for (int i = 0; i < n; ++i) {
+        int64_t s = mapping[2 * i], d = mapping[2 * i + 1];
+        if (s < 0 || d < 0) continue;
+        if (s >= src_blocks || d >= dst_blocks) return ORACLE_EBLOCK;
+        memcpy((char *)dst_k + d * block_bytes, (const char *)src_k + s * block_bytes,
+               (size_t)block_bytes);
+        memcpy((char *)dst_v + d * block_bytes, (const char *)src_v + s * block_bytes,
+               (size_t)block_bytes);
+    }
+    return ORACLE_OK;
+}
+
 /* Number of threads an OpenMP parallel region would use (1 without OpenMP). */
 int oracle_max_threads(void) {
 #ifdef _OPENMP

@@ -376,10 +376,43 @@ def pin_sinks_window_reduce_to_plain(lib):
     _close(high, torch.zeros_like(plain), TOL, "sink -> +inf")
 
 
+# ------------------------------------------------------------------- KV swap
+
+def pin_swap_by_indexing(lib):
+    """Swap-out then swap-in against tensor indexing, bit for bit."""
+    g = torch.Generator().manual_seed(51)
+    for dtype in (torch.bfloat16, torch.float32):
+        dev_k = torch.randn(12, 2, 16, 8, generator=g).to(dtype)
+        dev_v = torch.randn(12, 2, 16, 8, generator=g).to(dtype)
+        host_k = torch.randn(5, 2, 16, 8, generator=g).to(dtype)
+        host_v = torch.randn(5, 2, 16, 8, generator=g).to(dtype)
+        out_map = torch.tensor([[7, 0], [2, 3], [-1, 4], [11, 1]])
+        hk, hv = oracle.kv_swap(dev_k, dev_v, host_k, host_v, out_map, lib=lib)
+        ek, ev = host_k.clone(), host_v.clone()
+        ek[[0, 3, 1]] = dev_k[[7, 2, 11]]
+        ev[[0, 3, 1]] = dev_v[[7, 2, 11]]
+        iv = lambda t: t.view(torch.int16 if t.element_size() == 2 else torch.int32)
+        assert torch.equal(iv(hk), iv(ek)) and torch.equal(iv(hv), iv(ev)), "swap-out"
+        # Swap the three blocks back in to other device blocks.
+        in_map = torch.tensor([[0, 9], [3, 4], [1, 5]])
+        dk, dv = oracle.kv_swap(hk, hv, dev_k, dev_v, in_map, lib=lib)
+        fk, fv = dev_k.clone(), dev_v.clone()
+        fk[[9, 4, 5]] = dev_k[[7, 2, 11]]
+        fv[[9, 4, 5]] = dev_v[[7, 2, 11]]
+        assert torch.equal(iv(dk), iv(fk)) and torch.equal(iv(dv), iv(fv)), "swap-in"
+    # A block id past a pool is an error, never a silent copy.
+    try:
+        oracle.kv_swap(dev_k, dev_v, host_k, host_v, torch.tensor([[12, 0]]), lib=lib)
+    except oracle.OracleError:
+        pass
+    else:
+        raise AssertionError("out-of-range source block accepted")
+
+
 ALL_PINS = [
     pin_slots_by_hand, pin_gqa_paged_by_hand, pin_single_token, pin_dense_equivalence,
     pin_brute_force_python, pin_permutation_invariance, pin_constant_v, pin_zero_query_mean,
     pin_dominant_key, pin_linearity_in_v, pin_bf16_widening, pin_append_bytes,
     pin_cache_equals_recompute, pin_sink_window_by_hand, pin_sinks_window_dense,
-    pin_sinks_window_reduce_to_plain,
+    pin_sinks_window_reduce_to_plain, pin_swap_by_indexing,
 ]

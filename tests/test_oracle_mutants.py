@@ -32,6 +32,11 @@ MUTANTS = [
     ("append_offset_in_block", "int64_t blk = s / block_size, off = s % block_size;",
      "int64_t blk = s / block_size, off = 0;"),
     ("q_head_index", "const int64_t qbase = bh * D;", "const int64_t qbase = (int64_t)b * D;"),
+    ("swap_k_into_v", "memcpy((char *)dst_v + d * block_bytes, (const char *)src_v + s * block_bytes,",
+     "memcpy((char *)dst_v + d * block_bytes, (const char *)src_k + s * block_bytes,"),
+    # (every mutant must keep its accesses in bounds: it runs inside the test process)
+    ("swap_dst_stride", "memcpy((char *)dst_k + d * block_bytes, (const char *)src_k + s * block_bytes,",
+     "memcpy((char *)dst_k + d * (block_bytes / 2), (const char *)src_k + s * block_bytes,"),
     ("sink_dropped", "double den = sinks ? exp(sink - top) : 0.0;", "double den = 0.0;"),
     ("sink_scaled", "sink = widen(sinks, h, dtype);", "sink = scale * widen(sinks, h, dtype);"),
     ("window_one_short", "(window > 0 && n > window) ? n - window : 0;",
