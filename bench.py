@@ -468,6 +468,69 @@ def run_ours(args, rank, world, local, dist):
     print(json.dumps(line), flush=True)
 
 
+def run_swap(args, rank, world, local, dist):
+    """KV swap row: whole blocks between the device pool and a pinned host
+    swap pool (swap-out, swap-in), against the plain DMA rate of the same bytes."""
+    from paged_kv_cache_xs_gb300 import build as xsbuild
+    from paged_kv_cache_xs_gb300 import ops
+
+    xsbuild.build()
+    ops.load()
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    cfg = wl.CONFIGS[args.config]
+    nb = 262144 if args.config == 4 else 65536
+    n = args.swap_blocks
+    shape = (nb, cfg.Hkv, cfg.block_size, cfg.D)
+    kd = torch.empty(shape, dtype=cfg.dtype, device=dev).normal_()
+    vd = torch.empty(shape, dtype=cfg.dtype, device=dev).normal_()
+    kh = torch.empty((n,) + shape[1:], dtype=cfg.dtype).pin_memory()
+    vh = torch.empty((n,) + shape[1:], dtype=cfg.dtype).pin_memory()
+    g = torch.Generator().manual_seed(cfg.seed)
+    blocks = torch.randperm(nb, generator=g)[:n]
+    out_map = torch.stack([blocks, torch.arange(n)], 1).to(torch.int64).to(dev)
+    in_map = torch.stack([torch.arange(n), blocks], 1).to(torch.int64).to(dev)
+    moved = 2 * n * kd[0].numel() * kd.element_size()          # K + V bytes per direction
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def timed(fn, reps):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    t_out = timed(lambda: ops.xs_kv_swap(kd, vd, kh, vh, out_map, err_flag=err), args.steps)
+    t_in = timed(lambda: ops.xs_kv_swap(kh, vh, kd, vd, in_map, err_flag=err), args.steps)
+    assert int(err.item()) == 0
+    # Reference: one contiguous DMA copy of the same bytes each way.
+    flat_d = torch.empty(moved // 2, dtype=torch.uint8, device=dev)
+    flat_h = torch.empty(moved // 2, dtype=torch.uint8).pin_memory()
+    t_d2h = timed(lambda: flat_h.copy_(flat_d, non_blocking=True), args.steps) * 2
+    t_h2d = timed(lambda: flat_d.copy_(flat_h, non_blocking=True), args.steps) * 2
+    if rank != 0:
+        return
+    gbs = lambda ms: moved / (ms * 1e-3) / 1e9
+    line = {
+        "metric": "KV swap GB/s (device pool <-> pinned host swap pool)",
+        "value": round(gbs((t_out + t_in) / 2), 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t_out + t_in, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if cfg.dtype == torch.bfloat16 else "f32", "data": "synthetic",
+        "config": {"workload": f"{cfg.name}_swap", "blocks_per_direction": n,
+                   "block_bytes": kd[0].numel() * kd.element_size(), "pool_blocks": nb},
+        "swap_out_gbs": round(gbs(t_out), 2), "swap_in_gbs": round(gbs(t_in), 2),
+        "dma_copy_d2h_gbs": round(gbs(t_d2h), 2), "dma_copy_h2d_gbs": round(gbs(t_h2d), 2),
+        "gpu_launches": 2 * args.steps,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__)
     ap.add_argument("--gpus", type=int, default=1)
@@ -476,6 +539,10 @@ def main(argv=None):
     ap.add_argument("--config", type=int, default=4,
                     help="workload index (0-4); default: the large-batch long-context one")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--op", choices=["decode", "swap"], default="decode",
+                    help="decode: the decode step (default); swap: KV block swap to pinned host")
+    ap.add_argument("--swap-blocks", type=int, default=16384,
+                    help="blocks per swap direction for --op swap")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sinks", action="store_true",
                     help="gpt-oss variant: random per-head sink logits in the softmax")
@@ -498,6 +565,8 @@ def main(argv=None):
     try:
         if args.impl == "reference":
             run_reference(args, rank, world, dist)
+        elif args.op == "swap":
+            run_swap(args, rank, world, local, dist)
         else:
             run_ours(args, rank, world, local, dist)
     finally:

@@ -142,6 +142,31 @@ int xs_kv_append_paged(const void *k_new, const void *v_new, void *k_cache, void
                        int64_t num_blocks, int dtype, int *err_flag, cudaStream_t stream);
 
 /*
+ * xs_kv_swap - copy whole KV blocks from one pool to another, e.g. from the
+ * device pool to a swap pool in pinned host memory (swap-out) or back
+ * (swap-in): the pages' CPU swap of paged KV blocks ("xserv compare
+ * phase10...cf1e9e4", README, --swap-space-gb, KV swapped out to pinned CPU
+ * memory).
+ *
+ * For every i < n with s = block_mapping[2i] >= 0 and d = block_mapping[2i+1]
+ * >= 0, the block_bytes bytes of block s of src_k (and src_v) are copied to
+ * block d of dst_k (and dst_v); a block is [Hkv, block_size, D] of the pool
+ * layout, so block_bytes = Hkv * block_size * D * element size (a multiple of
+ * 16).  Any pool may live in device memory or in pinned host memory the GPU
+ * can address (GB300 reaches it over NVLink-C2C); block_mapping (int64
+ * [n, 2]) must be device-accessible too.  Destinations must be distinct.
+ * Ids at or past src_blocks / dst_blocks set XS_FLAG_BAD_BLOCK and are
+ * skipped; pairs with a negative id are skipped silently.  Bit-exact.
+ * Every pointer is checked first (cudaPointerGetAttributes): pinned host
+ * memory is used through its device alias, pageable host memory only where
+ * the device can access pageable memory; anything else returns
+ * XS_EUNSUPPORTED without launching.
+ */
+int xs_kv_swap(const void *src_k, const void *src_v, void *dst_k, void *dst_v,
+               const int64_t *block_mapping, int n, int64_t block_bytes, int64_t src_blocks,
+               int64_t dst_blocks, int *err_flag, cudaStream_t stream);
+
+/*
  * xs_paged_decode_partition_tokens - host-only heuristic for the split-K
  * partition size (tokens, a multiple of 16) of xs_paged_decode_attn.
  *

@@ -51,6 +51,7 @@ SIGNATURES = {
                                           _P]),
     "xs_paged_decode_sinks": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I,
                                    _I, _I, _L, _F, _I, _I, _I, _P, _P, _P]),
+    "xs_kv_swap": (_I, [_P, _P, _P, _P, _P, _I, _L, _L, _L, _P, _P]),
     "xs_version": (_I, []),
 }
 
@@ -241,6 +242,16 @@ def xs_paged_decode_reduce_sinks(out, part_o, part_m, part_l, context_lens, part
     _call("xs_paged_decode_reduce_sinks", _ptr(out), _ptr(part_o), _ptr(part_m), _ptr(part_l),
           _ptr(context_lens), _ptr(sinks), int(window), B, Hq, D, partition_tokens,
           max_partitions, dtype_code(out.dtype), _stream(stream))
+
+
+def xs_kv_swap(src_k, src_v, dst_k, dst_v, block_mapping, err_flag=None, stream=None):
+    """Copy whole blocks src[s] -> dst[d] for every (s, d) row of the int64
+    [n, 2] block_mapping (device or pinned host tensors; see xs_kv_swap)."""
+    n = block_mapping.shape[0] if block_mapping.dim() == 2 else block_mapping.numel() // 2
+    block_bytes = (src_k[0].numel() if src_k.shape[0] else dst_k[0].numel()) * src_k.element_size()
+    _call("xs_kv_swap", src_k.data_ptr(), src_v.data_ptr(), dst_k.data_ptr(), dst_v.data_ptr(),
+          _ptr(block_mapping), n, block_bytes, src_k.shape[0], dst_k.shape[0], _ptr(err_flag),
+          _stream(stream))
 
 
 def xs_version() -> int:
