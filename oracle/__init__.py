@@ -15,6 +15,8 @@ arguments.  Each function follows the definition cited in the C source:
   append already counts the token being written).
 * ``kv_append``     - byte copy of each new K/V row into its pool slot (same
   page, ``reshape_and_cache_bf16`` pool layout).
+* ``block_alloc_decode`` / ``block_free`` - the page allocator of a decode
+  step: a free stack of block ids, a new page whenever a token starts one.
 * ``kv_swap``       - whole-block copies between a device pool and a host
   swap pool (the README's CPU swap-out/in of KV blocks).
 * ``paged_decode_sinks`` - the gpt-oss variant: per-head sink logits in the
@@ -80,9 +82,12 @@ def _bind(lib):
     lib.oracle_paged_decode.argtypes = [P, P, P, P, I, P, I, I, I, I, I, L, D, I, P, I]
     lib.oracle_paged_decode_sinks.argtypes = [P, P, P, P, I, P, I, I, I, I, I, L, D, P, I, I, P, I]
     lib.oracle_kv_swap.argtypes = [P, P, P, P, P, I, L, L, L]
+    lib.oracle_block_alloc_decode.argtypes = [P, I, P, I, I, P, P, P]
+    lib.oracle_block_free.argtypes = [P, I, P, I, P, I, P, P, L]
     lib.oracle_max_threads.argtypes = []
     for f in (lib.oracle_slot_mapping, lib.oracle_kv_append, lib.oracle_paged_decode,
-              lib.oracle_paged_decode_sinks, lib.oracle_kv_swap, lib.oracle_max_threads):
+              lib.oracle_paged_decode_sinks, lib.oracle_kv_swap, lib.oracle_block_alloc_decode,
+              lib.oracle_block_free, lib.oracle_max_threads):
         f.restype = ctypes.c_int
     return lib
 
@@ -200,3 +205,34 @@ def kv_swap(src_k, src_v, dst_k, dst_v, mapping, lib=None):
                             mp.data_ptr(), mp.shape[0], block_bytes, sk.shape[0], dk.shape[0])
     _check(st, "kv_swap")
     return dk, dv
+
+
+def block_alloc_decode(block_tables, context_lens, block_size, free_stack, free_top, lib=None):
+    """One decode step's page allocation.  Returns new (block_tables,
+    context_lens, free_top, failed) - inputs are not modified."""
+    lib = lib or load()
+    bt = _cpu(block_tables, torch.int32).clone()
+    cl = _cpu(context_lens, torch.int32).clone()
+    fs = _cpu(free_stack, torch.int32)
+    top = torch.tensor([int(free_top)], dtype=torch.int32)
+    failed = torch.zeros(cl.numel(), dtype=torch.int32)
+    st = lib.oracle_block_alloc_decode(bt.data_ptr(), bt.shape[1], cl.data_ptr(), cl.numel(),
+                                       block_size, fs.data_ptr(), top.data_ptr(), failed.data_ptr())
+    _check(st, "block_alloc_decode")
+    return bt, cl, int(top.item()), failed
+
+
+def block_free(seq_ids, block_tables, context_lens, block_size, free_stack, free_top, lib=None):
+    """Release sequences.  Returns new (block_tables, context_lens,
+    free_stack, free_top)."""
+    lib = lib or load()
+    ids = _cpu(seq_ids, torch.int32)
+    bt = _cpu(block_tables, torch.int32).clone()
+    cl = _cpu(context_lens, torch.int32).clone()
+    fs = _cpu(free_stack, torch.int32).clone()
+    top = torch.tensor([int(free_top)], dtype=torch.int32)
+    st = lib.oracle_block_free(ids.data_ptr(), ids.numel(), bt.data_ptr(), bt.shape[1],
+                               cl.data_ptr(), block_size, fs.data_ptr(), top.data_ptr(),
+                               fs.numel())
+    _check(st, "block_free")
+    return bt, cl, fs, int(top.item())

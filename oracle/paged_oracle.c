@@ -300,6 +300,73 @@ int oracle_kv_swap(const void *src_k, const void *src_v, void *dst_k, void *dst_
     return ORACLE_OK;
 }
 
+/*
+ * Block allocation for one decode step (the pages' PagedKVCache hands each
+ * sequence a new physical block when its next token starts a page:
+ * "xserv compare phase10...cf1e9e4", bench-qwen3.rs / gpt-oss drivers,
+ * PagedKVCache::new_tp(.., total_blocks, .., max_blocks_per_seq, ..),
+ * register_sequence, free_sequence, seq_len; the struct's body is not on the
+ * pages).  Reading: a free list is a stack of block ids free_stack[0, top).
+ * For every active sequence b (context_lens[b] >= 0; -1 = no sequence):
+ * the new token's position is p = context_lens[b]; if p % bs == 0 it starts
+ * page p / bs, which takes the block on top of the stack.  Then
+ * context_lens[b] = p + 1.  A sequence whose page would lie past the table
+ * (failed[b] = 2) or that finds the stack empty (failed[b] = 1) is left
+ * unchanged.  Sequences are served in index order; the device kernel may
+ * hand the popped blocks out in another order.
+ */
+int oracle_block_alloc_decode(int32_t *block_tables, int max_blocks_per_seq, int32_t *context_lens,
+                              int B, int block_size, const int32_t *free_stack, int32_t *free_top,
+                              int32_t *failed) {
+    if (B < 0 || block_size <= 0 || max_blocks_per_seq < 0 || *free_top < 0) return ORACLE_EINVAL;
+    for (int b = 0; b < B; ++b) {
+        failed[b] = 0;
+        int32_t p = context_lens[b];
+        if (p < 0) continue;
+        int32_t page = p / block_size;
+        if (page >= max_blocks_per_seq) {
+            failed[b] = 2;
+            continue;
+        }
+        if (p % block_size == 0) {
+            if (*free_top == 0) {
+                failed[b] = 1;
+                continue;
+            }
+            *free_top -= 1;
+            block_tables[(int64_t)b * max_blocks_per_seq + page] = free_stack[*free_top];
+        }
+        context_lens[b] = p + 1;
+    }
+    return ORACLE_OK;
+}
+
+/*
+ * Release sequences (PagedKVCache::free_sequence): every block of the listed
+ * sequences, pages 0 .. ceil(len / bs) - 1 in order, is pushed on the free
+ * stack; their table rows become -1 and their lengths -1 (no sequence).
+ */
+int oracle_block_free(const int32_t *seq_ids, int n, int32_t *block_tables, int max_blocks_per_seq,
+                      int32_t *context_lens, int block_size, int32_t *free_stack,
+                      int32_t *free_top, int64_t stack_capacity) {
+    if (n < 0 || block_size <= 0) return ORACLE_EINVAL;
+    for (int i = 0; i < n; ++i) {
+        int32_t b = seq_ids[i];
+        int32_t len = context_lens[b];
+        int32_t pages = len > 0 ? (len + block_size - 1) / block_size : 0;
+        if (pages > max_blocks_per_seq) return ORACLE_ETABLE;
+        for (int32_t pg = 0; pg < pages; ++pg) {
+            if (*free_top >= stack_capacity) return ORACLE_EINVAL;
+            free_stack[*free_top] = block_tables[(int64_t)b * max_blocks_per_seq + pg];
+            *free_top += 1;
+        }
+        for (int32_t pg = 0; pg < max_blocks_per_seq; ++pg)
+            block_tables[(int64_t)b * max_blocks_per_seq + pg] = -1;
+        context_lens[b] = -1;
+    }
+    return ORACLE_OK;
+}
+
 /* Number of threads an OpenMP parallel region would use (1 without OpenMP). */
 int oracle_max_threads(void) {
 #ifdef _OPENMP

@@ -409,10 +409,59 @@ def pin_swap_by_indexing(lib):
         raise AssertionError("out-of-range source block accepted")
 
 
+# ---------------------------------------------------------------- allocator
+
+def pin_alloc_by_hand(lib):
+    c = gc.load_cases()["alloc_by_hand"]
+    bt, cl, top, failed = oracle.block_alloc_decode(
+        torch.tensor(c["block_tables"]), torch.tensor(c["context_lens"]), c["block_size"],
+        torch.tensor(c["free_stack"]), c["free_top"], lib=lib)
+    assert bt.tolist() == c["expected_tables"], bt.tolist()
+    assert cl.tolist() == c["expected_lens"] and top == c["expected_top"]
+    assert failed.tolist() == c["expected_failed"]
+
+
+def pin_alloc_free_conserve_blocks(lib):
+    """Blocks are neither lost nor duplicated: over many steps and releases,
+    the blocks in use plus the free stack are always a permutation of the
+    pool, and every sequence's table covers exactly its length."""
+    g = torch.Generator().manual_seed(61)
+    nb, B, bs, width = 40, 6, 4, 12
+    stack = torch.randperm(nb, generator=g).to(torch.int32)
+    top = nb
+    bt = torch.full((B, width), -1, dtype=torch.int32)
+    cl = torch.tensor([0, 3, -1, 7, 0, 1], dtype=torch.int32)
+    # Give the non-empty sequences their pages by allocating token by token.
+    lens0 = cl.clone()
+    cl = torch.where(cl >= 0, torch.zeros_like(cl), cl)
+    for step in range(int(lens0.max())):
+        live = cl < lens0
+        bt2, cl2, top, _ = oracle.block_alloc_decode(bt, torch.where(live, cl, -1), bs, stack, top,
+                                                     lib=lib)
+        bt, cl = bt2, torch.where(live, cl2, cl)
+    for step in range(30):
+        bt, cl, top, failed = oracle.block_alloc_decode(bt, cl, bs, stack, top, lib=lib)
+        if step % 7 == 6:
+            victim = int(torch.randint(0, B, (1,), generator=g))
+            if cl[victim] >= 0:
+                bt, cl, stack, top = oracle.block_free([victim], bt, cl, bs, stack, top, lib=lib)
+                cl[victim] = 0          # register a new sequence in the freed slot
+        used = [int(bt[b, p]) for b in range(B) if cl[b] > 0
+                for p in range((int(cl[b]) + bs - 1) // bs)]
+        pool = sorted(used + stack[:top].tolist())
+        assert pool == list(range(nb)), f"step {step}: blocks lost or duplicated"
+        for b in range(B):
+            n = int(cl[b])
+            if n >= 0:
+                pages = (n + bs - 1) // bs
+                assert (bt[b, :pages] >= 0).all() and (bt[b, pages:] == -1).all()
+
+
 ALL_PINS = [
     pin_slots_by_hand, pin_gqa_paged_by_hand, pin_single_token, pin_dense_equivalence,
     pin_brute_force_python, pin_permutation_invariance, pin_constant_v, pin_zero_query_mean,
     pin_dominant_key, pin_linearity_in_v, pin_bf16_widening, pin_append_bytes,
     pin_cache_equals_recompute, pin_sink_window_by_hand, pin_sinks_window_dense,
-    pin_sinks_window_reduce_to_plain, pin_swap_by_indexing,
+    pin_sinks_window_reduce_to_plain, pin_swap_by_indexing, pin_alloc_by_hand,
+    pin_alloc_free_conserve_blocks,
 ]

@@ -37,6 +37,13 @@ MUTANTS = [
     # (every mutant must keep its accesses in bounds: it runs inside the test process)
     ("swap_dst_stride", "memcpy((char *)dst_k + d * block_bytes, (const char *)src_k + s * block_bytes,",
      "memcpy((char *)dst_k + d * (block_bytes / 2), (const char *)src_k + s * block_bytes,"),
+    ("alloc_every_token", "if (p % block_size == 0) {\n            if (*free_top == 0) {",
+     "if (p % block_size >= 0) {\n            if (*free_top == 0) {"),
+    ("alloc_wrong_page", "block_tables[(int64_t)b * max_blocks_per_seq + page] = free_stack[*free_top];",
+     "block_tables[(int64_t)b * max_blocks_per_seq + (page > 0 ? page - 1 : 0)] = free_stack[*free_top];"),
+    ("alloc_length_not_advanced", "context_lens[b] = p + 1;", "context_lens[b] = p;"),
+    ("free_keeps_last_page", "for (int32_t pg = 0; pg < pages; ++pg) {\n            if (*free_top",
+     "for (int32_t pg = 0; pg + 1 < pages; ++pg) {\n            if (*free_top"),
     ("sink_dropped", "double den = sinks ? exp(sink - top) : 0.0;", "double den = 0.0;"),
     ("sink_scaled", "sink = widen(sinks, h, dtype);", "sink = scale * widen(sinks, h, dtype);"),
     ("window_one_short", "(window > 0 && n > window) ? n - window : 0;",
