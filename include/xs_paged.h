@@ -88,6 +88,9 @@ extern "C" {
                                kernel drained its copies and returned        */
 #define XS_FLAG_CONFIG 16   /* internal: a launch got less shared memory than
                                its batch needs; the kernel did nothing       */
+#define XS_FLAG_POOL_EMPTY 32 /* the free-block stack was empty (allocation)
+                                 or full (release); that sequence was left
+                                 as it was                                    */
 
 /*
  * xs_slot_mapping - where each sequence's new token goes (one decode step).
@@ -140,6 +143,39 @@ int xs_kv_append_paged(const void *k_new, const void *v_new, void *k_cache, void
                        const int32_t *block_tables, int max_blocks_per_seq,
                        const int32_t *context_lens, int B, int Hkv, int D, int block_size,
                        int64_t num_blocks, int dtype, int *err_flag, cudaStream_t stream);
+
+/*
+ * xs_block_alloc_decode - the page allocation of one decode step, on the
+ * device (the pages' PagedKVCache gives a sequence a new physical block when
+ * its next token starts a page; "xserv compare phase10...cf1e9e4", the
+ * bench-qwen3 and gpt-oss drivers: PagedKVCache::new_tp(.., total_blocks,
+ * .., max_blocks_per_seq, ..), register_sequence, free_sequence, seq_len).
+ *
+ * free_stack int32 [capacity] holds free block ids in [0, *free_top);
+ * free_top is one int32 on the device.  For every b with context_lens[b] >=
+ * 0 (a slot with -1 holds no sequence): the token this step writes sits at
+ * p = context_lens[b]; if p % block_size == 0 it starts page p / block_size,
+ * which gets the block popped from the stack; then context_lens[b] = p + 1,
+ * so the lengths mean what xs_kv_append_paged and xs_paged_decode_attn
+ * expect.  A page past the table sets XS_FLAG_BAD_LEN, an empty stack
+ * XS_FLAG_POOL_EMPTY; that sequence is left unchanged.  Which sequence gets
+ * which popped block depends on the order of atomic operations.
+ * Everything is device state, so the call can sit in a captured step.
+ */
+int xs_block_alloc_decode(int32_t *block_tables, int max_blocks_per_seq, int32_t *context_lens,
+                          int B, int block_size, const int32_t *free_stack, int32_t *free_top,
+                          int *err_flag, cudaStream_t stream);
+
+/*
+ * xs_block_free - release sequences (PagedKVCache::free_sequence): all blocks
+ * of each listed slot (seq_ids int32 [n], distinct, on the device) are pushed
+ * on the free stack, the slot's table row is set to -1 and its length to -1
+ * (no sequence; write 0 to register a new, empty one).  A full stack sets
+ * XS_FLAG_POOL_EMPTY; an id outside [0, B) sets XS_FLAG_BAD_SLOT.
+ */
+int xs_block_free(const int32_t *seq_ids, int n, int32_t *block_tables, int max_blocks_per_seq,
+                  int32_t *context_lens, int B, int block_size, int32_t *free_stack,
+                  int32_t *free_top, int64_t stack_capacity, int *err_flag, cudaStream_t stream);
 
 /*
  * xs_kv_swap - copy whole KV blocks from one pool to another, e.g. from the

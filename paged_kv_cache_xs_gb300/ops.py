@@ -27,6 +27,7 @@ STATUS = {
 }
 NOALLOC_SCRATCH_BYTES = 64 << 20
 FLAG_BAD_BLOCK, FLAG_BAD_LEN, FLAG_BAD_SLOT, FLAG_TIMEOUT, FLAG_CONFIG = 1, 2, 4, 8, 16
+FLAG_POOL_EMPTY = 32
 
 # name -> (restype, argtypes)
 _P, _I, _L, _F, _S = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float,
@@ -52,6 +53,8 @@ SIGNATURES = {
     "xs_paged_decode_sinks": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I,
                                    _I, _I, _L, _F, _I, _I, _I, _P, _P, _P]),
     "xs_kv_swap": (_I, [_P, _P, _P, _P, _P, _I, _L, _L, _L, _P, _P]),
+    "xs_block_alloc_decode": (_I, [_P, _I, _P, _I, _I, _P, _P, _P, _P]),
+    "xs_block_free": (_I, [_P, _I, _P, _I, _P, _I, _I, _P, _P, _L, _P, _P]),
     "xs_version": (_I, []),
 }
 
@@ -252,6 +255,24 @@ def xs_kv_swap(src_k, src_v, dst_k, dst_v, block_mapping, err_flag=None, stream=
     _call("xs_kv_swap", src_k.data_ptr(), src_v.data_ptr(), dst_k.data_ptr(), dst_v.data_ptr(),
           _ptr(block_mapping), n, block_bytes, src_k.shape[0], dst_k.shape[0], _ptr(err_flag),
           _stream(stream))
+
+
+def xs_block_alloc_decode(block_tables, context_lens, free_stack, free_top, block_size=BLOCK_SIZE,
+                          err_flag=None, stream=None):
+    """Advance every live sequence by one token, popping a block from the
+    device free stack for each token that starts a page."""
+    _call("xs_block_alloc_decode", _ptr(block_tables), block_tables.shape[1], _ptr(context_lens),
+          context_lens.numel(), block_size, _ptr(free_stack), _ptr(free_top), _ptr(err_flag),
+          _stream(stream))
+
+
+def xs_block_free(seq_ids, block_tables, context_lens, free_stack, free_top,
+                  block_size=BLOCK_SIZE, err_flag=None, stream=None):
+    """Release the slots in seq_ids (device int32): their blocks go back on
+    the free stack, their rows and lengths become -1."""
+    _call("xs_block_free", _ptr(seq_ids), seq_ids.numel(), _ptr(block_tables),
+          block_tables.shape[1], _ptr(context_lens), context_lens.numel(), block_size,
+          _ptr(free_stack), _ptr(free_top), free_stack.numel(), _ptr(err_flag), _stream(stream))
 
 
 def xs_version() -> int:
