@@ -15,6 +15,9 @@ arguments.  Each function follows the definition cited in the C source:
   append already counts the token being written).
 * ``kv_append``     - byte copy of each new K/V row into its pool slot (same
   page, ``reshape_and_cache_bf16`` pool layout).
+* ``prefill_append`` / ``paged_prefill`` - the prefill side: a chunk of T
+  tokens written at start_pos (reshape_and_cache_bf16) and its causal
+  attention over the paged cache (attention with an offset causal mask).
 * ``block_alloc_decode`` / ``block_free`` - the page allocator of a decode
   step: a free stack of block ids, a new page whenever a token starts one.
 * ``kv_swap``       - whole-block copies between a device pool and a host
@@ -84,10 +87,13 @@ def _bind(lib):
     lib.oracle_kv_swap.argtypes = [P, P, P, P, P, I, L, L, L]
     lib.oracle_block_alloc_decode.argtypes = [P, I, P, I, I, P, P, P]
     lib.oracle_block_free.argtypes = [P, I, P, I, P, I, P, P, L]
+    lib.oracle_prefill_append.argtypes = [P, P, P, P, P, I, I, I, I, I, L, I, I]
+    lib.oracle_paged_prefill.argtypes = [P, P, P, P, I, I, I, I, I, I, I, L, D, I, P, I]
     lib.oracle_max_threads.argtypes = []
     for f in (lib.oracle_slot_mapping, lib.oracle_kv_append, lib.oracle_paged_decode,
               lib.oracle_paged_decode_sinks, lib.oracle_kv_swap, lib.oracle_block_alloc_decode,
-              lib.oracle_block_free, lib.oracle_max_threads):
+              lib.oracle_block_free, lib.oracle_prefill_append, lib.oracle_paged_prefill,
+              lib.oracle_max_threads):
         f.restype = ctypes.c_int
     return lib
 
@@ -236,3 +242,37 @@ def block_free(seq_ids, block_tables, context_lens, block_size, free_stack, free
                                fs.numel())
     _check(st, "block_free")
     return bt, cl, fs, int(top.item())
+
+
+def prefill_append(k_src, v_src, k_cache, v_cache, block_ids, start_pos: int, lib=None):
+    """Copies of (k_cache, v_cache) with the chunk k_src/v_src ([Hkv, T, D])
+    written at positions start_pos .. start_pos + T - 1 of one sequence."""
+    lib = lib or load()
+    ks, vs = _cpu(k_src), _cpu(v_src)
+    kc, vc = _cpu(k_cache).clone(), _cpu(v_cache).clone()
+    ids = _cpu(block_ids, torch.int32).reshape(-1)
+    Hkv, T, D = ks.shape
+    num_blocks, _, bs, _ = kc.shape
+    st = lib.oracle_prefill_append(ks.data_ptr(), vs.data_ptr(), kc.data_ptr(), vc.data_ptr(),
+                                   ids.data_ptr(), ids.numel(), T, Hkv, D, bs, num_blocks,
+                                   int(start_pos), _code(ks.dtype))
+    _check(st, "prefill_append")
+    return kc, vc
+
+
+def paged_prefill(q, k_cache, v_cache, block_ids, start_pos: int, scale: float,
+                  nthreads: int | None = None, lib=None) -> torch.Tensor:
+    """fp64 [T, Hq, D]: causal attention of a T-token chunk (q [T, Hq, D],
+    positions start_pos ..) over one sequence's paged cache."""
+    lib = lib or load()
+    qq, kc, vc = _cpu(q), _cpu(k_cache), _cpu(v_cache)
+    ids = _cpu(block_ids, torch.int32).reshape(-1)
+    T, Hq, D = qq.shape
+    num_blocks, Hkv, bs, _ = kc.shape
+    out = torch.empty(T, Hq, D, dtype=torch.float64)
+    st = lib.oracle_paged_prefill(qq.data_ptr(), kc.data_ptr(), vc.data_ptr(), ids.data_ptr(),
+                                  ids.numel(), T, int(start_pos), Hq, Hkv, D, bs, num_blocks,
+                                  float(scale), _code(qq.dtype), out.data_ptr(),
+                                  nthreads or default_threads())
+    _check(st, "paged_prefill")
+    return out

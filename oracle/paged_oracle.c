@@ -367,6 +367,97 @@ int oracle_block_free(const int32_t *seq_ids, int n, int32_t *block_tables, int 
     return ORACLE_OK;
 }
 
+/*
+ * Prefill append for one sequence ("xserv compare phase10...cf1e9e4",
+ * attention.rs, reshape_and_cache_bf16: k_src/v_src are [num_kv_heads,
+ * num_tokens, head_dim]; token i goes to position start_pos + i of the
+ * sequence whose block list is block_ids, which must hold at least
+ * ceil((start_pos + num_tokens) / block_size) ids):
+ *     pool[block_ids[(start + i) / bs], h, (start + i) % bs, :] = src[h, i, :]
+ */
+int oracle_prefill_append(const void *k_src, const void *v_src, void *k_cache, void *v_cache,
+                          const int32_t *block_ids, int n_ids, int T, int Hkv, int D,
+                          int block_size, int64_t num_blocks, int start_pos, int dtype) {
+    int eb = elem_bytes(dtype);
+    if (!eb || T < 0 || Hkv <= 0 || D <= 0 || block_size <= 0 || start_pos < 0)
+        return ORACLE_EINVAL;
+    size_t row = (size_t)D * eb;
+    for (int i = 0; i < T; ++i) {
+        int64_t pos = (int64_t)start_pos + i;
+        if (pos / block_size >= n_ids) return ORACLE_ETABLE;
+        int64_t blk = block_ids[pos / block_size];
+        if (blk < 0 || blk >= num_blocks) return ORACLE_EBLOCK;
+        for (int h = 0; h < Hkv; ++h) {
+            size_t dst = (size_t)(((blk * Hkv + h) * block_size + pos % block_size) * D) * eb;
+            size_t src = (size_t)(((int64_t)h * T + i) * D) * eb;
+            memcpy((char *)k_cache + dst, (const char *)k_src + src, row);
+            memcpy((char *)v_cache + dst, (const char *)v_src + src, row);
+        }
+    }
+    return ORACLE_OK;
+}
+
+/*
+ * Chunked prefill attention over the paged cache for one sequence: query
+ * token i (q[i, h, :], q is [T, Hq, D]) sits at position start_pos + i and
+ * attends causally to every cached token t <= start_pos + i, keys and values
+ * gathered through block_ids, query head h reading KV head h / (Hq / Hkv)
+ * (the naive attention with a causal mask offset by the cached prefix:
+ * "xserv compare phase10...cf1e9e4", attention.rs, attention /
+ * apply_causal_mask(offset); flash_attention for q_len > 1).
+ *     out[i, h, :] = sum_{t <= start+i} softmax_t(scale q[i,h,:].K_t) V_t
+ */
+int oracle_paged_prefill(const void *q, const void *k_cache, const void *v_cache,
+                         const int32_t *block_ids, int n_ids, int T, int start_pos, int Hq,
+                         int Hkv, int D, int block_size, int64_t num_blocks, double scale,
+                         int dtype, double *out, int nthreads) {
+    if (!elem_bytes(dtype) || T < 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || block_size <= 0 ||
+        start_pos < 0 || Hq % Hkv != 0)
+        return ORACLE_EINVAL;
+    const int group = Hq / Hkv;
+    const int64_t total = (int64_t)start_pos + T;
+    const int64_t pages = (total + block_size - 1) / block_size;
+    if (pages > n_ids) return ORACLE_ETABLE;
+    for (int64_t i = 0; i < pages; ++i)
+        if (block_ids[i] < 0 || block_ids[i] >= num_blocks) return ORACLE_EBLOCK;
+    int status = ORACLE_OK;
+    if (nthreads <= 0) nthreads = 1;
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)
+    for (int64_t ih = 0; ih < (int64_t)T * Hq; ++ih) {
+        int i = (int)(ih / Hq), h = (int)(ih % Hq);
+        int kvh = h / group;
+        int64_t last = (int64_t)start_pos + i;  /* attends to tokens 0..last */
+        double *o = out + ih * D;
+        for (int d = 0; d < D; ++d) o[d] = 0.0;
+        double *sc = (double *)malloc(sizeof(double) * (size_t)(last + 1));
+        if (!sc) {
+#pragma omp atomic write
+            status = ORACLE_ENOMEM;
+            continue;
+        }
+        for (int64_t t = 0; t <= last; ++t) {
+            int64_t blk = block_ids[t / block_size];
+            int64_t kr = ((blk * Hkv + kvh) * block_size + t % block_size) * D;
+            double acc = 0.0;
+            for (int d = 0; d < D; ++d) acc += widen(q, ih * D + d, dtype) * widen(k_cache, kr + d, dtype);
+            sc[t] = scale * acc;
+        }
+        double mval = sc[0];
+        for (int64_t t = 1; t <= last; ++t) mval = sc[t] > mval ? sc[t] : mval;
+        double z = 0.0;
+        for (int64_t t = 0; t <= last; ++t) {
+            double e = exp(sc[t] - mval);
+            z += e;
+            int64_t blk = block_ids[t / block_size];
+            int64_t vr = ((blk * Hkv + kvh) * block_size + t % block_size) * D;
+            for (int d = 0; d < D; ++d) o[d] += e * widen(v_cache, vr + d, dtype);
+        }
+        for (int d = 0; d < D; ++d) o[d] /= z;
+        free(sc);
+    }
+    return status;
+}
+
 /* Number of threads an OpenMP parallel region would use (1 without OpenMP). */
 int oracle_max_threads(void) {
 #ifdef _OPENMP

@@ -457,11 +457,94 @@ def pin_alloc_free_conserve_blocks(lib):
                 assert (bt[b, :pages] >= 0).all() and (bt[b, pages:] == -1).all()
 
 
+# ------------------------------------------------------------------ prefill
+
+def pin_prefill_by_hand(lib):
+    c = gc.load_cases()["prefill_by_hand"]
+    kc, vc = gc.pool_tensor(c, "k_cache"), gc.pool_tensor(c, "v_cache")
+    ids = torch.tensor(c["block_ids"], dtype=torch.int32)
+    ks = torch.tensor(c["k_src"], dtype=torch.float32)
+    vs = torch.tensor(c["v_src"], dtype=torch.float32)
+    kc2, vc2 = oracle.prefill_append(ks, vs, kc, vc, ids, c["start_pos"], lib=lib)
+    out = oracle.paged_prefill(torch.tensor(c["q"], dtype=torch.float32), kc2, vc2, ids,
+                               c["start_pos"], gc.scale_of(c), lib=lib)
+    _close(out, gc.expected_of(c), 1e-14, "prefill_by_hand")
+
+
+def _prefill_case(seed, dtype, G, start, T, bs=16, Hkv=2, D=16):
+    g = torch.Generator().manual_seed(seed)
+    Hq = Hkv * G
+    total = start + T
+    pages = (total + bs - 1) // bs
+    nb = pages + 3
+    ids = torch.randperm(nb, generator=g)[:pages].to(torch.int32)
+    kc = torch.randn(nb, Hkv, bs, D, generator=g).to(dtype)
+    vc = torch.randn(nb, Hkv, bs, D, generator=g).to(dtype)
+    ks = torch.randn(Hkv, T, D, generator=g).to(dtype)
+    vs = torch.randn(Hkv, T, D, generator=g).to(dtype)
+    q = torch.randn(T, Hq, D, generator=g).to(dtype)
+    return q, kc, vc, ks, vs, ids
+
+
+def pin_prefill_dense_and_decode_rows(lib):
+    for seed, dtype, G, start, T in ((1, torch.float32, 1, 0, 37), (2, torch.bfloat16, 4, 21, 50),
+                                     (3, torch.float32, 2, 48, 16)):
+        q, kc, vc, ks, vs, ids = _prefill_case(seed, dtype, G, start, T)
+        kc2, vc2 = oracle.prefill_append(ks, vs, kc, vc, ids, start, lib=lib)
+        scale = 0.25
+        out = oracle.paged_prefill(q, kc2, vc2, ids, start, scale, lib=lib)
+        # Dense: contiguous copy of tokens 0 .. start+T-1, offset causal mask.
+        _, Hkv, bs, D = kc.shape
+        Hq = q.shape[1]
+        total = start + T
+        K = kc2[ids.long()].double().permute(0, 2, 1, 3).reshape(-1, Hkv, D)[:total]
+        V = vc2[ids.long()].double().permute(0, 2, 1, 3).reshape(-1, Hkv, D)[:total]
+        K = K.transpose(0, 1).repeat_interleave(Hq // Hkv, 0)           # [Hq, total, D]
+        V = V.transpose(0, 1).repeat_interleave(Hq // Hkv, 0)
+        s_ = torch.matmul(q.double().transpose(0, 1), K.transpose(1, 2)) * scale   # [Hq, T, total]
+        mask = torch.arange(total)[None, :] > (start + torch.arange(T))[:, None]
+        s_ = s_.masked_fill(mask, float("-inf"))
+        dense = torch.matmul(torch.softmax(s_, -1), V).transpose(0, 1)           # [T, Hq, D]
+        _close(out, dense, TOL, f"prefill dense seed {seed}")
+        # Row i is the decode step of the token at position start + i.
+        for i in (0, T // 2, T - 1):
+            bt = ids.unsqueeze(0)
+            dec = oracle.paged_decode(q[i:i + 1], kc2, vc2, bt,
+                                      torch.tensor([start + i + 1], dtype=torch.int32), scale,
+                                      lib=lib)
+            assert torch.equal(dec[0], out[i]), f"prefill row {i} differs from decode"
+
+
+def pin_prefill_chunking_and_append(lib):
+    q, kc, vc, ks, vs, ids = _prefill_case(9, torch.bfloat16, 4, 5, 40)
+    start, T, T1 = 5, 40, 17
+    whole_k, whole_v = oracle.prefill_append(ks, vs, kc, vc, ids, start, lib=lib)
+    a_k, a_v = oracle.prefill_append(ks[:, :T1].contiguous(), vs[:, :T1].contiguous(), kc, vc, ids,
+                                     start, lib=lib)
+    b_k, b_v = oracle.prefill_append(ks[:, T1:].contiguous(), vs[:, T1:].contiguous(), a_k, a_v,
+                                     ids, start + T1, lib=lib)
+    iv = lambda t: t.view(torch.int16)
+    assert torch.equal(iv(whole_k), iv(b_k)) and torch.equal(iv(whole_v), iv(b_v))
+    # The append against tensor indexing.
+    ek, ev = kc.clone(), vc.clone()
+    for i in range(T):
+        pos = start + i
+        ek[ids[pos // 16], :, pos % 16] = ks[:, i]
+        ev[ids[pos // 16], :, pos % 16] = vs[:, i]
+    assert torch.equal(iv(whole_k), iv(ek)) and torch.equal(iv(whole_v), iv(ev))
+    # Chunked attention equals one-shot attention row for row.
+    one = oracle.paged_prefill(q, whole_k, whole_v, ids, start, 0.3, lib=lib)
+    first = oracle.paged_prefill(q[:T1].contiguous(), a_k, a_v, ids, start, 0.3, lib=lib)
+    second = oracle.paged_prefill(q[T1:].contiguous(), b_k, b_v, ids, start + T1, 0.3, lib=lib)
+    assert torch.equal(one, torch.cat([first, second]))
+
+
 ALL_PINS = [
     pin_slots_by_hand, pin_gqa_paged_by_hand, pin_single_token, pin_dense_equivalence,
     pin_brute_force_python, pin_permutation_invariance, pin_constant_v, pin_zero_query_mean,
     pin_dominant_key, pin_linearity_in_v, pin_bf16_widening, pin_append_bytes,
     pin_cache_equals_recompute, pin_sink_window_by_hand, pin_sinks_window_dense,
     pin_sinks_window_reduce_to_plain, pin_swap_by_indexing, pin_alloc_by_hand,
-    pin_alloc_free_conserve_blocks,
+    pin_alloc_free_conserve_blocks, pin_prefill_by_hand, pin_prefill_dense_and_decode_rows,
+    pin_prefill_chunking_and_append,
 ]

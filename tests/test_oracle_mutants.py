@@ -44,6 +44,11 @@ MUTANTS = [
     ("alloc_length_not_advanced", "context_lens[b] = p + 1;", "context_lens[b] = p;"),
     ("free_keeps_last_page", "for (int32_t pg = 0; pg < pages; ++pg) {\n            if (*free_top",
      "for (int32_t pg = 0; pg + 1 < pages; ++pg) {\n            if (*free_top"),
+    ("prefill_causal_open", "for (int64_t t = 0; t <= last; ++t) {\n            int64_t blk = block_ids[t / block_size];\n            int64_t kr",
+     "for (int64_t t = 0; t < last; ++t) {\n            int64_t blk = block_ids[t / block_size];\n            int64_t kr"),
+    ("prefill_no_offset", "int64_t last = (int64_t)start_pos + i;", "int64_t last = i;"),
+    ("prefill_src_token_major", "size_t src = (size_t)(((int64_t)h * T + i) * D) * eb;",
+     "size_t src = (size_t)(((int64_t)i * Hkv + h) * D) * eb;"),
     ("sink_dropped", "double den = sinks ? exp(sink - top) : 0.0;", "double den = 0.0;"),
     ("sink_scaled", "sink = widen(sinks, h, dtype);", "sink = scale * widen(sinks, h, dtype);"),
     ("window_one_short", "(window > 0 && n > window) ? n - window : 0;",
