@@ -145,6 +145,49 @@ int xs_kv_append_paged(const void *k_new, const void *v_new, void *k_cache, void
                        int64_t num_blocks, int dtype, int *err_flag, cudaStream_t stream);
 
 /*
+ * xs_prefill_append - write a prefill chunk into one sequence's pages (the
+ * pages' reshape_and_cache_bf16, "xserv compare phase10...cf1e9e4",
+ * attention.rs): k_src, v_src are [Hkv, T, D] (the pages' layout); row i
+ * goes to position start_pos + i, i.e. block block_ids[(start_pos + i) / bs],
+ * offset (start_pos + i) % bs.  block_ids (int32 [n_ids], device) is the
+ * sequence's block list.  Positions past n_ids*bs set XS_FLAG_BAD_LEN, ids
+ * outside [0, num_blocks) XS_FLAG_BAD_BLOCK; both are skipped.  Bit-exact.
+ */
+int xs_prefill_append(const void *k_src, const void *v_src, void *k_cache, void *v_cache,
+                      const int32_t *block_ids, int n_ids, int T, int Hkv, int D, int block_size,
+                      int64_t num_blocks, int start_pos, int dtype, int *err_flag,
+                      cudaStream_t stream);
+
+/*
+ * xs_paged_prefill_attn / xs_paged_prefill_reduce / xs_paged_prefill -
+ * causal attention of a T-token prefill chunk over one sequence's paged
+ * cache (the chunk already appended): query token i (q [T, Hq, D], out
+ * [T, Hq, D]) sits at position start_pos + i and attends to every cached
+ * token t <= start_pos + i through block_ids (the pages' attention with a
+ * causal mask offset by the cached prefix, "xserv compare phase10...cf1e9e4",
+ * attention.rs, attention / apply_causal_mask / flash_attention).
+ * start_pos + T must not exceed n_ids * block_size (XS_ESHAPE).  Split-K and
+ * workspace as xs_paged_decode_attn with B = T and max_blocks_per_seq =
+ * n_ids: partials [T, Hq, max_partitions, D].  Row i equals the decode
+ * attention of the token at position start_pos + i.
+ */
+int xs_paged_prefill_attn(void *out, float *part_o, float *part_m, float *part_l, const void *q,
+                          const void *k_cache, const void *v_cache, const int32_t *block_ids,
+                          int n_ids, int T, int start_pos, int Hq, int Hkv, int D,
+                          int block_size, int64_t num_blocks, float scale, int partition_tokens,
+                          int max_partitions, int dtype, int *err_flag, int *work_counters,
+                          cudaStream_t stream);
+int xs_paged_prefill_reduce(void *out, const float *part_o, const float *part_m,
+                            const float *part_l, int T, int start_pos, int Hq, int D,
+                            int partition_tokens, int max_partitions, int dtype,
+                            cudaStream_t stream);
+int xs_paged_prefill(void *out, float *part_o, float *part_m, float *part_l, const void *q,
+                     const void *k_cache, const void *v_cache, const int32_t *block_ids,
+                     int n_ids, int T, int start_pos, int Hq, int Hkv, int D, int block_size,
+                     int64_t num_blocks, float scale, int partition_tokens, int max_partitions,
+                     int dtype, int *err_flag, int *work_counters, cudaStream_t stream);
+
+/*
  * xs_block_alloc_decode - the page allocation of one decode step, on the
  * device (the pages' PagedKVCache gives a sequence a new physical block when
  * its next token starts a page; "xserv compare phase10...cf1e9e4", the

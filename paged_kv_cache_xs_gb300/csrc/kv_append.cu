@@ -86,6 +86,44 @@ __global__ void __launch_bounds__(kAppendThreads)
     }
 }
 
+// Prefill append: chunk rows src[h, i, :] ([Hkv, T, D], the pages' layout)
+// to position start + i of one sequence.  One thread per 16-byte chunk.
+__global__ void __launch_bounds__(kAppendThreads)
+    prefill_append_kernel(const uint4 *__restrict__ k_src, const uint4 *__restrict__ v_src,
+                          uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
+                          const int32_t *__restrict__ block_ids, int n_ids, int T, int Hkv,
+                          int chunks_per_row, int bs, int64_t num_blocks, int start,
+                          int *err_flag) {
+    const int64_t per_token = static_cast<int64_t>(Hkv) * chunks_per_row;
+    const int64_t total = static_cast<int64_t>(T) * 2 * per_token;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t t = i / (2 * per_token);
+        const int64_t r = i - t * 2 * per_token;
+        const bool is_v = r >= per_token;
+        const int64_t hc = is_v ? r - per_token : r;
+        const int64_t h = hc / chunks_per_row, c = hc - h * chunks_per_row;
+        const int64_t pos = start + t;
+        const int64_t page = pos / bs;
+        if (page >= n_ids) {
+            if (r == 0) raise_flag(err_flag, XS_FLAG_BAD_LEN);
+            continue;
+        }
+        const int32_t blk = block_ids[page];
+        if (blk < 0 || blk >= num_blocks) {
+            if (r == 0) raise_flag(err_flag, XS_FLAG_BAD_BLOCK);
+            continue;
+        }
+        const int64_t dst = ((static_cast<int64_t>(blk) * Hkv + h) * bs + pos % bs) *
+                                chunks_per_row + c;
+        const int64_t src = (h * T + t) * chunks_per_row + c;
+        if (is_v)
+            v_cache[dst] = v_src[src];
+        else
+            k_cache[dst] = k_src[src];
+    }
+}
+
 int launch_append(bool from_table, const void *k_new, const void *v_new, void *k_cache,
                   void *v_cache, const int64_t *slot_mapping, const int32_t *block_tables,
                   int max_blocks, const int32_t *lens, int T, int Hkv, int D, int bs,
@@ -151,4 +189,30 @@ extern "C" int xs_kv_append_paged(const void *k_new, const void *v_new, void *k_
     return xs::launch_append(true, k_new, v_new, k_cache, v_cache, nullptr, block_tables,
                              max_blocks_per_seq, context_lens, B, Hkv, D, block_size, num_blocks,
                              dtype, err_flag, stream);
+}
+
+extern "C" int xs_prefill_append(const void *k_src, const void *v_src, void *k_cache,
+                                 void *v_cache, const int32_t *block_ids, int n_ids, int T,
+                                 int Hkv, int D, int block_size, int64_t num_blocks, int start_pos,
+                                 int dtype, int *err_flag, cudaStream_t stream) {
+    if (!k_src || !v_src || !k_cache || !v_cache || !block_ids) return XS_ENULL;
+    const int eb = xs::elem_bytes(dtype);
+    if (!eb) return XS_EDTYPE;
+    if (T < 0 || Hkv <= 0 || D <= 0 || block_size <= 0 || n_ids < 0 || start_pos < 0 ||
+        num_blocks < 0)
+        return XS_ESHAPE;
+    if ((static_cast<int64_t>(D) * eb) % 16 != 0) return XS_EUNSUPPORTED;
+    if (!xs::aligned16(k_src) || !xs::aligned16(v_src) || !xs::aligned16(k_cache) ||
+        !xs::aligned16(v_cache))
+        return XS_EALIGN;
+    if (T == 0) return XS_OK;
+    const int chunks = D * eb / 16;
+    const int64_t total = static_cast<int64_t>(T) * 2 * Hkv * chunks;
+    const int64_t blocks64 = (total + xs::kAppendThreads - 1) / xs::kAppendThreads;
+    const int grid = static_cast<int>(blocks64 < (1 << 20) ? blocks64 : (1 << 20));
+    xs::prefill_append_kernel<<<grid, xs::kAppendThreads, 0, stream>>>(
+        static_cast<const uint4 *>(k_src), static_cast<const uint4 *>(v_src),
+        static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), block_ids, n_ids, T, Hkv,
+        chunks, block_size, num_blocks, start_pos, err_flag);
+    return xs::launch_status();
 }

@@ -101,13 +101,18 @@ struct Params {
     float qscale;  // scale * log2(e)
     const void *sinks;  // [Hq] sink logits (q's dtype), or null
     int window;         // > 0: attend to the last `window` tokens only
+    // Prefill mode (prefill_start >= 0): "sequence" b is query token b of one
+    // chunk at position prefill_start + b, attending to prefill_start + b + 1
+    // tokens through the one block list (table_stride 0); context_lens unused.
+    int prefill_start;
+    int table_stride;   // elements between block-table rows (max_blocks, or 0)
     int *err_flag;
     int *work;     // [2] item counter + finished-CTA counter (zero between launches), or null
 };
 
 // Number of tokens sequence b attends to, clamped to the table's reach.
 __device__ __forceinline__ int seq_len(const Params &p, int b, bool report) {
-    int n = p.context_lens[b];
+    int n = p.prefill_start >= 0 ? p.prefill_start + b + 1 : p.context_lens[b];
     const int cap = p.max_blocks * kBlock;
     if (n > cap) {
         if (report) raise_flag(p.err_flag, XS_FLAG_BAD_LEN);
@@ -407,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
         }
     }
     // Sequences with no tokens produce zeros.
-    for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
+    for (int b = blockIdx.x; b < p.B && p.prefill_start < 0; b += gridDim.x) {
         if (p.context_lens[b] > 0) continue;
         T *o = static_cast<T *>(p.out) + static_cast<int64_t>(b) * p.Hq * D;
         for (int i = tid; i < p.Hq * D; i += kThreads) o[i] = Elem<T>::from_f32(0.f);
@@ -458,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
             int32_t blk = 0;
             const int pg = base + lane;
             if (it.b >= 0 && pg < it.pg1) {
-                blk = p.block_tables[static_cast<int64_t>(it.b) * p.max_blocks + pg];
+                blk = p.block_tables[static_cast<int64_t>(it.b) * p.table_stride + pg];
                 if (blk < 0 || blk >= p.num_blocks) {
                     raise_flag(p.err_flag, XS_FLAG_BAD_BLOCK);
                     blk = 0;
@@ -750,10 +755,10 @@ __global__ void paged_decode_reduce_kernel(T *__restrict__ out, const float *__r
                                            const float *__restrict__ part_l,
                                            const int32_t *__restrict__ lens, int Hq, int D, int P,
                                            int max_parts, const T *__restrict__ sinks,
-                                           int window) {
+                                           int window, int prefill_start) {
     const int bh = blockIdx.x;
     const int b = bh / Hq;
-    int n = lens[b];
+    int n = prefill_start >= 0 ? prefill_start + b + 1 : lens[b];
     if (window > 0 && n > window) n = window;
     int np = n > 0 ? (n + P - 1) / P : 0;
     np = min(np, max_parts);
@@ -928,8 +933,9 @@ extern "C" size_t xs_paged_decode_workspace_bytes(int B, int Hq, int D, int max_
 static int check_attn_args(const void *out, const float *po, const float *pm, const float *pl,
                            const void *q, const void *kc, const void *vc, const int32_t *bt,
                            int max_blocks, const int32_t *lens, int B, int Hq, int Hkv, int D,
-                           int bs, int64_t num_blocks, int P, int max_parts, int dtype) {
-    if (!out || !q || !kc || !vc || !bt || !lens) return XS_ENULL;
+                           int bs, int64_t num_blocks, int P, int max_parts, int dtype,
+                           bool prefill = false) {
+    if (!out || !q || !kc || !vc || !bt || (!lens && !prefill)) return XS_ENULL;
     if (!elem_bytes(dtype)) return XS_EDTYPE;
     if (B < 0 || Hq <= 0 || Hkv <= 0 || max_blocks < 0 || num_blocks < 0) return XS_ESHAPE;
     if (Hq % Hkv != 0) return XS_ESHAPE;
@@ -950,11 +956,13 @@ static int launch_attn(void *out, float *part_o, float *part_m, float *part_l, c
                        int max_blocks_per_seq, const int32_t *context_lens, int B, int Hq,
                        int Hkv, int D, int block_size, int64_t num_blocks, float scale,
                        const void *sinks, int window, int partition_tokens, int max_partitions,
-                       int dtype, int *err_flag, int *work_counters, cudaStream_t stream) {
+                       int dtype, int *err_flag, int *work_counters, cudaStream_t stream,
+                       int prefill_start = -1) {
     if (window < 0) return XS_ESHAPE;
+    const bool prefill = prefill_start >= 0;
     int st = check_attn_args(out, part_o, part_m, part_l, q, k_cache, v_cache, block_tables,
                              max_blocks_per_seq, context_lens, B, Hq, Hkv, D, block_size,
-                             num_blocks, partition_tokens, max_partitions, dtype);
+                             num_blocks, partition_tokens, max_partitions, dtype, prefill);
     if (st != XS_OK) return st;
     if (B == 0) return XS_OK;
     attn::DeviceInfo dev;
@@ -989,6 +997,8 @@ static int launch_attn(void *out, float *part_o, float *part_m, float *part_l, c
     p.qscale = scale * attn::kLog2e;
     p.sinks = sinks;
     p.window = window;
+    p.prefill_start = prefill_start;
+    p.table_stride = prefill ? 0 : max_blocks_per_seq;
     p.err_flag = err_flag;
     p.work = work_counters;
     fn<<<grid, attn::kThreads, smem, stream>>>(p);
@@ -1026,8 +1036,9 @@ extern "C" int xs_paged_decode_attn_sinks(void *out, float *part_o, float *part_
 static int launch_reduce(void *out, const float *part_o, const float *part_m,
                          const float *part_l, const int32_t *context_lens, const void *sinks,
                          int window, int B, int Hq, int D, int partition_tokens,
-                         int max_partitions, int dtype, cudaStream_t stream) {
-    if (!out || !context_lens) return XS_ENULL;
+                         int max_partitions, int dtype, cudaStream_t stream,
+                         int prefill_start = -1) {
+    if (!out || (!context_lens && prefill_start < 0)) return XS_ENULL;
     if (window < 0) return XS_ESHAPE;
     if (!elem_bytes(dtype)) return XS_EDTYPE;
     if (B < 0 || Hq <= 0 || D <= 0 || D > 1024 || partition_tokens <= 0 || max_partitions <= 0)
@@ -1041,11 +1052,13 @@ static int launch_reduce(void *out, const float *part_o, const float *part_m,
         attn::paged_decode_reduce_kernel<__nv_bfloat16><<<static_cast<int>(blocks), threads, 0,
                                                           stream>>>(
             static_cast<__nv_bfloat16 *>(out), part_o, part_m, part_l, context_lens, Hq, D,
-            partition_tokens, max_partitions, static_cast<const __nv_bfloat16 *>(sinks), window);
+            partition_tokens, max_partitions, static_cast<const __nv_bfloat16 *>(sinks), window,
+            prefill_start);
     else
         attn::paged_decode_reduce_kernel<float><<<static_cast<int>(blocks), threads, 0, stream>>>(
             static_cast<float *>(out), part_o, part_m, part_l, context_lens, Hq, D,
-            partition_tokens, max_partitions, static_cast<const float *>(sinks), window);
+            partition_tokens, max_partitions, static_cast<const float *>(sinks), window,
+            prefill_start);
     return launch_status();
 }
 
@@ -1098,6 +1111,52 @@ extern "C" int xs_paged_decode_sinks(void *out, float *part_o, float *part_m, fl
     if (st != XS_OK || max_partitions <= 1) return st;
     return xs_paged_decode_reduce_sinks(out, part_o, part_m, part_l, context_lens, sinks, window,
                                         B, Hq, D, partition_tokens, max_partitions, dtype, stream);
+}
+
+// ---------------------------------------------------------------- chunked prefill
+//
+// Causal attention of a T-token chunk at positions start_pos .. over one
+// sequence's paged cache, on the decode kernel: query token i is treated as
+// a sequence of start_pos + i + 1 tokens that shares the chunk's block list.
+
+extern "C" int xs_paged_prefill_attn(void *out, float *part_o, float *part_m, float *part_l,
+                                     const void *q, const void *k_cache, const void *v_cache,
+                                     const int32_t *block_ids, int n_ids, int T, int start_pos,
+                                     int Hq, int Hkv, int D, int block_size, int64_t num_blocks,
+                                     float scale, int partition_tokens, int max_partitions,
+                                     int dtype, int *err_flag, int *work_counters,
+                                     cudaStream_t stream) {
+    if (T < 0 || start_pos < 0 || n_ids < 0) return XS_ESHAPE;
+    if (static_cast<int64_t>(start_pos) + T > static_cast<int64_t>(n_ids) * block_size)
+        return XS_ESHAPE;  // the block list does not cover the chunk
+    return launch_attn(out, part_o, part_m, part_l, q, k_cache, v_cache, block_ids, n_ids,
+                       nullptr, T, Hq, Hkv, D, block_size, num_blocks, scale, nullptr, 0,
+                       partition_tokens, max_partitions, dtype, err_flag, work_counters, stream,
+                       start_pos);
+}
+
+extern "C" int xs_paged_prefill_reduce(void *out, const float *part_o, const float *part_m,
+                                       const float *part_l, int T, int start_pos, int Hq, int D,
+                                       int partition_tokens, int max_partitions, int dtype,
+                                       cudaStream_t stream) {
+    if (start_pos < 0) return XS_ESHAPE;
+    return launch_reduce(out, part_o, part_m, part_l, nullptr, nullptr, 0, T, Hq, D,
+                         partition_tokens, max_partitions, dtype, stream, start_pos);
+}
+
+extern "C" int xs_paged_prefill(void *out, float *part_o, float *part_m, float *part_l,
+                                const void *q, const void *k_cache, const void *v_cache,
+                                const int32_t *block_ids, int n_ids, int T, int start_pos, int Hq,
+                                int Hkv, int D, int block_size, int64_t num_blocks, float scale,
+                                int partition_tokens, int max_partitions, int dtype,
+                                int *err_flag, int *work_counters, cudaStream_t stream) {
+    int st = xs_paged_prefill_attn(out, part_o, part_m, part_l, q, k_cache, v_cache, block_ids,
+                                   n_ids, T, start_pos, Hq, Hkv, D, block_size, num_blocks, scale,
+                                   partition_tokens, max_partitions, dtype, err_flag,
+                                   work_counters, stream);
+    if (st != XS_OK || max_partitions <= 1) return st;
+    return xs_paged_prefill_reduce(out, part_o, part_m, part_l, T, start_pos, Hq, D,
+                                   partition_tokens, max_partitions, dtype, stream);
 }
 
 // ---------------------------------------------------------------- no-allocation variant

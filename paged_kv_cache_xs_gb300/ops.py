@@ -55,6 +55,12 @@ SIGNATURES = {
     "xs_kv_swap": (_I, [_P, _P, _P, _P, _P, _I, _L, _L, _L, _P, _P]),
     "xs_block_alloc_decode": (_I, [_P, _I, _P, _I, _I, _P, _P, _P, _P]),
     "xs_block_free": (_I, [_P, _I, _P, _I, _P, _I, _I, _P, _P, _L, _P, _P]),
+    "xs_prefill_append": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _L, _I, _I, _P, _P]),
+    "xs_paged_prefill_attn": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I,
+                                   _L, _F, _I, _I, _I, _P, _P, _P]),
+    "xs_paged_prefill_reduce": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P]),
+    "xs_paged_prefill": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _L, _F,
+                              _I, _I, _I, _P, _P, _P]),
     "xs_version": (_I, []),
 }
 
@@ -273,6 +279,28 @@ def xs_block_free(seq_ids, block_tables, context_lens, free_stack, free_top,
     _call("xs_block_free", _ptr(seq_ids), seq_ids.numel(), _ptr(block_tables),
           block_tables.shape[1], _ptr(context_lens), context_lens.numel(), block_size,
           _ptr(free_stack), _ptr(free_top), free_stack.numel(), _ptr(err_flag), _stream(stream))
+
+
+def xs_prefill_append(k_src, v_src, k_cache, v_cache, block_ids, start_pos, err_flag=None,
+                      stream=None):
+    """Write a [Hkv, T, D] chunk at positions start_pos .. of one sequence."""
+    Hkv, T, D = k_src.shape
+    num_blocks, _, bs, _ = k_cache.shape
+    _call("xs_prefill_append", _ptr(k_src), _ptr(v_src), _ptr(k_cache), _ptr(v_cache),
+          _ptr(block_ids), block_ids.numel(), T, Hkv, D, bs, num_blocks, int(start_pos),
+          dtype_code(k_src.dtype), _ptr(err_flag), _stream(stream))
+
+
+def xs_paged_prefill(out, part_o, part_m, part_l, q, k_cache, v_cache, block_ids, start_pos,
+                     scale, partition_tokens, max_partitions, err_flag=None, work_counters=None,
+                     stream=None):
+    """Causal attention of the chunk q [T, Hq, D] at start_pos over the pages."""
+    T, Hq, D = q.shape
+    num_blocks, Hkv, bs, _ = k_cache.shape
+    _call("xs_paged_prefill", _ptr(out), _ptr(part_o), _ptr(part_m), _ptr(part_l), _ptr(q),
+          _ptr(k_cache), _ptr(v_cache), _ptr(block_ids), block_ids.numel(), T, int(start_pos), Hq,
+          Hkv, D, bs, num_blocks, float(scale), partition_tokens, max_partitions,
+          dtype_code(q.dtype), _ptr(err_flag), _ptr(work_counters), _stream(stream))
 
 
 def xs_version() -> int:
