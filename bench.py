@@ -531,6 +531,75 @@ def run_swap(args, rank, world, local, dist):
     print(json.dumps(line), flush=True)
 
 
+def run_prefill(args, rank, world, local, dist):
+    """Chunked-prefill row: one Qwen3-8B-shaped sequence prefilled in chunks
+    (append + causal paged attention per chunk), timed per chunk."""
+    from paged_kv_cache_xs_gb300 import build as xsbuild
+    from paged_kv_cache_xs_gb300 import ops
+
+    xsbuild.build()
+    ops.load()
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    Hq, Hkv, D, bs = 32, 8, 128, 16
+    dtype = torch.bfloat16
+    total, chunk = args.prefill_tokens, args.prefill_chunk
+    pages = (total + bs - 1) // bs
+    g = torch.Generator(device=dev).manual_seed(2000 + rank)
+    ids = torch.randperm(pages * 2, generator=g, device=dev)[:pages].to(torch.int32)
+    kc = torch.empty(pages * 2, Hkv, bs, D, dtype=dtype, device=dev).normal_(generator=g)
+    vc = torch.empty_like(kc).normal_(generator=g)
+    ks = torch.randn(Hkv, total, D, generator=g, device=dev).to(dtype)
+    vs = torch.randn(Hkv, total, D, generator=g, device=dev).to(dtype)
+    q = torch.randn(total, Hq, D, generator=g, device=dev).to(dtype)
+    wss = {}
+
+    def prefill_all():
+        for start in range(0, total, chunk):
+            T = min(chunk, total - start)
+            ws = wss.get(T)
+            if ws is None:
+                ws = wss[T] = ops.DecodeWorkspace(T, Hq, Hkv, D, pages, dev,
+                                                  total_context_tokens=T * (start + T),
+                                                  max_context_len=total)
+            ops.xs_prefill_append(ks[:, start:start + T].contiguous(),
+                                  vs[:, start:start + T].contiguous(), kc, vc, ids, start)
+            out = torch.empty(T, Hq, D, dtype=dtype, device=dev)
+            ops.xs_paged_prefill(out, ws.part_o, ws.part_m, ws.part_l, q[start:start + T], kc, vc,
+                                 ids, start, D ** -0.5, ws.partition_tokens, ws.max_partitions,
+                                 work_counters=ws.work)
+
+    for _ in range(args.warmup):
+        prefill_all()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        prefill_all()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    if rank != 0:
+        return
+    # Causal attention flops: 4 * D per (query head, query token, key) pair.
+    pairs = total * (total + 1) / 2
+    tflops = 4 * D * Hq * pairs / (ms * 1e-3) / 1e12
+    line = {
+        "metric": "chunked prefill attention over the paged cache (tokens/s, TFLOP/s)",
+        "value": round(total / (ms * 1e-3), 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": "qwen3_8b_prefill", "tokens": total, "chunk": chunk, "Hq": Hq,
+                   "Hkv": Hkv, "D": D},
+        "attention_tflops": round(tflops, 2),
+        "roofline": {"bound": "alu", "achieved": round(tflops, 2), "unit": "TFLOP/s",
+                     "note": "fp32 CUDA-core FMA path (the decode kernel in prefill mode)"},
+        "gpu_launches": args.steps * 2 * ((total + chunk - 1) // chunk),
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__)
     ap.add_argument("--gpus", type=int, default=1)
@@ -539,8 +608,11 @@ def main(argv=None):
     ap.add_argument("--config", type=int, default=4,
                     help="workload index (0-4); default: the large-batch long-context one")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--op", choices=["decode", "swap"], default="decode",
-                    help="decode: the decode step (default); swap: KV block swap to pinned host")
+    ap.add_argument("--op", choices=["decode", "swap", "prefill"], default="decode",
+                    help="decode: the decode step (default); swap: KV block swap to pinned "
+                         "host; prefill: chunked prefill into the paged cache")
+    ap.add_argument("--prefill-tokens", type=int, default=8192)
+    ap.add_argument("--prefill-chunk", type=int, default=1024)
     ap.add_argument("--swap-blocks", type=int, default=16384,
                     help="blocks per swap direction for --op swap")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -567,6 +639,8 @@ def main(argv=None):
             run_reference(args, rank, world, dist)
         elif args.op == "swap":
             run_swap(args, rank, world, local, dist)
+        elif args.op == "prefill":
+            run_prefill(args, rank, world, local, dist)
         else:
             run_ours(args, rank, world, local, dist)
     finally:
