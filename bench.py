@@ -314,7 +314,7 @@ def run_ours(args, rank, world, local, dist):
                            total_context_tokens=win_tokens,
                            max_context_len=min(w.max_context_len, args.window or 1 << 30),
                            partition_tokens=args.partition_tokens or None,
-                           sinks=sinks, window=args.window)
+                           sinks=sinks, window=args.window, fused=args.fused == "on")
     out = torch.empty(L, cfg.B, cfg.Hq, cfg.D, dtype=cfg.dtype, device=dev)  # every layer's output
     stream = torch.cuda.current_stream()
     by = step_bytes(cfg, lens_cpu, args.window)
@@ -323,6 +323,15 @@ def run_ours(args, rank, world, local, dist):
     def one_step(ev=None):
         cur = torch.cuda.current_stream()
         for layer in range(L):
+            if args.fused == "on":  # append + attention + combine: one launch
+                if ev is not None:
+                    ev[layer][0].record(cur)
+                step.run(out[layer], w.q[layer], w.k_new[layer], w.v_new[layer],
+                         w.k_cache[layer], w.v_cache[layer], w.block_tables, w.context_lens,
+                         w.scale)
+                if ev is not None:
+                    ev[layer][1].record(cur)
+                continue
             step.append(w.k_new[layer], w.v_new[layer], w.k_cache[layer], w.v_cache[layer],
                         w.block_tables, w.context_lens)
             if ev is not None:
@@ -422,7 +431,9 @@ def run_ours(args, rank, world, local, dist):
         return
     peak, peak_kind = hbm_peak()
     attn_avg_ms = statistics.mean(attn_ms)
-    attn_gbs = by["attn"] / (attn_avg_ms * 1e-3) / 1e9
+    # The fused launch also appends the new rows and writes the output.
+    launch_bytes = by["step"] if args.fused == "on" else by["attn"]
+    attn_gbs = launch_bytes / (attn_avg_ms * 1e-3) / 1e9
     traffic = kernel_traffic(cfg.name)
     line = {
         "metric": METRIC,
@@ -455,12 +466,13 @@ def run_ours(args, rank, world, local, dist):
                      "achieved": round(attn_gbs, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(attn_gbs / peak, 4), "peak_kind": peak_kind,
                      "traffic": traffic,
-                     "algorithmic_bytes_per_launch": by["attn"],
+                     "algorithmic_bytes_per_launch": launch_bytes,
                      "avg_launch_ms": round(attn_avg_ms, 4)},
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_s * 1e3, 4)},
-        "gpu_launches": args.steps * L * step.launches_per_step,
+        "gpu_launches": args.steps * L * step.launches_per_step(args.fused == "on"),
         "cuda_graph": graph is not None,
+        "fused_step": args.fused == "on",
         "clocks": clock_info,
     }
     if not args.no_cpu_baseline:
@@ -620,6 +632,9 @@ def main(argv=None):
                     help="gpt-oss variant: random per-head sink logits in the softmax")
     ap.add_argument("--window", type=int, default=0,
                     help="gpt-oss variant: sliding window of the last W tokens (0 = all)")
+    ap.add_argument("--fused", choices=["on", "off"], default="on",
+                    help="on: each layer's step is one launch (append + attention + combine); "
+                         "off: three launches")
     ap.add_argument("--graph", choices=["auto", "on", "off"], default="auto",
                     help="replay each step as one CUDA graph (auto: when the workload has "
                          "more than one layer)")

@@ -382,6 +382,66 @@ int xs_paged_decode_sinks(void *out, float *part_o, float *part_m, float *part_l
                           cudaStream_t stream);
 
 /*
+ * xs_paged_decode_step - one whole decode step in ONE launch: the KV append
+ * of xs_kv_append_paged, the attention of xs_paged_decode_attn_sinks and the
+ * split-K combine of xs_paged_decode_reduce_sinks ("xserv compare
+ * phase10...cf1e9e4", attention.rs: reshape_and_cache_batched_bf16, then
+ * paged_decode_attention / paged_decode_attention_sinks).  The result equals
+ * those three calls in that order.
+ *
+ * How the launch does it:
+ *  - append: the work item that covers sequence b's last page for KV head g
+ *    writes k_new[b, g, :] and v_new[b, g, :] into slot
+ *    block_tables[b][(N-1)/16] * 16 + (N-1) % 16 (N = context_lens[b]) and
+ *    then loads that page, so the new token is attended to.  N <= 0 appends
+ *    nothing; N beyond the table appends nothing and raises XS_FLAG_BAD_LEN;
+ *    an out-of-pool block id appends nothing and raises XS_FLAG_BAD_BLOCK.
+ *    k_new and v_new are both NULL (attention only) or both [B, Hkv, D] in
+ *    dtype.  No other sequence may attend to a row written in the same step
+ *    (true of any block table where the block a sequence appends to is its
+ *    own, e.g. shared prefixes copied on write).
+ *  - combine: each item of a split (sequence, KV head) writes its partials,
+ *    then counts itself in; the item that completes the group merges the
+ *    group's partials for the G query heads into out.
+ *
+ * counters: int32 on the device, xs_paged_decode_step_counters(B, Hkv) of
+ * them (2 + B * Hkv: the work-item counters, then one arrival count per
+ * sequence and KV head), zero before the first launch; every completed
+ * launch leaves them zero.  Launches sharing counters must be ordered (one
+ * stream, or one CUDA graph).  After a launch that raised XS_FLAG_TIMEOUT,
+ * zero them before the next launch.  NULL counters is XS_EWORKSPACE.
+ *
+ * Other arguments, layouts, workspace rules and errors as
+ * xs_paged_decode_attn_sinks (sinks NULL and window 0 give the plain step).
+ * k_cache and v_cache are written (the new rows only).
+ */
+int xs_paged_decode_step(void *out, const void *q, const void *k_new, const void *v_new,
+                         void *k_cache, void *v_cache, const int32_t *block_tables,
+                         int max_blocks_per_seq, const int32_t *context_lens, const void *sinks,
+                         int window, int B, int Hq, int Hkv, int D, int block_size,
+                         int64_t num_blocks, float scale, int partition_tokens,
+                         int max_partitions, float *part_o, float *part_m, float *part_l,
+                         int *counters, int dtype, int *err_flag, cudaStream_t stream);
+
+/*
+ * xs_paged_decode_step_partition_tokens - partition length P for
+ * xs_paged_decode_step: the cost model of xs_paged_decode_partition_tokens
+ * plus the in-launch combine (the groups that complete last are combined
+ * after the last page is read, at a cost that grows with the longest
+ * sequence's partition count times the group size Hq / Hkv).  Same
+ * arguments plus Hq; XS_ESHAPE also when Hq % Hkv != 0.
+ */
+int xs_paged_decode_step_partition_tokens(int B, int Hq, int Hkv, int64_t total_context_tokens,
+                                          int max_context_len, int num_sms);
+
+/*
+ * xs_paged_decode_step_counters - how many int32 counters
+ * xs_paged_decode_step needs for B sequences and Hkv KV heads (2 + B * Hkv),
+ * or XS_ESHAPE (B < 0, Hkv <= 0).
+ */
+int64_t xs_paged_decode_step_counters(int B, int Hkv);
+
+/*
  * xs_paged_decode_noalloc - xs_paged_decode for callers that cannot allocate
  * device memory.  The paper has no counterpart of this entry point: it is a
  * service of this library.

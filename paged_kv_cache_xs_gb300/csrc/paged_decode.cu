@@ -32,6 +32,7 @@
 #include <algorithm>
 #include <cmath>
 #include <mutex>
+#include <type_traits>
 
 #include "xs_common.cuh"
 
@@ -77,14 +78,16 @@ struct Cfg {
     static constexpr int kWBytes = kConsumerWarps * kBlock * G * 8;   // (w, w) pairs
     static constexpr int kCombOff = kWOff + kWBytes;
     // A merge buffer: the item (32 B), then m[4][G], l[4][G], o[4][G][D] (fp32).
-    static constexpr int kCombBytes = 32 + kConsumerWarps * G * (D + 2) * 4;  // one of 2
-    static constexpr int kBarOff = (kCombOff + 2 * kCombBytes + 7) / 8 * 8;
-    static constexpr int kBarBytes = (2 * kStages + 8) * 8;
+    static constexpr int kCombBytes = 32 + kConsumerWarps * G * (D + 2) * 4;  // one buffer
+    static constexpr int kMergeBufs = 2;   // consumers run up to kMergeBufs - 1 items ahead
+    static constexpr int kBarOff = (kCombOff + kMergeBufs * kCombBytes + 7) / 8 * 8;
+    static constexpr int kBarBytes = (2 * kStages + 4 + 2 * kMergeBufs) * 8;
     static constexpr int kItemOff = kBarOff + kBarBytes;             // 2 published items
     static constexpr int kPrefixOff = kItemOff + 2 * 32;
     // The host sizes every launch with this same function.
     static __host__ __device__ constexpr int smem_bytes(int B) { return kPrefixOff + table_bytes(B); }
     static_assert(kStages % kConsumerWarps == 0, "each ring stage must belong to one consumer");
+    static_assert((kMergeBufs & (kMergeBufs - 1)) == 0, "item counters wrap: a power of two");
     static_assert(kChunksPerLane >= 1 && kChunksPerRow % 8 == 0, "row must split over 8 lanes");
     static_assert(D % 64 == 0, "PV works on dim pairs: D must split over 32 lanes x 2");
     static_assert(kCombOff % 16 == 0 && kCombBytes % 16 == 0 && (kConsumerWarps * G * 4) % 16 == 0,
@@ -108,6 +111,14 @@ struct Params {
     int table_stride;   // elements between block-table rows (max_blocks, or 0)
     int *err_flag;
     int *work;     // [2] item counter + finished-CTA counter (zero between launches), or null
+    // Fused decode step (decode mode only).  k_new/v_new [B, Hkv, D]: this
+    // step's rows, written into their slot by the item that covers the
+    // sequence's last page before it loads that page; null = no append.
+    const void *k_new, *v_new;
+    // [B * Hkv] arrival counts (zero between launches): the last item of a
+    // split sequence-head combines its partials into out; null = leave the
+    // partials for the separate combine kernel.
+    int *combine;
 };
 
 // Number of tokens sequence b attends to, clamped to the table's reach.
@@ -133,34 +144,50 @@ __device__ __forceinline__ int first_token(const Params &p, int n) {
 }
 
 // Largest b in [0, B) with table[b] <= x (table is non-decreasing).
-__device__ __forceinline__ int upper_index(const int *table, int B, int x) {
-    int lo = 0, hi = B - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (table[mid] <= x) lo = mid; else hi = mid - 1;
+// Largest b in [0, B) with table[b] <= x, for a nondecreasing table with
+// table[0] <= x, searched by the whole warp: each round the 32 lanes test
+// the starts of 32 equal segments of the range and a ballot picks the last
+// segment that starts at or below x (one round for B <= 32, two up to 1024).
+__device__ __forceinline__ int upper_index(const int *table, int B, int x, int lane) {
+    int lo = 0, n = B;  // search [lo, lo + n); table[lo] <= x throughout
+    while (n > 32) {
+        const int step = (n + 31) >> 5;
+        const bool le = lane * step < n && table[lo + lane * step] <= x;
+        const int seg = 31 - __clz(__ballot_sync(0xffffffffu, le));
+        lo += seg * step;
+        n = min(step, n - seg * step);
     }
-    return lo;
+    const bool le = lane < n && table[lo + lane] <= x;
+    return lo + 31 - __clz(__ballot_sync(0xffffffffu, le));
 }
 
-// Item numbering: first every full partition (P tokens) of every sequence and
-// KV head, in sequence order, then the ragged last partitions (and short
-// sequences) - so the end of a launch is made of small items that balance
-// the grid.  pfull/ptail are the exclusive prefix sums of those counts.
+// Item numbering.  Without the fused combine: first every full partition (P
+// tokens) of every sequence and KV head, in sequence order, then the ragged
+// last partitions (and short sequences) - so the end of a launch is made of
+// small items that balance the grid.  With it, the ragged partitions come
+// first: a sequence-head group is complete when its last item is, and with
+// the ragged ones last every group would complete - and be combined - in the
+// launch's final moments; full partitions last make groups complete, and
+// combine, all along.  pfull/ptail are the exclusive prefix sums of the
+// per-sequence counts of full and ragged items.
 __device__ __forceinline__ Item decode_item(const Params &p, const int *pfull, const int *ptail,
-                                            const int *nlen, int item) {
+                                            const int *nlen, int item, int lane) {
     Item it;
-    const int n_full = pfull[p.B];
+    const bool tails_first = p.combine != nullptr;
+    const int n_full = pfull[p.B], n_tail = ptail[p.B];
+    const int full_idx = tails_first ? item - n_tail : item;
+    const int tail_idx = tails_first ? item : item - n_full;
+    const bool is_full = tails_first ? item >= n_tail : item < n_full;
     int b;
-    if (item < n_full) {
-        b = upper_index(pfull, p.B, item);
-        const int r = item - pfull[b];
+    if (is_full) {
+        b = upper_index(pfull, p.B, full_idx, lane);
+        const int r = full_idx - pfull[b];
         const int nf = (pfull[b + 1] - pfull[b]) / p.Hkv;
         it.g = r / nf;
         it.part = r - it.g * nf;
     } else {
-        const int r2 = item - n_full;
-        b = upper_index(ptail, p.B, r2);
-        it.g = r2 - ptail[b];
+        b = upper_index(ptail, p.B, tail_idx, lane);
+        it.g = tail_idx - ptail[b];
         it.part = (nlen[b] - first_token(p, nlen[b])) / p.P;
     }
     it.b = b;
@@ -319,6 +346,116 @@ __device__ __forceinline__ void consume_page(const unsigned char *Ks, const unsi
     __syncwarp();
 }
 
+// Split-K combine of one split sequence-head group, run by one warp (the
+// merger of the item that finished last): for each of the G heads,
+//     out = sum_j 2^(m_j - M) l_j o_j / (sum_j 2^(m_j - M) l_j [+ sink term])
+// with M = max_j m_j, over the nparts partials (o_j already divided by l_j).
+// The partials were written by other CTAs of this launch: read through L2.
+// All G heads go together and every batch of loads is issued before any is
+// used, so a group costs a few L2 round trips, not a few per head.
+template <typename T, int D, int G>
+__device__ __noinline__ void combine_partials(const Params &p, const Item &it, int64_t head0,
+                                              int lane) {
+    constexpr int kDims = D / 32;              // output dims per lane
+    constexpr int kJ = G >= 16 ? 1 : 16 / G;   // partials per batch (16 row loads in flight)
+    using Vec = typename std::conditional<kDims == 4, float4, float2>::type;
+    const int np = it.nparts;
+    const float *pm = p.part_m + head0 * p.max_parts;
+    const float *pl = p.part_l + head0 * p.max_parts;
+    // Max and denominator per head (lanes stride over the partials).
+    float mx[G], den[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) mx[h] = -INFINITY;
+    for (int j = lane; j < np; j += 32)
+#pragma unroll
+        for (int h = 0; h < G; ++h) mx[h] = fmaxf(mx[h], __ldcg(pm + h * p.max_parts + j));
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], o));
+        den[h] = 0.f;
+    }
+    for (int j = lane; j < np; j += 32)
+#pragma unroll
+        for (int h = 0; h < G; ++h)
+            den[h] += fast_exp2(__ldcg(pm + h * p.max_parts + j) - mx[h]) *
+                      __ldcg(pl + h * p.max_parts + j);
+    // Weighted sum of the partial outputs; each lane re-reads the (broadcast)
+    // m and l of the partials it weights.
+    float acc[G][kDims];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) den[h] += __shfl_xor_sync(0xffffffffu, den[h], o);
+#pragma unroll
+        for (int d = 0; d < kDims; ++d) acc[h][d] = 0.f;
+    }
+    const float *po = p.part_o + head0 * p.max_parts * D + lane * kDims;
+    for (int j0 = 0; j0 < np; j0 += kJ) {
+        Vec v[kJ][G];
+        float wm[kJ][G], wl[kJ][G];
+#pragma unroll
+        for (int u = 0; u < kJ; ++u)
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                const int j = min(j0 + u, np - 1);  // past the end: reload the last, weight 0
+                const int64_t r = static_cast<int64_t>(h) * p.max_parts + j;
+                v[u][h] = __ldcg(reinterpret_cast<const Vec *>(po + r * D));
+                wm[u][h] = __ldcg(pm + r);
+                wl[u][h] = __ldcg(pl + r);
+            }
+#pragma unroll
+        for (int u = 0; u < kJ; ++u)
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                const float w = j0 + u < np ? fast_exp2(wm[u][h] - mx[h]) * wl[u][h] : 0.f;
+                const float *f = reinterpret_cast<const float *>(&v[u][h]);
+#pragma unroll
+                for (int d = 0; d < kDims; ++d) acc[h][d] += w * f[d];
+            }
+    }
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+        float lt = den[h];
+        if (p.sinks)
+            lt += fast_exp2(Elem<T>::to_f32(static_cast<const T *>(p.sinks)[it.g * G + h]) * kLog2e -
+                            mx[h]);
+        const float inv = 1.f / lt;
+        T *dst = static_cast<T *>(p.out) + (head0 + h) * D + lane * kDims;
+#pragma unroll
+        for (int d = 0; d < kDims; ++d) dst[d] = Elem<T>::from_f32(acc[h][d] * inv);
+    }
+}
+
+// The merger's batched count: queue entry k (held by lane k < npend) is a
+// split item of group (b, g) with np partitions whose partials this warp has
+// written.  One fence publishes them all; each entry's group count is then
+// raised (all in flight together) and every entry that completes its group
+// combines it and clears the count for the next launch.
+template <typename T, int D, int G>
+__device__ __noinline__ void count_and_combine(const Params &p, int lane, int pend_b, int pend_g,
+                                               int pend_np, int npend) {
+    __threadfence();
+    __syncwarp();
+    int *cnt = p.combine + static_cast<int64_t>(pend_b) * p.Hkv + pend_g;
+    int prior = 0;
+    if (lane < npend) prior = atomicAdd(cnt, 1);
+    const bool last = lane < npend && prior == pend_np - 1;
+    if (last) atomicExch(cnt, 0);
+    unsigned todo = __ballot_sync(0xffffffffu, last);
+    if (todo) __threadfence();
+    while (todo) {
+        const int k = __ffs(todo) - 1;
+        todo &= todo - 1;
+        Item ci;
+        ci.b = __shfl_sync(0xffffffffu, pend_b, k);
+        ci.g = __shfl_sync(0xffffffffu, pend_g, k);
+        ci.nparts = __shfl_sync(0xffffffffu, pend_np, k);
+        const int64_t h0 = static_cast<int64_t>(ci.b) * p.Hq + static_cast<int64_t>(ci.g) * G;
+        combine_partials<T, D, G>(p, ci, h0, lane);
+    }
+}
+
 template <typename T, int D, int G>
 __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
     paged_decode_kernel(const Params p) {
@@ -330,7 +467,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
     uint64_t *qfull = empty + kStages;
     uint64_t *qempty = qfull + 2;
     uint64_t *merged = qempty + 2;  // per merge buffer: the four consumer states are in
-    uint64_t *freed = merged + 2;   // per merge buffer: the merger has read it
+    uint64_t *freed = merged + C::kMergeBufs;  // per merge buffer: the merger has read it
     Item *item_slot = reinterpret_cast<Item *>(smem + C::kItemOff);
     int *pfull = reinterpret_cast<int *>(smem + C::kPrefixOff);
     int *ptail = pfull + p.B + 1;
@@ -356,6 +493,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
         for (int s = 0; s < 2; ++s) {
             mbar_init(&qfull[s], 1);
             mbar_init(&qempty[s], kConsumerWarps);
+        }
+        for (int s = 0; s < C::kMergeBufs; ++s) {
             mbar_init(&merged[s], kConsumerWarps);
             mbar_init(&freed[s], 1);
         }
@@ -438,20 +577,32 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
         int grabs = 0;
         // The first two items of CTA c are c and c + gridDim.x (no atomic on
         // the start-up path); later ones come from the shared counter (items
-        // 2*gridDim.x, 2*gridDim.x + 1, ...) or, without one, from
-        // c + k * gridDim.x.  Lane 0's value is the item: read it with a shuffle.
+        // 2*gridDim.x + its value) or, without one, from c + k * gridDim.x.
+        // grab() only starts the fetch; item_of() turns it into an item id
+        // when it is needed, so the counter's round trip is not waited for
+        // early (the warp issues in order).  Lane 0's value is the one used.
+        struct Ticket {
+            int raw;
+            bool counted;
+        };
         auto grab = [&]() {
-            int v = static_next;
-            if (p.work && grabs >= 2 && lane == 0)
-                v = 2 * static_cast<int>(gridDim.x) + atomicAdd(&p.work[0], 1);
+            Ticket t{static_next, false};
+            if (p.work && grabs >= 2) {
+                t.counted = true;
+                t.raw = atomic_add_if(&p.work[0], 1, lane == 0);  // no branch: not waited on here
+            }
             ++grabs;
             static_next += gridDim.x;
-            return v;
+            return t;
+        };
+        auto item_of = [&](const Ticket &t) {
+            const int raw = __shfl_sync(0xffffffffu, t.raw, 0);
+            return t.counted ? 2 * static_cast<int>(gridDim.x) + raw : raw;
         };
         auto decode = [&](int item) {
             Item it;
             if (item < total_items) {
-                it = decode_item(p, pfull, ptail, nlen, item);
+                it = decode_item(p, pfull, ptail, nlen, item, lane);
             } else {
                 it.b = -1;
                 it.g = it.part = it.nparts = it.tok0 = it.tok1 = it.pg0 = it.pg1 = 0;
@@ -459,17 +610,67 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
             return it;
         };
         // Block ids of pages [base, base + 32) of an item, one per lane (0 past the end).
+        // Only starts the loads; the ids are checked where they are used.
         auto load_ids = [&](const Item &it, int base) {
             int32_t blk = 0;
             const int pg = base + lane;
-            if (it.b >= 0 && pg < it.pg1) {
+            if (it.b >= 0 && pg < it.pg1)
                 blk = p.block_tables[static_cast<int64_t>(it.b) * p.table_stride + pg];
-                if (blk < 0 || blk >= p.num_blocks) {
-                    raise_flag(p.err_flag, XS_FLAG_BAD_BLOCK);
-                    blk = 0;
+            return blk;
+        };
+        // Fused append: the item whose range ends at the sequence's last
+        // token writes this step's K and V rows of head g into their slot
+        // before it loads that page.  Rows are fetched one item ahead, with
+        // the sequence's unclamped length (a length beyond the table appends
+        // nothing, as in the separate append).
+        constexpr int kRowChunks = 2 * C::kChunksPerRow;  // K row, then V row
+        constexpr int kRowPerLane = (kRowChunks + 31) / 32;
+        struct Row {
+            uint4 v[kRowPerLane];
+            int raw_len;  // context_lens[b]; 0 = this item appends nothing
+        };
+        auto load_row = [&](const Item &it) {
+            Row r;
+            r.raw_len = 0;
+            if (p.k_new && it.b >= 0 && it.tok1 == nlen[it.b] && it.tok1 > 0) {
+                r.raw_len = p.context_lens[it.b];
+                const int64_t row = static_cast<int64_t>(it.b) * p.Hkv + it.g;
+                const uint4 *kn = static_cast<const uint4 *>(p.k_new) + row * C::kChunksPerRow;
+                const uint4 *vn = static_cast<const uint4 *>(p.v_new) + row * C::kChunksPerRow;
+#pragma unroll
+                for (int u = 0; u < kRowPerLane; ++u) {
+                    const int c = lane + 32 * u;
+                    if (c < C::kChunksPerRow)
+                        r.v[u] = kn[c];
+                    else if (c < kRowChunks)
+                        r.v[u] = vn[c - C::kChunksPerRow];
                 }
             }
-            return blk;
+            return r;
+        };
+        // Write the row of item `it` into block `blk`, then order those
+        // generic-proxy writes before the bulk copies that read the page.
+        auto store_row = [&](const Item &it, const Row &r, int32_t blk) {
+            const int n = r.raw_len;
+            if (n <= 0 || n > p.max_blocks * kBlock) return;  // nothing to append
+            if (blk < 0 || blk >= p.num_blocks) {
+                if (lane == 0) raise_flag(p.err_flag, XS_FLAG_BAD_BLOCK);
+                return;
+            }
+            const int64_t dst_row =
+                ((static_cast<int64_t>(blk) * p.Hkv + it.g) * kBlock + (n - 1) % kBlock) *
+                C::kChunksPerRow;
+            uint4 *kc = static_cast<uint4 *>(const_cast<void *>(p.k_cache)) + dst_row;
+            uint4 *vc = static_cast<uint4 *>(const_cast<void *>(p.v_cache)) + dst_row;
+#pragma unroll
+            for (int u = 0; u < kRowPerLane; ++u) {
+                const int c = lane + 32 * u;
+                if (c < C::kChunksPerRow)
+                    kc[c] = r.v[u];
+                else if (c < kRowChunks)
+                    vc[c - C::kChunksPerRow] = r.v[u];
+            }
+            fence_proxy_async_global();
         };
         // Publish an item (or the end marker) in the next q slot.
         auto publish = [&](const Item &it) {
@@ -496,43 +697,73 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
         };
         // Item B is published (q rows copied in) before item A's pages are
         // issued, so consumers finishing A find B's q already in place.
-        Item A = decode(__shfl_sync(0xffffffffu, grab(), 0));
+        Item A = decode(item_of(grab()));
         int32_t idsA = load_ids(A, A.pg0);
-        int nextB = grab();
+        Row rowA = load_row(A);
+        Ticket nextB = grab();
         bool ok = publish(A);
         while (ok && A.b >= 0) {
-            Item Bt = decode(__shfl_sync(0xffffffffu, nextB, 0));
+            Item Bt = decode(item_of(nextB));
             const int32_t idsB = load_ids(Bt, Bt.pg0);
-            if (Bt.b >= 0) nextB = grab();
+            const Row rowB = load_row(Bt);
+            nextB = grab();  // unconditionally: a branch here would wait for the fetch
             ok = publish(Bt);
             if (!ok) break;
-            // Stream A's pages, 32 block ids at a time (the next 32 load meanwhile).
+            // Stream A's pages, 32 block ids at a time (the next 32 load
+            // meanwhile).  Lane i owns page base + i of a chunk.  Each round,
+            // the lanes test the stages of the next (up to kStages) pages and
+            // every lane of the leading run of free stages issues its page's
+            // two copies - one warp instruction for all of them - so a
+            // producer that has fallen behind catches up several pages at a time.
+            const int64_t head_off = static_cast<int64_t>(A.g) * C::kPageBytes;
+            const int64_t blk_stride = static_cast<int64_t>(p.Hkv) * C::kPageBytes;
             int32_t ids = idsA;
             for (int base = A.pg0; ok && base < A.pg1; base += 32) {
                 const int32_t ids_next = (base + 32 < A.pg1) ? load_ids(A, base + 32) : 0;
                 const int cnt = min(32, A.pg1 - base);
-                for (int i = 0; i < cnt; ++i) {
-                    const int32_t bi = __shfl_sync(0xffffffffu, ids, i);
-                    if (lane == 0) {
-                        const uint32_t s = page_ctr % kStages, k = page_ctr / kStages;
-                        ok = mbar_wait_bounded(&empty[s], (k & 1) ^ 1, kWaitLimitNs);
-                        if (ok) {
-                            unsigned char *dk = smem + s * 2 * C::kPageBytes;
-                            const int64_t off =
-                                (static_cast<int64_t>(bi) * p.Hkv + A.g) * C::kPageBytes;
-                            mbar_arrive_expect_tx(&full[s], 2 * C::kPageBytes);
-                            bulk_g2s(dk, kbase + off, C::kPageBytes, &full[s], pol);
-                            bulk_g2s(dk + C::kPageBytes, vbase + off, C::kPageBytes, &full[s], pol);
+                if (rowA.raw_len > 0 && base + 32 >= A.pg1)  // the chunk with the last page
+                    store_row(A, rowA, __shfl_sync(0xffffffffu, ids, A.pg1 - 1 - base));
+                __syncwarp();
+                // An id outside the pool reads block 0 instead (flagged).
+                const bool bad_id = lane < cnt && (ids < 0 || ids >= p.num_blocks);
+                if (__any_sync(0xffffffffu, bad_id) && lane == 0)
+                    raise_flag(p.err_flag, XS_FLAG_BAD_BLOCK);
+                const int64_t my_off = static_cast<int64_t>(bad_id ? 0 : ids) * blk_stride + head_off;
+                int done = 0;
+                while (done < cnt) {
+                    const int want = min(cnt - done, kStages);
+                    const uint32_t c = page_ctr + lane;
+                    const uint32_t st = c % kStages;
+                    const bool is_free =
+                        lane < want && mbar_test_wait(&empty[st], ((c / kStages) & 1) ^ 1);
+                    const int n = __ffs(~__ballot_sync(0xffffffffu, is_free)) - 1;
+                    const int64_t off = __shfl_sync(0xffffffffu, my_off, (done + lane) & 31);
+                    if (n == 0) {
+                        // No stage free yet: wait (bounded) for the next one.
+                        bool w = true;
+                        if (lane == 0)
+                            w = mbar_wait_bounded(&empty[page_ctr % kStages],
+                                                  ((page_ctr / kStages) & 1) ^ 1, kWaitLimitNs);
+                        if (!__shfl_sync(0xffffffffu, w, 0)) {
+                            ok = false;
+                            break;
                         }
+                        continue;
                     }
-                    ok = __shfl_sync(0xffffffffu, ok, 0);
-                    if (!ok) break;
-                    ++page_ctr;  // pages issued so far
+                    if (lane < n) {
+                        unsigned char *dk = smem + st * 2 * C::kPageBytes;
+                        mbar_arrive_expect_tx(&full[st], 2 * C::kPageBytes);
+                        bulk_g2s(dk, kbase + off, C::kPageBytes, &full[st], pol);
+                        bulk_g2s(dk + C::kPageBytes, vbase + off, C::kPageBytes, &full[st], pol);
+                    }
+                    done += n;
+                    page_ctr += n;  // pages issued so far
                 }
                 ids = ids_next;
             }
             A = Bt;
             idsA = idsB;
+            rowA = rowB;
         }
         if (lane == 0) {
             if (!ok) {
@@ -561,10 +792,28 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
         // Waits for the four consumer states of each item, merges them (each
         // lane 4 consecutive dims of one head at a time) and writes the final
         // output or the split-K partials, then frees the buffer.
+        //
+        // Fused combine: a split item's partials must be visible (a fence)
+        // before it is counted in its sequence-head group, and the count's
+        // result decides whether this item combines the group.  Both are
+        // memory round trips, so split items are queued (lane k holds entry
+        // k) and counted in batches - one fence, up to 32 counts in flight -
+        // whenever the next item's states are not ready yet, the queue is
+        // full, or the consumers are done.
+        constexpr int kMaxPend = 8;
+        int pend_b = 0, pend_g = 0, pend_np = 0, npend = 0;
+        auto flush = [&]() {
+            if (npend == 0) return;
+            count_and_combine<T, D, G>(p, lane, pend_b, pend_g, pend_np, npend);
+            npend = 0;
+        };
         for (uint32_t item_ctr = 0;; ++item_ctr) {
-            const int buf = item_ctr & 1;
+            const int buf = item_ctr % C::kMergeBufs;
             unsigned char *mb = smem + C::kCombOff + buf * C::kCombBytes;
-            if (!mbar_wait_bounded(&merged[buf], (item_ctr >> 1) & 1, kWaitLimitNs)) {
+            const uint32_t mpar = (item_ctr / C::kMergeBufs) & 1;
+            if (npend > 0 && !__shfl_sync(0xffffffffu, mbar_test_wait(&merged[buf], mpar), 0))
+                flush();  // idle until the next item: count the queued ones now
+            if (!mbar_wait_bounded(&merged[buf], mpar, kWaitLimitNs)) {
                 if (lane == 0) {
                     raise_flag(p.err_flag, XS_FLAG_TIMEOUT);
                     atomicExch(&s_abort, 1);
@@ -628,9 +877,19 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
                     }
                 }
             }
+            // The merge buffer is read: hand it back before any combine.
             __syncwarp();
             if (lane == 0) mbar_arrive(&freed[buf]);
+            if (valid && !single && p.combine) {
+                if (lane == npend) {
+                    pend_b = it.b;
+                    pend_g = it.g;
+                    pend_np = it.nparts;
+                }
+                if (++npend == kMaxPend) flush();
+            }
         }
+        if (!*static_cast<volatile int *>(&s_abort)) flush();
         return;
     }
 
@@ -708,12 +967,13 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
             atomicExch(&s_abort, 1);
         }
 
-        // ---- hand this warp's state to the merger (double-buffered by item
-        // parity; a buffer is reused once the merger has freed it).
-        const int buf = item_ctr & 1;
+        // ---- hand this warp's state to the merger (buffer item_ctr % kMergeBufs;
+        // a buffer is reused once the merger has freed it).
+        const int buf = item_ctr % C::kMergeBufs;
         unsigned char *mb = smem + C::kCombOff + buf * C::kCombBytes;
-        if (!__all_sync(0xffffffffu,
-                        mbar_wait_bounded(&freed[buf], ((item_ctr >> 1) & 1) ^ 1, kWaitLimitNs))) {
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(&freed[buf],
+                                                       ((item_ctr / C::kMergeBufs) & 1) ^ 1,
+                                                       kWaitLimitNs))) {
             if (lane == 0) {
                 raise_flag(p.err_flag, XS_FLAG_TIMEOUT);
                 atomicExch(&s_abort, 1);
@@ -916,6 +1176,37 @@ extern "C" int xs_paged_decode_partition_tokens(int B, int Hkv, int64_t total_co
     return best;
 }
 
+extern "C" int xs_paged_decode_step_partition_tokens(int B, int Hq, int Hkv,
+                                                     int64_t total_context_tokens,
+                                                     int max_context_len, int num_sms) {
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || max_context_len < 0 || num_sms <= 0)
+        return XS_ESHAPE;
+    if (B == 0) return 64;
+    const double tokens = total_context_tokens > 0
+                              ? static_cast<double>(total_context_tokens)
+                              : static_cast<double>(B) * std::max(max_context_len, 1);
+    // The cost model of xs_paged_decode_partition_tokens plus the in-launch
+    // combine: the groups that complete last are combined after every page
+    // is read, by one warp each, at about one memory round trip (~ one page
+    // time) per 16 partial rows (G heads per partial) plus three.
+    constexpr double kItemCost = 1.5;
+    const double ctas = 2.0 * num_sms;
+    const double G = static_cast<double>(Hq / Hkv);
+    int best = 64;
+    double best_cost = 1e300;
+    for (int P = 64; P <= 2048; P *= 2) {
+        const double items = std::max((tokens / P + 0.5 * B) * Hkv, static_cast<double>(B) * Hkv);
+        const double np_max = std::ceil(std::max(max_context_len, 1) / static_cast<double>(P));
+        const double combine = np_max > 1.0 ? np_max * G / 16.0 + 3.0 : 0.0;
+        const double cost = (items / ctas + 1.0) * (P / 64.0 + kItemCost) + combine;
+        if (cost <= best_cost * (1.0 + 1e-9)) {
+            best_cost = cost;
+            best = P;
+        }
+    }
+    return best;
+}
+
 extern "C" int xs_paged_decode_max_partitions(int max_blocks_per_seq, int block_size,
                                               int partition_tokens) {
     if (max_blocks_per_seq < 0 || block_size <= 0 || partition_tokens <= 0) return XS_ESHAPE;
@@ -957,7 +1248,8 @@ static int launch_attn(void *out, float *part_o, float *part_m, float *part_l, c
                        int Hkv, int D, int block_size, int64_t num_blocks, float scale,
                        const void *sinks, int window, int partition_tokens, int max_partitions,
                        int dtype, int *err_flag, int *work_counters, cudaStream_t stream,
-                       int prefill_start = -1) {
+                       int prefill_start = -1, const void *k_new = nullptr,
+                       const void *v_new = nullptr, int *combine = nullptr) {
     if (window < 0) return XS_ESHAPE;
     const bool prefill = prefill_start >= 0;
     int st = check_attn_args(out, part_o, part_m, part_l, q, k_cache, v_cache, block_tables,
@@ -1001,6 +1293,9 @@ static int launch_attn(void *out, float *part_o, float *part_m, float *part_l, c
     p.table_stride = prefill ? 0 : max_blocks_per_seq;
     p.err_flag = err_flag;
     p.work = work_counters;
+    p.k_new = k_new;
+    p.v_new = v_new;
+    p.combine = combine;
     fn<<<grid, attn::kThreads, smem, stream>>>(p);
     return launch_status();
 }
@@ -1111,6 +1406,35 @@ extern "C" int xs_paged_decode_sinks(void *out, float *part_o, float *part_m, fl
     if (st != XS_OK || max_partitions <= 1) return st;
     return xs_paged_decode_reduce_sinks(out, part_o, part_m, part_l, context_lens, sinks, window,
                                         B, Hq, D, partition_tokens, max_partitions, dtype, stream);
+}
+
+// ---------------------------------------------------------------- fused decode step
+//
+// Append + attention + split-K combine in one launch; see the header for the
+// contract.  counters = [item counter, finished-CTA counter, B * Hkv combine
+// counts], all zero between launches.
+
+extern "C" int xs_paged_decode_step(void *out, const void *q, const void *k_new,
+                                    const void *v_new, void *k_cache, void *v_cache,
+                                    const int32_t *block_tables, int max_blocks_per_seq,
+                                    const int32_t *context_lens, const void *sinks, int window,
+                                    int B, int Hq, int Hkv, int D, int block_size,
+                                    int64_t num_blocks, float scale, int partition_tokens,
+                                    int max_partitions, float *part_o, float *part_m,
+                                    float *part_l, int *counters, int dtype, int *err_flag,
+                                    cudaStream_t stream) {
+    if (!k_new != !v_new) return XS_ENULL;
+    if (!counters) return XS_EWORKSPACE;
+    if (k_new && (!aligned16(k_new) || !aligned16(v_new))) return XS_EALIGN;
+    return launch_attn(out, part_o, part_m, part_l, q, k_cache, v_cache, block_tables,
+                       max_blocks_per_seq, context_lens, B, Hq, Hkv, D, block_size, num_blocks,
+                       scale, sinks, window, partition_tokens, max_partitions, dtype, err_flag,
+                       counters, stream, -1, k_new, v_new, counters + 2);
+}
+
+extern "C" int64_t xs_paged_decode_step_counters(int B, int Hkv) {
+    if (B < 0 || Hkv <= 0) return XS_ESHAPE;
+    return 2 + static_cast<int64_t>(B) * Hkv;
 }
 
 // ---------------------------------------------------------------- chunked prefill

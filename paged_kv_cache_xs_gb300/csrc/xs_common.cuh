@@ -62,6 +62,25 @@ __device__ __forceinline__ void mbar_fence_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 
+// atomicAdd(ptr, v) on the threads where pred holds (returning the old
+// value; 0 elsewhere) as one predicated instruction, so no branch forces the
+// warp to wait for the result before it is used.
+__device__ __forceinline__ int atomic_add_if(int *ptr, int v, bool pred) {
+    int old = 0;
+    asm volatile(
+        "{\n .reg .pred q;\n setp.ne.u32 q, %2, 0;\n @q atom.global.add.u32 %0, [%1], %3;\n}"
+        : "+r"(old)
+        : "l"(ptr), "r"(static_cast<uint32_t>(pred)), "r"(v)
+        : "memory");
+    return old;
+}
+
+// Orders this thread's earlier generic-proxy writes to global memory before
+// later async-proxy operations (bulk copies) that read the same memory.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
     asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar))
                  : "memory");
@@ -79,6 +98,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     asm volatile(
         "{\n .reg .pred p;\n"
         " mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Non-blocking test of a phase (try_wait may suspend the thread for a while).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n"
+        " mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
         " selp.u32 %0, 1, 0, p;\n}"
         : "=r"(ok)
         : "r"(smem_addr(bar)), "r"(parity)

@@ -61,6 +61,10 @@ SIGNATURES = {
     "xs_paged_prefill_reduce": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P]),
     "xs_paged_prefill": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _L, _F,
                               _I, _I, _I, _P, _P, _P]),
+    "xs_paged_decode_step": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I,
+                                  _I, _L, _F, _I, _I, _P, _P, _P, _P, _I, _P, _P]),
+    "xs_paged_decode_step_counters": (_L, [_I, _I]),
+    "xs_paged_decode_step_partition_tokens": (_I, [_I, _I, _I, _L, _I, _I]),
     "xs_version": (_I, []),
 }
 
@@ -163,6 +167,15 @@ def xs_paged_decode_partition_tokens(B, Hkv, total_context_tokens, max_context_l
     return r
 
 
+def xs_paged_decode_step_partition_tokens(B, Hq, Hkv, total_context_tokens, max_context_len,
+                                          num_sms) -> int:
+    r = load().xs_paged_decode_step_partition_tokens(B, Hq, Hkv, total_context_tokens,
+                                                     max_context_len, num_sms)
+    if r < 0:
+        raise XsError("xs_paged_decode_step_partition_tokens", r)
+    return r
+
+
 def xs_paged_decode_max_partitions(max_blocks_per_seq, block_size, partition_tokens) -> int:
     r = load().xs_paged_decode_max_partitions(max_blocks_per_seq, block_size, partition_tokens)
     if r < 0:
@@ -204,6 +217,28 @@ def xs_paged_decode(out, part_o, part_m, part_l, q, k_cache, v_cache, block_tabl
           _ptr(context_lens), B, Hq, Hkv, D, bs, num_blocks, float(scale), partition_tokens,
           max_partitions, dtype_code(q.dtype), _ptr(err_flag), _ptr(work_counters),
           _stream(stream))
+
+
+def xs_paged_decode_step(out, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens,
+                         scale, partition_tokens, max_partitions, part_o, part_m, part_l,
+                         counters, sinks=None, window=0, err_flag=None, stream=None):
+    """The whole decode step in one launch: append k_new/v_new ([B, Hkv, D],
+    or both None), attend, combine the split-K partials.  ``counters`` holds
+    xs_paged_decode_step_counters(B, Hkv) int32 zeros (left zero)."""
+    B, Hq, D = q.shape
+    num_blocks, Hkv, bs, _ = k_cache.shape
+    _call("xs_paged_decode_step", _ptr(out), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache),
+          _ptr(v_cache), _ptr(block_tables), block_tables.shape[1], _ptr(context_lens),
+          _ptr(sinks), int(window), B, Hq, Hkv, D, bs, num_blocks, float(scale),
+          partition_tokens, max_partitions, _ptr(part_o), _ptr(part_m), _ptr(part_l),
+          _ptr(counters), dtype_code(q.dtype), _ptr(err_flag), _stream(stream))
+
+
+def xs_paged_decode_step_counters(B: int, Hkv: int) -> int:
+    n = load().xs_paged_decode_step_counters(B, Hkv)
+    if n < 0:
+        raise XsError("xs_paged_decode_step_counters", n)
+    return n
 
 
 def xs_paged_decode_noalloc(out, q, k_cache, v_cache, block_tables, context_lens, scale,
@@ -312,23 +347,35 @@ def xs_version() -> int:
 class DecodeWorkspace:
     """Split-K partials sized for a batch shape, allocated once through PyTorch.
 
-    ``partition_tokens`` comes from the library's heuristic unless given."""
+    ``partition_tokens`` comes from the library's heuristic unless given: the
+    one for the one-launch step (``fused``, the default) or the one for the
+    separate attention + combine calls."""
 
     def __init__(self, B: int, Hq: int, Hkv: int, D: int, max_blocks_per_seq: int,
                  device, total_context_tokens: int = 0, max_context_len: int | None = None,
-                 partition_tokens: int | None = None, num_sms: int | None = None):
+                 partition_tokens: int | None = None, num_sms: int | None = None,
+                 fused: bool = True):
         device = torch.device(device)
         if num_sms is None:
             num_sms = torch.cuda.get_device_properties(device).multi_processor_count
         if max_context_len is None:
             max_context_len = max_blocks_per_seq * BLOCK_SIZE
-        self.partition_tokens = partition_tokens or xs_paged_decode_partition_tokens(
-            B, Hkv, total_context_tokens, max_context_len, num_sms)
+        if partition_tokens:
+            self.partition_tokens = partition_tokens
+        elif fused:
+            self.partition_tokens = xs_paged_decode_step_partition_tokens(
+                B, Hq, Hkv, total_context_tokens, max_context_len, num_sms)
+        else:
+            self.partition_tokens = xs_paged_decode_partition_tokens(
+                B, Hkv, total_context_tokens, max_context_len, num_sms)
         self.max_partitions = xs_paged_decode_max_partitions(max_blocks_per_seq, BLOCK_SIZE,
                                                              self.partition_tokens)
         n = B * Hq * self.max_partitions
-        # Work counters for the dynamic item scheduler (zero between launches).
-        self.work = torch.zeros(2, dtype=torch.int32, device=device)
+        # Counters, zero between launches: the dynamic item scheduler's two,
+        # then the fused step's per-(sequence, KV head) combine counts.  The
+        # separate attention calls use the first two.
+        self.work = torch.zeros(xs_paged_decode_step_counters(B, Hkv), dtype=torch.int32,
+                                device=device)
         if self.max_partitions > 1:
             self.part_o = torch.empty(n * D, dtype=torch.float32, device=device)
             self.part_m = torch.empty(n, dtype=torch.float32, device=device)

@@ -1,15 +1,17 @@
 """One continuous-batching decode step over a paged KV cache.
 
 ``PagedDecodeStep`` owns nothing but the split-K workspace; the KV pools,
-block tables and lengths belong to the caller.  ``run`` enqueues, on the
-current stream:
+block tables and lengths belong to the caller.  A step is
 
-1. ``xs_kv_append_paged``  - slot resolution + KV append (the pages'
-   reshape_and_cache_batched_bf16, "xserv compare phase10...cf1e9e4",
-   attention.rs);
-2. ``xs_paged_decode_attn`` - paged decode attention, split-K partitions;
-3. ``xs_paged_decode_reduce`` - split-K combine (only when a sequence can
-   span several partitions).
+1. slot resolution + KV append (the pages' reshape_and_cache_batched_bf16,
+   "xserv compare phase10...cf1e9e4", attention.rs);
+2. paged decode attention over split-K partitions;
+3. the split-K combine (only when a sequence can span several partitions).
+
+``run`` enqueues all three as one launch (``xs_paged_decode_step``);
+``run_unfused`` enqueues them as the separate calls ``xs_kv_append_paged``,
+``xs_paged_decode_attn`` and ``xs_paged_decode_reduce`` (``append``,
+``attend`` and ``reduce`` below).
 
 ``run_from_host`` is the same step fed from pinned host buffers: it copies
 the step's inputs to the device, runs the step and copies the output back.
@@ -23,11 +25,14 @@ from . import ops
 
 class PagedDecodeStep:
     """sinks ([Hq] tensor of q's dtype, or None) and window (0 = all tokens)
-    select the gpt-oss variant: per-head sink logits and a sliding window."""
+    select the gpt-oss variant: per-head sink logits and a sliding window.
+    ``fused`` picks the partition heuristic for ``run`` (True) or for
+    ``run_unfused`` (False); both forms work with either."""
 
     def __init__(self, B: int, Hq: int, Hkv: int, D: int, max_blocks_per_seq: int, dtype,
                  device, total_context_tokens: int = 0, max_context_len: int | None = None,
-                 partition_tokens: int | None = None, sinks=None, window: int = 0):
+                 partition_tokens: int | None = None, sinks=None, window: int = 0,
+                 fused: bool = True):
         self.B, self.Hq, self.Hkv, self.D = B, Hq, Hkv, D
         self.sinks, self.window = sinks, int(window)
         self.dtype = dtype
@@ -36,7 +41,7 @@ class PagedDecodeStep:
         self.ws = ops.DecodeWorkspace(B, Hq, Hkv, D, max_blocks_per_seq, self.device,
                                       total_context_tokens=total_context_tokens,
                                       max_context_len=max_context_len,
-                                      partition_tokens=partition_tokens)
+                                      partition_tokens=partition_tokens, fused=fused)
         self.err_flag = torch.zeros(1, dtype=torch.int32, device=self.device)
         self._dev_inputs = None
 
@@ -48,8 +53,9 @@ class PagedDecodeStep:
     def max_partitions(self) -> int:
         return self.ws.max_partitions
 
-    @property
-    def launches_per_step(self) -> int:
+    def launches_per_step(self, fused: bool = True) -> int:
+        if fused:
+            return 1
         return 3 if self.ws.max_partitions > 1 else 2
 
     def append(self, k_new, v_new, k_cache, v_cache, block_tables, context_lens):
@@ -83,7 +89,18 @@ class PagedDecodeStep:
                                              sinks=self.sinks, window=self.window)
 
     def run(self, out, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, scale):
-        """Append this step's K/V, then attend; all tensors on the device."""
+        """Append this step's K/V, attend and combine in one launch; all
+        tensors on the device."""
+        ws = self.ws
+        ops.xs_paged_decode_step(out, q, k_new, v_new, k_cache, v_cache, block_tables,
+                                 context_lens, scale, ws.partition_tokens, ws.max_partitions,
+                                 ws.part_o, ws.part_m, ws.part_l, ws.work, sinks=self.sinks,
+                                 window=self.window, err_flag=self.err_flag)
+        return out
+
+    def run_unfused(self, out, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens,
+                    scale):
+        """The same step as three launches: append, attention, combine."""
         self.append(k_new, v_new, k_cache, v_cache, block_tables, context_lens)
         self.attend(out, q, k_cache, v_cache, block_tables, context_lens, scale)
         self.reduce(out, context_lens)

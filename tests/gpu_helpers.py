@@ -76,10 +76,11 @@ def max_abs(out: torch.Tensor, ref: torch.Tensor) -> float:
     return (out.detach().cpu().double() - ref).abs().max().item()
 
 
-def check_step(w, layer, step, seqs=None, check_unchanged=True, strict=True):
+def check_step(w, layer, step, seqs=None, check_unchanged=True, strict=True, fused=True):
     """Run one decode step (append + attention) of layer `layer` through the
-    CUDA path and compare it with the oracle on the sequences `seqs`.
-    Returns the attention max-abs error."""
+    CUDA path - as one fused launch, or as the three separate calls - and
+    compare it with the oracle on the sequences `seqs`.  Returns the
+    attention max-abs error."""
     cfg = w.cfg
     seqs = list(range(cfg.B)) if seqs is None else list(seqs)
     kc, vc = w.k_cache[layer], w.v_cache[layer]
@@ -88,10 +89,12 @@ def check_step(w, layer, step, seqs=None, check_unchanged=True, strict=True):
     before_v = vc.clone() if check_unchanged else None
     out = torch.empty(cfg.B, cfg.Hq, cfg.D, dtype=cfg.dtype, device=kc.device)
     step.err_flag.zero_()
-    step.run(out, w.q[layer], w.k_new[layer], w.v_new[layer], kc, vc, w.block_tables,
-             w.context_lens, w.scale)
+    run = step.run if fused else step.run_unfused
+    run(out, w.q[layer], w.k_new[layer], w.v_new[layer], kc, vc, w.block_tables,
+        w.context_lens, w.scale)
     torch.cuda.synchronize()
     assert step.error_flags() == 0, f"device error flag {step.error_flags()}"
+    assert int(step.ws.work.count_nonzero()) == 0, "counters not left at zero"
 
     # Append: bit-exact against the oracle's append of the same pre-state.
     sel = torch.tensor(seqs, dtype=torch.long, device=kc.device)

@@ -24,7 +24,7 @@ def declared_functions():
     names = set()
     for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
         text = open(h).read()
-        names.update(re.findall(r"^(?:int|size_t|void)\s+(xs_\w+)\s*\(", text, flags=re.M))
+        names.update(re.findall(r"^(?:int|int64_t|size_t|void)\s+(xs_\w+)\s*\(", text, flags=re.M))
     return sorted(names)
 
 
@@ -132,3 +132,30 @@ def test_binding_raises_on_error_code(lib):
     with pytest.raises(ops.XsError) as e:
         ops._call("xs_slot_mapping", None, 4, A, 3, 16, 10, A, None, None)
     assert e.value.code == -1
+
+
+def _fused(lib, **kw):
+    a = dict(out=A, q=A, kn=A, vn=A, k=A, v=A, bt=A, maxb=4, lens=A, sinks=None, window=0, B=2,
+             Hq=8, Hkv=2, D=128, bs=16, nb=10, scale=0.1, P=16, maxp=4, po=A, pm=A, pl=A,
+             counters=A, dtype=1, err=None, stream=None)
+    a.update(kw)
+    return lib.xs_paged_decode_step(a["out"], a["q"], a["kn"], a["vn"], a["k"], a["v"], a["bt"],
+                                    a["maxb"], a["lens"], a["sinks"], a["window"], a["B"],
+                                    a["Hq"], a["Hkv"], a["D"], a["bs"], a["nb"], a["scale"],
+                                    a["P"], a["maxp"], a["po"], a["pm"], a["pl"],
+                                    a["counters"], a["dtype"], a["err"], a["stream"])
+
+
+def test_fused_step_argument_validation(lib):
+    assert _fused(lib, B=0) == 0                     # nothing to do, nothing launched
+    assert _fused(lib, counters=None) == -6
+    assert _fused(lib, kn=None) == -1                # k_new and v_new: both or neither
+    assert _fused(lib, vn=None) == -1
+    assert _fused(lib, kn=A + 4) == -4
+    assert _fused(lib, window=-1) == -2
+    assert _fused(lib, maxp=3) == -6
+    assert _fused(lib, po=None) == -6
+    assert _fused(lib, D=96) == -5
+    assert _fused(lib, lens=None) == -1
+    assert ops.xs_paged_decode_step_counters(128, 8) == 2 + 128 * 8
+    assert lib.xs_paged_decode_step_counters(-1, 8) == -2

@@ -4,7 +4,8 @@ Configs 0-3 are checked on every sequence and every layer.  Config 4 (128
 sequences, contexts up to 32769 tokens, ~17 GB pool) runs in the launch
 configuration the benchmark times and is checked on 8 sampled sequences
 (including the longest and shortest) with all of their heads; its append is
-checked on every sequence (bytes at the new slots, nothing else touched)."""
+checked on every sequence (bytes at the new slots, nothing else touched).
+Each runs both as the one-launch fused step and as three separate launches."""
 import pytest
 import torch
 
@@ -22,16 +23,19 @@ def _step_for(w, dev):
                            max_context_len=w.max_context_len)
 
 
+@pytest.mark.parametrize("fused", [True, False], ids=["one-launch", "three-launch"])
 @pytest.mark.parametrize("cfg_id", [0, 1, 2, 3])
-def test_config_all_sequences(cfg_id):
+def test_config_all_sequences(cfg_id, fused):
     dev = gh.device()
     w = wl.make_workload(cfg_id, device=dev)
     step = _step_for(w, dev)
-    errs = [gh.check_step(w, layer, step) for layer in range(w.cfg.layers)]
-    print(f"{w.cfg.name}: P={step.partition_tokens} max err {max(errs):.3e}")
+    errs = [gh.check_step(w, layer, step, fused=fused) for layer in range(w.cfg.layers)]
+    print(f"{w.cfg.name}: P={step.partition_tokens} fused={fused} max err {max(errs):.3e}")
 
 
 def test_config4_sampled():
+    # Both forms of the step, one after the other on the same workload: the
+    # second appends the same rows again, so its pre-state is the first's result.
     dev = gh.device()
     w = wl.make_workload(4, device=dev)
     step = _step_for(w, dev)
@@ -39,6 +43,7 @@ def test_config4_sampled():
     g = torch.Generator().manual_seed(4)
     pick = set(torch.randperm(w.cfg.B, generator=g)[:6].tolist())
     pick |= {int(lens.argmax()), int(lens.argmin())}
-    err = gh.check_step(w, 0, step, seqs=sorted(pick), check_unchanged=True)
-    print(f"{w.cfg.name}: P={step.partition_tokens} parts<={step.max_partitions} "
-          f"sampled max err {err:.3e}")
+    for fused in (True, False):
+        err = gh.check_step(w, 0, step, seqs=sorted(pick), check_unchanged=True, fused=fused)
+        print(f"{w.cfg.name}: P={step.partition_tokens} parts<={step.max_partitions} "
+              f"fused={fused} sampled max err {err:.3e}")

@@ -71,7 +71,7 @@ def test_dynamic_scheduler_counters_reset():
     for _ in range(4):
         outs.append(_attend(w, 0, 128, dynamic=True, ws=ws))
     torch.cuda.synchronize()
-    assert ws.work.tolist() == [0, 0]
+    assert int(ws.work.count_nonzero()) == 0
     for out in outs:
         gh.assert_close(out, ref, torch.bfloat16)
 
