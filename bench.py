@@ -342,17 +342,23 @@ def run_ours(args, rank, world, local, dist):
                 ev[layer][1].record(cur)
             step.reduce(out[layer], w.context_lens)
 
+    fused = args.fused == "on"
+    # A multi-layer step replays as one CUDA graph (CapturedStep), its
+    # launches chained by programmatic dependent launch; a one-layer step is
+    # launched directly, where consecutive steps chain the same way.
     use_graph = args.graph == "on" or (args.graph == "auto" and L > 1)
     graph = None
     graph_ev = None
     if use_graph:
-        # One CUDA graph per step (all layers); attention launches are
-        # bracketed by event-record nodes so their device time is measured.
-        try:
-            graph_ev = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)]
-                        for _ in range(L)]
-        except TypeError:  # a torch without external events: time the graph only
-            graph_ev = None
+        # One CUDA graph per step (all layers).  In the three-launch form the
+        # attention launches are bracketed by event-record nodes so their
+        # device time is measured; the one-launch step is timed whole.
+        if not fused:
+            try:
+                graph_ev = [[torch.cuda.Event(enable_timing=True, external=True)
+                             for _ in range(2)] for _ in range(L)]
+            except TypeError:  # a torch without external events: time the graph only
+                graph_ev = None
         graph = CapturedStep(lambda: one_step(graph_ev))
 
     def run_step(ev=None):
@@ -373,7 +379,9 @@ def run_ours(args, rank, world, local, dist):
         torch.cuda.synchronize()
 
     # ---- timed region: exactly K steps
-    attn_ev = None if graph is not None else [
+    # Per-launch events only where the step has several kernels: the one-launch
+    # step's kernel time is the timed region over steps x layers launches.
+    attn_ev = None if (graph is not None or fused) else [
         [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(L)]
         for _ in range(args.steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -432,7 +440,7 @@ def run_ours(args, rank, world, local, dist):
     peak, peak_kind = hbm_peak()
     attn_avg_ms = statistics.mean(attn_ms)
     # The fused launch also appends the new rows and writes the output.
-    launch_bytes = by["step"] if args.fused == "on" else by["attn"]
+    launch_bytes = by["step"] if fused else by["attn"]
     attn_gbs = launch_bytes / (attn_avg_ms * 1e-3) / 1e9
     traffic = kernel_traffic(cfg.name)
     line = {
@@ -470,9 +478,9 @@ def run_ours(args, rank, world, local, dist):
                      "avg_launch_ms": round(attn_avg_ms, 4)},
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_s * 1e3, 4)},
-        "gpu_launches": args.steps * L * step.launches_per_step(args.fused == "on"),
+        "gpu_launches": args.steps * L * step.launches_per_step(fused),
         "cuda_graph": graph is not None,
-        "fused_step": args.fused == "on",
+        "fused_step": fused,
         "clocks": clock_info,
     }
     if not args.no_cpu_baseline:

@@ -351,8 +351,9 @@ __device__ __forceinline__ void consume_page(const unsigned char *Ks, const unsi
 //     out = sum_j 2^(m_j - M) l_j o_j / (sum_j 2^(m_j - M) l_j [+ sink term])
 // with M = max_j m_j, over the nparts partials (o_j already divided by l_j).
 // The partials were written by other CTAs of this launch: read through L2.
-// All G heads go together and every batch of loads is issued before any is
-// used, so a group costs a few L2 round trips, not a few per head.
+// Lane j holds m and l of partials j, j + 32, ... (one load round for up to
+// 32 partials), the weights reach the other lanes by shuffles, and the
+// partial rows are loaded 16 at a time, all G heads together.
 template <typename T, int D, int G>
 __device__ __noinline__ void combine_partials(const Params &p, const Item &it, int64_t head0,
                                               int lane) {
@@ -362,61 +363,65 @@ __device__ __noinline__ void combine_partials(const Params &p, const Item &it, i
     const int np = it.nparts;
     const float *pm = p.part_m + head0 * p.max_parts;
     const float *pl = p.part_l + head0 * p.max_parts;
-    // Max and denominator per head (lanes stride over the partials).
-    float mx[G], den[G];
+    const float *po = p.part_o + head0 * p.max_parts * D + lane * kDims;
+    float acc[G][kDims], den[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+        den[h] = 0.f;
+#pragma unroll
+        for (int d = 0; d < kDims; ++d) acc[h][d] = 0.f;
+    }
+    // Maximum per head over all partials.
+    float mx[G];
 #pragma unroll
     for (int h = 0; h < G; ++h) mx[h] = -INFINITY;
     for (int j = lane; j < np; j += 32)
 #pragma unroll
         for (int h = 0; h < G; ++h) mx[h] = fmaxf(mx[h], __ldcg(pm + h * p.max_parts + j));
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
+    for (int h = 0; h < G; ++h)
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], o));
-        den[h] = 0.f;
-    }
-    for (int j = lane; j < np; j += 32)
+    for (int j0 = 0; j0 < np; j0 += 32) {
+        // Weights of partials j0 .. j0 + 31, partial j0 + k in lane k.
+        float wgt[G];
 #pragma unroll
-        for (int h = 0; h < G; ++h)
-            den[h] += fast_exp2(__ldcg(pm + h * p.max_parts + j) - mx[h]) *
-                      __ldcg(pl + h * p.max_parts + j);
-    // Weighted sum of the partial outputs; each lane re-reads the (broadcast)
-    // m and l of the partials it weights.
-    float acc[G][kDims];
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) den[h] += __shfl_xor_sync(0xffffffffu, den[h], o);
-#pragma unroll
-        for (int d = 0; d < kDims; ++d) acc[h][d] = 0.f;
-    }
-    const float *po = p.part_o + head0 * p.max_parts * D + lane * kDims;
-    for (int j0 = 0; j0 < np; j0 += kJ) {
-        Vec v[kJ][G];
-        float wm[kJ][G], wl[kJ][G];
-#pragma unroll
-        for (int u = 0; u < kJ; ++u)
-#pragma unroll
-            for (int h = 0; h < G; ++h) {
-                const int j = min(j0 + u, np - 1);  // past the end: reload the last, weight 0
-                const int64_t r = static_cast<int64_t>(h) * p.max_parts + j;
-                v[u][h] = __ldcg(reinterpret_cast<const Vec *>(po + r * D));
-                wm[u][h] = __ldcg(pm + r);
-                wl[u][h] = __ldcg(pl + r);
+        for (int h = 0; h < G; ++h) {
+            wgt[h] = 0.f;
+            if (j0 + lane < np) {
+                const int64_t r = static_cast<int64_t>(h) * p.max_parts + j0 + lane;
+                wgt[h] = fast_exp2(__ldcg(pm + r) - mx[h]) * __ldcg(pl + r);
             }
+            den[h] += wgt[h];
+        }
+        const int cnt = min(32, np - j0);
+        for (int k0 = 0; k0 < cnt; k0 += kJ) {
+            Vec v[kJ][G];
 #pragma unroll
-        for (int u = 0; u < kJ; ++u)
+            for (int u = 0; u < kJ; ++u)
 #pragma unroll
-            for (int h = 0; h < G; ++h) {
-                const float w = j0 + u < np ? fast_exp2(wm[u][h] - mx[h]) * wl[u][h] : 0.f;
-                const float *f = reinterpret_cast<const float *>(&v[u][h]);
+                for (int h = 0; h < G; ++h) {
+                    const int k = min(k0 + u, cnt - 1);  // past the end: reload, weight 0
+                    v[u][h] = __ldcg(reinterpret_cast<const Vec *>(
+                        po + (static_cast<int64_t>(h) * p.max_parts + j0 + k) * D));
+                }
 #pragma unroll
-                for (int d = 0; d < kDims; ++d) acc[h][d] += w * f[d];
-            }
+            for (int u = 0; u < kJ; ++u)
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+                    const float w0 = __shfl_sync(0xffffffffu, wgt[h], (k0 + u) & 31);
+                    const float w = k0 + u < cnt ? w0 : 0.f;
+                    const float *f = reinterpret_cast<const float *>(&v[u][h]);
+#pragma unroll
+                    for (int d = 0; d < kDims; ++d) acc[h][d] += w * f[d];
+                }
+        }
     }
 #pragma unroll
     for (int h = 0; h < G; ++h) {
         float lt = den[h];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) lt += __shfl_xor_sync(0xffffffffu, lt, o);
         if (p.sinks)
             lt += fast_exp2(Elem<T>::to_f32(static_cast<const T *>(p.sinks)[it.g * G + h]) * kLog2e -
                             mx[h]);
@@ -501,6 +506,13 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
         mbar_fence_init();
         s_abort = 0;
     }
+    // Programmatic dependent launch: the next launch on the stream may start
+    // placing its CTAs as ours exit (all of ours are resident by now), and
+    // this launch reads nothing in global memory before the previous one has
+    // completed and its writes are visible.  (Both are no-ops in a launch
+    // made without the attribute.)
+    griddep_launch_dependents();
+    griddep_wait();
     {
         // Per sequence: nw/P full partitions and (nw % P != 0) ragged one, each
         // x Hkv heads (nw = tokens inside the window).  Chunked scan of both
@@ -1296,7 +1308,20 @@ static int launch_attn(void *out, float *part_o, float *part_m, float *part_l, c
     p.k_new = k_new;
     p.v_new = v_new;
     p.combine = combine;
-    fn<<<grid, attn::kThreads, smem, stream>>>(p);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(attn::kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, fn, p) != cudaSuccess) {
+        cudaGetLastError();
+        return XS_ELAUNCH;
+    }
     return launch_status();
 }
 

@@ -105,6 +105,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Programmatic dependent launch (sm_90+): let the next grid on the stream be
+// scheduled, and wait until the previous grid has completed with its memory
+// writes visible.  Both return at once when the launch had no such dependency.
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Non-blocking test of a phase (try_wait may suspend the thread for a while).
 __device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
     uint32_t ok;
