@@ -66,6 +66,17 @@ def hbm_peak() -> tuple[float, str]:
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def bf16_peak(sustained: bool) -> tuple[float, str]:
+    """Dense bf16 tensor peak, TFLOP/s: the measured cuBLAS figure (burst for a
+    kernel timed alone, sustained for one timed inside a long loop)."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peaks = json.load(f)
+        return float(peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return (1700.0 if sustained else 1900.0), "fallback"
+
+
 def kernel_traffic(workload: str) -> int | None:
     """Per-launch DRAM bytes of the attention kernel from the committed ncu
     summary, if it was taken on the current kernel source."""
@@ -573,21 +584,33 @@ def run_prefill(args, rank, world, local, dist):
     vs = torch.randn(Hkv, total, D, generator=g, device=dev).to(dtype)
     q = torch.randn(total, Hq, D, generator=g, device=dev).to(dtype)
     wss = {}
+    tensor = args.prefill_impl == "tensor"
+    nchunks = (total + chunk - 1) // chunk
+    ks_c = [ks[:, s0:s0 + chunk].contiguous() for s0 in range(0, total, chunk)]
+    vs_c = [vs[:, s0:s0 + chunk].contiguous() for s0 in range(0, total, chunk)]
+    out = torch.empty(total, Hq, D, dtype=dtype, device=dev)
 
-    def prefill_all():
-        for start in range(0, total, chunk):
+    def prefill_all(ev=None):
+        for c, start in enumerate(range(0, total, chunk)):
             T = min(chunk, total - start)
-            ws = wss.get(T)
-            if ws is None:
-                ws = wss[T] = ops.DecodeWorkspace(T, Hq, Hkv, D, pages, dev,
-                                                  total_context_tokens=T * (start + T),
-                                                  max_context_len=total)
-            ops.xs_prefill_append(ks[:, start:start + T].contiguous(),
-                                  vs[:, start:start + T].contiguous(), kc, vc, ids, start)
-            out = torch.empty(T, Hq, D, dtype=dtype, device=dev)
-            ops.xs_paged_prefill(out, ws.part_o, ws.part_m, ws.part_l, q[start:start + T], kc, vc,
-                                 ids, start, D ** -0.5, ws.partition_tokens, ws.max_partitions,
-                                 work_counters=ws.work)
+            ops.xs_prefill_append(ks_c[c], vs_c[c], kc, vc, ids, start)
+            if ev is not None:
+                ev[c][0].record()
+            if tensor:
+                ops.xs_paged_prefill_tc(out[start:start + T], q[start:start + T], kc, vc, ids,
+                                        start, D ** -0.5)
+            else:
+                ws = wss.get(T)
+                if ws is None:
+                    ws = wss[T] = ops.DecodeWorkspace(T, Hq, Hkv, D, pages, dev,
+                                                      total_context_tokens=T * (start + T),
+                                                      max_context_len=total, fused=False)
+                ops.xs_paged_prefill(out[start:start + T], ws.part_o, ws.part_m, ws.part_l,
+                                     q[start:start + T], kc, vc, ids, start, D ** -0.5,
+                                     ws.partition_tokens, ws.max_partitions,
+                                     work_counters=ws.work)
+            if ev is not None:
+                ev[c][1].record()
 
     for _ in range(args.warmup):
         prefill_all()
@@ -599,11 +622,30 @@ def run_prefill(args, rank, world, local, dist):
     e1.record()
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / args.steps
+    # The attention launches alone, bracketed by events (one more pass).
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(nchunks)]
+    prefill_all(ev)
+    torch.cuda.synchronize()
+    attn_ms = sum(a.elapsed_time(b) for a, b in ev)
     if rank != 0:
         return
     # Causal attention flops: 4 * D per (query head, query token, key) pair.
     pairs = total * (total + 1) / 2
-    tflops = 4 * D * Hq * pairs / (ms * 1e-3) / 1e12
+    flop = 4 * D * Hq * pairs
+    tflops = flop / (ms * 1e-3) / 1e12
+    attn_tflops = flop / (attn_ms * 1e-3) / 1e12
+    if tensor:
+        peak, peak_kind = bf16_peak(sustained=False)
+        roof = {"kernel": "prefill_tc_kernel", "bound": "tensor", "achieved": round(attn_tflops, 1),
+                "peak": peak, "unit": "TFLOP/s", "frac": round(attn_tflops / peak, 4),
+                "peak_kind": peak_kind, "traffic": None,
+                "algorithmic_flop": flop, "attention_ms": round(attn_ms, 4),
+                "note": "bf16 mma.sync m16n8k16, fp32 accumulation; K/V pages by TMA"}
+    else:
+        roof = {"kernel": "paged_decode_kernel (prefill mode)", "bound": "alu",
+                "achieved": round(attn_tflops, 2), "unit": "TFLOP/s",
+                "attention_ms": round(attn_ms, 4),
+                "note": "fp32 CUDA-core FMA path (the decode kernel in prefill mode)"}
     line = {
         "metric": "chunked prefill attention over the paged cache (tokens/s, TFLOP/s)",
         "value": round(total / (ms * 1e-3), 1), "unit": "tokens/s", "n_gpus": world,
@@ -611,11 +653,10 @@ def run_prefill(args, rank, world, local, dist):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
         "config": {"workload": "qwen3_8b_prefill", "tokens": total, "chunk": chunk, "Hq": Hq,
-                   "Hkv": Hkv, "D": D},
+                   "Hkv": Hkv, "D": D, "impl": args.prefill_impl},
         "attention_tflops": round(tflops, 2),
-        "roofline": {"bound": "alu", "achieved": round(tflops, 2), "unit": "TFLOP/s",
-                     "note": "fp32 CUDA-core FMA path (the decode kernel in prefill mode)"},
-        "gpu_launches": args.steps * 2 * ((total + chunk - 1) // chunk),
+        "roofline": roof,
+        "gpu_launches": args.steps * nchunks * (2 if tensor else 3),
     }
     print(json.dumps(line), flush=True)
 
@@ -633,6 +674,8 @@ def main(argv=None):
                          "host; prefill: chunked prefill into the paged cache")
     ap.add_argument("--prefill-tokens", type=int, default=8192)
     ap.add_argument("--prefill-chunk", type=int, default=1024)
+    ap.add_argument("--prefill-impl", choices=["tensor", "cuda-core"], default="tensor",
+                    help="prefill attention: tensor-core kernel or the decode kernel in prefill mode")
     ap.add_argument("--swap-blocks", type=int, default=16384,
                     help="blocks per swap direction for --op swap")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -188,6 +188,25 @@ int xs_paged_prefill(void *out, float *part_o, float *part_m, float *part_l, con
                      int dtype, int *err_flag, int *work_counters, cudaStream_t stream);
 
 /*
+ * xs_paged_prefill_tc - the same causal chunk attention as xs_paged_prefill
+ * (q [T, Hq, D], out [T, Hq, D], block_ids [n_ids], row i at position
+ * start_pos + i over the cached prefix and the chunk), on the tensor cores,
+ * in one launch with no workspace: CTAs of 64 (query token, query head) rows
+ * of one KV group stream K/V pages through shared memory with TMA and
+ * compute Q K^T and P V with bf16 mma (fp32 accumulation; the softmax
+ * weights P enter P V rounded to bf16).  bf16 only (XS_F32 is
+ * XS_EUNSUPPORTED); D in {64, 128}; G = Hq / Hkv in {1, 2, 4, 8};
+ * num_blocks * Hkv * 16 + 16 < 2^31 (TMA row coordinates).  A block id
+ * outside the pool reads as zeros and raises XS_FLAG_BAD_BLOCK.  Errors
+ * otherwise as xs_paged_prefill; XS_EDEVICE if the driver's tensor-map
+ * encoder cannot be found.
+ */
+int xs_paged_prefill_tc(void *out, const void *q, const void *k_cache, const void *v_cache,
+                        const int32_t *block_ids, int n_ids, int T, int start_pos, int Hq,
+                        int Hkv, int D, int block_size, int64_t num_blocks, float scale,
+                        int dtype, int *err_flag, cudaStream_t stream);
+
+/*
  * xs_block_alloc_decode - the page allocation of one decode step, on the
  * device (the pages' PagedKVCache gives a sequence a new physical block when
  * its next token starts a page; "xserv compare phase10...cf1e9e4", the

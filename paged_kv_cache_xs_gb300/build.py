@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_NAME = "libxs_paged.so"
 LIB_PATH = os.path.join(BUILD_DIR, LIB_NAME)
-SOURCES = ["kv_append.cu", "paged_decode.cu", "kv_swap.cu", "block_alloc.cu"]
+SOURCES = ["kv_append.cu", "paged_decode.cu", "kv_swap.cu", "block_alloc.cu", "paged_prefill_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -61,6 +61,8 @@ SIGNATURES = {
     "xs_paged_prefill_reduce": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P]),
     "xs_paged_prefill": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _L, _F,
                               _I, _I, _I, _P, _P, _P]),
+    "xs_paged_prefill_tc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _L, _F, _I, _P,
+                                 _P]),
     "xs_paged_decode_step": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I,
                                   _I, _L, _F, _I, _I, _P, _P, _P, _P, _I, _P, _P]),
     "xs_paged_decode_step_counters": (_L, [_I, _I]),
@@ -232,6 +234,17 @@ def xs_paged_decode_step(out, q, k_new, v_new, k_cache, v_cache, block_tables, c
           _ptr(sinks), int(window), B, Hq, Hkv, D, bs, num_blocks, float(scale),
           partition_tokens, max_partitions, _ptr(part_o), _ptr(part_m), _ptr(part_l),
           _ptr(counters), dtype_code(q.dtype), _ptr(err_flag), _stream(stream))
+
+
+def xs_paged_prefill_tc(out, q, k_cache, v_cache, block_ids, start_pos, scale, err_flag=None,
+                        stream=None):
+    """Causal attention of a prefill chunk (q [T, Hq, D]) over the paged
+    cache on the tensor cores (bf16); one launch, no workspace."""
+    T, Hq, D = q.shape
+    num_blocks, Hkv, bs, _ = k_cache.shape
+    _call("xs_paged_prefill_tc", _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+          _ptr(block_ids), block_ids.numel(), T, int(start_pos), Hq, Hkv, D, bs, num_blocks,
+          float(scale), dtype_code(q.dtype), _ptr(err_flag), _stream(stream))
 
 
 def xs_paged_decode_step_counters(B: int, Hkv: int) -> int:

@@ -159,3 +159,17 @@ def test_fused_step_argument_validation(lib):
     assert _fused(lib, lens=None) == -1
     assert ops.xs_paged_decode_step_counters(128, 8) == 2 + 128 * 8
     assert lib.xs_paged_decode_step_counters(-1, 8) == -2
+
+
+def test_prefill_tc_argument_validation(lib):
+    f = lib.xs_paged_prefill_tc
+    #        out q  k  v  ids n_ids T start Hq Hkv D  bs nb  scale dtype err stream
+    assert f(A, A, A, A, A, 4, 0, 0, 8, 2, 128, 16, 10, 0.1, 1, None, None) == 0   # T == 0
+    assert f(None, A, A, A, A, 4, 8, 0, 8, 2, 128, 16, 10, 0.1, 1, None, None) == -1
+    assert f(A, A, A, A, A, 4, 8, 0, 8, 2, 128, 16, 10, 0.1, 0, None, None) == -5  # fp32
+    assert f(A, A, A, A, A, 4, 8, 0, 8, 2, 128, 16, 10, 0.1, 7, None, None) == -3
+    assert f(A, A, A, A, A, 4, 8, 0, 8, 3, 128, 16, 10, 0.1, 1, None, None) == -2  # Hq % Hkv
+    assert f(A, A, A, A, A, 4, 8, 0, 8, 2, 96, 16, 10, 0.1, 1, None, None) == -5
+    assert f(A, A, A, A, A, 4, 8, 0, 32, 2, 128, 16, 10, 0.1, 1, None, None) == -5  # G = 16
+    assert f(A, A, A, A, A, 4, 60, 10, 8, 2, 128, 16, 10, 0.1, 1, None, None) == -2  # past ids
+    assert f(A, A, A + 8, A, A, 4, 8, 0, 8, 2, 128, 16, 10, 0.1, 1, None, None) == -4
