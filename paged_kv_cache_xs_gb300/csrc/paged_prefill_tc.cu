@@ -1,28 +1,37 @@
-// Chunked-prefill attention on the tensor cores: a T-token chunk at positions
-// start_pos .. start_pos + T - 1 attends causally to every cached token of
-// its sequence, gathered through the chunk's block list ("xserv compare
-// phase10...cf1e9e4", attention.rs, attention / apply_causal_mask /
-// flash_attention: softmax(scale * Q K^T + causal mask) V with the mask
-// offset by the cached prefix).
+// Chunked-prefill attention on the 5th-generation tensor cores: a T-token
+// chunk at positions start_pos .. start_pos + T - 1 attends causally to every
+// cached token of its sequence, gathered through the chunk's block list
+// ("xserv compare phase10...cf1e9e4", attention.rs, attention /
+// apply_causal_mask / flash_attention: softmax(scale * Q K^T + causal mask) V
+// with the mask offset by the cached prefix).
 //
 // Design (flash-attention style, one pass, no split):
-//  * CTA = (64 query rows, KV head g).  A row is a (query token, query head)
-//    pair: the CTA takes 64 / G tokens x the G query heads of the group, so
-//    every K/V byte a CTA stages serves all G heads.  Four consumer warps own
-//    16 rows each; a fifth warp is the producer.
-//  * K and V go through shared memory in tiles of 64 keys (4 pages), a
-//    3-stage ring filled by TMA tensor copies: one 3-D copy per page, box
-//    [64 elements, 16 rows, D/64 halves] of a tensor map over the pool, with
-//    128-byte swizzle.  The layout that lands in shared memory is [half][row]
-//    of 128-byte lines, so the 8 rows of every 8x8 ldmatrix block sit in 8
-//    different bank groups.  Pages past the chunk's last key are requested at
-//    a row beyond the pool: TMA fills them with zeros.
-//  * S = Q K^T and O += P V with mma.sync m16n8k16 (bf16 in, fp32 accumulate);
-//    Q stays in registers as A fragments, K and V fragments come from
-//    ldmatrix (V transposed), and the S accumulators of two 8-key tiles are
-//    repacked in registers as the A fragment of P (bf16) for P V.
-//  * Online softmax in base 2 per row, causal mask per (row, key); the row
-//    sum is kept per lane and reduced over the quad at the end.
+//  * CTA = 128 query rows x one KV head g.  A row is a (query token, query
+//    head) pair: 128 / G tokens x the G query heads of the group, so every
+//    K/V byte a CTA stages serves all G heads.  Row r is TMEM lane r.
+//  * Warp 0 (TMA): Q once (one 3-D tensor copy per 64-wide D half, box
+//    [64, G heads, 128/G tokens]); then 64-key K/V tiles (4 pages) into a
+//    2-stage ring, one 3-D copy per page and D half from a tensor map over the
+//    pool.  Every box is 128-byte swizzled, so a D half of a tile is the
+//    canonical K-major layout (8-row groups 1024 B apart).  Pages past the
+//    last key are requested at a row beyond the pool and arrive as zeros.
+//  * Warp 1 (one thread): S = Q K^T with tcgen05.mma (M=128, N=64, K=16 per
+//    instruction, A and B from shared-memory descriptors, fp32 accumulators
+//    in TMEM columns 0-63); then O += P V (M=128, N=D) with P read from TMEM
+//    (A operand, columns 64-95) and V as an MN-major B descriptor (8-key
+//    groups 1024 B apart, D halves one tile-half apart); tcgen05.commit
+//    signals each step on an mbarrier.
+//  * Warps 2-5 (softmax; warp w reads TMEM lanes 32*(w%4)..+31, one row per
+//    thread): load the row of S, causal mask, row max, P = 2^(s - m) in base
+//    2, write P (bf16) back to TMEM for the P V step.  The reference m only
+//    moves when a tile's maximum exceeds it by more than 8 (log2 units), and
+//    only then is the row of O in TMEM rescaled, so P stays <= 2^8 and most
+//    tiles never touch O.  Unwritten slots of the last page (any bits at all)
+//    are zeroed in the staged V tile, since 0 * NaN = NaN.  At the end:
+//    O / l, bf16, out.
+//  * TMEM: 256 columns (S 64, P 32, O D), so two CTAs share an SM and one
+//    CTA's softmax overlaps the other's MMAs.  Every wait is bounded; the
+//    MMA thread waits for its last MMA before the CTA frees TMEM.
 #include <cuda.h>
 
 #include <algorithm>
@@ -35,57 +44,110 @@ namespace xs {
 namespace pftc {
 
 constexpr int kBlock = 16;
-constexpr int kConsumers = 4;
-constexpr int kThreads = 32 * (kConsumers + 1);
-constexpr int kKeys = 64;  // keys per tile
+constexpr int kRows = 128;               // M
+constexpr int kKeys = 64;                // keys per tile: N of Q K^T, K of P V
 constexpr int kPagesPerTile = kKeys / kBlock;
-constexpr int kStages = 3;
-constexpr int kRows = 16 * kConsumers;  // query rows per CTA
+constexpr int kStages = 2;
+constexpr int kThreads = 192;            // TMA warp, MMA warp, 4 softmax warps
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kColS = 0, kColP = 64, kColO = 128;
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kHeadroom = 8.f;         // log2 units P may exceed 1 before O is rescaled
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
 
 template <int D>
 struct TCfg {
     static constexpr int kHalves = D / 64;
-    static constexpr int kPageBytes = kBlock * D * 2;  // bf16
-    static constexpr int kTileBytes = kPagesPerTile * kPageBytes;
-    static constexpr int kStageBytes = 2 * kTileBytes;  // K tile, then V tile
-    static constexpr int kRingBytes = kStages * kStageBytes;
-    // ring (1024-aligned for the 128-byte swizzle) + barriers + alignment slack
-    static constexpr int kSmemBytes = kRingBytes + 2 * kStages * 8 + 1024;
+    static constexpr int kQHalf = kRows * 128;      // one 64-wide D half of Q
+    static constexpr int kQBytes = kHalves * kQHalf;
+    static constexpr int kKVHalf = kKeys * 128;     // one D half of a K or V tile
+    static constexpr int kTile = kHalves * kKVHalf;
+    static constexpr int kStageBytes = 2 * kTile;   // K tile, then V tile
+    static constexpr int kBarOff = kQBytes + kStages * kStageBytes;
+    static constexpr int kBarBytes = 16 * 8;
+    static constexpr int kSmemBytes = kBarOff + kBarBytes + 1024;  // + alignment slack
+    // Instruction descriptors (kind::f16): fp32 D, bf16 A and B, M = 128;
+    // Q K^T: both K-major, N = 64; P V: B (V) MN-major, N = D.
+    static constexpr uint32_t kIdS = (1u << 4) | (1u << 7) | (1u << 10) |
+                                     (static_cast<uint32_t>(kKeys >> 3) << 17) |
+                                     (static_cast<uint32_t>(kRows >> 4) << 24);
+    static constexpr uint32_t kIdPV = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) |
+                                      (static_cast<uint32_t>(D >> 3) << 17) |
+                                      (static_cast<uint32_t>(kRows >> 4) << 24);
 };
 
 struct PParams {
     __nv_bfloat16 *out;            // [T, Hq, D]
-    const __nv_bfloat16 *q;        // [T, Hq, D]
     const int32_t *block_ids;      // [n_ids]
-    int n_ids, T, start, Hq, Hkv;
+    int T, start, Hq, Hkv;
     int64_t num_blocks;
     int oob_row;                   // a row coordinate past the pool: zero-filled pages
     float qscale;                  // scale * log2(e)
     int *err_flag;
 };
 
-__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
-                                            uint32_t &r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
+// Shared-memory matrix descriptor: start, leading and stride byte offsets,
+// descriptor version 1, 128-byte swizzle.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+    return static_cast<uint64_t>((addr >> 4) & 0x3fff) |
+           (static_cast<uint64_t>((lbo >> 4) & 0x3fff) << 16) |
+           (static_cast<uint64_t>((sbo >> 4) & 0x3fff) << 32) | (1ull << 46) | (2ull << 61);
 }
-__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t addr, uint32_t &r0, uint32_t &r1,
-                                                  uint32_t &r2, uint32_t &r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
-}
-// d = a (16x16, row) * b (16x8, col) + d; bf16 inputs, fp32 accumulators.
-__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                         uint32_t b1) {
+__device__ __forceinline__ void umma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t id, int acc) {
     asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
-        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d),
+        "l"(a), "l"(b), "r"(id), "r"(acc));
+}
+__device__ __forceinline__ void umma_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t id,
+                                        int acc) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d),
+        "r"(a_tmem), "l"(b), "r"(id), "r"(acc));
+}
+__device__ __forceinline__ void umma_commit(uint64_t *bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_addr(bar))
+        : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// 32 consecutive TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+        "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+        "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(
+            taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+        "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+        "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -100,54 +162,73 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *tm,
         : "memory");
 }
 
-// Shared-memory address of (key, dims d .. d+7) in a tile staged by TMA:
-// page key/16, line (d/64) * 16 + key%16 of 128 bytes, 16-byte chunk
-// (d%64)/8 stored at chunk ^ (line % 8) (the 128-byte swizzle; tile bases are
-// 1024-byte aligned, so the line index is the address's swizzle phase).
-template <int D>
-__device__ __forceinline__ uint32_t tile_addr(uint32_t base, int key, int d) {
-    const int line = (d >> 6) * kBlock + (key & 15);
-    return base + (key >> 4) * TCfg<D>::kPageBytes + line * 128 +
-           ((((d & 63) >> 3) ^ (line & 7)) << 4);
-}
-
 template <int D, int G>
 __global__ void __launch_bounds__(kThreads, 2)
-    prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
+    prefill_tc_kernel(const __grid_constant__ CUtensorMap tmq,
+                      const __grid_constant__ CUtensorMap tmk,
                       const __grid_constant__ CUtensorMap tmv, const PParams p) {
     using C = TCfg<D>;
     constexpr int kTq = kRows / G;  // query tokens per CTA
     extern __shared__ unsigned char smem_raw[];
-    unsigned char *ring = reinterpret_cast<unsigned char *>(
+    unsigned char *sm = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint64_t *full = reinterpret_cast<uint64_t *>(ring + C::kRingBytes);
-    uint64_t *empty = full + kStages;
+    unsigned char *qs = sm;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + C::kBarOff);
+    uint64_t *q_full = bars, *kv_full = bars + 1, *kv_empty = bars + 3;
+    uint64_t *s_full = bars + 5, *s_free = bars + 6, *p_full = bars + 7, *pv_done = bars + 8;
+    uint64_t *mma_idle = bars + 9;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 10);
     __shared__ int s_abort;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = blockIdx.y;
     const int tok0 = blockIdx.x * kTq;
     const int ntok = min(kTq, p.T - tok0);
-    const int kmax = p.start + tok0 + ntok;  // keys [0, kmax) are read
+    const int kmax = p.start + tok0 + ntok;  // keys [0, kmax) are attended
     const int ntiles = (kmax + kKeys - 1) / kKeys;
+    const int npages = (kmax + kBlock - 1) / kBlock;
 
     if (tid == 0) {
+        mbar_init(q_full, 1);
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kConsumers);
+            mbar_init(&kv_full[s], 1);
+            mbar_init(&kv_empty[s], 1);
         }
+        mbar_init(s_full, 1);
+        mbar_init(s_free, 4);
+        mbar_init(p_full, 4);
+        mbar_init(pv_done, 1);
+        mbar_init(mma_idle, 1);
         mbar_fence_init();
         s_abort = 0;
     }
+    if (warp == 1) {
+        asm volatile(
+            "tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                smem_addr(tmem_slot)),
+            "r"(kTmemCols));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    tc_fence_before();
     __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    auto abort_now = [&]() {
+        raise_flag(p.err_flag, XS_FLAG_TIMEOUT);
+        atomicExch(&s_abort, 1);
+    };
+    auto aborted = [&]() { return *static_cast<volatile int *>(&s_abort) != 0; };
 
-    if (warp == kConsumers) {
-        // ============================================================ producer
-        const int npages = (kmax + kBlock - 1) / kBlock;
+    if (warp == 0) {
+        // ============================================================== TMA
         int issued = 0;
+        if (lane == 0) {
+            mbar_arrive_expect_tx(q_full, C::kQBytes);
+            for (int h = 0; h < C::kHalves; ++h)
+                tma_load_3d(smem_addr(qs + h * C::kQHalf), &tmq, 64 * h, g * G, tok0, q_full);
+        }
         for (int kt = 0; kt < ntiles; ++kt) {
             const int s = kt % kStages;
-            const uint32_t ph = (kt / kStages) & 1;
             int row = p.oob_row;
             const int pg = kt * kPagesPerTile + lane;
             if (lane < kPagesPerTile && pg < npages) {
@@ -159,186 +240,201 @@ __global__ void __launch_bounds__(kThreads, 2)
             }
             bool ok = true;
             if (lane == 0) {
-                ok = mbar_wait_bounded(&empty[s], ph ^ 1, kWaitLimitNs);
-                if (ok) mbar_arrive_expect_tx(&full[s], C::kStageBytes);
+                ok = mbar_wait_bounded(&kv_empty[s], ((kt / kStages) & 1) ^ 1, kWaitLimitNs) &&
+                     !aborted();
+                if (ok) mbar_arrive_expect_tx(&kv_full[s], C::kStageBytes);
             }
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) {
-                if (lane == 0) {
-                    raise_flag(p.err_flag, XS_FLAG_TIMEOUT);
-                    atomicExch(&s_abort, 1);
-                }
+            if (!__shfl_sync(0xffffffffu, ok, 0)) {
+                if (lane == 0) abort_now();
                 break;
             }
             if (lane < kPagesPerTile) {
-                const uint32_t kdst = smem_addr(ring + s * C::kStageBytes + lane * C::kPageBytes);
-                tma_load_3d(kdst, &tmk, 0, row, 0, &full[s]);
-                tma_load_3d(kdst + C::kTileBytes, &tmv, 0, row, 0, &full[s]);
+                unsigned char *kst = sm + C::kQBytes + s * C::kStageBytes;
+                for (int h = 0; h < C::kHalves; ++h) {
+                    const uint32_t dst = smem_addr(kst + h * C::kKVHalf + lane * kBlock * 128);
+                    tma_load_3d(dst, &tmk, 0, row, h, &kv_full[s]);
+                    tma_load_3d(dst + C::kTile, &tmv, 0, row, h, &kv_full[s]);
+                }
             }
             ++issued;
         }
-        // Let every copy this CTA issued land before it can exit.
+        // Let the copies this CTA issued land before it can exit.
         if (lane == 0) {
+            mbar_wait_bounded(q_full, 0, kWaitLimitNs);
             for (int kt = max(0, issued - kStages); kt < issued; ++kt)
-                mbar_wait_bounded(&full[kt % kStages], (kt / kStages) & 1, kWaitLimitNs);
+                mbar_wait_bounded(&kv_full[kt % kStages], (kt / kStages) & 1, kWaitLimitNs);
         }
-        return;
-    }
-
-    // ================================================================ consumers
-    const int group = lane >> 2, tq = lane & 3;
-    const int r0 = 16 * warp + group, r1 = r0 + 8;  // this lane's two rows
-    const int i0 = r0 % kTq, j0 = r0 / kTq, i1 = r1 % kTq, j1 = r1 / kTq;
-    const bool v0 = i0 < ntok, v1 = i1 < ntok;
-    const int qpos0 = p.start + tok0 + i0, qpos1 = p.start + tok0 + i1;
-    const __nv_bfloat16 *q0 =
-        p.q + (static_cast<int64_t>(tok0 + (v0 ? i0 : 0)) * p.Hq + g * G + j0) * D;
-    const __nv_bfloat16 *q1 =
-        p.q + (static_cast<int64_t>(tok0 + (v1 ? i1 : 0)) * p.Hq + g * G + j1) * D;
-
-    uint32_t qa[D / 16][4];
-#pragma unroll
-    for (int ks = 0; ks < D / 16; ++ks) {
-        const int d = 16 * ks + 2 * tq;
-        qa[ks][0] = v0 ? *reinterpret_cast<const uint32_t *>(q0 + d) : 0u;
-        qa[ks][1] = v1 ? *reinterpret_cast<const uint32_t *>(q1 + d) : 0u;
-        qa[ks][2] = v0 ? *reinterpret_cast<const uint32_t *>(q0 + d + 8) : 0u;
-        qa[ks][3] = v1 ? *reinterpret_cast<const uint32_t *>(q1 + d + 8) : 0u;
-    }
-    float oacc[D / 8][4];
-#pragma unroll
-    for (int n = 0; n < D / 8; ++n)
-#pragma unroll
-        for (int c = 0; c < 4; ++c) oacc[n][c] = 0.f;
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-
-    // ldmatrix lane roles: matrix mi = lane / 8, row ri = lane % 8 of it.
-    const int mi = lane >> 3, ri = lane & 7;
-    bool ok = true;
-    for (int kt = 0; kt < ntiles; ++kt) {
-        const int s = kt % kStages;
-        if (!__all_sync(0xffffffffu,
-                        mbar_wait_bounded(&full[s], (kt / kStages) & 1, kWaitLimitNs)) ||
-            *static_cast<volatile int *>(&s_abort)) {
-            ok = false;
-            break;
-        }
-        const uint32_t kbase = smem_addr(ring + s * C::kStageBytes);
-        const uint32_t vbase = kbase + C::kTileBytes;
-
-        // ---- S = Q K^T: 8 tiles of 8 keys
-        float sacc[8][4];
-#pragma unroll
-        for (int n = 0; n < 8; ++n)
-#pragma unroll
-            for (int c = 0; c < 4; ++c) sacc[n][c] = 0.f;
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks)
-#pragma unroll
-            for (int np = 0; np < 4; ++np) {
-                uint32_t b0, b1, b2, b3;
-                ldmatrix_x4(tile_addr<D>(kbase, 16 * np + ((mi >> 1) << 3) + ri,
-                                         16 * ks + ((mi & 1) << 3)),
-                            b0, b1, b2, b3);
-                mma_bf16(sacc[2 * np], qa[ks], b0, b1);
-                mma_bf16(sacc[2 * np + 1], qa[ks], b2, b3);
-            }
-
-        // ---- causal mask, online softmax (base 2)
-        const int kb = kt * kKeys + 2 * tq;
-        float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-        for (int n = 0; n < 8; ++n) {
-            const int k = kb + 8 * n;
-            sacc[n][0] = k <= qpos0 ? sacc[n][0] * p.qscale : -INFINITY;
-            sacc[n][1] = k + 1 <= qpos0 ? sacc[n][1] * p.qscale : -INFINITY;
-            sacc[n][2] = k <= qpos1 ? sacc[n][2] * p.qscale : -INFINITY;
-            sacc[n][3] = k + 1 <= qpos1 ? sacc[n][3] * p.qscale : -INFINITY;
-            mx0 = fmaxf(mx0, fmaxf(sacc[n][0], sacc[n][1]));
-            mx1 = fmaxf(mx1, fmaxf(sacc[n][2], sacc[n][3]));
-        }
-#pragma unroll
-        for (int o = 1; o <= 2; o <<= 1) {
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
-        }
-        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-        // A row with nothing unmasked yet keeps reference 0 (no -inf - -inf).
-        const float ref0 = mn0 == -INFINITY ? 0.f : mn0, ref1 = mn1 == -INFINITY ? 0.f : mn1;
-        const float corr0 = fast_exp2(m0 - ref0), corr1 = fast_exp2(m1 - ref1);
-        m0 = mn0;
-        m1 = mn1;
-        float ps0 = 0.f, ps1 = 0.f;
-#pragma unroll
-        for (int n = 0; n < 8; ++n) {
-            sacc[n][0] = fast_exp2(sacc[n][0] - ref0);
-            sacc[n][1] = fast_exp2(sacc[n][1] - ref0);
-            sacc[n][2] = fast_exp2(sacc[n][2] - ref1);
-            sacc[n][3] = fast_exp2(sacc[n][3] - ref1);
-            ps0 += sacc[n][0] + sacc[n][1];
-            ps1 += sacc[n][2] + sacc[n][3];
-        }
-        l0 = l0 * corr0 + ps0;
-        l1 = l1 * corr1 + ps1;
-#pragma unroll
-        for (int n = 0; n < D / 8; ++n) {
-            oacc[n][0] *= corr0;
-            oacc[n][1] *= corr0;
-            oacc[n][2] *= corr1;
-            oacc[n][3] *= corr1;
-        }
-
-        // ---- O += P V: 4 steps of 16 keys, D/8 tiles of 8 dims.  In the
-        // last tile, V rows of keys >= kmax (unwritten slots of the last page:
-        // any bits at all) are zeroed in the fragments, since 0 * NaN = NaN.
-        const bool last = (kt + 1) * kKeys > kmax;
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-            const int kq = kt * kKeys + 16 * kk + 2 * tq;
-            const uint32_t mlo = last ? ((kq < kmax ? 0xffffu : 0u) | (kq + 1 < kmax ? 0xffff0000u : 0u))
-                                      : 0xffffffffu;
-            const uint32_t mhi = last ? ((kq + 8 < kmax ? 0xffffu : 0u) |
-                                         (kq + 9 < kmax ? 0xffff0000u : 0u))
-                                      : 0xffffffffu;
-            const uint32_t pa[4] = {pack_bf16(sacc[2 * kk][0], sacc[2 * kk][1]),
-                                    pack_bf16(sacc[2 * kk][2], sacc[2 * kk][3]),
-                                    pack_bf16(sacc[2 * kk + 1][0], sacc[2 * kk + 1][1]),
-                                    pack_bf16(sacc[2 * kk + 1][2], sacc[2 * kk + 1][3])};
-#pragma unroll
-            for (int dn = 0; dn < D / 16; ++dn) {
-                uint32_t b0, b1, b2, b3;
-                ldmatrix_x4_trans(tile_addr<D>(vbase, 16 * kk + ((mi & 1) << 3) + ri,
-                                               16 * dn + ((mi >> 1) << 3)),
-                                  b0, b1, b2, b3);
-                mma_bf16(oacc[2 * dn], pa, b0 & mlo, b1 & mhi);
-                mma_bf16(oacc[2 * dn + 1], pa, b2 & mlo, b3 & mhi);
-            }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
-    }
-    if (!ok) {
+    } else if (warp == 1) {
+        // ============================================================== MMA
         if (lane == 0) {
-            raise_flag(p.err_flag, XS_FLAG_TIMEOUT);
-            atomicExch(&s_abort, 1);
+            const uint32_t qaddr = smem_addr(qs);
+            bool ok = mbar_wait_bounded(q_full, 0, kWaitLimitNs);
+            for (int kt = 0; ok && kt < ntiles; ++kt) {
+                const int s = kt % kStages;
+                ok = mbar_wait_bounded(&kv_full[s], (kt / kStages) & 1, kWaitLimitNs) &&
+                     (kt == 0 || mbar_wait_bounded(s_free, (kt - 1) & 1, kWaitLimitNs)) &&
+                     !aborted();
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t kaddr = smem_addr(sm + C::kQBytes + s * C::kStageBytes);
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks)
+                    umma_ss(tmem + kColS,
+                            smem_desc(qaddr + (ks >> 2) * C::kQHalf + 32 * (ks & 3), 16, 1024),
+                            smem_desc(kaddr + (ks >> 2) * C::kKVHalf + 32 * (ks & 3), 16, 1024),
+                            C::kIdS, ks > 0);
+                umma_commit(s_full);
+                ok = mbar_wait_bounded(p_full, kt & 1, kWaitLimitNs) && !aborted();
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t vaddr = kaddr + C::kTile;
+#pragma unroll
+                for (int kk = 0; kk < kKeys / 16; ++kk)
+                    umma_ts(tmem + kColO, tmem + kColP + 8 * kk,
+                            smem_desc(vaddr + 2048 * kk, C::kKVHalf, 1024), C::kIdPV,
+                            kt > 0 || kk > 0);
+                umma_commit(pv_done);
+                umma_commit(&kv_empty[s]);
+            }
+            if (!ok) abort_now();
+            // Every MMA issued has completed before the CTA leaves (and TMEM is freed).
+            umma_commit(mma_idle);
+            mbar_wait_bounded(mma_idle, 0, kWaitLimitNs);
         }
-        return;
-    }
+    } else {
+        // ========================================================== softmax
+        const int quad = warp & 3;
+        const int r = 32 * quad + lane;  // this thread's row = TMEM lane
+        const int tl = r / G;            // query token within the CTA
+        const bool valid = tl < ntok;
+        const int qpos = p.start + tok0 + tl;
+        const uint32_t lane_off = static_cast<uint32_t>(32 * quad) << 16;
+        float m_ref = 0.f, l = 0.f;
+        bool ok = true;
+        for (int kt = 0; kt < ntiles; ++kt) {
+            ok = __all_sync(0xffffffffu, mbar_wait_bounded(s_full, kt & 1, kWaitLimitNs)) &&
+                 !aborted();
+            if (!ok) break;
+            tc_fence_after();
+            uint32_t sr[2][32];
+            tmem_ld32(tmem + lane_off + kColS, sr[0]);
+            tmem_ld32(tmem + lane_off + kColS + 32, sr[1]);
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(s_free);  // S may be overwritten
 
-    // ---- out = O / l (the row sum over the quad's lanes)
+            // causal mask (by selection: a masked slot may hold any bits), tile max
+            const int k0 = kt * kKeys;
+            float sv[64], tmax = -INFINITY;
 #pragma unroll
-    for (int o = 1; o <= 2; o <<= 1) {
-        l0 += __shfl_xor_sync(0xffffffffu, l0, o);
-        l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+            for (int j = 0; j < 64; ++j) {
+                const float x = __uint_as_float(sr[j >> 5][j & 31]) * p.qscale;
+                sv[j] = k0 + j <= qpos ? x : -INFINITY;
+                tmax = fmaxf(tmax, sv[j]);
+            }
+            bool rescale = false;
+            float m_new = m_ref;
+            if (kt == 0) {
+                m_ref = tmax == -INFINITY ? 0.f : tmax;
+                m_new = m_ref;
+            } else if (tmax > m_ref + kHeadroom) {
+                rescale = true;
+                m_new = tmax;
+            }
+            float ps = 0.f;
+            uint32_t pr[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const float a = fast_exp2(sv[2 * j] - m_new), b = fast_exp2(sv[2 * j + 1] - m_new);
+                ps += a + b;
+                pr[j] = pack_bf16(a, b);
+            }
+            // P V of the previous tile must be done: it reads the P columns,
+            // and a rescale reads and writes O.
+            if (kt > 0) {
+                ok = __all_sync(0xffffffffu,
+                                mbar_wait_bounded(pv_done, (kt - 1) & 1, kWaitLimitNs)) &&
+                     !aborted();
+                if (!ok) break;
+                tc_fence_after();
+            }
+            if (__any_sync(0xffffffffu, rescale)) {
+                const float corr = rescale ? fast_exp2(m_ref - m_new) : 1.f;
+                l *= corr;
+#pragma unroll 1
+                for (int c = 0; c < D; c += 32) {
+                    uint32_t o[32];
+                    tmem_ld32(tmem + lane_off + kColO + c, o);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        o[j] = __float_as_uint(__uint_as_float(o[j]) * corr);
+                    tmem_st32(tmem + lane_off + kColO + c, o);
+                }
+                m_ref = m_new;
+            }
+            l += ps;
+            tmem_st32(tmem + lane_off + kColP, pr);
+            tmem_wait_st();
+            if (kt == ntiles - 1 && npages * kBlock > kmax) {
+                // Unwritten slots of the last page: zero their V rows (128-byte
+                // lines, whole, so the swizzle inside a line does not matter).
+                unsigned char *vt =
+                    sm + C::kQBytes + (kt % kStages) * C::kStageBytes + C::kTile;
+                const int first = kmax - k0, nrow = npages * kBlock - kmax;
+                for (int i = r; i < nrow * C::kHalves * 8; i += kRows) {
+                    const int line = i >> 3, chunk = i & 7;
+                    const int key = first + line % nrow, h = line / nrow;
+                    *reinterpret_cast<uint4 *>(vt + h * C::kKVHalf + key * 128 + chunk * 16) =
+                        make_uint4(0u, 0u, 0u, 0u);
+                }
+                fence_proxy_async_shared();
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(p_full);
+        }
+        if (ok && ntiles > 0) {
+            ok = __all_sync(0xffffffffu,
+                            mbar_wait_bounded(pv_done, (ntiles - 1) & 1, kWaitLimitNs));
+            tc_fence_after();
+        }
+        if (!ok) {
+            if (lane == 0) abort_now();
+        } else {
+            // out = O / l for this row
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            __nv_bfloat16 *orow =
+                p.out + (static_cast<int64_t>(tok0 + (valid ? tl : 0)) * p.Hq + g * G + r % G) * D;
+#pragma unroll 1
+            for (int c = 0; c < D; c += 32) {
+                uint32_t o[32];
+                tmem_ld32(tmem + lane_off + kColO + c, o);
+                tmem_wait_ld();
+                if (valid) {
+#pragma unroll
+                    for (int j = 0; j < 32; j += 8) {
+                        uint4 w;
+                        w.x = pack_bf16(__uint_as_float(o[j]) * inv, __uint_as_float(o[j + 1]) * inv);
+                        w.y = pack_bf16(__uint_as_float(o[j + 2]) * inv,
+                                        __uint_as_float(o[j + 3]) * inv);
+                        w.z = pack_bf16(__uint_as_float(o[j + 4]) * inv,
+                                        __uint_as_float(o[j + 5]) * inv);
+                        w.w = pack_bf16(__uint_as_float(o[j + 6]) * inv,
+                                        __uint_as_float(o[j + 7]) * inv);
+                        *reinterpret_cast<uint4 *>(orow + c + j) = w;
+                    }
+                }
+            }
+        }
     }
-    const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f, inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
-    __nv_bfloat16 *o0 = p.out + (static_cast<int64_t>(tok0 + i0) * p.Hq + g * G + j0) * D;
-    __nv_bfloat16 *o1 = p.out + (static_cast<int64_t>(tok0 + i1) * p.Hq + g * G + j1) * D;
-#pragma unroll
-    for (int n = 0; n < D / 8; ++n) {
-        const int d = 8 * n + 2 * tq;
-        if (v0) *reinterpret_cast<uint32_t *>(o0 + d) = pack_bf16(oacc[n][0] * inv0, oacc[n][1] * inv0);
-        if (v1) *reinterpret_cast<uint32_t *>(o1 + d) = pack_bf16(oacc[n][2] * inv1, oacc[n][3] * inv1);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(kTmemCols));
     }
 }
 
@@ -365,24 +461,20 @@ EncodeFn encode_fn() {
     return fn;
 }
 
-// Tensor map over a pool [num_blocks, Hkv, 16, D] bf16 seen as 3-D
-// (64 elements, num_blocks*Hkv*16 rows, D/64 halves) with box
-// (64, 16, D/64): one box is one page of one head, landing as [half][row].
-int encode_pool(CUtensorMap *tm, const void *pool, int64_t rows, int D) {
+// A 3-D bf16 tensor map with 128-byte swizzle (zero fill outside the tensor).
+int encode(CUtensorMap *tm, const void *base, const cuuint64_t (&dims)[3],
+           const cuuint64_t (&strides)[2], const cuuint32_t (&box)[3]) {
     EncodeFn fn = encode_fn();
     if (!fn) return XS_EDEVICE;
-    const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(D / 64)};
-    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, 128};
-    const cuuint32_t box[3] = {64, kBlock, static_cast<cuuint32_t>(D / 64)};
     const cuuint32_t estr[3] = {1, 1, 1};
-    const CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(pool), dims,
+    const CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? XS_OK : XS_EUNSUPPORTED;
 }
 
-using KernelFn = void (*)(const CUtensorMap, const CUtensorMap, const PParams);
+using KernelFn = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const PParams);
 
 template <int D, int G>
 KernelFn kernel_for() {
@@ -432,9 +524,23 @@ extern "C" int xs_paged_prefill_tc(void *out, const void *q, const void *k_cache
     if (T == 0 || num_blocks == 0) return XS_OK;
     pftc::KernelFn fn = pftc::pick(D, G);
     if (!fn) return XS_EUNSUPPORTED;
-    CUtensorMap tmk, tmv;
-    int st = pftc::encode_pool(&tmk, k_cache, rows, D);
-    if (st == XS_OK) st = pftc::encode_pool(&tmv, v_cache, rows, D);
+    // q [T, Hq, D] as (D, Hq, T), box (64, G, 128 / G): one D half of a CTA's rows.
+    // Pools [num_blocks, Hkv, 16, D] as (64, rows, D / 64) with strides (2 D, 128)
+    // bytes, box (64, 16, 1): one D half of one page.
+    CUtensorMap tmq, tmk, tmv;
+    const cuuint64_t qdims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(Hq),
+                                 static_cast<cuuint64_t>(T)};
+    const cuuint64_t qstr[2] = {static_cast<cuuint64_t>(D) * 2,
+                                static_cast<cuuint64_t>(Hq) * D * 2};
+    const cuuint32_t qbox[3] = {64, static_cast<cuuint32_t>(G),
+                                static_cast<cuuint32_t>(pftc::kRows / G)};
+    const cuuint64_t pdims[3] = {64, static_cast<cuuint64_t>(rows),
+                                 static_cast<cuuint64_t>(D / 64)};
+    const cuuint64_t pstr[2] = {static_cast<cuuint64_t>(D) * 2, 128};
+    const cuuint32_t pbox[3] = {64, pftc::kBlock, 1};
+    int st = pftc::encode(&tmq, q, qdims, qstr, qbox);
+    if (st == XS_OK) st = pftc::encode(&tmk, k_cache, pdims, pstr, pbox);
+    if (st == XS_OK) st = pftc::encode(&tmv, v_cache, pdims, pstr, pbox);
     if (st != XS_OK) return st;
     const int smem = D == 128 ? pftc::TCfg<128>::kSmemBytes : pftc::TCfg<64>::kSmemBytes;
     static std::mutex mu;
@@ -459,9 +565,7 @@ extern "C" int xs_paged_prefill_tc(void *out, const void *q, const void *k_cache
     }
     pftc::PParams p;
     p.out = static_cast<__nv_bfloat16 *>(out);
-    p.q = static_cast<const __nv_bfloat16 *>(q);
     p.block_ids = block_ids;
-    p.n_ids = n_ids;
     p.T = T;
     p.start = start_pos;
     p.Hq = Hq;
@@ -472,6 +576,6 @@ extern "C" int xs_paged_prefill_tc(void *out, const void *q, const void *k_cache
     p.err_flag = err_flag;
     const int tq = pftc::kRows / G;
     dim3 grid((T + tq - 1) / tq, Hkv);
-    fn<<<grid, pftc::kThreads, smem, stream>>>(tmk, tmv, p);
+    fn<<<grid, pftc::kThreads, smem, stream>>>(tmq, tmk, tmv, p);
     return launch_status();
 }
