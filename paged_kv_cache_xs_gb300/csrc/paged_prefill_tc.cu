@@ -10,15 +10,17 @@
 //    head) pair: 128 / G tokens x the G query heads of the group, so every
 //    K/V byte a CTA stages serves all G heads.  Row r is TMEM lane r.
 //  * Warp 0 (TMA): Q once (one 3-D tensor copy per 64-wide D half, box
-//    [64, G heads, 128/G tokens]); then 64-key K/V tiles (4 pages) into a
-//    2-stage ring, one 3-D copy per page and D half from a tensor map over the
-//    pool.  Every box is 128-byte swizzled, so a D half of a tile is the
+//    [64, G heads, 128/G tokens]); then 64-key K and V tiles (4 pages) into
+//    two 2-slot rings (a K slot frees after Q K^T, a V slot after P V), one
+//    3-D copy per page and D half from a tensor map over the pool.  Every box is 128-byte swizzled, so a D half of a tile is the
 //    canonical K-major layout (8-row groups 1024 B apart).  Pages past the
 //    last key are requested at a row beyond the pool and arrive as zeros.
 //  * Warp 1 (one thread): S = Q K^T with tcgen05.mma (M=128, N=64, K=16 per
 //    instruction, A and B from shared-memory descriptors, fp32 accumulators
 //    in TMEM columns 0-63); then O += P V (M=128, N=D) with P read from TMEM
-//    (A operand, columns 64-95) and V as an MN-major B descriptor (8-key
+//    (A operand, columns 64-95 or 96-127: P is double-buffered, so the
+//    softmax of tile t+1 never waits for P V of tile t) and V as an MN-major
+//    B descriptor (8-key
 //    groups 1024 B apart, D halves one tile-half apart); tcgen05.commit
 //    signals each step on an mbarrier.
 //  * Warps 2-5 (softmax; warp w reads TMEM lanes 32*(w%4)..+31, one row per
@@ -29,7 +31,7 @@
 //    tiles never touch O.  Unwritten slots of the last page (any bits at all)
 //    are zeroed in the staged V tile, since 0 * NaN = NaN.  At the end:
 //    O / l, bf16, out.
-//  * TMEM: 256 columns (S 64, P 32, O D), so two CTAs share an SM and one
+//  * TMEM: 256 columns (S 64, P 2 x 32, O D), so two CTAs share an SM and one
 //    CTA's softmax overlaps the other's MMAs.  Every wait is bounded; the
 //    MMA thread waits for its last MMA before the CTA frees TMEM.
 #include <cuda.h>
@@ -50,7 +52,7 @@ constexpr int kPagesPerTile = kKeys / kBlock;
 constexpr int kStages = 2;
 constexpr int kThreads = 192;            // TMA warp, MMA warp, 4 softmax warps
 constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kColS = 0, kColP = 64, kColO = 128;
+constexpr uint32_t kColS = 0, kColP = 64, kColO = 128;  // P: two buffers of 32 columns
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kHeadroom = 8.f;         // log2 units P may exceed 1 before O is rescaled
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
@@ -62,9 +64,13 @@ struct TCfg {
     static constexpr int kQBytes = kHalves * kQHalf;
     static constexpr int kKVHalf = kKeys * 128;     // one D half of a K or V tile
     static constexpr int kTile = kHalves * kKVHalf;
-    static constexpr int kStageBytes = 2 * kTile;   // K tile, then V tile
-    static constexpr int kBarOff = kQBytes + kStages * kStageBytes;
-    static constexpr int kBarBytes = 16 * 8;
+    // Separate rings for K and V tiles: a K slot frees when Q K^T of its tile
+    // is done, long before P V of that tile, so K of the next tiles streams in
+    // while the current ones are still in use.
+    static constexpr int kKOff = kQBytes;
+    static constexpr int kVOff = kQBytes + kStages * kTile;
+    static constexpr int kBarOff = kQBytes + 2 * kStages * kTile;
+    static constexpr int kBarBytes = 20 * 8;
     static constexpr int kSmemBytes = kBarOff + kBarBytes + 1024;  // + alignment slack
     // Instruction descriptors (kind::f16): fp32 D, bf16 A and B, M = 128;
     // Q K^T: both K-major, N = 64; P V: B (V) MN-major, N = D.
@@ -174,10 +180,14 @@ __global__ void __launch_bounds__(kThreads, 2)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     unsigned char *qs = sm;
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + C::kBarOff);
-    uint64_t *q_full = bars, *kv_full = bars + 1, *kv_empty = bars + 3;
-    uint64_t *s_full = bars + 5, *s_free = bars + 6, *p_full = bars + 7, *pv_done = bars + 8;
-    uint64_t *mma_idle = bars + 9;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 10);
+    uint64_t *q_full = bars, *k_full = bars + 1, *k_empty = bars + 3;
+    uint64_t *v_full = bars + 5, *v_empty = bars + 7;
+    // P is double-buffered (tile t uses buffer t % 2), and so are the barriers
+    // that hand it over: each then completes once per two tiles, and neither
+    // side can run two phases ahead of the other.
+    uint64_t *s_full = bars + 9, *s_free = bars + 10, *p_full = bars + 11, *pv_done = bars + 13;
+    uint64_t *mma_idle = bars + 15;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 16);
     __shared__ int s_abort;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -191,13 +201,17 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (tid == 0) {
         mbar_init(q_full, 1);
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(&kv_full[s], 1);
-            mbar_init(&kv_empty[s], 1);
+            mbar_init(&k_full[s], 1);
+            mbar_init(&k_empty[s], 1);
+            mbar_init(&v_full[s], 1);
+            mbar_init(&v_empty[s], 1);
         }
         mbar_init(s_full, 1);
         mbar_init(s_free, 4);
-        mbar_init(p_full, 4);
-        mbar_init(pv_done, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&p_full[b], 4);
+            mbar_init(&pv_done[b], 1);
+        }
         mbar_init(mma_idle, 1);
         mbar_fence_init();
         s_abort = 0;
@@ -229,6 +243,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         for (int kt = 0; kt < ntiles; ++kt) {
             const int s = kt % kStages;
+            const uint32_t par = ((kt / kStages) & 1) ^ 1;
             int row = p.oob_row;
             const int pg = kt * kPagesPerTile + lane;
             if (lane < kPagesPerTile && pg < npages) {
@@ -238,45 +253,47 @@ __global__ void __launch_bounds__(kThreads, 2)
                 else
                     row = (blk * p.Hkv + g) * kBlock;
             }
+            // K tile, then V tile, each into its own ring.
             bool ok = true;
-            if (lane == 0) {
-                ok = mbar_wait_bounded(&kv_empty[s], ((kt / kStages) & 1) ^ 1, kWaitLimitNs) &&
-                     !aborted();
-                if (ok) mbar_arrive_expect_tx(&kv_full[s], C::kStageBytes);
+            for (int which = 0; which < 2 && ok; ++which) {
+                uint64_t *emp = which ? &v_empty[s] : &k_empty[s];
+                uint64_t *ful = which ? &v_full[s] : &k_full[s];
+                if (lane == 0) {
+                    ok = mbar_wait_bounded(emp, par, kWaitLimitNs) && !aborted();
+                    if (ok) mbar_arrive_expect_tx(ful, C::kTile);
+                }
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (ok && lane < kPagesPerTile) {
+                    unsigned char *base = sm + (which ? C::kVOff : C::kKOff) + s * C::kTile;
+                    for (int h = 0; h < C::kHalves; ++h)
+                        tma_load_3d(smem_addr(base + h * C::kKVHalf + lane * kBlock * 128),
+                                    which ? &tmv : &tmk, 0, row, h, ful);
+                }
             }
-            if (!__shfl_sync(0xffffffffu, ok, 0)) {
+            if (!ok) {
                 if (lane == 0) abort_now();
                 break;
-            }
-            if (lane < kPagesPerTile) {
-                unsigned char *kst = sm + C::kQBytes + s * C::kStageBytes;
-                for (int h = 0; h < C::kHalves; ++h) {
-                    const uint32_t dst = smem_addr(kst + h * C::kKVHalf + lane * kBlock * 128);
-                    tma_load_3d(dst, &tmk, 0, row, h, &kv_full[s]);
-                    tma_load_3d(dst + C::kTile, &tmv, 0, row, h, &kv_full[s]);
-                }
             }
             ++issued;
         }
         // Let the copies this CTA issued land before it can exit.
         if (lane == 0) {
             mbar_wait_bounded(q_full, 0, kWaitLimitNs);
-            for (int kt = max(0, issued - kStages); kt < issued; ++kt)
-                mbar_wait_bounded(&kv_full[kt % kStages], (kt / kStages) & 1, kWaitLimitNs);
+            for (int kt = max(0, issued - kStages); kt < issued; ++kt) {
+                mbar_wait_bounded(&k_full[kt % kStages], (kt / kStages) & 1, kWaitLimitNs);
+                mbar_wait_bounded(&v_full[kt % kStages], (kt / kStages) & 1, kWaitLimitNs);
+            }
         }
     } else if (warp == 1) {
         // ============================================================== MMA
+        // Order: S(0); then per tile t: S(t+1) as soon as the softmax has
+        // read S(t) and tile t+1 is staged, then P V(t) once P(t) is in TMEM,
+        // so the tensor cores compute the next scores while the softmax warps
+        // work on the current ones.
         if (lane == 0) {
             const uint32_t qaddr = smem_addr(qs);
-            bool ok = mbar_wait_bounded(q_full, 0, kWaitLimitNs);
-            for (int kt = 0; ok && kt < ntiles; ++kt) {
-                const int s = kt % kStages;
-                ok = mbar_wait_bounded(&kv_full[s], (kt / kStages) & 1, kWaitLimitNs) &&
-                     (kt == 0 || mbar_wait_bounded(s_free, (kt - 1) & 1, kWaitLimitNs)) &&
-                     !aborted();
-                if (!ok) break;
-                tc_fence_after();
-                const uint32_t kaddr = smem_addr(sm + C::kQBytes + s * C::kStageBytes);
+            auto issue_s = [&](int kt) {
+                const uint32_t kaddr = smem_addr(sm + C::kKOff + (kt % kStages) * C::kTile);
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks)
                     umma_ss(tmem + kColS,
@@ -284,17 +301,37 @@ __global__ void __launch_bounds__(kThreads, 2)
                             smem_desc(kaddr + (ks >> 2) * C::kKVHalf + 32 * (ks & 3), 16, 1024),
                             C::kIdS, ks > 0);
                 umma_commit(s_full);
-                ok = mbar_wait_bounded(p_full, kt & 1, kWaitLimitNs) && !aborted();
+                umma_commit(&k_empty[kt % kStages]);
+            };
+            bool ok = mbar_wait_bounded(q_full, 0, kWaitLimitNs) &&
+                      mbar_wait_bounded(&k_full[0], 0, kWaitLimitNs);
+            if (ok) {
+                tc_fence_after();
+                issue_s(0);
+            }
+            for (int kt = 0; ok && kt < ntiles; ++kt) {
+                const int s = kt % kStages;
+                if (kt + 1 < ntiles) {
+                    const int s1 = (kt + 1) % kStages;
+                    ok = mbar_wait_bounded(&k_full[s1], ((kt + 1) / kStages) & 1, kWaitLimitNs) &&
+                         mbar_wait_bounded(s_free, kt & 1, kWaitLimitNs) && !aborted();
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_s(kt + 1);
+                }
+                ok = mbar_wait_bounded(&p_full[kt & 1], (kt >> 1) & 1, kWaitLimitNs) &&
+                     mbar_wait_bounded(&v_full[s], (kt / kStages) & 1, kWaitLimitNs) &&
+                     !aborted();
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t vaddr = kaddr + C::kTile;
+                const uint32_t vaddr = smem_addr(sm + C::kVOff + s * C::kTile);
 #pragma unroll
                 for (int kk = 0; kk < kKeys / 16; ++kk)
-                    umma_ts(tmem + kColO, tmem + kColP + 8 * kk,
+                    umma_ts(tmem + kColO, tmem + kColP + 32 * (kt & 1) + 8 * kk,
                             smem_desc(vaddr + 2048 * kk, C::kKVHalf, 1024), C::kIdPV,
                             kt > 0 || kk > 0);
-                umma_commit(pv_done);
-                umma_commit(&kv_empty[s]);
+                umma_commit(&pv_done[kt & 1]);
+                umma_commit(&v_empty[s]);
             }
             if (!ok) abort_now();
             // Every MMA issued has completed before the CTA leaves (and TMEM is freed).
@@ -324,15 +361,20 @@ __global__ void __launch_bounds__(kThreads, 2)
             __syncwarp();
             if (lane == 0) mbar_arrive(s_free);  // S may be overwritten
 
-            // causal mask (by selection: a masked slot may hold any bits), tile max
+            // Causal mask (by selection: a masked slot may hold any bits) - only
+            // tiles that reach past the CTA's first query position need one.
+            // The maximum is taken on raw scores (qscale > 0), the exponent
+            // is one fma: 2^(s * qscale - m).
             const int k0 = kt * kKeys;
-            float sv[64], tmax = -INFINITY;
+            const bool need_mask = k0 + kKeys - 1 > p.start + tok0;
+            float sv[64], smax = -INFINITY;
 #pragma unroll
             for (int j = 0; j < 64; ++j) {
-                const float x = __uint_as_float(sr[j >> 5][j & 31]) * p.qscale;
-                sv[j] = k0 + j <= qpos ? x : -INFINITY;
-                tmax = fmaxf(tmax, sv[j]);
+                const float x = __uint_as_float(sr[j >> 5][j & 31]);
+                sv[j] = !need_mask || k0 + j <= qpos ? x : -INFINITY;
+                smax = fmaxf(smax, sv[j]);
             }
+            const float tmax = smax * p.qscale;
             bool rescale = false;
             float m_new = m_ref;
             if (kt == 0) {
@@ -342,24 +384,33 @@ __global__ void __launch_bounds__(kThreads, 2)
                 rescale = true;
                 m_new = tmax;
             }
-            float ps = 0.f;
+            float ps0 = 0.f, ps1 = 0.f;
             uint32_t pr[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
-                const float a = fast_exp2(sv[2 * j] - m_new), b = fast_exp2(sv[2 * j + 1] - m_new);
-                ps += a + b;
+                const float a = fast_exp2(fmaf(sv[2 * j], p.qscale, -m_new));
+                const float b = fast_exp2(fmaf(sv[2 * j + 1], p.qscale, -m_new));
+                ps0 += a;
+                ps1 += b;
                 pr[j] = pack_bf16(a, b);
             }
-            // P V of the previous tile must be done: it reads the P columns,
-            // and a rescale reads and writes O.
-            if (kt > 0) {
-                ok = __all_sync(0xffffffffu,
-                                mbar_wait_bounded(pv_done, (kt - 1) & 1, kWaitLimitNs)) &&
+            const float ps = ps0 + ps1;
+            // P buffer kt % 2 was last read by P V of tile kt - 2; a rescale
+            // reads and writes O, so it waits for P V of tile kt - 1.
+            if (kt >= 2) {
+                ok = __all_sync(0xffffffffu, mbar_wait_bounded(&pv_done[kt & 1],
+                                                               ((kt - 2) >> 1) & 1, kWaitLimitNs)) &&
                      !aborted();
                 if (!ok) break;
                 tc_fence_after();
             }
             if (__any_sync(0xffffffffu, rescale)) {
+                ok = __all_sync(0xffffffffu,
+                                mbar_wait_bounded(&pv_done[(kt - 1) & 1], ((kt - 1) >> 1) & 1,
+                                                  kWaitLimitNs)) &&
+                     !aborted();
+                if (!ok) break;
+                tc_fence_after();
                 const float corr = rescale ? fast_exp2(m_ref - m_new) : 1.f;
                 l *= corr;
 #pragma unroll 1
@@ -372,16 +423,20 @@ __global__ void __launch_bounds__(kThreads, 2)
                         o[j] = __float_as_uint(__uint_as_float(o[j]) * corr);
                     tmem_st32(tmem + lane_off + kColO + c, o);
                 }
-                m_ref = m_new;
+                if (rescale) m_ref = m_new;
             }
             l += ps;
-            tmem_st32(tmem + lane_off + kColP, pr);
+            tmem_st32(tmem + lane_off + kColP + 32 * (kt & 1), pr);
             tmem_wait_st();
             if (kt == ntiles - 1 && npages * kBlock > kmax) {
                 // Unwritten slots of the last page: zero their V rows (128-byte
-                // lines, whole, so the swizzle inside a line does not matter).
-                unsigned char *vt =
-                    sm + C::kQBytes + (kt % kStages) * C::kStageBytes + C::kTile;
+                // lines, whole, so the swizzle inside a line does not matter),
+                // once the V tile has landed.
+                ok = __all_sync(0xffffffffu,
+                                mbar_wait_bounded(&v_full[kt % kStages], (kt / kStages) & 1,
+                                                  kWaitLimitNs));
+                if (!ok) break;
+                unsigned char *vt = sm + C::kVOff + (kt % kStages) * C::kTile;
                 const int first = kmax - k0, nrow = npages * kBlock - kmax;
                 for (int i = r; i < nrow * C::kHalves * 8; i += kRows) {
                     const int line = i >> 3, chunk = i & 7;
@@ -393,11 +448,12 @@ __global__ void __launch_bounds__(kThreads, 2)
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(p_full);
+            if (lane == 0) mbar_arrive(&p_full[kt & 1]);
         }
         if (ok && ntiles > 0) {
+            const int kt = ntiles - 1;
             ok = __all_sync(0xffffffffu,
-                            mbar_wait_bounded(pv_done, (ntiles - 1) & 1, kWaitLimitNs));
+                            mbar_wait_bounded(&pv_done[kt & 1], (kt >> 1) & 1, kWaitLimitNs));
             tc_fence_after();
         }
         if (!ok) {
