@@ -241,9 +241,9 @@ __global__ void __launch_bounds__(kThreads, 2)
             for (int h = 0; h < C::kHalves; ++h)
                 tma_load_3d(smem_addr(qs + h * C::kQHalf), &tmq, 64 * h, g * G, tok0, q_full);
         }
-        for (int kt = 0; kt < ntiles; ++kt) {
-            const int s = kt % kStages;
-            const uint32_t par = ((kt / kStages) & 1) ^ 1;
+        // K runs one tile ahead of V: K(t + 1) is issued before V(t), so the
+        // next Q K^T never queues behind a V slot that P V still holds.
+        auto page_row = [&](int kt) {
             int row = p.oob_row;
             const int pg = kt * kPagesPerTile + lane;
             if (lane < kPagesPerTile && pg < npages) {
@@ -253,36 +253,46 @@ __global__ void __launch_bounds__(kThreads, 2)
                 else
                     row = (blk * p.Hkv + g) * kBlock;
             }
-            // K tile, then V tile, each into its own ring.
+            return row;
+        };
+        auto issue = [&](int kt, int which, int row) {
+            const int s = kt % kStages;
+            uint64_t *emp = which ? &v_empty[s] : &k_empty[s];
+            uint64_t *ful = which ? &v_full[s] : &k_full[s];
             bool ok = true;
-            for (int which = 0; which < 2 && ok; ++which) {
-                uint64_t *emp = which ? &v_empty[s] : &k_empty[s];
-                uint64_t *ful = which ? &v_full[s] : &k_full[s];
-                if (lane == 0) {
-                    ok = mbar_wait_bounded(emp, par, kWaitLimitNs) && !aborted();
-                    if (ok) mbar_arrive_expect_tx(ful, C::kTile);
-                }
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (ok && lane < kPagesPerTile) {
-                    unsigned char *base = sm + (which ? C::kVOff : C::kKOff) + s * C::kTile;
-                    for (int h = 0; h < C::kHalves; ++h)
-                        tma_load_3d(smem_addr(base + h * C::kKVHalf + lane * kBlock * 128),
-                                    which ? &tmv : &tmk, 0, row, h, ful);
-                }
+            if (lane == 0) {
+                ok = mbar_wait_bounded(emp, ((kt / kStages) & 1) ^ 1, kWaitLimitNs) && !aborted();
+                if (ok) mbar_arrive_expect_tx(ful, C::kTile);
             }
-            if (!ok) {
-                if (lane == 0) abort_now();
-                break;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (ok && lane < kPagesPerTile) {
+                unsigned char *base = sm + (which ? C::kVOff : C::kKOff) + s * C::kTile;
+                for (int h = 0; h < C::kHalves; ++h)
+                    tma_load_3d(smem_addr(base + h * C::kKVHalf + lane * kBlock * 128),
+                                which ? &tmv : &tmk, 0, row, h, ful);
             }
-            ++issued;
+            return ok;
+        };
+        int row_next = ntiles > 0 ? page_row(0) : 0;
+        bool ok = ntiles == 0 || issue(0, 0, row_next);
+        for (int kt = 0; ok && kt < ntiles; ++kt) {
+            const int row = row_next;
+            if (kt + 1 < ntiles) {
+                row_next = page_row(kt + 1);
+                ok = issue(kt + 1, 0, row_next);
+            }
+            ok = ok && issue(kt, 1, row);
+            if (ok) ++issued;
         }
+        if (!ok && lane == 0) abort_now();
         // Let the copies this CTA issued land before it can exit.
         if (lane == 0) {
             mbar_wait_bounded(q_full, 0, kWaitLimitNs);
-            for (int kt = max(0, issued - kStages); kt < issued; ++kt) {
+            // (K may be one tile ahead of V.)
+            for (int kt = max(0, issued - kStages); kt < min(ntiles, issued + 1); ++kt)
                 mbar_wait_bounded(&k_full[kt % kStages], (kt / kStages) & 1, kWaitLimitNs);
+            for (int kt = max(0, issued - kStages); kt < issued; ++kt)
                 mbar_wait_bounded(&v_full[kt % kStages], (kt / kStages) & 1, kWaitLimitNs);
-            }
         }
     } else if (warp == 1) {
         // ============================================================== MMA
