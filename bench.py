@@ -640,7 +640,7 @@ def run_prefill(args, rank, world, local, dist):
                 "peak": peak, "unit": "TFLOP/s", "frac": round(attn_tflops / peak, 4),
                 "peak_kind": peak_kind, "traffic": None,
                 "algorithmic_flop": flop, "attention_ms": round(attn_ms, 4),
-                "note": "bf16 mma.sync m16n8k16, fp32 accumulation; K/V pages by TMA"}
+                "note": "tcgen05.mma (M=128) with TMEM accumulators, bf16 operands; K/V pages by TMA"}
     else:
         roof = {"kernel": "paged_decode_kernel (prefill mode)", "bound": "alu",
                 "achieved": round(attn_tflops, 2), "unit": "TFLOP/s",
