@@ -29,11 +29,15 @@
 //    sequence) or fp32 partials (o, m, l) for the split-K reduce.
 //  * Logits are kept in base-2 units (q is pre-scaled by scale*log2(e)) so
 //    exponentials are single ex2 instructions.
+#include <cuda.h>
+
 #include <algorithm>
+#include <cstring>
 #include <cmath>
 #include <mutex>
 #include <type_traits>
 
+#include "tensor_map.h"
 #include "xs_common.cuh"
 
 namespace xs {
@@ -85,7 +89,15 @@ struct Cfg {
     static constexpr int kItemOff = kBarOff + kBarBytes;             // 2 published items
     static constexpr int kPrefixOff = kItemOff + 2 * 32;
     // The host sizes every launch with this same function.
-    static __host__ __device__ constexpr int smem_bytes(int B) { return kPrefixOff + table_bytes(B); }
+    // bf16 pages arrive by TMA tensor copies in the 128-byte swizzled
+    // [half][row] layout and feed bf16 mma; fp32 pages by 1-D bulk copies
+    // and CUDA-core FMA.  The ring must then be 1024-byte aligned: 1024 bytes
+    // of slack let the kernel align the dynamic shared memory base.
+    static constexpr bool kMma = sizeof(T) == 2;
+    static constexpr int kAlignSlack = 1024;
+    static __host__ __device__ constexpr int smem_bytes(int B) {
+        return kPrefixOff + table_bytes(B) + kAlignSlack;
+    }
     static_assert(kStages % kConsumerWarps == 0, "each ring stage must belong to one consumer");
     static_assert((kMergeBufs & (kMergeBufs - 1)) == 0, "item counters wrap: a power of two");
     static_assert(kChunksPerLane >= 1 && kChunksPerRow % 8 == 0, "row must split over 8 lanes");
@@ -432,6 +444,120 @@ __device__ __noinline__ void combine_partials(const Params &p, const Item &it, i
     }
 }
 
+// ---- bf16 tensor-core pieces (the page layout they read is the one the
+// producer's tensor copies write: per page, [D/64 halves][16 rows] of 128-byte
+// lines, the 16-byte chunk c of line L stored at chunk c ^ (L % 8)).
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                        uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                          uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+// d += a (16x16 bf16, rows 8-15 zero) * b (16x8 bf16): only a0/a2 (rows 0-7) given.
+__device__ __forceinline__ void mma_rows8(float (&d)[4], uint32_t a0, uint32_t a2, uint32_t b0,
+                                          uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&v);
+}
+template <int D>
+__device__ __forceinline__ uint32_t page_addr(uint32_t base, int key, int d) {
+    const int line = (d >> 6) * kBlock + key;
+    return base + line * 128 + ((((d & 63) >> 3) ^ (line & 7)) << 4);
+}
+
+// One page of the bf16 path for one consumer warp, on the tensor cores
+// (mma.sync m16n8k16): the G heads are rows 0..G-1 of the A operand (lane
+// quad g holds head g), the 16 keys two 8-column tiles.  S = q K^T in fp32,
+// online softmax in base 2 per head, then O += P V with P (bf16) repacked
+// from the S accumulators.  Keys outside [t_lo, t_hi) are masked out of S
+// and their V rows zeroed in the fragments (a slot past the sequence's end
+// may hold any bits).  qa: per 16-dim step, the head row's two bf16 pairs.
+template <int D, bool kFull>
+__device__ __forceinline__ void consume_page_mma(uint32_t kaddr, uint32_t vaddr, int t_lo, int t_hi,
+                                                 const uint32_t (&qa)[D / 16][2], float qscale,
+                                                 float &m_row, float &l_lane, float (&oacc)[D / 8][4],
+                                                 int lane) {
+    const int tq = lane & 3, mi = lane >> 3, ri = lane & 7;
+    float sacc[2][4];
+#pragma unroll
+    for (int n = 0; n < 2; ++n)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) sacc[n][c] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(page_addr<D>(kaddr, ((mi >> 1) << 3) + ri, 16 * ks + ((mi & 1) << 3)), b0, b1, b2,
+                b3);
+        mma_rows8(sacc[0], qa[ks][0], qa[ks][1], b0, b1);
+        mma_rows8(sacc[1], qa[ks][0], qa[ks][1], b2, b3);
+    }
+    // Scores of this lane's head row for keys 8n + 2tq + {0, 1}.
+    float sc[4];
+#pragma unroll
+    for (int n = 0; n < 2; ++n)
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            const int t = 8 * n + 2 * tq + c;
+            const float x = sacc[n][c] * qscale;
+            sc[2 * n + c] = (kFull || (t >= t_lo && t < t_hi)) ? x : -INFINITY;
+        }
+    float mx = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    const float m_new = fmaxf(m_row, mx);
+    const float ref = m_new == -INFINITY ? 0.f : m_new;
+    const float corr = fast_exp2(m_row - ref);
+    m_row = m_new;
+    float pv[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) pv[i] = fast_exp2(sc[i] - ref);
+    l_lane = l_lane * corr + (pv[0] + pv[1] + pv[2] + pv[3]);
+#pragma unroll
+    for (int n = 0; n < D / 8; ++n) {
+        oacc[n][0] *= corr;
+        oacc[n][1] *= corr;
+    }
+    const uint32_t pa0 = pack_bf16x2(pv[0], pv[1]), pa2 = pack_bf16x2(pv[2], pv[3]);
+    // V fragment masks: key 2tq + {0,1} (low, high half), and +8.
+    uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
+    if (!kFull) {
+        const int k = 2 * tq;
+        mlo = ((k >= t_lo && k < t_hi) ? 0xffffu : 0u) | ((k + 1 >= t_lo && k + 1 < t_hi) ? 0xffff0000u : 0u);
+        mhi = ((k + 8 >= t_lo && k + 8 < t_hi) ? 0xffffu : 0u) |
+              ((k + 9 >= t_lo && k + 9 < t_hi) ? 0xffff0000u : 0u);
+    }
+#pragma unroll
+    for (int dn = 0; dn < D / 16; ++dn) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(page_addr<D>(vaddr, ((mi & 1) << 3) + ri, 16 * dn + ((mi >> 1) << 3)), b0, b1, b2,
+                  b3);
+        mma_rows8(oacc[2 * dn], pa0, pa2, b0 & mlo, b1 & mhi);
+        mma_rows8(oacc[2 * dn + 1], pa0, pa2, b2 & mlo, b3 & mhi);
+    }
+}
+
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *tm, int w,
+                                            uint64_t *bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %2, %2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(0), "r"(w), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
 // The merger's batched count: queue entry k (held by lane k < npend) is a
 // split item of group (b, g) with np partitions whose partials this warp has
 // written.  One fence publishes them all; each entry's group count is then
@@ -463,10 +589,13 @@ __device__ __noinline__ void count_and_combine(const Params &p, int lane, int pe
 
 template <typename T, int D, int G>
 __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
-    paged_decode_kernel(const Params p) {
+    paged_decode_kernel(const __grid_constant__ CUtensorMap tmk,
+                        const __grid_constant__ CUtensorMap tmv, const Params p) {
     using C = Cfg<T, D, G>;
     constexpr int kStages = C::kStages;
-    extern __shared__ __align__(128) unsigned char smem[];
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    unsigned char *smem = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::kBarOff);
     uint64_t *empty = full + kStages;
     uint64_t *qfull = empty + kStages;
@@ -741,6 +870,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
                 if (__any_sync(0xffffffffu, bad_id) && lane == 0)
                     raise_flag(p.err_flag, XS_FLAG_BAD_BLOCK);
                 const int64_t my_off = static_cast<int64_t>(bad_id ? 0 : ids) * blk_stride + head_off;
+                const int my_page = (bad_id ? 0 : ids) * p.Hkv + A.g;  // tensor-map page index
                 int done = 0;
                 while (done < cnt) {
                     const int want = min(cnt - done, kStages);
@@ -750,6 +880,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
                         lane < want && mbar_test_wait(&empty[st], ((c / kStages) & 1) ^ 1);
                     const int n = __ffs(~__ballot_sync(0xffffffffu, is_free)) - 1;
                     const int64_t off = __shfl_sync(0xffffffffu, my_off, (done + lane) & 31);
+                    const int pidx = __shfl_sync(0xffffffffu, my_page, (done + lane) & 31);
                     if (n == 0) {
                         // No stage free yet: wait (bounded) for the next one.
                         bool w = true;
@@ -765,8 +896,13 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
                     if (lane < n) {
                         unsigned char *dk = smem + st * 2 * C::kPageBytes;
                         mbar_arrive_expect_tx(&full[st], 2 * C::kPageBytes);
-                        bulk_g2s(dk, kbase + off, C::kPageBytes, &full[st], pol);
-                        bulk_g2s(dk + C::kPageBytes, vbase + off, C::kPageBytes, &full[st], pol);
+                        if constexpr (C::kMma) {
+                            tma_load_4d(smem_addr(dk), &tmk, pidx, &full[st], pol);
+                            tma_load_4d(smem_addr(dk + C::kPageBytes), &tmv, pidx, &full[st], pol);
+                        } else {
+                            bulk_g2s(dk, kbase + off, C::kPageBytes, &full[st], pol);
+                            bulk_g2s(dk + C::kPageBytes, vbase + off, C::kPageBytes, &full[st], pol);
+                        }
                     }
                     done += n;
                     page_ctr += n;  // pages issued so far
@@ -907,114 +1043,209 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
 
     // ==================================================================== consumers
     const int cw = warp - 1;
-    const int j = lane & 7;
-    float2 *W2 = reinterpret_cast<float2 *>(smem + C::kWOff) + cw * kBlock * G;
-    uint32_t page_ctr = 0;
-
-    for (uint32_t item_ctr = 0;; ++item_ctr) {
-        // Every consumer sees the producer's end marker (b < 0) in the same
-        // slot and leaves; warp 0 passes the marker on to the merger.  A
-        // failed (timed-out) wait marks the item bad: the warp skips its pages.
-        // All waits in the CTA are bounded, so no warp can wait forever.
-        const uint32_t slot = item_ctr & 1;
-        bool bad = !__all_sync(0xffffffffu,
-                               mbar_wait_bounded(&qfull[slot], (item_ctr >> 1) & 1, kWaitLimitNs));
-        Item it = item_slot[slot];
-        const bool done = !bad && it.b < 0;
-        float qf[G][C::kQkDims];
-        if (!done) {
-            const unsigned char *qs = smem + C::kQSlotOff + slot * C::kQBytes;
+    if constexpr (C::kMma) {
+        // bf16: tensor-core pages (consume_page_mma); per item the G query rows
+        // become A fragments (lane quad g holds head g, unscaled: scores are
+        // scaled after the product), and the state handed to the merger is
+        // this lane quad's head row: m, l (summed over the quad) and O.
+        const int grp = lane >> 2, tq = lane & 3;
+        uint32_t page_ctr = 0;
+        for (uint32_t item_ctr = 0;; ++item_ctr) {
+            const uint32_t slot = item_ctr & 1;
+            bool bad = !__all_sync(0xffffffffu, mbar_wait_bounded(&qfull[slot], (item_ctr >> 1) & 1,
+                                                                  kWaitLimitNs));
+            Item it = item_slot[slot];
+            const bool done = !bad && it.b < 0;
+            uint32_t qa[D / 16][2];
+            if (!done) {
+                const unsigned char *qs = smem + C::kQSlotOff + slot * C::kQBytes;
 #pragma unroll
-            for (int h = 0; h < G; ++h)
-#pragma unroll
-                for (int c = 0; c < C::kChunksPerLane; ++c) {
-                    const uint4 raw = *reinterpret_cast<const uint4 *>(
-                        qs + h * C::kRowBytes + (j + 8 * c) * 16);
-                    float f[C::kElemsPerChunk];
-                    unpack16(raw, f, static_cast<T *>(nullptr));
-#pragma unroll
-                    for (int e = 0; e < C::kElemsPerChunk; ++e)
-                        qf[h][c * C::kElemsPerChunk + e] = f[e] * p.qscale;
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const unsigned char *row = qs + (grp < G ? grp : 0) * C::kRowBytes + (16 * ks + 2 * tq) * 2;
+                    qa[ks][0] = grp < G ? *reinterpret_cast<const uint32_t *>(row) : 0u;
+                    qa[ks][1] = grp < G ? *reinterpret_cast<const uint32_t *>(row + 16) : 0u;
                 }
-            __syncwarp();
-            if (lane == 0 && !bad) mbar_arrive(&qempty[slot]);
-        }
-        if (bad || done) {
-            it.b = -1;
-            it.pg0 = it.pg1 = 0;
-        }
-
-        float m_own = -INFINITY, l_own = 0.f;
-        float2 o[G][C::kPvDims / 2];
-#pragma unroll
-        for (int h = 0; h < G; ++h)
-#pragma unroll
-            for (int d = 0; d < C::kPvDims / 2; ++d) o[h][d] = make_float2(0.f, 0.f);
-
-        // Pages of this item for this warp: page_ctr advances over every page of
-        // the item; this warp takes those with page_ctr % kConsumerWarps == cw.
-        const int first = (cw - static_cast<int>(page_ctr % kConsumerWarps) + kConsumerWarps) %
-                          kConsumerWarps;
-        for (int pg = it.pg0 + first; pg < it.pg1; pg += kConsumerWarps) {
-            const uint32_t c = page_ctr + (pg - it.pg0);
-            const uint32_t s = c % kStages, k = c / kStages;
-            if (!__all_sync(0xffffffffu, mbar_wait_bounded(&full[s], k & 1, kWaitLimitNs)) ||
-                *static_cast<volatile int *>(&s_abort)) {
-                bad = true;
-                break;
+                __syncwarp();
+                if (lane == 0 && !bad) mbar_arrive(&qempty[slot]);
             }
-            const unsigned char *Ks = smem + s * 2 * C::kPageBytes;
-            const unsigned char *Vs = Ks + C::kPageBytes;
-            const int t_lo = max(0, it.tok0 - pg * kBlock);
-            const int t_hi = min(kBlock, it.tok1 - pg * kBlock);
-            if (t_lo == 0 && t_hi == kBlock)
-                consume_page<T, D, G, true>(Ks, Vs, 0, kBlock, qf, m_own, l_own, o, W2, lane);
-            else
-                consume_page<T, D, G, false>(Ks, Vs, t_lo, t_hi, qf, m_own, l_own, o, W2, lane);
-            if (lane == 0) mbar_arrive(&empty[s]);
-        }
-        page_ctr += static_cast<uint32_t>(it.pg1 - it.pg0);
-        if (bad && lane == 0) {
-            raise_flag(p.err_flag, XS_FLAG_TIMEOUT);
-            atomicExch(&s_abort, 1);
-        }
-
-        // ---- hand this warp's state to the merger (buffer item_ctr % kMergeBufs;
-        // a buffer is reused once the merger has freed it).
-        const int buf = item_ctr % C::kMergeBufs;
-        unsigned char *mb = smem + C::kCombOff + buf * C::kCombBytes;
-        if (!__all_sync(0xffffffffu, mbar_wait_bounded(&freed[buf],
-                                                       ((item_ctr / C::kMergeBufs) & 1) ^ 1,
-                                                       kWaitLimitNs))) {
-            if (lane == 0) {
+            if (bad || done) {
+                it.b = -1;
+                it.pg0 = it.pg1 = 0;
+            }
+            float m_row = -INFINITY, l_lane = 0.f;
+            float oacc[D / 8][4];
+#pragma unroll
+            for (int n = 0; n < D / 8; ++n)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) oacc[n][c] = 0.f;
+            const int first = (cw - static_cast<int>(page_ctr % kConsumerWarps) + kConsumerWarps) %
+                              kConsumerWarps;
+            for (int pg = it.pg0 + first; pg < it.pg1; pg += kConsumerWarps) {
+                const uint32_t c = page_ctr + (pg - it.pg0);
+                const uint32_t s = c % kStages, k = c / kStages;
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(&full[s], k & 1, kWaitLimitNs)) ||
+                    *static_cast<volatile int *>(&s_abort)) {
+                    bad = true;
+                    break;
+                }
+                const uint32_t kaddr = smem_addr(smem + s * 2 * C::kPageBytes);
+                const int t_lo = max(0, it.tok0 - pg * kBlock);
+                const int t_hi = min(kBlock, it.tok1 - pg * kBlock);
+                if (t_lo == 0 && t_hi == kBlock)
+                    consume_page_mma<D, true>(kaddr, kaddr + C::kPageBytes, 0, kBlock, qa, p.qscale,
+                                              m_row, l_lane, oacc, lane);
+                else
+                    consume_page_mma<D, false>(kaddr, kaddr + C::kPageBytes, t_lo, t_hi, qa,
+                                               p.qscale, m_row, l_lane, oacc, lane);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[s]);
+            }
+            page_ctr += static_cast<uint32_t>(it.pg1 - it.pg0);
+            if (bad && lane == 0) {
                 raise_flag(p.err_flag, XS_FLAG_TIMEOUT);
                 atomicExch(&s_abort, 1);
             }
-            break;
-        }
-        float *cM = reinterpret_cast<float *>(mb + 32);
-        float *cL = cM + kConsumerWarps * G;
-        float *cO = cL + kConsumerWarps * G;
-        if (cw == 0 && lane == 0) *reinterpret_cast<Item *>(mb) = it;
-        if (!done) {
+            const int buf = item_ctr % C::kMergeBufs;
+            unsigned char *mb = smem + C::kCombOff + buf * C::kCombBytes;
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(&freed[buf],
+                                                           ((item_ctr / C::kMergeBufs) & 1) ^ 1,
+                                                           kWaitLimitNs))) {
+                if (lane == 0) {
+                    raise_flag(p.err_flag, XS_FLAG_TIMEOUT);
+                    atomicExch(&s_abort, 1);
+                }
+                break;
+            }
+            float *cM = reinterpret_cast<float *>(mb + 32);
+            float *cL = cM + kConsumerWarps * G;
+            float *cO = cL + kConsumerWarps * G;
+            if (cw == 0 && lane == 0) *reinterpret_cast<Item *>(mb) = it;
+            float l_row = l_lane + __shfl_xor_sync(0xffffffffu, l_lane, 1);
+            l_row += __shfl_xor_sync(0xffffffffu, l_row, 2);
+            if (!done && grp < G) {
+                float *dst = &cO[(cw * G + grp) * D + 2 * tq];
 #pragma unroll
-            for (int h = 0; h < G; ++h) {
-                float *dst = &cO[(cw * G + h) * D + lane * C::kPvDims];
-                if constexpr (C::kPvDims == 4)
-                    *reinterpret_cast<float4 *>(dst) =
-                        make_float4(o[h][0].x, o[h][0].y, o[h][1].x, o[h][1].y);
-                else
-                    *reinterpret_cast<float2 *>(dst) = o[h][0];
+                for (int n = 0; n < D / 8; ++n)
+                    *reinterpret_cast<float2 *>(dst + 8 * n) = make_float2(oacc[n][0], oacc[n][1]);
+                if (tq == 0) {
+                    cM[cw * G + grp] = m_row;
+                    cL[cw * G + grp] = l_row;
+                }
             }
-            if (lane < 8 && (j & ((1 << C::kHeadShift) - 1)) == 0) {
-                const int own_head = j >> C::kHeadShift;
-                cM[cw * G + own_head] = m_own;
-                cL[cw * G + own_head] = l_own;
-            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&merged[buf]);
+            if (done || *static_cast<volatile int *>(&s_abort)) break;
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&merged[buf]);
-        if (done || *static_cast<volatile int *>(&s_abort)) break;
+    } else {
+        const int j = lane & 7;
+        float2 *W2 = reinterpret_cast<float2 *>(smem + C::kWOff) + cw * kBlock * G;
+        uint32_t page_ctr = 0;
+
+        for (uint32_t item_ctr = 0;; ++item_ctr) {
+            // Every consumer sees the producer's end marker (b < 0) in the same
+            // slot and leaves; warp 0 passes the marker on to the merger.  A
+            // failed (timed-out) wait marks the item bad: the warp skips its pages.
+            // All waits in the CTA are bounded, so no warp can wait forever.
+            const uint32_t slot = item_ctr & 1;
+            bool bad = !__all_sync(0xffffffffu,
+                                   mbar_wait_bounded(&qfull[slot], (item_ctr >> 1) & 1, kWaitLimitNs));
+            Item it = item_slot[slot];
+            const bool done = !bad && it.b < 0;
+            float qf[G][C::kQkDims];
+            if (!done) {
+                const unsigned char *qs = smem + C::kQSlotOff + slot * C::kQBytes;
+    #pragma unroll
+                for (int h = 0; h < G; ++h)
+    #pragma unroll
+                    for (int c = 0; c < C::kChunksPerLane; ++c) {
+                        const uint4 raw = *reinterpret_cast<const uint4 *>(
+                            qs + h * C::kRowBytes + (j + 8 * c) * 16);
+                        float f[C::kElemsPerChunk];
+                        unpack16(raw, f, static_cast<T *>(nullptr));
+    #pragma unroll
+                        for (int e = 0; e < C::kElemsPerChunk; ++e)
+                            qf[h][c * C::kElemsPerChunk + e] = f[e] * p.qscale;
+                    }
+                __syncwarp();
+                if (lane == 0 && !bad) mbar_arrive(&qempty[slot]);
+            }
+            if (bad || done) {
+                it.b = -1;
+                it.pg0 = it.pg1 = 0;
+            }
+
+            float m_own = -INFINITY, l_own = 0.f;
+            float2 o[G][C::kPvDims / 2];
+    #pragma unroll
+            for (int h = 0; h < G; ++h)
+    #pragma unroll
+                for (int d = 0; d < C::kPvDims / 2; ++d) o[h][d] = make_float2(0.f, 0.f);
+
+            // Pages of this item for this warp: page_ctr advances over every page of
+            // the item; this warp takes those with page_ctr % kConsumerWarps == cw.
+            const int first = (cw - static_cast<int>(page_ctr % kConsumerWarps) + kConsumerWarps) %
+                              kConsumerWarps;
+            for (int pg = it.pg0 + first; pg < it.pg1; pg += kConsumerWarps) {
+                const uint32_t c = page_ctr + (pg - it.pg0);
+                const uint32_t s = c % kStages, k = c / kStages;
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(&full[s], k & 1, kWaitLimitNs)) ||
+                    *static_cast<volatile int *>(&s_abort)) {
+                    bad = true;
+                    break;
+                }
+                const unsigned char *Ks = smem + s * 2 * C::kPageBytes;
+                const unsigned char *Vs = Ks + C::kPageBytes;
+                const int t_lo = max(0, it.tok0 - pg * kBlock);
+                const int t_hi = min(kBlock, it.tok1 - pg * kBlock);
+                if (t_lo == 0 && t_hi == kBlock)
+                    consume_page<T, D, G, true>(Ks, Vs, 0, kBlock, qf, m_own, l_own, o, W2, lane);
+                else
+                    consume_page<T, D, G, false>(Ks, Vs, t_lo, t_hi, qf, m_own, l_own, o, W2, lane);
+                if (lane == 0) mbar_arrive(&empty[s]);
+            }
+            page_ctr += static_cast<uint32_t>(it.pg1 - it.pg0);
+            if (bad && lane == 0) {
+                raise_flag(p.err_flag, XS_FLAG_TIMEOUT);
+                atomicExch(&s_abort, 1);
+            }
+
+            // ---- hand this warp's state to the merger (buffer item_ctr % kMergeBufs;
+            // a buffer is reused once the merger has freed it).
+            const int buf = item_ctr % C::kMergeBufs;
+            unsigned char *mb = smem + C::kCombOff + buf * C::kCombBytes;
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(&freed[buf],
+                                                           ((item_ctr / C::kMergeBufs) & 1) ^ 1,
+                                                           kWaitLimitNs))) {
+                if (lane == 0) {
+                    raise_flag(p.err_flag, XS_FLAG_TIMEOUT);
+                    atomicExch(&s_abort, 1);
+                }
+                break;
+            }
+            float *cM = reinterpret_cast<float *>(mb + 32);
+            float *cL = cM + kConsumerWarps * G;
+            float *cO = cL + kConsumerWarps * G;
+            if (cw == 0 && lane == 0) *reinterpret_cast<Item *>(mb) = it;
+            if (!done) {
+    #pragma unroll
+                for (int h = 0; h < G; ++h) {
+                    float *dst = &cO[(cw * G + h) * D + lane * C::kPvDims];
+                    if constexpr (C::kPvDims == 4)
+                        *reinterpret_cast<float4 *>(dst) =
+                            make_float4(o[h][0].x, o[h][0].y, o[h][1].x, o[h][1].y);
+                    else
+                        *reinterpret_cast<float2 *>(dst) = o[h][0];
+                }
+                if (lane < 8 && (j & ((1 << C::kHeadShift) - 1)) == 0) {
+                    const int own_head = j >> C::kHeadShift;
+                    cM[cw * G + own_head] = m_own;
+                    cL[cw * G + own_head] = l_own;
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&merged[buf]);
+            if (done || *static_cast<volatile int *>(&s_abort)) break;
+        }
     }
 }
 
@@ -1053,7 +1284,7 @@ __global__ void paged_decode_reduce_kernel(T *__restrict__ out, const float *__r
 
 // ------------------------------------------------------------------ host side
 
-using KernelFn = void (*)(Params);
+using KernelFn = void (*)(const CUtensorMap, const CUtensorMap, const Params);
 
 template <typename T, int D, int G>
 KernelFn kernel_for() {
@@ -1149,6 +1380,40 @@ int occupancy(KernelFn fn, int smem, int *per_sm) {
     *per_sm = n > 0 ? n : 1;
     Entry e{fn, dev, smem, *per_sm};
     if (n_cached < 64) cache[n_cached++] = e;  // a full cache just stops caching
+    return XS_OK;
+}
+
+// Tensor maps of a K and a V pool (bf16), cached per pool and shape: a
+// decode loop launches over the same pools every step.
+int pool_maps(const void *k, const void *v, int64_t num_blocks, int Hkv, int D, CUtensorMap *tmk,
+              CUtensorMap *tmv) {
+    struct Entry {
+        const void *k, *v;
+        int64_t nb;
+        int hkv, d;
+        CUtensorMap mk, mv;
+    };
+    static std::mutex mu;
+    static Entry cache[16];
+    static int n_cached = 0, next = 0;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < n_cached; ++i)
+        if (cache[i].k == k && cache[i].v == v && cache[i].nb == num_blocks &&
+            cache[i].hkv == Hkv && cache[i].d == D) {
+            *tmk = cache[i].mk;
+            *tmv = cache[i].mv;
+            return XS_OK;
+        }
+    const cuuint64_t dims[4] = {64, kBlock, static_cast<cuuint64_t>(D / 64),
+                                static_cast<cuuint64_t>(num_blocks) * Hkv};
+    const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2, 128,
+                                   static_cast<cuuint64_t>(kBlock) * D * 2};
+    const cuuint32_t box[4] = {64, kBlock, static_cast<cuuint32_t>(D / 64), 1};
+    int st = encode_bf16_map<4>(tmk, k, dims, strides, box);
+    if (st == XS_OK) st = encode_bf16_map<4>(tmv, v, dims, strides, box);
+    if (st != XS_OK) return st;
+    Entry &e = cache[n_cached < 16 ? n_cached++ : (next++ % 16)];
+    e = Entry{k, v, num_blocks, Hkv, D, *tmk, *tmv};
     return XS_OK;
 }
 
@@ -1274,13 +1539,24 @@ static int launch_attn(void *out, float *part_o, float *part_m, float *part_l, c
     int smem0 = 0;
     attn::KernelFn fn = attn::pick_kernel(dtype, D, Hq / Hkv, &smem0);
     if (!fn) return XS_EUNSUPPORTED;
-    const int smem = smem0 + attn::table_bytes(B);  // = Cfg<...>::smem_bytes(B)
+    const int smem = smem0 + attn::table_bytes(B) + 1024;  // = Cfg<...>::smem_bytes(B)
     if (smem + 1024 > dev.max_smem_optin) return XS_EUNSUPPORTED;  // room for static smem
     int per_sm = 1;
     if ((st = attn::occupancy(fn, smem, &per_sm)) != XS_OK) return st;
     const int64_t max_items = static_cast<int64_t>(B) * Hkv * max_partitions;
     const int64_t resident = static_cast<int64_t>(dev.sms) * per_sm;
     const int grid = static_cast<int>(std::max<int64_t>(1, std::min(max_items, resident)));
+    // bf16 pages travel as TMA tensor copies: the pools as 4-D (64 elements,
+    // 16 rows, D/64 halves, num_blocks * Hkv pages) with strides (2 D, 128,
+    // 32 D) bytes, one box (64, 16, D/64, 1) per page.  fp32 uses 1-D copies.
+    CUtensorMap tmk, tmv;
+    memset(&tmk, 0, sizeof(tmk));
+    memset(&tmv, 0, sizeof(tmv));
+    if (dtype == XS_BF16) {
+        if (num_blocks * Hkv > 0x7fffffff) return XS_EUNSUPPORTED;  // 32-bit page coordinate
+        if ((st = attn::pool_maps(k_cache, v_cache, num_blocks, Hkv, D, &tmk, &tmv)) != XS_OK)
+            return st;
+    }
     attn::Params p;
     p.out = out;
     p.part_o = part_o;
@@ -1318,7 +1594,7 @@ static int launch_attn(void *out, float *part_o, float *part_m, float *part_l, c
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, fn, p) != cudaSuccess) {
+    if (cudaLaunchKernelEx(&cfg, fn, tmk, tmv, p) != cudaSuccess) {
         cudaGetLastError();
         return XS_ELAUNCH;
     }
