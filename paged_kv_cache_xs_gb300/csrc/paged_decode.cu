@@ -131,7 +131,16 @@ struct Params {
     // split sequence-head combines its partials into out; null = leave the
     // partials for the separate combine kernel.
     int *combine;
+    // Shared memory after the per-sequence tables where the merger stages
+    // partial rows for a combine: stage_parts partials (x G heads x D fp32)
+    // per round trip; stage_bytes is what the launch added for it.
+    int stage_bytes, stage_parts;
 };
+
+// Byte offset of the combine staging area (16-byte aligned, after the tables).
+__host__ __device__ constexpr int stage_offset(int prefix_off, int B) {
+    return (prefix_off + table_bytes(B) + 15) / 16 * 16;
+}
 
 // Number of tokens sequence b attends to, clamped to the table's reach.
 __device__ __forceinline__ int seq_len(const Params &p, int b, bool report) {
@@ -173,34 +182,46 @@ __device__ __forceinline__ int upper_index(const int *table, int B, int x, int l
     return lo + 31 - __clz(__ballot_sync(0xffffffffu, le));
 }
 
-// Item numbering.  Without the fused combine: first every full partition (P
-// tokens) of every sequence and KV head, in sequence order, then the ragged
-// last partitions (and short sequences) - so the end of a launch is made of
-// small items that balance the grid.  With it, the ragged partitions come
-// first: a sequence-head group is complete when its last item is, and with
-// the ragged ones last every group would complete - and be combined - in the
-// launch's final moments; full partitions last make groups complete, and
-// combine, all along.  pfull/ptail are the exclusive prefix sums of the
-// per-sequence counts of full and ragged items.
+// Item numbering: two classes of items, class A numbered before class B,
+// each in sequence order; pfull/ptail hold the exclusive prefix sums of the
+// per-sequence counts of class A and class B items (item_counts).
+//
+// Without the fused combine, A = every full partition (P tokens) of every
+// sequence and KV head, B = the ragged last partitions (and short
+// sequences): the end of a launch is made of small items that balance the
+// grid.  With it, A = all items of the sequences split into more than one
+// partition, group by group ((b, g) then the partition), and B = the
+// sequences that fit one partition (one item per KV head, no combine).  The
+// partitions of a group are taken back to back, finish together, and the
+// group is combined while the rest of the grid still streams pages; the
+// launch ends on single-partition items, which write their output directly.
+__device__ __forceinline__ void item_counts(const Params &p, int nw, int &ca, int &cb) {
+    if (p.combine) {
+        const int np = (nw + p.P - 1) / p.P;
+        ca = np > 1 ? np * p.Hkv : 0;
+        cb = np == 1 ? p.Hkv : 0;
+    } else {
+        ca = (nw / p.P) * p.Hkv;
+        cb = (nw % p.P != 0) * p.Hkv;
+    }
+}
+
 __device__ __forceinline__ Item decode_item(const Params &p, const int *pfull, const int *ptail,
                                             const int *nlen, int item, int lane) {
     Item it;
-    const bool tails_first = p.combine != nullptr;
-    const int n_full = pfull[p.B], n_tail = ptail[p.B];
-    const int full_idx = tails_first ? item - n_tail : item;
-    const int tail_idx = tails_first ? item : item - n_full;
-    const bool is_full = tails_first ? item >= n_tail : item < n_full;
+    const int n_a = pfull[p.B];
     int b;
-    if (is_full) {
-        b = upper_index(pfull, p.B, full_idx, lane);
-        const int r = full_idx - pfull[b];
-        const int nf = (pfull[b + 1] - pfull[b]) / p.Hkv;
-        it.g = r / nf;
-        it.part = r - it.g * nf;
+    if (item < n_a) {
+        b = upper_index(pfull, p.B, item, lane);
+        const int r = item - pfull[b];
+        const int na = (pfull[b + 1] - pfull[b]) / p.Hkv;  // class-A items per KV head
+        it.g = r / na;
+        it.part = r - it.g * na;
     } else {
-        b = upper_index(ptail, p.B, tail_idx, lane);
-        it.g = tail_idx - ptail[b];
-        it.part = (nlen[b] - first_token(p, nlen[b])) / p.P;
+        const int j = item - n_a;
+        b = upper_index(ptail, p.B, j, lane);
+        it.g = j - ptail[b];
+        it.part = p.combine ? 0 : (nlen[b] - first_token(p, nlen[b])) / p.P;
     }
     it.b = b;
     const int n = nlen[b], t0 = first_token(p, n);
@@ -366,68 +387,99 @@ __device__ __forceinline__ void consume_page(const unsigned char *Ks, const unsi
 // Lane j holds m and l of partials j, j + 32, ... (one load round for up to
 // 32 partials), the weights reach the other lanes by shuffles, and the
 // partial rows are loaded 16 at a time, all G heads together.
+// The merger's staging area: an mbarrier, its phase, then the rows.
+struct Stage {
+    uint64_t bar;
+    uint32_t phase;
+    uint32_t pad;
+    __device__ float *rows() { return reinterpret_cast<float *>(this + 1); }
+};
+static_assert(sizeof(Stage) == 16, "staged rows start 16 bytes in");
+
+// Split-K combine of one (sequence, KV head) group by one warp: for each of
+// the G heads, out = sum_j e^(m_j - M) o_j / sum_j e^(m_j - M) l_j over the
+// group's np partials (o_j already divided by l_j's partition sum, so the
+// weight of o_j is e^(m_j - M) l_j).  Partials are taken stage_parts at a
+// time: for each head, the chunk's rows are contiguous in part_o and arrive
+// in the staging area by one bulk copy (the copy engine, not the load unit),
+// while lane k loads m and l of partial k, so a chunk costs one memory round
+// trip; the running maximum M is raised per chunk and what was accumulated
+// is rescaled.  The caller has acquired the partials (generic proxy); the
+// proxy fence below orders the bulk copies after that.  Returns false if a
+// copy did not complete in time (nothing is written then).
 template <typename T, int D, int G>
-__device__ __noinline__ void combine_partials(const Params &p, const Item &it, int64_t head0,
-                                              int lane) {
-    constexpr int kDims = D / 32;              // output dims per lane
-    constexpr int kJ = G >= 16 ? 1 : 16 / G;   // partials per batch (16 row loads in flight)
+__device__ __noinline__ bool combine_partials(const Params &p, const Item &it, int64_t head0,
+                                              int lane, Stage *stage) {
+    constexpr int kDims = D / 32;   // output dims per lane
     using Vec = typename std::conditional<kDims == 4, float4, float2>::type;
     const int np = it.nparts;
+    const int K = p.stage_parts;
     const float *pm = p.part_m + head0 * p.max_parts;
     const float *pl = p.part_l + head0 * p.max_parts;
-    const float *po = p.part_o + head0 * p.max_parts * D + lane * kDims;
-    float acc[G][kDims], den[G];
+    float *rows = stage->rows();
+    float acc[G][kDims], den[G], run_m[G];
 #pragma unroll
     for (int h = 0; h < G; ++h) {
         den[h] = 0.f;
+        run_m[h] = -INFINITY;
 #pragma unroll
         for (int d = 0; d < kDims; ++d) acc[h][d] = 0.f;
     }
-    // Maximum per head over all partials.
-    float mx[G];
+    for (int j0 = 0; j0 < np; j0 += K) {
+        const int cnt = min(K, np - j0);
+        // Row h * cnt + k of the staging area receives partial j0 + k of head h.
+        const uint32_t phase = stage->phase;
+        if (lane == 0) {
+            fence_proxy_async_global();  // partials acquired above -> async-proxy reads
+            fence_proxy_async_shared();  // last chunk's reads of the rows -> overwrite
+            mbar_arrive_expect_tx(&stage->bar, static_cast<uint32_t>(G * cnt * D * 4));
 #pragma unroll
-    for (int h = 0; h < G; ++h) mx[h] = -INFINITY;
-    for (int j = lane; j < np; j += 32)
-#pragma unroll
-        for (int h = 0; h < G; ++h) mx[h] = fmaxf(mx[h], __ldcg(pm + h * p.max_parts + j));
-#pragma unroll
-    for (int h = 0; h < G; ++h)
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], o));
-    for (int j0 = 0; j0 < np; j0 += 32) {
-        // Weights of partials j0 .. j0 + 31, partial j0 + k in lane k.
+            for (int h = 0; h < G; ++h)
+                bulk_g2s(rows + h * cnt * D, p.part_o + ((head0 + h) * p.max_parts + j0) * D,
+                         static_cast<uint32_t>(cnt * D * 4), &stage->bar);
+        }
         float wgt[G];
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-            wgt[h] = 0.f;
-            if (j0 + lane < np) {
-                const int64_t r = static_cast<int64_t>(h) * p.max_parts + j0 + lane;
-                wgt[h] = fast_exp2(__ldcg(pm + r) - mx[h]) * __ldcg(pl + r);
+            float mj = -INFINITY, lj = 0.f;
+            if (lane < cnt) {
+                mj = __ldcg(pm + h * p.max_parts + j0 + lane);
+                lj = __ldcg(pl + h * p.max_parts + j0 + lane);
             }
-            den[h] += wgt[h];
+            float cm = mj;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, o));
+            const float m_new = fmaxf(run_m[h], cm);
+            const float ref = m_new == -INFINITY ? 0.f : m_new;
+            const float corr = fast_exp2(run_m[h] - ref);  // 0 while nothing is accumulated
+            run_m[h] = m_new;
+            wgt[h] = lane < cnt ? fast_exp2(mj - ref) * lj : 0.f;
+            den[h] = den[h] * corr + wgt[h];
+#pragma unroll
+            for (int d = 0; d < kDims; ++d) acc[h][d] *= corr;
         }
-        const int cnt = min(32, np - j0);
-        for (int k0 = 0; k0 < cnt; k0 += kJ) {
-            Vec v[kJ][G];
-#pragma unroll
-            for (int u = 0; u < kJ; ++u)
-#pragma unroll
-                for (int h = 0; h < G; ++h) {
-                    const int k = min(k0 + u, cnt - 1);  // past the end: reload, weight 0
-                    v[u][h] = __ldcg(reinterpret_cast<const Vec *>(
-                        po + (static_cast<int64_t>(h) * p.max_parts + j0 + k) * D));
-                }
-#pragma unroll
-            for (int u = 0; u < kJ; ++u)
-#pragma unroll
-                for (int h = 0; h < G; ++h) {
-                    const float w0 = __shfl_sync(0xffffffffu, wgt[h], (k0 + u) & 31);
-                    const float w = k0 + u < cnt ? w0 : 0.f;
-                    const float *f = reinterpret_cast<const float *>(&v[u][h]);
-#pragma unroll
-                    for (int d = 0; d < kDims; ++d) acc[h][d] += w * f[d];
-                }
+        const bool landed =
+            __all_sync(0xffffffffu, mbar_wait_bounded(&stage->bar, phase, kWaitLimitNs));
+        __syncwarp();
+        if (lane == 0) stage->phase = phase ^ 1u;
+        if (!landed) {
+            // The caller flags it; first give the copies in flight (bounded)
+            // time to land, so none writes into this CTA's memory after it exits.
+            if (lane == 0) mbar_wait_bounded(&stage->bar, phase, kWaitLimitNs);
+            __syncwarp();
+            return false;
         }
+        for (int k = 0; k < cnt; ++k) {
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                const float w = __shfl_sync(0xffffffffu, wgt[h], k);
+                const Vec v = *reinterpret_cast<const Vec *>(rows + (h * cnt + k) * D + lane * kDims);
+                const float *f = reinterpret_cast<const float *>(&v);
+#pragma unroll
+                for (int d = 0; d < kDims; ++d) acc[h][d] += w * f[d];
+            }
+        }
+        __syncwarp();  // the next chunk overwrites the staging area
     }
 #pragma unroll
     for (int h = 0; h < G; ++h) {
@@ -436,12 +488,13 @@ __device__ __noinline__ void combine_partials(const Params &p, const Item &it, i
         for (int o = 16; o > 0; o >>= 1) lt += __shfl_xor_sync(0xffffffffu, lt, o);
         if (p.sinks)
             lt += fast_exp2(Elem<T>::to_f32(static_cast<const T *>(p.sinks)[it.g * G + h]) * kLog2e -
-                            mx[h]);
+                            run_m[h]);
         const float inv = 1.f / lt;
         T *dst = static_cast<T *>(p.out) + (head0 + h) * D + lane * kDims;
 #pragma unroll
         for (int d = 0; d < kDims; ++d) dst[d] = Elem<T>::from_f32(acc[h][d] * inv);
     }
+    return true;
 }
 
 // ---- bf16 tensor-core pieces (the page layout they read is the one the
@@ -564,8 +617,8 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *tm,
 // raised (all in flight together) and every entry that completes its group
 // combines it and clears the count for the next launch.
 template <typename T, int D, int G>
-__device__ __noinline__ void count_and_combine(const Params &p, int lane, int pend_b, int pend_g,
-                                               int pend_np, int npend) {
+__device__ __noinline__ bool count_and_combine(const Params &p, int lane, int pend_b, int pend_g,
+                                               int pend_np, int npend, Stage *stage) {
     __threadfence();
     __syncwarp();
     int *cnt = p.combine + static_cast<int64_t>(pend_b) * p.Hkv + pend_g;
@@ -575,7 +628,8 @@ __device__ __noinline__ void count_and_combine(const Params &p, int lane, int pe
     if (last) atomicExch(cnt, 0);
     unsigned todo = __ballot_sync(0xffffffffu, last);
     if (todo) __threadfence();
-    while (todo) {
+    bool ok = true;
+    while (todo && ok) {
         const int k = __ffs(todo) - 1;
         todo &= todo - 1;
         Item ci;
@@ -583,8 +637,9 @@ __device__ __noinline__ void count_and_combine(const Params &p, int lane, int pe
         ci.g = __shfl_sync(0xffffffffu, pend_g, k);
         ci.nparts = __shfl_sync(0xffffffffu, pend_np, k);
         const int64_t h0 = static_cast<int64_t>(ci.b) * p.Hq + static_cast<int64_t>(ci.g) * G;
-        combine_partials<T, D, G>(p, ci, h0, lane);
+        ok = combine_partials<T, D, G>(p, ci, h0, lane, stage);
     }
+    return ok;
 }
 
 template <typename T, int D, int G>
@@ -613,7 +668,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
 
     // The launch must provide the shared memory this B needs; refuse (flag,
     // return before touching shared memory) if it does not.
-    if (dynamic_smem_bytes() < static_cast<uint32_t>(C::smem_bytes(p.B))) {
+    if (dynamic_smem_bytes() < static_cast<uint32_t>(C::smem_bytes(p.B) + p.stage_bytes) ||
+        (p.combine && p.stage_parts < 1)) {
         if (tid == 0) raise_flag(p.err_flag, XS_FLAG_CONFIG);
         return;
     }
@@ -632,6 +688,11 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
             mbar_init(&merged[s], kConsumerWarps);
             mbar_init(&freed[s], 1);
         }
+        if (p.combine) {
+            Stage *st = reinterpret_cast<Stage *>(smem + stage_offset(C::kPrefixOff, p.B));
+            mbar_init(&st->bar, 1);
+            st->phase = 0;
+        }
         mbar_fence_init();
         s_abort = 0;
     }
@@ -643,17 +704,17 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
     griddep_launch_dependents();
     griddep_wait();
     {
-        // Per sequence: nw/P full partitions and (nw % P != 0) ragged one, each
-        // x Hkv heads (nw = tokens inside the window).  Chunked scan of both
-        // counts over the block.
+        // Per sequence: its class A and class B item counts (item_counts).
+        // Chunked scan of both counts over the block.
         const int per = (p.B + kThreads - 1) / kThreads;
         const int b0 = min(p.B, tid * per), b1 = min(p.B, b0 + per);
         int lf = 0, lt = 0;
         for (int b = b0; b < b1; ++b) {
             const int n = max(seq_len(p, b, blockIdx.x == 0), 0);
-            const int nw = n - first_token(p, n);  // tokens inside the window
-            lf += (nw / p.P) * p.Hkv;
-            lt += (nw % p.P != 0) * p.Hkv;
+            int ca, cb;
+            item_counts(p, n - first_token(p, n), ca, cb);  // tokens inside the window
+            lf += ca;
+            lt += cb;
         }
         int xf = lf, xt = lt;
 #pragma unroll
@@ -679,12 +740,13 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
         int runf = basef + xf - lf, runt = baset + xt - lt;  // exclusive prefixes
         for (int b = b0; b < b1; ++b) {
             const int n = max(seq_len(p, b, false), 0);
-            const int nw = n - first_token(p, n);
+            int ca, cb;
+            item_counts(p, n - first_token(p, n), ca, cb);
             pfull[b] = runf;
             ptail[b] = runt;
             nlen[b] = n;
-            runf += (nw / p.P) * p.Hkv;
-            runt += (nw % p.P != 0) * p.Hkv;
+            runf += ca;
+            runt += cb;
         }
         if (tid == kThreads - 1) {
             pfull[p.B] = basef + xf;
@@ -950,9 +1012,14 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
         // full, or the consumers are done.
         constexpr int kMaxPend = 8;
         int pend_b = 0, pend_g = 0, pend_np = 0, npend = 0;
+        Stage *stage = reinterpret_cast<Stage *>(smem + stage_offset(C::kPrefixOff, p.B));
         auto flush = [&]() {
             if (npend == 0) return;
-            count_and_combine<T, D, G>(p, lane, pend_b, pend_g, pend_np, npend);
+            if (!count_and_combine<T, D, G>(p, lane, pend_b, pend_g, pend_np, npend, stage) &&
+                lane == 0) {
+                raise_flag(p.err_flag, XS_FLAG_TIMEOUT);
+                atomicExch(&s_abort, 1);
+            }
             npend = 0;
         };
         for (uint32_t item_ctr = 0;; ++item_ctr) {
@@ -1314,6 +1381,8 @@ KernelFn pick_kernel(int dtype, int D, int G, int *smem_base_fn_B0) {
 struct DeviceInfo {
     int sms = 0;
     int max_smem_optin = 0;
+    int smem_per_sm = 0;         // shared memory of one SM
+    int reserved_per_block = 0;  // what the system keeps of it per resident CTA
 };
 
 int device_info(DeviceInfo *info) {
@@ -1326,11 +1395,40 @@ int device_info(DeviceInfo *info) {
         DeviceInfo d;
         if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin,
+                                   dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor,
+                                   dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.reserved_per_block, cudaDevAttrReservedSharedMemoryPerBlock,
                                    dev) != cudaSuccess)
             return XS_EDEVICE;
         cache[dev] = d;
     }
     *info = cache[dev];
+    return XS_OK;
+}
+
+// Static shared memory of a kernel, cached.
+int static_smem(KernelFn fn, int *bytes) {
+    struct Entry {
+        KernelFn fn;
+        int bytes;
+    };
+    static std::mutex mu;
+    static Entry cache[32];
+    static int n_cached = 0;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < n_cached; ++i)
+        if (cache[i].fn == fn) {
+            *bytes = cache[i].bytes;
+            return XS_OK;
+        }
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, reinterpret_cast<const void *>(fn)) != cudaSuccess) {
+        cudaGetLastError();
+        return XS_ELAUNCH;
+    }
+    *bytes = static_cast<int>(fa.sharedSizeBytes);
+    if (n_cached < 32) cache[n_cached++] = Entry{fn, *bytes};
     return XS_OK;
 }
 
@@ -1465,8 +1563,13 @@ extern "C" int xs_paged_decode_step_partition_tokens(int B, int Hq, int Hkv,
     // The cost model of xs_paged_decode_partition_tokens plus the in-launch
     // combine: the groups that complete last are combined after every page
     // is read, by one warp each, at about one memory round trip (~ one page
-    // time) per 16 partial rows (G heads per partial) plus three.
-    constexpr double kItemCost = 1.5;
+    // time) per 8 partials staged in shared memory, plus two (the count).
+    // With the tensor-core page loop a page costs less, so the fixed cost
+    // of an item (q staging, first-page latency, the merge, and the
+    // combines the merge warp runs meanwhile) weighs more: kItemCost is
+    // fitted to one-launch step times measured on the mix, single-stream and
+    // long-batch workloads (mix: 65 / 52 / 55 us at P = 256 / 512 / 1024).
+    constexpr double kItemCost = 6.0;
     const double ctas = 2.0 * num_sms;
     const double G = static_cast<double>(Hq / Hkv);
     int best = 64;
@@ -1474,7 +1577,7 @@ extern "C" int xs_paged_decode_step_partition_tokens(int B, int Hq, int Hkv,
     for (int P = 64; P <= 2048; P *= 2) {
         const double items = std::max((tokens / P + 0.5 * B) * Hkv, static_cast<double>(B) * Hkv);
         const double np_max = std::ceil(std::max(max_context_len, 1) / static_cast<double>(P));
-        const double combine = np_max > 1.0 ? np_max * G / 16.0 + 3.0 : 0.0;
+        const double combine = np_max > 1.0 ? std::ceil(np_max / 8.0) + 2.0 : 0.0;
         const double cost = (items / ctas + 1.0) * (P / 64.0 + kItemCost) + combine;
         if (cost <= best_cost * (1.0 + 1e-9)) {
             best_cost = cost;
@@ -1539,10 +1642,26 @@ static int launch_attn(void *out, float *part_o, float *part_m, float *part_l, c
     int smem0 = 0;
     attn::KernelFn fn = attn::pick_kernel(dtype, D, Hq / Hkv, &smem0);
     if (!fn) return XS_EUNSUPPORTED;
-    const int smem = smem0 + attn::table_bytes(B) + 1024;  // = Cfg<...>::smem_bytes(B)
+    int smem = smem0 + attn::table_bytes(B) + 1024;  // = Cfg<...>::smem_bytes(B)
     if (smem + 1024 > dev.max_smem_optin) return XS_EUNSUPPORTED;  // room for static smem
     int per_sm = 1;
     if ((st = attn::occupancy(fn, smem, &per_sm)) != XS_OK) return st;
+    // The in-launch combine stages partial rows in shared memory: as many
+    // partials (G rows of D fp32 each) as fit beside the CTAs that are
+    // resident anyway, at least one, at most 32 or 32 KB.
+    int stage_bytes = 0, stage_parts = 0;
+    if (combine) {
+        int st_smem = 0;
+        if ((st = attn::static_smem(fn, &st_smem)) != XS_OK) return st;
+        const int part_bytes = Hq / Hkv * D * 4;
+        const int avail = dev.smem_per_sm / per_sm - dev.reserved_per_block - st_smem - smem - 32;
+        stage_parts = std::max(1, std::min({avail / part_bytes, 32, 32768 / part_bytes,
+                                            std::max(max_partitions, 1)}));
+        stage_bytes = stage_parts * part_bytes + 32;  // + its header and alignment
+        smem += stage_bytes;
+        if (smem + 1024 > dev.max_smem_optin) return XS_EUNSUPPORTED;
+        if ((st = attn::occupancy(fn, smem, &per_sm)) != XS_OK) return st;
+    }
     const int64_t max_items = static_cast<int64_t>(B) * Hkv * max_partitions;
     const int64_t resident = static_cast<int64_t>(dev.sms) * per_sm;
     const int grid = static_cast<int>(std::max<int64_t>(1, std::min(max_items, resident)));
@@ -1584,6 +1703,8 @@ static int launch_attn(void *out, float *part_o, float *part_m, float *part_l, c
     p.k_new = k_new;
     p.v_new = v_new;
     p.combine = combine;
+    p.stage_bytes = stage_bytes;
+    p.stage_parts = stage_parts;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(attn::kThreads);

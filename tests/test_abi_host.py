@@ -64,6 +64,21 @@ def test_partition_heuristic(lib):
     assert ops.load().xs_paged_decode_partition_tokens(-1, 8, 0, 0, 152) == -2
 
 
+def test_step_partition_heuristic(lib):
+    # The one-launch step's choice on the measured workloads: its per-item
+    # cost was fitted to one-launch step times (the mix ran 65 / 52 / 55 us at
+    # P = 256 / 512 / 1024; single stream best at 256; long batch at 2048).
+    pick = ops.xs_paged_decode_step_partition_tokens
+    assert pick(64, 32, 8, 63638, 7598, 152) == 512
+    assert pick(1, 32, 8, 4097, 4097, 152) == 256
+    assert pick(128, 32, 8, 2538762, 32769, 152) == 2048
+    for B, Hq, Hkv, total, mx in [(8, 12, 12, 3439, 926), (2, 12, 12, 29, 21), (512, 32, 8, 10**6, 8193)]:
+        P = pick(B, Hq, Hkv, total, mx, 152)
+        assert 64 <= P <= 2048 and (P & (P - 1)) == 0
+    with pytest.raises(ops.XsError):
+        pick(4, 12, 8, 100, 50, 152)   # Hq not a multiple of Hkv
+
+
 def test_max_partitions_and_workspace(lib):
     assert ops.xs_paged_decode_max_partitions(2049, 16, 1024) == 33
     assert ops.xs_paged_decode_max_partitions(1, 16, 1024) == 1
