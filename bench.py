@@ -331,6 +331,11 @@ def run_ours(args, rank, world, local, dist):
     by = step_bytes(cfg, lens_cpu, args.window)
     bytes_per_step = by["step"] * L
 
+    # Early reads: each launch reads lengths, tables and its first pages while
+    # the launch before it (the previous layer's, or the previous step's on
+    # these same lengths) finishes; neither writes what is read early.
+    early = args.fused == "on" and args.early_reads == "on"
+
     def one_step(ev=None):
         cur = torch.cuda.current_stream()
         for layer in range(L):
@@ -339,7 +344,7 @@ def run_ours(args, rank, world, local, dist):
                     ev[layer][0].record(cur)
                 step.run(out[layer], w.q[layer], w.k_new[layer], w.v_new[layer],
                          w.k_cache[layer], w.v_cache[layer], w.block_tables, w.context_lens,
-                         w.scale)
+                         w.scale, early_reads=early)
                 if ev is not None:
                     ev[layer][1].record(cur)
                 continue
@@ -492,6 +497,7 @@ def run_ours(args, rank, world, local, dist):
         "gpu_launches": args.steps * L * step.launches_per_step(fused),
         "cuda_graph": graph is not None,
         "fused_step": fused,
+        "early_reads": early,
         "clocks": clock_info,
     }
     if not args.no_cpu_baseline:
@@ -686,6 +692,9 @@ def main(argv=None):
     ap.add_argument("--fused", choices=["on", "off"], default="on",
                     help="on: each layer's step is one launch (append + attention + combine); "
                          "off: three launches")
+    ap.add_argument("--early-reads", choices=["on", "off"], default="on",
+                    help="on: one-launch steps read lengths, tables and first pages before the "
+                         "previous launch completes (XS_STEP_EARLY_READS)")
     ap.add_argument("--graph", choices=["auto", "on", "off"], default="auto",
                     help="replay each step as one CUDA graph (auto: when the workload has "
                          "more than one layer)")

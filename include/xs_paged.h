@@ -443,6 +443,37 @@ int xs_paged_decode_step(void *out, const void *q, const void *k_new, const void
                          int *counters, int dtype, int *err_flag, cudaStream_t stream);
 
 /*
+ * xs_paged_decode_step_ex - xs_paged_decode_step with launch flags (flags 0
+ * is xs_paged_decode_step).  Unknown flag bits are XS_EUNSUPPORTED.
+ *
+ * XS_STEP_EARLY_READS: the launch is made programmatically dependent on the
+ * previous kernel on the stream (as every launch of this library is), and
+ * reads context_lens, block_tables and the first pages of each CTA's first
+ * work item BEFORE waiting for that kernel to complete, overlapping that
+ * start-up (lengths -> item tables -> block ids -> pages: dependent memory
+ * round trips) with the previous kernel's tail.  q, k_new/v_new, the
+ * counters and every write wait for it as usual; a page that receives this
+ * launch's appended row is not read early.  The caller promises that the
+ * kernel launched just before this one on the stream (if it is still
+ * running) writes none of context_lens, block_tables, or the pages of
+ * k_cache/v_cache this launch attends to (other than the rows it appends
+ * itself), and neither does any earlier kernel that kernel lets run beside
+ * it - true, for instance, when the previous kernel is a projection GEMM or
+ * the attention step of another layer.  (No launch of this library lets its
+ * successor start before its own wait has returned, so behind one of them
+ * only that launch can still be running.)
+ */
+#define XS_STEP_EARLY_READS 1
+int xs_paged_decode_step_ex(void *out, const void *q, const void *k_new, const void *v_new,
+                            void *k_cache, void *v_cache, const int32_t *block_tables,
+                            int max_blocks_per_seq, const int32_t *context_lens, const void *sinks,
+                            int window, int B, int Hq, int Hkv, int D, int block_size,
+                            int64_t num_blocks, float scale, int partition_tokens,
+                            int max_partitions, float *part_o, float *part_m, float *part_l,
+                            int *counters, int flags, int dtype, int *err_flag,
+                            cudaStream_t stream);
+
+/*
  * xs_paged_decode_step_partition_tokens - partition length P for
  * xs_paged_decode_step: the cost model of xs_paged_decode_partition_tokens
  * plus the in-launch combine (the groups that complete last are combined

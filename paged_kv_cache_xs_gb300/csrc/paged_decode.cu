@@ -135,6 +135,9 @@ struct Params {
     // partial rows for a combine: stage_parts partials (x G heads x D fp32)
     // per round trip; stage_bytes is what the launch added for it.
     int stage_bytes, stage_parts;
+    // Nonzero: read lengths, tables and the first pages before waiting for
+    // the previous launch on the stream (see the kernel's start).
+    int early;
 };
 
 // Byte offset of the combine staging area (16-byte aligned, after the tables).
@@ -696,13 +699,20 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
         mbar_fence_init();
         s_abort = 0;
     }
-    // Programmatic dependent launch: the next launch on the stream may start
-    // placing its CTAs as ours exit (all of ours are resident by now), and
-    // this launch reads nothing in global memory before the previous one has
-    // completed and its writes are visible.  (Both are no-ops in a launch
-    // made without the attribute.)
-    griddep_launch_dependents();
-    griddep_wait();
+    // Programmatic dependent launch.  griddep_wait returns once the previous
+    // launch on the stream has completed and its writes are visible; only
+    // then may the next launch start placing CTAs (so a launch never runs
+    // beside any but its immediate predecessor).  By default nothing in
+    // global memory is touched before the wait.  With p.early the lengths,
+    // the item tables, the first item's block ids and its first pages (all
+    // but a page that receives this launch's appended row) are read before
+    // it: the caller promises that the previous launch writes none of them.
+    // q, k_new/v_new and every write come after the wait.  (No-ops in a
+    // launch made without the attribute.)
+    if (!p.early) {
+        griddep_wait();
+        griddep_launch_dependents();
+    }
     {
         // Per sequence: its class A and class B item counts (item_counts).
         // Chunked scan of both counts over the block.
@@ -753,14 +763,22 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
             ptail[p.B] = baset + xt;
         }
     }
-    // Sequences with no tokens produce zeros.
-    for (int b = blockIdx.x; b < p.B && p.prefill_start < 0; b += gridDim.x) {
-        if (p.context_lens[b] > 0) continue;
-        T *o = static_cast<T *>(p.out) + static_cast<int64_t>(b) * p.Hq * D;
-        for (int i = tid; i < p.Hq * D; i += kThreads) o[i] = Elem<T>::from_f32(0.f);
-    }
     __syncthreads();
     const int total_items = pfull[p.B] + ptail[p.B];
+    if (warp != 0) {
+        // Every warp but the producer passes the wait here; the producer
+        // passes it after its early reads.
+        if (p.early) {
+            griddep_wait();
+            griddep_launch_dependents();
+        }
+        // Sequences with no tokens produce zeros.
+        for (int b = blockIdx.x; b < p.B && p.prefill_start < 0; b += gridDim.x) {
+            if (nlen[b] > 0) continue;
+            T *o = static_cast<T *>(p.out) + static_cast<int64_t>(b) * p.Hq * D;
+            for (int i = tid - 32; i < p.Hq * D; i += kThreads - 32) o[i] = Elem<T>::from_f32(0.f);
+        }
+    }
 
     if (warp == 0) {
         // ================================================================ producer
@@ -898,13 +916,76 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
             ++item_ctr;
             return __shfl_sync(0xffffffffu, ok, 0);
         };
+        // Issue the copies of pages base + [from, to) of item `it`: lane i
+        // holds the block id of page base + i (cnt of them valid).  Each
+        // round, the lanes test the stages of the next (up to kStages) pages
+        // and every lane of the leading run of free stages issues its page's
+        // two copies - one warp instruction for all of them - so a producer
+        // that has fallen behind catches up several pages at a time.  False
+        // if a bounded wait for a free stage ran out.
+        auto issue = [&](const Item &it, int32_t ids, int cnt, int from, int to) {
+            const int64_t head_off = static_cast<int64_t>(it.g) * C::kPageBytes;
+            const int64_t blk_stride = static_cast<int64_t>(p.Hkv) * C::kPageBytes;
+            // An id outside the pool reads block 0 instead (flagged).
+            const bool bad_id = lane < cnt && (ids < 0 || ids >= p.num_blocks);
+            if (__any_sync(0xffffffffu, bad_id) && lane == 0) raise_flag(p.err_flag, XS_FLAG_BAD_BLOCK);
+            const int64_t my_off = static_cast<int64_t>(bad_id ? 0 : ids) * blk_stride + head_off;
+            const int my_page = (bad_id ? 0 : ids) * p.Hkv + it.g;  // tensor-map page index
+            int done = from;
+            while (done < to) {
+                const int want = min(to - done, kStages);
+                const uint32_t c = page_ctr + lane;
+                const uint32_t st = c % kStages;
+                const bool is_free =
+                    lane < want && mbar_test_wait(&empty[st], ((c / kStages) & 1) ^ 1);
+                const int n = __ffs(~__ballot_sync(0xffffffffu, is_free)) - 1;
+                const int64_t off = __shfl_sync(0xffffffffu, my_off, (done + lane) & 31);
+                const int pidx = __shfl_sync(0xffffffffu, my_page, (done + lane) & 31);
+                if (n == 0) {
+                    // No stage free yet: wait (bounded) for the next one.
+                    bool w = true;
+                    if (lane == 0)
+                        w = mbar_wait_bounded(&empty[page_ctr % kStages],
+                                              ((page_ctr / kStages) & 1) ^ 1, kWaitLimitNs);
+                    if (!__shfl_sync(0xffffffffu, w, 0)) return false;
+                    continue;
+                }
+                if (lane < n) {
+                    unsigned char *dk = smem + st * 2 * C::kPageBytes;
+                    mbar_arrive_expect_tx(&full[st], 2 * C::kPageBytes);
+                    if constexpr (C::kMma) {
+                        tma_load_4d(smem_addr(dk), &tmk, pidx, &full[st], pol);
+                        tma_load_4d(smem_addr(dk + C::kPageBytes), &tmv, pidx, &full[st], pol);
+                    } else {
+                        bulk_g2s(dk, kbase + off, C::kPageBytes, &full[st], pol);
+                        bulk_g2s(dk + C::kPageBytes, vbase + off, C::kPageBytes, &full[st], pol);
+                    }
+                }
+                done += n;
+                page_ctr += n;  // pages issued so far
+            }
+            return true;
+        };
         // Item B is published (q rows copied in) before item A's pages are
         // issued, so consumers finishing A find B's q already in place.
         Item A = decode(item_of(grab()));
         int32_t idsA = load_ids(A, A.pg0);
+        bool ok = true;
+        int pre = 0;  // pages of the first item issued before the wait
+        if (p.early) {
+            // Up to a ring of the first item's pages, stopping before a page
+            // that receives this launch's appended row.
+            if (A.b >= 0) {
+                const int end = A.tok1 == nlen[A.b] ? A.pg1 - 1 : A.pg1;
+                pre = min(kStages, max(0, end - A.pg0));
+                if (pre > 0) ok = issue(A, idsA, min(32, A.pg1 - A.pg0), 0, pre);
+            }
+            griddep_wait();
+            griddep_launch_dependents();
+        }
         Row rowA = load_row(A);
         Ticket nextB = grab();
-        bool ok = publish(A);
+        if (ok) ok = publish(A);
         while (ok && A.b >= 0) {
             Item Bt = decode(item_of(nextB));
             const int32_t idsB = load_ids(Bt, Bt.pg0);
@@ -913,13 +994,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
             ok = publish(Bt);
             if (!ok) break;
             // Stream A's pages, 32 block ids at a time (the next 32 load
-            // meanwhile).  Lane i owns page base + i of a chunk.  Each round,
-            // the lanes test the stages of the next (up to kStages) pages and
-            // every lane of the leading run of free stages issues its page's
-            // two copies - one warp instruction for all of them - so a
-            // producer that has fallen behind catches up several pages at a time.
-            const int64_t head_off = static_cast<int64_t>(A.g) * C::kPageBytes;
-            const int64_t blk_stride = static_cast<int64_t>(p.Hkv) * C::kPageBytes;
+            // meanwhile); lane i owns page base + i of a chunk.
             int32_t ids = idsA;
             for (int base = A.pg0; ok && base < A.pg1; base += 32) {
                 const int32_t ids_next = (base + 32 < A.pg1) ? load_ids(A, base + 32) : 0;
@@ -927,50 +1002,10 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
                 if (rowA.raw_len > 0 && base + 32 >= A.pg1)  // the chunk with the last page
                     store_row(A, rowA, __shfl_sync(0xffffffffu, ids, A.pg1 - 1 - base));
                 __syncwarp();
-                // An id outside the pool reads block 0 instead (flagged).
-                const bool bad_id = lane < cnt && (ids < 0 || ids >= p.num_blocks);
-                if (__any_sync(0xffffffffu, bad_id) && lane == 0)
-                    raise_flag(p.err_flag, XS_FLAG_BAD_BLOCK);
-                const int64_t my_off = static_cast<int64_t>(bad_id ? 0 : ids) * blk_stride + head_off;
-                const int my_page = (bad_id ? 0 : ids) * p.Hkv + A.g;  // tensor-map page index
-                int done = 0;
-                while (done < cnt) {
-                    const int want = min(cnt - done, kStages);
-                    const uint32_t c = page_ctr + lane;
-                    const uint32_t st = c % kStages;
-                    const bool is_free =
-                        lane < want && mbar_test_wait(&empty[st], ((c / kStages) & 1) ^ 1);
-                    const int n = __ffs(~__ballot_sync(0xffffffffu, is_free)) - 1;
-                    const int64_t off = __shfl_sync(0xffffffffu, my_off, (done + lane) & 31);
-                    const int pidx = __shfl_sync(0xffffffffu, my_page, (done + lane) & 31);
-                    if (n == 0) {
-                        // No stage free yet: wait (bounded) for the next one.
-                        bool w = true;
-                        if (lane == 0)
-                            w = mbar_wait_bounded(&empty[page_ctr % kStages],
-                                                  ((page_ctr / kStages) & 1) ^ 1, kWaitLimitNs);
-                        if (!__shfl_sync(0xffffffffu, w, 0)) {
-                            ok = false;
-                            break;
-                        }
-                        continue;
-                    }
-                    if (lane < n) {
-                        unsigned char *dk = smem + st * 2 * C::kPageBytes;
-                        mbar_arrive_expect_tx(&full[st], 2 * C::kPageBytes);
-                        if constexpr (C::kMma) {
-                            tma_load_4d(smem_addr(dk), &tmk, pidx, &full[st], pol);
-                            tma_load_4d(smem_addr(dk + C::kPageBytes), &tmv, pidx, &full[st], pol);
-                        } else {
-                            bulk_g2s(dk, kbase + off, C::kPageBytes, &full[st], pol);
-                            bulk_g2s(dk + C::kPageBytes, vbase + off, C::kPageBytes, &full[st], pol);
-                        }
-                    }
-                    done += n;
-                    page_ctr += n;  // pages issued so far
-                }
+                ok = issue(A, ids, cnt, base == A.pg0 ? pre : 0, cnt);
                 ids = ids_next;
             }
+            pre = 0;
             A = Bt;
             idsA = idsB;
             rowA = rowB;
@@ -1629,7 +1664,7 @@ static int launch_attn(void *out, float *part_o, float *part_m, float *part_l, c
                        const void *sinks, int window, int partition_tokens, int max_partitions,
                        int dtype, int *err_flag, int *work_counters, cudaStream_t stream,
                        int prefill_start = -1, const void *k_new = nullptr,
-                       const void *v_new = nullptr, int *combine = nullptr) {
+                       const void *v_new = nullptr, int *combine = nullptr, int early = 0) {
     if (window < 0) return XS_ESHAPE;
     const bool prefill = prefill_start >= 0;
     int st = check_attn_args(out, part_o, part_m, part_l, q, k_cache, v_cache, block_tables,
@@ -1703,6 +1738,7 @@ static int launch_attn(void *out, float *part_o, float *part_m, float *part_l, c
     p.k_new = k_new;
     p.v_new = v_new;
     p.combine = combine;
+    p.early = early;
     p.stage_bytes = stage_bytes;
     p.stage_parts = stage_parts;
     cudaLaunchConfig_t cfg = {};
@@ -1836,6 +1872,26 @@ extern "C" int xs_paged_decode_sinks(void *out, float *part_o, float *part_m, fl
 // contract.  counters = [item counter, finished-CTA counter, B * Hkv combine
 // counts], all zero between launches.
 
+extern "C" int xs_paged_decode_step_ex(void *out, const void *q, const void *k_new,
+                                       const void *v_new, void *k_cache, void *v_cache,
+                                       const int32_t *block_tables, int max_blocks_per_seq,
+                                       const int32_t *context_lens, const void *sinks, int window,
+                                       int B, int Hq, int Hkv, int D, int block_size,
+                                       int64_t num_blocks, float scale, int partition_tokens,
+                                       int max_partitions, float *part_o, float *part_m,
+                                       float *part_l, int *counters, int flags, int dtype,
+                                       int *err_flag, cudaStream_t stream) {
+    if (flags & ~XS_STEP_EARLY_READS) return XS_EUNSUPPORTED;
+    if (!k_new != !v_new) return XS_ENULL;
+    if (!counters) return XS_EWORKSPACE;
+    if (k_new && (!aligned16(k_new) || !aligned16(v_new))) return XS_EALIGN;
+    return launch_attn(out, part_o, part_m, part_l, q, k_cache, v_cache, block_tables,
+                       max_blocks_per_seq, context_lens, B, Hq, Hkv, D, block_size, num_blocks,
+                       scale, sinks, window, partition_tokens, max_partitions, dtype, err_flag,
+                       counters, stream, -1, k_new, v_new, counters + 2,
+                       (flags & XS_STEP_EARLY_READS) ? 1 : 0);
+}
+
 extern "C" int xs_paged_decode_step(void *out, const void *q, const void *k_new,
                                     const void *v_new, void *k_cache, void *v_cache,
                                     const int32_t *block_tables, int max_blocks_per_seq,
@@ -1845,13 +1901,11 @@ extern "C" int xs_paged_decode_step(void *out, const void *q, const void *k_new,
                                     int max_partitions, float *part_o, float *part_m,
                                     float *part_l, int *counters, int dtype, int *err_flag,
                                     cudaStream_t stream) {
-    if (!k_new != !v_new) return XS_ENULL;
-    if (!counters) return XS_EWORKSPACE;
-    if (k_new && (!aligned16(k_new) || !aligned16(v_new))) return XS_EALIGN;
-    return launch_attn(out, part_o, part_m, part_l, q, k_cache, v_cache, block_tables,
-                       max_blocks_per_seq, context_lens, B, Hq, Hkv, D, block_size, num_blocks,
-                       scale, sinks, window, partition_tokens, max_partitions, dtype, err_flag,
-                       counters, stream, -1, k_new, v_new, counters + 2);
+    return xs_paged_decode_step_ex(out, q, k_new, v_new, k_cache, v_cache, block_tables,
+                                   max_blocks_per_seq, context_lens, sinks, window, B, Hq, Hkv, D,
+                                   block_size, num_blocks, scale, partition_tokens,
+                                   max_partitions, part_o, part_m, part_l, counters, 0, dtype,
+                                   err_flag, stream);
 }
 
 extern "C" int64_t xs_paged_decode_step_counters(int B, int Hkv) {

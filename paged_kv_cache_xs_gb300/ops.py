@@ -65,6 +65,8 @@ SIGNATURES = {
                                  _P]),
     "xs_paged_decode_step": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I,
                                   _I, _L, _F, _I, _I, _P, _P, _P, _P, _I, _P, _P]),
+    "xs_paged_decode_step_ex": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I,
+                                     _I, _L, _F, _I, _I, _P, _P, _P, _P, _I, _I, _P, _P]),
     "xs_paged_decode_step_counters": (_L, [_I, _I]),
     "xs_paged_decode_step_partition_tokens": (_I, [_I, _I, _I, _L, _I, _I]),
     "xs_version": (_I, []),
@@ -221,14 +223,29 @@ def xs_paged_decode(out, part_o, part_m, part_l, q, k_cache, v_cache, block_tabl
           _stream(stream))
 
 
+XS_STEP_EARLY_READS = 1
+
+
 def xs_paged_decode_step(out, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens,
                          scale, partition_tokens, max_partitions, part_o, part_m, part_l,
-                         counters, sinks=None, window=0, err_flag=None, stream=None):
+                         counters, sinks=None, window=0, err_flag=None, stream=None,
+                         early_reads=False):
     """The whole decode step in one launch: append k_new/v_new ([B, Hkv, D],
     or both None), attend, combine the split-K partials.  ``counters`` holds
-    xs_paged_decode_step_counters(B, Hkv) int32 zeros (left zero)."""
+    xs_paged_decode_step_counters(B, Hkv) int32 zeros (left zero).
+    ``early_reads`` (XS_STEP_EARLY_READS): lengths, tables and the first pages
+    are read before the previous kernel on the stream completes; the caller
+    promises that kernel writes none of them."""
     B, Hq, D = q.shape
     num_blocks, Hkv, bs, _ = k_cache.shape
+    if early_reads:
+        _call("xs_paged_decode_step_ex", _ptr(out), _ptr(q), _ptr(k_new), _ptr(v_new),
+              _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1],
+              _ptr(context_lens), _ptr(sinks), int(window), B, Hq, Hkv, D, bs, num_blocks,
+              float(scale), partition_tokens, max_partitions, _ptr(part_o), _ptr(part_m),
+              _ptr(part_l), _ptr(counters), XS_STEP_EARLY_READS, dtype_code(q.dtype),
+              _ptr(err_flag), _stream(stream))
+        return
     _call("xs_paged_decode_step", _ptr(out), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache),
           _ptr(v_cache), _ptr(block_tables), block_tables.shape[1], _ptr(context_lens),
           _ptr(sinks), int(window), B, Hq, Hkv, D, bs, num_blocks, float(scale),

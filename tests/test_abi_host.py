@@ -188,3 +188,12 @@ def test_prefill_tc_argument_validation(lib):
     assert f(A, A, A, A, A, 4, 8, 0, 32, 2, 128, 16, 10, 0.1, 1, None, None) == -5  # G = 16
     assert f(A, A, A, A, A, 4, 60, 10, 8, 2, 128, 16, 10, 0.1, 1, None, None) == -2  # past ids
     assert f(A, A, A + 8, A, A, 4, 8, 0, 8, 2, 128, 16, 10, 0.1, 1, None, None) == -4
+
+
+def test_step_ex_flags_validated(lib):
+    # Unknown flag bits are refused before anything else is looked at.
+    args = [None] * 7 + [0, None, None, 0, 1, 8, 8, 64, 16, 1, 0.125, 64, 1, None, None, None, None]
+    assert lib.xs_paged_decode_step_ex(*args, 2, ops.XS_BF16, None, None) == -5
+    assert lib.xs_paged_decode_step_ex(*args, 1 << 30, ops.XS_BF16, None, None) == -5
+    # A known flag passes through to the usual checks (NULL counters here).
+    assert lib.xs_paged_decode_step_ex(*args, 1, ops.XS_BF16, None, None) == -6

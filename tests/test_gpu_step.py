@@ -21,34 +21,37 @@ def _ws(w, P):
                                partition_tokens=P)
 
 
-def _step(w, ws, sinks=None, window=0, append=True, out=None, err=None):
+def _step(w, ws, sinks=None, window=0, append=True, out=None, err=None, early=False, layer=0):
     cfg = w.cfg
     dev = w.q.device
     out = torch.full((cfg.B, cfg.Hq, cfg.D), float("nan"), dtype=cfg.dtype, device=dev) \
         if out is None else out
     err = torch.zeros(1, dtype=torch.int32, device=dev) if err is None else err
-    ops.xs_paged_decode_step(out, w.q[0], w.k_new[0] if append else None,
-                             w.v_new[0] if append else None, w.k_cache[0], w.v_cache[0],
-                             w.block_tables, w.context_lens, w.scale, ws.partition_tokens,
-                             ws.max_partitions, ws.part_o, ws.part_m, ws.part_l, ws.work,
-                             sinks=sinks, window=window, err_flag=err)
+    ops.xs_paged_decode_step(out, w.q[layer], w.k_new[layer] if append else None,
+                             w.v_new[layer] if append else None, w.k_cache[layer],
+                             w.v_cache[layer], w.block_tables, w.context_lens, w.scale,
+                             ws.partition_tokens, ws.max_partitions, ws.part_o, ws.part_m,
+                             ws.part_l, ws.work, sinks=sinks, window=window, err_flag=err,
+                             early_reads=early)
     return out, err
 
 
-def _appended(w):
+def _appended(w, layer=0):
     """The oracle's append of this step's rows into copies of the pools."""
     slots = oracle.slot_mapping(w.block_tables.cpu(), w.context_lens.cpu(), gh.BS, w.num_blocks)
-    return oracle.kv_append(w.k_new[0].cpu(), w.v_new[0].cpu(), w.k_cache[0].cpu(),
-                            w.v_cache[0].cpu(), slots)
+    return oracle.kv_append(w.k_new[layer].cpu(), w.v_new[layer].cpu(), w.k_cache[layer].cpu(),
+                            w.v_cache[layer].cpu(), slots)
 
 
-CASES = list(itertools.product([torch.bfloat16, torch.float32], [1, 4, 8], [16, 64, 4096]))
+CASES = [(d, G, P, False) for d, G, P in
+         itertools.product([torch.bfloat16, torch.float32], [1, 4, 8], [16, 64, 4096])]
+CASES += [(torch.bfloat16, 4, 16, True), (torch.bfloat16, 8, 64, True), (torch.float32, 1, 64, True)]
 
 
-@pytest.mark.parametrize("dtype,G,P", CASES,
+@pytest.mark.parametrize("dtype,G,P,early", CASES,
                          ids=[f"{'bf16' if d == torch.bfloat16 else 'f32'}-G{G}-P{P}"
-                              for d, G, P in CASES])
-def test_step_matches_oracle(dtype, G, P):
+                              f"{'-early' if e else ''}" for d, G, P, e in CASES])
+def test_step_matches_oracle(dtype, G, P, early):
     # Lengths around page and partition edges, up to 63 partitions of 16
     # tokens (the combine walks its partials 32 at a time), and an empty slot.
     dev = gh.device()
@@ -58,7 +61,7 @@ def test_step_matches_oracle(dtype, G, P):
     w = wl.make_workload(cfg, device=dev, history=hist)
     ek, ev = _appended(w)
     ws = _ws(w, P)
-    out, err = _step(w, ws)
+    out, err = _step(w, ws, early=early)
     torch.cuda.synchronize()
     assert int(err.item()) == 0 and int(ws.work.count_nonzero()) == 0
     assert torch.equal(gh.int_view(w.k_cache[0].cpu()), gh.int_view(ek))
@@ -156,3 +159,62 @@ def test_counters_zero_across_many_launches():
     assert int(ws.work.count_nonzero()) == 0
     for out in outs:
         gh.assert_close(out, ref, torch.bfloat16)
+
+
+@pytest.mark.parametrize("P", [16, 128])
+def test_early_reads_layers_back_to_back(P):
+    # Layers launched back to back with early reads: each launch reads its
+    # lengths, tables and first pages while the previous layer's launch may
+    # still run (it writes other pools), and sequences shorter than a ring
+    # put the page that receives the new row in the first item.  Every layer
+    # matches the oracle, and a second pass over the same pools (the previous
+    # launch then appends the same rows) gives the same outputs.
+    dev = gh.device()
+    hist = torch.tensor([0, 3, 15, 16, 40, 127, 128, 129, 700, 2000, -1], dtype=torch.int32)
+    L = 4
+    cfg = wl.custom_config(len(hist), 32, 8, 128, torch.bfloat16, layers=L,
+                           history=("uniform", (0, 1)), pool=("factor", 1.5), seed=790 + P)
+    w = wl.make_workload(cfg, device=dev, history=hist)
+    refs = []
+    for layer in range(L):
+        ek, ev = _appended(w, layer)
+        refs.append(oracle.paged_decode(w.q[layer].cpu(), ek, ev, w.block_tables.cpu(),
+                                        w.context_lens.cpu(), w.scale))
+    ws = _ws(w, P)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    outs = [[_step(w, ws, err=err, early=True, layer=layer)[0] for layer in range(L)]
+            for _ in range(2)]
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0 and int(ws.work.count_nonzero()) == 0
+    for rep in outs:
+        for layer in range(L):
+            gh.assert_close(rep[layer], refs[layer], torch.bfloat16, what=f"layer {layer}")
+
+
+
+def test_early_reads_in_a_cuda_graph():
+    # The same back-to-back layers captured in one CUDA graph (the launches
+    # keep their programmatic dependencies), replayed three times.
+    from paged_kv_cache_xs_gb300.step import CapturedStep
+    dev = gh.device()
+    L = 3
+    cfg = wl.custom_config(7, 32, 8, 128, torch.bfloat16, layers=L,
+                           history=("loguniform", (1, 3000)), pool=("factor", 1.4), seed=811)
+    w = wl.make_workload(cfg, device=dev)
+    refs = []
+    for layer in range(L):
+        ek, ev = _appended(w, layer)
+        refs.append(oracle.paged_decode(w.q[layer].cpu(), ek, ev, w.block_tables.cpu(),
+                                        w.context_lens.cpu(), w.scale))
+    ws = _ws(w, 64)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    outs = [torch.full((cfg.B, cfg.Hq, cfg.D), float("nan"), dtype=cfg.dtype, device=dev)
+            for _ in range(L)]
+    g = CapturedStep(lambda: [_step(w, ws, err=err, early=True, layer=layer, out=outs[layer])
+                              for layer in range(L)])
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0 and int(ws.work.count_nonzero()) == 0
+    for layer in range(L):
+        gh.assert_close(outs[layer], refs[layer], torch.bfloat16, what=f"layer {layer}")
