@@ -622,16 +622,22 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *tm,
 template <typename T, int D, int G>
 __device__ __noinline__ bool count_and_combine(const Params &p, int lane, int pend_b, int pend_g,
                                                int pend_np, int npend, Stage *stage) {
-    __threadfence();
+    // Release: every lane's partial stores (gathered by the warp barrier)
+    // before the counts, by a cumulative fence in each counting lane.
     __syncwarp();
+    fence_acq_rel_gpu();
     int *cnt = p.combine + static_cast<int64_t>(pend_b) * p.Hkv + pend_g;
     int prior = 0;
     if (lane < npend) prior = atomicAdd(cnt, 1);
     const bool last = lane < npend && prior == pend_np - 1;
-    if (last) atomicExch(cnt, 0);
     unsigned todo = __ballot_sync(0xffffffffu, last);
-    if (todo) __threadfence();
+    if (todo) {
+        // Acquire: the group's other partials, then handed to every lane.
+        fence_acq_rel_gpu();
+        __syncwarp();
+    }
     bool ok = true;
+    const unsigned combined = todo;
     while (todo && ok) {
         const int k = __ffs(todo) - 1;
         todo &= todo - 1;
@@ -642,6 +648,9 @@ __device__ __noinline__ bool count_and_combine(const Params &p, int lane, int pe
         const int64_t h0 = static_cast<int64_t>(ci.b) * p.Hq + static_cast<int64_t>(ci.g) * G;
         ok = combine_partials<T, D, G>(p, ci, h0, lane, stage);
     }
+    // Leave the completed groups' counts zero for the next launch - after
+    // the combines, so no fence above waits for these writes.
+    if (combined & (1u << lane)) atomicExch(cnt, 0);
     return ok;
 }
 

@@ -75,6 +75,12 @@ __device__ __forceinline__ int atomic_add_if(int *ptr, int v, bool pred) {
     return old;
 }
 
+// Acquire-release fence at GPU scope: this thread's earlier memory operations
+// (and those it has synchronized with) happen before its later ones, as
+// seen by any thread of the GPU that synchronizes with it.
+__device__ __forceinline__ void fence_acq_rel_gpu() {
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
 // Orders this thread's earlier generic-proxy writes to global memory before
 // later async-proxy operations (bulk copies) that read the same memory.
 __device__ __forceinline__ void fence_proxy_async_global() {
