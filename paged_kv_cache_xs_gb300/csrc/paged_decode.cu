@@ -49,6 +49,7 @@ constexpr int kThreads = 32 * (kConsumerWarps + 2);  // producer, consumers, mer
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s per bounded wait
 constexpr int kMaxBatch = 8192;                   // per-sequence tables live in shared memory
+constexpr int kClaimAhead = 8;  // pages of the current item left to issue when the next is claimed
 
 // Per-sequence tables a CTA keeps in shared memory: pfull[B + 1], ptail[B + 1]
 // (item numbering) and nlen[B] (clamped context lengths).
@@ -993,17 +994,15 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
             griddep_launch_dependents();
         }
         Row rowA = load_row(A);
-        Ticket nextB = grab();
         if (ok) ok = publish(A);
         while (ok && A.b >= 0) {
-            Item Bt = decode(item_of(nextB));
-            const int32_t idsB = load_ids(Bt, Bt.pg0);
-            const Row rowB = load_row(Bt);
-            nextB = grab();  // unconditionally: a branch here would wait for the fetch
-            ok = publish(Bt);
-            if (!ok) break;
             // Stream A's pages, 32 block ids at a time (the next 32 load
-            // meanwhile); lane i owns page base + i of a chunk.
+            // meanwhile); lane i owns page base + i of a chunk.  The next item
+            // is claimed only when kClaimAhead of A's pages are left to issue
+            // (its counter fetch then returns while they stream): a CTA holds
+            // no item it will not start soon, so the grid's ends even out.
+            const int claim_at = max(A.pg0, A.pg1 - kClaimAhead);
+            Ticket next{0, false};
             int32_t ids = idsA;
             for (int base = A.pg0; ok && base < A.pg1; base += 32) {
                 const int32_t ids_next = (base + 32 < A.pg1) ? load_ids(A, base + 32) : 0;
@@ -1011,13 +1010,23 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
                 if (rowA.raw_len > 0 && base + 32 >= A.pg1)  // the chunk with the last page
                     store_row(A, rowA, __shfl_sync(0xffffffffu, ids, A.pg1 - 1 - base));
                 __syncwarp();
-                ok = issue(A, ids, cnt, base == A.pg0 ? pre : 0, cnt);
+                const int from = base == A.pg0 ? pre : 0;
+                if (claim_at >= base && claim_at < base + cnt) {
+                    const int split = max(from, claim_at - base);
+                    ok = issue(A, ids, cnt, from, split);
+                    next = grab();  // unconditionally: a branch here would wait for the fetch
+                    ok = ok && issue(A, ids, cnt, split, cnt);
+                } else {
+                    ok = issue(A, ids, cnt, from, cnt);
+                }
                 ids = ids_next;
             }
+            if (!ok) break;
             pre = 0;
-            A = Bt;
-            idsA = idsB;
-            rowA = rowB;
+            A = decode(item_of(next));
+            idsA = load_ids(A, A.pg0);
+            rowA = load_row(A);
+            ok = publish(A);
         }
         if (lane == 0) {
             if (!ok) {
