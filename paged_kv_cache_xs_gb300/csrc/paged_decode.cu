@@ -403,19 +403,25 @@ static_assert(sizeof(Stage) == 16, "staged rows start 16 bytes in");
 // Split-K combine of one (sequence, KV head) group by one warp: for each of
 // the G heads, out = sum_j e^(m_j - M) o_j / sum_j e^(m_j - M) l_j over the
 // group's np partials (o_j already divided by l_j's partition sum, so the
-// weight of o_j is e^(m_j - M) l_j).  Partials are taken stage_parts at a
-// time: for each head, the chunk's rows are contiguous in part_o and arrive
-// in the staging area by one bulk copy (the copy engine, not the load unit),
-// while lane k loads m and l of partial k, so a chunk costs one memory round
-// trip; the running maximum M is raised per chunk and what was accumulated
-// is rescaled.  The caller has acquired the partials (generic proxy); the
-// proxy fence below orders the bulk copies after that.  Returns false if a
-// copy did not complete in time (nothing is written then).
+// weight of o_j is e^(m_j - M) l_j).  Partials are taken in chunks, each
+// one memory round trip: for each head, the first stage_parts partials of a
+// chunk are contiguous in part_o and arrive in the staging area by one bulk
+// copy (the copy engine, not the load unit); the first chunk also takes up
+// to kRegParts more straight into registers, and lane k loads m and l of
+// partial k, all in flight together.  The running maximum M is raised per
+// chunk and what was accumulated is rescaled.  The caller has acquired the
+// partials (generic proxy); the proxy fence below orders the bulk copies
+// after that.  Returns false if a copy did not complete in time (nothing is
+// written then).
 template <typename T, int D, int G>
 __device__ __noinline__ bool combine_partials(const Params &p, const Item &it, int64_t head0,
                                               int lane, Stage *stage) {
     constexpr int kDims = D / 32;   // output dims per lane
     using Vec = typename std::conditional<kDims == 4, float4, float2>::type;
+    // 16 rows held in registers, where the register budget allows (not at
+    // three resident CTAs per SM).
+    constexpr int kRegParts = Cfg<T, D, G>::kMinBlocks >= 3 ? 0 : 16 / G;
+    constexpr int kRegSlots = kRegParts > 0 ? kRegParts : 1;
     const int np = it.nparts;
     const int K = p.stage_parts;
     const float *pm = p.part_m + head0 * p.max_parts;
@@ -429,8 +435,19 @@ __device__ __noinline__ bool combine_partials(const Params &p, const Item &it, i
 #pragma unroll
         for (int d = 0; d < kDims; ++d) acc[h][d] = 0.f;
     }
-    for (int j0 = 0; j0 < np; j0 += K) {
-        const int cnt = min(K, np - j0);
+    for (int j0 = 0; j0 < np;) {
+        const int cnt = min(K, np - j0);  // staged partials
+        // The first chunk's next partials (up to kRegParts, 32 in all) go to registers.
+        const int nreg = j0 == 0 ? min(np - cnt, min(kRegParts, 32 - cnt)) : 0;
+        Vec vr[kRegSlots][G];
+#pragma unroll
+        for (int u = 0; u < kRegParts; ++u)
+#pragma unroll
+            for (int h = 0; h < G; ++h)
+                if (u < nreg)
+                    vr[u][h] = __ldcg(reinterpret_cast<const Vec *>(
+                        p.part_o + ((head0 + h) * p.max_parts + cnt + u) * D + lane * kDims));
+        const int tot = cnt + nreg;  // partials of this chunk (<= 32: lane k holds k's m, l)
         // Row h * cnt + k of the staging area receives partial j0 + k of head h.
         const uint32_t phase = stage->phase;
         if (lane == 0) {
@@ -446,7 +463,7 @@ __device__ __noinline__ bool combine_partials(const Params &p, const Item &it, i
 #pragma unroll
         for (int h = 0; h < G; ++h) {
             float mj = -INFINITY, lj = 0.f;
-            if (lane < cnt) {
+            if (lane < tot) {
                 mj = __ldcg(pm + h * p.max_parts + j0 + lane);
                 lj = __ldcg(pl + h * p.max_parts + j0 + lane);
             }
@@ -457,7 +474,7 @@ __device__ __noinline__ bool combine_partials(const Params &p, const Item &it, i
             const float ref = m_new == -INFINITY ? 0.f : m_new;
             const float corr = fast_exp2(run_m[h] - ref);  // 0 while nothing is accumulated
             run_m[h] = m_new;
-            wgt[h] = lane < cnt ? fast_exp2(mj - ref) * lj : 0.f;
+            wgt[h] = lane < tot ? fast_exp2(mj - ref) * lj : 0.f;
             den[h] = den[h] * corr + wgt[h];
 #pragma unroll
             for (int d = 0; d < kDims; ++d) acc[h][d] *= corr;
@@ -483,7 +500,19 @@ __device__ __noinline__ bool combine_partials(const Params &p, const Item &it, i
                 for (int d = 0; d < kDims; ++d) acc[h][d] += w * f[d];
             }
         }
+#pragma unroll
+        for (int u = 0; u < kRegParts; ++u)
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                const float w = __shfl_sync(0xffffffffu, wgt[h], (cnt + u) & 31);
+                if (u < nreg) {
+                    const float *f = reinterpret_cast<const float *>(&vr[u][h]);
+#pragma unroll
+                    for (int d = 0; d < kDims; ++d) acc[h][d] += w * f[d];
+                }
+            }
         __syncwarp();  // the next chunk overwrites the staging area
+        j0 += tot;
     }
 #pragma unroll
     for (int h = 0; h < G; ++h) {
@@ -623,20 +652,17 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *tm,
 template <typename T, int D, int G>
 __device__ __noinline__ bool count_and_combine(const Params &p, int lane, int pend_b, int pend_g,
                                                int pend_np, int npend, Stage *stage) {
-    // Release: every lane's partial stores (gathered by the warp barrier)
-    // before the counts, by a cumulative fence in each counting lane.
+    // Every lane's partial stores are gathered by the warp barrier; each
+    // counting lane's acquire-release add releases them (cumulatively) and
+    // acquires the group's earlier partials; a second barrier hands that to
+    // every lane.
     __syncwarp();
-    fence_acq_rel_gpu();
     int *cnt = p.combine + static_cast<int64_t>(pend_b) * p.Hkv + pend_g;
     int prior = 0;
-    if (lane < npend) prior = atomicAdd(cnt, 1);
+    if (lane < npend) prior = atomic_add_acq_rel_gpu(cnt, 1);
     const bool last = lane < npend && prior == pend_np - 1;
     unsigned todo = __ballot_sync(0xffffffffu, last);
-    if (todo) {
-        // Acquire: the group's other partials, then handed to every lane.
-        fence_acq_rel_gpu();
-        __syncwarp();
-    }
+    if (todo) __syncwarp();
     bool ok = true;
     const unsigned combined = todo;
     while (todo && ok) {

@@ -65,6 +65,16 @@ __device__ __forceinline__ void mbar_fence_init() {
 // atomicAdd(ptr, v) on the threads where pred holds (returning the old
 // value; 0 elsewhere) as one predicated instruction, so no branch forces the
 // warp to wait for the result before it is used.
+// Atomic add with acquire-release semantics at GPU scope: this thread's
+// earlier writes (and those it has synchronized with) are released by it,
+// and the writes released to the counter before are acquired.
+__device__ __forceinline__ int atomic_add_acq_rel_gpu(int *ptr, int v) {
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(ptr), "r"(v)
+                 : "memory");
+    return old;
+}
+
 __device__ __forceinline__ int atomic_add_if(int *ptr, int v, bool pred) {
     int old = 0;
     asm volatile(
