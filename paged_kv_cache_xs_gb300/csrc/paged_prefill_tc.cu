@@ -375,16 +375,23 @@ __global__ void __launch_bounds__(kThreads, 2)
             // tiles that reach past the CTA's first query position need one.
             // The maximum is taken on raw scores (qscale > 0), the exponent
             // is one fma: 2^(s * qscale - m).
+            // The row maximum and the sums run as 8 independent chains (a
+            // single 64-long chain of dependent fmax was the softmax's
+            // critical path: few warps per scheduler hide no latency).
             const int k0 = kt * kKeys;
             const bool need_mask = k0 + kKeys - 1 > p.start + tok0;
-            float sv[64], smax = -INFINITY;
+            float sv[64], mx8[8];
 #pragma unroll
             for (int j = 0; j < 64; ++j) {
                 const float x = __uint_as_float(sr[j >> 5][j & 31]);
                 sv[j] = !need_mask || k0 + j <= qpos ? x : -INFINITY;
-                smax = fmaxf(smax, sv[j]);
+                mx8[j & 7] = j < 8 ? sv[j] : fmaxf(mx8[j & 7], sv[j]);
             }
-            const float tmax = smax * p.qscale;
+#pragma unroll
+            for (int w = 4; w > 0; w >>= 1)
+#pragma unroll
+                for (int i = 0; i < w; ++i) mx8[i] = fmaxf(mx8[i], mx8[i + w]);
+            const float tmax = mx8[0] * p.qscale;
             bool rescale = false;
             float m_new = m_ref;
             if (kt == 0) {
@@ -394,17 +401,20 @@ __global__ void __launch_bounds__(kThreads, 2)
                 rescale = true;
                 m_new = tmax;
             }
-            float ps0 = 0.f, ps1 = 0.f;
+            float ps8[8];
             uint32_t pr[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
                 const float a = fast_exp2(fmaf(sv[2 * j], p.qscale, -m_new));
                 const float b = fast_exp2(fmaf(sv[2 * j + 1], p.qscale, -m_new));
-                ps0 += a;
-                ps1 += b;
+                ps8[j & 7] = j < 8 ? a + b : ps8[j & 7] + (a + b);
                 pr[j] = pack_bf16(a, b);
             }
-            const float ps = ps0 + ps1;
+#pragma unroll
+            for (int w = 4; w > 0; w >>= 1)
+#pragma unroll
+                for (int i = 0; i < w; ++i) ps8[i] += ps8[i + w];
+            const float ps = ps8[0];
             // P buffer kt % 2 was last read by P V of tile kt - 2; a rescale
             // reads and writes O, so it waits for P V of tile kt - 1.
             if (kt >= 2) {
