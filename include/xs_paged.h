@@ -191,10 +191,11 @@ int xs_paged_prefill(void *out, float *part_o, float *part_m, float *part_l, con
  * xs_paged_prefill_tc - the same causal chunk attention as xs_paged_prefill
  * (q [T, Hq, D], out [T, Hq, D], block_ids [n_ids], row i at position
  * start_pos + i over the cached prefix and the chunk), on the tensor cores,
- * in one launch with no workspace: CTAs of 128 (query token, query head)
- * rows of one KV group stream K/V pages through shared memory with TMA and
- * compute Q K^T and P V with tcgen05.mma into TMEM (bf16 operands, fp32
- * accumulation; the softmax weights P enter P V rounded to bf16).  bf16 only (XS_F32 is
+ * in one launch with no workspace: CTAs of two tiles of 128 (query token,
+ * query head) rows of one KV group stream 128-key K/V tiles through shared
+ * memory with TMA and compute Q K^T and P V with tcgen05.mma into TMEM (bf16
+ * operands, fp32 accumulation; the softmax weights P enter P V rounded to
+ * bf16).  bf16 only (XS_F32 is
  * XS_EUNSUPPORTED); D in {64, 128}; G = Hq / Hkv in {1, 2, 4, 8};
  * num_blocks * Hkv * 16 + 16 < 2^31 (TMA row coordinates).  A block id
  * outside the pool reads as zeros and raises XS_FLAG_BAD_BLOCK.  Errors

@@ -6,34 +6,41 @@
 // with the mask offset by the cached prefix).
 //
 // Design (flash-attention style, one pass, no split):
-//  * CTA = 128 query rows x one KV head g.  A row is a (query token, query
-//    head) pair: 128 / G tokens x the G query heads of the group, so every
-//    K/V byte a CTA stages serves all G heads.  Row r is TMEM lane r.
-//  * Warp 0 (TMA): Q once (one 3-D tensor copy per 64-wide D half, box
-//    [64, G heads, 128/G tokens]); then 64-key K and V tiles (4 pages) into
-//    two 2-slot rings (a K slot frees after Q K^T, a V slot after P V), one
-//    3-D copy per page and D half from a tensor map over the pool.  Every box is 128-byte swizzled, so a D half of a tile is the
+//  * CTA = two Q tiles of 128 query rows, one KV head g, one CTA per SM.  A
+//    row is a (query token, query head) pair: 128 / G tokens x the G query
+//    heads of the group, so every K/V byte staged serves all G heads of both
+//    tiles.  Row r of tile i is TMEM lane r of tile i's 256 columns.
+//  * Warp 0 (TMA): Q once (one 3-D tensor copy per tile and 64-wide D half,
+//    box [64, G heads, 128/G tokens]); then 128-key K and V tiles (8 pages)
+//    into two 2-slot rings (a K slot frees after both tiles' Q K^T, a V slot
+//    after both P V), one 3-D copy per page and D half from a tensor map over
+//    the pool.  Every box is 128-byte swizzled, so a D half of a tile is the
 //    canonical K-major layout (8-row groups 1024 B apart).  Pages past the
 //    last key are requested at a row beyond the pool and arrive as zeros.
-//  * Warp 1 (one thread): S = Q K^T with tcgen05.mma (M=128, N=64, K=16 per
+//  * Warp 1 (one thread): S = Q K^T with tcgen05.mma (M=128, N=128, K=16 per
 //    instruction, A and B from shared-memory descriptors, fp32 accumulators
-//    in TMEM columns 0-63); then O += P V (M=128, N=D) with P read from TMEM
-//    (A operand, columns 64-95 or 96-127: P is double-buffered, so the
-//    softmax of tile t+1 never waits for P V of tile t) and V as an MN-major
-//    B descriptor (8-key
-//    groups 1024 B apart, D halves one tile-half apart); tcgen05.commit
-//    signals each step on an mbarrier.
-//  * Warps 2-5 (softmax; warp w reads TMEM lanes 32*(w%4)..+31, one row per
-//    thread): load the row of S, causal mask, row max, P = 2^(s - m) in base
-//    2, write P (bf16) back to TMEM for the P V step.  The reference m only
+//    in TMEM); O += P V (M=128, N=D) with P read from TMEM (A operand) and V
+//    as an MN-major B descriptor (8-key groups 1024 B apart, D halves one
+//    tile-half apart); tcgen05.commit signals each step on an mbarrier.  The
+//    softmax writes P (bf16) over the first half of S's columns, so per tile
+//    the thread issues P V(t) and then S(t + 1) into the same columns - the
+//    tensor pipe runs a thread's MMAs in order - and the two Q tiles
+//    alternate: while one tile's softmax works, the tensor cores run the
+//    other tile's P V and next scores.  (With 64-key tiles, one Q tile and
+//    two CTAs per SM, each Q K^T instruction read 6 KB of shared-memory
+//    operands for 128 x 64 x 16 MACs: 681 / 825 TFLOP/s on the 8K / 32K
+//    chunked prefills; 128-key tiles read 8 KB for twice the MACs: 809 / 986.)
+//  * Warps 2-9 (softmax, four per Q tile; warp w reads TMEM lanes
+//    32*(w%4)..+31, one row per thread): load the row of S, causal mask, row
+//    max, P = 2^(s - m) in base 2 (maximum and sums as 8 independent
+//    chains), write P back to TMEM for the P V step.  The reference m only
 //    moves when a tile's maximum exceeds it by more than 8 (log2 units), and
 //    only then is the row of O in TMEM rescaled, so P stays <= 2^8 and most
 //    tiles never touch O.  Unwritten slots of the last page (any bits at all)
 //    are zeroed in the staged V tile, since 0 * NaN = NaN.  At the end:
 //    O / l, bf16, out.
-//  * TMEM: 256 columns (S 64, P 2 x 32, O D), so two CTAs share an SM and one
-//    CTA's softmax overlaps the other's MMAs.  Every wait is bounded; the
-//    MMA thread waits for its last MMA before the CTA frees TMEM.
+//  * TMEM: all 512 columns (per Q tile S/P 128, O 128).  Every wait is
+//    bounded; the MMA thread waits for its last MMA before the CTA frees TMEM.
 #include <cuda.h>
 
 #include <algorithm>
@@ -46,13 +53,15 @@ namespace xs {
 namespace pftc {
 
 constexpr int kBlock = 16;
-constexpr int kRows = 128;               // M
-constexpr int kKeys = 64;                // keys per tile: N of Q K^T, K of P V
+constexpr int kRows = 128;               // M: rows of one Q tile
+constexpr int kQTiles = 2;               // Q tiles per CTA, one softmax warp group each
+constexpr int kKeys = 128;               // keys per tile: N of Q K^T, K of P V
 constexpr int kPagesPerTile = kKeys / kBlock;
-constexpr int kStages = 2;
-constexpr int kThreads = 192;            // TMA warp, MMA warp, 4 softmax warps
-constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kColS = 0, kColP = 64, kColO = 128;  // P: two buffers of 32 columns
+constexpr int kStages = 2;               // depth of the K and V rings
+constexpr int kThreads = 64 + 128 * kQTiles;  // TMA warp, MMA warp, 4 softmax warps per Q tile
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kGroupCols = 256;     // per Q tile: S 128 (P written over its first 64), O 128
+constexpr uint32_t kColS = 0, kColP = 0, kColO = 128;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kHeadroom = 8.f;         // log2 units P may exceed 1 before O is rescaled
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
@@ -60,17 +69,21 @@ constexpr uint64_t kWaitLimitNs = 4000000000ull;
 template <int D>
 struct TCfg {
     static constexpr int kHalves = D / 64;
-    static constexpr int kQHalf = kRows * 128;      // one 64-wide D half of Q
-    static constexpr int kQBytes = kHalves * kQHalf;
+    static constexpr int kQHalf = kRows * 128;      // one 64-wide D half of a Q tile
+    static constexpr int kQTile = kHalves * kQHalf;
+    static constexpr int kQBytes = kQTiles * kQTile;
     static constexpr int kKVHalf = kKeys * 128;     // one D half of a K or V tile
     static constexpr int kTile = kHalves * kKVHalf;
     // Separate rings for K and V tiles: a K slot frees when Q K^T of its tile
-    // is done, long before P V of that tile, so K of the next tiles streams in
-    // while the current ones are still in use.
+    // is done (for both Q tiles), long before P V of that tile, so K of the
+    // next tiles streams in while the current ones are still in use.
     static constexpr int kKOff = kQBytes;
     static constexpr int kVOff = kQBytes + kStages * kTile;
     static constexpr int kBarOff = kQBytes + 2 * kStages * kTile;
-    static constexpr int kBarBytes = 20 * 8;
+    // q_full, k_full/k_empty/v_full/v_empty per stage, per Q tile s_full,
+    // p_full, pv_done, then mma_idle and the TMEM address.
+    static constexpr int kNumBars = 1 + 4 * kStages + 3 * kQTiles + 1;
+    static constexpr int kBarBytes = (kNumBars + 1) * 8;
     static constexpr int kSmemBytes = kBarOff + kBarBytes + 1024;  // + alignment slack
     // Instruction descriptors (kind::f16): fp32 D, bf16 A and B, M = 128;
     // Q K^T: both K-major, N = 64; P V: B (V) MN-major, N = D.
@@ -169,34 +182,43 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *tm,
 }
 
 template <int D, int G>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmq,
                       const __grid_constant__ CUtensorMap tmk,
                       const __grid_constant__ CUtensorMap tmv, const PParams p) {
     using C = TCfg<D>;
-    constexpr int kTq = kRows / G;  // query tokens per CTA
+    constexpr int kTq = kRows / G;  // query tokens per Q tile
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     unsigned char *qs = sm;
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + C::kBarOff);
-    uint64_t *q_full = bars, *k_full = bars + 1, *k_empty = bars + 3;
-    uint64_t *v_full = bars + 5, *v_empty = bars + 7;
-    // P is double-buffered (tile t uses buffer t % 2), and so are the barriers
-    // that hand it over: each then completes once per two tiles, and neither
-    // side can run two phases ahead of the other.
-    uint64_t *s_full = bars + 9, *s_free = bars + 10, *p_full = bars + 11, *pv_done = bars + 13;
-    uint64_t *mma_idle = bars + 15;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 16);
+    uint64_t *q_full = bars, *k_full = bars + 1, *k_empty = k_full + kStages;
+    uint64_t *v_full = k_empty + kStages, *v_empty = v_full + kStages;
+    // Per Q tile qi: s_full (S(t) is in TMEM: and, the tensor pipe being in
+    // order, P V(t - 1) is done), p_full (P(t) is in TMEM), pv_done.
+    uint64_t *grp0 = v_empty + kStages;
+    auto s_full = [&](int qi) { return grp0 + 3 * qi; };
+    auto p_full = [&](int qi) { return grp0 + 3 * qi + 1; };
+    auto pv_done = [&](int qi) { return grp0 + 3 * qi + 2; };
+    uint64_t *mma_idle = grp0 + 3 * kQTiles;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_idle + 1);
     __shared__ int s_abort;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = blockIdx.y;
-    const int tok0 = blockIdx.x * kTq;
-    const int ntok = min(kTq, p.T - tok0);
-    const int kmax = p.start + tok0 + ntok;  // keys [0, kmax) are attended
+    const int tok0 = blockIdx.x * kQTiles * kTq;
+    const int ntok = min(kQTiles * kTq, p.T - tok0);  // tokens of this CTA
+    const int kmax = p.start + tok0 + ntok;            // keys [0, kmax) are read
     const int ntiles = (kmax + kKeys - 1) / kKeys;
     const int npages = (kmax + kBlock - 1) / kBlock;
+    // Q tile qi holds tokens [qi * kTq, qi * kTq + tile_tokens(qi)) of the CTA
+    // and attends to key tiles [0, tile_ntiles(qi)).
+    auto tile_tokens = [&](int qi) { return max(0, min(kTq, ntok - qi * kTq)); };
+    auto tile_ntiles = [&](int qi) {
+        const int n = tile_tokens(qi);
+        return n > 0 ? (p.start + tok0 + qi * kTq + n + kKeys - 1) / kKeys : 0;
+    };
 
     if (tid == 0) {
         mbar_init(q_full, 1);
@@ -206,11 +228,10 @@ __global__ void __launch_bounds__(kThreads, 2)
             mbar_init(&v_full[s], 1);
             mbar_init(&v_empty[s], 1);
         }
-        mbar_init(s_full, 1);
-        mbar_init(s_free, 4);
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&p_full[b], 4);
-            mbar_init(&pv_done[b], 1);
+        for (int qi = 0; qi < kQTiles; ++qi) {
+            mbar_init(s_full(qi), 1);
+            mbar_init(p_full(qi), 4);
+            mbar_init(pv_done(qi), 1);
         }
         mbar_init(mma_idle, 1);
         mbar_fence_init();
@@ -238,8 +259,10 @@ __global__ void __launch_bounds__(kThreads, 2)
         int issued = 0;
         if (lane == 0) {
             mbar_arrive_expect_tx(q_full, C::kQBytes);
-            for (int h = 0; h < C::kHalves; ++h)
-                tma_load_3d(smem_addr(qs + h * C::kQHalf), &tmq, 64 * h, g * G, tok0, q_full);
+            for (int qi = 0; qi < kQTiles; ++qi)
+                for (int h = 0; h < C::kHalves; ++h)
+                    tma_load_3d(smem_addr(qs + qi * C::kQTile + h * C::kQHalf), &tmq, 64 * h,
+                                g * G, tok0 + qi * kTq, q_full);
         }
         // K runs one tile ahead of V: K(t + 1) is issued before V(t), so the
         // next Q K^T never queues behind a V slot that P V still holds.
@@ -296,52 +319,74 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
     } else if (warp == 1) {
         // ============================================================== MMA
-        // Order: S(0); then per tile t: S(t+1) as soon as the softmax has
-        // read S(t) and tile t+1 is staged, then P V(t) once P(t) is in TMEM,
-        // so the tensor cores compute the next scores while the softmax warps
-        // work on the current ones.
+        // Per Q tile the softmax writes P(t) over the first half of S(t) in
+        // TMEM, so the MMA thread issues, per Q tile, P V(t) and then S(t + 1)
+        // into the same columns: the tensor pipe executes a thread's MMAs in
+        // order, so P V(t) has read P before S(t + 1) overwrites it, and when
+        // S(t + 1) is complete so is P V(t).  The two Q tiles alternate: the
+        // tensor cores run one tile's P V and next scores while the other
+        // tile's softmax works.  One staged K or V tile serves both Q tiles.
         if (lane == 0) {
             const uint32_t qaddr = smem_addr(qs);
-            auto issue_s = [&](int kt) {
+            int nt_q[kQTiles];
+#pragma unroll
+            for (int qi = 0; qi < kQTiles; ++qi) nt_q[qi] = tile_ntiles(qi);
+            auto issue_s = [&](int qi, int kt) {
                 const uint32_t kaddr = smem_addr(sm + C::kKOff + (kt % kStages) * C::kTile);
+                const uint32_t qa = qaddr + qi * C::kQTile;
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks)
-                    umma_ss(tmem + kColS,
-                            smem_desc(qaddr + (ks >> 2) * C::kQHalf + 32 * (ks & 3), 16, 1024),
+                    umma_ss(tmem + qi * kGroupCols + kColS,
+                            smem_desc(qa + (ks >> 2) * C::kQHalf + 32 * (ks & 3), 16, 1024),
                             smem_desc(kaddr + (ks >> 2) * C::kKVHalf + 32 * (ks & 3), 16, 1024),
                             C::kIdS, ks > 0);
-                umma_commit(s_full);
-                umma_commit(&k_empty[kt % kStages]);
+                umma_commit(s_full(qi));
             };
-            bool ok = mbar_wait_bounded(q_full, 0, kWaitLimitNs) &&
-                      mbar_wait_bounded(&k_full[0], 0, kWaitLimitNs);
-            if (ok) {
-                tc_fence_after();
-                issue_s(0);
-            }
-            for (int kt = 0; ok && kt < ntiles; ++kt) {
-                const int s = kt % kStages;
-                if (kt + 1 < ntiles) {
-                    const int s1 = (kt + 1) % kStages;
-                    ok = mbar_wait_bounded(&k_full[s1], ((kt + 1) / kStages) & 1, kWaitLimitNs) &&
-                         mbar_wait_bounded(s_free, kt & 1, kWaitLimitNs) && !aborted();
-                    if (!ok) break;
-                    tc_fence_after();
-                    issue_s(kt + 1);
-                }
-                ok = mbar_wait_bounded(&p_full[kt & 1], (kt >> 1) & 1, kWaitLimitNs) &&
-                     mbar_wait_bounded(&v_full[s], (kt / kStages) & 1, kWaitLimitNs) &&
-                     !aborted();
-                if (!ok) break;
-                tc_fence_after();
-                const uint32_t vaddr = smem_addr(sm + C::kVOff + s * C::kTile);
+            auto issue_pv = [&](int qi, int kt) {
+                const uint32_t vaddr = smem_addr(sm + C::kVOff + (kt % kStages) * C::kTile);
+                const uint32_t cols = tmem + qi * kGroupCols;
 #pragma unroll
                 for (int kk = 0; kk < kKeys / 16; ++kk)
-                    umma_ts(tmem + kColO, tmem + kColP + 32 * (kt & 1) + 8 * kk,
+                    umma_ts(cols + kColO, cols + kColP + 8 * kk,
                             smem_desc(vaddr + 2048 * kk, C::kKVHalf, 1024), C::kIdPV,
                             kt > 0 || kk > 0);
-                umma_commit(&pv_done[kt & 1]);
+                umma_commit(pv_done(qi));
+            };
+            bool ok = ntiles == 0 || (mbar_wait_bounded(q_full, 0, kWaitLimitNs) &&
+                                      mbar_wait_bounded(&k_full[0], 0, kWaitLimitNs));
+            if (ok && ntiles > 0) {
+                tc_fence_after();
+                for (int qi = 0; qi < kQTiles; ++qi)
+                    if (nt_q[qi] > 0) issue_s(qi, 0);
+                umma_commit(&k_empty[0]);
+            }
+            for (int kt = 0; ok && kt < ntiles; ++kt) {
+                const int s = kt % kStages, s1 = (kt + 1) % kStages;
+                bool v_ready = false, k_ready = false;
+                for (int qi = 0; ok && qi < kQTiles; ++qi) {
+                    if (kt >= nt_q[qi]) continue;
+                    ok = mbar_wait_bounded(p_full(qi), kt & 1, kWaitLimitNs) && !aborted();
+                    if (ok && !v_ready) {
+                        ok = mbar_wait_bounded(&v_full[s], (kt / kStages) & 1, kWaitLimitNs);
+                        v_ready = true;
+                    }
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_pv(qi, kt);
+                    if (kt + 1 < nt_q[qi]) {
+                        if (!k_ready) {
+                            ok = mbar_wait_bounded(&k_full[s1], ((kt + 1) / kStages) & 1,
+                                                   kWaitLimitNs);
+                            k_ready = true;
+                            if (!ok) break;
+                            tc_fence_after();
+                        }
+                        issue_s(qi, kt + 1);
+                    }
+                }
+                if (!ok) break;
                 umma_commit(&v_empty[s]);
+                if (k_ready) umma_commit(&k_empty[s1]);
             }
             if (!ok) abort_now();
             // Every MMA issued has completed before the CTA leaves (and TMEM is freed).
@@ -350,42 +395,41 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
     } else {
         // ========================================================== softmax
-        const int quad = warp & 3;
-        const int r = 32 * quad + lane;  // this thread's row = TMEM lane
-        const int tl = r / G;            // query token within the CTA
-        const bool valid = tl < ntok;
+        const int qi = (warp - 2) >> 2;    // Q tile of this warp group
+        const int quad = warp & 3;         // TMEM lanes 32 * quad .. + 31 (warp rank in its warpgroup)
+        const int r = 32 * quad + lane;    // this thread's row = TMEM lane
+        const int tl = qi * kTq + r / G;   // query token within the CTA
+        const bool valid = r / G < tile_tokens(qi);
         const int qpos = p.start + tok0 + tl;
+        const int my_ntiles = tile_ntiles(qi);
         const uint32_t lane_off = static_cast<uint32_t>(32 * quad) << 16;
+        const uint32_t cols = tmem + lane_off + qi * kGroupCols;
         float m_ref = 0.f, l = 0.f;
         bool ok = true;
-        for (int kt = 0; kt < ntiles; ++kt) {
-            ok = __all_sync(0xffffffffu, mbar_wait_bounded(s_full, kt & 1, kWaitLimitNs)) &&
+        for (int kt = 0; kt < my_ntiles; ++kt) {
+            ok = __all_sync(0xffffffffu, mbar_wait_bounded(s_full(qi), kt & 1, kWaitLimitNs)) &&
                  !aborted();
             if (!ok) break;
             tc_fence_after();
-            uint32_t sr[2][32];
-            tmem_ld32(tmem + lane_off + kColS, sr[0]);
-            tmem_ld32(tmem + lane_off + kColS + 32, sr[1]);
+            uint32_t sr[4][32];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tmem_ld32(cols + kColS + 32 * c, sr[c]);
             tmem_wait_ld();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(s_free);  // S may be overwritten
 
             // Causal mask (by selection: a masked slot may hold any bits) - only
-            // tiles that reach past the CTA's first query position need one.
+            // tiles that reach past the Q tile's first query position need one.
             // The maximum is taken on raw scores (qscale > 0), the exponent
-            // is one fma: 2^(s * qscale - m).
-            // The row maximum and the sums run as 8 independent chains (a
-            // single 64-long chain of dependent fmax was the softmax's
-            // critical path: few warps per scheduler hide no latency).
+            // is one fma: 2^(s * qscale - m).  Maximum and sums run as 8
+            // independent chains.
             const int k0 = kt * kKeys;
-            const bool need_mask = k0 + kKeys - 1 > p.start + tok0;
-            float sv[64], mx8[8];
+            const bool need_mask = k0 + kKeys - 1 > p.start + tok0 + qi * kTq;
+            float mx8[8];
 #pragma unroll
-            for (int j = 0; j < 64; ++j) {
-                const float x = __uint_as_float(sr[j >> 5][j & 31]);
-                sv[j] = !need_mask || k0 + j <= qpos ? x : -INFINITY;
-                mx8[j & 7] = j < 8 ? sv[j] : fmaxf(mx8[j & 7], sv[j]);
+            for (int j = 0; j < kKeys; ++j) {
+                float x = __uint_as_float(sr[j >> 5][j & 31]);
+                x = !need_mask || k0 + j <= qpos ? x : -INFINITY;
+                sr[j >> 5][j & 31] = __float_as_uint(x);
+                mx8[j & 7] = j < 8 ? x : fmaxf(mx8[j & 7], x);
             }
 #pragma unroll
             for (int w = 4; w > 0; w >>= 1)
@@ -402,11 +446,13 @@ __global__ void __launch_bounds__(kThreads, 2)
                 m_new = tmax;
             }
             float ps8[8];
-            uint32_t pr[32];
+            uint32_t pr[kKeys / 2];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const float a = fast_exp2(fmaf(sv[2 * j], p.qscale, -m_new));
-                const float b = fast_exp2(fmaf(sv[2 * j + 1], p.qscale, -m_new));
+            for (int j = 0; j < kKeys / 2; ++j) {
+                const float a = fast_exp2(fmaf(__uint_as_float(sr[(2 * j) >> 5][(2 * j) & 31]),
+                                               p.qscale, -m_new));
+                const float b = fast_exp2(fmaf(__uint_as_float(sr[(2 * j + 1) >> 5][(2 * j + 1) & 31]),
+                                               p.qscale, -m_new));
                 ps8[j & 7] = j < 8 ? a + b : ps8[j & 7] + (a + b);
                 pr[j] = pack_bf16(a, b);
             }
@@ -415,43 +461,32 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
                 for (int i = 0; i < w; ++i) ps8[i] += ps8[i + w];
             const float ps = ps8[0];
-            // P buffer kt % 2 was last read by P V of tile kt - 2; a rescale
-            // reads and writes O, so it waits for P V of tile kt - 1.
-            if (kt >= 2) {
-                ok = __all_sync(0xffffffffu, mbar_wait_bounded(&pv_done[kt & 1],
-                                                               ((kt - 2) >> 1) & 1, kWaitLimitNs)) &&
-                     !aborted();
-                if (!ok) break;
-                tc_fence_after();
-            }
+            // A rescale reads and writes O: P V(t - 1) is done (S(t) was issued after it).
             if (__any_sync(0xffffffffu, rescale)) {
-                ok = __all_sync(0xffffffffu,
-                                mbar_wait_bounded(&pv_done[(kt - 1) & 1], ((kt - 1) >> 1) & 1,
-                                                  kWaitLimitNs)) &&
-                     !aborted();
-                if (!ok) break;
-                tc_fence_after();
                 const float corr = rescale ? fast_exp2(m_ref - m_new) : 1.f;
                 l *= corr;
 #pragma unroll 1
                 for (int c = 0; c < D; c += 32) {
                     uint32_t o[32];
-                    tmem_ld32(tmem + lane_off + kColO + c, o);
+                    tmem_ld32(cols + kColO + c, o);
                     tmem_wait_ld();
 #pragma unroll
                     for (int j = 0; j < 32; ++j)
                         o[j] = __float_as_uint(__uint_as_float(o[j]) * corr);
-                    tmem_st32(tmem + lane_off + kColO + c, o);
+                    tmem_st32(cols + kColO + c, o);
                 }
                 if (rescale) m_ref = m_new;
             }
             l += ps;
-            tmem_st32(tmem + lane_off + kColP + 32 * (kt & 1), pr);
+            // P over the first half of S's columns.
+            tmem_st32(cols + kColP, *reinterpret_cast<uint32_t(*)[32]>(&pr[0]));
+            tmem_st32(cols + kColP + 32, *reinterpret_cast<uint32_t(*)[32]>(&pr[32]));
             tmem_wait_st();
             if (kt == ntiles - 1 && npages * kBlock > kmax) {
-                // Unwritten slots of the last page: zero their V rows (128-byte
-                // lines, whole, so the swizzle inside a line does not matter),
-                // once the V tile has landed.
+                // Unwritten slots of the CTA's last page: zero their V rows
+                // (128-byte lines, whole, so the swizzle inside a line does not
+                // matter), once the V tile has landed.  (Both Q tiles may end
+                // on this tile; each writes the same zeros before its P V.)
                 ok = __all_sync(0xffffffffu,
                                 mbar_wait_bounded(&v_full[kt % kStages], (kt / kStages) & 1,
                                                   kWaitLimitNs));
@@ -468,17 +503,16 @@ __global__ void __launch_bounds__(kThreads, 2)
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&p_full[kt & 1]);
+            if (lane == 0) mbar_arrive(p_full(qi));
         }
-        if (ok && ntiles > 0) {
-            const int kt = ntiles - 1;
-            ok = __all_sync(0xffffffffu,
-                            mbar_wait_bounded(&pv_done[kt & 1], (kt >> 1) & 1, kWaitLimitNs));
+        if (ok && my_ntiles > 0) {
+            const int kt = my_ntiles - 1;
+            ok = __all_sync(0xffffffffu, mbar_wait_bounded(pv_done(qi), kt & 1, kWaitLimitNs));
             tc_fence_after();
         }
         if (!ok) {
             if (lane == 0) abort_now();
-        } else {
+        } else if (my_ntiles > 0) {
             // out = O / l for this row
             const float inv = l > 0.f ? 1.f / l : 0.f;
             __nv_bfloat16 *orow =
@@ -486,7 +520,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll 1
             for (int c = 0; c < D; c += 32) {
                 uint32_t o[32];
-                tmem_ld32(tmem + lane_off + kColO + c, o);
+                tmem_ld32(cols + kColO + c, o);
                 tmem_wait_ld();
                 if (valid) {
 #pragma unroll
@@ -650,7 +684,7 @@ extern "C" int xs_paged_prefill_tc(void *out, const void *q, const void *k_cache
     p.oob_row = static_cast<int>(rows);
     p.qscale = scale * pftc::kLog2e;
     p.err_flag = err_flag;
-    const int tq = pftc::kRows / G;
+    const int tq = pftc::kQTiles * pftc::kRows / G;  // query tokens per CTA
     dim3 grid((T + tq - 1) / tq, Hkv);
     fn<<<grid, pftc::kThreads, smem, stream>>>(tmq, tmk, tmv, p);
     return launch_status();
