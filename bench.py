@@ -255,11 +255,22 @@ def cpu_baseline(w: wl.DecodeWorkload, target_s: float) -> dict:
     oracle_step(sample, threads)
     dt = time.perf_counter() - t0
     gbs = sample_bytes(w.cfg, sample) / dt / 1e9
+    # The same oracle on one core, on a smaller sample of its own (a few seconds).
+    seqs1 = pick_sample(w, min(target_s, 10.0) / 3.0, 1, seed=1)
+    sample1 = oracle_sample(w, seqs1)
+    t1 = time.perf_counter()
+    oracle_step(sample1, 1)
+    dt1 = time.perf_counter() - t1
+    gbs1 = sample_bytes(w.cfg, sample1) / dt1 / 1e9
     return {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
             "seconds": round(dt, 3),
             "sample": f"{len(seqs)} of {w.cfg.B} sequences (seeded), all {w.cfg.Hq} query heads, "
                       f"1 layer: append + fp64 attention over {int(sample['context_lens'].sum())} "
-                      f"tokens"}
+                      f"tokens",
+            "single_core": {"value": round(gbs1, 4), "unit": "GB/s", "cores": 1,
+                            "seconds": round(dt1, 3),
+                            "sample": f"{len(seqs1)} of {w.cfg.B} sequences (seeded), "
+                                      f"{int(sample1['context_lens'].sum())} tokens"}}
 
 
 # ------------------------------------------------------------------ arms
