@@ -31,9 +31,10 @@
 //    operands for 128 x 64 x 16 MACs: 681 / 825 TFLOP/s on the 8K / 32K
 //    chunked prefills; 128-key tiles read 8 KB for twice the MACs: 809 / 986.)
 //  * Warps 2-9 (softmax, four per Q tile; warp w reads TMEM lanes
-//    32*(w%4)..+31, one row per thread): load the row of S, causal mask, row
-//    max, P = 2^(s - m) in base 2 (maximum and sums as 8 independent
-//    chains), write P back to TMEM for the P V step.  The reference m only
+//    32*(w%4)..+31, one row per thread): load the row of S, causal mask
+//    (diagonal tiles only), row max (8 chains of three-input maxima),
+//    P = 2^(s - m) in base 2 (arguments and sums as packed fp32x2
+//    operations), write P back to TMEM for the P V step.  The reference m only
 //    moves when a tile's maximum exceeds it by more than 8 (log2 units), and
 //    only then is the row of O in TMEM rescaled, so P stays <= 2^8 and most
 //    tiles never touch O.  Unwritten slots of the last page (any bits at all)
@@ -171,6 +172,12 @@ __device__ __forceinline__ void tmem_wait_st() {
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<const uint32_t *>(&v);
+}
+// Maximum of three (one instruction).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
 }
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *tm, int x, int y,
                                             int z, uint64_t *bar) {
@@ -423,19 +430,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             // independent chains.
             const int k0 = kt * kKeys;
             const bool need_mask = k0 + kKeys - 1 > p.start + tok0 + qi * kTq;
+            float v[kKeys];
+#pragma unroll
+            for (int j = 0; j < kKeys; ++j) v[j] = __uint_as_float(sr[j >> 5][j & 31]);
+            if (need_mask) {
+#pragma unroll
+                for (int j = 0; j < kKeys; ++j) v[j] = k0 + j <= qpos ? v[j] : -INFINITY;
+            }
+            // Row maximum: 8 independent chains of three-input maxima.
             float mx8[8];
 #pragma unroll
-            for (int j = 0; j < kKeys; ++j) {
-                float x = __uint_as_float(sr[j >> 5][j & 31]);
-                x = !need_mask || k0 + j <= qpos ? x : -INFINITY;
-                sr[j >> 5][j & 31] = __float_as_uint(x);
-                mx8[j & 7] = j < 8 ? x : fmaxf(mx8[j & 7], x);
-            }
+            for (int c = 0; c < 8; ++c) mx8[c] = fmaxf(v[c], v[c + 8]);
 #pragma unroll
-            for (int w = 4; w > 0; w >>= 1)
+            for (int base = 16; base < kKeys; base += 16)
 #pragma unroll
-                for (int i = 0; i < w; ++i) mx8[i] = fmaxf(mx8[i], mx8[i + w]);
-            const float tmax = mx8[0] * p.qscale;
+                for (int c = 0; c < 8; ++c) mx8[c] = fmax3(mx8[c], v[base + c], v[base + 8 + c]);
+            const float tmax = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
+                                     fmaxf(mx8[6], mx8[7])) *
+                               p.qscale;
             bool rescale = false;
             float m_new = m_ref;
             if (kt == 0) {
@@ -445,22 +457,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 rescale = true;
                 m_new = tmax;
             }
-            float ps8[8];
+            // 2^(s * qscale - m) for key pairs: the arguments as packed fp32x2
+            // fmas, the sums as 4 packed chains.
+            const float2 qs2 = make_float2(p.qscale, p.qscale), nm2 = make_float2(-m_new, -m_new);
+            float2 ps4[4];
             uint32_t pr[kKeys / 2];
 #pragma unroll
             for (int j = 0; j < kKeys / 2; ++j) {
-                const float a = fast_exp2(fmaf(__uint_as_float(sr[(2 * j) >> 5][(2 * j) & 31]),
-                                               p.qscale, -m_new));
-                const float b = fast_exp2(fmaf(__uint_as_float(sr[(2 * j + 1) >> 5][(2 * j + 1) & 31]),
-                                               p.qscale, -m_new));
-                ps8[j & 7] = j < 8 ? a + b : ps8[j & 7] + (a + b);
-                pr[j] = pack_bf16(a, b);
+                const float2 t = __ffma2_rn(make_float2(v[2 * j], v[2 * j + 1]), qs2, nm2);
+                const float2 e = make_float2(fast_exp2(t.x), fast_exp2(t.y));
+                ps4[j & 3] = j < 4 ? e : __fadd2_rn(ps4[j & 3], e);
+                pr[j] = pack_bf16(e.x, e.y);
             }
-#pragma unroll
-            for (int w = 4; w > 0; w >>= 1)
-#pragma unroll
-                for (int i = 0; i < w; ++i) ps8[i] += ps8[i + w];
-            const float ps = ps8[0];
+            const float2 s01 = __fadd2_rn(__fadd2_rn(ps4[0], ps4[1]), __fadd2_rn(ps4[2], ps4[3]));
+            const float ps = s01.x + s01.y;
             // A rescale reads and writes O: P V(t - 1) is done (S(t) was issued after it).
             if (__any_sync(0xffffffffu, rescale)) {
                 const float corr = rescale ? fast_exp2(m_ref - m_new) : 1.f;
