@@ -10,23 +10,30 @@
 //
 // Design (flash-decoding, persistent, warp-specialised):
 //  * Work item = (sequence b, KV head g, partition p of P tokens).  Items are
-//    numbered by a per-CTA prefix sum over context_lens and dealt to a
-//    persistent grid round-robin; all items have the same size except a
-//    sequence's last one, so the grid drains evenly.
+//    numbered by a per-CTA prefix sum over context_lens (item_counts,
+//    decode_item) and taken by a persistent grid: the first two per CTA
+//    statically, the rest from a device counter that the last CTA resets.
 //  * Warp 0 is the producer: it reads block ids (32 at a time, coalesced) and
-//    streams each page pair (K page + V page of head g, 16 tokens x D, one
-//    contiguous run per the pool layout) into an S-stage shared-memory ring
-//    with 1-D bulk copies (cp.async.bulk) completing on mbarriers.  It also
-//    stages the G query rows of each item into a double-buffered q slot.
+//    streams each page pair (K page + V page of head g, 16 tokens x D) into an
+//    8-stage shared-memory ring completing on mbarriers - bf16 pages as 4-D
+//    TMA tensor copies with the 128-byte swizzle, fp32 pages as 1-D bulk
+//    copies - and stages the G query rows of each item in a double-buffered
+//    q slot.  It claims the next item when a ring of the current one is left.
 //  * Warps 1..4 are consumers.  Consumer c takes ring pages c, c+4, ... and
 //    keeps its own online-softmax state (running max m, sum l, output o) for
-//    all G heads.  QK: 8 lanes per token x 4 tokens per pass, each lane a
-//    D/8 slice of the row, reduce-scatter over the 8 lanes so each lane ends
-//    with one head's score.  PV: each lane owns D/32 output dims for all G
-//    heads; weights are broadcast through a per-warp shared buffer.
-//  * At the end of an item the four consumer states are merged in shared
-//    memory; the item writes the final bf16/fp32 output (single-partition
-//    sequence) or fp32 partials (o, m, l) for the split-K reduce.
+//    all G heads.  bf16: Q K^T and P V with mma.sync m16n8k16 (the G heads as
+//    the rows of A, the page's 16 keys as N), fragments by ldmatrix from the
+//    swizzled page.  fp32: QK with 8 lanes per token and a reduce-scatter; PV
+//    with each lane owning D/32 output dims.
+//  * Warp 5 is the merger: it merges the four consumer states of each item
+//    and writes the final output (single-partition sequence) or fp32
+//    partials (o, m, l) for the split-K combine.
+//  * One-launch step (xs_paged_decode_step): the item covering a sequence's
+//    last page first writes this step's K/V row into its slot, and the
+//    merger counts split items into their group; the item that completes a
+//    group combines its partials (staged in shared memory by bulk copies)
+//    into out.  With early reads, lengths, item tables, block ids and the
+//    first pages are read before waiting on the previous launch.
 //  * Logits are kept in base-2 units (q is pre-scaled by scale*log2(e)) so
 //    exponentials are single ex2 instructions.
 #include <cuda.h>
