@@ -76,11 +76,14 @@ def max_abs(out: torch.Tensor, ref: torch.Tensor) -> float:
     return (out.detach().cpu().double() - ref).abs().max().item()
 
 
-def check_step(w, layer, step, seqs=None, check_unchanged=True, strict=True, fused=True):
+def check_step(w, layer, step, seqs=None, check_unchanged=True, strict=True, fused=True,
+               repeat=1, early_reads=False):
     """Run one decode step (append + attention) of layer `layer` through the
     CUDA path - as one fused launch, or as the three separate calls - and
-    compare it with the oracle on the sequences `seqs`.  Returns the
-    attention max-abs error."""
+    compare it with the oracle on the sequences `seqs`.  `repeat` launches
+    the same step back to back (each appends the same rows again), with
+    early reads if asked, as the benchmark loop does.  Returns the attention
+    max-abs error of the last launch."""
     cfg = w.cfg
     seqs = list(range(cfg.B)) if seqs is None else list(seqs)
     kc, vc = w.k_cache[layer], w.v_cache[layer]
@@ -89,9 +92,13 @@ def check_step(w, layer, step, seqs=None, check_unchanged=True, strict=True, fus
     before_v = vc.clone() if check_unchanged else None
     out = torch.empty(cfg.B, cfg.Hq, cfg.D, dtype=cfg.dtype, device=kc.device)
     step.err_flag.zero_()
-    run = step.run if fused else step.run_unfused
-    run(out, w.q[layer], w.k_new[layer], w.v_new[layer], kc, vc, w.block_tables,
-        w.context_lens, w.scale)
+    for _ in range(repeat):
+        if fused:
+            step.run(out, w.q[layer], w.k_new[layer], w.v_new[layer], kc, vc, w.block_tables,
+                     w.context_lens, w.scale, early_reads=early_reads)
+        else:
+            step.run_unfused(out, w.q[layer], w.k_new[layer], w.v_new[layer], kc, vc,
+                             w.block_tables, w.context_lens, w.scale)
     torch.cuda.synchronize()
     assert step.error_flags() == 0, f"device error flag {step.error_flags()}"
     assert int(step.ws.work.count_nonzero()) == 0, "counters not left at zero"

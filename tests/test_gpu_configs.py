@@ -47,3 +47,27 @@ def test_config4_sampled():
         err = gh.check_step(w, 0, step, seqs=sorted(pick), check_unchanged=True, fused=fused)
         print(f"{w.cfg.name}: P={step.partition_tokens} parts<={step.max_partitions} "
               f"fused={fused} sampled max err {err:.3e}")
+
+
+@pytest.mark.parametrize("cfg_id", [1, 3])
+def test_config_early_reads_back_to_back(cfg_id):
+    # The benchmark's loop: the one-launch step with early reads, several
+    # launches back to back on the same pools and lengths (each appends the
+    # same rows again and may start while the previous one finishes).
+    dev = gh.device()
+    w = wl.make_workload(cfg_id, device=dev)
+    step = _step_for(w, dev)
+    for layer in range(min(w.cfg.layers, 2)):
+        gh.check_step(w, layer, step, repeat=4, early_reads=True)
+
+
+def test_config4_sampled_early_reads():
+    dev = gh.device()
+    w = wl.make_workload(4, device=dev)
+    step = _step_for(w, dev)
+    lens = w.context_lens.cpu()
+    g = torch.Generator().manual_seed(44)
+    pick = set(torch.randperm(w.cfg.B, generator=g)[:6].tolist())
+    pick |= {int(lens.argmax()), int(lens.argmin())}
+    gh.check_step(w, 0, step, seqs=sorted(pick), check_unchanged=True, repeat=3,
+                  early_reads=True)
