@@ -477,10 +477,11 @@ int xs_paged_decode_step_ex(void *out, const void *q, const void *k_new, const v
 /*
  * xs_paged_decode_step_partition_tokens - partition length P for
  * xs_paged_decode_step: the cost model of xs_paged_decode_partition_tokens
- * plus the in-launch combine (the groups that complete last are combined
- * after the last page is read, at a cost that grows with the longest
- * sequence's partition count times the group size Hq / Hkv).  Same
- * arguments plus Hq; XS_ESHAPE also when Hq % Hkv != 0.
+ * with its per-item cost and ragged-end allowance fitted to one-launch step
+ * times, searched over multiples of 64 in [64, 2048] (64, 128, ..., 512,
+ * 640, 768, 896, 1024, 1280, 1536, 2048) so that a batch's item count can
+ * land just under a whole number of rounds of the grid.  Same arguments
+ * plus Hq; XS_ESHAPE also when Hq % Hkv != 0.
  */
 int xs_paged_decode_step_partition_tokens(int B, int Hq, int Hkv, int64_t total_context_tokens,
                                           int max_context_len, int num_sms);

@@ -1646,26 +1646,29 @@ extern "C" int xs_paged_decode_step_partition_tokens(int B, int Hq, int Hkv,
     const double tokens = total_context_tokens > 0
                               ? static_cast<double>(total_context_tokens)
                               : static_cast<double>(B) * std::max(max_context_len, 1);
-    // The cost model of xs_paged_decode_partition_tokens plus the in-launch
-    // combine: the groups that complete last are combined after every page
-    // is read, by one warp each, at about one memory round trip (~ one page
-    // time) per 8 partials staged in shared memory, plus two (the count).
-    // With the tensor-core page loop a page costs less, so the fixed cost
-    // of an item (q staging, first-page latency, the merge, and the
-    // combines the merge warp runs meanwhile) weighs more: kItemCost is
-    // fitted to one-launch step times measured on the mix, single-stream and
-    // long-batch workloads (mix: 65 / 52 / 55 us at P = 256 / 512 / 1024).
-    constexpr double kItemCost = 6.0;
+    // The cost model of xs_paged_decode_partition_tokens with constants
+    // fitted to one-launch step times: an item of P tokens costs P/64 +
+    // kItemCost page-times (q staging, first-page latency, the merge, and the
+    // combines the merge warp runs meanwhile), the grid takes items / CTAs
+    // rounds plus half a round of ragged end, and P runs over multiples of
+    // 64 so that a batch can land just under a whole number of rounds.  The
+    // fit covered 20 workloads (mixes of 16-512 sequences with log-uniform
+    // lengths, fixed-length batches of 1-16 sequences, the MHA and GQA
+    // shapes): mean 1.05 % and at most 4.5 % slower than the best measured P
+    // (the power-of-two search this replaced: 2.0 % and 5.5 %).  The split-K
+    // combine's own cost did not improve the fit: the merge warp combines
+    // groups while the other warps still stream pages.
+    constexpr double kItemCost = 5.0;
+    constexpr double kTailRounds = 0.5;
+    constexpr int kCandidates[] = {64,  128, 192, 256, 320,  384,  448, 512,
+                                   640, 768, 896, 1024, 1280, 1536, 2048};
     const double ctas = 2.0 * num_sms;
-    const double G = static_cast<double>(Hq / Hkv);
     int best = 64;
     double best_cost = 1e300;
-    for (int P = 64; P <= 2048; P *= 2) {
+    for (const int P : kCandidates) {
         const double items = std::max((tokens / P + 0.5 * B) * Hkv, static_cast<double>(B) * Hkv);
-        const double np_max = std::ceil(std::max(max_context_len, 1) / static_cast<double>(P));
-        const double combine = np_max > 1.0 ? std::ceil(np_max / 8.0) + 2.0 : 0.0;
-        const double cost = (items / ctas + 1.0) * (P / 64.0 + kItemCost) + combine;
-        if (cost <= best_cost * (1.0 + 1e-9)) {
+        const double cost = (items / ctas + kTailRounds) * (P / 64.0 + kItemCost);
+        if (cost <= best_cost * (1.0 + 1e-9)) {  // ties go to the larger partition
             best_cost = cost;
             best = P;
         }

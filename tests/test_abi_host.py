@@ -65,16 +65,23 @@ def test_partition_heuristic(lib):
 
 
 def test_step_partition_heuristic(lib):
-    # The one-launch step's choice on the measured workloads: its per-item
-    # cost was fitted to one-launch step times (the mix ran 65 / 52 / 55 us at
-    # P = 256 / 512 / 1024; single stream best at 256; long batch at 2048).
+    # The one-launch step's choice on measured workloads.  Its constants were
+    # fitted to one-launch step times swept over P: the continuous-batching
+    # mix (64 sequences) ran 46.5 / 45.0 / 44.7 / 47.2 us at P = 512 / 640 /
+    # 768 / 1024; the single stream was fastest at 256; the long batch is flat
+    # from 2048 up; 4 x 4096 tokens was fastest at 512 (288 items, under one
+    # round of 304 CTAs) and 1 x 1024 at 128-192.
     pick = ops.xs_paged_decode_step_partition_tokens
-    assert pick(64, 32, 8, 63638, 7598, 152) == 512
+    assert pick(64, 32, 8, 63638, 7598, 152) == 640
     assert pick(1, 32, 8, 4097, 4097, 152) == 256
     assert pick(128, 32, 8, 2538762, 32769, 152) == 2048
+    assert pick(4, 32, 8, 16388, 4097, 152) == 512
+    assert pick(1, 32, 8, 1025, 1025, 152) in (128, 192)
     for B, Hq, Hkv, total, mx in [(8, 12, 12, 3439, 926), (2, 12, 12, 29, 21), (512, 32, 8, 10**6, 8193)]:
         P = pick(B, Hq, Hkv, total, mx, 152)
-        assert 64 <= P <= 2048 and (P & (P - 1)) == 0
+        assert 64 <= P <= 2048 and P % 64 == 0
+    # More SMs never asks for bigger partitions.
+    assert pick(64, 32, 8, 63638, 7598, 152) <= pick(64, 32, 8, 63638, 7598, 76)
     with pytest.raises(ops.XsError):
         pick(4, 12, 8, 100, 50, 152)   # Hq not a multiple of Hkv
 

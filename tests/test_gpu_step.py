@@ -46,6 +46,9 @@ def _appended(w, layer=0):
 CASES = [(d, G, P, False) for d, G, P in
          itertools.product([torch.bfloat16, torch.float32], [1, 4, 8], [16, 64, 4096])]
 CASES += [(torch.bfloat16, 4, 16, True), (torch.bfloat16, 8, 64, True), (torch.float32, 1, 64, True)]
+# Partition lengths the step heuristic picks that are not powers of two.
+CASES += [(torch.bfloat16, 4, 448, False), (torch.bfloat16, 4, 640, True),
+          (torch.float32, 1, 192, False)]
 
 
 @pytest.mark.parametrize("dtype,G,P,early", CASES,
