@@ -247,13 +247,25 @@ def pick_sample(w: wl.DecodeWorkload, target_s: float, threads: int, seed: int =
     return sorted(chosen)
 
 
-def cpu_baseline(w: wl.DecodeWorkload, target_s: float) -> dict:
+def cpu_baseline(w: wl.DecodeWorkload, target_s: float, gpu_out: torch.Tensor | None = None):
+    """The oracle timed on the host cores on a seeded sample of the workload.
+    With gpu_out (layer 0's output of the timed steps, [B, Hq, D]) it also
+    returns the largest absolute difference between the GPU output and the
+    oracle's on the sampled sequences, against the stated tolerance."""
     threads = len(os.sched_getaffinity(0))
     seqs = pick_sample(w, target_s, threads)
     sample = oracle_sample(w, seqs)
     t0 = time.perf_counter()
-    oracle_step(sample, threads)
+    ref = oracle_step(sample, threads)
     dt = time.perf_counter() - t0
+    parity = None
+    if gpu_out is not None:
+        sel = torch.tensor(seqs, dtype=torch.long, device=gpu_out.device)
+        got = gpu_out.index_select(0, sel).cpu().double()
+        tol = 1e-2 if w.cfg.dtype == torch.bfloat16 else 1e-5
+        err = float((got - ref).abs().max()) if got.numel() else 0.0
+        parity = {"max_abs_err": err, "tolerance": tol, "ok": bool(err <= tol),
+                  "sequences": len(seqs), "reference": "fp64 CPU oracle, same seeded sample"}
     gbs = sample_bytes(w.cfg, sample) / dt / 1e9
     # The same oracle on one core, on a smaller sample of its own (a few seconds).
     seqs1 = pick_sample(w, min(target_s, 10.0) / 3.0, 1, seed=1)
@@ -262,7 +274,7 @@ def cpu_baseline(w: wl.DecodeWorkload, target_s: float) -> dict:
     oracle_step(sample1, 1)
     dt1 = time.perf_counter() - t1
     gbs1 = sample_bytes(w.cfg, sample1) / dt1 / 1e9
-    return {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+    line = {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
             "seconds": round(dt, 3),
             "sample": f"{len(seqs)} of {w.cfg.B} sequences (seeded), all {w.cfg.Hq} query heads, "
                       f"1 layer: append + fp64 attention over {int(sample['context_lens'].sum())} "
@@ -271,6 +283,7 @@ def cpu_baseline(w: wl.DecodeWorkload, target_s: float) -> dict:
                             "seconds": round(dt1, 3),
                             "sample": f"{len(seqs1)} of {w.cfg.B} sequences (seeded), "
                                       f"{int(sample1['context_lens'].sum())} tokens"}}
+    return line, parity
 
 
 # ------------------------------------------------------------------ arms
@@ -512,7 +525,13 @@ def run_ours(args, rank, world, local, dist):
         "clocks": clock_info,
     }
     if not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+        # The sampled parity check compares with the plain oracle: not for
+        # the sinks / window variant, whose oracle is a different function.
+        plain = sinks is None and args.window == 0
+        line["cpu_baseline"], parity = cpu_baseline(w, args.cpu_seconds,
+                                                    gpu_out=out[0] if plain else None)
+        if parity is not None:
+            line["parity"] = parity
     print(json.dumps(line), flush=True)
 
 

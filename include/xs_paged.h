@@ -91,6 +91,11 @@ extern "C" {
 #define XS_FLAG_POOL_EMPTY 32 /* the free-block stack was empty (allocation)
                                  or full (release); that sequence was left
                                  as it was                                    */
+#define XS_FLAG_BOUNDS 64   /* only in the debug build (libxs_paged_debug.so,
+                               compiled with -DXS_DEBUG_BOUNDS): a computed
+                               global-memory index fell outside its buffer;
+                               the access was skipped.  Release builds never
+                               set it (the checks compile away).              */
 
 /*
  * xs_slot_mapping - where each sequence's new token goes (one decode step).
@@ -543,6 +548,21 @@ int xs_paged_decode_noalloc(void *out, const void *q, const void *k_cache, const
  * xs_version - library version as MAJOR*10000 + MINOR*100 + PATCH.
  */
 int xs_version(void);
+
+/*
+ * xs_debug_bounds_failures - in the debug library (libxs_paged_debug.so,
+ * the same sources compiled with -DXS_DEBUG_BOUNDS), the number of in-kernel
+ * bounds checks that failed on the current device since the last reset
+ * (reset != 0 clears the count after reading it).  Every global-memory index
+ * the kernels compute is checked there against its buffer's extent before
+ * the access; a failure skips the access and raises XS_FLAG_BOUNDS.  The
+ * paper has no counterpart of this entry point: the checks are a test aid
+ * standing in for a device memory checker.  Synchronous (it copies the
+ * counters).
+ * Returns XS_EUNSUPPORTED in the release library, XS_EDEVICE if the copy
+ * failed.
+ */
+int xs_debug_bounds_failures(int reset);
 
 #ifdef __cplusplus
 }

@@ -79,6 +79,8 @@ __global__ void __launch_bounds__(kAppendThreads)
         const int64_t blk = slot / bs, off = slot - (slot / bs) * bs;
         const int64_t dst = ((blk * Hkv + h) * bs + off) * chunks_per_row + c;
         const int64_t src = t * per_token + hc;
+        if (!XS_BOUNDS(dst >= 0 && dst < num_blocks * Hkv * bs * chunks_per_row, err_flag))
+            continue;
         if (is_v)
             v_cache[dst] = v_new[src];
         else
@@ -117,6 +119,8 @@ __global__ void __launch_bounds__(kAppendThreads)
         const int64_t dst = ((static_cast<int64_t>(blk) * Hkv + h) * bs + pos % bs) *
                                 chunks_per_row + c;
         const int64_t src = (h * T + t) * chunks_per_row + c;
+        if (!XS_BOUNDS(dst >= 0 && dst < num_blocks * Hkv * bs * chunks_per_row, err_flag))
+            continue;
         if (is_v)
             v_cache[dst] = v_src[src];
         else
@@ -158,6 +162,8 @@ int launch_append(bool from_table, const void *k_new, const void *v_new, void *k
 }
 
 }  // namespace
+XS_DEFINE_BOUNDS_COUNTER(bounds_failures_append)
+
 }  // namespace xs
 
 extern "C" int xs_slot_mapping(const int32_t *block_tables, int max_blocks_per_seq,

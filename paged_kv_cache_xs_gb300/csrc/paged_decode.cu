@@ -434,6 +434,11 @@ __device__ __noinline__ bool combine_partials(const Params &p, const Item &it, i
     const float *pm = p.part_m + head0 * p.max_parts;
     const float *pl = p.part_l + head0 * p.max_parts;
     float *rows = stage->rows();
+    if (!XS_BOUNDS(np >= 1 && np <= p.max_parts && head0 >= 0 &&
+                       head0 + G <= static_cast<int64_t>(p.B) * p.Hq &&
+                       static_cast<int>(sizeof(Stage)) + G * K * D * 4 <= p.stage_bytes,
+                   p.err_flag))
+        return true;  // (debug build) nothing read or written
     float acc[G][kDims], den[G], run_m[G];
 #pragma unroll
     for (int h = 0; h < G; ++h) {
@@ -666,7 +671,9 @@ __device__ __noinline__ bool count_and_combine(const Params &p, int lane, int pe
     __syncwarp();
     int *cnt = p.combine + static_cast<int64_t>(pend_b) * p.Hkv + pend_g;
     int prior = 0;
-    if (lane < npend) prior = atomic_add_acq_rel_gpu(cnt, 1);
+    if (lane < npend &&
+        XS_BOUNDS(pend_b >= 0 && pend_b < p.B && pend_g >= 0 && pend_g < p.Hkv, p.err_flag))
+        prior = atomic_add_acq_rel_gpu(cnt, 1);
     const bool last = lane < npend && prior == pend_np - 1;
     unsigned todo = __ballot_sync(0xffffffffu, last);
     if (todo) __syncwarp();
@@ -878,7 +885,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
         auto load_ids = [&](const Item &it, int base) {
             int32_t blk = 0;
             const int pg = base + lane;
-            if (it.b >= 0 && pg < it.pg1)
+            if (it.b >= 0 && pg < it.pg1 &&
+                XS_BOUNDS(it.b < p.B && pg >= 0 && pg < p.max_blocks, p.err_flag))
                 blk = p.block_tables[static_cast<int64_t>(it.b) * p.table_stride + pg];
             return blk;
         };
@@ -896,7 +904,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
         auto load_row = [&](const Item &it) {
             Row r;
             r.raw_len = 0;
-            if (p.k_new && it.b >= 0 && it.tok1 == nlen[it.b] && it.tok1 > 0) {
+            if (p.k_new && it.b >= 0 && it.tok1 == nlen[it.b] && it.tok1 > 0 &&
+                XS_BOUNDS(it.b < p.B && it.g >= 0 && it.g < p.Hkv, p.err_flag)) {
                 r.raw_len = p.context_lens[it.b];
                 const int64_t row = static_cast<int64_t>(it.b) * p.Hkv + it.g;
                 const uint4 *kn = static_cast<const uint4 *>(p.k_new) + row * C::kChunksPerRow;
@@ -944,8 +953,9 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
                 ok = mbar_wait_bounded(&qempty[slot], (k & 1) ^ 1, kWaitLimitNs);
                 if (ok) {
                     item_slot[slot] = it;
-                    if (it.b < 0) {
-                        mbar_arrive(&qfull[slot]);
+                    if (it.b < 0 || !XS_BOUNDS(it.b < p.B && it.g >= 0 && (it.g + 1) * G <= p.Hq,
+                                               p.err_flag)) {
+                        mbar_arrive(&qfull[slot]);  // end marker (or, debug build: skipped rows)
                     } else {
                         unsigned char *dst = smem + C::kQSlotOff + slot * C::kQBytes;
                         const int64_t qoff = (static_cast<int64_t>(it.b) * p.Hq +
@@ -1602,11 +1612,28 @@ int pool_maps(const void *k, const void *v, int64_t num_blocks, int Hkv, int D, 
 }
 
 }  // namespace attn
+XS_DEFINE_BOUNDS_COUNTER(bounds_failures_decode)
+
 }  // namespace xs
 
 using namespace xs;
 
 extern "C" int xs_version(void) { return 100; }
+
+extern "C" int xs_debug_bounds_failures(int reset) {
+#ifdef XS_DEBUG_BOUNDS
+    int total = 0;
+    for (const int v : {bounds_failures_append(reset), bounds_failures_decode(reset),
+                        bounds_failures_prefill_tc(reset)}) {
+        if (v < 0) return v;
+        total += v;
+    }
+    return total;
+#else
+    (void)reset;
+    return XS_EUNSUPPORTED;
+#endif
+}
 
 extern "C" int xs_paged_decode_partition_tokens(int B, int Hkv, int64_t total_context_tokens,
                                                 int max_context_len, int num_sms) {

@@ -99,6 +99,7 @@ struct TCfg {
 struct PParams {
     __nv_bfloat16 *out;            // [T, Hq, D]
     const int32_t *block_ids;      // [n_ids]
+    int n_ids;
     int T, start, Hq, Hkv;
     int64_t num_blocks;
     int oob_row;                   // a row coordinate past the pool: zero-filled pages
@@ -276,7 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto page_row = [&](int kt) {
             int row = p.oob_row;
             const int pg = kt * kPagesPerTile + lane;
-            if (lane < kPagesPerTile && pg < npages) {
+            if (lane < kPagesPerTile && pg < npages && XS_BOUNDS(pg < p.n_ids, p.err_flag)) {
                 const int32_t blk = p.block_ids[pg];
                 if (blk < 0 || blk >= p.num_blocks)
                     raise_flag(p.err_flag, XS_FLAG_BAD_BLOCK);  // read as zeros
@@ -532,7 +533,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t o[32];
                 tmem_ld32(cols + kColO + c, o);
                 tmem_wait_ld();
-                if (valid) {
+                if (valid && XS_BOUNDS(tok0 + tl < p.T && (g + 1) * G <= p.Hq, p.err_flag)) {
 #pragma unroll
                     for (int j = 0; j < 32; j += 8) {
                         uint4 w;
@@ -617,6 +618,8 @@ KernelFn pick(int D, int G) {
 }
 
 }  // namespace pftc
+XS_DEFINE_BOUNDS_COUNTER(bounds_failures_prefill_tc)
+
 }  // namespace xs
 
 using namespace xs;
@@ -686,6 +689,7 @@ extern "C" int xs_paged_prefill_tc(void *out, const void *q, const void *k_cache
     pftc::PParams p;
     p.out = static_cast<__nv_bfloat16 *>(out);
     p.block_ids = block_ids;
+    p.n_ids = n_ids;
     p.T = T;
     p.start = start_pos;
     p.Hq = Hq;

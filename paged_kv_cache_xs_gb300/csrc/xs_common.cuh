@@ -48,6 +48,49 @@ __device__ __forceinline__ void raise_flag(int *err_flag, int bit) {
     if (err_flag) atomicOr(err_flag, bit);
 }
 
+// ------------------------------------------------------------------ debug bounds checks
+// Compiled with -DXS_DEBUG_BOUNDS (the debug library), XS_BOUNDS(cond, flag)
+// evaluates cond - that a computed global-memory index lies inside its
+// buffer - and when it does not, ORs XS_FLAG_BOUNDS into *flag and yields
+// false, so the guarded access is skipped.  It stands in for a device memory
+// checker: the debug library runs the same cases as the release one and the
+// flag must stay clear.  In release builds it is the constant true.
+// Failed checks are also counted per translation unit (err_flag is optional),
+// and xs_debug_bounds_failures() returns the sum over the library.
+#ifdef XS_DEBUG_BOUNDS
+static __device__ unsigned int g_bounds_failures;
+__device__ __forceinline__ bool bounds_ok(bool ok, int *err_flag) {
+    if (!ok) {
+        raise_flag(err_flag, XS_FLAG_BOUNDS);
+        atomicAdd(&g_bounds_failures, 1u);
+    }
+    return ok;
+}
+#define XS_BOUNDS(cond, err_flag) (::xs::bounds_ok(static_cast<bool>(cond), (err_flag)))
+// This translation unit's count of failed checks on the current device
+// (optionally cleared), or a negative XS_E* code.
+#define XS_DEFINE_BOUNDS_COUNTER(fn)                                                       \
+    int fn(int reset) {                                                                   \
+        unsigned int v = 0;                                                               \
+        if (cudaMemcpyFromSymbol(&v, ::xs::g_bounds_failures, sizeof(v)) != cudaSuccess) \
+            return XS_EDEVICE;                                                            \
+        if (reset) {                                                                      \
+            const unsigned int z = 0;                                                     \
+            if (cudaMemcpyToSymbol(::xs::g_bounds_failures, &z, sizeof(z)) != cudaSuccess) \
+                return XS_EDEVICE;                                                        \
+        }                                                                                 \
+        return static_cast<int>(v);                                                       \
+    }
+#else
+#define XS_BOUNDS(cond, err_flag) true
+#define XS_DEFINE_BOUNDS_COUNTER(fn) \
+    int fn(int) { return 0; }
+#endif
+// Per translation unit (kv_append.cu, paged_decode.cu, paged_prefill_tc.cu).
+int bounds_failures_append(int reset);
+int bounds_failures_decode(int reset);
+int bounds_failures_prefill_tc(int reset);
+
 // ------------------------------------------------------------------ mbarrier + bulk copy
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {

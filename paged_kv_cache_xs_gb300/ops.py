@@ -70,6 +70,7 @@ SIGNATURES = {
     "xs_paged_decode_step_counters": (_L, [_I, _I]),
     "xs_paged_decode_step_partition_tokens": (_I, [_I, _I, _I, _L, _I, _I]),
     "xs_version": (_I, []),
+    "xs_debug_bounds_failures": (_I, [_I]),
 }
 
 _lock = threading.Lock()
@@ -370,6 +371,28 @@ def xs_paged_prefill(out, part_o, part_m, part_l, q, k_cache, v_cache, block_ids
 
 def xs_version() -> int:
     return load().xs_version()
+
+
+def xs_debug_bounds_failures(reset: bool = False, lib=None) -> int:
+    """Failed in-kernel bounds checks on the current device (debug library
+    only; the release library returns XS_EUNSUPPORTED)."""
+    return (lib or load()).xs_debug_bounds_failures(int(bool(reset)))
+
+
+def load_debug():
+    """The debug library (in-kernel bounds checks), as a separate handle: the
+    release library stays the one the wrappers above use unless a caller
+    installs this one with use_library()."""
+    return load(_build.DEBUG_LIB_PATH)
+
+
+def use_library(lib):
+    """Make `lib` (e.g. load_debug()) the library every wrapper calls; returns
+    the previous one (None if none was loaded yet)."""
+    global _lib
+    with _lock:
+        prev, _lib = _lib, lib
+    return prev
 
 
 # ---------------------------------------------------------------- workspace holder
