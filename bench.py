@@ -572,8 +572,10 @@ def run_swap(args, rank, world, local, dist):
         torch.cuda.synchronize()
         return e0.elapsed_time(e1) / reps
 
+    clocks = ClockSampler(local)
     t_out = timed(lambda: ops.xs_kv_swap(kd, vd, kh, vh, out_map, err_flag=err), args.steps)
     t_in = timed(lambda: ops.xs_kv_swap(kh, vh, kd, vd, in_map, err_flag=err), args.steps)
+    clock_info = clocks.stop()
     assert int(err.item()) == 0
     # Reference: one contiguous DMA copy of the same bytes each way.
     flat_d = torch.empty(moved // 2, dtype=torch.uint8, device=dev)
@@ -593,9 +595,54 @@ def run_swap(args, rank, world, local, dist):
                    "block_bytes": kd[0].numel() * kd.element_size(), "pool_blocks": nb},
         "swap_out_gbs": round(gbs(t_out), 2), "swap_in_gbs": round(gbs(t_in), 2),
         "dma_copy_d2h_gbs": round(gbs(t_d2h), 2), "dma_copy_h2d_gbs": round(gbs(t_h2d), 2),
+        # Bound by the host link, not HBM: the peak is the plain DMA copy of the
+        # same bytes over that link, measured in this run (both directions).
+        "roofline": {"kernel": "kv_swap_kernel", "bound": "link",
+                     "achieved": round(gbs((t_out + t_in) / 2), 2),
+                     "peak": round(gbs((t_d2h + t_h2d) / 2), 2), "unit": "GB/s",
+                     "frac": round((t_d2h + t_h2d) / (t_out + t_in), 4),
+                     "peak_kind": "DMA copy (cudaMemcpyAsync) of the same bytes, this run",
+                     "traffic": None},
         "gpu_launches": 2 * args.steps,
+        "clocks": clock_info,
     }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"], line["parity"] = swap_cpu_baseline(kd, vd, kh, vh, blocks,
+                                                                 args.cpu_seconds)
     print(json.dumps(line), flush=True)
+
+
+def swap_cpu_baseline(kd, vd, kh, vh, blocks, target_s: float):
+    """The oracle's swap-out (block copies between two host pools) timed on a
+    seeded sample of the swapped blocks, repeated for about target_s / 4
+    seconds; and a bit-exact check of the GPU's swap-out of those blocks
+    against the oracle's."""
+    import oracle
+    g = torch.Generator().manual_seed(11)
+    n = blocks.numel()
+    pick = torch.randperm(n, generator=g)[:min(n, 1024)]
+    src_k = kd.index_select(0, blocks[pick].to(kd.device)).cpu()
+    src_v = vd.index_select(0, blocks[pick].to(vd.device)).cpu()
+    m = len(pick)
+    mapping = torch.stack([torch.arange(m), torch.arange(m)], 1).to(torch.int64)
+    dst_k, dst_v = torch.zeros_like(src_k), torch.zeros_like(src_v)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        ek, ev = oracle.kv_swap(src_k, src_v, dst_k, dst_v, mapping)
+        reps += 1
+        dt = time.perf_counter() - t0
+        if dt >= target_s / 4:
+            break
+    moved = 2 * m * src_k[0].numel() * src_k.element_size()
+    got_k, got_v = kh[pick], vh[pick]
+    exact = bool(torch.equal(got_k.view(torch.int16), ek.view(torch.int16)) and
+                 torch.equal(got_v.view(torch.int16), ev.view(torch.int16)))
+    base = {"value": round(moved * reps / dt / 1e9, 3), "unit": "GB/s", "cores": 1,
+            "kind": "oracle", "seconds": round(dt, 3),
+            "sample": f"{m} of {n} swapped blocks (seeded), K and V, host pool to host pool, "
+                      f"{reps} repetitions"}
+    parity = {"bit_exact": exact, "blocks": m, "reference": "oracle swap-out of the same blocks"}
+    return base, parity
 
 
 def run_prefill(args, rank, world, local, dist):
@@ -648,9 +695,14 @@ def run_prefill(args, rank, world, local, dist):
             if ev is not None:
                 ev[c][1].record()
 
+    clocks = ClockSampler(local)
     for _ in range(args.warmup):
         prefill_all()
     torch.cuda.synchronize()
+    t_load = time.time()
+    while time.time() - t_load < args.load_seconds:  # >= ~1 s under load for the clock sampler
+        prefill_all()
+        torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
     for _ in range(args.steps):
@@ -658,6 +710,7 @@ def run_prefill(args, rank, world, local, dist):
     e1.record()
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / args.steps
+    clock_info = clocks.stop()
     # The attention launches alone, bracketed by events (one more pass).
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(nchunks)]
     prefill_all(ev)
@@ -693,8 +746,46 @@ def run_prefill(args, rank, world, local, dist):
         "attention_tflops": round(tflops, 2),
         "roofline": roof,
         "gpu_launches": args.steps * nchunks * (2 if tensor else 3),
+        "clocks": clock_info,
     }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"], line["parity"] = prefill_cpu_baseline(
+            q, kc, vc, ids, out, total, flop, args.cpu_seconds)
     print(json.dumps(line), flush=True)
+
+
+def prefill_cpu_baseline(q, kc, vc, ids, out, total: int, total_flop: float, target_s: float):
+    """The fp64 oracle's chunked-prefill attention on the host cores, timed on
+    the last n query tokens of the sequence (the rows with the longest
+    contexts; n calibrated on one row for about target_s seconds), reported as
+    the whole sequence's tokens/s at the oracle's measured flop rate; and the
+    max-abs difference of the GPU's output rows against the oracle's."""
+    import oracle
+    threads = len(os.sched_getaffinity(0))
+    Hq, D = q.shape[1], q.shape[2]
+    kc_h, vc_h, ids_h = kc.cpu(), vc.cpu(), ids.cpu()
+    scale = D ** -0.5
+
+    def rows_flop(s0, n):  # 4 D flop per (query head, query token, attended key)
+        return 4 * D * Hq * sum(p + 1 for p in range(s0, s0 + n))
+
+    t0 = time.perf_counter()
+    oracle.paged_prefill(q[total - 1:].cpu(), kc_h, vc_h, ids_h, total - 1, scale, nthreads=threads)
+    dt1 = max(time.perf_counter() - t0, 1e-4)
+    n = max(1, min(total, int(target_s / dt1)))
+    s0 = total - n
+    t0 = time.perf_counter()
+    ref = oracle.paged_prefill(q[s0:].cpu(), kc_h, vc_h, ids_h, s0, scale, nthreads=threads)
+    dt = time.perf_counter() - t0
+    rate = rows_flop(s0, n) / dt  # flop/s
+    err = float((out[s0:].cpu().double() - ref).abs().max())
+    base = {"value": round(total / (total_flop / rate), 2), "unit": "tokens/s", "cores": threads,
+            "kind": "oracle", "tflops": round(rate / 1e12, 5), "seconds": round(dt, 3),
+            "sample": f"query tokens {s0}..{total - 1} of {total} (all {Hq} heads), fp64; "
+                      f"value = the whole sequence at the sample's flop rate"}
+    parity = {"max_abs_err": err, "tolerance": 1e-2, "ok": bool(err <= 1e-2), "rows": n,
+              "reference": "fp64 CPU oracle on the same rows"}
+    return base, parity
 
 
 def main(argv=None):
