@@ -211,19 +211,26 @@ def oracle_sample(w: wl.DecodeWorkload, seqs: list[int], layer: int = 0):
                 block_tables=nbt, context_lens=lens, scale=w.scale)
 
 
-def oracle_step(sample: dict, threads: int):
+def oracle_step(sample: dict, threads: int, sinks=None, window: int = 0):
+    """Append + attention of the sampled sequences in the oracle (with sinks
+    and a window: the gpt-oss variant's oracle)."""
     import oracle
     slots = oracle.slot_mapping(sample["block_tables"], sample["context_lens"], 16,
                                 sample["k_cache"].shape[0])
     kc, vc = oracle.kv_append(sample["k_new"], sample["v_new"], sample["k_cache"],
                               sample["v_cache"], slots)
+    if sinks is not None or window > 0:
+        return oracle.paged_decode_sinks(sample["q"], kc, vc, sample["block_tables"],
+                                         sample["context_lens"], sample["scale"],
+                                         sinks=None if sinks is None else sinks.cpu(),
+                                         window=window, nthreads=threads)
     return oracle.paged_decode(sample["q"], kc, vc, sample["block_tables"],
                                sample["context_lens"], sample["scale"], nthreads=threads)
 
 
-def sample_bytes(cfg, sample) -> int:
+def sample_bytes(cfg, sample, window: int = 0) -> int:
     sub = wl.DecodeConfig(**{**cfg.__dict__, "B": len(sample["context_lens"])})
-    return step_bytes(sub, sample["context_lens"])["step"]
+    return step_bytes(sub, sample["context_lens"], window)["step"]
 
 
 def pick_sample(w: wl.DecodeWorkload, target_s: float, threads: int, seed: int = 0):
@@ -247,7 +254,8 @@ def pick_sample(w: wl.DecodeWorkload, target_s: float, threads: int, seed: int =
     return sorted(chosen)
 
 
-def cpu_baseline(w: wl.DecodeWorkload, target_s: float, gpu_out: torch.Tensor | None = None):
+def cpu_baseline(w: wl.DecodeWorkload, target_s: float, gpu_out: torch.Tensor | None = None,
+                 sinks=None, window: int = 0):
     """The oracle timed on the host cores on a seeded sample of the workload.
     With gpu_out (layer 0's output of the timed steps, [B, Hq, D]) it also
     returns the largest absolute difference between the GPU output and the
@@ -256,7 +264,7 @@ def cpu_baseline(w: wl.DecodeWorkload, target_s: float, gpu_out: torch.Tensor | 
     seqs = pick_sample(w, target_s, threads)
     sample = oracle_sample(w, seqs)
     t0 = time.perf_counter()
-    ref = oracle_step(sample, threads)
+    ref = oracle_step(sample, threads, sinks, window)
     dt = time.perf_counter() - t0
     parity = None
     if gpu_out is not None:
@@ -266,14 +274,14 @@ def cpu_baseline(w: wl.DecodeWorkload, target_s: float, gpu_out: torch.Tensor | 
         err = float((got - ref).abs().max()) if got.numel() else 0.0
         parity = {"max_abs_err": err, "tolerance": tol, "ok": bool(err <= tol),
                   "sequences": len(seqs), "reference": "fp64 CPU oracle, same seeded sample"}
-    gbs = sample_bytes(w.cfg, sample) / dt / 1e9
+    gbs = sample_bytes(w.cfg, sample, window) / dt / 1e9
     # The same oracle on one core, on a smaller sample of its own (a few seconds).
     seqs1 = pick_sample(w, min(target_s, 10.0) / 3.0, 1, seed=1)
     sample1 = oracle_sample(w, seqs1)
     t1 = time.perf_counter()
-    oracle_step(sample1, 1)
+    oracle_step(sample1, 1, sinks, window)
     dt1 = time.perf_counter() - t1
-    gbs1 = sample_bytes(w.cfg, sample1) / dt1 / 1e9
+    gbs1 = sample_bytes(w.cfg, sample1, window) / dt1 / 1e9
     line = {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
             "seconds": round(dt, 3),
             "sample": f"{len(seqs)} of {w.cfg.B} sequences (seeded), all {w.cfg.Hq} query heads, "
@@ -525,13 +533,11 @@ def run_ours(args, rank, world, local, dist):
         "clocks": clock_info,
     }
     if not args.no_cpu_baseline:
-        # The sampled parity check compares with the plain oracle: not for
-        # the sinks / window variant, whose oracle is a different function.
-        plain = sinks is None and args.window == 0
-        line["cpu_baseline"], parity = cpu_baseline(w, args.cpu_seconds,
-                                                    gpu_out=out[0] if plain else None)
-        if parity is not None:
-            line["parity"] = parity
+        # The oracle of the step that ran (with sinks / a window: the gpt-oss
+        # variant's), timed on the host and compared with layer 0's output.
+        line["cpu_baseline"], parity = cpu_baseline(w, args.cpu_seconds, gpu_out=out[0],
+                                                    sinks=sinks, window=args.window)
+        line["parity"] = parity
     print(json.dumps(line), flush=True)
 
 
@@ -643,6 +649,104 @@ def swap_cpu_baseline(kd, vd, kh, vh, blocks, target_s: float):
                       f"{reps} repetitions"}
     parity = {"bit_exact": exact, "blocks": m, "reference": "oracle swap-out of the same blocks"}
     return base, parity
+
+
+def run_alloc(args, rank, world, local, dist):
+    """Device page allocator row: every step, one launch advances each of the
+    workload's sequences by one token and pops a free block for each token
+    that starts a page; the oracle replays the same steps on its own copy."""
+    from paged_kv_cache_xs_gb300 import build as xsbuild
+    from paged_kv_cache_xs_gb300 import ops
+    import oracle
+
+    xsbuild.build()
+    ops.load()
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    cfg = wl.CONFIGS[args.config]
+    bs = cfg.block_size
+    gen = torch.Generator().manual_seed(cfg.seed + 7919 * rank)
+    hist = wl.draw_history(cfg, gen)                      # tokens already in the cache
+    nsteps = args.warmup + args.steps
+    width = int((hist.max() + nsteps + bs - 1) // bs) + 1  # room for every step's growth
+    pages = [(int(n) + bs - 1) // bs for n in hist.tolist()]
+    need = sum(pages) + cfg.B * ((nsteps + bs - 1) // bs + 1)
+    nb = max(2 * need, 1024)
+    perm = torch.randperm(nb, generator=gen).to(torch.int32)
+    bt = torch.full((cfg.B, width), -1, dtype=torch.int32)
+    pos = 0
+    for b, p in enumerate(pages):
+        bt[b, :p] = perm[pos:pos + p]
+        pos += p
+    stack, top0 = perm[pos:].clone(), nb - pos
+    dbt, dlens = bt.to(dev), hist.to(dev)
+    dstack = stack.to(dev)
+    dtop = torch.tensor([top0], dtype=torch.int32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    step = lambda: ops.xs_block_alloc_decode(dbt, dlens, dstack, dtop, block_size=bs,
+                                             err_flag=err)
+    # Eager warm-up, then the K timed steps as one CUDA graph (the allocator
+    # runs inside a captured decode step; eager launches from Python would
+    # time the host's launch path instead).  Capture executes nothing.
+    clocks = ClockSampler(local)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for _ in range(args.steps):
+            step()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    graph.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    clock_info = clocks.stop()
+    if clock_info is not None:
+        clock_info["note"] = "the timed replay is shorter than the sampling interval"
+    us = e0.elapsed_time(e1) * 1e3 / args.steps
+    assert int(err.item()) == 0, f"device error flags {int(err.item())}"
+    if rank != 0:
+        return
+    # The oracle: the same steps from the same state, timed on the host.
+    obt, olens, otop = bt, hist, top0
+    t0 = time.perf_counter()
+    for _ in range(nsteps):
+        obt, olens, otop, failed = oracle.block_alloc_decode(obt, olens, bs, stack, otop)
+    dt_cpu = time.perf_counter() - t0
+    gbt, glens, gtop = dbt.cpu(), dlens.cpu(), int(dtop.item())
+    used_gpu = sorted(int(x) for x in gbt[gbt >= 0].tolist())
+    used_cpu = sorted(int(x) for x in obt[obt >= 0].tolist())
+    # Which popped block went to which sequence depends on the order of the
+    # atomics: compare what is unique, and that every table covers its length.
+    covered = all(int((gbt[b] >= 0).sum()) == (int(glens[b]) + bs - 1) // bs
+                  for b in range(cfg.B))
+    exact = bool(torch.equal(glens, olens) and gtop == otop and used_gpu == used_cpu and
+                 len(set(used_gpu)) == len(used_gpu) and covered)
+    line = {
+        "metric": "device page allocation (sequence-steps/s; one launch per decode step)",
+        "value": round(cfg.B / (us * 1e-6), 1), "unit": "sequence-steps/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us / 1e3, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int32",
+        "data": "synthetic",
+        "config": {"workload": f"{cfg.name}_alloc", "B": cfg.B, "block_size": bs,
+                   "pool_blocks": nb, "max_blocks_per_seq": width},
+        "roofline": {"kernel": "block_alloc_decode_kernel", "bound": "latency",
+                     "achieved": round(us, 3), "peak": None, "unit": "us per launch",
+                     "note": "a few hundred bytes per launch (lengths, popped ids, table "
+                             "entries): one dependent load / atomic / store chain; "
+                             "no bandwidth or compute roofline applies", "traffic": None},
+        "gpu_launches": args.steps,
+        "cuda_graph": True,
+        "clocks": clock_info,
+        "cpu_baseline": {"value": round(cfg.B * nsteps / dt_cpu, 1), "unit": "sequence-steps/s",
+                         "cores": 1, "kind": "oracle", "seconds": round(dt_cpu, 3),
+                         "sample": f"all {cfg.B} sequences, {nsteps} steps"},
+        "parity": {"exact": exact, "steps": nsteps,
+                   "compared": "lengths, stack top and the set of blocks in use equal the "
+                               "oracle's; no block twice; every table covers its length"},
+    }
+    print(json.dumps(line), flush=True)
 
 
 def run_prefill(args, rank, world, local, dist):
@@ -796,9 +900,10 @@ def main(argv=None):
     ap.add_argument("--config", type=int, default=4,
                     help="workload index (0-4); default: the large-batch long-context one")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--op", choices=["decode", "swap", "prefill"], default="decode",
+    ap.add_argument("--op", choices=["decode", "swap", "prefill", "alloc"], default="decode",
                     help="decode: the decode step (default); swap: KV block swap to pinned "
-                         "host; prefill: chunked prefill into the paged cache")
+                         "host; prefill: chunked prefill into the paged cache; alloc: the "
+                         "device page allocator")
     ap.add_argument("--prefill-tokens", type=int, default=8192)
     ap.add_argument("--prefill-chunk", type=int, default=1024)
     ap.add_argument("--prefill-impl", choices=["tensor", "cuda-core"], default="tensor",
@@ -837,6 +942,8 @@ def main(argv=None):
             run_swap(args, rank, world, local, dist)
         elif args.op == "prefill":
             run_prefill(args, rank, world, local, dist)
+        elif args.op == "alloc":
+            run_alloc(args, rank, world, local, dist)
         else:
             run_ours(args, rank, world, local, dist)
     finally:
