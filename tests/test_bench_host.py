@@ -64,3 +64,36 @@ def test_max_over_ranks_gloo_two_ranks():
     for p in procs:
         p.join(timeout=60)
     assert res == {0: 2.5, 1: 2.5}
+
+
+def test_prefill_oracle_leg_on_host_tensors():
+    # The prefill line's oracle leg on a small CPU case whose "GPU output" is
+    # the oracle's own: the parity object reports zero error and the rate
+    # bookkeeping is positive and consistent.
+    import oracle
+    g = torch.Generator().manual_seed(5)
+    Hq, Hkv, D, bs, total = 4, 2, 64, 16, 48
+    pages = total // bs
+    ids = torch.randperm(2 * pages, generator=g)[:pages].to(torch.int32)
+    kc = torch.randn(2 * pages, Hkv, bs, D, generator=g).to(torch.bfloat16)
+    vc = torch.randn(2 * pages, Hkv, bs, D, generator=g).to(torch.bfloat16)
+    q = torch.randn(total, Hq, D, generator=g).to(torch.bfloat16)
+    out = oracle.paged_prefill(q, kc, vc, ids, 0, D ** -0.5)
+    flop = 4 * D * Hq * total * (total + 1) / 2
+    base, parity = bench.prefill_cpu_baseline(q, kc, vc, ids, out, total, flop, 0.01)
+    assert parity["max_abs_err"] == 0.0 and parity["ok"] and 1 <= parity["rows"] <= total
+    assert base["kind"] == "oracle" and base["value"] > 0 and base["tflops"] > 0
+
+
+def test_swap_oracle_leg_on_host_tensors():
+    g = torch.Generator().manual_seed(6)
+    nb, n = 40, 12
+    kd = torch.randn(nb, 2, 16, 64, generator=g).to(torch.bfloat16)
+    vd = torch.randn(nb, 2, 16, 64, generator=g).to(torch.bfloat16)
+    blocks = torch.randperm(nb, generator=g)[:n]
+    kh, vh = kd[blocks].clone(), vd[blocks].clone()      # a correct swap-out
+    base, parity = bench.swap_cpu_baseline(kd, vd, kh, vh, blocks, 0.02)
+    assert parity["bit_exact"] and parity["blocks"] == n and base["value"] > 0
+    vh[3, 1, 5, 7] += 1                                  # one element off
+    _, parity = bench.swap_cpu_baseline(kd, vd, kh, vh, blocks, 0.02)
+    assert not parity["bit_exact"]
