@@ -657,7 +657,6 @@ def run_alloc(args, rank, world, local, dist):
     that starts a page; the oracle replays the same steps on its own copy."""
     from paged_kv_cache_xs_gb300 import build as xsbuild
     from paged_kv_cache_xs_gb300 import ops
-    import oracle
 
     xsbuild.build()
     ops.load()
@@ -708,21 +707,6 @@ def run_alloc(args, rank, world, local, dist):
     assert int(err.item()) == 0, f"device error flags {int(err.item())}"
     if rank != 0:
         return
-    # The oracle: the same steps from the same state, timed on the host.
-    obt, olens, otop = bt, hist, top0
-    t0 = time.perf_counter()
-    for _ in range(nsteps):
-        obt, olens, otop, failed = oracle.block_alloc_decode(obt, olens, bs, stack, otop)
-    dt_cpu = time.perf_counter() - t0
-    gbt, glens, gtop = dbt.cpu(), dlens.cpu(), int(dtop.item())
-    used_gpu = sorted(int(x) for x in gbt[gbt >= 0].tolist())
-    used_cpu = sorted(int(x) for x in obt[obt >= 0].tolist())
-    # Which popped block went to which sequence depends on the order of the
-    # atomics: compare what is unique, and that every table covers its length.
-    covered = all(int((gbt[b] >= 0).sum()) == (int(glens[b]) + bs - 1) // bs
-                  for b in range(cfg.B))
-    exact = bool(torch.equal(glens, olens) and gtop == otop and used_gpu == used_cpu and
-                 len(set(used_gpu)) == len(used_gpu) and covered)
     line = {
         "metric": "device page allocation (sequence-steps/s; one launch per decode step)",
         "value": round(cfg.B / (us * 1e-6), 1), "unit": "sequence-steps/s", "n_gpus": world,
@@ -739,14 +723,39 @@ def run_alloc(args, rank, world, local, dist):
         "gpu_launches": args.steps,
         "cuda_graph": True,
         "clocks": clock_info,
-        "cpu_baseline": {"value": round(cfg.B * nsteps / dt_cpu, 1), "unit": "sequence-steps/s",
-                         "cores": 1, "kind": "oracle", "seconds": round(dt_cpu, 3),
-                         "sample": f"all {cfg.B} sequences, {nsteps} steps"},
-        "parity": {"exact": exact, "steps": nsteps,
-                   "compared": "lengths, stack top and the set of blocks in use equal the "
-                               "oracle's; no block twice; every table covers its length"},
     }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"], line["parity"] = alloc_cpu_baseline(
+            bt, hist, stack, top0, nsteps, bs, dbt.cpu(), dlens.cpu(), int(dtop.item()))
     print(json.dumps(line), flush=True)
+
+
+def alloc_cpu_baseline(bt, lens, stack, top, nsteps: int, bs: int, gbt, glens, gtop: int):
+    """The oracle's allocation over the same steps from the same state, timed
+    on one host core, and compared with the device's result.  Which popped
+    block went to which sequence depends on the order of the atomics, so what
+    is unique is compared (lengths, stack top, the set of blocks in use), and
+    every table must hold each block once and cover its length."""
+    import oracle
+    obt, olens, otop = bt, lens, top
+    t0 = time.perf_counter()
+    for _ in range(nsteps):
+        obt, olens, otop, _ = oracle.block_alloc_decode(obt, olens, bs, stack, otop)
+    dt = time.perf_counter() - t0
+    B = lens.numel()
+    used_gpu = sorted(int(x) for x in gbt[gbt >= 0].tolist())
+    used_cpu = sorted(int(x) for x in obt[obt >= 0].tolist())
+    covered = all(int((gbt[b] >= 0).sum()) == (max(int(glens[b]), 0) + bs - 1) // bs
+                  for b in range(B))
+    exact = bool(torch.equal(glens, olens) and gtop == otop and used_gpu == used_cpu and
+                 len(set(used_gpu)) == len(used_gpu) and covered)
+    base = {"value": round(B * nsteps / dt, 1), "unit": "sequence-steps/s", "cores": 1,
+            "kind": "oracle", "seconds": round(dt, 3),
+            "sample": f"all {B} sequences, {nsteps} steps"}
+    parity = {"exact": exact, "steps": nsteps,
+              "compared": "lengths, stack top and the set of blocks in use equal the oracle's; "
+                          "no block twice; every table covers its length"}
+    return base, parity
 
 
 def run_prefill(args, rank, world, local, dist):

@@ -97,3 +97,27 @@ def test_swap_oracle_leg_on_host_tensors():
     vh[3, 1, 5, 7] += 1                                  # one element off
     _, parity = bench.swap_cpu_baseline(kd, vd, kh, vh, blocks, 0.02)
     assert not parity["bit_exact"]
+
+
+def test_alloc_oracle_leg_on_host_tensors():
+    import oracle
+    g = torch.Generator().manual_seed(7)
+    B, bs, width, nb, nsteps = 6, 16, 8, 64, 20
+    lens = torch.randint(0, 60, (B,), generator=g, dtype=torch.int32)
+    perm = torch.randperm(nb, generator=g).to(torch.int32)
+    bt = torch.full((B, width), -1, dtype=torch.int32)
+    pos = 0
+    for b in range(B):
+        p = (int(lens[b]) + bs - 1) // bs
+        bt[b, :p] = perm[pos:pos + p]
+        pos += p
+    stack, top = perm[pos:].clone(), nb - pos
+    obt, olens, otop = bt, lens, top
+    for _ in range(nsteps):                       # stands in for the device's result
+        obt, olens, otop, _ = oracle.block_alloc_decode(obt, olens, bs, stack, otop)
+    base, parity = bench.alloc_cpu_baseline(bt, lens, stack, top, nsteps, bs, obt, olens, otop)
+    assert parity["exact"] and base["value"] > 0
+    bad = olens.clone()
+    bad[2] += 1                                    # one length off
+    _, parity = bench.alloc_cpu_baseline(bt, lens, stack, top, nsteps, bs, obt, bad, otop)
+    assert not parity["exact"]
