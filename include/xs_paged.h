@@ -293,6 +293,18 @@ int xs_paged_decode_partition_tokens(int B, int Hkv, int64_t total_context_token
 int xs_paged_decode_max_partitions(int max_blocks_per_seq, int block_size, int partition_tokens);
 
 /*
+ * xs_paged_decode_num_splits - the split-K factor of the longest sequence:
+ * how many partitions of xs_paged_decode_partition_tokens(B, Hkv,
+ * B * max_context_len, max_context_len, sm_count) tokens a context of
+ * max_context_len tokens is cut into (1 = no split, no reduce needed).  The
+ * split is chosen from the batch, the KV heads, the context length and the
+ * SM count so that the work items fill the resident CTAs (2 per SM).  Host
+ * only.  Returns the count (>= 1), or XS_ESHAPE (B < 0, Hkv <= 0,
+ * max_context_len < 0, sm_count <= 0).
+ */
+int xs_paged_decode_num_splits(int B, int Hkv, int max_context_len, int sm_count);
+
+/*
  * xs_paged_decode_workspace_bytes - bytes of fp32 partials for the split:
  * part_o [B, Hq, max_partitions, D], part_m and part_l [B, Hq,
  * max_partitions], each rounded up to 256 bytes (the caller may carve one

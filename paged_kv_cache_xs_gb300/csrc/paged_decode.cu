@@ -1710,6 +1710,14 @@ extern "C" int xs_paged_decode_max_partitions(int max_blocks_per_seq, int block_
     return static_cast<int>(std::max<int64_t>(1, (cap + partition_tokens - 1) / partition_tokens));
 }
 
+extern "C" int xs_paged_decode_num_splits(int B, int Hkv, int max_context_len, int sm_count) {
+    if (B < 0 || Hkv <= 0 || max_context_len < 0 || sm_count <= 0) return XS_ESHAPE;
+    const int P = xs_paged_decode_partition_tokens(
+        B, Hkv, static_cast<int64_t>(B) * max_context_len, max_context_len, sm_count);
+    if (P < 0) return P;
+    return std::max(1, (max_context_len + P - 1) / P);
+}
+
 extern "C" size_t xs_paged_decode_workspace_bytes(int B, int Hq, int D, int max_partitions) {
     if (B <= 0 || Hq <= 0 || D <= 0 || max_partitions <= 0) return 0;
     auto up = [](size_t x) { return (x + 255) / 256 * 256; };

@@ -38,6 +38,7 @@ SIGNATURES = {
     "xs_kv_append_paged": (_I, [_P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _L, _I, _P, _P]),
     "xs_paged_decode_partition_tokens": (_I, [_I, _I, _L, _I, _I]),
     "xs_paged_decode_max_partitions": (_I, [_I, _I, _I]),
+    "xs_paged_decode_num_splits": (_I, [_I, _I, _I, _I]),
     "xs_paged_decode_workspace_bytes": (_S, [_I, _I, _I, _I]),
     "xs_paged_decode_attn": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I,
                                   _L, _F, _I, _I, _I, _P, _P, _P]),
@@ -185,6 +186,15 @@ def xs_paged_decode_max_partitions(max_blocks_per_seq, block_size, partition_tok
     r = load().xs_paged_decode_max_partitions(max_blocks_per_seq, block_size, partition_tokens)
     if r < 0:
         raise XsError("xs_paged_decode_max_partitions", r)
+    return r
+
+
+def xs_paged_decode_num_splits(B, Hkv, max_context_len, sm_count) -> int:
+    """Partitions (split-K factor) of the longest sequence under the
+    library's heuristic; 1 means no split."""
+    r = load().xs_paged_decode_num_splits(B, Hkv, max_context_len, sm_count)
+    if r < 0:
+        raise XsError("xs_paged_decode_num_splits", r)
     return r
 
 

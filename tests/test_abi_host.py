@@ -86,6 +86,19 @@ def test_step_partition_heuristic(lib):
         pick(4, 12, 8, 100, 50, 152)   # Hq not a multiple of Hkv
 
 
+def test_num_splits(lib):
+    # The split-K factor of the longest sequence: the context cut into the
+    # heuristic's partitions; a single stream is split, a large batch of
+    # short contexts is not.
+    for B, Hkv, mx in [(1, 8, 4097), (128, 8, 32769), (64, 8, 8193), (8, 12, 1025), (2, 12, 21)]:
+        P = ops.xs_paged_decode_partition_tokens(B, Hkv, B * mx, mx, 152)
+        assert ops.xs_paged_decode_num_splits(B, Hkv, mx, 152) == max(1, -(-mx // P))
+    assert ops.xs_paged_decode_num_splits(1, 8, 4097, 152) > 1
+    assert ops.xs_paged_decode_num_splits(512, 8, 64, 152) == 1
+    assert ops.xs_paged_decode_num_splits(1, 8, 0, 152) == 1
+    assert lib.xs_paged_decode_num_splits(1, 0, 100, 152) == -2   # XS_ESHAPE
+
+
 def test_max_partitions_and_workspace(lib):
     assert ops.xs_paged_decode_max_partitions(2049, 16, 1024) == 33
     assert ops.xs_paged_decode_max_partitions(1, 16, 1024) == 1
