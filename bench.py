@@ -490,7 +490,9 @@ def run_ours(args, rank, world, local, dist):
     # The fused launch also appends the new rows and writes the output.
     launch_bytes = by["step"] if fused else by["attn"]
     attn_gbs = launch_bytes / (attn_avg_ms * 1e-3) / 1e9
-    traffic = kernel_traffic(cfg.name)
+    # The committed DRAM counters were taken on the plain one-launch step
+    # (no sinks, no window); any other form of the launch reports none.
+    traffic = kernel_traffic(cfg.name) if fused and sinks is None and args.window == 0 else None
     line = {
         "metric": METRIC,
         "value": round(value, 2),
