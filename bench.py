@@ -491,8 +491,10 @@ def run_ours(args, rank, world, local, dist):
     launch_bytes = by["step"] if fused else by["attn"]
     attn_gbs = launch_bytes / (attn_avg_ms * 1e-3) / 1e9
     # The committed DRAM counters were taken on the plain one-launch step
-    # (no sinks, no window); any other form of the launch reports none.
-    traffic = kernel_traffic(cfg.name) if fused and sinks is None and args.window == 0 else None
+    # (no sinks, no window, the heuristic's partition); any other form of the
+    # launch reports none.
+    plain = fused and sinks is None and args.window == 0 and not args.partition_tokens
+    traffic = kernel_traffic(cfg.name) if plain else None
     line = {
         "metric": METRIC,
         "value": round(value, 2),
