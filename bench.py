@@ -77,10 +77,11 @@ def bf16_peak(sustained: bool) -> tuple[float, str]:
         return (1700.0 if sustained else 1900.0), "fallback"
 
 
-def kernel_traffic(workload: str) -> int | None:
+def kernel_traffic(workload: str, variant: str = "") -> int | None:
     """Per-launch DRAM bytes of the attention kernel from the committed ncu
-    summary, if it was taken on the current kernel source."""
-    path = os.path.join(ROOT, "profiles", f"paged_decode_attn_{workload}.md")
+    summary of this workload (and launch variant, e.g. "_sinks_w4096"), if
+    it was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", f"paged_decode_attn_{workload}{variant}.md")
     try:
         text = open(path).read()
     except OSError:
@@ -490,11 +491,12 @@ def run_ours(args, rank, world, local, dist):
     # The fused launch also appends the new rows and writes the output.
     launch_bytes = by["step"] if fused else by["attn"]
     attn_gbs = launch_bytes / (attn_avg_ms * 1e-3) / 1e9
-    # The committed DRAM counters were taken on the plain one-launch step
-    # (no sinks, no window, the heuristic's partition); any other form of the
-    # launch reports none.
-    plain = fused and sinks is None and args.window == 0 and not args.partition_tokens
-    traffic = kernel_traffic(cfg.name) if plain else None
+    # The committed DRAM counters were taken on the one-launch step at the
+    # heuristic's partition, plain or with sinks and a window (a summary per
+    # variant); any other form of the launch reports none.
+    variant = (f"_sinks_w{args.window}" if sinks is not None else f"_w{args.window}") \
+        if (sinks is not None or args.window > 0) else ""
+    traffic = kernel_traffic(cfg.name, variant) if fused and not args.partition_tokens else None
     line = {
         "metric": METRIC,
         "value": round(value, 2),
