@@ -33,7 +33,9 @@
 //    merger counts split items into their group; the item that completes a
 //    group combines its partials (staged in shared memory by bulk copies)
 //    into out.  With early reads, lengths, item tables, block ids and the
-//    first pages are read before waiting on the previous launch.
+//    first pages are read before waiting on the previous launch (in a launch
+//    of 1-16 rounds of items, the first item's next pages are also
+//    prefetched into L2).
 //  * Logits are kept in base-2 units (q is pre-scaled by scale*log2(e)) so
 //    exponentials are single ex2 instructions.
 #include <cuda.h>
@@ -57,6 +59,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s per bounded wait
 constexpr int kMaxBatch = 8192;                   // per-sequence tables live in shared memory
 constexpr int kClaimAhead = 8;  // pages of the current item left to issue when the next is claimed
+constexpr int kL2Ahead = 16;    // pages of the first item prefetched into L2 before the launch wait
 
 // Per-sequence tables a CTA keeps in shared memory: pfull[B + 1], ptail[B + 1]
 // (item numbering) and nlen[B] (clamped context lengths).
@@ -1032,6 +1035,23 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
                 const int end = A.tok1 == nlen[A.b] ? A.pg1 - 1 : A.pg1;
                 pre = min(kStages, max(0, end - A.pg0));
                 if (pre > 0) ok = issue(A, idsA, min(32, A.pg1 - A.pg0), 0, pre);
+                // In a launch of 1 to 16 rounds of items, the item's next
+                // kL2Ahead pages also go to L2 (a cache hint: no shared memory,
+                // nothing waits for it), so after the wait they stream from L2
+                // while the previous launch's tail has left HBM underused.  L2
+                // is the device's point of coherence, so a page the previous
+                // launch writes later still reads right.  (Measured: 64-sequence
+                // mixes 1.3-3.3 % faster; a 30-round launch 0.3 % slower and a
+                // launch of under one round 0.7 % slower, hence the bounds.)
+                const bool l2_ahead = total_items >= static_cast<int>(gridDim.x) &&
+                                      total_items <= 16 * static_cast<int>(gridDim.x);
+                const int lim = l2_ahead ? min(min(32, A.pg1 - A.pg0), pre + kL2Ahead) : 0;
+                if (lane >= pre && lane < lim && idsA >= 0 && idsA < p.num_blocks) {
+                    const int64_t off =
+                        (static_cast<int64_t>(idsA) * p.Hkv + A.g) * C::kPageBytes;
+                    prefetch_l2(kbase + off, C::kPageBytes);
+                    prefetch_l2(vbase + off, C::kPageBytes);
+                }
             }
             griddep_wait();
             griddep_launch_dependents();
