@@ -34,7 +34,7 @@
 //    group combines its partials (staged in shared memory by bulk copies)
 //    into out.  With early reads, lengths, item tables, block ids and the
 //    first pages are read before waiting on the previous launch (in a launch
-//    of 1-16 rounds of items, the first item's next pages are also
+//    of at most 16 rounds of items, the first item's next pages are also
 //    prefetched into L2).
 //  * Logits are kept in base-2 units (q is pre-scaled by scale*log2(e)) so
 //    exponentials are single ex2 instructions.
@@ -1035,16 +1035,15 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
                 const int end = A.tok1 == nlen[A.b] ? A.pg1 - 1 : A.pg1;
                 pre = min(kStages, max(0, end - A.pg0));
                 if (pre > 0) ok = issue(A, idsA, min(32, A.pg1 - A.pg0), 0, pre);
-                // In a launch of 1 to 16 rounds of items, the item's next
+                // In a launch of at most 16 rounds of items, the item's next
                 // kL2Ahead pages also go to L2 (a cache hint: no shared memory,
                 // nothing waits for it), so after the wait they stream from L2
                 // while the previous launch's tail has left HBM underused.  L2
                 // is the device's point of coherence, so a page the previous
                 // launch writes later still reads right.  (Measured: 64-sequence
-                // mixes 1.3-3.3 % faster; a 30-round launch 0.3 % slower and a
-                // launch of under one round 0.7 % slower, hence the bounds.)
-                const bool l2_ahead = total_items >= static_cast<int>(gridDim.x) &&
-                                      total_items <= 16 * static_cast<int>(gridDim.x);
+                // mixes 1.3-3.3 % faster; a 30-round launch, where the start
+                // is a small share, 0.3 % slower, hence the bound.)
+                const bool l2_ahead = total_items <= 16 * static_cast<int>(gridDim.x);
                 const int lim = l2_ahead ? min(min(32, A.pg1 - A.pg0), pre + kL2Ahead) : 0;
                 if (lane >= pre && lane < lim && idsA >= 0 && idsA < p.num_blocks) {
                     const int64_t off =
