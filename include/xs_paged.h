@@ -469,9 +469,13 @@ int xs_paged_decode_step(void *out, const void *q, const void *k_new, const void
  * reads context_lens, block_tables and the first pages of each CTA's first
  * work item BEFORE waiting for that kernel to complete, overlapping that
  * start-up (lengths -> item tables -> block ids -> pages: dependent memory
- * round trips) with the previous kernel's tail.  q, k_new/v_new, the
- * counters and every write wait for it as usual; a page that receives this
- * launch's appended row is not read early.  The caller promises that the
+ * round trips) with the previous kernel's tail.  In a launch of at most 16
+ * rounds of work items (a round: one item per resident CTA), each CTA also
+ * prefetches the next 16 pages of its first item into L2 at that point (a
+ * cache hint: L2 is coherent, so nothing stale can be read through it).
+ * q, k_new/v_new, the counters and every write wait for it as usual; a page
+ * that receives this launch's appended row is not read early.  The caller
+ * promises that the
  * kernel launched just before this one on the stream (if it is still
  * running) writes none of context_lens, block_tables, or the pages of
  * k_cache/v_cache this launch attends to (other than the rows it appends
