@@ -572,9 +572,10 @@ def run_swap(args, rank, world, local, dist):
     moved = 2 * n * kd[0].numel() * kd.element_size()          # K + V bytes per direction
     err = torch.zeros(1, dtype=torch.int32, device=dev)
 
-    def timed(fn, reps):
+    def timed(fn, reps):  # slowest rank's time per call
         for _ in range(args.warmup):
             fn()
+        barrier(dist)
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
@@ -582,7 +583,7 @@ def run_swap(args, rank, world, local, dist):
             fn()
         e1.record()
         torch.cuda.synchronize()
-        return e0.elapsed_time(e1) / reps
+        return max_over_ranks(e0.elapsed_time(e1) / reps, dist)
 
     clocks = ClockSampler(local)
     t_out = timed(lambda: ops.xs_kv_swap(kd, vd, kh, vh, out_map, err_flag=err), args.steps)
@@ -599,7 +600,7 @@ def run_swap(args, rank, world, local, dist):
     gbs = lambda ms: moved / (ms * 1e-3) / 1e9
     line = {
         "metric": "KV swap GB/s (device pool <-> pinned host swap pool)",
-        "value": round(gbs((t_out + t_in) / 2), 2), "unit": "GB/s", "n_gpus": world,
+        "value": round(world * gbs((t_out + t_in) / 2), 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t_out + t_in, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if cfg.dtype == torch.bfloat16 else "f32", "data": "synthetic",
@@ -702,6 +703,8 @@ def run_alloc(args, rank, world, local, dist):
         for _ in range(args.steps):
             step()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(dist)
+    torch.cuda.synchronize()
     e0.record()
     graph.replay()
     e1.record()
@@ -709,13 +712,14 @@ def run_alloc(args, rank, world, local, dist):
     clock_info = clocks.stop()
     if clock_info is not None:
         clock_info["note"] = "the timed replay is shorter than the sampling interval"
-    us = e0.elapsed_time(e1) * 1e3 / args.steps
+    us = max_over_ranks(e0.elapsed_time(e1) * 1e3 / args.steps, dist)  # slowest rank
     assert int(err.item()) == 0, f"device error flags {int(err.item())}"
     if rank != 0:
         return
     line = {
         "metric": "device page allocation (sequence-steps/s; one launch per decode step)",
-        "value": round(cfg.B / (us * 1e-6), 1), "unit": "sequence-steps/s", "n_gpus": world,
+        "value": round(world * cfg.B / (us * 1e-6), 1), "unit": "sequence-steps/s",
+        "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us / 1e3, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int32",
         "data": "synthetic",
@@ -823,12 +827,14 @@ def run_prefill(args, rank, world, local, dist):
         prefill_all()
         torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(dist)
+    torch.cuda.synchronize()
     e0.record()
     for _ in range(args.steps):
         prefill_all()
     e1.record()
     torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / args.steps
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, dist)  # slowest rank
     clock_info = clocks.stop()
     # The attention launches alone, bracketed by events (one more pass).
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(nchunks)]
@@ -856,7 +862,7 @@ def run_prefill(args, rank, world, local, dist):
                 "note": "fp32 CUDA-core FMA path (the decode kernel in prefill mode)"}
     line = {
         "metric": "chunked prefill attention over the paged cache (tokens/s, TFLOP/s)",
-        "value": round(total / (ms * 1e-3), 1), "unit": "tokens/s", "n_gpus": world,
+        "value": round(world * total / (ms * 1e-3), 1), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
