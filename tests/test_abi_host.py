@@ -35,6 +35,19 @@ def test_header_declares_entry_points():
         assert required in names
 
 
+def test_every_defined_entry_point_is_declared():
+    # The reverse direction: no extern "C" function of the sources ships
+    # without its declaration (and documentation) in the header.
+    defined = set()
+    for src in glob.glob(os.path.join(ROOT, "paged_kv_cache_xs_gb300", "csrc", "*.cu")):
+        text = open(src).read()
+        defined.update(re.findall(r'extern "C"\s+(?:int|int64_t|size_t|void)\s+(xs_\w+)\s*\(',
+                                  text))
+    assert "xs_paged_decode_step" in defined
+    undeclared = sorted(defined - set(declared_functions()))
+    assert not undeclared, f"defined but not declared in include/: {undeclared}"
+
+
 def test_library_exports_every_declared_symbol(lib):
     missing = [n for n in declared_functions() if not hasattr(lib, n)]
     assert not missing, f"not exported: {missing}"
