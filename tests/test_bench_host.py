@@ -121,3 +121,25 @@ def test_alloc_oracle_leg_on_host_tensors():
     bad[2] += 1                                    # one length off
     _, parity = bench.alloc_cpu_baseline(bt, lens, stack, top, nsteps, bs, obt, bad, otop)
     assert not parity["exact"]
+
+
+def test_reference_arm_under_torchrun_two_ranks():
+    # The launch the driver uses for N > 1 (torchrun, one process per rank,
+    # rendezvous on 127.0.0.1), here on gloo without a GPU: rank 0 alone runs
+    # the oracle arm and prints one JSON line; the other rank exits 0.
+    import socket
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    r = subprocess.run([sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+                        "--nproc-per-node", "2", "--master-addr", "127.0.0.1",
+                        "--master-port", str(port), os.path.join(ROOT, "bench.py"),
+                        "--impl", "reference", "--config", "0", "--gpus", "2", "--steps", "2",
+                        "--warmup", "3", "--ref-step-seconds", "0.05"],
+                       capture_output=True, text=True, timeout=300,
+                       env={**os.environ, "CUDA_VISIBLE_DEVICES": "", "OMP_NUM_THREADS": "1"})
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
