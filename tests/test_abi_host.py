@@ -230,3 +230,20 @@ def test_step_ex_flags_validated(lib):
     assert lib.xs_paged_decode_step_ex(*args, 1 << 30, ops.XS_BF16, None, None) == -5
     # A known flag passes through to the usual checks (NULL counters here).
     assert lib.xs_paged_decode_step_ex(*args, 1, ops.XS_BF16, None, None) == -6
+
+
+def test_missing_library_fails_loudly(tmp_path, monkeypatch):
+    # No CPU fallback: without the compiled library every wrapper raises
+    # instead of computing anything another way.
+    from paged_kv_cache_xs_gb300 import build as b
+    with pytest.raises(ImportError):
+        ops.load(str(tmp_path / "libxs_paged.so"))
+    monkeypatch.setattr(b, "LIB_PATH", str(tmp_path / "libxs_paged.so"))
+    prev = ops.use_library(None)
+    try:
+        with pytest.raises(ImportError):
+            ops.xs_version()
+        with pytest.raises(ImportError):
+            ops.xs_paged_decode_num_splits(1, 8, 4097, 152)
+    finally:
+        ops.use_library(prev)
