@@ -7,8 +7,8 @@ Prints ONE JSON line (rank 0).  A step is one pass of the whole hot path over
 one batch: for every layer, the paged KV append of the new token of each
 sequence, the split-K paged decode attention and the split-K reduce.  The
 default workload is the large-batch long-context one (128 sequences, contexts
-U[4097, 32769], Qwen3-8B attention shape, bf16, ~17 GB pool): it reads ~9.7 GB
-per step, far more than the 126 MB L2, so no flush is needed between steps.
+U[4097, 32769], Qwen3-8B attention shape, bf16, ~17 GB pool): it reads ~10.4 GB
+per step, far more than the 129 MB L2, so no flush is needed between steps.
 
 ``--impl reference`` times the CPU fp64 oracle instead (the baseline arm), on
 a bounded sample of the same workload, on the host cores.
