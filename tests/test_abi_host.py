@@ -247,3 +247,25 @@ def test_missing_library_fails_loudly(tmp_path, monkeypatch):
             ops.xs_paged_decode_num_splits(1, 8, 4097, 152)
     finally:
         ops.use_library(prev)
+
+
+def test_workspace_holder_sizes(lib):
+    # The binding's workspace holder (built on the host here: only sizes are
+    # checked) agrees with the library's sizing calls: partition length from
+    # the one-launch heuristic, partials for every partition a sequence of
+    # the table's width can need, and the step's counters.
+    import torch
+    B, Hq, Hkv, D, maxb = 64, 32, 8, 128, 475
+    ws = ops.DecodeWorkspace(B, Hq, Hkv, D, maxb, "cpu", total_context_tokens=63638,
+                             max_context_len=7598, num_sms=152)
+    assert ws.partition_tokens == ops.xs_paged_decode_step_partition_tokens(B, Hq, Hkv, 63638,
+                                                                            7598, 152)
+    mp = ops.xs_paged_decode_max_partitions(maxb, 16, ws.partition_tokens)
+    assert ws.max_partitions == mp
+    assert ws.part_o.numel() == B * Hq * mp * D and ws.part_m.numel() == B * Hq * mp
+    assert ws.part_o.dtype == torch.float32
+    assert ws.work.numel() == ops.xs_paged_decode_step_counters(B, Hkv) == 2 + B * Hkv
+    assert not bool(ws.work.any())
+    assert ws.partial_bytes <= ops.xs_paged_decode_workspace_bytes(B, Hq, D, mp)
+    one = ops.DecodeWorkspace(4, 32, 8, 128, 2, "cpu", partition_tokens=64, num_sms=152)
+    assert one.max_partitions == 1 and one.part_o is None and one.partial_bytes == 0
