@@ -10,6 +10,13 @@ default workload is the large-batch long-context one (128 sequences, contexts
 U[4097, 32769], Qwen3-8B attention shape, bf16, ~17 GB pool): it reads ~10.4 GB
 per step, far more than the 129 MB L2, so no flush is needed between steps.
 
+With the default workload the line also carries ``rows``: the other four
+decode workloads (tiny fp32 MHA, GPT-2 12 layers, Qwen3-8B single stream 36
+layers, the continuous-batching mix) and the 8K-token chunked prefill, each
+measured in the same process with its own timing, roofline, clocks and
+oracle parity (every sequence and layer for the decode rows).  Rows whose
+bytes fit twice in L2 are timed step by step with L2 flushed in between.
+
 ``--impl reference`` times the CPU fp64 oracle instead (the baseline arm), on
 a bounded sample of the same workload, on the host cores.
 """
@@ -334,52 +341,53 @@ def run_reference(args, rank, world, dist):
     print(json.dumps(line), flush=True)
 
 
-def run_ours(args, rank, world, local, dist):
-    from paged_kv_cache_xs_gb300 import build as xsbuild
-    from paged_kv_cache_xs_gb300 import ops
+L2_BYTES = 129 * 1024 * 1024  # L2 of one GB300
+
+
+def measure_decode(args, cfg: wl.DecodeConfig, rank, world, local, dist, *, steps: int,
+                   warmup: int, load_seconds: float, sinks_on: bool = False, window: int = 0,
+                   partition_tokens: int = 0, with_e2e: bool = True):
+    """Time exactly `steps` decode steps of workload `cfg` on this rank
+    (weak scaling: every rank its own seeded batch of the same shape) and
+    return what the JSON line reports: the slowest rank's time per step, the
+    per-launch time of the step kernel, clocks sampled under load, the
+    end-to-end time through host buffers (with_e2e) and the objects the
+    oracle leg needs (workload, outputs).  A step whose bytes are under twice
+    the L2 size is timed launch by launch with L2 flushed in between."""
     from paged_kv_cache_xs_gb300.step import CapturedStep, PagedDecodeStep
 
-    xsbuild.build()
-    ops.load()
     dev = torch.device(f"cuda:{local}")
-    torch.cuda.set_device(dev)
-    cfg = wl.CONFIGS[args.config]
-    # Weak scaling: every rank runs its own independent batch of the same shape.
     w = wl.make_workload(cfg, device=dev, seed=cfg.seed + 7919 * rank)
     L = cfg.layers
     sinks = None
-    if args.sinks:
+    if sinks_on:
         g = torch.Generator(device=dev).manual_seed(cfg.seed + 17)
         sinks = torch.randn(cfg.Hq, generator=g, device=dev).to(cfg.dtype)
     lens_cpu = w.context_lens.cpu()
-    win_tokens = int(lens_cpu.clamp(max=args.window).sum()) if args.window > 0 \
-        else w.total_context_tokens
+    win_tokens = int(lens_cpu.clamp(max=window).sum()) if window > 0 else w.total_context_tokens
+    fused = args.fused == "on"
     step = PagedDecodeStep(cfg.B, cfg.Hq, cfg.Hkv, cfg.D, w.max_blocks_per_seq, cfg.dtype, dev,
                            total_context_tokens=win_tokens,
-                           max_context_len=min(w.max_context_len, args.window or 1 << 30),
-                           partition_tokens=args.partition_tokens or None,
-                           sinks=sinks, window=args.window, fused=args.fused == "on")
+                           max_context_len=min(w.max_context_len, window or 1 << 30),
+                           partition_tokens=partition_tokens or None,
+                           sinks=sinks, window=window, fused=fused)
     out = torch.empty(L, cfg.B, cfg.Hq, cfg.D, dtype=cfg.dtype, device=dev)  # every layer's output
     stream = torch.cuda.current_stream()
-    by = step_bytes(cfg, lens_cpu, args.window)
+    by = step_bytes(cfg, lens_cpu, window)
     bytes_per_step = by["step"] * L
 
     # Early reads: each launch reads lengths, tables and its first pages while
     # the launch before it (the previous layer's, or the previous step's on
     # these same lengths) finishes; neither writes what is read early.
-    early = args.fused == "on" and args.early_reads == "on"
+    early = fused and args.early_reads == "on"
 
     def one_step(ev=None):
         cur = torch.cuda.current_stream()
         for layer in range(L):
-            if args.fused == "on":  # append + attention + combine: one launch
-                if ev is not None:
-                    ev[layer][0].record(cur)
+            if fused:  # append + attention + combine: one launch
                 step.run(out[layer], w.q[layer], w.k_new[layer], w.v_new[layer],
                          w.k_cache[layer], w.v_cache[layer], w.block_tables, w.context_lens,
                          w.scale, early_reads=early)
-                if ev is not None:
-                    ev[layer][1].record(cur)
                 continue
             step.append(w.k_new[layer], w.v_new[layer], w.k_cache[layer], w.v_cache[layer],
                         w.block_tables, w.context_lens)
@@ -391,7 +399,6 @@ def run_ours(args, rank, world, local, dist):
                 ev[layer][1].record(cur)
             step.reduce(out[layer], w.context_lens)
 
-    fused = args.fused == "on"
     # A multi-layer step replays as one CUDA graph (CapturedStep), its
     # launches chained by programmatic dependent launch; a one-layer step is
     # launched directly, where consecutive steps chain the same way.
@@ -416,46 +423,66 @@ def run_ours(args, rank, world, local, dist):
         else:
             one_step(ev)
 
+    # Inputs smaller than twice L2 could be served from L2 by the previous
+    # step: flush it (write a buffer larger than L2) before every timed step.
+    flush_buf = None
+    if bytes_per_step < 2 * L2_BYTES:
+        flush_buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.int32, device=dev)
+
     clocks = ClockSampler(local)
-    # Warm-up, then keep the GPU loaded for >= ~1 s so the clock sampler sees it.
-    for _ in range(args.warmup):
+    # Warm-up, then keep the GPU loaded for a while so the clock sampler sees it.
+    for _ in range(warmup):
         run_step()
     torch.cuda.synchronize()
     t_load = time.time()
-    while time.time() - t_load < args.load_seconds:
+    while time.time() - t_load < load_seconds:
         for _ in range(4):
             run_step()
         torch.cuda.synchronize()
 
-    # ---- timed region: exactly K steps
-    # Per-launch events only where the step has several kernels: the one-launch
-    # step's kernel time is the timed region over steps x layers launches.
+    # ---- timed region: exactly `steps` steps
     attn_ev = None if (graph is not None or fused) else [
         [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(L)]
-        for _ in range(args.steps)]
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for _ in range(steps)]
     barrier(dist)
     torch.cuda.synchronize()
-    start.record(stream)
-    for k in range(args.steps):
-        run_step(None if attn_ev is None else attn_ev[k])
-    end.record(stream)
-    torch.cuda.synchronize()
+    if flush_buf is None:
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for k in range(steps):
+            run_step(None if attn_ev is None else attn_ev[k])
+        end.record(stream)
+        torch.cuda.synchronize()
+        elapsed_ms = start.elapsed_time(end)
+    else:
+        step_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+        for k in range(steps):
+            flush_buf.fill_(k)
+            step_ev[k][0].record(stream)
+            run_step(None if attn_ev is None else attn_ev[k])
+            step_ev[k][1].record(stream)
+        torch.cuda.synchronize()
+        elapsed_ms = sum(a.elapsed_time(b) for a, b in step_ev)
     barrier(dist)
-    elapsed_ms = start.elapsed_time(end)
     if attn_ev is not None:
         attn_ms = [e[0].elapsed_time(e[1]) for ev in attn_ev for e in ev]
     elif graph_ev is not None:  # the last replay's attention launches
         attn_ms = [e[0].elapsed_time(e[1]) for e in graph_ev]
     else:
-        attn_ms = [elapsed_ms / (args.steps * L)]
+        attn_ms = [elapsed_ms / (steps * L)]
     clock_info = clocks.stop()
     assert step.error_flags() == 0, f"device error flags {step.error_flags()}"
+    del flush_buf
 
     max_ms = max_over_ranks(elapsed_ms, dist)
-    ms_per_step = max_ms / args.steps
-    value = world * bytes_per_step / (ms_per_step * 1e-3) / 1e9
-    seq_steps = world * cfg.B * L / (ms_per_step * 1e-3)
+    ms_per_step = max_ms / steps
+    res = dict(w=w, out=out, step=step, sinks=sinks, by=by, L=L, fused=fused, early=early,
+               graph=graph is not None, bytes_per_step=bytes_per_step, ms_per_step=ms_per_step,
+               value=world * bytes_per_step / (ms_per_step * 1e-3) / 1e9,
+               seq_steps=world * cfg.B * L / (ms_per_step * 1e-3), attn_ms=attn_ms,
+               clocks=clock_info, l2_flushed=flush_buf is not None, e2e=None)
+    if not with_e2e:
+        return res
 
     # ---- e2e: the same step fed from pinned host buffers: every step copies that
     # step's inputs (all layers' q and new K/V rows, block tables, lengths) to the
@@ -479,72 +506,168 @@ def run_ours(args, rank, world, local, dist):
     barrier(dist)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
-    for _ in range(args.steps):
+    for _ in range(steps):
         e2e_step()
-    e2e_s = max_over_ranks(time.perf_counter() - t0, dist) / args.steps
-    e2e_value = world * bytes_per_step / e2e_s / 1e9
+    e2e_s = max_over_ranks(time.perf_counter() - t0, dist) / steps
+    res["e2e"] = {"value": round(world * bytes_per_step / e2e_s / 1e9, 2), "unit": "GB/s",
+                  "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                  "ms_per_step": round(e2e_s * 1e3, 4)}
+    return res
 
-    if rank != 0:
-        return
+
+def decode_roofline(m: dict, traffic=None) -> dict:
+    """Roofline object of the step kernel: algorithmic bytes per launch over
+    the average launch time, against the measured HBM copy peak."""
     peak, peak_kind = hbm_peak()
-    attn_avg_ms = statistics.mean(attn_ms)
+    attn_avg_ms = statistics.mean(m["attn_ms"])
     # The fused launch also appends the new rows and writes the output.
-    launch_bytes = by["step"] if fused else by["attn"]
-    attn_gbs = launch_bytes / (attn_avg_ms * 1e-3) / 1e9
-    # The committed DRAM counters were taken on the one-launch step at the
-    # heuristic's partition, plain or with sinks and a window (a summary per
-    # variant); any other form of the launch reports none.
-    variant = (f"_sinks_w{args.window}" if sinks is not None else f"_w{args.window}") \
-        if (sinks is not None or args.window > 0) else ""
-    traffic = kernel_traffic(cfg.name, variant) if fused and not args.partition_tokens else None
-    line = {
-        "metric": METRIC,
-        "value": round(value, 2),
-        "unit": "GB/s",
-        "n_gpus": world,
-        "steps": args.steps,
-        "warmup": args.warmup,
-        "ms_per_step": round(ms_per_step, 4),
-        "higher_is_better": True,
-        "scaling": "weak",
-        "vs_baseline": None,
+    launch_bytes = m["by"]["step"] if m["fused"] else m["by"]["attn"]
+    gbs = launch_bytes / (attn_avg_ms * 1e-3) / 1e9
+    return {"kernel": "paged_decode_kernel", "bound": "hbm", "achieved": round(gbs, 1),
+            "peak": peak, "unit": "GB/s", "frac": round(gbs / peak, 4), "peak_kind": peak_kind,
+            "traffic": traffic, "algorithmic_bytes_per_launch": launch_bytes,
+            "avg_launch_ms": round(attn_avg_ms, 4)}
+
+
+def oracle_parity_all(w: wl.DecodeWorkload, out: torch.Tensor, sinks=None, window: int = 0):
+    """Every sequence of every layer of the timed output against the oracle
+    (append + fp64 attention from the same pools), on all host cores."""
+    threads = len(os.sched_getaffinity(0))
+    tol = 1e-2 if w.cfg.dtype == torch.bfloat16 else 1e-5
+    seqs = list(range(w.cfg.B))
+    worst = 0.0
+    for layer in range(w.cfg.layers):
+        ref = oracle_step(oracle_sample(w, seqs, layer), threads, sinks, window)
+        got = out[layer].cpu().double()
+        worst = max(worst, float((got - ref).abs().max()) if got.numel() else 0.0)
+    return {"max_abs_err": worst, "tolerance": tol, "ok": bool(worst <= tol),
+            "sequences": w.cfg.B, "layers": w.cfg.layers,
+            "reference": "fp64 CPU oracle, every sequence and layer of the timed output"}
+
+
+def decode_row(args, idx: int, rank, world, local, dist) -> dict:
+    """One workload measured in the same process as the headline line, for
+    its `rows` object: the same timing, roofline, clocks and oracle parity."""
+    cfg = wl.CONFIGS[idx]
+    m = measure_decode(args, cfg, rank, world, local, dist, steps=args.row_steps,
+                       warmup=args.warmup, load_seconds=args.row_load_seconds, with_e2e=False)
+    peak, peak_kind = hbm_peak()
+    row = {
+        "workload": cfg.name, "value": round(m["value"], 2), "unit": "GB/s",
+        "ms_per_step": round(m["ms_per_step"], 5), "steps": args.row_steps,
+        "seq_steps_per_s": round(m["seq_steps"], 1),
+        "pct_of_hbm_peak": {"of_measured": round(100 * m["value"] / world / peak, 2),
+                            "of_nominal_8TBps": round(100 * m["value"] / world / NOMINAL_HBM_GBS,
+                                                      2), "peak_kind": peak_kind},
+        "roofline": decode_roofline(m),
         "dtype": "bf16" if cfg.dtype == torch.bfloat16 else "f32",
-        "data": "synthetic (seeded; lengths, shuffled block order and N(0,1) values drawn "
-                "per the workload recipe)",
-        "config": {"workload": cfg.name, "B": cfg.B, "Hq": cfg.Hq, "Hkv": cfg.Hkv, "D": cfg.D,
-                   "block_size": cfg.block_size, "layers": L, "pool_blocks": w.num_blocks,
-                   "context_tokens": w.total_context_tokens,
-                   "max_context_len": w.max_context_len,
-                   "partition_tokens": step.partition_tokens,
-                   "sinks": bool(args.sinks), "window": args.window,
-                   "max_partitions": step.max_partitions,
-                   "l2": f"inputs larger than L2 ({bytes_per_step / 1e9:.2f} GB read per step)",
-                   "parallelism": f"replicas x{world} (independent batches, no collective)"},
-        "seq_steps_per_s": round(seq_steps, 1),
-        "pct_of_hbm_peak": {"of_measured": round(100 * value / world / peak, 2),
-                            "of_nominal_8TBps": round(100 * value / world / NOMINAL_HBM_GBS, 2),
-                            "peak_kind": peak_kind},
-        "roofline": {"kernel": "paged_decode_kernel", "bound": "hbm",
-                     "achieved": round(attn_gbs, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(attn_gbs / peak, 4), "peak_kind": peak_kind,
-                     "traffic": traffic,
-                     "algorithmic_bytes_per_launch": launch_bytes,
-                     "avg_launch_ms": round(attn_avg_ms, 4)},
-        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_s * 1e3, 4)},
-        "gpu_launches": args.steps * L * step.launches_per_step(fused),
-        "cuda_graph": graph is not None,
-        "fused_step": fused,
-        "early_reads": early,
-        "clocks": clock_info,
+        "config": {"B": cfg.B, "Hq": cfg.Hq, "Hkv": cfg.Hkv, "D": cfg.D, "layers": m["L"],
+                   "context_tokens": m["w"].total_context_tokens,
+                   "partition_tokens": m["step"].partition_tokens,
+                   "l2": ("flushed before every timed step (a write of twice the L2 size); "
+                          "each step timed by its own events") if m["l2_flushed"] else
+                         f"inputs larger than L2 ({m['bytes_per_step'] / 1e9:.3f} GB per step)"},
+        "gpu_launches": args.row_steps * m["L"] * m["step"].launches_per_step(m["fused"]),
+        "cuda_graph": m["graph"], "fused_step": m["fused"], "early_reads": m["early"],
+        "clocks": m["clocks"],
     }
-    if not args.no_cpu_baseline:
-        # The oracle of the step that ran (with sinks / a window: the gpt-oss
-        # variant's), timed on the host and compared with layer 0's output.
-        line["cpu_baseline"], parity = cpu_baseline(w, args.cpu_seconds, gpu_out=out[0],
-                                                    sinks=sinks, window=args.window)
-        line["parity"] = parity
-    print(json.dumps(line), flush=True)
+    if rank == 0 and not args.no_cpu_baseline:
+        row["parity"] = oracle_parity_all(m["w"], m["out"])
+    del m
+    torch.cuda.empty_cache()
+    return row
+
+
+def run_ours(args, rank, world, local, dist):
+    from paged_kv_cache_xs_gb300 import build as xsbuild
+    from paged_kv_cache_xs_gb300 import ops
+
+    xsbuild.build()
+    ops.load()
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    cfg = wl.CONFIGS[args.config]
+    m = measure_decode(args, cfg, rank, world, local, dist, steps=args.steps, warmup=args.warmup,
+                       load_seconds=args.load_seconds, sinks_on=args.sinks, window=args.window,
+                       partition_tokens=args.partition_tokens, with_e2e=True)
+    w, step, sinks, L = m["w"], m["step"], m["sinks"], m["L"]
+    fused, early = m["fused"], m["early"]
+    line = None
+    if rank == 0:
+        peak, peak_kind = hbm_peak()
+        value = m["value"]
+        # The committed DRAM counters were taken on the one-launch step at the
+        # heuristic's partition, plain or with sinks and a window (a summary per
+        # variant); any other form of the launch reports none.
+        variant = (f"_sinks_w{args.window}" if sinks is not None else f"_w{args.window}") \
+            if (sinks is not None or args.window > 0) else ""
+        traffic = kernel_traffic(cfg.name, variant) if fused and not args.partition_tokens \
+            else None
+        l2 = ("flushed before every timed step (a write of twice the L2 size); each step timed "
+              "by its own events") if m["l2_flushed"] else \
+            f"inputs larger than L2 ({m['bytes_per_step'] / 1e9:.2f} GB read per step)"
+        line = {
+            "metric": METRIC,
+            "value": round(value, 2),
+            "unit": "GB/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": round(m["ms_per_step"], 4),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "bf16" if cfg.dtype == torch.bfloat16 else "f32",
+            "data": "synthetic (seeded; lengths, shuffled block order and N(0,1) values drawn "
+                    "per the workload recipe)",
+            "config": {"workload": cfg.name, "B": cfg.B, "Hq": cfg.Hq, "Hkv": cfg.Hkv,
+                       "D": cfg.D, "block_size": cfg.block_size, "layers": L,
+                       "pool_blocks": w.num_blocks, "context_tokens": w.total_context_tokens,
+                       "max_context_len": w.max_context_len,
+                       "partition_tokens": step.partition_tokens,
+                       "sinks": bool(args.sinks), "window": args.window,
+                       "max_partitions": step.max_partitions, "l2": l2,
+                       "parallelism": f"replicas x{world} (independent batches, no collective)"},
+            "seq_steps_per_s": round(m["seq_steps"], 1),
+            "pct_of_hbm_peak": {"of_measured": round(100 * value / world / peak, 2),
+                                "of_nominal_8TBps": round(100 * value / world / NOMINAL_HBM_GBS,
+                                                          2),
+                                "peak_kind": peak_kind},
+            "roofline": decode_roofline(m, traffic),
+            "e2e": m["e2e"],
+            "gpu_launches": args.steps * L * step.launches_per_step(fused),
+            "cuda_graph": m["graph"],
+            "fused_step": fused,
+            "early_reads": early,
+            "clocks": m["clocks"],
+        }
+        if not args.no_cpu_baseline:
+            # The oracle of the step that ran (with sinks / a window: the gpt-oss
+            # variant's), timed on the host and compared with layer 0's output.
+            line["cpu_baseline"], parity = cpu_baseline(w, args.cpu_seconds, gpu_out=m["out"][0],
+                                                        sinks=sinks, window=args.window)
+            line["parity"] = parity
+    # The other workloads (and the chunked prefill) measured in this same
+    # process, each with its own timing, roofline, clocks and oracle parity.
+    want_rows = args.rows == "on" or (args.rows == "auto" and args.config == 4 and
+                                      not args.sinks and args.window == 0 and
+                                      not args.partition_tokens)
+    if want_rows:
+        del m, w, step
+        torch.cuda.empty_cache()
+        rows = {}
+        for idx in (0, 1, 2, 3):
+            row = decode_row(args, idx, rank, world, local, dist)
+            rows[row["workload"]] = row
+        pre = prefill_measure(args, rank, world, local, dist, tokens=8192, chunk=1024,
+                              steps=args.row_steps, load_seconds=args.row_load_seconds,
+                              cpu_seconds=args.row_cpu_seconds)
+        if pre is not None:
+            rows[pre["config"]["workload"]] = pre
+        if line is not None:
+            line["rows"] = rows
+    if line is not None:
+        print(json.dumps(line), flush=True)
 
 
 def run_swap(args, rank, world, local, dist):
@@ -776,11 +899,25 @@ def run_prefill(args, rank, world, local, dist):
 
     xsbuild.build()
     ops.load()
+    torch.cuda.set_device(torch.device(f"cuda:{local}"))
+    line = prefill_measure(args, rank, world, local, dist, tokens=args.prefill_tokens,
+                           chunk=args.prefill_chunk, steps=args.steps,
+                           load_seconds=args.load_seconds, cpu_seconds=args.cpu_seconds,
+                           impl=args.prefill_impl)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+def prefill_measure(args, rank, world, local, dist, *, tokens: int, chunk: int, steps: int,
+                    load_seconds: float, cpu_seconds: float, impl: str = "tensor"):
+    """Time `steps` prefills of one Qwen3-8B-shaped sequence of `tokens`
+    tokens in `chunk`-token chunks; returns the line (rank 0) or None."""
+    from paged_kv_cache_xs_gb300 import ops
+
     dev = torch.device(f"cuda:{local}")
-    torch.cuda.set_device(dev)
     Hq, Hkv, D, bs = 32, 8, 128, 16
     dtype = torch.bfloat16
-    total, chunk = args.prefill_tokens, args.prefill_chunk
+    total = tokens
     pages = (total + bs - 1) // bs
     g = torch.Generator(device=dev).manual_seed(2000 + rank)
     ids = torch.randperm(pages * 2, generator=g, device=dev)[:pages].to(torch.int32)
@@ -790,7 +927,7 @@ def run_prefill(args, rank, world, local, dist):
     vs = torch.randn(Hkv, total, D, generator=g, device=dev).to(dtype)
     q = torch.randn(total, Hq, D, generator=g, device=dev).to(dtype)
     wss = {}
-    tensor = args.prefill_impl == "tensor"
+    tensor = impl == "tensor"
     nchunks = (total + chunk - 1) // chunk
     ks_c = [ks[:, s0:s0 + chunk].contiguous() for s0 in range(0, total, chunk)]
     vs_c = [vs[:, s0:s0 + chunk].contiguous() for s0 in range(0, total, chunk)]
@@ -823,26 +960,32 @@ def run_prefill(args, rank, world, local, dist):
         prefill_all()
     torch.cuda.synchronize()
     t_load = time.time()
-    while time.time() - t_load < args.load_seconds:  # >= ~1 s under load for the clock sampler
+    while time.time() - t_load < load_seconds:  # >= ~1 s under load for the clock sampler
         prefill_all()
         torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # The sequence's pages fit in L2: flush it (write a buffer twice its
+    # size) before every timed prefill, each timed by its own events.
+    flush_buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.int32, device=dev)
+    step_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
     barrier(dist)
     torch.cuda.synchronize()
-    e0.record()
-    for _ in range(args.steps):
+    for k in range(steps):
+        flush_buf.fill_(k)
+        step_ev[k][0].record()
         prefill_all()
-    e1.record()
+        step_ev[k][1].record()
     torch.cuda.synchronize()
-    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, dist)  # slowest rank
+    ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in step_ev) / steps, dist)  # slowest rank
     clock_info = clocks.stop()
     # The attention launches alone, bracketed by events (one more pass).
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(nchunks)]
+    flush_buf.fill_(-1)
     prefill_all(ev)
     torch.cuda.synchronize()
     attn_ms = sum(a.elapsed_time(b) for a, b in ev)
+    del flush_buf
     if rank != 0:
-        return
+        return None
     # Causal attention flops: 4 * D per (query head, query token, key) pair.
     pairs = total * (total + 1) / 2
     flop = 4 * D * Hq * pairs
@@ -863,20 +1006,22 @@ def run_prefill(args, rank, world, local, dist):
     line = {
         "metric": "chunked prefill attention over the paged cache (tokens/s, TFLOP/s)",
         "value": round(world * total / (ms * 1e-3), 1), "unit": "tokens/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "steps": steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": "qwen3_8b_prefill", "tokens": total, "chunk": chunk, "Hq": Hq,
-                   "Hkv": Hkv, "D": D, "impl": args.prefill_impl},
+        "config": {"workload": f"qwen3_8b_prefill_{total}_chunk{chunk}", "tokens": total,
+                   "chunk": chunk, "Hq": Hq, "Hkv": Hkv, "D": D, "impl": impl,
+                   "l2": "flushed before every timed prefill (a write of twice the L2 "
+                         "size); each prefill timed by its own events"},
         "attention_tflops": round(tflops, 2),
         "roofline": roof,
-        "gpu_launches": args.steps * nchunks * (2 if tensor else 3),
+        "gpu_launches": steps * nchunks * (2 if tensor else 3),
         "clocks": clock_info,
     }
     if not args.no_cpu_baseline:
         line["cpu_baseline"], line["parity"] = prefill_cpu_baseline(
-            q, kc, vc, ids, out, total, flop, args.cpu_seconds)
-    print(json.dumps(line), flush=True)
+            q, kc, vc, ids, out, total, flop, cpu_seconds)
+    return line
 
 
 def prefill_cpu_baseline(q, kc, vc, ids, out, total: int, total_flop: float, target_s: float):
@@ -953,6 +1098,16 @@ def main(argv=None):
                     help="target duration of one reference-arm step")
     ap.add_argument("--load-seconds", type=float, default=1.0,
                     help="untimed load before the timed region (clock sampling)")
+    ap.add_argument("--rows", choices=["auto", "on", "off"], default="auto",
+                    help="also measure workloads 0-3 and the 8K/1K chunked prefill in the same "
+                         "process and report them under 'rows' (auto: with the default "
+                         "long-batch decode line)")
+    ap.add_argument("--row-steps", type=int, default=20,
+                    help="timed steps of each extra row")
+    ap.add_argument("--row-load-seconds", type=float, default=0.4,
+                    help="untimed load before each extra row's timed region")
+    ap.add_argument("--row-cpu-seconds", type=float, default=3.0,
+                    help="target duration of the prefill row's oracle sample")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)  # at least 3 untimed warm-up steps
     rank, world, local, dist = dist_setup(args.gpus)

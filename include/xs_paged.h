@@ -530,10 +530,12 @@ int64_t xs_paged_decode_step_counters(int B, int Hkv);
  * The partials live in one array that the library defines at file scope in
  * device memory, XS_NOALLOC_SCRATCH_BYTES (64 MiB) in size.  Every GPU that
  * loads the library reserves that array until the process exits.  The call
- * allocates nothing: it looks the array's device address up with
- * cudaGetSymbolAddress the first time it runs on a device (with that device
- * current) and caches it, so make that first call on each device before any
- * stream capture.
+ * allocates nothing: on every call it looks up the array's device address for
+ * the current device and context with cudaGetSymbolAddress (nothing is
+ * cached, so a cudaDeviceReset or another current context cannot leave a
+ * stale address).  The first call on a device may load the library's device
+ * code there (lazy module loading), so make that first call on each device -
+ * any call that passes the argument checks - before any stream capture.
  *
  * Arguments as xs_paged_decode, without part_o/part_m/part_l and
  * max_partitions (derived as xs_paged_decode_max_partitions(
@@ -579,6 +581,27 @@ int xs_version(void);
  * failed.
  */
 int xs_debug_bounds_failures(int reset);
+
+/*
+ * xs_debug_wait_injection - in the debug library only, a way to make the
+ * decode kernel's bounded waits run out on purpose, so the recovery path can
+ * be exercised without a device fault.  The paper has no counterpart of this
+ * entry point: it is a test aid.
+ *
+ * wait_limit_ns (> 0) becomes the limit of every bounded wait of the decode
+ * kernel (default 4e9, i.e. 4 s).  skip_page >= 0 makes CTA 0's producer skip
+ * issuing the copies of its page number skip_page (its pages counted from 0
+ * in the order it issues them) in every later launch: nothing is in flight
+ * for that page, the consumer's wait for it runs out, the launch raises
+ * XS_FLAG_TIMEOUT, drains the copies it did issue and returns; -1 issues
+ * every page.  Both settings hold on the current device until changed.
+ * After a launch that raised XS_FLAG_TIMEOUT the outputs of the affected
+ * sequences are unspecified and the step's counters must be zeroed (see
+ * xs_paged_decode_step).  Synchronous.  Returns XS_OK, XS_ESHAPE
+ * (wait_limit_ns <= 0 or skip_page < -1), XS_EDEVICE if the copy failed, and
+ * XS_EUNSUPPORTED in the release library.
+ */
+int xs_debug_wait_injection(int64_t wait_limit_ns, int skip_page);
 
 #ifdef __cplusplus
 }

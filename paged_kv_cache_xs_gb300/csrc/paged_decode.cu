@@ -61,6 +61,23 @@ constexpr int kMaxBatch = 8192;                   // per-sequence tables live in
 constexpr int kClaimAhead = 8;  // pages of the current item left to issue when the next is claimed
 constexpr int kL2Ahead = 16;    // pages of the first item prefetched into L2 before the launch wait
 
+// Limit of every bounded wait.  The debug library (XS_DEBUG_BOUNDS) makes it
+// settable, and can make CTA 0's producer skip issuing the copies of one of
+// its pages (xs_debug_wait_injection), so a test can make a consumer's wait
+// for that page run out: nothing is in flight for the skipped page, so the
+// abort path (flag, drain, return) runs with every copy accounted for.
+#ifdef XS_DEBUG_BOUNDS
+__device__ unsigned long long g_wait_limit_ns = kWaitLimitNs;
+__device__ int g_skip_page = -1;  // CTA 0's page counter value whose copies are not issued
+__device__ __forceinline__ uint64_t wait_limit() { return g_wait_limit_ns; }
+__device__ __forceinline__ bool skip_page(uint32_t c) {
+    return blockIdx.x == 0 && static_cast<int>(c) == g_skip_page;
+}
+#else
+__device__ __forceinline__ constexpr uint64_t wait_limit() { return kWaitLimitNs; }
+__device__ __forceinline__ constexpr bool skip_page(uint32_t) { return false; }
+#endif
+
 // Per-sequence tables a CTA keeps in shared memory: pfull[B + 1], ptail[B + 1]
 // (item numbering) and nlen[B] (clamped context lengths).
 __host__ __device__ constexpr int table_bytes(int B) { return 4 * (3 * B + 2); }
@@ -495,13 +512,13 @@ __device__ __noinline__ bool combine_partials(const Params &p, const Item &it, i
             for (int d = 0; d < kDims; ++d) acc[h][d] *= corr;
         }
         const bool landed =
-            __all_sync(0xffffffffu, mbar_wait_bounded(&stage->bar, phase, kWaitLimitNs));
+            __all_sync(0xffffffffu, mbar_wait_bounded(&stage->bar, phase, wait_limit()));
         __syncwarp();
         if (lane == 0) stage->phase = phase ^ 1u;
         if (!landed) {
             // The caller flags it; first give the copies in flight (bounded)
             // time to land, so none writes into this CTA's memory after it exits.
-            if (lane == 0) mbar_wait_bounded(&stage->bar, phase, kWaitLimitNs);
+            if (lane == 0) mbar_wait_bounded(&stage->bar, phase, wait_limit());
             __syncwarp();
             return false;
         }
@@ -718,6 +735,9 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
     int *ptail = pfull + p.B + 1;
     int *nlen = ptail + p.B + 1;
     __shared__ int s_abort;
+    // Completes when the consumers and the merger have finished (static, so
+    // no register holds its address through the roles' loops).
+    __shared__ uint64_t roles_done;
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
@@ -744,6 +764,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
             mbar_init(&merged[s], kConsumerWarps);
             mbar_init(&freed[s], 1);
         }
+        mbar_init(&roles_done, kConsumerWarps + 1);
         if (p.combine) {
             Stage *st = reinterpret_cast<Stage *>(smem + stage_offset(C::kPrefixOff, p.B));
             mbar_init(&st->bar, 1);
@@ -953,7 +974,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
             bool ok = true;
             if (lane == 0) {
                 const uint32_t slot = item_ctr & 1, k = item_ctr >> 1;
-                ok = mbar_wait_bounded(&qempty[slot], (k & 1) ^ 1, kWaitLimitNs);
+                ok = mbar_wait_bounded(&qempty[slot], (k & 1) ^ 1, wait_limit());
                 if (ok) {
                     item_slot[slot] = it;
                     if (it.b < 0 || !XS_BOUNDS(it.b < p.B && it.g >= 0 && (it.g + 1) * G <= p.Hq,
@@ -1002,11 +1023,11 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
                     bool w = true;
                     if (lane == 0)
                         w = mbar_wait_bounded(&empty[page_ctr % kStages],
-                                              ((page_ctr / kStages) & 1) ^ 1, kWaitLimitNs);
+                                              ((page_ctr / kStages) & 1) ^ 1, wait_limit());
                     if (!__shfl_sync(0xffffffffu, w, 0)) return false;
                     continue;
                 }
-                if (lane < n) {
+                if (lane < n && !skip_page(c)) {  // (a skipped page: debug library only)
                     unsigned char *dk = smem + st * 2 * C::kPageBytes;
                     mbar_arrive_expect_tx(&full[st], 2 * C::kPageBytes);
                     if constexpr (C::kMma) {
@@ -1094,10 +1115,22 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
             if (!ok) {
                 raise_flag(p.err_flag, XS_FLAG_TIMEOUT);
                 atomicExch(&s_abort, 1);
-                // Drain: let every copy this CTA issued land before the CTA exits.
+            }
+            // Whether any warp aborted is known once the consumers and the
+            // merger have finished (bounded, like every wait here).
+            mbar_wait_bounded(&roles_done, 0, wait_limit());
+            if (!ok || *static_cast<volatile int *>(&s_abort)) {
+                // Drain: after an abort (here or in another warp) consumers may
+                // leave without waiting for their pages, so let every copy this
+                // CTA issued land before it exits.  Only the last kStages pages
+                // can be in flight (an older page's stage was reissued, which
+                // took its consumer's release after the page landed), and only
+                // the last two q slots.
                 const uint32_t first = page_ctr > kStages ? page_ctr - kStages : 0;
                 for (uint32_t c = first; c < page_ctr; ++c)
-                    mbar_wait_bounded(&full[c % kStages], (c / kStages) & 1, kWaitLimitNs);
+                    mbar_wait_bounded(&full[c % kStages], (c / kStages) & 1, wait_limit());
+                for (uint32_t k = item_ctr > 2 ? item_ctr - 2 : 0; k < item_ctr; ++k)
+                    mbar_wait_bounded(&qfull[k & 1], (k >> 1) & 1, wait_limit());
             }
             if (p.work) {
                 // The last CTA to stop taking items resets the counters for the
@@ -1143,7 +1176,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
             const uint32_t mpar = (item_ctr / C::kMergeBufs) & 1;
             if (npend > 0 && !__shfl_sync(0xffffffffu, mbar_test_wait(&merged[buf], mpar), 0))
                 flush();  // idle until the next item: count the queued ones now
-            if (!mbar_wait_bounded(&merged[buf], mpar, kWaitLimitNs)) {
+            if (!mbar_wait_bounded(&merged[buf], mpar, wait_limit())) {
                 if (lane == 0) {
                     raise_flag(p.err_flag, XS_FLAG_TIMEOUT);
                     atomicExch(&s_abort, 1);
@@ -1220,6 +1253,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
             }
         }
         if (!*static_cast<volatile int *>(&s_abort)) flush();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&roles_done);
         return;
     }
 
@@ -1235,7 +1270,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
         for (uint32_t item_ctr = 0;; ++item_ctr) {
             const uint32_t slot = item_ctr & 1;
             bool bad = !__all_sync(0xffffffffu, mbar_wait_bounded(&qfull[slot], (item_ctr >> 1) & 1,
-                                                                  kWaitLimitNs));
+                                                                  wait_limit()));
             Item it = item_slot[slot];
             const bool done = !bad && it.b < 0;
             uint32_t qa[D / 16][2];
@@ -1265,7 +1300,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
             for (int pg = it.pg0 + first; pg < it.pg1; pg += kConsumerWarps) {
                 const uint32_t c = page_ctr + (pg - it.pg0);
                 const uint32_t s = c % kStages, k = c / kStages;
-                if (!__all_sync(0xffffffffu, mbar_wait_bounded(&full[s], k & 1, kWaitLimitNs)) ||
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(&full[s], k & 1, wait_limit())) ||
                     *static_cast<volatile int *>(&s_abort)) {
                     bad = true;
                     break;
@@ -1291,7 +1326,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
             unsigned char *mb = smem + C::kCombOff + buf * C::kCombBytes;
             if (!__all_sync(0xffffffffu, mbar_wait_bounded(&freed[buf],
                                                            ((item_ctr / C::kMergeBufs) & 1) ^ 1,
-                                                           kWaitLimitNs))) {
+                                                           wait_limit()))) {
                 if (lane == 0) {
                     raise_flag(p.err_flag, XS_FLAG_TIMEOUT);
                     atomicExch(&s_abort, 1);
@@ -1330,7 +1365,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
             // All waits in the CTA are bounded, so no warp can wait forever.
             const uint32_t slot = item_ctr & 1;
             bool bad = !__all_sync(0xffffffffu,
-                                   mbar_wait_bounded(&qfull[slot], (item_ctr >> 1) & 1, kWaitLimitNs));
+                                   mbar_wait_bounded(&qfull[slot], (item_ctr >> 1) & 1, wait_limit()));
             Item it = item_slot[slot];
             const bool done = !bad && it.b < 0;
             float qf[G][C::kQkDims];
@@ -1370,7 +1405,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
             for (int pg = it.pg0 + first; pg < it.pg1; pg += kConsumerWarps) {
                 const uint32_t c = page_ctr + (pg - it.pg0);
                 const uint32_t s = c % kStages, k = c / kStages;
-                if (!__all_sync(0xffffffffu, mbar_wait_bounded(&full[s], k & 1, kWaitLimitNs)) ||
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(&full[s], k & 1, wait_limit())) ||
                     *static_cast<volatile int *>(&s_abort)) {
                     bad = true;
                     break;
@@ -1397,7 +1432,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
             unsigned char *mb = smem + C::kCombOff + buf * C::kCombBytes;
             if (!__all_sync(0xffffffffu, mbar_wait_bounded(&freed[buf],
                                                            ((item_ctr / C::kMergeBufs) & 1) ^ 1,
-                                                           kWaitLimitNs))) {
+                                                           wait_limit()))) {
                 if (lane == 0) {
                     raise_flag(p.err_flag, XS_FLAG_TIMEOUT);
                     atomicExch(&s_abort, 1);
@@ -1429,6 +1464,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
             if (done || *static_cast<volatile int *>(&s_abort)) break;
         }
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&roles_done);
 }
 
 // Split-K combine: one CTA of D threads per (sequence, query head).
@@ -1650,6 +1687,23 @@ extern "C" int xs_debug_bounds_failures(int reset) {
     return total;
 #else
     (void)reset;
+    return XS_EUNSUPPORTED;
+#endif
+}
+
+extern "C" int xs_debug_wait_injection(int64_t wait_limit_ns, int skip_page) {
+#ifdef XS_DEBUG_BOUNDS
+    if (wait_limit_ns <= 0 || skip_page < -1) return XS_ESHAPE;
+    const unsigned long long limit = static_cast<unsigned long long>(wait_limit_ns);
+    if (cudaMemcpyToSymbol(attn::g_wait_limit_ns, &limit, sizeof(limit)) != cudaSuccess ||
+        cudaMemcpyToSymbol(attn::g_skip_page, &skip_page, sizeof(skip_page)) != cudaSuccess) {
+        cudaGetLastError();
+        return XS_EDEVICE;
+    }
+    return XS_OK;
+#else
+    (void)wait_limit_ns;
+    (void)skip_page;
     return XS_EUNSUPPORTED;
 #endif
 }
@@ -2072,24 +2126,20 @@ extern "C" int xs_paged_prefill(void *out, float *part_o, float *part_m, float *
 // Split-K partials for callers that cannot allocate device memory: a fixed
 // array of XS_NOALLOC_SCRATCH_BYTES at file scope, reserved on every device
 // that loads this library.  Host code must not use the symbol itself as a
-// pointer (in host code it names a host-side stand-in), so its device
-// address is looked up once per device with cudaGetSymbolAddress and cached.
+// pointer (in host code it names a host-side stand-in), so every call looks
+// up the array's device address for the current device and context with
+// cudaGetSymbolAddress.  Nothing is cached: a cached address could outlive
+// its context (cudaDeviceReset, or another context made current).
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[XS_NOALLOC_SCRATCH_BYTES];
 
 static int noalloc_scratch(unsigned char **out) {
-    static std::mutex mu;
-    static unsigned char *cache[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return XS_EDEVICE;
-    std::lock_guard<std::mutex> lock(mu);
-    if (cache[dev] == nullptr) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
-            return XS_EDEVICE;
-        cache[dev] = static_cast<unsigned char *>(p);
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+        cudaGetLastError();  // do not leave the failure for an unrelated later check
+        return XS_EDEVICE;
     }
-    *out = cache[dev];
+    *out = static_cast<unsigned char *>(p);
     return XS_OK;
 }
 
@@ -2113,22 +2163,26 @@ extern "C" int xs_paged_decode_noalloc(void *out, const void *q, const void *k_c
     const int max_parts =
         xs_paged_decode_max_partitions(max_blocks_per_seq, block_size, partition_tokens);
     if (max_parts < 0) return max_parts;
-    float *po = nullptr, *pm = nullptr, *pl = nullptr;
-    if (max_parts > 1 && B > 0) {
-        const size_t need = xs_paged_decode_workspace_bytes(B, Hq, D, max_parts);
+    const bool split = max_parts > 1 && B > 0;
+    size_t need = 0;
+    if (split) {
+        need = xs_paged_decode_workspace_bytes(B, Hq, D, max_parts);
         if (need == 0) return XS_ESHAPE;
         if (need > XS_NOALLOC_SCRATCH_BYTES) return XS_ESCRATCH;
-        // Validate everything else before touching the device.
-        const int st = check_attn_args(out, reinterpret_cast<float *>(256),
-                                       reinterpret_cast<float *>(256),
-                                       reinterpret_cast<float *>(256), q, k_cache, v_cache,
-                                       block_tables, max_blocks_per_seq, context_lens, B, Hq, Hkv,
-                                       D, block_size, num_blocks, partition_tokens, max_parts,
-                                       dtype);
-        if (st != XS_OK) return st;
-        unsigned char *base = nullptr;
-        const int sst = noalloc_scratch(&base);
-        if (sst != XS_OK) return sst;
+    }
+    // Validate everything else before touching the device (the partial
+    // pointers stand in for the array's aligned address).
+    float *const stand_in = reinterpret_cast<float *>(256);
+    int st = check_attn_args(out, stand_in, stand_in, stand_in, q, k_cache, v_cache, block_tables,
+                             max_blocks_per_seq, context_lens, B, Hq, Hkv, D, block_size,
+                             num_blocks, partition_tokens, max_parts, dtype);
+    if (st != XS_OK) return st;
+    // The array's address on the current device, looked up on every call
+    // (the first call on a device may load the library's device code).
+    unsigned char *base = nullptr;
+    if ((st = noalloc_scratch(&base)) != XS_OK) return st;
+    float *po = nullptr, *pm = nullptr, *pl = nullptr;
+    if (split) {
         const size_t n = static_cast<size_t>(B) * Hq * max_parts;
         const size_t o_bytes = (n * D * 4 + 255) / 256 * 256;
         const size_t ml_bytes = (n * 4 + 255) / 256 * 256;

@@ -72,6 +72,7 @@ SIGNATURES = {
     "xs_paged_decode_step_partition_tokens": (_I, [_I, _I, _I, _L, _I, _I]),
     "xs_version": (_I, []),
     "xs_debug_bounds_failures": (_I, [_I]),
+    "xs_debug_wait_injection": (_I, [_L, _I]),
 }
 
 _lock = threading.Lock()
@@ -387,6 +388,15 @@ def xs_debug_bounds_failures(reset: bool = False, lib=None) -> int:
     """Failed in-kernel bounds checks on the current device (debug library
     only; the release library returns XS_EUNSUPPORTED)."""
     return (lib or load()).xs_debug_bounds_failures(int(bool(reset)))
+
+
+def xs_debug_wait_injection(wait_limit_ns: int, skip_page: int = -1, lib=None) -> None:
+    """Debug library only: set the decode kernel's wait limit and make CTA
+    0's producer skip issuing one page (-1: none); see the header."""
+    lib = lib or load()
+    code = lib.xs_debug_wait_injection(int(wait_limit_ns), int(skip_page))
+    if code != 0:
+        raise XsError("xs_debug_wait_injection", code)
 
 
 def load_debug():

@@ -269,3 +269,13 @@ def test_workspace_holder_sizes(lib):
     assert ws.partial_bytes <= ops.xs_paged_decode_workspace_bytes(B, Hq, D, mp)
     one = ops.DecodeWorkspace(4, 32, 8, 128, 2, "cpu", partition_tokens=64, num_sms=152)
     assert one.max_partitions == 1 and one.part_o is None and one.partial_bytes == 0
+
+
+def test_wait_injection_is_debug_only(lib):
+    # The release library refuses the debug-only wait injection without
+    # touching the device; the debug library checks its arguments first.
+    assert lib.xs_debug_wait_injection(1_000_000, 2) == -5       # XS_EUNSUPPORTED
+    xsbuild.build(debug_bounds=True)
+    dbg = ops.load_debug()
+    assert dbg.xs_debug_wait_injection(0, -1) == -2              # XS_ESHAPE: no limit
+    assert dbg.xs_debug_wait_injection(1_000_000, -2) == -2      # XS_ESHAPE: bad page

@@ -143,3 +143,19 @@ def test_reference_arm_under_torchrun_two_ranks():
     assert len(lines) == 1, r.stdout
     line = json.loads(lines[0])
     assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
+
+
+def test_decode_row_parity_covers_every_sequence_and_layer():
+    # The rows' oracle leg: every sequence of every layer of the timed output
+    # against the oracle.  Here the "GPU output" is the oracle's own, rounded
+    # to bf16 (within tolerance); one element off in the last layer is caught.
+    cfg = wl.custom_config(3, 8, 2, 64, torch.bfloat16, layers=2, history=("uniform", (1, 60)),
+                           seed=9)
+    w = wl.make_workload(cfg, device="cpu")
+    out = torch.stack([bench.oracle_step(bench.oracle_sample(w, [0, 1, 2], layer), 1)
+                       for layer in range(2)]).to(torch.bfloat16)
+    par = bench.oracle_parity_all(w, out)
+    assert par["ok"] and par["layers"] == 2 and par["sequences"] == 3
+    assert par["max_abs_err"] <= 1e-2
+    out[1, 2, 3, 4] += 0.5
+    assert not bench.oracle_parity_all(w, out)["ok"]
