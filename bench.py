@@ -15,7 +15,7 @@ decode workloads (tiny fp32 MHA, GPT-2 12 layers, Qwen3-8B single stream 36
 layers, the continuous-batching mix) and the 8K-token chunked prefill, each
 measured in the same process with its own timing, roofline, clocks and
 oracle parity (every sequence and layer for the decode rows).  Rows whose
-bytes fit twice in L2 are timed step by step with L2 flushed in between.
+bytes fit in L2 are timed step by step with L2 flushed in between.
 
 ``--impl reference`` times the CPU fp64 oracle instead (the baseline arm), on
 a bounded sample of the same workload, on the host cores.
@@ -352,8 +352,8 @@ def measure_decode(args, cfg: wl.DecodeConfig, rank, world, local, dist, *, step
     return what the JSON line reports: the slowest rank's time per step, the
     per-launch time of the step kernel, clocks sampled under load, the
     end-to-end time through host buffers (with_e2e) and the objects the
-    oracle leg needs (workload, outputs).  A step whose bytes are under twice
-    the L2 size is timed launch by launch with L2 flushed in between."""
+    oracle leg needs (workload, outputs).  A step whose bytes are under the
+    L2 size is timed step by step with L2 flushed in between."""
     from paged_kv_cache_xs_gb300.step import CapturedStep, PagedDecodeStep
 
     dev = torch.device(f"cuda:{local}")
@@ -423,10 +423,10 @@ def measure_decode(args, cfg: wl.DecodeConfig, rank, world, local, dist, *, step
         else:
             one_step(ev)
 
-    # Inputs smaller than twice L2 could be served from L2 by the previous
-    # step: flush it (write a buffer larger than L2) before every timed step.
+    # Inputs smaller than L2 could be served from it by the previous step:
+    # flush it (write a buffer twice its size) before every timed step.
     flush_buf = None
-    if bytes_per_step < 2 * L2_BYTES:
+    if bytes_per_step < L2_BYTES:
         flush_buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.int32, device=dev)
 
     clocks = ClockSampler(local)
@@ -472,6 +472,7 @@ def measure_decode(args, cfg: wl.DecodeConfig, rank, world, local, dist, *, step
         attn_ms = [elapsed_ms / (steps * L)]
     clock_info = clocks.stop()
     assert step.error_flags() == 0, f"device error flags {step.error_flags()}"
+    l2_flushed = flush_buf is not None
     del flush_buf
 
     max_ms = max_over_ranks(elapsed_ms, dist)
@@ -480,7 +481,7 @@ def measure_decode(args, cfg: wl.DecodeConfig, rank, world, local, dist, *, step
                graph=graph is not None, bytes_per_step=bytes_per_step, ms_per_step=ms_per_step,
                value=world * bytes_per_step / (ms_per_step * 1e-3) / 1e9,
                seq_steps=world * cfg.B * L / (ms_per_step * 1e-3), attn_ms=attn_ms,
-               clocks=clock_info, l2_flushed=flush_buf is not None, e2e=None)
+               clocks=clock_info, l2_flushed=l2_flushed, e2e=None)
     if not with_e2e:
         return res
 

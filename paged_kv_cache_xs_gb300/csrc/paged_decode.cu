@@ -735,9 +735,10 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
     int *ptail = pfull + p.B + 1;
     int *nlen = ptail + p.B + 1;
     __shared__ int s_abort;
-    // Completes when the consumers and the merger have finished (static, so
-    // no register holds its address through the roles' loops).
-    __shared__ uint64_t roles_done;
+    // Role warps still running, and the producer's page and item counts:
+    // the last warp to finish drains the copies after an abort (exit_role).
+    __shared__ int s_roles_left;
+    __shared__ uint32_t s_issued[2];
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
@@ -764,7 +765,6 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
             mbar_init(&merged[s], kConsumerWarps);
             mbar_init(&freed[s], 1);
         }
-        mbar_init(&roles_done, kConsumerWarps + 1);
         if (p.combine) {
             Stage *st = reinterpret_cast<Stage *>(smem + stage_offset(C::kPrefixOff, p.B));
             mbar_init(&st->bar, 1);
@@ -772,6 +772,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
         }
         mbar_fence_init();
         s_abort = 0;
+        s_roles_left = kConsumerWarps + 2;
+        s_issued[0] = s_issued[1] = 0;
     }
     // Programmatic dependent launch.  griddep_wait returns once the previous
     // launch on the stream has completed and its writes are visible; only
@@ -839,6 +841,26 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
     }
     __syncthreads();
     const int total_items = pfull[p.B] + ptail[p.B];
+    // Every role warp calls this once, as its last action.  After an abort
+    // (a bounded wait that ran out, in any warp) consumers may have left
+    // without waiting for pages already requested, so the last warp to
+    // finish lets every copy the producer issued land before the CTA exits:
+    // only the last kStages pages can be in flight (an older page's stage
+    // was reissued, which took its consumer's release after the page
+    // landed), and only the last two q slots.  Nothing waits otherwise.
+    auto exit_role = [&]() {
+        __syncwarp();
+        if (lane != 0) return;
+        __threadfence_block();
+        if (atomicSub(&s_roles_left, 1) != 1) return;
+        __threadfence_block();
+        if (!*static_cast<volatile int *>(&s_abort)) return;
+        const uint32_t pages = s_issued[0], items = s_issued[1];
+        for (uint32_t c = pages > kStages ? pages - kStages : 0; c < pages; ++c)
+            mbar_wait_bounded(&full[c % kStages], (c / kStages) & 1, wait_limit());
+        for (uint32_t k = items > 2 ? items - 2 : 0; k < items; ++k)
+            mbar_wait_bounded(&qfull[k & 1], (k >> 1) & 1, wait_limit());
+    };
     if (warp != 0) {
         // Every warp but the producer passes the wait here; the producer
         // passes it after its early reads.
@@ -1116,22 +1138,6 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
                 raise_flag(p.err_flag, XS_FLAG_TIMEOUT);
                 atomicExch(&s_abort, 1);
             }
-            // Whether any warp aborted is known once the consumers and the
-            // merger have finished (bounded, like every wait here).
-            mbar_wait_bounded(&roles_done, 0, wait_limit());
-            if (!ok || *static_cast<volatile int *>(&s_abort)) {
-                // Drain: after an abort (here or in another warp) consumers may
-                // leave without waiting for their pages, so let every copy this
-                // CTA issued land before it exits.  Only the last kStages pages
-                // can be in flight (an older page's stage was reissued, which
-                // took its consumer's release after the page landed), and only
-                // the last two q slots.
-                const uint32_t first = page_ctr > kStages ? page_ctr - kStages : 0;
-                for (uint32_t c = first; c < page_ctr; ++c)
-                    mbar_wait_bounded(&full[c % kStages], (c / kStages) & 1, wait_limit());
-                for (uint32_t k = item_ctr > 2 ? item_ctr - 2 : 0; k < item_ctr; ++k)
-                    mbar_wait_bounded(&qfull[k & 1], (k >> 1) & 1, wait_limit());
-            }
             if (p.work) {
                 // The last CTA to stop taking items resets the counters for the
                 // next launch on this workspace.
@@ -1141,7 +1147,10 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
                     atomicExch(&p.work[1], 0);
                 }
             }
+            s_issued[0] = page_ctr;
+            s_issued[1] = item_ctr;
         }
+        exit_role();
         return;
     }
 
@@ -1253,8 +1262,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
             }
         }
         if (!*static_cast<volatile int *>(&s_abort)) flush();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&roles_done);
+        exit_role();
         return;
     }
 
@@ -1464,8 +1472,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
             if (done || *static_cast<volatile int *>(&s_abort)) break;
         }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&roles_done);
+    exit_role();
 }
 
 // Split-K combine: one CTA of D threads per (sequence, query head).
