@@ -109,11 +109,12 @@ struct Cfg {
     static constexpr int kWOff = kQSlotOff + 2 * kQBytes;
     static constexpr int kWBytes = kConsumerWarps * kBlock * G * 8;   // (w, w) pairs
     static constexpr int kCombOff = kWOff + kWBytes;
-    // A merge buffer: the item (32 B), then m[4][G], l[4][G], o[4][G][D] (fp32).
+    // A merge buffer: the item (32 B), then m[G][4], l[G][4] (each head's
+    // four consumer values together), o[4][G][D] (fp32).
     static constexpr int kCombBytes = 32 + kConsumerWarps * G * (D + 2) * 4;  // one buffer
     static constexpr int kMergeBufs = 2;   // consumers run up to kMergeBufs - 1 items ahead
     static constexpr int kBarOff = (kCombOff + kMergeBufs * kCombBytes + 7) / 8 * 8;
-    static constexpr int kBarBytes = (2 * kStages + 4 + 2 * kMergeBufs) * 8;
+    static constexpr int kBarBytes = (2 * kStages + 4 + 3 * kMergeBufs) * 8;
     static constexpr int kItemOff = kBarOff + kBarBytes;             // 2 published items
     static constexpr int kPrefixOff = kItemOff + 2 * 32;
     // The host sizes every launch with this same function.
@@ -418,6 +419,31 @@ __device__ __forceinline__ void consume_page(const unsigned char *Ks, const unsi
 // Lane j holds m and l of partials j, j + 32, ... (one load round for up to
 // 32 partials), the weights reach the other lanes by shuffles, and the
 // partial rows are loaded 16 at a time, all G heads together.
+// Store n consecutive output values (fp32 in, T out, round to nearest)
+// with one vector store.
+template <typename T, int n>
+__device__ __forceinline__ void store_row(T *dst, const float *v) {
+    if constexpr (sizeof(T) == 2) {
+        static_assert(n == 2 || n == 4, "bf16 rows of 2 or 4 values");
+        uint32_t w[n / 2];
+#pragma unroll
+        for (int i = 0; i < n / 2; ++i) {
+            const __nv_bfloat162 b = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+            w[i] = *reinterpret_cast<const uint32_t *>(&b);
+        }
+        if constexpr (n == 4)
+            *reinterpret_cast<uint2 *>(dst) = make_uint2(w[0], w[1]);
+        else
+            *reinterpret_cast<uint32_t *>(dst) = w[0];
+    } else {
+        static_assert(n == 2 || n == 4, "fp32 rows of 2 or 4 values");
+        if constexpr (n == 4)
+            *reinterpret_cast<float4 *>(dst) = make_float4(v[0], v[1], v[2], v[3]);
+        else
+            *reinterpret_cast<float2 *>(dst) = make_float2(v[0], v[1]);
+    }
+}
+
 // The merger's staging area: an mbarrier, its phase, then the rows.
 struct Stage {
     uint64_t bar;
@@ -426,6 +452,14 @@ struct Stage {
     __device__ float *rows() { return reinterpret_cast<float *>(this + 1); }
 };
 static_assert(sizeof(Stage) == 16, "staged rows start 16 bytes in");
+
+// The launch's dynamic shared memory.  Helpers that are not inlined take
+// byte offsets into it (not pointers, which would be generic there), so their
+// shared-memory accesses stay shared-memory accesses.
+__device__ __forceinline__ unsigned char *dyn_smem() {
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    return smem_raw;
+}
 
 // Split-K combine of one (sequence, KV head) group by one warp: for each of
 // the G heads, out = sum_j e^(m_j - M) o_j / sum_j e^(m_j - M) l_j over the
@@ -442,7 +476,8 @@ static_assert(sizeof(Stage) == 16, "staged rows start 16 bytes in");
 // written then).
 template <typename T, int D, int G>
 __device__ __noinline__ bool combine_partials(const Params &p, const Item &it, int64_t head0,
-                                              int lane, Stage *stage) {
+                                              int lane, int stage_off) {
+    Stage *stage = reinterpret_cast<Stage *>(dyn_smem() + stage_off);
     constexpr int kDims = D / 32;   // output dims per lane
     using Vec = typename std::conditional<kDims == 4, float4, float2>::type;
     // 16 rows held in registers, where the register budget allows (not at
@@ -491,47 +526,37 @@ __device__ __noinline__ bool combine_partials(const Params &p, const Item &it, i
                 bulk_g2s(rows + h * cnt * D, p.part_o + ((head0 + h) * p.max_parts + j0) * D,
                          static_cast<uint32_t>(cnt * D * 4), &stage->bar);
         }
+        // m and l of partial j0 + lane, all G heads in flight together; the
+        // G maxima reduce side by side (independent shuffle chains).
+        float mj[G], lj[G], cm[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            mj[h] = -INFINITY;
+            lj[h] = 0.f;
+            if (lane < tot) {
+                mj[h] = __ldcg(pm + h * p.max_parts + j0 + lane);
+                lj[h] = __ldcg(pl + h * p.max_parts + j0 + lane);
+            }
+            cm[h] = mj[h];
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+            for (int h = 0; h < G; ++h) cm[h] = fmaxf(cm[h], __shfl_xor_sync(0xffffffffu, cm[h], o));
         float wgt[G];
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-            float mj = -INFINITY, lj = 0.f;
-            if (lane < tot) {
-                mj = __ldcg(pm + h * p.max_parts + j0 + lane);
-                lj = __ldcg(pl + h * p.max_parts + j0 + lane);
-            }
-            float cm = mj;
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, o));
-            const float m_new = fmaxf(run_m[h], cm);
+            const float m_new = fmaxf(run_m[h], cm[h]);
             const float ref = m_new == -INFINITY ? 0.f : m_new;
             const float corr = fast_exp2(run_m[h] - ref);  // 0 while nothing is accumulated
             run_m[h] = m_new;
-            wgt[h] = lane < tot ? fast_exp2(mj - ref) * lj : 0.f;
+            wgt[h] = lane < tot ? fast_exp2(mj[h] - ref) * lj[h] : 0.f;
             den[h] = den[h] * corr + wgt[h];
 #pragma unroll
             for (int d = 0; d < kDims; ++d) acc[h][d] *= corr;
         }
-        const bool landed =
-            __all_sync(0xffffffffu, mbar_wait_bounded(&stage->bar, phase, wait_limit()));
-        __syncwarp();
-        if (lane == 0) stage->phase = phase ^ 1u;
-        if (!landed) {
-            // The caller flags it; first give the copies in flight (bounded)
-            // time to land, so none writes into this CTA's memory after it exits.
-            if (lane == 0) mbar_wait_bounded(&stage->bar, phase, wait_limit());
-            __syncwarp();
-            return false;
-        }
-        for (int k = 0; k < cnt; ++k) {
-#pragma unroll
-            for (int h = 0; h < G; ++h) {
-                const float w = __shfl_sync(0xffffffffu, wgt[h], k);
-                const Vec v = *reinterpret_cast<const Vec *>(rows + (h * cnt + k) * D + lane * kDims);
-                const float *f = reinterpret_cast<const float *>(&v);
-#pragma unroll
-                for (int d = 0; d < kDims; ++d) acc[h][d] += w * f[d];
-            }
-        }
+        // The register partials were requested first: fold them in while the
+        // staged rows land.
 #pragma unroll
         for (int u = 0; u < kRegParts; ++u)
 #pragma unroll
@@ -543,21 +568,67 @@ __device__ __noinline__ bool combine_partials(const Params &p, const Item &it, i
                     for (int d = 0; d < kDims; ++d) acc[h][d] += w * f[d];
                 }
             }
+        const bool landed =
+            __all_sync(0xffffffffu, mbar_wait_bounded(&stage->bar, phase, wait_limit()));
+        __syncwarp();
+        if (lane == 0) stage->phase = phase ^ 1u;
+        if (!landed) {
+            // The caller flags it; first give the copies in flight (bounded)
+            // time to land, so none writes into this CTA's memory after it exits.
+            if (lane == 0) mbar_wait_bounded(&stage->bar, phase, wait_limit());
+            __syncwarp();
+            return false;
+        }
+        // Staged rows, kRound partials per round (8 rows of the G heads): the
+        // weights' shuffles and the rows' shared-memory loads of a round are
+        // all issued before its FMAs.
+        auto fold = [&](int k, auto kU) {
+            constexpr int kU_ = decltype(kU)::value;
+            float w[kU_][G];
+            Vec v[kU_][G];
+#pragma unroll
+            for (int u = 0; u < kU_; ++u)
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+                    w[u][h] = __shfl_sync(0xffffffffu, wgt[h], k + u);
+                    v[u][h] = *reinterpret_cast<const Vec *>(rows + (h * cnt + k + u) * D +
+                                                             lane * kDims);
+                }
+#pragma unroll
+            for (int u = 0; u < kU_; ++u)
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+                    const float *f = reinterpret_cast<const float *>(&v[u][h]);
+#pragma unroll
+                    for (int d = 0; d < kDims; ++d) acc[h][d] += w[u][h] * f[d];
+                }
+        };
+        constexpr int kRound = G >= 4 ? 1 : 8 / G;  // (more rows per round spill at G = 4)
+        int k = 0;
+        for (; k + kRound <= cnt; k += kRound) fold(k, std::integral_constant<int, kRound>());
+        for (; k < cnt; ++k) fold(k, std::integral_constant<int, 1>());
         __syncwarp();  // the next chunk overwrites the staging area
         j0 += tot;
     }
+    // The G denominators reduce side by side, then each head's output row.
+    float lt[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) lt[h] = den[h];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+        for (int h = 0; h < G; ++h) lt[h] += __shfl_xor_sync(0xffffffffu, lt[h], o);
 #pragma unroll
     for (int h = 0; h < G; ++h) {
-        float lt = den[h];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) lt += __shfl_xor_sync(0xffffffffu, lt, o);
         if (p.sinks)
-            lt += fast_exp2(Elem<T>::to_f32(static_cast<const T *>(p.sinks)[it.g * G + h]) * kLog2e -
-                            run_m[h]);
-        const float inv = 1.f / lt;
-        T *dst = static_cast<T *>(p.out) + (head0 + h) * D + lane * kDims;
+            lt[h] += fast_exp2(Elem<T>::to_f32(static_cast<const T *>(p.sinks)[it.g * G + h]) *
+                                   kLog2e -
+                               run_m[h]);
+        const float inv = 1.f / lt[h];
+        float o[kDims];
 #pragma unroll
-        for (int d = 0; d < kDims; ++d) dst[d] = Elem<T>::from_f32(acc[h][d] * inv);
+        for (int d = 0; d < kDims; ++d) o[d] = acc[h][d] * inv;
+        store_row<T, kDims>(static_cast<T *>(p.out) + (head0 + h) * D + lane * kDims, o);
     }
     return true;
 }
@@ -676,14 +747,202 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *tm,
         : "memory");
 }
 
+// One consumer warp's share of an item's merge, once all four consumer
+// states are in the merge buffer: for dims [cw * D/4, (cw + 1) * D/4) of
+// every head, the four (m, l, O) are combined by their log-sum-exp weights
+// into the final output (a sequence in one partition: with the sink in the
+// denominator) or that quarter of the item's fp32 partial (consumer 0 also
+// writes the partial's m and l).  The four warps merge side by side.
+template <typename T, int D, int G>
+__device__ __forceinline__ void merge_quarter(const Params &p, const Item &it,
+                                              const unsigned char *mb, int cw, int lane) {
+    static_assert(kConsumerWarps == 4, "m and l of a head's four consumers are one float4");
+    constexpr int kQ = D / kConsumerWarps;     // dims per consumer
+    constexpr int kPerHead = kQ / 4;           // float4 chunks per head and consumer
+    constexpr int kChunks = G * kPerHead, kIters = (kChunks + 31) / 32;
+    const float *cM = reinterpret_cast<const float *>(mb + 32);
+    const float *cL = cM + kConsumerWarps * G;
+    const float *cO = cL + kConsumerWarps * G;
+    const bool single = it.nparts == 1;
+    const int64_t head0 = static_cast<int64_t>(it.b) * p.Hq + static_cast<int64_t>(it.g) * G;
+#pragma unroll
+    for (int i = 0; i < kIters; ++i) {
+        const int ch = lane + 32 * i;
+        if (kChunks % 32 != 0 && ch >= kChunks) continue;
+        const int h = ch / kPerHead, d = cw * kQ + (ch - h * kPerHead) * 4;
+        const float4 m4 = *reinterpret_cast<const float4 *>(cM + h * kConsumerWarps);
+        const float4 l4 = *reinterpret_cast<const float4 *>(cL + h * kConsumerWarps);
+        const float mx = fmaxf(fmaxf(m4.x, m4.y), fmaxf(m4.z, m4.w));
+        const float f[kConsumerWarps] = {fast_exp2(m4.x - mx), fast_exp2(m4.y - mx),
+                                         fast_exp2(m4.z - mx), fast_exp2(m4.w - mx)};
+        const float lt = f[0] * l4.x + f[1] * l4.y + f[2] * l4.z + f[3] * l4.w;
+        float4 ot = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int w2 = 0; w2 < kConsumerWarps; ++w2) {
+            const float4 v = *reinterpret_cast<const float4 *>(&cO[(w2 * G + h) * D + d]);
+            ot.x += f[w2] * v.x;
+            ot.y += f[w2] * v.y;
+            ot.z += f[w2] * v.z;
+            ot.w += f[w2] * v.w;
+        }
+        // A sink is one more logit with no value row: it only adds to the
+        // final denominator (partials leave it to the combine).
+        float den = lt;
+        if (single && p.sinks)
+            den += fast_exp2(Elem<T>::to_f32(static_cast<const T *>(p.sinks)[it.g * G + h]) *
+                                 kLog2e -
+                             mx);
+        const float inv = 1.f / den;
+        const float o4[4] = {ot.x * inv, ot.y * inv, ot.z * inv, ot.w * inv};
+        if (single) {
+            store_row<T, 4>(static_cast<T *>(p.out) + (head0 + h) * D + d, o4);
+        } else {
+            const int64_t pi = (head0 + h) * p.max_parts + it.part;
+            store_row<float, 4>(&p.part_o[pi * D + d], o4);
+            if (d == 0) {
+                p.part_m[pi] = mx;
+                p.part_l[pi] = lt;
+            }
+        }
+    }
+}
+
+// One consumer warp's share of a split group's combine (a job the merger
+// hands over once the producer has no more items, so the four consumer
+// warps are free): for dims [cw * D/4, (cw + 1) * D/4) of the G heads,
+//     out = sum_j 2^(m_j - M) l_j o_j / sum_j 2^(m_j - M) l_j  (+ sink term)
+// over the group's np partials.  Partials are read straight from L2 into
+// registers, kRound of them per round trip together with their m and l
+// (lane j holds partial j0 + j's); the round's weights go through this
+// warp's scratch in shared memory (its own ring stage, idle by then).  The
+// partials were acquired by the merger's count and handed over through a
+// CTA barrier.
+template <typename T, int D, int G>
+__device__ __noinline__ void combine_quarter(const Params &p, int b, int g, int np, int cw, int lane,
+                                             int scratch_off) {
+    using Vec = float4;
+    constexpr int kQ = D / kConsumerWarps;       // dims per warp
+    constexpr int kPerHead = kQ / 4;             // float4 chunks per head
+    constexpr int kChunks = G * kPerHead;        // chunks per warp
+    constexpr int kPer = (kChunks + 31) / 32;    // chunks per lane
+    // Partials per round trip, as many as the register budget holds.
+    constexpr int kRound = Cfg<T, D, G>::kMinBlocks >= 3 ? 6 : (kPer == 1 ? 20 : 10);
+    float *W = reinterpret_cast<float *>(dyn_smem() + scratch_off);  // [G][kRound]
+    if (!XS_BOUNDS(np >= 1 && np <= p.max_parts && b >= 0 && b < p.B && g >= 0 && g < p.Hkv,
+                   p.err_flag))
+        return;  // (debug build) nothing read or written
+    const int64_t head0 = static_cast<int64_t>(b) * p.Hq + static_cast<int64_t>(g) * G;
+    int hh[kPer], dd[kPer];
+    bool on[kPer];
+    float acc[kPer][4];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+        const int c = lane + 32 * i;
+        on[i] = kChunks % 32 == 0 || c < kChunks;
+        hh[i] = on[i] ? c / kPerHead : 0;
+        dd[i] = cw * kQ + (c - hh[i] * kPerHead) * 4;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[i][e] = 0.f;
+    }
+    float run_m[G], den[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+        run_m[h] = -INFINITY;
+        den[h] = 0.f;
+    }
+    const float *pm = p.part_m + head0 * p.max_parts;
+    const float *pl = p.part_l + head0 * p.max_parts;
+    for (int j0 = 0; j0 < np; j0 += kRound) {
+        const int n = min(kRound, np - j0);
+        // The round's rows first (no dependence on the weights), then m, l.
+        Vec rows[kRound][kPer];
+#pragma unroll
+        for (int u = 0; u < kRound; ++u)
+#pragma unroll
+            for (int i = 0; i < kPer; ++i)
+                if (u < n && on[i])
+                    rows[u][i] = __ldcg(reinterpret_cast<const Vec *>(
+                        p.part_o + ((head0 + hh[i]) * p.max_parts + j0 + u) * D + dd[i]));
+        float mj[G], lj[G], cm[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            mj[h] = -INFINITY;
+            lj[h] = 0.f;
+            if (lane < n) {
+                mj[h] = __ldcg(pm + h * p.max_parts + j0 + lane);
+                lj[h] = __ldcg(pl + h * p.max_parts + j0 + lane);
+            }
+            cm[h] = mj[h];
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+            for (int h = 0; h < G; ++h) cm[h] = fmaxf(cm[h], __shfl_xor_sync(0xffffffffu, cm[h], o));
+        float corr[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            const float m_new = fmaxf(run_m[h], cm[h]);
+            const float ref = m_new == -INFINITY ? 0.f : m_new;
+            corr[h] = fast_exp2(run_m[h] - ref);  // 0 while nothing is accumulated
+            run_m[h] = m_new;
+            const float w = lane < n ? fast_exp2(mj[h] - ref) * lj[h] : 0.f;
+            den[h] = den[h] * corr[h] + w;
+            if (lane < kRound) W[h * kRound + lane] = w;
+        }
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+            float c = corr[0];
+#pragma unroll
+            for (int h = 1; h < G; ++h) c = hh[i] == h ? corr[h] : c;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[i][e] *= c;
+        }
+#pragma unroll
+        for (int u = 0; u < kRound; ++u)
+#pragma unroll
+            for (int i = 0; i < kPer; ++i)
+                if (u < n && on[i]) {
+                    const float w = W[hh[i] * kRound + u];
+                    acc[i][0] += w * rows[u][i].x;
+                    acc[i][1] += w * rows[u][i].y;
+                    acc[i][2] += w * rows[u][i].z;
+                    acc[i][3] += w * rows[u][i].w;
+                }
+        __syncwarp();  // the next round overwrites the weights
+    }
+    // Denominators: the lanes' sums, reduced side by side for the G heads.
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+        for (int h = 0; h < G; ++h) den[h] += __shfl_xor_sync(0xffffffffu, den[h], o);
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+        if (!on[i]) continue;
+        float lt = den[0], mh = run_m[0];
+#pragma unroll
+        for (int h = 1; h < G; ++h) {
+            lt = hh[i] == h ? den[h] : lt;
+            mh = hh[i] == h ? run_m[h] : mh;
+        }
+        if (p.sinks)
+            lt += fast_exp2(Elem<T>::to_f32(static_cast<const T *>(p.sinks)[g * G + hh[i]]) * kLog2e -
+                            mh);
+        const float inv = 1.f / lt;
+        const float o4[4] = {acc[i][0] * inv, acc[i][1] * inv, acc[i][2] * inv, acc[i][3] * inv};
+        store_row<T, 4>(static_cast<T *>(p.out) + (head0 + hh[i]) * D + dd[i], o4);
+    }
+}
+
 // The merger's batched count: queue entry k (held by lane k < npend) is a
 // split item of group (b, g) with np partitions whose partials this warp has
 // written.  One fence publishes them all; each entry's group count is then
 // raised (all in flight together) and every entry that completes its group
 // combines it and clears the count for the next launch.
-template <typename T, int D, int G>
-__device__ __noinline__ bool count_and_combine(const Params &p, int lane, int pend_b, int pend_g,
-                                               int pend_np, int npend, Stage *stage) {
+template <typename T, int D, int G, typename Post>
+__device__ __forceinline__ bool count_and_combine(const Params &p, int lane, int pend_b, int pend_g,
+                                                  int pend_np, int npend, int stage_off,
+                                                  bool to_consumers, Post &&post) {
     // Every lane's partial stores are gathered by the warp barrier; each
     // counting lane's acquire-release add releases them (cumulatively) and
     // acquires the group's earlier partials; a second barrier hands that to
@@ -707,10 +966,12 @@ __device__ __noinline__ bool count_and_combine(const Params &p, int lane, int pe
         ci.g = __shfl_sync(0xffffffffu, pend_g, k);
         ci.nparts = __shfl_sync(0xffffffffu, pend_np, k);
         const int64_t h0 = static_cast<int64_t>(ci.b) * p.Hq + static_cast<int64_t>(ci.g) * G;
-        ok = combine_partials<T, D, G>(p, ci, h0, lane, stage);
+        ok = to_consumers ? post(ci.b, ci.g, ci.nparts)
+                          : combine_partials<T, D, G>(p, ci, h0, lane, stage_off);
     }
     // Leave the completed groups' counts zero for the next launch - after
-    // the combines, so no fence above waits for these writes.
+    // the combines (or their hand-over), so no fence above waits for these
+    // writes.
     if (combined & (1u << lane)) atomicExch(cnt, 0);
     return ok;
 }
@@ -722,14 +983,17 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
     using C = Cfg<T, D, G>;
     constexpr int kStages = C::kStages;
     extern __shared__ __align__(128) unsigned char smem_raw[];
-    unsigned char *smem = reinterpret_cast<unsigned char *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    // The base rounded up to 1024 bytes by pointer arithmetic on the shared
+    // array (not through an integer), so accesses through it stay
+    // shared-memory accesses.
+    unsigned char *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::kBarOff);
     uint64_t *empty = full + kStages;
     uint64_t *qfull = empty + kStages;
     uint64_t *qempty = qfull + 2;
     uint64_t *merged = qempty + 2;  // per merge buffer: the four consumer states are in
     uint64_t *freed = merged + C::kMergeBufs;  // per merge buffer: the merger has read it
+    uint64_t *quartered = freed + C::kMergeBufs;  // per merge buffer: the four quarters are merged
     Item *item_slot = reinterpret_cast<Item *>(smem + C::kItemOff);
     int *pfull = reinterpret_cast<int *>(smem + C::kPrefixOff);
     int *ptail = pfull + p.B + 1;
@@ -739,6 +1003,15 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
     // the last warp to finish drains the copies after an abort (exit_role).
     __shared__ int s_roles_left;
     __shared__ uint32_t s_issued[2];
+    // Set by the producer once it has no more items for this CTA.  From then
+    // on the merger hands the combines of completed groups to the consumer
+    // warps (s_job: b, g, nparts; b < 0 ends the consumers' service).
+    __shared__ int s_no_more;
+    __shared__ int s_job[3];
+    __shared__ uint64_t s_job_full, s_job_done;
+    // Only where a quarter of a group's dims fills a warp (G * D / 16 float4
+    // chunks per warp >= 32 lanes); narrower groups stay with the merger.
+    constexpr bool kJobs = G * D >= 512;
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
@@ -764,7 +1037,10 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
         for (int s = 0; s < C::kMergeBufs; ++s) {
             mbar_init(&merged[s], kConsumerWarps);
             mbar_init(&freed[s], 1);
+            mbar_init(&quartered[s], kConsumerWarps);
         }
+        mbar_init(&s_job_full, 1);
+        mbar_init(&s_job_done, kConsumerWarps);
         if (p.combine) {
             Stage *st = reinterpret_cast<Stage *>(smem + stage_offset(C::kPrefixOff, p.B));
             mbar_init(&st->bar, 1);
@@ -774,6 +1050,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
         s_abort = 0;
         s_roles_left = kConsumerWarps + 2;
         s_issued[0] = s_issued[1] = 0;
+        s_no_more = 0;
     }
     // Programmatic dependent launch.  griddep_wait returns once the previous
     // launch on the stream has completed and its writes are visible; only
@@ -921,6 +1198,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
             if (item < total_items) {
                 it = decode_item(p, pfull, ptail, nlen, item, lane);
             } else {
+                if (lane == 0) *static_cast<volatile int *>(&s_no_more) = 1;
                 it.b = -1;
                 it.g = it.part = it.nparts = it.tok0 = it.tok1 = it.pg0 = it.pg1 = 0;
             }
@@ -1169,10 +1447,29 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
         // full, or the consumers are done.
         constexpr int kMaxPend = 8;
         int pend_b = 0, pend_g = 0, pend_np = 0, npend = 0;
-        Stage *stage = reinterpret_cast<Stage *>(smem + stage_offset(C::kPrefixOff, p.B));
-        auto flush = [&]() {
+        const int stage_off =
+            static_cast<int>(smem - smem_raw) + stage_offset(C::kPrefixOff, p.B);
+        // Hand a completed group's combine to the consumer warps (their job
+        // slot is reused once all four have finished the previous job).
+        uint32_t njobs = 0;
+        auto post = [&](int b, int g, int np) {
+            bool ok = true;
+            if (lane == 0) {
+                if (njobs > 0) ok = mbar_wait_bounded(&s_job_done, (njobs - 1) & 1, wait_limit());
+                if (ok) {
+                    s_job[0] = b;
+                    s_job[1] = g;
+                    s_job[2] = np;
+                    mbar_arrive(&s_job_full);
+                }
+            }
+            ++njobs;
+            return __shfl_sync(0xffffffffu, ok, 0);
+        };
+        auto flush = [&](bool to_consumers) {
             if (npend == 0) return;
-            if (!count_and_combine<T, D, G>(p, lane, pend_b, pend_g, pend_np, npend, stage) &&
+            if (!count_and_combine<T, D, G>(p, lane, pend_b, pend_g, pend_np, npend, stage_off,
+                                            to_consumers, post) &&
                 lane == 0) {
                 raise_flag(p.err_flag, XS_FLAG_TIMEOUT);
                 atomicExch(&s_abort, 1);
@@ -1183,9 +1480,13 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
             const int buf = item_ctr % C::kMergeBufs;
             unsigned char *mb = smem + C::kCombOff + buf * C::kCombBytes;
             const uint32_t mpar = (item_ctr / C::kMergeBufs) & 1;
-            if (npend > 0 && !__shfl_sync(0xffffffffu, mbar_test_wait(&merged[buf], mpar), 0))
-                flush();  // idle until the next item: count the queued ones now
-            if (!mbar_wait_bounded(&merged[buf], mpar, wait_limit())) {
+            // Idle until the next item: count the queued ones now - unless the
+            // producer is out of items, when the consumers will soon be free
+            // to share the combines (counted after their last item).
+            if (npend > 0 && !(kJobs && *static_cast<volatile int *>(&s_no_more)) &&
+                !__shfl_sync(0xffffffffu, mbar_test_wait(&quartered[buf], mpar), 0))
+                flush(false);
+            if (!mbar_wait_bounded(&quartered[buf], mpar, wait_limit())) {
                 if (lane == 0) {
                     raise_flag(p.err_flag, XS_FLAG_TIMEOUT);
                     atomicExch(&s_abort, 1);
@@ -1194,62 +1495,11 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
             }
             const Item it = *reinterpret_cast<const Item *>(mb);
             if (it.b < 0) break;  // the consumers have no more items
-            const float *cM = reinterpret_cast<const float *>(mb + 32);
-            const float *cL = cM + kConsumerWarps * G;
-            const float *cO = cL + kConsumerWarps * G;
             const bool valid = it.b < p.B && it.g >= 0 && it.g < p.Hkv && it.part >= 0 &&
                                it.part < p.max_parts && !*static_cast<volatile int *>(&s_abort);
             const bool single = it.nparts == 1;
-            const int64_t head0 =
-                static_cast<int64_t>(it.b) * p.Hq + static_cast<int64_t>(it.g) * G;
-            for (int ch = lane; valid && ch < G * D / 4; ch += 32) {
-                const int h = ch / (D / 4), d = (ch - h * (D / 4)) * 4;
-                float mw[kConsumerWarps], mx = -INFINITY;
-#pragma unroll
-                for (int w2 = 0; w2 < kConsumerWarps; ++w2) {
-                    mw[w2] = cM[w2 * G + h];
-                    mx = fmaxf(mx, mw[w2]);
-                }
-                float lt = 0.f;
-                float4 ot = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                for (int w2 = 0; w2 < kConsumerWarps; ++w2) {
-                    const float f = fast_exp2(mw[w2] - mx);
-                    lt += f * cL[w2 * G + h];
-                    const float4 v = *reinterpret_cast<const float4 *>(&cO[(w2 * G + h) * D + d]);
-                    ot.x += f * v.x;
-                    ot.y += f * v.y;
-                    ot.z += f * v.z;
-                    ot.w += f * v.w;
-                }
-                // A sink is one more logit with no value row: it only adds to
-                // the final denominator (partials leave it to the reduce).
-                float den = lt;
-                if (single && p.sinks)
-                    den += fast_exp2(Elem<T>::to_f32(static_cast<const T *>(p.sinks)[it.g * G + h]) *
-                                         kLog2e -
-                                     mx);
-                const float inv = 1.f / (single ? den : lt);
-                ot.x *= inv;
-                ot.y *= inv;
-                ot.z *= inv;
-                ot.w *= inv;
-                if (single) {
-                    T *dst = static_cast<T *>(p.out) + (head0 + h) * D + d;
-                    dst[0] = Elem<T>::from_f32(ot.x);
-                    dst[1] = Elem<T>::from_f32(ot.y);
-                    dst[2] = Elem<T>::from_f32(ot.z);
-                    dst[3] = Elem<T>::from_f32(ot.w);
-                } else {
-                    const int64_t pi = (head0 + h) * p.max_parts + it.part;
-                    *reinterpret_cast<float4 *>(&p.part_o[pi * D + d]) = ot;
-                    if (d == 0) {
-                        p.part_m[pi] = mx;
-                        p.part_l[pi] = lt;
-                    }
-                }
-            }
-            // The merge buffer is read: hand it back before any combine.
+            // The consumers have merged and stored this item (its output, or
+            // its partial): the buffer is free again.
             __syncwarp();
             if (lane == 0) mbar_arrive(&freed[buf]);
             if (valid && !single && p.combine) {
@@ -1258,16 +1508,44 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
                     pend_g = it.g;
                     pend_np = it.nparts;
                 }
-                if (++npend == kMaxPend) flush();
+                if (++npend == kMaxPend) flush(false);
             }
         }
-        if (!*static_cast<volatile int *>(&s_abort)) flush();
+        // The consumers are past their last item: the remaining combines are
+        // theirs, then the end of their service.
+        if (!*static_cast<volatile int *>(&s_abort)) flush(kJobs);
+        if (kJobs && p.combine) post(-1, 0, 0);
         exit_role();
         return;
     }
 
     // ==================================================================== consumers
     const int cw = warp - 1;
+    // A consumer's state for item `it` is in merge buffer `buf`: announce it,
+    // wait (bounded) for the other three, merge this warp's quarter of the
+    // dims, and report the quarter done to the merger.  False if the wait
+    // for the other states ran out.
+    auto hand_over = [&](const Item &it, const unsigned char *mb, int buf, uint32_t item_ctr,
+                         bool done) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&merged[buf]);
+        const bool in = __all_sync(0xffffffffu, mbar_wait_bounded(&merged[buf],
+                                                                  (item_ctr / C::kMergeBufs) & 1,
+                                                                  wait_limit()));
+        if (!in) {
+            if (lane == 0) {
+                raise_flag(p.err_flag, XS_FLAG_TIMEOUT);
+                atomicExch(&s_abort, 1);
+            }
+            return false;
+        }
+        const bool valid = it.b >= 0 && it.b < p.B && it.g >= 0 && it.g < p.Hkv && it.part >= 0 &&
+                           it.part < p.max_parts && !*static_cast<volatile int *>(&s_abort);
+        if (!done && valid) merge_quarter<T, D, G>(p, it, mb, cw, lane);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&quartered[buf]);
+        return true;
+    };
     if constexpr (C::kMma) {
         // bf16: tensor-core pages (consume_page_mma); per item the G query rows
         // become A fragments (lane quad g holds head g, unscaled: scores are
@@ -1353,12 +1631,11 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
                 for (int n = 0; n < D / 8; ++n)
                     *reinterpret_cast<float2 *>(dst + 8 * n) = make_float2(oacc[n][0], oacc[n][1]);
                 if (tq == 0) {
-                    cM[cw * G + grp] = m_row;
-                    cL[cw * G + grp] = l_row;
+                    cM[grp * kConsumerWarps + cw] = m_row;
+                    cL[grp * kConsumerWarps + cw] = l_row;
                 }
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&merged[buf]);
+            if (!hand_over(it, mb, buf, item_ctr, done)) break;
             if (done || *static_cast<volatile int *>(&s_abort)) break;
         }
     } else {
@@ -1463,13 +1740,33 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
                 }
                 if (lane < 8 && (j & ((1 << C::kHeadShift) - 1)) == 0) {
                     const int own_head = j >> C::kHeadShift;
-                    cM[cw * G + own_head] = m_own;
-                    cL[cw * G + own_head] = l_own;
+                    cM[own_head * kConsumerWarps + cw] = m_own;
+                    cL[own_head * kConsumerWarps + cw] = l_own;
                 }
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&merged[buf]);
+            if (!hand_over(it, mb, buf, item_ctr, done)) break;
             if (done || *static_cast<volatile int *>(&s_abort)) break;
+        }
+    }
+    // Combine jobs from the merger (one per split group completed after the
+    // producer ran out of items), each shared by the four consumer warps.
+    // This warp's scratch is its own first ring stage: every page copied
+    // into it has been consumed by now.
+    if (kJobs && p.combine && !*static_cast<volatile int *>(&s_abort)) {
+        const int scratch_off = static_cast<int>(smem - smem_raw) + cw * 2 * C::kPageBytes;
+        for (uint32_t k = 0;; ++k) {
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(&s_job_full, k & 1, wait_limit()))) {
+                if (lane == 0) {
+                    raise_flag(p.err_flag, XS_FLAG_TIMEOUT);
+                    atomicExch(&s_abort, 1);
+                }
+                break;
+            }
+            const int jb = s_job[0], jg = s_job[1], jnp = s_job[2];
+            if (jb < 0) break;
+            combine_quarter<T, D, G>(p, jb, jg, jnp, cw, lane, scratch_off);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s_job_done);
         }
     }
     exit_role();
