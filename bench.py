@@ -23,6 +23,7 @@ a bounded sample of the same workload, on the host cores.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -588,6 +589,11 @@ def run_ours(args, rank, world, local, dist):
     dev = torch.device(f"cuda:{local}")
     torch.cuda.set_device(dev)
     cfg = wl.CONFIGS[args.config]
+    if args.batch:
+        # The same length distribution with fewer sequences and a pool of
+        # just the pages they need (a small case for counter captures).
+        cfg = dataclasses.replace(cfg, B=args.batch, pool="needed", pool_arg=1,
+                                  name=f"{cfg.name}_b{args.batch}")
     m = measure_decode(args, cfg, rank, world, local, dist, steps=args.steps, warmup=args.warmup,
                        load_seconds=args.load_seconds, sinks_on=args.sinks, window=args.window,
                        partition_tokens=args.partition_tokens, with_e2e=True)
@@ -652,7 +658,7 @@ def run_ours(args, rank, world, local, dist):
     # process, each with its own timing, roofline, clocks and oracle parity.
     want_rows = args.rows == "on" or (args.rows == "auto" and args.config == 4 and
                                       not args.sinks and args.window == 0 and
-                                      not args.partition_tokens)
+                                      not args.partition_tokens and not args.batch)
     if want_rows:
         del m, w, step
         torch.cuda.empty_cache()
@@ -1091,6 +1097,9 @@ def main(argv=None):
     ap.add_argument("--graph", choices=["auto", "on", "off"], default="auto",
                     help="replay each step as one CUDA graph (auto: when the workload has "
                          "more than one layer)")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="draw the workload with this many sequences (same length "
+                         "distribution, pool of the pages needed); 0 = the workload's own")
     ap.add_argument("--partition-tokens", type=int, default=0,
                     help="split-K partition size (multiple of 16); 0 = the library's heuristic")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,

@@ -498,11 +498,13 @@ int xs_paged_decode_step_ex(void *out, const void *q, const void *k_new, const v
 /*
  * xs_paged_decode_step_partition_tokens - partition length P for
  * xs_paged_decode_step: the cost model of xs_paged_decode_partition_tokens
- * with its per-item cost and ragged-end allowance fitted to one-launch step
- * times, searched over multiples of 64 in [64, 2048] (64, 128, ..., 512,
- * 640, 768, 896, 1024, 1280, 1536, 2048) so that a batch's item count can
- * land just under a whole number of rounds of the grid.  Same arguments
- * plus Hq; XS_ESHAPE also when Hq % Hkv != 0.
+ * fitted to one-launch step times, with whole rounds of the grid when every
+ * sequence has the same length (total_context_tokens = B * max_context_len)
+ * and a cost per partition of the longest sequence for its split-K combine,
+ * searched over multiples of 64 in [64, 2048] (64, 128, ..., 512, 640, 768,
+ * 896, 1024, 1280, 1536, 2048) so that a batch's item count can land just
+ * under a whole number of rounds of the grid.  Same arguments plus Hq;
+ * XS_ESHAPE also when Hq % Hkv != 0.
  */
 int xs_paged_decode_step_partition_tokens(int B, int Hq, int Hkv, int64_t total_context_tokens,
                                           int max_context_len, int num_sms);

@@ -2050,28 +2050,41 @@ extern "C" int xs_paged_decode_step_partition_tokens(int B, int Hq, int Hkv,
     const double tokens = total_context_tokens > 0
                               ? static_cast<double>(total_context_tokens)
                               : static_cast<double>(B) * std::max(max_context_len, 1);
-    // The cost model of xs_paged_decode_partition_tokens with constants
-    // fitted to one-launch step times: an item of P tokens costs P/64 +
-    // kItemCost page-times (q staging, first-page latency, the merge, and the
-    // combines the merge warp runs meanwhile), the grid takes items / CTAs
-    // rounds plus half a round of ragged end, and P runs over multiples of
-    // 64 so that a batch can land just under a whole number of rounds.  The
-    // fit covered 20 workloads (mixes of 16-512 sequences with log-uniform
-    // lengths, fixed-length batches of 1-16 sequences, the MHA and GQA
-    // shapes): mean 1.05 % and at most 4.5 % slower than the best measured P
-    // (the power-of-two search this replaced: 2.0 % and 5.5 %).  The split-K
-    // combine's own cost did not improve the fit: the merge warp combines
-    // groups while the other warps still stream pages.
-    constexpr double kItemCost = 5.0;
-    constexpr double kTailRounds = 0.5;
+    // The cost model of xs_paged_decode_partition_tokens, refitted to
+    // one-launch step times: an item of P tokens costs P/64 + kItemCost
+    // page-times (q staging, first-page latency, the four-warp merge); the
+    // grid takes items / CTAs rounds plus kTailRounds of ragged end - or,
+    // when every sequence has the same length, exactly ceil(items / CTAs)
+    // rounds (a batch one item over a round takes a whole second round) -
+    // and the split-K combine at the end of the longest sequence adds
+    // kCombineCost per partition.  P runs over multiples of 64 so that a
+    // batch can land just under a whole number of rounds.  Fitted to a sweep
+    // of every candidate P on 14 workloads (log-uniform mixes of 16-256
+    // sequences, equal-length batches of 1-16 sequences, the GQA and MHA
+    // shapes, the long batch): mean 0.7 % and at most 2.1 % slower than the
+    // best measured P.
+    constexpr double kItemCost = 1.5;
+    constexpr double kTailRounds = 0.4;
+    constexpr double kCombineCost = 0.2;
     constexpr int kCandidates[] = {64,  128, 192, 256, 320,  384,  448, 512,
                                    640, 768, 896, 1024, 1280, 1536, 2048};
     const double ctas = 2.0 * num_sms;
+    const int longest = std::max(max_context_len, 1);
+    const bool uniform = tokens >= 0.98 * static_cast<double>(B) * longest;
     int best = 64;
     double best_cost = 1e300;
     for (const int P : kCandidates) {
-        const double items = std::max((tokens / P + 0.5 * B) * Hkv, static_cast<double>(B) * Hkv);
-        const double cost = (items / ctas + kTailRounds) * (P / 64.0 + kItemCost);
+        const int np = (longest + P - 1) / P;
+        double cost;
+        if (uniform) {
+            const double items = static_cast<double>(B) * Hkv * np;
+            cost = std::ceil(items / ctas) * (P / 64.0 + kItemCost);
+        } else {
+            const double items =
+                std::max((tokens / P + 0.5 * B) * Hkv, static_cast<double>(B) * Hkv);
+            cost = (items / ctas + kTailRounds) * (P / 64.0 + kItemCost);
+        }
+        if (np > 1) cost += kCombineCost * np;
         if (cost <= best_cost * (1.0 + 1e-9)) {  // ties go to the larger partition
             best_cost = cost;
             best = P;

@@ -79,16 +79,20 @@ def test_partition_heuristic(lib):
 
 def test_step_partition_heuristic(lib):
     # The one-launch step's choice on measured workloads.  Its constants were
-    # fitted to one-launch step times swept over P: the continuous-batching
-    # mix (64 sequences) ran 46.5 / 45.0 / 44.7 / 47.2 us at P = 512 / 640 /
-    # 768 / 1024; the single stream was fastest at 256; the long batch is flat
-    # from 2048 up; 4 x 4096 tokens was fastest at 512 (288 items, under one
-    # round of 304 CTAs) and 1 x 1024 at 128-192.
+    # fitted to one-launch step times swept over every candidate P: the
+    # continuous-batching mix (64 sequences) ran 41.96 / 41.60 / 43.83 us at
+    # P = 448 / 512 / 640; the single stream was fastest at 256 (33
+    # partitions at 128 cost more in the combine); the long batch is fastest
+    # at 2048; equal-length batches land on a whole round of 304 CTAs: 4 x
+    # 4097 tokens at 512 (256 items), 8 x 2049 and 16 x 1025 at 640 (256
+    # items; 448 gives 320 items, a second round, +22 %), 1 x 1025 at 128.
     pick = ops.xs_paged_decode_step_partition_tokens
-    assert pick(64, 32, 8, 63638, 7598, 152) == 640
+    assert pick(64, 32, 8, 63638, 7598, 152) == 448
     assert pick(1, 32, 8, 4097, 4097, 152) == 256
     assert pick(128, 32, 8, 2538762, 32769, 152) == 2048
     assert pick(4, 32, 8, 16388, 4097, 152) == 512
+    assert pick(8, 32, 8, 8 * 2049, 2049, 152) == 640
+    assert pick(16, 32, 8, 16 * 1025, 1025, 152) == 640
     assert pick(1, 32, 8, 1025, 1025, 152) in (128, 192)
     for B, Hq, Hkv, total, mx in [(8, 12, 12, 3439, 926), (2, 12, 12, 29, 21), (512, 32, 8, 10**6, 8193)]:
         P = pick(B, Hq, Hkv, total, mx, 152)
