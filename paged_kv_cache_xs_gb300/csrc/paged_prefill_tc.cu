@@ -214,8 +214,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ int s_abort;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int g = blockIdx.y;
-    const int tok0 = blockIdx.x * kQTiles * kTq;
+    // Longest first: CTA i takes token tile (tiles - 1 - i / Hkv) of KV head
+    // i % Hkv, so the CTAs with the most keys start in the first wave and the
+    // launch ends on the short ones.
+    const int n_tok_tiles = static_cast<int>(gridDim.x) / p.Hkv;
+    const int g = static_cast<int>(blockIdx.x) % p.Hkv;
+    const int tok0 = (n_tok_tiles - 1 - static_cast<int>(blockIdx.x) / p.Hkv) * kQTiles * kTq;
     const int ntok = min(kQTiles * kTq, p.T - tok0);  // tokens of this CTA
     const int kmax = p.start + tok0 + ntok;            // keys [0, kmax) are read
     const int ntiles = (kmax + kKeys - 1) / kKeys;
@@ -699,7 +703,9 @@ extern "C" int xs_paged_prefill_tc(void *out, const void *q, const void *k_cache
     p.qscale = scale * pftc::kLog2e;
     p.err_flag = err_flag;
     const int tq = pftc::kQTiles * pftc::kRows / G;  // query tokens per CTA
-    dim3 grid((T + tq - 1) / tq, Hkv);
+    const int64_t ctas = static_cast<int64_t>((T + tq - 1) / tq) * Hkv;
+    if (ctas > 0x7fffffff) return XS_EUNSUPPORTED;
+    dim3 grid(static_cast<unsigned>(ctas));
     fn<<<grid, pftc::kThreads, smem, stream>>>(tmq, tmk, tmv, p);
     return launch_status();
 }
