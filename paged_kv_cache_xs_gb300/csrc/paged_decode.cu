@@ -82,7 +82,12 @@ __device__ __forceinline__ constexpr bool skip_page(uint32_t) { return false; }
 // (item numbering) and nlen[B] (clamped context lengths).
 __host__ __device__ constexpr int table_bytes(int B) { return 4 * (3 * B + 2); }
 
-template <typename T, int D, int G>
+// S: stages of the page ring.  The default (8) leaves room for two or three
+// resident CTAs per SM; the deep ring (16, one CTA per SM) serves launches
+// with at most one work item per SM, whose whole first item then fits the
+// ring before the launch wait.
+constexpr int kRing = 2 * kConsumerWarps, kDeepRing = 4 * kConsumerWarps;
+template <typename T, int D, int G, int S = kRing>
 struct Cfg {
     static constexpr int kRowBytes = D * static_cast<int>(sizeof(T));
     static constexpr int kPageBytes = kBlock * kRowBytes;
@@ -91,7 +96,7 @@ struct Cfg {
     // every stage is only ever used by one warp.  Otherwise a warp could wait
     // for phase k of a stage whose phase k-1 (another warp's page) has not
     // completed yet, and a parity wait cannot tell phase k from phase k-2.
-    static constexpr int kStages = 2 * kConsumerWarps;
+    static constexpr int kStages = S;
     static constexpr int kChunksPerRow = kRowBytes / 16;
     static constexpr int kChunksPerLane = kChunksPerRow / 8;   // QK: 8 lanes per token
     static constexpr int kElemsPerChunk = 16 / static_cast<int>(sizeof(T));
@@ -102,7 +107,8 @@ struct Cfg {
     static constexpr int kLogG = G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : 3;
     static constexpr int kHeadShift = 3 - kLogG;  // lane j of a token group owns head j >> shift
     // Resident CTAs per SM the register budget is sized for.
-    static constexpr int kMinBlocks = G == 8 ? 1 : ((2 * kPageBytes <= 4096) ? 3 : 2);
+    static constexpr int kMinBlocks =
+        (G == 8 || S > kRing) ? 1 : ((2 * kPageBytes <= 4096) ? 3 : 2);
     // Shared memory carve-up (bytes).
     static constexpr int kRingBytes = kStages * 2 * kPageBytes;
     static constexpr int kQSlotOff = kRingBytes;
@@ -976,11 +982,11 @@ __device__ __forceinline__ bool count_and_combine(const Params &p, int lane, int
     return ok;
 }
 
-template <typename T, int D, int G>
-__global__ void __launch_bounds__(kThreads, Cfg<T, D, G>::kMinBlocks)
+template <typename T, int D, int G, int S>
+__global__ void __launch_bounds__(kThreads, Cfg<T, D, G, S>::kMinBlocks)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmk,
                         const __grid_constant__ CUtensorMap tmv, const Params p) {
-    using C = Cfg<T, D, G>;
+    using C = Cfg<T, D, G, S>;
     constexpr int kStages = C::kStages;
     extern __shared__ __align__(128) unsigned char smem_raw[];
     // The base rounded up to 1024 bytes by pointer arithmetic on the shared
@@ -1809,16 +1815,27 @@ __global__ void paged_decode_reduce_kernel(T *__restrict__ out, const float *__r
 
 using KernelFn = void (*)(const CUtensorMap, const CUtensorMap, const Params);
 
-template <typename T, int D, int G>
+template <typename T, int D, int G, int S>
 KernelFn kernel_for() {
-    return paged_decode_kernel<T, D, G>;
+    return paged_decode_kernel<T, D, G, S>;
 }
 
-KernelFn pick_kernel(int dtype, int D, int G, int *smem_base_fn_B0) {
+// The kernel for a shape, with the deep ring when asked and instantiated
+// (bf16, D = 128).
+KernelFn pick_kernel(int dtype, int D, int G, bool deep, int *smem_base_fn_B0) {
 #define XS_PICK(TT, DD, GG)                                                          \
     if (D == DD && G == GG) {                                                        \
         *smem_base_fn_B0 = Cfg<TT, DD, GG>::kPrefixOff;                              \
-        return kernel_for<TT, DD, GG>();                                             \
+        return kernel_for<TT, DD, GG, kRing>();                                      \
+    }
+#define XS_PICK_DEEP(TT, DD, GG)                                                     \
+    if (D == DD && G == GG) {                                                        \
+        *smem_base_fn_B0 = Cfg<TT, DD, GG, kDeepRing>::kPrefixOff;                   \
+        return kernel_for<TT, DD, GG, kDeepRing>();                                  \
+    }
+    if (dtype == XS_BF16 && deep) {
+        XS_PICK_DEEP(__nv_bfloat16, 128, 1) XS_PICK_DEEP(__nv_bfloat16, 128, 2)
+        XS_PICK_DEEP(__nv_bfloat16, 128, 4) XS_PICK_DEEP(__nv_bfloat16, 128, 8)
     }
     if (dtype == XS_BF16) {
         XS_PICK(__nv_bfloat16, 64, 1) XS_PICK(__nv_bfloat16, 64, 2)
@@ -1831,6 +1848,7 @@ KernelFn pick_kernel(int dtype, int D, int G, int *smem_base_fn_B0) {
         XS_PICK(float, 128, 8)
     }
 #undef XS_PICK
+#undef XS_PICK_DEEP
     return nullptr;
 }
 
@@ -2154,7 +2172,9 @@ static int launch_attn(void *out, float *part_o, float *part_m, float *part_l, c
     attn::DeviceInfo dev;
     if ((st = attn::device_info(&dev)) != XS_OK) return st;
     int smem0 = 0;
-    attn::KernelFn fn = attn::pick_kernel(dtype, D, Hq / Hkv, &smem0);
+    // At most one work item per SM: one CTA per SM with the deep ring.
+    const bool deep = static_cast<int64_t>(B) * Hkv * max_partitions <= dev.sms;
+    attn::KernelFn fn = attn::pick_kernel(dtype, D, Hq / Hkv, deep, &smem0);
     if (!fn) return XS_EUNSUPPORTED;
     int smem = smem0 + attn::table_bytes(B) + 1024;  // = Cfg<...>::smem_bytes(B)
     if (smem + 1024 > dev.max_smem_optin) return XS_EUNSUPPORTED;  // room for static smem
