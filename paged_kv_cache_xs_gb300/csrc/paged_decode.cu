@@ -680,25 +680,36 @@ __device__ __forceinline__ uint32_t page_addr(uint32_t base, int key, int d) {
 // from the S accumulators.  Keys outside [t_lo, t_hi) are masked out of S
 // and their V rows zeroed in the fragments (a slot past the sequence's end
 // may hold any bits).  qa: per 16-dim step, the head row's two bf16 pairs.
-template <int D, bool kFull>
+// kSplit: Q K^T as two independent accumulator chains (even and odd
+// 16-dim steps) added at the end, halving the dependent MMA chain of a page
+// (for the deep-ring kernel, whose one CTA per SM leaves the registers).
+template <int D, bool kFull, bool kSplit = false>
 __device__ __forceinline__ void consume_page_mma(uint32_t kaddr, uint32_t vaddr, int t_lo, int t_hi,
                                                  const uint32_t (&qa)[D / 16][2], float qscale,
                                                  float &m_row, float &l_lane, float (&oacc)[D / 8][4],
                                                  int lane) {
     const int tq = lane & 3, mi = lane >> 3, ri = lane & 7;
-    float sacc[2][4];
+    constexpr int kChains = kSplit ? 2 : 1;
+    float sch[kChains][2][4];
 #pragma unroll
-    for (int n = 0; n < 2; ++n)
+    for (int k = 0; k < kChains; ++k)
 #pragma unroll
-        for (int c = 0; c < 4; ++c) sacc[n][c] = 0.f;
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) sch[k][n][c] = 0.f;
 #pragma unroll
     for (int ks = 0; ks < D / 16; ++ks) {
         uint32_t b0, b1, b2, b3;
         ldsm_x4(page_addr<D>(kaddr, ((mi >> 1) << 3) + ri, 16 * ks + ((mi & 1) << 3)), b0, b1, b2,
                 b3);
-        mma_rows8(sacc[0], qa[ks][0], qa[ks][1], b0, b1);
-        mma_rows8(sacc[1], qa[ks][0], qa[ks][1], b2, b3);
+        mma_rows8(sch[ks % kChains][0], qa[ks][0], qa[ks][1], b0, b1);
+        mma_rows8(sch[ks % kChains][1], qa[ks][0], qa[ks][1], b2, b3);
     }
+    float sacc[2][4];
+#pragma unroll
+    for (int n = 0; n < 2; ++n)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) sacc[n][c] = kSplit ? sch[0][n][c] + sch[kChains - 1][n][c] : sch[0][n][c];
     // Scores of this lane's head row for keys 8n + 2tq + {0, 1}.
     float sc[4];
 #pragma unroll
@@ -1601,10 +1612,10 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G, S>::kMinBlocks)
                 const int t_lo = max(0, it.tok0 - pg * kBlock);
                 const int t_hi = min(kBlock, it.tok1 - pg * kBlock);
                 if (t_lo == 0 && t_hi == kBlock)
-                    consume_page_mma<D, true>(kaddr, kaddr + C::kPageBytes, 0, kBlock, qa, p.qscale,
+                    consume_page_mma<D, true, (S > kRing)>(kaddr, kaddr + C::kPageBytes, 0, kBlock, qa, p.qscale,
                                               m_row, l_lane, oacc, lane);
                 else
-                    consume_page_mma<D, false>(kaddr, kaddr + C::kPageBytes, t_lo, t_hi, qa,
+                    consume_page_mma<D, false, (S > kRing)>(kaddr, kaddr + C::kPageBytes, t_lo, t_hi, qa,
                                                p.qscale, m_row, l_lane, oacc, lane);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[s]);
