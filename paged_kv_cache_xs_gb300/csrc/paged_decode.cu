@@ -654,14 +654,21 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t 
                  : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
                  : "r"(addr));
 }
-// d += a (16x16 bf16, rows 8-15 zero) * b (16x8 bf16): only a0/a2 (rows 0-7) given.
-__device__ __forceinline__ void mma_rows8(float (&d)[4], uint32_t a0, uint32_t a2, uint32_t b0,
-                                          uint32_t b1) {
+// d += a (16x16 bf16, row-major) * b (16x8 bf16, column-major), fp32 accumulate.
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                          uint32_t a3, uint32_t b0, uint32_t b1) {
     asm volatile(
         "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
         "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// Transpose of an 8x8 b16 matrix spread over the warp as in an mma
+// accumulator (thread t: row t/4, columns 2 (t%4) and 2 (t%4) + 1).
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
 }
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -674,70 +681,82 @@ __device__ __forceinline__ uint32_t page_addr(uint32_t base, int key, int d) {
 }
 
 // One page of the bf16 path for one consumer warp, on the tensor cores
-// (mma.sync m16n8k16): the G heads are rows 0..G-1 of the A operand (lane
-// quad g holds head g), the 16 keys two 8-column tiles.  S = q K^T in fp32,
-// online softmax in base 2 per head, then O += P V with P (bf16) repacked
-// from the S accumulators.  Keys outside [t_lo, t_hi) are masked out of S
-// and their V rows zeroed in the fragments (a slot past the sequence's end
-// may hold any bits).  qa: per 16-dim step, the head row's two bf16 pairs.
-// kSplit: Q K^T as two independent accumulator chains (even and odd
-// 16-dim steps) added at the end, halving the dependent MMA chain of a page
-// (for the deep-ring kernel, whose one CTA per SM leaves the registers).
+// (mma.sync m16n8k16), both products transposed so that the page's 16 keys
+// (and, for P V, 16 output dims) fill the 16 rows of A and the G query heads
+// are the 8 columns of B (rows G..7 of B zero):
+//   S^T = K q^T:      A = K (16 keys x 16 dims, ldmatrix), B = q^T (qa);
+//   O^T += V^T P^T:   A = V^T (16 dims x 16 keys, ldmatrix.trans), B = P^T;
+// one MMA per 16 dims for each product.  Thread t holds S^T for keys t/4 and
+// t/4 + 8 of heads 2 (t%4) and 2 (t%4) + 1, so a head's maximum is reduced
+// over the 8 threads with the same t % 4, and P^T moves from that layout to
+// the B layout with one movmatrix.trans per 8 keys.  O^T: oacc[dn] holds dims
+// 16 dn + t/4 and 16 dn + t/4 + 8 of heads 2 (t%4) (elements 0, 2) and
+// 2 (t%4) + 1 (elements 1, 3); m2, l2: the running maximum (base 2) and this
+// thread's share of the sum for those two heads.  Keys outside [t_lo, t_hi)
+// are masked out of S and their V entries zeroed in the fragments (a slot past
+// the sequence's end may hold any bits).  qa: per 16-dim step, row t/4 of q
+// (head t/4) as two bf16 pairs.  kSplit: Q K^T as two independent
+// accumulator chains (even and odd 16-dim steps) added at the end (for the
+// deep-ring kernel, whose one CTA per SM leaves the registers).
 template <int D, bool kFull, bool kSplit = false>
 __device__ __forceinline__ void consume_page_mma(uint32_t kaddr, uint32_t vaddr, int t_lo, int t_hi,
                                                  const uint32_t (&qa)[D / 16][2], float qscale,
-                                                 float &m_row, float &l_lane, float (&oacc)[D / 8][4],
-                                                 int lane) {
-    const int tq = lane & 3, mi = lane >> 3, ri = lane & 7;
+                                                 float (&m2)[2], float (&l2)[2],
+                                                 float (&oacc)[D / 16][4], int lane) {
+    const int tq = lane & 3, mi = lane >> 3, ri = lane & 7, kr = lane >> 2;
     constexpr int kChains = kSplit ? 2 : 1;
-    float sch[kChains][2][4];
+    float sch[kChains][4];
 #pragma unroll
     for (int k = 0; k < kChains; ++k)
 #pragma unroll
-        for (int n = 0; n < 2; ++n)
-#pragma unroll
-            for (int c = 0; c < 4; ++c) sch[k][n][c] = 0.f;
+        for (int c = 0; c < 4; ++c) sch[k][c] = 0.f;
 #pragma unroll
     for (int ks = 0; ks < D / 16; ++ks) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(page_addr<D>(kaddr, ((mi >> 1) << 3) + ri, 16 * ks + ((mi & 1) << 3)), b0, b1, b2,
-                b3);
-        mma_rows8(sch[ks % kChains][0], qa[ks][0], qa[ks][1], b0, b1);
-        mma_rows8(sch[ks % kChains][1], qa[ks][0], qa[ks][1], b2, b3);
+        // Tiles: keys 0-7 / dims 0-7, keys 0-7 / dims 8-15, keys 8-15 / dims
+        // 0-7, keys 8-15 / dims 8-15; A wants rows 0-7 k 0-7, rows 8-15 k 0-7,
+        // rows 0-7 k 8-15, rows 8-15 k 8-15.
+        uint32_t r0, r1, r2, r3;
+        ldsm_x4(page_addr<D>(kaddr, ((mi >> 1) << 3) + ri, 16 * ks + ((mi & 1) << 3)), r0, r1, r2,
+                r3);
+        mma_16816(sch[ks % kChains], r0, r2, r1, r3, qa[ks][0], qa[ks][1]);
     }
-    float sacc[2][4];
+    // s: (key kr, head 2tq), (kr, 2tq + 1), (kr + 8, 2tq), (kr + 8, 2tq + 1).
+    float s[4];
 #pragma unroll
-    for (int n = 0; n < 2; ++n)
+    for (int c = 0; c < 4; ++c) {
+        const float x = (kSplit ? sch[0][c] + sch[kChains - 1][c] : sch[0][c]) * qscale;
+        const int t = kr + ((c >> 1) << 3);
+        s[c] = (kFull || (t >= t_lo && t < t_hi)) ? x : -INFINITY;
+    }
+    float mx[2] = {fmaxf(s[0], s[2]), fmaxf(s[1], s[3])};
 #pragma unroll
-        for (int c = 0; c < 4; ++c) sacc[n][c] = kSplit ? sch[0][n][c] + sch[kChains - 1][n][c] : sch[0][n][c];
-    // Scores of this lane's head row for keys 8n + 2tq + {0, 1}.
-    float sc[4];
+    for (int o = 4; o <= 16; o <<= 1)
 #pragma unroll
-    for (int n = 0; n < 2; ++n)
+        for (int e = 0; e < 2; ++e) mx[e] = fmaxf(mx[e], __shfl_xor_sync(0xffffffffu, mx[e], o));
+    float ref[2], corr[2];
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-            const int t = 8 * n + 2 * tq + c;
-            const float x = sacc[n][c] * qscale;
-            sc[2 * n + c] = (kFull || (t >= t_lo && t < t_hi)) ? x : -INFINITY;
-        }
-    float mx = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-    const float m_new = fmaxf(m_row, mx);
-    const float ref = m_new == -INFINITY ? 0.f : m_new;
-    const float corr = fast_exp2(m_row - ref);
-    m_row = m_new;
+    for (int e = 0; e < 2; ++e) {
+        const float m_new = fmaxf(m2[e], mx[e]);
+        ref[e] = m_new == -INFINITY ? 0.f : m_new;
+        corr[e] = fast_exp2(m2[e] - ref[e]);
+        m2[e] = m_new;
+    }
     float pv[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) pv[i] = fast_exp2(sc[i] - ref);
-    l_lane = l_lane * corr + (pv[0] + pv[1] + pv[2] + pv[3]);
+    for (int c = 0; c < 4; ++c) pv[c] = fast_exp2(s[c] - ref[c & 1]);
 #pragma unroll
-    for (int n = 0; n < D / 8; ++n) {
-        oacc[n][0] *= corr;
-        oacc[n][1] *= corr;
+    for (int e = 0; e < 2; ++e) l2[e] = l2[e] * corr[e] + (pv[e] + pv[e + 2]);
+#pragma unroll
+    for (int dn = 0; dn < D / 16; ++dn) {
+        oacc[dn][0] *= corr[0];
+        oacc[dn][1] *= corr[1];
+        oacc[dn][2] *= corr[0];
+        oacc[dn][3] *= corr[1];
     }
-    const uint32_t pa0 = pack_bf16x2(pv[0], pv[1]), pa2 = pack_bf16x2(pv[2], pv[3]);
-    // V fragment masks: key 2tq + {0,1} (low, high half), and +8.
+    // P^T in the B layout: keys 0-7, then keys 8-15.
+    const uint32_t pb0 = movmatrix_trans(pack_bf16x2(pv[0], pv[1]));
+    const uint32_t pb1 = movmatrix_trans(pack_bf16x2(pv[2], pv[3]));
+    // V fragment masks: keys 2tq + {0,1} (low, high half), and +8.
     uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
     if (!kFull) {
         const int k = 2 * tq;
@@ -747,11 +766,13 @@ __device__ __forceinline__ void consume_page_mma(uint32_t kaddr, uint32_t vaddr,
     }
 #pragma unroll
     for (int dn = 0; dn < D / 16; ++dn) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(page_addr<D>(vaddr, ((mi & 1) << 3) + ri, 16 * dn + ((mi >> 1) << 3)), b0, b1, b2,
-                  b3);
-        mma_rows8(oacc[2 * dn], pa0, pa2, b0 & mlo, b1 & mhi);
-        mma_rows8(oacc[2 * dn + 1], pa0, pa2, b2 & mlo, b3 & mhi);
+        // Transposed tiles (same addresses as for K): V^T dims 0-7 / keys 0-7,
+        // dims 8-15 / keys 0-7, dims 0-7 / keys 8-15, dims 8-15 / keys 8-15 -
+        // already the A order.
+        uint32_t v0, v1, v2, v3;
+        ldsm_x4_t(page_addr<D>(vaddr, ((mi >> 1) << 3) + ri, 16 * dn + ((mi & 1) << 3)), v0, v1, v2,
+                  v3);
+        mma_16816(oacc[dn], v0 & mlo, v1 & mlo, v2 & mhi, v3 & mhi, pb0, pb1);
     }
 }
 
@@ -1592,10 +1613,10 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G, S>::kMinBlocks)
                 it.b = -1;
                 it.pg0 = it.pg1 = 0;
             }
-            float m_row = -INFINITY, l_lane = 0.f;
-            float oacc[D / 8][4];
+            float m2[2] = {-INFINITY, -INFINITY}, l2[2] = {0.f, 0.f};
+            float oacc[D / 16][4];
 #pragma unroll
-            for (int n = 0; n < D / 8; ++n)
+            for (int n = 0; n < D / 16; ++n)
 #pragma unroll
                 for (int c = 0; c < 4; ++c) oacc[n][c] = 0.f;
             const int first = (cw - static_cast<int>(page_ctr % kConsumerWarps) + kConsumerWarps) %
@@ -1612,11 +1633,11 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G, S>::kMinBlocks)
                 const int t_lo = max(0, it.tok0 - pg * kBlock);
                 const int t_hi = min(kBlock, it.tok1 - pg * kBlock);
                 if (t_lo == 0 && t_hi == kBlock)
-                    consume_page_mma<D, true, (S > kRing)>(kaddr, kaddr + C::kPageBytes, 0, kBlock, qa, p.qscale,
-                                              m_row, l_lane, oacc, lane);
+                    consume_page_mma<D, true, (S > kRing)>(kaddr, kaddr + C::kPageBytes, 0, kBlock, qa,
+                                                           p.qscale, m2, l2, oacc, lane);
                 else
-                    consume_page_mma<D, false, (S > kRing)>(kaddr, kaddr + C::kPageBytes, t_lo, t_hi, qa,
-                                               p.qscale, m_row, l_lane, oacc, lane);
+                    consume_page_mma<D, false, (S > kRing)>(kaddr, kaddr + C::kPageBytes, t_lo, t_hi,
+                                                            qa, p.qscale, m2, l2, oacc, lane);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[s]);
             }
@@ -1640,16 +1661,27 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G, S>::kMinBlocks)
             float *cL = cM + kConsumerWarps * G;
             float *cO = cL + kConsumerWarps * G;
             if (cw == 0 && lane == 0) *reinterpret_cast<Item *>(mb) = it;
-            float l_row = l_lane + __shfl_xor_sync(0xffffffffu, l_lane, 1);
-            l_row += __shfl_xor_sync(0xffffffffu, l_row, 2);
-            if (!done && grp < G) {
-                float *dst = &cO[(cw * G + grp) * D + 2 * tq];
+            // Each head's sum: the shares of the 8 threads that hold it.
+            float lsum[2] = {l2[0], l2[1]};
 #pragma unroll
-                for (int n = 0; n < D / 8; ++n)
-                    *reinterpret_cast<float2 *>(dst + 8 * n) = make_float2(oacc[n][0], oacc[n][1]);
-                if (tq == 0) {
-                    cM[grp * kConsumerWarps + cw] = m_row;
-                    cL[grp * kConsumerWarps + cw] = l_row;
+            for (int o = 4; o <= 16; o <<= 1)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) lsum[e] += __shfl_xor_sync(0xffffffffu, lsum[e], o);
+            if (!done) {
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int h = 2 * tq + e;
+                    if (h >= G) continue;
+                    float *dst = &cO[(cw * G + h) * D + grp];
+#pragma unroll
+                    for (int dn = 0; dn < D / 16; ++dn) {
+                        dst[16 * dn] = oacc[dn][e];
+                        dst[16 * dn + 8] = oacc[dn][e + 2];
+                    }
+                    if (grp == 0) {
+                        cM[h * kConsumerWarps + cw] = m2[e];
+                        cL[h * kConsumerWarps + cw] = lsum[e];
+                    }
                 }
             }
             if (!hand_over(it, mb, buf, item_ctr, done)) break;
