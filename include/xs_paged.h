@@ -440,6 +440,14 @@ int xs_paged_decode_sinks(void *out, float *part_o, float *part_m, float *part_l
  *  - combine: each item of a split (sequence, KV head) writes its partials,
  *    then counts itself in; the item that completes the group merges the
  *    group's partials for the G query heads into out.
+ *  - small launches (xs_paged_decode_step_cluster_size > 0: bf16, D = 128,
+ *    every (sequence, KV head) group in one wave of thread-block clusters)
+ *    run one cluster per group instead: its CTAs split the group's tokens
+ *    into their own partitions (partition_tokens is not used), and the
+ *    split-K combine reads the CTAs' partials from distributed shared
+ *    memory, so part_o/part_m/part_l and the counters are not touched (they
+ *    must still be valid).  The result is the same up to the order of the
+ *    fp32 sums.
  *
  * counters: int32 on the device, xs_paged_decode_step_counters(B, Hkv) of
  * them (2 + B * Hkv: the work-item counters, then one arrival count per
@@ -462,7 +470,8 @@ int xs_paged_decode_step(void *out, const void *q, const void *k_new, const void
 
 /*
  * xs_paged_decode_step_ex - xs_paged_decode_step with launch flags (flags 0
- * is xs_paged_decode_step).  Unknown flag bits are XS_EUNSUPPORTED.
+ * is xs_paged_decode_step; XS_STEP_EARLY_READS and XS_STEP_PERSISTENT may be
+ * combined).  Unknown flag bits are XS_EUNSUPPORTED.
  *
  * XS_STEP_EARLY_READS: the launch is made programmatically dependent on the
  * previous kernel on the stream (as every launch of this library is), and
@@ -486,6 +495,13 @@ int xs_paged_decode_step(void *out, const void *q, const void *k_new, const void
  * only that launch can still be running.)
  */
 #define XS_STEP_EARLY_READS 1
+/*
+ * XS_STEP_PERSISTENT: run the persistent grid (partials in part_o/part_m/
+ * part_l, counted through the counters) even where the launch would run as
+ * clusters (xs_paged_decode_step_cluster_size > 0).  Same result up to the
+ * order of the fp32 sums.
+ */
+#define XS_STEP_PERSISTENT 2
 int xs_paged_decode_step_ex(void *out, const void *q, const void *k_new, const void *v_new,
                             void *k_cache, void *v_cache, const int32_t *block_tables,
                             int max_blocks_per_seq, const int32_t *context_lens, const void *sinks,
@@ -508,6 +524,20 @@ int xs_paged_decode_step_ex(void *out, const void *q, const void *k_new, const v
  */
 int xs_paged_decode_step_partition_tokens(int B, int Hq, int Hkv, int64_t total_context_tokens,
                                           int max_context_len, int num_sms);
+
+/*
+ * xs_paged_decode_step_cluster_size - the cluster size (2..16) with which
+ * xs_paged_decode_step / _ex runs a launch of this shape on the current
+ * device, or 0 when it runs the persistent grid.  Clusters are used for bf16,
+ * D = 128, when the tokens a sequence can hold (max_blocks_per_seq * 16, or
+ * the window when smaller) split into at most 16 partitions of at most 24
+ * pages (23 with a window) and all B * Hkv clusters fit the device at once;
+ * the largest such size is taken (at most one CTA per 64 tokens).  Only the
+ * shape decides: B, Hq, Hkv, D, max_blocks_per_seq, window and dtype are
+ * those of the step.  XS_ESHAPE for a negative size, Hq % Hkv != 0.
+ */
+int xs_paged_decode_step_cluster_size(int B, int Hq, int Hkv, int D, int max_blocks_per_seq,
+                                      int window, int dtype);
 
 /*
  * xs_paged_decode_step_counters - how many int32 counters

@@ -1821,6 +1821,338 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G, S>::kMinBlocks)
     exit_role();
 }
 
+// ---------------------------------------------------------------- cluster step
+//
+// A one-launch step whose (sequence, KV head) groups all fit one wave of
+// thread-block clusters runs as one cluster per group instead of the
+// persistent grid: CTA r of the cluster takes partition r of the group's
+// tokens, copies all of its pages into shared memory at once (one warp
+// issues them, one lane per page) and eight consumer warps attend over them
+// (consume_page_mma).  The consumers' eight states are merged into the CTA's
+// partial (m, l, unnormalised o per head) in its own shared memory; after a
+// cluster barrier every CTA combines a slice of the group's output from all
+// partials, read over distributed shared memory:
+//     out = sum_r 2^(m_r - M) o_r / (sum_r 2^(m_r - M) l_r  [+ 2^(sink - M)])
+// (flash-decoding's split-K combine).  No partial leaves the GPC and no
+// count goes through global memory, which is what a small launch's latency
+// is made of.  A second cluster barrier keeps every CTA's shared memory
+// alive until the others have read it.  Every wait is bounded; a wait that
+// runs out raises XS_FLAG_TIMEOUT, and every thread still reaches both
+// cluster barriers, so no CTA waits for one that left.
+constexpr int kCluConsumers = 8;
+constexpr int kCluThreads = 32 * (1 + kCluConsumers);  // producer + consumers
+constexpr int kCluMaxPages = 24;  // pages of one partition, all resident at once
+constexpr int kCluMaxSize = 16;   // CTAs per cluster (the non-portable maximum)
+
+template <int D, int G>
+struct CluCfg {
+    static constexpr int kRowBytes = D * 2;
+    static constexpr int kPageBytes = kBlock * kRowBytes;
+    static constexpr int kStageBytes = 2 * kPageBytes;  // K page, then V page (swizzled)
+    static constexpr int kQOff = kCluMaxPages * kStageBytes;
+    // The CTA's partial: m[8], l[8], o[G][D] (fp32, o not divided by l).
+    // A consumer's state has the same layout and goes in the consumer's
+    // first stage, which only it ever reads.
+    static constexpr int kPartOff = kQOff + G * kRowBytes;
+    static constexpr int kPartBytes = 64 + G * D * 4;
+    static constexpr int kBarOff = kPartOff + kPartBytes;
+    static constexpr int kBarBytes = (kCluMaxPages + 1) * 8;  // pages, then q
+    static constexpr int kAlignSlack = 1024;  // the stages are 1024-byte aligned
+    static constexpr int kBytes = kBarOff + kBarBytes + kAlignSlack;
+    static_assert(kPartBytes <= kStageBytes, "a consumer state fits its stage");
+    static_assert(kCluMaxPages >= kCluConsumers && kCluMaxPages <= 32, "one lane per page");
+    static_assert(kPartOff % 16 == 0 && kBarOff % 8 == 0, "float4 partial rows, 8-byte barriers");
+};
+
+__device__ __forceinline__ void cluster_barrier() {
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+// The address of a shared-memory location in cluster CTA `rank`.
+__device__ __forceinline__ uint32_t dsmem_map(uint32_t local, uint32_t rank) {
+    uint32_t a;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(local), "r"(rank));
+    return a;
+}
+__device__ __forceinline__ float dsmem_ld_f32(uint32_t a) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
+    return v;
+}
+__device__ __forceinline__ float4 dsmem_ld_v4(uint32_t a) {
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(a)
+                 : "memory");
+    return v;
+}
+
+// Grid (cluster size, B * Hkv), clusters along x: blockIdx.y = b * Hkv + g,
+// blockIdx.x = the partition.  p.P is the partition length (a multiple of
+// 16, at most kCluMaxPages pages, one fewer with a window, whose start need
+// not fall on a page); the host picked it so that gridDim.x partitions
+// cover every sequence.
+template <int D, int G>
+__global__ void __launch_bounds__(kCluThreads, 1)
+    paged_decode_cluster_kernel(const __grid_constant__ CUtensorMap tmk,
+                                const __grid_constant__ CUtensorMap tmv, const Params p) {
+    using C = CluCfg<D, G>;
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    unsigned char *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::kBarOff);
+    uint64_t *qbar = full + kCluMaxPages;
+    float *part = reinterpret_cast<float *>(smem + C::kPartOff);
+    __shared__ int s_abort;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int r = blockIdx.x, cs = gridDim.x;
+    const int b = blockIdx.y / p.Hkv, g = blockIdx.y - b * p.Hkv;
+    // Uniform over the launch, so every CTA of every cluster returns here
+    // together (before any cluster barrier).
+    if (dynamic_smem_bytes() < static_cast<uint32_t>(C::kBytes) || b >= p.B) {
+        if (tid == 0) raise_flag(p.err_flag, XS_FLAG_CONFIG);
+        return;
+    }
+    if (tid == 0) {
+        for (int i = 0; i <= kCluMaxPages; ++i) mbar_init(&full[i], 1);  // (full[24] = qbar)
+        mbar_fence_init();
+        s_abort = 0;
+    }
+    __syncthreads();
+    // This CTA's tokens [tok0, tok1) of the window [first_token, n), its
+    // pages [pg0, pg0 + np).  Lengths are read after the launch wait, or
+    // before it with p.early (the caller promises the previous launch does
+    // not write them).
+    auto range = [&](int n, int &tok0, int &tok1, int &pg0, int &np) {
+        tok0 = first_token(p, n) + r * p.P;
+        tok1 = min(n, tok0 + p.P);
+        pg0 = tok0 / kBlock;
+        np = tok1 > tok0 ? (tok1 + kBlock - 1) / kBlock - pg0 : 0;
+    };
+    if (warp == 0) {
+        // ======================================================== producer
+        if (!p.early) {
+            griddep_wait();
+            griddep_launch_dependents();
+        }
+        const int n = seq_len(p, b, r == 0 && g == 0 && lane == 0);
+        int tok0, tok1, pg0, np;
+        range(n, tok0, tok1, pg0, np);
+        if (np > kCluMaxPages) np = 0;  // (the host's choice of p.P rules this out)
+        // The page holding the sequence's last token receives this step's
+        // row: it is copied after the row is written (and only when the
+        // length is within the table, as in the separate append).
+        const int raw_len = p.k_new && tok1 == n && np > 0 ? p.context_lens[b] : 0;
+        const bool appends = raw_len == n && n > 0;
+        const int last = appends ? np - 1 : -1;
+        int32_t blk = 0;
+        if (lane < np) blk = p.block_tables[static_cast<int64_t>(b) * p.table_stride + pg0 + lane];
+        const bool bad_id = lane < np && (blk < 0 || blk >= p.num_blocks);
+        if (__any_sync(0xffffffffu, bad_id) && lane == 0) raise_flag(p.err_flag, XS_FLAG_BAD_BLOCK);
+        // An id outside the pool reads block 0 instead (flagged) and takes no
+        // appended row.
+        const bool appends_ok = appends && !__shfl_sync(0xffffffffu, bad_id, max(last, 0));
+        if (bad_id) blk = 0;
+        const uint64_t pol = policy_evict_first();
+        // Lane i issues page i's two copies.  (The debug library can skip
+        // one page of CTA (0, 0) to make a consumer's wait run out.)
+        const bool skip = blockIdx.y == 0 && skip_page(static_cast<uint32_t>(lane));
+        auto issue = [&](bool pred) {
+            if (!pred || skip) return;
+            const uint32_t dk = smem_addr(smem + lane * C::kStageBytes);
+            mbar_arrive_expect_tx(&full[lane], 2 * C::kPageBytes);
+            tma_load_4d(dk, &tmk, blk * p.Hkv + g, &full[lane], pol);
+            tma_load_4d(dk + C::kPageBytes, &tmv, blk * p.Hkv + g, &full[lane], pol);
+        };
+        issue(lane < np && lane != last);
+        if (p.early) {
+            griddep_wait();
+            griddep_launch_dependents();
+        }
+        if (np > 0 && lane == 0) {
+            mbar_arrive_expect_tx(qbar, C::kRowBytes * G);
+            bulk_g2s(smem + C::kQOff,
+                     static_cast<const unsigned char *>(p.q) +
+                         (static_cast<int64_t>(b) * p.Hq + static_cast<int64_t>(g) * G) * C::kRowBytes,
+                     C::kRowBytes * G, qbar);
+        }
+        if (appends) {
+            // K row then V row, one 16-byte chunk per lane, into slot (n - 1)
+            // of the last page; then the generic-proxy writes are ordered
+            // before the tensor copy that reads the page.
+            constexpr int kChunks = C::kRowBytes / 16;
+            const int32_t lblk = __shfl_sync(0xffffffffu, blk, last);
+            const int64_t row = static_cast<int64_t>(b) * p.Hkv + g;
+            const int64_t dst = ((static_cast<int64_t>(lblk) * p.Hkv + g) * kBlock + (n - 1) % kBlock) *
+                                kChunks;
+            for (int c = lane; appends_ok && c < 2 * kChunks; c += 32) {
+                const bool is_k = c < kChunks;
+                const int cc = is_k ? c : c - kChunks;
+                const uint4 v = static_cast<const uint4 *>(is_k ? p.k_new : p.v_new)[row * kChunks + cc];
+                static_cast<uint4 *>(const_cast<void *>(is_k ? p.k_cache : p.v_cache))[dst + cc] = v;
+            }
+            fence_proxy_async_global();
+            __syncwarp();
+            issue(lane == last);
+        }
+        // Every copy issued lands before the CTA can exit: in the normal
+        // path the consumers have waited for all of them; after an abort
+        // this wait (bounded) covers the ones they gave up on.  Done after
+        // the first cluster barrier, when the consumers are finished.
+        cluster_barrier();
+        if (lane < np && !skip) mbar_wait_bounded(&full[lane], 0, wait_limit());
+        if (np > 0 && lane == 0) mbar_wait_bounded(qbar, 0, wait_limit());
+    } else {
+        // ======================================================== consumers
+        griddep_wait();
+        griddep_launch_dependents();
+        const int cw = warp - 1;
+        const int n = seq_len(p, b, false);
+        int tok0, tok1, pg0, np;
+        range(n, tok0, tok1, pg0, np);
+        if (np > kCluMaxPages) np = 0;
+        const int grp = lane >> 2, tq = lane & 3;
+        float m2[2] = {-INFINITY, -INFINITY}, l2[2] = {0.f, 0.f};
+        float oacc[D / 16][4];
+#pragma unroll
+        for (int i = 0; i < D / 16; ++i)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) oacc[i][c] = 0.f;
+        if (cw < np) {
+            bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(qbar, 0, wait_limit()));
+            uint32_t qa[D / 16][2];
+            const unsigned char *qs = smem + C::kQOff + (grp < G ? grp : 0) * C::kRowBytes;
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks) {
+                const unsigned char *row = qs + (16 * ks + 2 * tq) * 2;
+                qa[ks][0] = grp < G ? *reinterpret_cast<const uint32_t *>(row) : 0u;
+                qa[ks][1] = grp < G ? *reinterpret_cast<const uint32_t *>(row + 16) : 0u;
+            }
+            for (int i = cw; ok && i < np; i += kCluConsumers) {
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(&full[i], 0, wait_limit())) ||
+                    *static_cast<volatile int *>(&s_abort)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t kaddr = smem_addr(smem + i * C::kStageBytes);
+                const int pg = pg0 + i;
+                const int t_lo = max(0, tok0 - pg * kBlock);
+                const int t_hi = min(kBlock, tok1 - pg * kBlock);
+                if (t_lo == 0 && t_hi == kBlock)
+                    consume_page_mma<D, true, true>(kaddr, kaddr + C::kPageBytes, 0, kBlock, qa,
+                                                    p.qscale, m2, l2, oacc, lane);
+                else
+                    consume_page_mma<D, false, true>(kaddr, kaddr + C::kPageBytes, t_lo, t_hi, qa,
+                                                     p.qscale, m2, l2, oacc, lane);
+            }
+            if (!ok && lane == 0) {
+                raise_flag(p.err_flag, XS_FLAG_TIMEOUT);
+                atomicExch(&s_abort, 1);
+            }
+        }
+        // This consumer's state into its own stage (its first page, consumed).
+        float lsum[2] = {l2[0], l2[1]};
+#pragma unroll
+        for (int o = 4; o <= 16; o <<= 1)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) lsum[e] += __shfl_xor_sync(0xffffffffu, lsum[e], o);
+        float *st = reinterpret_cast<float *>(smem + cw * C::kStageBytes);
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int h = 2 * tq + e;
+            if (h >= G) continue;
+            float *dst = st + 16 + h * D + grp;
+#pragma unroll
+            for (int dn = 0; dn < D / 16; ++dn) {
+                dst[16 * dn] = oacc[dn][e];
+                dst[16 * dn + 8] = oacc[dn][e + 2];
+            }
+            if (grp == 0) {
+                st[h] = m2[e];
+                st[8 + h] = lsum[e];
+            }
+        }
+        named_barrier_sync(1, 32 * kCluConsumers);
+        // The eight states merged into the CTA's partial, a float4 of one
+        // head per thread.
+        for (int c = tid - 32; c < G * D / 4; c += 32 * kCluConsumers) {
+            const int h = c / (D / 4), d = (c - h * (D / 4)) * 4;
+            float mx = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < kCluConsumers; ++w)
+                mx = fmaxf(mx, reinterpret_cast<const float *>(smem + w * C::kStageBytes)[h]);
+            const float ref = mx == -INFINITY ? 0.f : mx;
+            float lt = 0.f;
+            float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int w = 0; w < kCluConsumers; ++w) {
+                const float *sw = reinterpret_cast<const float *>(smem + w * C::kStageBytes);
+                const float f = fast_exp2(sw[h] - ref);  // 0 for a consumer with no pages
+                lt += f * sw[8 + h];
+                const float4 v = *reinterpret_cast<const float4 *>(sw + 16 + h * D + d);
+                o.x += f * v.x;
+                o.y += f * v.y;
+                o.z += f * v.z;
+                o.w += f * v.w;
+            }
+            *reinterpret_cast<float4 *>(part + 16 + h * D + d) = o;
+            if (d == 0) {
+                part[h] = mx;
+                part[8 + h] = lt;
+            }
+        }
+        cluster_barrier();
+    }
+    // ============================================================ combine
+    // Every partial of the group is in place.  This CTA writes float4
+    // chunks r, r + cs, ... of the group's G x D outputs; a half-warp per
+    // chunk, lane j of it reading partial j.
+    {
+        constexpr int kChunks = G * D / 4;
+        constexpr int kHalves = 2 * (kCluThreads / 32);
+        const int j = lane & 15;
+        const int n = seq_len(p, b, false);
+        const uint32_t remote = dsmem_map(smem_addr(part), static_cast<uint32_t>(j < cs ? j : 0));
+        for (int k0 = 2 * warp; r + k0 * cs < kChunks; k0 += kHalves) {
+            const int c = r + (k0 + (lane >> 4)) * cs;
+            const bool valid = c < kChunks;
+            const int h = valid ? c / (D / 4) : 0, d = valid ? (c - h * (D / 4)) * 4 : 0;
+            float mj = -INFINITY, lj = 0.f;
+            float4 oj = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (valid && j < cs) {
+                mj = dsmem_ld_f32(remote + 4 * h);
+                lj = dsmem_ld_f32(remote + 4 * (8 + h));
+                oj = dsmem_ld_v4(remote + 4 * (16 + h * D + d));
+            }
+            float mx = mj;
+#pragma unroll
+            for (int o = 1; o < 16; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            const float ref = mx == -INFINITY ? 0.f : mx;
+            const float f = fast_exp2(mj - ref);
+            float s[5] = {f * lj, f * oj.x, f * oj.y, f * oj.z, f * oj.w};
+#pragma unroll
+            for (int o = 1; o < 16; o <<= 1)
+#pragma unroll
+                for (int e = 0; e < 5; ++e) s[e] += __shfl_xor_sync(0xffffffffu, s[e], o);
+            if (valid && j == 0) {
+                float den = s[0];
+                if (p.sinks)
+                    den += fast_exp2(Elem<__nv_bfloat16>::to_f32(
+                                         static_cast<const __nv_bfloat16 *>(p.sinks)[g * G + h]) *
+                                         kLog2e -
+                                     ref);
+                // A sequence with no tokens produces zeros.
+                const float inv = n > 0 ? 1.f / den : 0.f;
+                const float o4[4] = {s[1] * inv, s[2] * inv, s[3] * inv, s[4] * inv};
+                store_row<__nv_bfloat16, 4>(
+                    static_cast<__nv_bfloat16 *>(p.out) +
+                        (static_cast<int64_t>(b) * p.Hq + static_cast<int64_t>(g) * G + h) * D + d,
+                    o4);
+            }
+        }
+    }
+    cluster_barrier();  // no CTA leaves while another may still read its partial
+}
+
 // Split-K combine: one CTA of D threads per (sequence, query head).
 // With sinks, a sink is one more logit (no value row) in the denominator;
 // with a window, only the last `window` tokens were split into partitions.
@@ -1893,6 +2225,96 @@ KernelFn pick_kernel(int dtype, int D, int G, bool deep, int *smem_base_fn_B0) {
 #undef XS_PICK
 #undef XS_PICK_DEEP
     return nullptr;
+}
+
+template <int D, int G>
+KernelFn cluster_kernel_for() {
+    return paged_decode_cluster_kernel<D, G>;
+}
+
+// The cluster-step kernel for a shape (bf16, D = 128) and its dynamic shared
+// memory, or null.
+KernelFn pick_cluster_kernel(int D, int G, int *smem) {
+#define XS_PICK_CLU(DD, GG)                                                          \
+    if (D == DD && G == GG) {                                                        \
+        *smem = CluCfg<DD, GG>::kBytes;                                              \
+        return cluster_kernel_for<DD, GG>();                                         \
+    }
+    XS_PICK_CLU(128, 1) XS_PICK_CLU(128, 2) XS_PICK_CLU(128, 4) XS_PICK_CLU(128, 8)
+#undef XS_PICK_CLU
+    return nullptr;
+}
+
+// Clusters of `cs` CTAs of a cluster-step kernel that an idle device holds at
+// once (0 if none, or if a query failed), cached per (kernel, device, cs).
+int cluster_capacity(KernelFn fn, int smem, int cs) {
+    struct Entry {
+        KernelFn fn;
+        int dev, cs, n;
+    };
+    static std::mutex mu;
+    static Entry cache[64];
+    static int n_cached = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    bool configured = false;
+    for (int i = 0; i < n_cached; ++i) {
+        if (cache[i].fn == fn && cache[i].dev == dev && cache[i].cs == cs) return cache[i].n;
+        configured |= cache[i].fn == fn && cache[i].dev == dev;
+    }
+    int n = 0;
+    const void *f = reinterpret_cast<const void *>(fn);
+    if (configured ||
+        (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) == cudaSuccess &&
+         cudaFuncSetAttribute(f, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess)) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(cs, 1);
+        cfg.blockDim = dim3(kCluThreads);
+        cfg.dynamicSmemBytes = smem;
+        cudaLaunchAttribute a[1];
+        a[0].id = cudaLaunchAttributeClusterDimension;
+        a[0].val.clusterDim.x = cs;
+        a[0].val.clusterDim.y = 1;
+        a[0].val.clusterDim.z = 1;
+        cfg.attrs = a;
+        cfg.numAttrs = 1;
+        if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) n = 0;
+    }
+    cudaGetLastError();  // do not leave a failed query for an unrelated later check
+    if (n_cached < 64) cache[n_cached++] = Entry{fn, dev, cs, n};
+    return n;
+}
+
+// Whether a one-launch step runs as clusters (paged_decode_cluster_kernel):
+// bf16, D = 128, and every (sequence, KV head) group's tokens - at most the
+// table's reach, or the window - split into cs partitions of at most
+// kCluMaxPages pages (one fewer with a window) with all B * Hkv clusters
+// resident at once.  The largest such cs up to 16 (and no more than one
+// partition per 64 tokens) is taken: the fewer pages a CTA holds, the
+// shorter the launch.  Returns cs (0: the persistent grid) and sets the
+// partition length, kernel and shared memory.
+int cluster_plan(int B, int Hkv, int D, int G, int max_blocks, int window, int dtype, int *P,
+                 KernelFn *fn, int *smem) {
+    if (dtype != XS_BF16 || static_cast<int64_t>(B) * Hkv > 65535) return 0;
+    *fn = pick_cluster_kernel(D, G, smem);
+    if (!*fn) return 0;
+    int64_t L = static_cast<int64_t>(max_blocks) * kBlock;
+    if (window > 0) L = std::min<int64_t>(L, window);
+    const int spare = window > 0 ? 1 : 0;  // a window's first token need not start a page
+    int cs = static_cast<int>(std::min<int64_t>(kCluMaxSize, (L + 63) / 64));
+    for (; cs >= 2; --cs) {
+        const int64_t part = ((L + cs - 1) / cs + kBlock - 1) / kBlock * kBlock;
+        if (part / kBlock + spare > kCluMaxPages) return 0;  // fewer CTAs only add pages
+        if (static_cast<int64_t>(B) * Hkv <= cluster_capacity(*fn, *smem, cs)) {
+            *P = static_cast<int>(part);
+            return cs;
+        }
+    }
+    return 0;
 }
 
 struct DeviceInfo {
@@ -2204,7 +2626,8 @@ static int launch_attn(void *out, float *part_o, float *part_m, float *part_l, c
                        const void *sinks, int window, int partition_tokens, int max_partitions,
                        int dtype, int *err_flag, int *work_counters, cudaStream_t stream,
                        int prefill_start = -1, const void *k_new = nullptr,
-                       const void *v_new = nullptr, int *combine = nullptr, int early = 0) {
+                       const void *v_new = nullptr, int *combine = nullptr, int early = 0,
+                       bool allow_cluster = true) {
     if (window < 0) return XS_ESHAPE;
     const bool prefill = prefill_start >= 0;
     int st = check_attn_args(out, part_o, part_m, part_l, q, k_cache, v_cache, block_tables,
@@ -2214,20 +2637,28 @@ static int launch_attn(void *out, float *part_o, float *part_m, float *part_l, c
     if (B == 0) return XS_OK;
     attn::DeviceInfo dev;
     if ((st = attn::device_info(&dev)) != XS_OK) return st;
-    int smem0 = 0;
-    // At most one work item per SM: one CTA per SM with the deep ring.
-    const bool deep = static_cast<int64_t>(B) * Hkv * max_partitions <= dev.sms;
-    attn::KernelFn fn = attn::pick_kernel(dtype, D, Hq / Hkv, deep, &smem0);
-    if (!fn) return XS_EUNSUPPORTED;
-    int smem = smem0 + attn::table_bytes(B) + 1024;  // = Cfg<...>::smem_bytes(B)
-    if (smem + 1024 > dev.max_smem_optin) return XS_EUNSUPPORTED;  // room for static smem
+    // A step small enough for one wave of clusters runs as clusters.
+    attn::KernelFn fn = nullptr;
+    int smem = 0, cluster = 0, cluster_P = 0;
+    if (combine && !prefill && allow_cluster)
+        cluster = attn::cluster_plan(B, Hkv, D, Hq / Hkv, max_blocks_per_seq, window, dtype,
+                                     &cluster_P, &fn, &smem);
     int per_sm = 1;
-    if ((st = attn::occupancy(fn, smem, &per_sm)) != XS_OK) return st;
+    if (!cluster) {
+        int smem0 = 0;
+        // At most one work item per SM: one CTA per SM with the deep ring.
+        const bool deep = static_cast<int64_t>(B) * Hkv * max_partitions <= dev.sms;
+        fn = attn::pick_kernel(dtype, D, Hq / Hkv, deep, &smem0);
+        if (!fn) return XS_EUNSUPPORTED;
+        smem = smem0 + attn::table_bytes(B) + 1024;  // = Cfg<...>::smem_bytes(B)
+        if (smem + 1024 > dev.max_smem_optin) return XS_EUNSUPPORTED;  // room for static smem
+        if ((st = attn::occupancy(fn, smem, &per_sm)) != XS_OK) return st;
+    }
     // The in-launch combine stages partial rows in shared memory: as many
     // partials (G rows of D fp32 each) as fit beside the CTAs that are
     // resident anyway, at least one, at most 32 or 32 KB.
     int stage_bytes = 0, stage_parts = 0;
-    if (combine) {
+    if (combine && !cluster) {
         int st_smem = 0;
         if ((st = attn::static_smem(fn, &st_smem)) != XS_OK) return st;
         const int part_bytes = Hq / Hkv * D * 4;
@@ -2288,11 +2719,23 @@ static int launch_attn(void *out, float *part_o, float *part_m, float *part_l, c
     cfg.blockDim = dim3(attn::kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    if (cluster) {
+        // One cluster of `cluster` CTAs per (sequence, KV head).
+        p.P = cluster_P;
+        p.max_parts = cluster;
+        cfg.gridDim = dim3(cluster, B * Hkv);
+        cfg.blockDim = dim3(attn::kCluThreads);
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = cluster;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
+    }
     if (cudaLaunchKernelEx(&cfg, fn, tmk, tmv, p) != cudaSuccess) {
         cudaGetLastError();
         return XS_ELAUNCH;
@@ -2423,7 +2866,7 @@ extern "C" int xs_paged_decode_step_ex(void *out, const void *q, const void *k_n
                                        int max_partitions, float *part_o, float *part_m,
                                        float *part_l, int *counters, int flags, int dtype,
                                        int *err_flag, cudaStream_t stream) {
-    if (flags & ~XS_STEP_EARLY_READS) return XS_EUNSUPPORTED;
+    if (flags & ~(XS_STEP_EARLY_READS | XS_STEP_PERSISTENT)) return XS_EUNSUPPORTED;
     if (!k_new != !v_new) return XS_ENULL;
     if (!counters) return XS_EWORKSPACE;
     if (k_new && (!aligned16(k_new) || !aligned16(v_new))) return XS_EALIGN;
@@ -2431,7 +2874,7 @@ extern "C" int xs_paged_decode_step_ex(void *out, const void *q, const void *k_n
                        max_blocks_per_seq, context_lens, B, Hq, Hkv, D, block_size, num_blocks,
                        scale, sinks, window, partition_tokens, max_partitions, dtype, err_flag,
                        counters, stream, -1, k_new, v_new, counters + 2,
-                       (flags & XS_STEP_EARLY_READS) ? 1 : 0);
+                       (flags & XS_STEP_EARLY_READS) ? 1 : 0, !(flags & XS_STEP_PERSISTENT));
 }
 
 extern "C" int xs_paged_decode_step(void *out, const void *q, const void *k_new,
@@ -2448,6 +2891,17 @@ extern "C" int xs_paged_decode_step(void *out, const void *q, const void *k_new,
                                    block_size, num_blocks, scale, partition_tokens,
                                    max_partitions, part_o, part_m, part_l, counters, 0, dtype,
                                    err_flag, stream);
+}
+
+extern "C" int xs_paged_decode_step_cluster_size(int B, int Hq, int Hkv, int D,
+                                                 int max_blocks_per_seq, int window, int dtype) {
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || max_blocks_per_seq < 0 || window < 0)
+        return XS_ESHAPE;
+    if (B == 0) return 0;
+    int P = 0, smem = 0;
+    attn::KernelFn fn = nullptr;
+    return attn::cluster_plan(B, Hkv, D, Hq / Hkv, max_blocks_per_seq, window, dtype, &P, &fn,
+                              &smem);
 }
 
 extern "C" int64_t xs_paged_decode_step_counters(int B, int Hkv) {

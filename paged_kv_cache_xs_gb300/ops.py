@@ -69,6 +69,7 @@ SIGNATURES = {
     "xs_paged_decode_step_ex": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I,
                                      _I, _L, _F, _I, _I, _P, _P, _P, _P, _I, _I, _P, _P]),
     "xs_paged_decode_step_counters": (_L, [_I, _I]),
+    "xs_paged_decode_step_cluster_size": (_I, [_I, _I, _I, _I, _I, _I, _I]),
     "xs_paged_decode_step_partition_tokens": (_I, [_I, _I, _I, _L, _I, _I]),
     "xs_version": (_I, []),
     "xs_debug_bounds_failures": (_I, [_I]),
@@ -236,26 +237,30 @@ def xs_paged_decode(out, part_o, part_m, part_l, q, k_cache, v_cache, block_tabl
 
 
 XS_STEP_EARLY_READS = 1
+XS_STEP_PERSISTENT = 2
 
 
 def xs_paged_decode_step(out, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens,
                          scale, partition_tokens, max_partitions, part_o, part_m, part_l,
                          counters, sinks=None, window=0, err_flag=None, stream=None,
-                         early_reads=False):
+                         early_reads=False, persistent=False):
     """The whole decode step in one launch: append k_new/v_new ([B, Hkv, D],
     or both None), attend, combine the split-K partials.  ``counters`` holds
     xs_paged_decode_step_counters(B, Hkv) int32 zeros (left zero).
     ``early_reads`` (XS_STEP_EARLY_READS): lengths, tables and the first pages
     are read before the previous kernel on the stream completes; the caller
-    promises that kernel writes none of them."""
+    promises that kernel writes none of them.  ``persistent``
+    (XS_STEP_PERSISTENT): the persistent grid even for a launch that would
+    run as clusters."""
     B, Hq, D = q.shape
     num_blocks, Hkv, bs, _ = k_cache.shape
-    if early_reads:
+    flags = (XS_STEP_EARLY_READS if early_reads else 0) | (XS_STEP_PERSISTENT if persistent else 0)
+    if flags:
         _call("xs_paged_decode_step_ex", _ptr(out), _ptr(q), _ptr(k_new), _ptr(v_new),
               _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1],
               _ptr(context_lens), _ptr(sinks), int(window), B, Hq, Hkv, D, bs, num_blocks,
               float(scale), partition_tokens, max_partitions, _ptr(part_o), _ptr(part_m),
-              _ptr(part_l), _ptr(counters), XS_STEP_EARLY_READS, dtype_code(q.dtype),
+              _ptr(part_l), _ptr(counters), flags, dtype_code(q.dtype),
               _ptr(err_flag), _stream(stream))
         return
     _call("xs_paged_decode_step", _ptr(out), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache),
@@ -281,6 +286,16 @@ def xs_paged_decode_step_counters(B: int, Hkv: int) -> int:
     if n < 0:
         raise XsError("xs_paged_decode_step_counters", n)
     return n
+
+
+def xs_paged_decode_step_cluster_size(B, Hq, Hkv, D, max_blocks_per_seq, window, dtype) -> int:
+    """Cluster size of a one-launch step of this shape on the current device
+    (0: the persistent grid).  dtype: a torch dtype or an XS_* code."""
+    code = dtype if isinstance(dtype, int) else dtype_code(dtype)
+    r = load().xs_paged_decode_step_cluster_size(B, Hq, Hkv, D, max_blocks_per_seq, window, code)
+    if r < 0:
+        raise XsError("xs_paged_decode_step_cluster_size", r)
+    return r
 
 
 def xs_paged_decode_noalloc(out, q, k_cache, v_cache, block_tables, context_lens, scale,

@@ -89,18 +89,19 @@ class PagedDecodeStep:
                                              sinks=self.sinks, window=self.window)
 
     def run(self, out, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, scale,
-            early_reads: bool = False):
+            early_reads: bool = False, persistent: bool = False):
         """Append this step's K/V, attend and combine in one launch; all
         tensors on the device.  ``early_reads``: the launch reads lengths,
         tables and its first pages before the previous kernel on the stream
         completes (that kernel must write none of them: e.g. another layer's
-        step, or a projection)."""
+        step, or a projection).  ``persistent``: the persistent grid even
+        where the launch would run as clusters."""
         ws = self.ws
         ops.xs_paged_decode_step(out, q, k_new, v_new, k_cache, v_cache, block_tables,
                                  context_lens, scale, ws.partition_tokens, ws.max_partitions,
                                  ws.part_o, ws.part_m, ws.part_l, ws.work, sinks=self.sinks,
                                  window=self.window, err_flag=self.err_flag,
-                                 early_reads=early_reads)
+                                 early_reads=early_reads, persistent=persistent)
         return out
 
     def run_unfused(self, out, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens,

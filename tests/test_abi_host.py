@@ -230,10 +230,12 @@ def test_prefill_tc_argument_validation(lib):
 def test_step_ex_flags_validated(lib):
     # Unknown flag bits are refused before anything else is looked at.
     args = [None] * 7 + [0, None, None, 0, 1, 8, 8, 64, 16, 1, 0.125, 64, 1, None, None, None, None]
-    assert lib.xs_paged_decode_step_ex(*args, 2, ops.XS_BF16, None, None) == -5
+    assert lib.xs_paged_decode_step_ex(*args, 4, ops.XS_BF16, None, None) == -5
     assert lib.xs_paged_decode_step_ex(*args, 1 << 30, ops.XS_BF16, None, None) == -5
-    # A known flag passes through to the usual checks (NULL counters here).
-    assert lib.xs_paged_decode_step_ex(*args, 1, ops.XS_BF16, None, None) == -6
+    # Known flags (XS_STEP_EARLY_READS, XS_STEP_PERSISTENT, both) pass through
+    # to the usual checks (NULL counters here).
+    for flags in (1, 2, 3):
+        assert lib.xs_paged_decode_step_ex(*args, flags, ops.XS_BF16, None, None) == -6
 
 
 def test_missing_library_fails_loudly(tmp_path, monkeypatch):

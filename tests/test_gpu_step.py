@@ -21,7 +21,8 @@ def _ws(w, P):
                                partition_tokens=P)
 
 
-def _step(w, ws, sinks=None, window=0, append=True, out=None, err=None, early=False, layer=0):
+def _step(w, ws, sinks=None, window=0, append=True, out=None, err=None, early=False, layer=0,
+          persistent=False):
     cfg = w.cfg
     dev = w.q.device
     out = torch.full((cfg.B, cfg.Hq, cfg.D), float("nan"), dtype=cfg.dtype, device=dev) \
@@ -32,7 +33,7 @@ def _step(w, ws, sinks=None, window=0, append=True, out=None, err=None, early=Fa
                              w.v_cache[layer], w.block_tables, w.context_lens, w.scale,
                              ws.partition_tokens, ws.max_partitions, ws.part_o, ws.part_m,
                              ws.part_l, ws.work, sinks=sinks, window=window, err_flag=err,
-                             early_reads=early)
+                             early_reads=early, persistent=persistent)
     return out, err
 
 
@@ -51,10 +52,16 @@ CASES += [(torch.bfloat16, 4, 448, False), (torch.bfloat16, 4, 640, True),
           (torch.float32, 1, 192, False)]
 
 
-@pytest.mark.parametrize("dtype,G,P,early", CASES,
+# The bf16 cases again on the persistent grid (these small batches would run
+# as clusters).
+CASES = [c + (False,) for c in CASES] + [c + (True,) for c in CASES if c[0] == torch.bfloat16]
+
+
+@pytest.mark.parametrize("dtype,G,P,early,persistent", CASES,
                          ids=[f"{'bf16' if d == torch.bfloat16 else 'f32'}-G{G}-P{P}"
-                              f"{'-early' if e else ''}" for d, G, P, e in CASES])
-def test_step_matches_oracle(dtype, G, P, early):
+                              f"{'-early' if e else ''}{'-persistent' if pe else ''}"
+                              for d, G, P, e, pe in CASES])
+def test_step_matches_oracle(dtype, G, P, early, persistent):
     # Lengths around page and partition edges, up to 63 partitions of 16
     # tokens (the combine walks its partials 32 at a time), and an empty slot.
     dev = gh.device()
@@ -64,7 +71,7 @@ def test_step_matches_oracle(dtype, G, P, early):
     w = wl.make_workload(cfg, device=dev, history=hist)
     ek, ev = _appended(w)
     ws = _ws(w, P)
-    out, err = _step(w, ws, early=early)
+    out, err = _step(w, ws, early=early, persistent=persistent)
     torch.cuda.synchronize()
     assert int(err.item()) == 0 and int(ws.work.count_nonzero()) == 0
     assert torch.equal(gh.int_view(w.k_cache[0].cpu()), gh.int_view(ek))
@@ -86,11 +93,11 @@ def test_step_sinks_window(window):
     ref = oracle.paged_decode_sinks(w.q[0].cpu(), ek, ev, w.block_tables.cpu(),
                                     w.context_lens.cpu(), w.scale, sinks=sinks.cpu(),
                                     window=window)
-    for P in (64, 256, 4096):
-        out, err = _step(w, _ws(w, P), sinks=sinks, window=window)
+    for P, persistent in itertools.product((64, 256, 4096), (False, True)):
+        out, err = _step(w, _ws(w, P), sinks=sinks, window=window, persistent=persistent)
         torch.cuda.synchronize()
         assert int(err.item()) == 0
-        gh.assert_close(out, ref, cfg.dtype, what=f"P={P}")
+        gh.assert_close(out, ref, cfg.dtype, what=f"P={P} persistent={persistent}")
 
 
 def test_attention_only_launch():
@@ -129,7 +136,7 @@ def test_bad_length_and_bad_block_append_nothing():
     want = gh.expected_rows(w.block_tables, lens_ok, w.num_blocks, cfg.Hkv)
     kc0, vc0 = w.k_cache[0].clone(), w.v_cache[0].clone()
     ws = _ws(w, 64)
-    out, err = _step(w, ws)
+    out, err = _step(w, ws, persistent=True)
     torch.cuda.synchronize()
     flags = int(err.item())
     assert flags & ops.FLAG_BAD_LEN and flags & ops.FLAG_BAD_BLOCK
