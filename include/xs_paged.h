@@ -530,8 +530,8 @@ int xs_paged_decode_step_partition_tokens(int B, int Hq, int Hkv, int64_t total_
  * xs_paged_decode_step / _ex runs a launch of this shape on the current
  * device, or 0 when it runs the persistent grid.  Clusters are used for bf16,
  * D = 128, when the tokens a sequence can hold (max_blocks_per_seq * 16, or
- * the window when smaller) split into at most 16 partitions of at most 24
- * pages (23 with a window) and all B * Hkv clusters fit the device at once;
+ * the window when smaller) split into at most 16 partitions of at most 192
+ * pages (191 with a window) and all B * Hkv clusters fit the device at once;
  * the largest such size is taken (at most one CTA per 64 tokens).  Only the
  * shape decides: B, Hq, Hkv, D, max_blocks_per_seq, window and dtype are
  * those of the step.  XS_ESHAPE for a negative size, Hq % Hkv != 0.

@@ -1841,26 +1841,30 @@ __global__ void __launch_bounds__(kThreads, Cfg<T, D, G, S>::kMinBlocks)
 // cluster barriers, so no CTA waits for one that left.
 constexpr int kCluConsumers = 8;
 constexpr int kCluThreads = 32 * (1 + kCluConsumers);  // producer + consumers
-constexpr int kCluMaxPages = 24;  // pages of one partition, all resident at once
+constexpr int kCluStages = 24;    // ring stages (page pairs) of a CTA
 constexpr int kCluMaxSize = 16;   // CTAs per cluster (the non-portable maximum)
+// Pages of a partition up to which clusters were measured faster than the
+// persistent grid over every SM (a 32768-token sequence split 12 ways is
+// 171 pages a CTA: 27.5 against 30.8 us); beyond, the persistent grid.
+constexpr int kCluMaxPartPages = 192;
 
 template <int D, int G>
 struct CluCfg {
     static constexpr int kRowBytes = D * 2;
     static constexpr int kPageBytes = kBlock * kRowBytes;
     static constexpr int kStageBytes = 2 * kPageBytes;  // K page, then V page (swizzled)
-    static constexpr int kQOff = kCluMaxPages * kStageBytes;
+    static constexpr int kQOff = kCluStages * kStageBytes;
     // The CTA's partial: m[8], l[8], o[G][D] (fp32, o not divided by l).
     // A consumer's state has the same layout and goes in the consumer's
     // first stage, which only it ever reads.
     static constexpr int kPartOff = kQOff + G * kRowBytes;
     static constexpr int kPartBytes = 64 + G * D * 4;
     static constexpr int kBarOff = kPartOff + kPartBytes;
-    static constexpr int kBarBytes = (kCluMaxPages + 1) * 8;  // pages, then q
+    static constexpr int kBarBytes = (2 * kCluStages + 1) * 8;  // full, empty, then q
     static constexpr int kAlignSlack = 1024;  // the stages are 1024-byte aligned
     static constexpr int kBytes = kBarOff + kBarBytes + kAlignSlack;
     static_assert(kPartBytes <= kStageBytes, "a consumer state fits its stage");
-    static_assert(kCluMaxPages >= kCluConsumers && kCluMaxPages <= 32, "one lane per page");
+    static_assert(kCluStages >= kCluConsumers && kCluStages <= 32, "one lane per page");
     static_assert(kPartOff % 16 == 0 && kBarOff % 8 == 0, "float4 partial rows, 8-byte barriers");
 };
 
@@ -1889,9 +1893,11 @@ __device__ __forceinline__ float4 dsmem_ld_v4(uint32_t a) {
 
 // Grid (cluster size, B * Hkv), clusters along x: blockIdx.y = b * Hkv + g,
 // blockIdx.x = the partition.  p.P is the partition length (a multiple of
-// 16, at most kCluMaxPages pages, one fewer with a window, whose start need
-// not fall on a page); the host picked it so that gridDim.x partitions
-// cover every sequence.
+// 16; with a window a partition's start need not fall on a page); the host
+// picked it so that gridDim.x partitions cover every sequence.  A CTA's
+// pages go round a ring of kCluStages stages; page i uses stage
+// i % kCluStages and consumer i % kCluConsumers, so every stage belongs to
+// one consumer.
 template <int D, int G>
 __global__ void __launch_bounds__(kCluThreads, 1)
     paged_decode_cluster_kernel(const __grid_constant__ CUtensorMap tmk,
@@ -1900,7 +1906,8 @@ __global__ void __launch_bounds__(kCluThreads, 1)
     extern __shared__ __align__(128) unsigned char smem_raw[];
     unsigned char *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::kBarOff);
-    uint64_t *qbar = full + kCluMaxPages;
+    uint64_t *empty = full + kCluStages;
+    uint64_t *qbar = empty + kCluStages;
     float *part = reinterpret_cast<float *>(smem + C::kPartOff);
     __shared__ int s_abort;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1913,7 +1920,7 @@ __global__ void __launch_bounds__(kCluThreads, 1)
         return;
     }
     if (tid == 0) {
-        for (int i = 0; i <= kCluMaxPages; ++i) mbar_init(&full[i], 1);  // (full[24] = qbar)
+        for (int i = 0; i <= 2 * kCluStages; ++i) mbar_init(&full[i], 1);  // full, empty, q
         mbar_fence_init();
         s_abort = 0;
     }
@@ -1937,33 +1944,43 @@ __global__ void __launch_bounds__(kCluThreads, 1)
         const int n = seq_len(p, b, r == 0 && g == 0 && lane == 0);
         int tok0, tok1, pg0, np;
         range(n, tok0, tok1, pg0, np);
-        if (np > kCluMaxPages) np = 0;  // (the host's choice of p.P rules this out)
         // The page holding the sequence's last token receives this step's
         // row: it is copied after the row is written (and only when the
         // length is within the table, as in the separate append).
         const int raw_len = p.k_new && tok1 == n && np > 0 ? p.context_lens[b] : 0;
         const bool appends = raw_len == n && n > 0;
         const int last = appends ? np - 1 : -1;
-        int32_t blk = 0;
-        if (lane < np) blk = p.block_tables[static_cast<int64_t>(b) * p.table_stride + pg0 + lane];
-        const bool bad_id = lane < np && (blk < 0 || blk >= p.num_blocks);
-        if (__any_sync(0xffffffffu, bad_id) && lane == 0) raise_flag(p.err_flag, XS_FLAG_BAD_BLOCK);
-        // An id outside the pool reads block 0 instead (flagged) and takes no
-        // appended row.
-        const bool appends_ok = appends && !__shfl_sync(0xffffffffu, bad_id, max(last, 0));
-        if (bad_id) blk = 0;
         const uint64_t pol = policy_evict_first();
-        // Lane i issues page i's two copies.  (The debug library can skip
-        // one page of CTA (0, 0) to make a consumer's wait run out.)
-        const bool skip = blockIdx.y == 0 && skip_page(static_cast<uint32_t>(lane));
-        auto issue = [&](bool pred) {
-            if (!pred || skip) return;
-            const uint32_t dk = smem_addr(smem + lane * C::kStageBytes);
-            mbar_arrive_expect_tx(&full[lane], 2 * C::kPageBytes);
-            tma_load_4d(dk, &tmk, blk * p.Hkv + g, &full[lane], pol);
-            tma_load_4d(dk + C::kPageBytes, &tmv, blk * p.Hkv + g, &full[lane], pol);
+        // Pages go round the ring kCluStages at a time, lane j issuing page
+        // base + j into stage j.  An id outside the pool reads block 0
+        // instead (flagged) and takes no appended row.
+        auto load_id = [&](int i) {
+            int32_t id = 0;
+            if (i < np) {
+                id = p.block_tables[static_cast<int64_t>(b) * p.table_stride + pg0 + i];
+                if (id < 0 || id >= p.num_blocks) {
+                    raise_flag(p.err_flag, XS_FLAG_BAD_BLOCK);
+                    id = -1;
+                }
+            }
+            return id;
         };
-        issue(lane < np && lane != last);
+        int my_last = -1;  // the last page this lane issued (its stage's last phase)
+        auto issue = [&](int i, int32_t id) {
+            // (The debug library can skip one page of CTA (0, 0) to make a
+            // consumer's wait run out.)
+            if (blockIdx.y == 0 && skip_page(static_cast<uint32_t>(i))) return;
+            const int st = i % kCluStages;
+            const uint32_t dk = smem_addr(smem + st * C::kStageBytes);
+            const int page = max(id, 0) * p.Hkv + g;
+            mbar_arrive_expect_tx(&full[st], 2 * C::kPageBytes);
+            tma_load_4d(dk, &tmk, page, &full[st], pol);
+            tma_load_4d(dk + C::kPageBytes, &tmv, page, &full[st], pol);
+            my_last = i;
+        };
+        const bool first = lane < kCluStages && lane < np;
+        const int32_t id0 = first ? load_id(lane) : 0;
+        if (first && lane != last) issue(lane, id0);
         if (p.early) {
             griddep_wait();
             griddep_launch_dependents();
@@ -1980,11 +1997,14 @@ __global__ void __launch_bounds__(kCluThreads, 1)
             // of the last page; then the generic-proxy writes are ordered
             // before the tensor copy that reads the page.
             constexpr int kChunks = C::kRowBytes / 16;
-            const int32_t lblk = __shfl_sync(0xffffffffu, blk, last);
+            const int32_t lid = last < kCluStages ? __shfl_sync(0xffffffffu, id0, last)
+                                                  : p.block_tables[static_cast<int64_t>(b) *
+                                                                       p.table_stride + pg0 + last];
+            const bool ok_id = lid >= 0 && lid < p.num_blocks;
             const int64_t row = static_cast<int64_t>(b) * p.Hkv + g;
-            const int64_t dst = ((static_cast<int64_t>(lblk) * p.Hkv + g) * kBlock + (n - 1) % kBlock) *
-                                kChunks;
-            for (int c = lane; appends_ok && c < 2 * kChunks; c += 32) {
+            const int64_t dst =
+                ((static_cast<int64_t>(lid) * p.Hkv + g) * kBlock + (n - 1) % kBlock) * kChunks;
+            for (int c = lane; ok_id && c < 2 * kChunks; c += 32) {
                 const bool is_k = c < kChunks;
                 const int cc = is_k ? c : c - kChunks;
                 const uint4 v = static_cast<const uint4 *>(is_k ? p.k_new : p.v_new)[row * kChunks + cc];
@@ -1992,14 +2012,35 @@ __global__ void __launch_bounds__(kCluThreads, 1)
             }
             fence_proxy_async_global();
             __syncwarp();
-            issue(lane == last);
+            if (last < kCluStages && lane == last) issue(lane, id0);  // (later: in the ring loop)
+        }
+        // The rest of the pages, each into its stage once the consumer has
+        // released the stage's previous page (bounded wait).
+        bool ok = true;
+        for (int base = kCluStages; ok && base < np; base += kCluStages) {
+            const int i = base + lane;
+            const bool mine = lane < kCluStages && i < np;
+            const int32_t id = mine ? load_id(i) : 0;
+            bool w = true;
+            if (mine) {
+                w = mbar_wait_bounded(&empty[lane], (base / kCluStages - 1) & 1, wait_limit());
+                if (w) issue(i, id);
+            }
+            ok = __all_sync(0xffffffffu, w);
+        }
+        if (!ok && lane == 0) {
+            raise_flag(p.err_flag, XS_FLAG_TIMEOUT);
+            atomicExch(&s_abort, 1);
         }
         // Every copy issued lands before the CTA can exit: in the normal
         // path the consumers have waited for all of them; after an abort
-        // this wait (bounded) covers the ones they gave up on.  Done after
-        // the first cluster barrier, when the consumers are finished.
+        // this wait (bounded) covers the ones they gave up on - per stage
+        // the last page issued, whose phase is the only one that can still
+        // be open.  Done after the first cluster barrier, when the consumers
+        // are finished.
         cluster_barrier();
-        if (lane < np && !skip) mbar_wait_bounded(&full[lane], 0, wait_limit());
+        if (my_last >= 0)
+            mbar_wait_bounded(&full[my_last % kCluStages], (my_last / kCluStages) & 1, wait_limit());
         if (np > 0 && lane == 0) mbar_wait_bounded(qbar, 0, wait_limit());
     } else {
         // ======================================================== consumers
@@ -2009,7 +2050,6 @@ __global__ void __launch_bounds__(kCluThreads, 1)
         const int n = seq_len(p, b, false);
         int tok0, tok1, pg0, np;
         range(n, tok0, tok1, pg0, np);
-        if (np > kCluMaxPages) np = 0;
         const int grp = lane >> 2, tq = lane & 3;
         float m2[2] = {-INFINITY, -INFINITY}, l2[2] = {0.f, 0.f};
         float oacc[D / 16][4];
@@ -2028,12 +2068,14 @@ __global__ void __launch_bounds__(kCluThreads, 1)
                 qa[ks][1] = grp < G ? *reinterpret_cast<const uint32_t *>(row + 16) : 0u;
             }
             for (int i = cw; ok && i < np; i += kCluConsumers) {
-                if (!__all_sync(0xffffffffu, mbar_wait_bounded(&full[i], 0, wait_limit())) ||
+                const int st = i % kCluStages;
+                if (!__all_sync(0xffffffffu,
+                                mbar_wait_bounded(&full[st], (i / kCluStages) & 1, wait_limit())) ||
                     *static_cast<volatile int *>(&s_abort)) {
                     ok = false;
                     break;
                 }
-                const uint32_t kaddr = smem_addr(smem + i * C::kStageBytes);
+                const uint32_t kaddr = smem_addr(smem + st * C::kStageBytes);
                 const int pg = pg0 + i;
                 const int t_lo = max(0, tok0 - pg * kBlock);
                 const int t_hi = min(kBlock, tok1 - pg * kBlock);
@@ -2043,6 +2085,10 @@ __global__ void __launch_bounds__(kCluThreads, 1)
                 else
                     consume_page_mma<D, false, true>(kaddr, kaddr + C::kPageBytes, t_lo, t_hi, qa,
                                                      p.qscale, m2, l2, oacc, lane);
+                // The stage's next page may come in once every lane has its
+                // fragments of this one.
+                __syncwarp();
+                if (i + kCluStages < np && lane == 0) mbar_arrive(&empty[st]);
             }
             if (!ok && lane == 0) {
                 raise_flag(p.err_flag, XS_FLAG_TIMEOUT);
@@ -2292,7 +2338,7 @@ int cluster_capacity(KernelFn fn, int smem, int cs) {
 // Whether a one-launch step runs as clusters (paged_decode_cluster_kernel):
 // bf16, D = 128, and every (sequence, KV head) group's tokens - at most the
 // table's reach, or the window - split into cs partitions of at most
-// kCluMaxPages pages (one fewer with a window) with all B * Hkv clusters
+// kCluMaxPartPages pages (one fewer with a window) with all B * Hkv clusters
 // resident at once.  The largest such cs up to 16 (and no more than one
 // partition per 64 tokens) is taken: the fewer pages a CTA holds, the
 // shorter the launch.  Returns cs (0: the persistent grid) and sets the
@@ -2308,7 +2354,7 @@ int cluster_plan(int B, int Hkv, int D, int G, int max_blocks, int window, int d
     int cs = static_cast<int>(std::min<int64_t>(kCluMaxSize, (L + 63) / 64));
     for (; cs >= 2; --cs) {
         const int64_t part = ((L + cs - 1) / cs + kBlock - 1) / kBlock * kBlock;
-        if (part / kBlock + spare > kCluMaxPages) return 0;  // fewer CTAs only add pages
+        if (part / kBlock + spare > kCluMaxPartPages) return 0;  // fewer CTAs only add pages
         if (static_cast<int64_t>(B) * Hkv <= cluster_capacity(*fn, *smem, cs)) {
             *P = static_cast<int>(part);
             return cs;

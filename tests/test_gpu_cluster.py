@@ -72,9 +72,11 @@ def test_which_launches_run_as_clusters():
     bf16, f32 = torch.bfloat16, torch.float32
     size = ops.xs_paged_decode_step_cluster_size
     # One group (one sequence, one KV head): a single cluster of up to 16.
-    # 6144 tokens split 16 ways is 24 pages a CTA; 6160 tokens would be 25.
+    # 49152 tokens split 16 ways is 192 pages a CTA, the most it takes;
+    # 49168 tokens would be 193.
     assert size(1, 4, 1, 128, 384, 0, bf16) == 16
-    assert size(1, 4, 1, 128, 385, 0, bf16) == 0
+    assert size(1, 4, 1, 128, 3072, 0, bf16) == 16
+    assert size(1, 4, 1, 128, 3073, 0, bf16) == 0
     # A window bounds the tokens: 4096 of a 16000-token table (17 pages a CTA).
     assert size(1, 4, 1, 128, 1000, 4096, bf16) == 16
     # No more than one CTA per 64 tokens.
@@ -124,9 +126,9 @@ def test_ragged_small_batch(G):
 @pytest.mark.parametrize("G", [4, 8])
 @pytest.mark.parametrize("hist", [6143, 6143 - 384, 5000, 0])
 def test_full_and_empty_partitions(hist, G):
-    # One KV head, a 384-block table split 16 ways: 24 pages a CTA.  6144
-    # tokens fill every page of every partition; 5760 leave the last
-    # partition empty; one token leaves fifteen of them empty.
+    # One KV head, a 384-block table split 16 ways: 24 pages a CTA, one lap
+    # of the ring.  6144 tokens fill every page of every partition; 5760
+    # leave the last partition empty; one token leaves fifteen of them empty.
     dev = gh.device()
     cfg = wl.custom_config(1, G, 1, 128, torch.bfloat16, history=("uniform", (0, 1)),
                            pool=("factor", 1.2), seed=910 + G)
@@ -139,6 +141,26 @@ def test_full_and_empty_partitions(hist, G):
     ek, ev = _appended(w)
     out, err = _step(w, _ws(w))
     _check(w, out, err, ek, ev, what=f"history {hist} G={G}")
+
+
+@pytest.mark.parametrize("hist,early", [((16383,), False), ((16383,), True),
+                                        ((3000, 2500), False), ((3000, 2500), True),
+                                        ((9000, 1, 0, 4000, 6000), False)])
+def test_ring_laps(hist, early):
+    # Partitions longer than the 24-stage ring: one sequence of 16384 tokens
+    # (86 pages a CTA, four laps), two of 3001 and 2501 (the appended page
+    # past the first lap), and a ragged batch; with and without early reads.
+    dev = gh.device()
+    cfg = wl.custom_config(len(hist), 32, 8, 128, torch.bfloat16, history=("uniform", (0, 1)),
+                           pool=("factor", 1.2), seed=950 + len(hist))
+    w = wl.make_workload(cfg, device=dev, history=torch.tensor(hist, dtype=torch.int32))
+    cs = _cluster_size(w)
+    assert cs > 0
+    tokens = w.max_blocks_per_seq * gh.BS
+    assert -(-tokens // cs) > 24 * gh.BS   # more than one lap of the ring
+    ek, ev = _appended(w)
+    out, err = _step(w, _ws(w), early=early)
+    _check(w, out, err, ek, ev, what=f"{hist} early={early}")
 
 
 @pytest.mark.parametrize("window", [0, 16, 37, 300, 1000])

@@ -78,11 +78,15 @@ def test_a_wait_that_runs_out_in_a_cluster_launch():
     dbg = ops.load_debug()
     prev = ops.use_library(dbg)
     try:
-        cfg = wl.custom_config(1, 32, 8, 128, torch.bfloat16, history=("fixed", (3000,)),
+        # 8001 tokens split 12-16 ways: more pages a CTA than the ring has
+        # stages, so after the consumer's wait for page 2 runs out, the
+        # producer's wait for stage 2 to come free (for page 26) runs out too.
+        cfg = wl.custom_config(1, 32, 8, 128, torch.bfloat16, history=("fixed", (8000,)),
                                pool=("factor", 1.2), seed=405, name="timeout_cluster_case")
         w = wl.make_workload(cfg, device=dev)
-        assert ops.xs_paged_decode_step_cluster_size(cfg.B, cfg.Hq, cfg.Hkv, cfg.D,
-                                                     w.max_blocks_per_seq, 0, cfg.dtype) > 0
+        cs = ops.xs_paged_decode_step_cluster_size(cfg.B, cfg.Hq, cfg.Hkv, cfg.D,
+                                                   w.max_blocks_per_seq, 0, cfg.dtype)
+        assert cs > 0 and -(-w.max_blocks_per_seq // cs) > 26
         step = PagedDecodeStep(cfg.B, cfg.Hq, cfg.Hkv, cfg.D, w.max_blocks_per_seq, cfg.dtype,
                                dev, partition_tokens=256)
         out = torch.empty(cfg.B, cfg.Hq, cfg.D, dtype=cfg.dtype, device=dev)
