@@ -482,7 +482,8 @@ def measure_decode(args, cfg: wl.DecodeConfig, rank, world, local, dist, *, step
                graph=graph is not None, bytes_per_step=bytes_per_step, ms_per_step=ms_per_step,
                value=world * bytes_per_step / (ms_per_step * 1e-3) / 1e9,
                seq_steps=world * cfg.B * L / (ms_per_step * 1e-3), attn_ms=attn_ms,
-               clocks=clock_info, l2_flushed=l2_flushed, e2e=None)
+               clocks=clock_info, l2_flushed=l2_flushed, e2e=None,
+               cluster=step.cluster_size(fused))
     if not with_e2e:
         return res
 
@@ -517,6 +518,15 @@ def measure_decode(args, cfg: wl.DecodeConfig, rank, world, local, dist, *, step
     return res
 
 
+def split_config(m: dict) -> dict:
+    """How the step kernel split the work: one cluster of `cluster_size` CTAs
+    per (sequence, KV head), or the persistent grid's partitions."""
+    if m["cluster"]:
+        return {"kernel": "cluster", "cluster_size": m["cluster"]}
+    return {"kernel": "persistent", "partition_tokens": m["step"].partition_tokens,
+            "max_partitions": m["step"].max_partitions}
+
+
 def decode_roofline(m: dict, traffic=None) -> dict:
     """Roofline object of the step kernel: algorithmic bytes per launch over
     the average launch time, against the measured HBM copy peak."""
@@ -525,7 +535,8 @@ def decode_roofline(m: dict, traffic=None) -> dict:
     # The fused launch also appends the new rows and writes the output.
     launch_bytes = m["by"]["step"] if m["fused"] else m["by"]["attn"]
     gbs = launch_bytes / (attn_avg_ms * 1e-3) / 1e9
-    return {"kernel": "paged_decode_kernel", "bound": "hbm", "achieved": round(gbs, 1),
+    kernel = "paged_decode_cluster_kernel" if m["cluster"] else "paged_decode_kernel"
+    return {"kernel": kernel, "bound": "hbm", "achieved": round(gbs, 1),
             "peak": peak, "unit": "GB/s", "frac": round(gbs / peak, 4), "peak_kind": peak_kind,
             "traffic": traffic, "algorithmic_bytes_per_launch": launch_bytes,
             "avg_launch_ms": round(attn_avg_ms, 4)}
@@ -565,7 +576,7 @@ def decode_row(args, idx: int, rank, world, local, dist) -> dict:
         "dtype": "bf16" if cfg.dtype == torch.bfloat16 else "f32",
         "config": {"B": cfg.B, "Hq": cfg.Hq, "Hkv": cfg.Hkv, "D": cfg.D, "layers": m["L"],
                    "context_tokens": m["w"].total_context_tokens,
-                   "partition_tokens": m["step"].partition_tokens,
+                   **split_config(m),
                    "l2": ("flushed before every timed step (a write of twice the L2 size); "
                           "each step timed by its own events") if m["l2_flushed"] else
                          f"inputs larger than L2 ({m['bytes_per_step'] / 1e9:.3f} GB per step)"},
@@ -631,9 +642,8 @@ def run_ours(args, rank, world, local, dist):
                        "D": cfg.D, "block_size": cfg.block_size, "layers": L,
                        "pool_blocks": w.num_blocks, "context_tokens": w.total_context_tokens,
                        "max_context_len": w.max_context_len,
-                       "partition_tokens": step.partition_tokens,
-                       "sinks": bool(args.sinks), "window": args.window,
-                       "max_partitions": step.max_partitions, "l2": l2,
+                       **split_config(m),
+                       "sinks": bool(args.sinks), "window": args.window, "l2": l2,
                        "parallelism": f"replicas x{world} (independent batches, no collective)"},
             "seq_steps_per_s": round(m["seq_steps"], 1),
             "pct_of_hbm_peak": {"of_measured": round(100 * value / world / peak, 2),

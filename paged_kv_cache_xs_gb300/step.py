@@ -53,6 +53,15 @@ class PagedDecodeStep:
     def max_partitions(self) -> int:
         return self.ws.max_partitions
 
+    def cluster_size(self, fused: bool = True) -> int:
+        """Cluster size the one-launch step runs with on the current device
+        (0: the persistent grid, whose split is partition_tokens)."""
+        if not fused:
+            return 0
+        return ops.xs_paged_decode_step_cluster_size(self.B, self.Hq, self.Hkv, self.D,
+                                                     self.max_blocks_per_seq, self.window,
+                                                     self.dtype)
+
     def launches_per_step(self, fused: bool = True) -> int:
         if fused:
             return 1
