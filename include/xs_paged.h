@@ -440,8 +440,8 @@ int xs_paged_decode_sinks(void *out, float *part_o, float *part_m, float *part_l
  *  - combine: each item of a split (sequence, KV head) writes its partials,
  *    then counts itself in; the item that completes the group merges the
  *    group's partials for the G query heads into out.
- *  - small launches (xs_paged_decode_step_cluster_size > 0: bf16, D = 128,
- *    every (sequence, KV head) group in one wave of thread-block clusters)
+ *  - small launches (xs_paged_decode_step_cluster_size > 0: bf16, every
+ *    (sequence, KV head) group in one wave of thread-block clusters)
  *    run one cluster per group instead: its CTAs split the group's tokens
  *    into their own partitions (partition_tokens is not used), and the
  *    split-K combine reads the CTAs' partials from distributed shared
@@ -528,8 +528,8 @@ int xs_paged_decode_step_partition_tokens(int B, int Hq, int Hkv, int64_t total_
 /*
  * xs_paged_decode_step_cluster_size - the cluster size (2..16) with which
  * xs_paged_decode_step / _ex runs a launch of this shape on the current
- * device, or 0 when it runs the persistent grid.  Clusters are used for bf16,
- * D = 128, when the tokens a sequence can hold (max_blocks_per_seq * 16, or
+ * device, or 0 when it runs the persistent grid.  Clusters are used for bf16
+ * (D = 64 or 128) when the tokens a sequence can hold (max_blocks_per_seq * 16, or
  * the window when smaller) split into at most 16 partitions of at most 192
  * pages (191 with a window) and all B * Hkv clusters fit the device at once;
  * the largest such size is taken (at most one CTA per 64 tokens).  Only the

@@ -1863,6 +1863,9 @@ struct CluCfg {
     static constexpr int kBarBytes = (2 * kCluStages + 1) * 8;  // full, empty, then q
     static constexpr int kAlignSlack = 1024;  // the stages are 1024-byte aligned
     static constexpr int kBytes = kBarOff + kBarBytes + kAlignSlack;
+    // D = 64: a 98 KB ring and fewer registers, so two CTAs share an SM and
+    // twice as many clusters fit at once.
+    static constexpr int kMinBlocks = D == 64 ? 2 : 1;
     static_assert(kPartBytes <= kStageBytes, "a consumer state fits its stage");
     static_assert(kCluStages >= kCluConsumers && kCluStages <= 32, "one lane per page");
     static_assert(kPartOff % 16 == 0 && kBarOff % 8 == 0, "float4 partial rows, 8-byte barriers");
@@ -1899,7 +1902,7 @@ __device__ __forceinline__ float4 dsmem_ld_v4(uint32_t a) {
 // i % kCluStages and consumer i % kCluConsumers, so every stage belongs to
 // one consumer.
 template <int D, int G>
-__global__ void __launch_bounds__(kCluThreads, 1)
+__global__ void __launch_bounds__(kCluThreads, CluCfg<D, G>::kMinBlocks)
     paged_decode_cluster_kernel(const __grid_constant__ CUtensorMap tmk,
                                 const __grid_constant__ CUtensorMap tmv, const Params p) {
     using C = CluCfg<D, G>;
@@ -2278,8 +2281,8 @@ KernelFn cluster_kernel_for() {
     return paged_decode_cluster_kernel<D, G>;
 }
 
-// The cluster-step kernel for a shape (bf16, D = 128) and its dynamic shared
-// memory, or null.
+// The cluster-step kernel for a shape (bf16, D = 64 or 128) and its dynamic
+// shared memory, or null.
 KernelFn pick_cluster_kernel(int D, int G, int *smem) {
 #define XS_PICK_CLU(DD, GG)                                                          \
     if (D == DD && G == GG) {                                                        \
@@ -2287,6 +2290,7 @@ KernelFn pick_cluster_kernel(int D, int G, int *smem) {
         return cluster_kernel_for<DD, GG>();                                         \
     }
     XS_PICK_CLU(128, 1) XS_PICK_CLU(128, 2) XS_PICK_CLU(128, 4) XS_PICK_CLU(128, 8)
+    XS_PICK_CLU(64, 1) XS_PICK_CLU(64, 2) XS_PICK_CLU(64, 4) XS_PICK_CLU(64, 8)
 #undef XS_PICK_CLU
     return nullptr;
 }
@@ -2336,7 +2340,7 @@ int cluster_capacity(KernelFn fn, int smem, int cs) {
 }
 
 // Whether a one-launch step runs as clusters (paged_decode_cluster_kernel):
-// bf16, D = 128, and every (sequence, KV head) group's tokens - at most the
+// bf16, and every (sequence, KV head) group's tokens - at most the
 // table's reach, or the window - split into cs partitions of at most
 // kCluMaxPartPages pages (one fewer with a window) with all B * Hkv clusters
 // resident at once.  The largest such cs up to 16 (and no more than one

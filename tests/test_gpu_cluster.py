@@ -88,10 +88,12 @@ def test_which_launches_run_as_clusters():
     single = size(1, 32, 8, 128, 257, 0, bf16)
     assert 11 <= single <= 16   # at most 24 pages a CTA: at least 11 CTAs
     assert 2 <= size(4, 32, 8, 128, 63, 0, bf16) <= single
-    # Not for fp32, D = 64, no batch, or batches whose clusters do not fit
-    # at once.
+    # D = 64 runs two CTAs per SM: the GPT-2 shape (8 sequences, 12 heads)
+    # fits where D = 128 would not.
+    assert size(8, 12, 12, 64, 65, 0, bf16) >= 2
+    assert size(8, 12, 12, 128, 65, 0, bf16) == 0
+    # Not for fp32, no batch, or batches whose clusters do not fit at once.
     assert size(1, 32, 8, 128, 257, 0, f32) == 0
-    assert size(1, 32, 8, 64, 257, 0, bf16) == 0
     assert size(64, 32, 8, 128, 257, 0, bf16) == 0
     assert size(0, 32, 8, 128, 257, 0, bf16) == 0
 
@@ -107,20 +109,33 @@ def test_single_stream_matches_oracle(early):
     assert err_oracle <= gh.TOL[torch.bfloat16]
 
 
+@pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("G", [1, 2, 4, 8])
-def test_ragged_small_batch(G):
+def test_ragged_small_batch(G, D):
     # Lengths around pages and partitions, an empty sequence and an unset
     # slot (length 0 after the append of nothing: history -1).
     dev = gh.device()
     hist = torch.tensor([0, 1, 14, 15, 16, 17, 255, 256, 257, 1000, -1], dtype=torch.int32)
-    cfg = wl.custom_config(len(hist), 2 * G, 2, 128, torch.bfloat16, history=("uniform", (0, 1)),
-                           pool=("factor", 1.5), seed=900 + G)
+    cfg = wl.custom_config(len(hist), 2 * G, 2, D, torch.bfloat16, history=("uniform", (0, 1)),
+                           pool=("factor", 1.5), seed=900 + G + D)
     w = wl.make_workload(cfg, device=dev, history=hist)
     assert _cluster_size(w) > 0
     ek, ev = _appended(w)
     ws = _ws(w, 64)
     out, err = _step(w, ws)
-    _check(w, out, err, ek, ev, ws, what=f"G={G}")
+    _check(w, out, err, ek, ev, ws, what=f"G={G} D={D}")
+
+
+@pytest.mark.parametrize("early", [False, True])
+def test_gpt2_shape(early):
+    # The GPT-2 workload's layer (8 sequences, 12 heads x 64, MHA): clusters
+    # of two CTAs per SM.
+    dev = gh.device()
+    w = wl.make_workload(1, device=dev, layers=1)
+    assert _cluster_size(w) >= 2
+    ek, ev = _appended(w)
+    out, err = _step(w, _ws(w), early=early)
+    _check(w, out, err, ek, ev, what=f"early={early}")
 
 
 @pytest.mark.parametrize("G", [4, 8])
