@@ -1874,6 +1874,13 @@ struct CluCfg {
 __device__ __forceinline__ void cluster_barrier() {
     asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
 }
+// The same barrier without ordering this thread's earlier memory accesses:
+// for a barrier that only has to know the other CTAs are past their reads of
+// this CTA's shared memory (values they have already used), so the arrive
+// need not wait for this thread's global stores to complete.
+__device__ __forceinline__ void cluster_barrier_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed;\n\tbarrier.cluster.wait;" ::: "memory");
+}
 // The address of a shared-memory location in cluster CTA `rank`.
 __device__ __forceinline__ uint32_t dsmem_map(uint32_t local, uint32_t rank) {
     uint32_t a;
@@ -2199,7 +2206,10 @@ __global__ void __launch_bounds__(kCluThreads, CluCfg<D, G>::kMinBlocks)
             }
         }
     }
-    cluster_barrier();  // no CTA leaves while another may still read its partial
+    // No CTA leaves while another may still read its partial.  (Every read of
+    // a partial has delivered its value, which the reader used before it
+    // arrives; the output stores need not complete before the exit.)
+    cluster_barrier_relaxed();
 }
 
 // Split-K combine: one CTA of D threads per (sequence, query head).
