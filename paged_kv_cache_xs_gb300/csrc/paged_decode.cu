@@ -1853,14 +1853,13 @@ struct CluCfg {
     static constexpr int kRowBytes = D * 2;
     static constexpr int kPageBytes = kBlock * kRowBytes;
     static constexpr int kStageBytes = 2 * kPageBytes;  // K page, then V page (swizzled)
-    static constexpr int kQOff = kCluStages * kStageBytes;
     // The CTA's partial: m[8], l[8], o[G][D] (fp32, o not divided by l).
     // A consumer's state has the same layout and goes in the consumer's
     // first stage, which only it ever reads.
-    static constexpr int kPartOff = kQOff + G * kRowBytes;
+    static constexpr int kPartOff = kCluStages * kStageBytes;
     static constexpr int kPartBytes = 64 + G * D * 4;
     static constexpr int kBarOff = kPartOff + kPartBytes;
-    static constexpr int kBarBytes = (2 * kCluStages + 1) * 8;  // full, empty, then q
+    static constexpr int kBarBytes = 2 * kCluStages * 8;  // full, then empty
     static constexpr int kAlignSlack = 1024;  // the stages are 1024-byte aligned
     static constexpr int kBytes = kBarOff + kBarBytes + kAlignSlack;
     // D = 64: a 98 KB ring and fewer registers, so two CTAs share an SM and
@@ -1917,7 +1916,6 @@ __global__ void __launch_bounds__(kCluThreads, CluCfg<D, G>::kMinBlocks)
     unsigned char *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::kBarOff);
     uint64_t *empty = full + kCluStages;
-    uint64_t *qbar = empty + kCluStages;
     float *part = reinterpret_cast<float *>(smem + C::kPartOff);
     __shared__ int s_abort;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1930,7 +1928,7 @@ __global__ void __launch_bounds__(kCluThreads, CluCfg<D, G>::kMinBlocks)
         return;
     }
     if (tid == 0) {
-        for (int i = 0; i <= 2 * kCluStages; ++i) mbar_init(&full[i], 1);  // full, empty, q
+        for (int i = 0; i < 2 * kCluStages; ++i) mbar_init(&full[i], 1);  // full, then empty
         mbar_fence_init();
         s_abort = 0;
     }
@@ -1945,6 +1943,7 @@ __global__ void __launch_bounds__(kCluThreads, CluCfg<D, G>::kMinBlocks)
         pg0 = tok0 / kBlock;
         np = tok1 > tok0 ? (tok1 + kBlock - 1) / kBlock - pg0 : 0;
     };
+    int n_seq;  // the sequence's length (clamped to the table), read once per thread
     if (warp == 0) {
         // ======================================================== producer
         if (!p.early) {
@@ -1952,6 +1951,7 @@ __global__ void __launch_bounds__(kCluThreads, CluCfg<D, G>::kMinBlocks)
             griddep_launch_dependents();
         }
         const int n = seq_len(p, b, r == 0 && g == 0 && lane == 0);
+        n_seq = n;
         int tok0, tok1, pg0, np;
         range(n, tok0, tok1, pg0, np);
         // The page holding the sequence's last token receives this step's
@@ -1994,13 +1994,6 @@ __global__ void __launch_bounds__(kCluThreads, CluCfg<D, G>::kMinBlocks)
         if (p.early) {
             griddep_wait();
             griddep_launch_dependents();
-        }
-        if (np > 0 && lane == 0) {
-            mbar_arrive_expect_tx(qbar, C::kRowBytes * G);
-            bulk_g2s(smem + C::kQOff,
-                     static_cast<const unsigned char *>(p.q) +
-                         (static_cast<int64_t>(b) * p.Hq + static_cast<int64_t>(g) * G) * C::kRowBytes,
-                     C::kRowBytes * G, qbar);
         }
         if (appends) {
             // K row then V row, one 16-byte chunk per lane, into slot (n - 1)
@@ -2051,13 +2044,13 @@ __global__ void __launch_bounds__(kCluThreads, CluCfg<D, G>::kMinBlocks)
         cluster_barrier();
         if (my_last >= 0)
             mbar_wait_bounded(&full[my_last % kCluStages], (my_last / kCluStages) & 1, wait_limit());
-        if (np > 0 && lane == 0) mbar_wait_bounded(qbar, 0, wait_limit());
     } else {
         // ======================================================== consumers
         griddep_wait();
         griddep_launch_dependents();
         const int cw = warp - 1;
         const int n = seq_len(p, b, false);
+        n_seq = n;
         int tok0, tok1, pg0, np;
         range(n, tok0, tok1, pg0, np);
         const int grp = lane >> 2, tq = lane & 3;
@@ -2068,14 +2061,19 @@ __global__ void __launch_bounds__(kCluThreads, CluCfg<D, G>::kMinBlocks)
 #pragma unroll
             for (int c = 0; c < 4; ++c) oacc[i][c] = 0.f;
         if (cw < np) {
-            bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(qbar, 0, wait_limit()));
+            bool ok = true;
+            // The G query rows straight from global memory into the B
+            // fragments (lane quad grp holds head grp; rows G..7 zero): one
+            // round trip after the launch wait, nothing staged.
             uint32_t qa[D / 16][2];
-            const unsigned char *qs = smem + C::kQOff + (grp < G ? grp : 0) * C::kRowBytes;
+            const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
+                static_cast<const unsigned char *>(p.q) +
+                ((static_cast<int64_t>(b) * p.Hq + static_cast<int64_t>(g) * G + (grp < G ? grp : 0)) *
+                     C::kRowBytes));
 #pragma unroll
             for (int ks = 0; ks < D / 16; ++ks) {
-                const unsigned char *row = qs + (16 * ks + 2 * tq) * 2;
-                qa[ks][0] = grp < G ? *reinterpret_cast<const uint32_t *>(row) : 0u;
-                qa[ks][1] = grp < G ? *reinterpret_cast<const uint32_t *>(row + 16) : 0u;
+                qa[ks][0] = grp < G ? qrow[8 * ks + tq] : 0u;
+                qa[ks][1] = grp < G ? qrow[8 * ks + 4 + tq] : 0u;
             }
             for (int i = cw; ok && i < np; i += kCluConsumers) {
                 const int st = i % kCluStages;
@@ -2166,7 +2164,7 @@ __global__ void __launch_bounds__(kCluThreads, CluCfg<D, G>::kMinBlocks)
         constexpr int kChunks = G * D / 4;
         constexpr int kHalves = 2 * (kCluThreads / 32);
         const int j = lane & 15;
-        const int n = seq_len(p, b, false);
+        const int n = n_seq;
         const uint32_t remote = dsmem_map(smem_addr(part), static_cast<uint32_t>(j < cs ? j : 0));
         for (int k0 = 2 * warp; r + k0 * cs < kChunks; k0 += kHalves) {
             const int c = r + (k0 + (lane >> 4)) * cs;
