@@ -1950,6 +1950,14 @@ __global__ void __launch_bounds__(kCluThreads, CluCfg<D, G>::kMinBlocks)
             griddep_wait();
             griddep_launch_dependents();
         }
+        // Without a window the partition's first page does not depend on the
+        // length: its first ring of block ids is requested together with the
+        // length (entries past the sequence are read but not used).
+        const bool no_window = p.window == 0;
+        const int pg_first = (r * p.P) / kBlock;
+        int32_t id_early = 0;
+        if (no_window && lane < kCluStages && pg_first + lane < p.max_blocks)
+            id_early = p.block_tables[static_cast<int64_t>(b) * p.table_stride + pg_first + lane];
         const int n = seq_len(p, b, r == 0 && g == 0 && lane == 0);
         n_seq = n;
         int tok0, tok1, pg0, np;
@@ -1964,16 +1972,16 @@ __global__ void __launch_bounds__(kCluThreads, CluCfg<D, G>::kMinBlocks)
         // Pages go round the ring kCluStages at a time, lane j issuing page
         // base + j into stage j.  An id outside the pool reads block 0
         // instead (flagged) and takes no appended row.
-        auto load_id = [&](int i) {
-            int32_t id = 0;
-            if (i < np) {
-                id = p.block_tables[static_cast<int64_t>(b) * p.table_stride + pg0 + i];
-                if (id < 0 || id >= p.num_blocks) {
-                    raise_flag(p.err_flag, XS_FLAG_BAD_BLOCK);
-                    id = -1;
-                }
+        auto check_id = [&](int32_t id) {
+            if (id < 0 || id >= p.num_blocks) {
+                raise_flag(p.err_flag, XS_FLAG_BAD_BLOCK);
+                id = -1;
             }
             return id;
+        };
+        auto load_id = [&](int i) {
+            return i < np ? check_id(p.block_tables[static_cast<int64_t>(b) * p.table_stride + pg0 + i])
+                          : 0;
         };
         int my_last = -1;  // the last page this lane issued (its stage's last phase)
         auto issue = [&](int i, int32_t id) {
@@ -1989,7 +1997,7 @@ __global__ void __launch_bounds__(kCluThreads, CluCfg<D, G>::kMinBlocks)
             my_last = i;
         };
         const bool first = lane < kCluStages && lane < np;
-        const int32_t id0 = first ? load_id(lane) : 0;
+        const int32_t id0 = !first ? 0 : no_window ? check_id(id_early) : load_id(lane);
         if (first && lane != last) issue(lane, id0);
         if (p.early) {
             griddep_wait();
@@ -2049,11 +2057,25 @@ __global__ void __launch_bounds__(kCluThreads, CluCfg<D, G>::kMinBlocks)
         griddep_wait();
         griddep_launch_dependents();
         const int cw = warp - 1;
+        const int grp = lane >> 2, tq = lane & 3;
+        // The G query rows straight from global memory into the B fragments
+        // (lane quad grp holds head grp; rows G..7 zero), requested together
+        // with the length: one round trip after the launch wait, nothing
+        // staged.
+        uint32_t qa[D / 16][2];
+        const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
+            static_cast<const unsigned char *>(p.q) +
+            ((static_cast<int64_t>(b) * p.Hq + static_cast<int64_t>(g) * G + (grp < G ? grp : 0)) *
+             C::kRowBytes));
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+            qa[ks][0] = grp < G ? qrow[8 * ks + tq] : 0u;
+            qa[ks][1] = grp < G ? qrow[8 * ks + 4 + tq] : 0u;
+        }
         const int n = seq_len(p, b, false);
         n_seq = n;
         int tok0, tok1, pg0, np;
         range(n, tok0, tok1, pg0, np);
-        const int grp = lane >> 2, tq = lane & 3;
         float m2[2] = {-INFINITY, -INFINITY}, l2[2] = {0.f, 0.f};
         float oacc[D / 16][4];
 #pragma unroll
@@ -2062,19 +2084,6 @@ __global__ void __launch_bounds__(kCluThreads, CluCfg<D, G>::kMinBlocks)
             for (int c = 0; c < 4; ++c) oacc[i][c] = 0.f;
         if (cw < np) {
             bool ok = true;
-            // The G query rows straight from global memory into the B
-            // fragments (lane quad grp holds head grp; rows G..7 zero): one
-            // round trip after the launch wait, nothing staged.
-            uint32_t qa[D / 16][2];
-            const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
-                static_cast<const unsigned char *>(p.q) +
-                ((static_cast<int64_t>(b) * p.Hq + static_cast<int64_t>(g) * G + (grp < G ? grp : 0)) *
-                     C::kRowBytes));
-#pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks) {
-                qa[ks][0] = grp < G ? qrow[8 * ks + tq] : 0u;
-                qa[ks][1] = grp < G ? qrow[8 * ks + 4 + tq] : 0u;
-            }
             for (int i = cw; ok && i < np; i += kCluConsumers) {
                 const int st = i % kCluStages;
                 if (!__all_sync(0xffffffffu,
