@@ -1122,8 +1122,10 @@ def main(argv=None):
                     help="also measure workloads 0-3 and the 8K/1K chunked prefill in the same "
                          "process and report them under 'rows' (auto: with the default "
                          "long-batch decode line)")
-    ap.add_argument("--row-steps", type=int, default=20,
-                    help="timed steps of each extra row")
+    ap.add_argument("--row-steps", type=int, default=200,
+                    help="timed steps of each extra row (enough that the first launch's "
+                         "host-side start, a few us before the GPU has work, is a small share "
+                         "of a row whose launches are tens of us)")
     ap.add_argument("--row-load-seconds", type=float, default=0.4,
                     help="untimed load before each extra row's timed region")
     ap.add_argument("--row-cpu-seconds", type=float, default=3.0,

@@ -532,7 +532,11 @@ int xs_paged_decode_step_partition_tokens(int B, int Hq, int Hkv, int64_t total_
  * (D = 64 or 128) when the tokens a sequence can hold (max_blocks_per_seq * 16, or
  * the window when smaller) split into at most 16 partitions of at most 192
  * pages (191 with a window) and all B * Hkv clusters fit the device at once;
- * the largest such size is taken (at most one CTA per 64 tokens).  Only the
+ * the largest such size is taken (at most one CTA per 64 tokens), except
+ * that a launch of short partitions (at most 32 pages) which would fill
+ * every cluster slot takes the largest smaller size that leaves a slot free
+ * (so the next launch can start early), if that adds at most half again to
+ * the pages of a CTA.  Only the
  * shape decides: B, Hq, Hkv, D, max_blocks_per_seq, window and dtype are
  * those of the step.  XS_ESHAPE for a negative size, Hq % Hkv != 0.
  */

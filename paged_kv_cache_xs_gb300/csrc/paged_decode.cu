@@ -1847,6 +1847,9 @@ constexpr int kCluMaxSize = 16;   // CTAs per cluster (the non-portable maximum)
 // persistent grid over every SM (a 32768-token sequence split 12 ways is
 // 171 pages a CTA: 27.5 against 30.8 us); beyond, the persistent grid.
 constexpr int kCluMaxPartPages = 192;
+// Pages of a partition up to which a launch trades larger partitions for a
+// spare cluster slot (cluster_plan).
+constexpr int kCluSpareMaxPages = 32;
 
 template <int D, int G>
 struct CluCfg {
@@ -2361,9 +2364,12 @@ int cluster_capacity(KernelFn fn, int smem, int cs) {
 // table's reach, or the window - split into cs partitions of at most
 // kCluMaxPartPages pages (one fewer with a window) with all B * Hkv clusters
 // resident at once.  The largest such cs up to 16 (and no more than one
-// partition per 64 tokens) is taken: the fewer pages a CTA holds, the
-// shorter the launch.  Returns cs (0: the persistent grid) and sets the
-// partition length, kernel and shared memory.
+// partition per 64 tokens) is taken - the fewer pages a CTA holds, the
+// shorter the launch - unless it fills every cluster slot with partitions of
+// at most kCluSpareMaxPages pages: then the largest smaller cs that leaves a
+// slot free, if its partitions are at most half as long again.  Returns cs
+// (0: the persistent grid) and sets the partition length, kernel and shared
+// memory.
 int cluster_plan(int B, int Hkv, int D, int G, int max_blocks, int window, int dtype, int *P,
                  KernelFn *fn, int *smem) {
     if (dtype != XS_BF16 || static_cast<int64_t>(B) * Hkv > 65535) return 0;
@@ -2371,17 +2377,37 @@ int cluster_plan(int B, int Hkv, int D, int G, int max_blocks, int window, int d
     if (!*fn) return 0;
     int64_t L = static_cast<int64_t>(max_blocks) * kBlock;
     if (window > 0) L = std::min<int64_t>(L, window);
-    const int spare = window > 0 ? 1 : 0;  // a window's first token need not start a page
-    int cs = static_cast<int>(std::min<int64_t>(kCluMaxSize, (L + 63) / 64));
-    for (; cs >= 2; --cs) {
-        const int64_t part = ((L + cs - 1) / cs + kBlock - 1) / kBlock * kBlock;
-        if (part / kBlock + spare > kCluMaxPartPages) return 0;  // fewer CTAs only add pages
-        if (static_cast<int64_t>(B) * Hkv <= cluster_capacity(*fn, *smem, cs)) {
-            *P = static_cast<int>(part);
-            return cs;
+    const int extra = window > 0 ? 1 : 0;  // a window's first token need not start a page
+    const int64_t groups = static_cast<int64_t>(B) * Hkv;
+    auto part_of = [&](int cs) { return ((L + cs - 1) / cs + kBlock - 1) / kBlock * kBlock; };
+    int fit = 0;
+    for (int cs = static_cast<int>(std::min<int64_t>(kCluMaxSize, (L + 63) / 64)); cs >= 2; --cs) {
+        if (part_of(cs) / kBlock + extra > kCluMaxPartPages) return 0;  // fewer CTAs only add pages
+        if (groups <= cluster_capacity(*fn, *smem, cs)) {
+            fit = cs;
+            break;
         }
     }
-    return 0;
+    if (fit == 0) return 0;
+    // A launch that fills the device's cluster slots exactly leaves the next
+    // launch nowhere to start until it ends; with a slot to spare, the next
+    // layer's first clusters begin (and read their pages early) while this
+    // one finishes.  For short partitions that overlap is worth more than a
+    // few extra pages a CTA: measured per layer, one 4,097-token sequence
+    // with 8 KV heads ran 6.26 us at cs = 12 (8 slots, 22 pages a CTA) and
+    // 5.64 us at cs = 10 (13 slots, 26 pages); at 8,192 tokens (43 pages at
+    // cs = 12) the extra pages cost more (9.78 against 10.24 us).
+    int cs = fit;
+    const int64_t fit_pages = part_of(fit) / kBlock;
+    if (groups == cluster_capacity(*fn, *smem, fit) && fit_pages <= kCluSpareMaxPages) {
+        for (int c = fit - 1; c >= 2 && 2 * (part_of(c) / kBlock) <= 3 * fit_pages; --c)
+            if (groups < cluster_capacity(*fn, *smem, c)) {
+                cs = c;
+                break;
+            }
+    }
+    *P = static_cast<int>(part_of(cs));
+    return cs;
 }
 
 struct DeviceInfo {

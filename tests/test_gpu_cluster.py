@@ -83,10 +83,11 @@ def test_which_launches_run_as_clusters():
     assert size(1, 4, 1, 128, 8, 0, bf16) == 2
     assert size(1, 4, 1, 128, 4, 0, bf16) == 0
     assert size(1, 4, 1, 128, 1000, 64, bf16) == 0
-    # Eight KV heads of one 4097-token sequence: eight clusters, as large as
-    # the device holds eight of at once; more groups, smaller clusters.
+    # Eight KV heads of one 4097-token sequence: eight clusters, a little
+    # smaller than the largest eight of which fit at once, so that a slot is
+    # left for the next launch; more groups, smaller clusters.
     single = size(1, 32, 8, 128, 257, 0, bf16)
-    assert 11 <= single <= 16   # at most 24 pages a CTA: at least 11 CTAs
+    assert 8 <= single <= 16
     assert 2 <= size(4, 32, 8, 128, 63, 0, bf16) <= single
     # D = 64 runs two CTAs per SM: the GPT-2 shape (8 sequences, 12 heads)
     # fits where D = 128 would not.
@@ -270,3 +271,50 @@ def test_layers_back_to_back_in_a_cuda_graph():
         torch.cuda.synchronize()
         torch.testing.assert_close(outs[layer].float(), other.float(), atol=1e-2, rtol=0)
     assert step.error_flags() == 0
+
+
+def test_decode_loop_in_a_graph_with_a_growing_sequence():
+    # One sequence, 8 KV heads: a step captured once and replayed 40 times
+    # while the sequence grows from 1041 to 1080 tokens (a table of 70 pages,
+    # so the launch's partitions stay fixed while the sequence crosses
+    # page boundaries and a partition boundary).  Each replay reads the new
+    # length, q and rows from the captured buffers; every step's append and
+    # attention match the oracle's.
+    from paged_kv_cache_xs_gb300.step import PagedDecodeStep
+    dev = gh.device()
+    cfg = wl.custom_config(1, 32, 8, 128, torch.bfloat16, history=("fixed", (1040,)),
+                           pool=("factor", 3.0), seed=960)
+    w = wl.make_workload(cfg, device=dev)
+    width = 70
+    used = w.block_tables[0, :w.max_blocks_per_seq].tolist()
+    spare = [i for i in range(w.num_blocks) if i not in set(used)][:width - len(used)]
+    bt = torch.tensor([used + spare], dtype=torch.int32, device=dev)
+    assert bt.shape[1] == width
+    w.block_tables = bt
+    assert _cluster_size(w) > 0
+    step = PagedDecodeStep(cfg.B, cfg.Hq, cfg.Hkv, cfg.D, width, cfg.dtype, dev,
+                           partition_tokens=256)
+    out = torch.empty(cfg.B, cfg.Hq, cfg.D, dtype=cfg.dtype, device=dev)
+    q, kn, vn = w.q[0].clone(), w.k_new[0].clone(), w.v_new[0].clone()
+    lens = w.context_lens.clone()
+    graph = CapturedStep(lambda: step.run(out, q, kn, vn, w.k_cache[0], w.v_cache[0], bt, lens,
+                                          w.scale, early_reads=True))
+    g = torch.Generator(device=dev).manual_seed(961)
+    lens.fill_(1041)
+    graph.replay()  # (the capture's warm-up appended at 1041 too: replay it once more first)
+    torch.cuda.synchronize()
+    kc, vc = w.k_cache[0].cpu(), w.v_cache[0].cpu()
+    for n in range(1041, 1081):
+        lens.fill_(n)
+        q.copy_(torch.randn(q.shape, generator=g, device=dev).to(cfg.dtype))
+        kn.copy_(torch.randn(kn.shape, generator=g, device=dev).to(cfg.dtype))
+        vn.copy_(torch.randn(vn.shape, generator=g, device=dev).to(cfg.dtype))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert step.error_flags() == 0
+        slots = oracle.slot_mapping(bt.cpu(), lens.cpu(), gh.BS, w.num_blocks)
+        kc, vc = oracle.kv_append(kn.cpu(), vn.cpu(), kc, vc, slots)
+        assert torch.equal(gh.int_view(w.k_cache[0].cpu()), gh.int_view(kc)), f"n={n}"
+        assert torch.equal(gh.int_view(w.v_cache[0].cpu()), gh.int_view(vc)), f"n={n}"
+        ref = oracle.paged_decode(q.cpu(), kc, vc, bt.cpu(), lens.cpu(), w.scale)
+        gh.assert_close(out, ref, torch.bfloat16, what=f"n={n}")
