@@ -572,7 +572,7 @@ def decode_row(args, idx: int, rank, world, local, dist) -> dict:
         "pct_of_hbm_peak": {"of_measured": round(100 * m["value"] / world / peak, 2),
                             "of_nominal_8TBps": round(100 * m["value"] / world / NOMINAL_HBM_GBS,
                                                       2), "peak_kind": peak_kind},
-        "roofline": decode_roofline(m),
+        "roofline": decode_roofline(m, kernel_traffic(cfg.name) if m["fused"] else None),
         "dtype": "bf16" if cfg.dtype == torch.bfloat16 else "f32",
         "config": {"B": cfg.B, "Hq": cfg.Hq, "Hkv": cfg.Hkv, "D": cfg.D, "layers": m["L"],
                    "context_tokens": m["w"].total_context_tokens,
