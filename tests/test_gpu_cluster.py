@@ -318,3 +318,21 @@ def test_decode_loop_in_a_graph_with_a_growing_sequence():
         assert torch.equal(gh.int_view(w.v_cache[0].cpu()), gh.int_view(vc)), f"n={n}"
         ref = oracle.paged_decode(q.cpu(), kc, vc, bt.cpu(), lens.cpu(), w.scale)
         gh.assert_close(out, ref, torch.bfloat16, what=f"n={n}")
+
+
+@pytest.mark.parametrize("window", [6000, 3001])
+def test_window_over_a_long_sequence(window):
+    # One 16,384-token sequence with sinks and a window whose first token
+    # does not start a page: the window's partitions (one page more than
+    # their length, for the unaligned start) run past the 24-stage ring at
+    # window 6000.
+    dev = gh.device()
+    cfg = wl.custom_config(1, 32, 8, 128, torch.bfloat16, history=("fixed", (16383,)),
+                           pool=("factor", 1.1), seed=970 + window)
+    w = wl.make_workload(cfg, device=dev)
+    assert _cluster_size(w, window) > 0
+    g = torch.Generator(device=dev).manual_seed(window)
+    sinks = (torch.randn(cfg.Hq, generator=g, device=dev) * 2).to(cfg.dtype)
+    ek, ev = _appended(w)
+    out, err = _step(w, _ws(w), sinks=sinks, window=window, early=True)
+    _check(w, out, err, ek, ev, sinks=sinks, window=window, what=f"window={window}")
