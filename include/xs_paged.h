@@ -373,6 +373,33 @@ int xs_paged_decode_reduce(void *out, const float *part_o, const float *part_m,
                            cudaStream_t stream);
 
 /*
+ * xs_paged_decode_attn_splits, xs_paged_decode_reduce_splits - the two
+ * passes with the split given as a count, as in the survey's sketch of this
+ * boundary: num_splits >= 1 partitions of
+ *     P = round_up(ceil(max_blocks_per_seq * block_size / num_splits), 16)
+ * tokens cover the longest sequence the table can hold, so partials sized by
+ * xs_paged_decode_workspace_bytes(B, Hq, D, num_splits) hold every split.
+ * They are xs_paged_decode_attn / xs_paged_decode_reduce with
+ * partition_tokens = P and max_partitions = num_splits (and no work
+ * counters); a sequence shorter than P still gets its out[b] from the first
+ * pass, so out is required in both.  With num_splits == 1 every sequence is
+ * one partition, out is final after the first pass and the partials may be
+ * NULL; the second pass then does nothing.  The reduce takes
+ * max_blocks_per_seq and block_size to derive the same P.  XS_ESHAPE for
+ * num_splits <= 0; other arguments and errors as the two passes.
+ */
+int xs_paged_decode_attn_splits(void *out, float *part_o, float *part_m, float *part_l,
+                                const void *q, const void *k_cache, const void *v_cache,
+                                const int32_t *block_tables, int max_blocks_per_seq,
+                                const int32_t *context_lens, int B, int Hq, int Hkv, int D,
+                                int block_size, int64_t num_blocks, float scale, int num_splits,
+                                int dtype, int *err_flag, cudaStream_t stream);
+int xs_paged_decode_reduce_splits(void *out, const float *part_o, const float *part_m,
+                                  const float *part_l, const int32_t *context_lens,
+                                  int max_blocks_per_seq, int B, int Hq, int D, int block_size,
+                                  int num_splits, int dtype, cudaStream_t stream);
+
+/*
  * xs_paged_decode - xs_paged_decode_attn followed, when max_partitions > 1,
  * by xs_paged_decode_reduce on the same stream.
  */
@@ -517,7 +544,7 @@ int xs_paged_decode_step_ex(void *out, const void *q, const void *k_new, const v
  * fitted to one-launch step times, with whole rounds of the grid when every
  * sequence has the same length (total_context_tokens = B * max_context_len)
  * and a cost per partition of the longest sequence for its split-K combine,
- * searched over multiples of 64 in [64, 2048] (64, 128, ..., 512, 640, 768,
+ * searched over multiples of 64 in [64, 2048] (64, 128, ..., 576, 640, 768,
  * 896, 1024, 1280, 1536, 2048) so that a batch's item count can land just
  * under a whole number of rounds of the grid.  Same arguments plus Hq;
  * XS_ESHAPE also when Hq % Hkv != 0.

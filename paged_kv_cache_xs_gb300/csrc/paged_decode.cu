@@ -2635,15 +2635,16 @@ extern "C" int xs_paged_decode_step_partition_tokens(int B, int Hq, int Hkv,
     // and the split-K combine at the end of the longest sequence adds
     // kCombineCost per partition.  P runs over multiples of 64 so that a
     // batch can land just under a whole number of rounds.  Fitted to a sweep
-    // of every candidate P on 14 workloads (log-uniform mixes of 16-256
-    // sequences, equal-length batches of 1-16 sequences, the GQA and MHA
-    // shapes, the long batch): mean 0.7 % and at most 2.1 % slower than the
-    // best measured P.
-    constexpr double kItemCost = 1.5;
-    constexpr double kTailRounds = 0.4;
+    // of every candidate P on the 11 shapes of the persistent grid
+    // (launches too large for one wave of thread-block clusters: log-uniform
+    // mixes of 48-256 sequences, equal-length batches of 32-64 sequences, a
+    // uniform-length batch, the long batch), launched back to back: mean
+    // 0.6 % and at most 2.1 % slower than the best measured P.
+    constexpr double kItemCost = 2.25;
+    constexpr double kTailRounds = 0.5;
     constexpr double kCombineCost = 0.2;
-    constexpr int kCandidates[] = {64,  128, 192, 256, 320,  384,  448, 512,
-                                   640, 768, 896, 1024, 1280, 1536, 2048};
+    constexpr int kCandidates[] = {64,  128, 192, 256,  320,  384,  448,  512,
+                                   576, 640, 768, 896, 1024, 1280, 1536, 2048};
     const double ctas = 2.0 * num_sms;
     const int longest = std::max(max_context_len, 1);
     const bool uniform = tokens >= 0.98 * static_cast<double>(B) * longest;
@@ -2899,6 +2900,43 @@ extern "C" int xs_paged_decode_reduce(void *out, const float *part_o, const floa
                                       int dtype, cudaStream_t stream) {
     return launch_reduce(out, part_o, part_m, part_l, context_lens, nullptr, 0, B, Hq, D,
                          partition_tokens, max_partitions, dtype, stream);
+}
+
+// The partition length for a split given as a count (num_splits partitions
+// cover the table's reach), or XS_ESHAPE.
+static int splits_partition(int max_blocks_per_seq, int block_size, int num_splits) {
+    if (num_splits <= 0 || max_blocks_per_seq < 0 || block_size <= 0) return XS_ESHAPE;
+    const int64_t cap = static_cast<int64_t>(max_blocks_per_seq) * block_size;
+    const int64_t per = (cap + num_splits - 1) / num_splits;
+    const int64_t P = std::max<int64_t>(attn::kBlock, (per + attn::kBlock - 1) / attn::kBlock *
+                                                          attn::kBlock);
+    return P > 0x7fffffff ? XS_ESHAPE : static_cast<int>(P);
+}
+
+extern "C" int xs_paged_decode_attn_splits(void *out, float *part_o, float *part_m,
+                                           float *part_l, const void *q, const void *k_cache,
+                                           const void *v_cache, const int32_t *block_tables,
+                                           int max_blocks_per_seq, const int32_t *context_lens,
+                                           int B, int Hq, int Hkv, int D, int block_size,
+                                           int64_t num_blocks, float scale, int num_splits,
+                                           int dtype, int *err_flag, cudaStream_t stream) {
+    const int P = splits_partition(max_blocks_per_seq, block_size, num_splits);
+    if (P < 0) return P;
+    return xs_paged_decode_attn(out, part_o, part_m, part_l, q, k_cache, v_cache, block_tables,
+                                max_blocks_per_seq, context_lens, B, Hq, Hkv, D, block_size,
+                                num_blocks, scale, P, num_splits, dtype, err_flag, nullptr, stream);
+}
+
+extern "C" int xs_paged_decode_reduce_splits(void *out, const float *part_o, const float *part_m,
+                                             const float *part_l, const int32_t *context_lens,
+                                             int max_blocks_per_seq, int B, int Hq, int D,
+                                             int block_size, int num_splits, int dtype,
+                                             cudaStream_t stream) {
+    const int P = splits_partition(max_blocks_per_seq, block_size, num_splits);
+    if (P < 0) return P;
+    if (num_splits == 1) return XS_OK;  // every sequence was one partition
+    return xs_paged_decode_reduce(out, part_o, part_m, part_l, context_lens, B, Hq, D, P,
+                                  num_splits, dtype, stream);
 }
 
 extern "C" int xs_paged_decode_reduce_sinks(void *out, const float *part_o, const float *part_m,

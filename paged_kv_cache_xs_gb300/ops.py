@@ -70,6 +70,9 @@ SIGNATURES = {
                                      _I, _L, _F, _I, _I, _P, _P, _P, _P, _I, _I, _P, _P]),
     "xs_paged_decode_step_counters": (_L, [_I, _I]),
     "xs_paged_decode_step_cluster_size": (_I, [_I, _I, _I, _I, _I, _I, _I]),
+    "xs_paged_decode_attn_splits": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I,
+                                         _I, _L, _F, _I, _I, _P, _P]),
+    "xs_paged_decode_reduce_splits": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P]),
     "xs_paged_decode_step_partition_tokens": (_I, [_I, _I, _I, _L, _I, _I]),
     "xs_version": (_I, []),
     "xs_debug_bounds_failures": (_I, [_I]),
@@ -286,6 +289,22 @@ def xs_paged_decode_step_counters(B: int, Hkv: int) -> int:
     if n < 0:
         raise XsError("xs_paged_decode_step_counters", n)
     return n
+
+
+def xs_paged_decode_splits(out, part_o, part_m, part_l, q, k_cache, v_cache, block_tables,
+                           context_lens, scale, num_splits, err_flag=None, stream=None):
+    """The two passes with the split given as a count (xs_paged_decode_attn_splits,
+    then xs_paged_decode_reduce_splits); partials sized for num_splits."""
+    B, Hq, D = q.shape
+    num_blocks, Hkv, bs, _ = k_cache.shape
+    mb = block_tables.shape[1]
+    _call("xs_paged_decode_attn_splits", _ptr(out), _ptr(part_o), _ptr(part_m), _ptr(part_l),
+          _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), mb, _ptr(context_lens), B,
+          Hq, Hkv, D, bs, num_blocks, float(scale), int(num_splits), dtype_code(q.dtype),
+          _ptr(err_flag), _stream(stream))
+    _call("xs_paged_decode_reduce_splits", _ptr(out), _ptr(part_o), _ptr(part_m), _ptr(part_l),
+          _ptr(context_lens), mb, B, Hq, D, bs, int(num_splits), dtype_code(q.dtype),
+          _stream(stream))
 
 
 def xs_paged_decode_step_cluster_size(B, Hq, Hkv, D, max_blocks_per_seq, window, dtype) -> int:

@@ -78,21 +78,23 @@ def test_partition_heuristic(lib):
 
 
 def test_step_partition_heuristic(lib):
-    # The one-launch step's choice on measured workloads.  Its constants were
-    # fitted to one-launch step times swept over every candidate P: the
-    # continuous-batching mix (64 sequences) ran 41.96 / 41.60 / 43.83 us at
-    # P = 448 / 512 / 640; the single stream was fastest at 256 (33
-    # partitions at 128 cost more in the combine); the long batch is fastest
-    # at 2048; equal-length batches land on a whole round of 304 CTAs: 4 x
-    # 4097 tokens at 512 (256 items), 8 x 2049 and 16 x 1025 at 640 (256
-    # items; 448 gives 320 items, a second round, +22 %), 1 x 1025 at 128.
+    # The one-launch step's choice on measured workloads (the persistent grid;
+    # launches small enough for one wave of clusters take their own split).
+    # Its constants were fitted to per-launch times swept over every
+    # candidate P, launched back to back: the continuous-batching mix (64
+    # sequences) ran 41.05 / 40.60 / 40.69 / 42.80 us at P = 448 / 512 / 576 /
+    # 640; 48 log-uniform sequences 38.56 / 36.42 / 37.63 at 448 / 512 / 576;
+    # the long batch is fastest at 2048.  Equal-length batches land on a
+    # whole round of 304 CTAs: 4 x 4097 tokens at 512 (256 items), 8 x 2049
+    # and 16 x 1025 at 576 (256 items, each shorter than at 640).
     pick = ops.xs_paged_decode_step_partition_tokens
-    assert pick(64, 32, 8, 63638, 7598, 152) == 448
+    assert pick(64, 32, 8, 63638, 7598, 152) == 512
+    assert pick(48, 32, 8, 55827, 7399, 152) == 512
     assert pick(1, 32, 8, 4097, 4097, 152) == 256
     assert pick(128, 32, 8, 2538762, 32769, 152) == 2048
     assert pick(4, 32, 8, 16388, 4097, 152) == 512
-    assert pick(8, 32, 8, 8 * 2049, 2049, 152) == 640
-    assert pick(16, 32, 8, 16 * 1025, 1025, 152) == 640
+    assert pick(8, 32, 8, 8 * 2049, 2049, 152) == 576
+    assert pick(16, 32, 8, 16 * 1025, 1025, 152) == 576
     assert pick(1, 32, 8, 1025, 1025, 152) in (128, 192)
     for B, Hq, Hkv, total, mx in [(8, 12, 12, 3439, 926), (2, 12, 12, 29, 21), (512, 32, 8, 10**6, 8193)]:
         P = pick(B, Hq, Hkv, total, mx, 152)
@@ -285,3 +287,15 @@ def test_wait_injection_is_debug_only(lib):
     dbg = ops.load_debug()
     assert dbg.xs_debug_wait_injection(0, -1) == -2              # XS_ESHAPE: no limit
     assert dbg.xs_debug_wait_injection(1_000_000, -2) == -2      # XS_ESHAPE: bad page
+
+
+def test_num_splits_form_validation(lib):
+    # The split as a count: num_splits <= 0 is refused before anything else;
+    # B == 0 does nothing; num_splits == 1 needs no partials and no reduce.
+    f, r = lib.xs_paged_decode_attn_splits, lib.xs_paged_decode_reduce_splits
+    base = [A, A, A, A, A, A, A, A, 4, A, 2, 8, 2, 128, 16, 10, 0.1]
+    assert f(*base, 0, 1, None, None) == -2
+    assert f(*base, -3, 1, None, None) == -2
+    assert r(A, A, A, A, A, 4, 2, 8, 128, 16, 0, 1, None) == -2
+    assert f(A, A, A, A, A, A, A, A, 4, A, 0, 8, 2, 128, 16, 10, 0.1, 3, 1, None, None) == 0
+    assert r(A, None, None, None, A, 4, 2, 8, 128, 16, 1, 1, None) == 0

@@ -228,3 +228,26 @@ def test_early_reads_in_a_cuda_graph():
     assert int(err.item()) == 0 and int(ws.work.count_nonzero()) == 0
     for layer in range(L):
         gh.assert_close(outs[layer], refs[layer], torch.bfloat16, what=f"layer {layer}")
+
+
+@pytest.mark.parametrize("num_splits", [1, 3, 8])
+def test_num_splits_form_matches_oracle(num_splits):
+    # xs_paged_decode_attn_splits + xs_paged_decode_reduce_splits: the split
+    # as a count for the whole batch, partials sized for num_splits.
+    dev = gh.device()
+    cfg = wl.custom_config(7, 32, 8, 128, torch.bfloat16, history=("loguniform", (1, 3000)),
+                           pool=("factor", 1.3), seed=990 + num_splits)
+    w = wl.make_workload(cfg, device=dev)
+    B, Hq, D = cfg.B, cfg.Hq, cfg.D
+    part_o = torch.empty(B, Hq, num_splits, D, dtype=torch.float32, device=dev)
+    part_m = torch.empty(B, Hq, num_splits, dtype=torch.float32, device=dev)
+    part_l = torch.empty(B, Hq, num_splits, dtype=torch.float32, device=dev)
+    out = torch.full((B, Hq, D), float("nan"), dtype=cfg.dtype, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    ops.xs_paged_decode_splits(out, part_o, part_m, part_l, w.q[0], w.k_cache[0], w.v_cache[0],
+                               w.block_tables, w.context_lens, w.scale, num_splits, err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    ref = oracle.paged_decode(w.q[0].cpu(), w.k_cache[0].cpu(), w.v_cache[0].cpu(),
+                              w.block_tables.cpu(), w.context_lens.cpu(), w.scale)
+    gh.assert_close(out, ref, cfg.dtype, what=f"num_splits={num_splits}")
