@@ -36,6 +36,11 @@
 //    first pages are read before waiting on the previous launch (in a launch
 //    of at most 16 rounds of items, the first item's next pages are also
 //    prefetched into L2).
+//  * Small one-launch steps (every (sequence, KV head) group in one wave of
+//    thread-block clusters: a single stream, small batches) run a second
+//    kernel instead, paged_decode_cluster_kernel: one cluster per group, CTA
+//    r taking partition r, the split-K combine over distributed shared
+//    memory after a cluster barrier (see its own comment).
 //  * Logits are kept in base-2 units (q is pre-scaled by scale*log2(e)) so
 //    exponentials are single ex2 instructions.
 #include <cuda.h>
@@ -2379,6 +2384,10 @@ int cluster_plan(int B, int Hkv, int D, int G, int max_blocks, int window, int d
     if (window > 0) L = std::min<int64_t>(L, window);
     const int extra = window > 0 ? 1 : 0;  // a window's first token need not start a page
     const int64_t groups = static_cast<int64_t>(B) * Hkv;
+    // More groups than even the smallest clusters can hold at once: no
+    // cluster size fits (the common case for large batches, settled here
+    // with one cached lookup).
+    if (groups > cluster_capacity(*fn, *smem, 2)) return 0;
     auto part_of = [&](int cs) { return ((L + cs - 1) / cs + kBlock - 1) / kBlock * kBlock; };
     int fit = 0;
     for (int cs = static_cast<int>(std::min<int64_t>(kCluMaxSize, (L + 63) / 64)); cs >= 2; --cs) {
