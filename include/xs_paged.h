@@ -164,6 +164,40 @@ int xs_prefill_append(const void *k_src, const void *v_src, void *k_cache, void 
                       cudaStream_t stream);
 
 /*
+ * XS_PREFILL_OVERLAP - lets the launches of a chunked prefill overlap: chunk
+ * c + 1's append and attention may start while chunk c's attention is still
+ * running, on the SMs it leaves idle.
+ *
+ * xs_prefill_append_ex with this flag is launched programmatically dependent
+ * on the previous kernel on the stream and does not wait for it: the caller
+ * promises that kernel (if still running) writes none of k_src, v_src and
+ * block_ids, and reads or writes none of the rows this launch appends - true
+ * when it is the attention of the previous chunk of the same sequence, which
+ * reads positions before start_pos only.
+ *
+ * xs_paged_prefill_tc_ex with this flag is launched programmatically
+ * dependent on the previous kernel and reads q, block_ids and the K/V rows
+ * of positions before start_pos (key tiles that end before it) before
+ * waiting for that kernel; the rows from start_pos on, and every write, wait
+ * for it.  The caller promises the previous kernel writes none of what is
+ * read early - true when it is this chunk's append (which writes positions
+ * from start_pos on) launched with the same flag behind the previous chunk's
+ * attention.  Its successor may start once that wait has returned, so a
+ * chain append(c), attention(c), append(c + 1), ... never lets a launch read
+ * rows whose append has not completed: each attention's wait covers its own
+ * chunk's append, which started only after the previous attention's wait
+ * covered the append before it.
+ *
+ * flags 0 is xs_prefill_append / xs_paged_prefill_tc; unknown bits are
+ * XS_EUNSUPPORTED.
+ */
+#define XS_PREFILL_OVERLAP 1
+int xs_prefill_append_ex(const void *k_src, const void *v_src, void *k_cache, void *v_cache,
+                         const int32_t *block_ids, int n_ids, int T, int Hkv, int D,
+                         int block_size, int64_t num_blocks, int start_pos, int flags, int dtype,
+                         int *err_flag, cudaStream_t stream);
+
+/*
  * xs_paged_prefill_attn / xs_paged_prefill_reduce / xs_paged_prefill -
  * causal attention of a T-token prefill chunk over one sequence's paged
  * cache (the chunk already appended): query token i (q [T, Hq, D], out
@@ -211,6 +245,11 @@ int xs_paged_prefill_tc(void *out, const void *q, const void *k_cache, const voi
                         const int32_t *block_ids, int n_ids, int T, int start_pos, int Hq,
                         int Hkv, int D, int block_size, int64_t num_blocks, float scale,
                         int dtype, int *err_flag, cudaStream_t stream);
+/* xs_paged_prefill_tc with launch flags (XS_PREFILL_OVERLAP, above). */
+int xs_paged_prefill_tc_ex(void *out, const void *q, const void *k_cache, const void *v_cache,
+                           const int32_t *block_ids, int n_ids, int T, int start_pos, int Hq,
+                           int Hkv, int D, int block_size, int64_t num_blocks, float scale,
+                           int flags, int dtype, int *err_flag, cudaStream_t stream);
 
 /*
  * xs_block_alloc_decode - the page allocation of one decode step, on the

@@ -96,6 +96,11 @@ __global__ void __launch_bounds__(kAppendThreads)
                           const int32_t *__restrict__ block_ids, int n_ids, int T, int Hkv,
                           int chunks_per_row, int bs, int64_t num_blocks, int start,
                           int *err_flag) {
+    // Launched programmatically dependent on the previous kernel only when
+    // the caller promised it does not wait for it (XS_PREFILL_OVERLAP): then
+    // the next launch (this chunk's attention) may be placed at once.  (A
+    // no-op in a launch made without the attribute.)
+    griddep_launch_dependents();
     const int64_t per_token = static_cast<int64_t>(Hkv) * chunks_per_row;
     const int64_t total = static_cast<int64_t>(T) * 2 * per_token;
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
@@ -201,6 +206,16 @@ extern "C" int xs_prefill_append(const void *k_src, const void *v_src, void *k_c
                                  void *v_cache, const int32_t *block_ids, int n_ids, int T,
                                  int Hkv, int D, int block_size, int64_t num_blocks, int start_pos,
                                  int dtype, int *err_flag, cudaStream_t stream) {
+    return xs_prefill_append_ex(k_src, v_src, k_cache, v_cache, block_ids, n_ids, T, Hkv, D,
+                                block_size, num_blocks, start_pos, 0, dtype, err_flag, stream);
+}
+
+extern "C" int xs_prefill_append_ex(const void *k_src, const void *v_src, void *k_cache,
+                                    void *v_cache, const int32_t *block_ids, int n_ids, int T,
+                                    int Hkv, int D, int block_size, int64_t num_blocks,
+                                    int start_pos, int flags, int dtype, int *err_flag,
+                                    cudaStream_t stream) {
+    if (flags & ~XS_PREFILL_OVERLAP) return XS_EUNSUPPORTED;
     if (!k_src || !v_src || !k_cache || !v_cache || !block_ids) return XS_ENULL;
     const int eb = xs::elem_bytes(dtype);
     if (!eb) return XS_EDTYPE;
@@ -216,9 +231,23 @@ extern "C" int xs_prefill_append(const void *k_src, const void *v_src, void *k_c
     const int64_t total = static_cast<int64_t>(T) * 2 * Hkv * chunks;
     const int64_t blocks64 = (total + xs::kAppendThreads - 1) / xs::kAppendThreads;
     const int grid = static_cast<int>(blocks64 < (1 << 20) ? blocks64 : (1 << 20));
-    xs::prefill_append_kernel<<<grid, xs::kAppendThreads, 0, stream>>>(
-        static_cast<const uint4 *>(k_src), static_cast<const uint4 *>(v_src),
-        static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), block_ids, n_ids, T, Hkv,
-        chunks, block_size, num_blocks, start_pos, err_flag);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(xs::kAppendThreads);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    if (flags & XS_PREFILL_OVERLAP) {  // (the kernel never waits: the caller's promise)
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    if (cudaLaunchKernelEx(&cfg, xs::prefill_append_kernel, static_cast<const uint4 *>(k_src),
+                           static_cast<const uint4 *>(v_src), static_cast<uint4 *>(k_cache),
+                           static_cast<uint4 *>(v_cache), block_ids, n_ids, T, Hkv, chunks,
+                           block_size, num_blocks, start_pos, err_flag) != cudaSuccess) {
+        cudaGetLastError();
+        return XS_ELAUNCH;
+    }
     return xs::launch_status();
 }

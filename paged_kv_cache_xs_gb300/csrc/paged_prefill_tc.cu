@@ -105,6 +105,10 @@ struct PParams {
     int oob_row;                   // a row coordinate past the pool: zero-filled pages
     float qscale;                  // scale * log2(e)
     int *err_flag;
+    // Nonzero (XS_PREFILL_OVERLAP): q, the block ids and the key tiles that
+    // end before position start are read before waiting for the previous
+    // launch on the stream; the tiles from start on and every write after.
+    int early;
 };
 
 // Shared-memory matrix descriptor: start, leading and stride byte offsets,
@@ -290,7 +294,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             return row;
         };
+        // With p.early, the first tile that holds a position from start on
+        // (this chunk's rows, which the previous launch appends) waits for
+        // that launch, and the next launch may start once it has.
+        bool waited = !p.early;
+        auto gate = [&](int kt) {
+            if (!waited && (kt + 1) * kKeys > p.start) {
+                griddep_wait();
+                griddep_launch_dependents();
+                waited = true;
+            }
+        };
         auto issue = [&](int kt, int which, int row) {
+            gate(kt);
             const int s = kt % kStages;
             uint64_t *emp = which ? &v_empty[s] : &k_empty[s];
             uint64_t *ful = which ? &v_full[s] : &k_full[s];
@@ -320,6 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (ok) ++issued;
         }
         if (!ok && lane == 0) abort_now();
+        gate(ntiles);  // (every launch waits once, whatever it issued)
         // Let the copies this CTA issued land before it can exit.
         if (lane == 0) {
             mbar_wait_bounded(q_full, 0, kWaitLimitNs);
@@ -525,6 +542,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = __all_sync(0xffffffffu, mbar_wait_bounded(pv_done(qi), kt & 1, kWaitLimitNs));
             tc_fence_after();
         }
+        if (p.early) griddep_wait();  // writes come after the previous launch (no-op otherwise)
         if (!ok) {
             if (lane == 0) abort_now();
         } else if (my_ntiles > 0) {
@@ -633,6 +651,17 @@ extern "C" int xs_paged_prefill_tc(void *out, const void *q, const void *k_cache
                                    int T, int start_pos, int Hq, int Hkv, int D, int block_size,
                                    int64_t num_blocks, float scale, int dtype, int *err_flag,
                                    cudaStream_t stream) {
+    return xs_paged_prefill_tc_ex(out, q, k_cache, v_cache, block_ids, n_ids, T, start_pos, Hq,
+                                  Hkv, D, block_size, num_blocks, scale, 0, dtype, err_flag,
+                                  stream);
+}
+
+extern "C" int xs_paged_prefill_tc_ex(void *out, const void *q, const void *k_cache,
+                                      const void *v_cache, const int32_t *block_ids, int n_ids,
+                                      int T, int start_pos, int Hq, int Hkv, int D,
+                                      int block_size, int64_t num_blocks, float scale, int flags,
+                                      int dtype, int *err_flag, cudaStream_t stream) {
+    if (flags & ~XS_PREFILL_OVERLAP) return XS_EUNSUPPORTED;
     if (!out || !q || !k_cache || !v_cache || !block_ids) return XS_ENULL;
     if (dtype != XS_BF16) return dtype == XS_F32 ? XS_EUNSUPPORTED : XS_EDTYPE;
     if (T < 0 || start_pos < 0 || n_ids < 0 || Hq <= 0 || Hkv <= 0 || num_blocks < 0 ||
@@ -702,10 +731,25 @@ extern "C" int xs_paged_prefill_tc(void *out, const void *q, const void *k_cache
     p.oob_row = static_cast<int>(rows);
     p.qscale = scale * pftc::kLog2e;
     p.err_flag = err_flag;
+    p.early = (flags & XS_PREFILL_OVERLAP) ? 1 : 0;
     const int tq = pftc::kQTiles * pftc::kRows / G;  // query tokens per CTA
     const int64_t ctas = static_cast<int64_t>((T + tq - 1) / tq) * Hkv;
     if (ctas > 0x7fffffff) return XS_EUNSUPPORTED;
-    dim3 grid(static_cast<unsigned>(ctas));
-    fn<<<grid, pftc::kThreads, smem, stream>>>(tmq, tmk, tmv, p);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(ctas));
+    cfg.blockDim = dim3(pftc::kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    if (p.early) {
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    if (cudaLaunchKernelEx(&cfg, fn, tmq, tmk, tmv, p) != cudaSuccess) {
+        cudaGetLastError();
+        return XS_ELAUNCH;
+    }
     return launch_status();
 }

@@ -57,6 +57,8 @@ SIGNATURES = {
     "xs_block_alloc_decode": (_I, [_P, _I, _P, _I, _I, _P, _P, _P, _P]),
     "xs_block_free": (_I, [_P, _I, _P, _I, _P, _I, _I, _P, _P, _L, _P, _P]),
     "xs_prefill_append": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _L, _I, _I, _P, _P]),
+    "xs_prefill_append_ex": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _L, _I, _I, _I, _P,
+                                  _P]),
     "xs_paged_prefill_attn": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I,
                                    _L, _F, _I, _I, _I, _P, _P, _P]),
     "xs_paged_prefill_reduce": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P]),
@@ -64,6 +66,8 @@ SIGNATURES = {
                               _I, _I, _I, _P, _P, _P]),
     "xs_paged_prefill_tc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _L, _F, _I, _P,
                                  _P]),
+    "xs_paged_prefill_tc_ex": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _L, _F, _I,
+                                    _I, _P, _P]),
     "xs_paged_decode_step": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I,
                                   _I, _L, _F, _I, _I, _P, _P, _P, _P, _I, _P, _P]),
     "xs_paged_decode_step_ex": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I,
@@ -241,6 +245,7 @@ def xs_paged_decode(out, part_o, part_m, part_l, q, k_cache, v_cache, block_tabl
 
 XS_STEP_EARLY_READS = 1
 XS_STEP_PERSISTENT = 2
+XS_PREFILL_OVERLAP = 1
 
 
 def xs_paged_decode_step(out, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens,
@@ -274,14 +279,18 @@ def xs_paged_decode_step(out, q, k_new, v_new, k_cache, v_cache, block_tables, c
 
 
 def xs_paged_prefill_tc(out, q, k_cache, v_cache, block_ids, start_pos, scale, err_flag=None,
-                        stream=None):
+                        stream=None, overlap=False):
     """Causal attention of a prefill chunk (q [T, Hq, D]) over the paged
-    cache on the tensor cores (bf16); one launch, no workspace."""
+    cache on the tensor cores (bf16); one launch, no workspace.  ``overlap``
+    (XS_PREFILL_OVERLAP): q, the block ids and the rows before start_pos are
+    read before the previous kernel on the stream completes (it must write
+    none of them: e.g. this chunk's append launched with overlap)."""
     T, Hq, D = q.shape
     num_blocks, Hkv, bs, _ = k_cache.shape
-    _call("xs_paged_prefill_tc", _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+    _call("xs_paged_prefill_tc_ex", _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
           _ptr(block_ids), block_ids.numel(), T, int(start_pos), Hq, Hkv, D, bs, num_blocks,
-          float(scale), dtype_code(q.dtype), _ptr(err_flag), _stream(stream))
+          float(scale), XS_PREFILL_OVERLAP if overlap else 0, dtype_code(q.dtype),
+          _ptr(err_flag), _stream(stream))
 
 
 def xs_paged_decode_step_counters(B: int, Hkv: int) -> int:
@@ -393,13 +402,17 @@ def xs_block_free(seq_ids, block_tables, context_lens, free_stack, free_top,
 
 
 def xs_prefill_append(k_src, v_src, k_cache, v_cache, block_ids, start_pos, err_flag=None,
-                      stream=None):
-    """Write a [Hkv, T, D] chunk at positions start_pos .. of one sequence."""
+                      stream=None, overlap=False):
+    """Write a [Hkv, T, D] chunk at positions start_pos .. of one sequence.
+    ``overlap`` (XS_PREFILL_OVERLAP): the launch does not wait for the
+    previous kernel on the stream (which must write none of its inputs and
+    touch none of these rows: e.g. the previous chunk's attention)."""
     Hkv, T, D = k_src.shape
     num_blocks, _, bs, _ = k_cache.shape
-    _call("xs_prefill_append", _ptr(k_src), _ptr(v_src), _ptr(k_cache), _ptr(v_cache),
+    _call("xs_prefill_append_ex", _ptr(k_src), _ptr(v_src), _ptr(k_cache), _ptr(v_cache),
           _ptr(block_ids), block_ids.numel(), T, Hkv, D, bs, num_blocks, int(start_pos),
-          dtype_code(k_src.dtype), _ptr(err_flag), _stream(stream))
+          XS_PREFILL_OVERLAP if overlap else 0, dtype_code(k_src.dtype), _ptr(err_flag),
+          _stream(stream))
 
 
 def xs_paged_prefill(out, part_o, part_m, part_l, q, k_cache, v_cache, block_ids, start_pos,

@@ -299,3 +299,14 @@ def test_num_splits_form_validation(lib):
     assert r(A, A, A, A, A, 4, 2, 8, 128, 16, 0, 1, None) == -2
     assert f(A, A, A, A, A, A, A, A, 4, A, 0, 8, 2, 128, 16, 10, 0.1, 3, 1, None, None) == 0
     assert r(A, None, None, None, A, 4, 2, 8, 128, 16, 1, 1, None) == 0
+
+
+def test_prefill_overlap_flags_validated(lib):
+    # Unknown flag bits are refused first; XS_PREFILL_OVERLAP passes to the
+    # usual checks (a NULL pointer here).
+    app = lib.xs_prefill_append_ex
+    assert app(A, A, A, A, A, 4, 8, 2, 128, 16, 10, 0, 2, 1, None, None) == -5
+    assert app(None, A, A, A, A, 4, 8, 2, 128, 16, 10, 0, 1, 1, None, None) == -1
+    tc = lib.xs_paged_prefill_tc_ex
+    assert tc(A, A, A, A, A, 4, 8, 0, 8, 2, 128, 16, 10, 0.1, 2, 1, None, None) == -5
+    assert tc(None, A, A, A, A, 4, 8, 0, 8, 2, 128, 16, 10, 0.1, 1, 1, None, None) == -1

@@ -96,3 +96,49 @@ def test_bad_block_is_flagged_and_read_as_zeros():
     # Rows that only see page 0 are unaffected.
     ref = oracle.paged_prefill(q[:16], kc, vc, ids, 0, D ** -0.5)
     gh.assert_close(out[:16], ref, torch.bfloat16, what="rows before the bad page")
+
+
+@pytest.mark.parametrize("G,D", [(4, 128), (1, 64), (8, 128)], ids=["G4-D128", "G1-D64", "G8-D128"])
+def test_overlapped_chunks_match_oracle(G, D):
+    # XS_PREFILL_OVERLAP: every chunk's append and attention launched back to
+    # back with nothing between them on the stream (no host synchronisation,
+    # no event), so chunk c + 1's append and the start of its attention run
+    # beside chunk c's attention.  Ragged chunks at unaligned positions, the
+    # pool starting as NaN; every chunk's output against the oracle's, and the
+    # pages against the oracle's appends.
+    dev = gh.device()
+    g = torch.Generator().manual_seed(700 + 10 * G + D)
+    Hkv = 2
+    Hq = Hkv * G
+    chunks = [300, 37, 512, 1, 129, 256, 70, 1024]
+    ids, kc, vc = _setup(g, Hkv, G, D, sum(chunks), 5, fill_nan=True)
+    dkc, dvc, dids = kc.to(dev), vc.to(dev), ids.to(dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    outs, refs = [], []
+    start = 0
+    inputs = []
+    for T in chunks:
+        ks = torch.randn(Hkv, T, D, generator=g).to(torch.bfloat16)
+        vs = torch.randn(Hkv, T, D, generator=g).to(torch.bfloat16)
+        q = torch.randn(T, Hq, D, generator=g).to(torch.bfloat16)
+        inputs.append((ks.to(dev), vs.to(dev), q.to(dev)))
+        kc, vc = oracle.prefill_append(ks, vs, kc, vc, ids, start)
+        refs.append(oracle.paged_prefill(q, kc, vc, ids, start, D ** -0.5))
+        outs.append(torch.full((T, Hq, D), float("nan"), dtype=torch.bfloat16, device=dev))
+        start += T
+    torch.cuda.synchronize()
+    start = 0
+    for (ks, vs, q), out, T in zip(inputs, outs, chunks):
+        ops.xs_prefill_append(ks, vs, dkc, dvc, dids, start, err_flag=err, overlap=True)
+        ops.xs_paged_prefill_tc(out, q, dkc, dvc, dids, start, D ** -0.5, err_flag=err,
+                                overlap=True)
+        start += T
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    start = 0
+    for out, ref, T in zip(outs, refs, chunks):
+        assert not torch.isnan(out).any(), f"NaN in the output of the chunk at {start}"
+        gh.assert_close(out, ref, torch.bfloat16, what=f"chunk at {start} (T={T})")
+        start += T
+    assert torch.equal(gh.int_view(dkc.cpu()), gh.int_view(kc))
+    assert torch.equal(gh.int_view(dvc.cpu()), gh.int_view(vc))
