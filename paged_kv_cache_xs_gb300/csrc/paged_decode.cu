@@ -1964,7 +1964,8 @@ __global__ void __launch_bounds__(kCluThreads, CluCfg<D, G>::kMinBlocks)
         const bool no_window = p.window == 0;
         const int pg_first = (r * p.P) / kBlock;
         int32_t id_early = 0;
-        if (no_window && lane < kCluStages && pg_first + lane < p.max_blocks)
+        if (no_window && lane < kCluStages && pg_first + lane < p.max_blocks &&
+            XS_BOUNDS(b < p.B && pg_first + lane >= 0, p.err_flag))
             id_early = p.block_tables[static_cast<int64_t>(b) * p.table_stride + pg_first + lane];
         const int n = seq_len(p, b, r == 0 && g == 0 && lane == 0);
         n_seq = n;
@@ -1988,8 +1989,8 @@ __global__ void __launch_bounds__(kCluThreads, CluCfg<D, G>::kMinBlocks)
             return id;
         };
         auto load_id = [&](int i) {
-            return i < np ? check_id(p.block_tables[static_cast<int64_t>(b) * p.table_stride + pg0 + i])
-                          : 0;
+            if (i >= np || !XS_BOUNDS(pg0 + i >= 0 && pg0 + i < p.max_blocks, p.err_flag)) return 0;
+            return check_id(p.block_tables[static_cast<int64_t>(b) * p.table_stride + pg0 + i]);
         };
         int my_last = -1;  // the last page this lane issued (its stage's last phase)
         auto issue = [&](int i, int32_t id) {
@@ -2016,9 +2017,11 @@ __global__ void __launch_bounds__(kCluThreads, CluCfg<D, G>::kMinBlocks)
             // of the last page; then the generic-proxy writes are ordered
             // before the tensor copy that reads the page.
             constexpr int kChunks = C::kRowBytes / 16;
-            const int32_t lid = last < kCluStages ? __shfl_sync(0xffffffffu, id0, last)
-                                                  : p.block_tables[static_cast<int64_t>(b) *
-                                                                       p.table_stride + pg0 + last];
+            const bool in_table = XS_BOUNDS(pg0 + last < p.max_blocks && b < p.B, p.err_flag);
+            const int32_t lid = !in_table ? -1
+                                : last < kCluStages ? __shfl_sync(0xffffffffu, id0, last)
+                                                    : p.block_tables[static_cast<int64_t>(b) *
+                                                                         p.table_stride + pg0 + last];
             const bool ok_id = lid >= 0 && lid < p.num_blocks;
             const int64_t row = static_cast<int64_t>(b) * p.Hkv + g;
             const int64_t dst =
@@ -2075,10 +2078,11 @@ __global__ void __launch_bounds__(kCluThreads, CluCfg<D, G>::kMinBlocks)
             static_cast<const unsigned char *>(p.q) +
             ((static_cast<int64_t>(b) * p.Hq + static_cast<int64_t>(g) * G + (grp < G ? grp : 0)) *
              C::kRowBytes));
+        const bool q_in = grp < G && XS_BOUNDS((g + 1) * G <= p.Hq && b < p.B, p.err_flag);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
-            qa[ks][0] = grp < G ? qrow[8 * ks + tq] : 0u;
-            qa[ks][1] = grp < G ? qrow[8 * ks + 4 + tq] : 0u;
+            qa[ks][0] = q_in ? qrow[8 * ks + tq] : 0u;
+            qa[ks][1] = q_in ? qrow[8 * ks + 4 + tq] : 0u;
         }
         const int n = seq_len(p, b, false);
         n_seq = n;
@@ -2204,7 +2208,7 @@ __global__ void __launch_bounds__(kCluThreads, CluCfg<D, G>::kMinBlocks)
             for (int o = 1; o < 16; o <<= 1)
 #pragma unroll
                 for (int e = 0; e < 5; ++e) s[e] += __shfl_xor_sync(0xffffffffu, s[e], o);
-            if (valid && j == 0) {
+            if (valid && j == 0 && XS_BOUNDS(g * G + h < p.Hq && b < p.B, p.err_flag)) {
                 float den = s[0];
                 if (p.sinks)
                     den += fast_exp2(Elem<__nv_bfloat16>::to_f32(
