@@ -30,7 +30,10 @@
 //    two CTAs per SM, each Q K^T instruction read 6 KB of shared-memory
 //    operands for 128 x 64 x 16 MACs: 681 / 825 TFLOP/s on the 8K / 32K
 //    chunked prefills; 128-key tiles read 8 KB for twice the MACs: 809 / 986.)
-//  * Warps 2-9 (softmax, four per Q tile; warp w reads TMEM lanes
+//  * Warps 2-3 idle: warpgroup 0 gives up registers to the softmax
+//    warpgroups with setmaxnreg (80 a thread there, 208 in the softmax), so
+//    nothing spills.
+//  * Warps 4-11 (softmax, four per Q tile; warp w reads TMEM lanes
 //    32*(w%4)..+31, one row per thread): load the row of S, causal mask
 //    (diagonal tiles only), row max (8 chains of three-input maxima),
 //    P = 2^(s - m) in base 2 (arguments and sums as packed fp32x2
@@ -59,7 +62,15 @@ constexpr int kQTiles = 2;               // Q tiles per CTA, one softmax warp gr
 constexpr int kKeys = 128;               // keys per tile: N of Q K^T, K of P V
 constexpr int kPagesPerTile = kKeys / kBlock;
 constexpr int kStages = 2;               // depth of the K and V rings
-constexpr int kThreads = 64 + 128 * kQTiles;  // TMA warp, MMA warp, 4 softmax warps per Q tile
+// Warpgroup 0: the TMA warp, the MMA warp and two idle warps; then one
+// warpgroup of 4 softmax warps per Q tile.
+constexpr int kThreads = 128 + 128 * kQTiles;
+// Registers a thread: at launch (65536 / kThreads, rounded down to 8), then
+// moved from warpgroup 0 to the softmax warpgroups (setmaxnreg); the shares
+// add up to the launch's total.
+constexpr int kRegsLaunch = 168, kRegsCtl = 96, kRegsSoftmax = 200;
+static_assert(128 * kRegsCtl + 128 * kQTiles * kRegsSoftmax <= kThreads * kRegsLaunch,
+              "register split exceeds the launch's registers");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kGroupCols = 256;     // per Q tile: S 128 (P written over its first 64), O 128
 constexpr uint32_t kColS = 0, kColP = 0, kColO = 128;
@@ -270,161 +281,167 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     auto aborted = [&]() { return *static_cast<volatile int *>(&s_abort) != 0; };
 
-    if (warp == 0) {
-        // ============================================================== TMA
-        int issued = 0;
-        if (lane == 0) {
-            mbar_arrive_expect_tx(q_full, C::kQBytes);
-            for (int qi = 0; qi < kQTiles; ++qi)
-                for (int h = 0; h < C::kHalves; ++h)
-                    tma_load_3d(smem_addr(qs + qi * C::kQTile + h * C::kQHalf), &tmq, 64 * h,
-                                g * G, tok0 + qi * kTq, q_full);
-        }
-        // K runs one tile ahead of V: K(t + 1) is issued before V(t), so the
-        // next Q K^T never queues behind a V slot that P V still holds.
-        auto page_row = [&](int kt) {
-            int row = p.oob_row;
-            const int pg = kt * kPagesPerTile + lane;
-            if (lane < kPagesPerTile && pg < npages && XS_BOUNDS(pg < p.n_ids, p.err_flag)) {
-                const int32_t blk = p.block_ids[pg];
-                if (blk < 0 || blk >= p.num_blocks)
-                    raise_flag(p.err_flag, XS_FLAG_BAD_BLOCK);  // read as zeros
-                else
-                    row = (blk * p.Hkv + g) * kBlock;
-            }
-            return row;
-        };
-        // With p.early, the first tile that holds a position from start on
-        // (this chunk's rows, which the previous launch appends) waits for
-        // that launch, and the next launch may start once it has.
-        bool waited = !p.early;
-        auto gate = [&](int kt) {
-            if (!waited && (kt + 1) * kKeys > p.start) {
-                griddep_wait();
-                griddep_launch_dependents();
-                waited = true;
-            }
-        };
-        auto issue = [&](int kt, int which, int row) {
-            gate(kt);
-            const int s = kt % kStages;
-            uint64_t *emp = which ? &v_empty[s] : &k_empty[s];
-            uint64_t *ful = which ? &v_full[s] : &k_full[s];
-            bool ok = true;
-            if (lane == 0) {
-                ok = mbar_wait_bounded(emp, ((kt / kStages) & 1) ^ 1, kWaitLimitNs) && !aborted();
-                if (ok) mbar_arrive_expect_tx(ful, C::kTile);
-            }
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (ok && lane < kPagesPerTile) {
-                unsigned char *base = sm + (which ? C::kVOff : C::kKOff) + s * C::kTile;
-                for (int h = 0; h < C::kHalves; ++h)
-                    tma_load_3d(smem_addr(base + h * C::kKVHalf + lane * kBlock * 128),
-                                which ? &tmv : &tmk, 0, row, h, ful);
-            }
-            return ok;
-        };
-        int row_next = ntiles > 0 ? page_row(0) : 0;
-        bool ok = ntiles == 0 || issue(0, 0, row_next);
-        for (int kt = 0; ok && kt < ntiles; ++kt) {
-            const int row = row_next;
-            if (kt + 1 < ntiles) {
-                row_next = page_row(kt + 1);
-                ok = issue(kt + 1, 0, row_next);
-            }
-            ok = ok && issue(kt, 1, row);
-            if (ok) ++issued;
-        }
-        if (!ok && lane == 0) abort_now();
-        gate(ntiles);  // (every launch waits once, whatever it issued)
-        // Let the copies this CTA issued land before it can exit.
-        if (lane == 0) {
-            mbar_wait_bounded(q_full, 0, kWaitLimitNs);
-            // (K may be one tile ahead of V.)
-            for (int kt = max(0, issued - kStages); kt < min(ntiles, issued + 1); ++kt)
-                mbar_wait_bounded(&k_full[kt % kStages], (kt / kStages) & 1, kWaitLimitNs);
-            for (int kt = max(0, issued - kStages); kt < issued; ++kt)
-                mbar_wait_bounded(&v_full[kt % kStages], (kt / kStages) & 1, kWaitLimitNs);
-        }
-    } else if (warp == 1) {
-        // ============================================================== MMA
-        // Per Q tile the softmax writes P(t) over the first half of S(t) in
-        // TMEM, so the MMA thread issues, per Q tile, P V(t) and then S(t + 1)
-        // into the same columns: the tensor pipe executes a thread's MMAs in
-        // order, so P V(t) has read P before S(t + 1) overwrites it, and when
-        // S(t + 1) is complete so is P V(t).  The two Q tiles alternate: the
-        // tensor cores run one tile's P V and next scores while the other
-        // tile's softmax works.  One staged K or V tile serves both Q tiles.
-        if (lane == 0) {
-            const uint32_t qaddr = smem_addr(qs);
-            int nt_q[kQTiles];
-#pragma unroll
-            for (int qi = 0; qi < kQTiles; ++qi) nt_q[qi] = tile_ntiles(qi);
-            auto issue_s = [&](int qi, int kt) {
-                const uint32_t kaddr = smem_addr(sm + C::kKOff + (kt % kStages) * C::kTile);
-                const uint32_t qa = qaddr + qi * C::kQTile;
-#pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks)
-                    umma_ss(tmem + qi * kGroupCols + kColS,
-                            smem_desc(qa + (ks >> 2) * C::kQHalf + 32 * (ks & 3), 16, 1024),
-                            smem_desc(kaddr + (ks >> 2) * C::kKVHalf + 32 * (ks & 3), 16, 1024),
-                            C::kIdS, ks > 0);
-                umma_commit(s_full(qi));
-            };
-            auto issue_pv = [&](int qi, int kt) {
-                const uint32_t vaddr = smem_addr(sm + C::kVOff + (kt % kStages) * C::kTile);
-                const uint32_t cols = tmem + qi * kGroupCols;
-#pragma unroll
-                for (int kk = 0; kk < kKeys / 16; ++kk)
-                    umma_ts(cols + kColO, cols + kColP + 8 * kk,
-                            smem_desc(vaddr + 2048 * kk, C::kKVHalf, 1024), C::kIdPV,
-                            kt > 0 || kk > 0);
-                umma_commit(pv_done(qi));
-            };
-            bool ok = ntiles == 0 || (mbar_wait_bounded(q_full, 0, kWaitLimitNs) &&
-                                      mbar_wait_bounded(&k_full[0], 0, kWaitLimitNs));
-            if (ok && ntiles > 0) {
-                tc_fence_after();
+    if (warp < 4) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsCtl));
+        if (warp == 0 || warp == 3) {
+            // ============================================================== TMA
+            // Warp 0 loads Q and the K tiles, warp 3 the V tiles: each streams
+            // its ring on its own, a tile as soon as its slot is free.
+            const int which = warp == 3;  // 0: K, 1: V
+            if (which == 0 && lane == 0) {
+                mbar_arrive_expect_tx(q_full, C::kQBytes);
                 for (int qi = 0; qi < kQTiles; ++qi)
-                    if (nt_q[qi] > 0) issue_s(qi, 0);
-                umma_commit(&k_empty[0]);
+                    for (int h = 0; h < C::kHalves; ++h)
+                        tma_load_3d(smem_addr(qs + qi * C::kQTile + h * C::kQHalf), &tmq, 64 * h,
+                                    g * G, tok0 + qi * kTq, q_full);
             }
+            auto page_row = [&](int kt) {
+                int row = p.oob_row;
+                const int pg = kt * kPagesPerTile + lane;
+                if (lane < kPagesPerTile && pg < npages && XS_BOUNDS(pg < p.n_ids, p.err_flag)) {
+                    const int32_t blk = p.block_ids[pg];
+                    if (blk < 0 || blk >= p.num_blocks)
+                        raise_flag(p.err_flag, XS_FLAG_BAD_BLOCK);  // read as zeros
+                    else
+                        row = (blk * p.Hkv + g) * kBlock;
+                }
+                return row;
+            };
+            // With p.early, the first tile that holds a position from start on
+            // (this chunk's rows, which the previous launch appends) waits for
+            // that launch, and (warp 0) the next launch may start once it has.
+            bool waited = !p.early;
+            auto gate = [&](int kt) {
+                if (!waited && (kt + 1) * kKeys > p.start) {
+                    griddep_wait();
+                    if (which == 0) griddep_launch_dependents();
+                    waited = true;
+                }
+            };
+            uint64_t *full = which ? v_full : k_full;
+            uint64_t *empty = which ? v_empty : k_empty;
+            auto issue = [&](int kt, int row) {
+                gate(kt);
+                const int s = kt % kStages;
+                bool ok = true;
+                if (lane == 0) {
+                    ok = mbar_wait_bounded(&empty[s], ((kt / kStages) & 1) ^ 1, kWaitLimitNs) &&
+                         !aborted();
+                    if (ok) mbar_arrive_expect_tx(&full[s], C::kTile);
+                }
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (ok && lane < kPagesPerTile) {
+                    unsigned char *base = sm + (which ? C::kVOff : C::kKOff) + s * C::kTile;
+                    for (int h = 0; h < C::kHalves; ++h)
+                        tma_load_3d(smem_addr(base + h * C::kKVHalf + lane * kBlock * 128),
+                                    which ? &tmv : &tmk, 0, row, h, &full[s]);
+                }
+                return ok;
+            };
+            int issued = 0;
+            bool ok = true;
             for (int kt = 0; ok && kt < ntiles; ++kt) {
-                const int s = kt % kStages, s1 = (kt + 1) % kStages;
-                bool v_ready = false, k_ready = false;
-                for (int qi = 0; ok && qi < kQTiles; ++qi) {
-                    if (kt >= nt_q[qi]) continue;
-                    ok = mbar_wait_bounded(p_full(qi), kt & 1, kWaitLimitNs) && !aborted();
-                    if (ok && !v_ready) {
-                        ok = mbar_wait_bounded(&v_full[s], (kt / kStages) & 1, kWaitLimitNs);
-                        v_ready = true;
+                ok = issue(kt, page_row(kt));
+                if (ok) ++issued;
+            }
+            if (!ok && lane == 0) abort_now();
+            gate(ntiles);  // (every launch waits once, whatever it issued)
+            // Let the copies this warp issued land before the CTA can exit.
+            if (lane == 0) {
+                if (which == 0) mbar_wait_bounded(q_full, 0, kWaitLimitNs);
+                for (int kt = max(0, issued - kStages); kt < issued; ++kt)
+                    mbar_wait_bounded(&full[kt % kStages], (kt / kStages) & 1, kWaitLimitNs);
+            }
+        } else if (warp == 1) {
+            // ============================================================== MMA
+            // Per Q tile the softmax writes P(t) over the first half of S(t) in
+            // TMEM, so the MMA thread issues, per Q tile, P V(t) and then S(t + 1)
+            // into the same columns: the tensor pipe executes a thread's MMAs in
+            // order, so P V(t) has read P before S(t + 1) overwrites it, and when
+            // S(t + 1) is complete so is P V(t).  The two Q tiles alternate: the
+            // tensor cores run one tile's P V and next scores while the other
+            // tile's softmax works.  One staged K or V tile serves both Q tiles.
+            if (lane == 0) {
+                const uint32_t qaddr = smem_addr(qs);
+                int nt_q[kQTiles];
+#pragma unroll
+                for (int qi = 0; qi < kQTiles; ++qi) nt_q[qi] = tile_ntiles(qi);
+                // Descriptors of the Q tiles and the K and V slots, built once:
+                // an operand's start address is (address >> 4) in the low 14
+                // bits, so a step within a tile adds (offset >> 4) (no carry:
+                // shared addresses stay below 256 KB).
+                uint64_t dq[kQTiles], dk[kStages], dv[kStages];
+#pragma unroll
+                for (int qi = 0; qi < kQTiles; ++qi)
+                    dq[qi] = smem_desc(qaddr + qi * C::kQTile, 16, 1024);
+#pragma unroll
+                for (int st = 0; st < kStages; ++st) {
+                    dk[st] = smem_desc(smem_addr(sm + C::kKOff + st * C::kTile), 16, 1024);
+                    dv[st] = smem_desc(smem_addr(sm + C::kVOff + st * C::kTile), C::kKVHalf, 1024);
+                }
+                static_assert(C::kQHalf == C::kKVHalf, "Q and K D-halves step alike");
+                auto issue_s = [&](int qi, int kt) {
+                    const uint64_t kd = (kt % kStages) ? dk[1] : dk[0];
+                    const uint64_t qd = qi ? dq[1] : dq[0];
+#pragma unroll
+                    for (int ks = 0; ks < D / 16; ++ks) {
+                        const uint64_t off = static_cast<uint64_t>(
+                            ((ks >> 2) * C::kQHalf + 32 * (ks & 3)) >> 4);
+                        umma_ss(tmem + qi * kGroupCols + kColS, qd + off, kd + off, C::kIdS,
+                                ks > 0);
+                    }
+                    umma_commit(s_full(qi));
+                };
+                auto issue_pv = [&](int qi, int kt) {
+                    const uint64_t vd = (kt % kStages) ? dv[1] : dv[0];
+                    const uint32_t cols = tmem + qi * kGroupCols;
+#pragma unroll
+                    for (int kk = 0; kk < kKeys / 16; ++kk)
+                        umma_ts(cols + kColO, cols + kColP + 8 * kk,
+                                vd + static_cast<uint64_t>((2048 * kk) >> 4), C::kIdPV,
+                                kt > 0 || kk > 0);
+                    umma_commit(pv_done(qi));
+                };
+                bool ok = ntiles == 0 || (mbar_wait_bounded(q_full, 0, kWaitLimitNs) &&
+                                          mbar_wait_bounded(&k_full[0], 0, kWaitLimitNs));
+                if (ok && ntiles > 0) {
+                    tc_fence_after();
+                    for (int qi = 0; qi < kQTiles; ++qi)
+                        if (nt_q[qi] > 0) issue_s(qi, 0);
+                    umma_commit(&k_empty[0]);
+                }
+                // V(kt) and K(kt + 1) have landed once P(kt) is published.  A
+                // V slot is released after the step's last P V, before that
+                // tile's next scores; a K slot after both tiles' S(kt + 1).
+                for (int kt = 0; ok && kt < ntiles; ++kt) {
+                    const int s = kt % kStages, s1 = (kt + 1) % kStages;
+                    const int last_v = kt < nt_q[kQTiles - 1] ? kQTiles - 1 : 0;
+                    bool k_used = false;
+                    for (int qi = 0; ok && qi < kQTiles; ++qi) {
+                        if (kt >= nt_q[qi]) continue;
+                        ok = mbar_wait_bounded(p_full(qi), kt & 1, kWaitLimitNs) && !aborted();
+                        if (!ok) break;
+                        tc_fence_after();
+                        issue_pv(qi, kt);
+                        if (qi == last_v) umma_commit(&v_empty[s]);
+                        if (kt + 1 < nt_q[qi]) {
+                            issue_s(qi, kt + 1);
+                            k_used = true;
+                        }
                     }
                     if (!ok) break;
-                    tc_fence_after();
-                    issue_pv(qi, kt);
-                    if (kt + 1 < nt_q[qi]) {
-                        if (!k_ready) {
-                            ok = mbar_wait_bounded(&k_full[s1], ((kt + 1) / kStages) & 1,
-                                                   kWaitLimitNs);
-                            k_ready = true;
-                            if (!ok) break;
-                            tc_fence_after();
-                        }
-                        issue_s(qi, kt + 1);
-                    }
+                    if (k_used) umma_commit(&k_empty[s1]);
                 }
-                if (!ok) break;
-                umma_commit(&v_empty[s]);
-                if (k_ready) umma_commit(&k_empty[s1]);
+                if (!ok) abort_now();
+                // Every MMA issued has completed before the CTA leaves (and TMEM is freed).
+                umma_commit(mma_idle);
+                mbar_wait_bounded(mma_idle, 0, kWaitLimitNs);
             }
-            if (!ok) abort_now();
-            // Every MMA issued has completed before the CTA leaves (and TMEM is freed).
-            umma_commit(mma_idle);
-            mbar_wait_bounded(mma_idle, 0, kWaitLimitNs);
         }
     } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
         // ========================================================== softmax
-        const int qi = (warp - 2) >> 2;    // Q tile of this warp group
+        const int qi = (warp - 4) >> 2;    // Q tile of this warp group
         const int quad = warp & 3;         // TMEM lanes 32 * quad .. + 31 (warp rank in its warpgroup)
         const int r = 32 * quad + lane;    // this thread's row = TMEM lane
         const int tl = qi * kTq + r / G;   // query token within the CTA
@@ -532,6 +549,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                         make_uint4(0u, 0u, 0u, 0u);
                 }
                 fence_proxy_async_shared();
+            }
+            // The tiles this Q tile's next MMAs read, V(kt) and K(kt + 1), have
+            // landed before P(kt) is published, so the MMA thread waits for P
+            // alone: a barrier wait in the thread that issues the MMAs costs
+            // ~300 cycles of an idle tensor pipe, even on a completed phase.
+            // (Their copies were issued once every MMA that used the slots
+            // before was complete, which S(kt) being here implies.)
+            if (quad == 2) {
+                bool landed = true;
+                if (lane == 0)
+                    landed = mbar_wait_bounded(&v_full[kt % kStages], (kt / kStages) & 1,
+                                               kWaitLimitNs) &&
+                             (kt + 1 >= my_ntiles ||
+                              mbar_wait_bounded(&k_full[(kt + 1) % kStages],
+                                                ((kt + 1) / kStages) & 1, kWaitLimitNs));
+                ok = __all_sync(0xffffffffu, landed);
+                if (!ok) break;
             }
             tc_fence_before();
             __syncwarp();
