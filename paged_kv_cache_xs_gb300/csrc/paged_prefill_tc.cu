@@ -10,11 +10,12 @@
 //    row is a (query token, query head) pair: 128 / G tokens x the G query
 //    heads of the group, so every K/V byte staged serves all G heads of both
 //    tiles.  Row r of tile i is TMEM lane r of tile i's 256 columns.
-//  * Warp 0 (TMA): Q once (one 3-D tensor copy per tile and 64-wide D half,
-//    box [64, G heads, 128/G tokens]); then 128-key K and V tiles (8 pages)
-//    into two 2-slot rings (a K slot frees after both tiles' Q K^T, a V slot
-//    after both P V), one 3-D copy per page and D half from a tensor map over
-//    the pool.  Every box is 128-byte swizzled, so a D half of a tile is the
+//  * Warps 0 and 3 (TMA): warp 0 copies Q once (one 3-D tensor copy per
+//    tile and 64-wide D half, box [64, G heads, 128/G tokens]) and the
+//    128-key K tiles (8 pages), warp 3 the V tiles, each into its own 2-slot
+//    ring as soon as a slot is free (a K slot frees after both tiles'
+//    Q K^T, a V slot after the step's last P V), one 3-D copy per page and
+//    D half from a tensor map over the pool.  Every box is 128-byte swizzled, so a D half of a tile is the
 //    canonical K-major layout (8-row groups 1024 B apart).  Pages past the
 //    last key are requested at a row beyond the pool and arrive as zeros.
 //  * Warp 1 (one thread): S = Q K^T with tcgen05.mma (M=128, N=128, K=16 per
@@ -26,13 +27,18 @@
 //    the thread issues P V(t) and then S(t + 1) into the same columns - the
 //    tensor pipe runs a thread's MMAs in order - and the two Q tiles
 //    alternate: while one tile's softmax works, the tensor cores run the
-//    other tile's P V and next scores.  (With 64-key tiles, one Q tile and
+//    other tile's P V and next scores.  A 128 x 128 x 16 MMA is 64 cycles
+//    of tensor pipe and about as long for one thread to issue, and every
+//    barrier wait in that thread leaves the pipe idle for ~300 cycles, so
+//    it waits for P alone (the softmax checks that V(t) and K(t + 1) have
+//    landed before publishing P) and builds its descriptors once.  (With
+//    64-key tiles, one Q tile and
 //    two CTAs per SM, each Q K^T instruction read 6 KB of shared-memory
 //    operands for 128 x 64 x 16 MACs: 681 / 825 TFLOP/s on the 8K / 32K
 //    chunked prefills; 128-key tiles read 8 KB for twice the MACs: 809 / 986.)
-//  * Warps 2-3 idle: warpgroup 0 gives up registers to the softmax
-//    warpgroups with setmaxnreg (80 a thread there, 208 in the softmax), so
-//    nothing spills.
+//  * Warp 2 idle.  Warpgroup 0 gives up registers to the softmax
+//    warpgroups with setmaxnreg (kRegsCtl a thread there, kRegsSoftmax in
+//    the softmax), so nothing spills at D = 128.
 //  * Warps 4-11 (softmax, four per Q tile; warp w reads TMEM lanes
 //    32*(w%4)..+31, one row per thread): load the row of S, causal mask
 //    (diagonal tiles only), row max (8 chains of three-input maxima),
