@@ -676,11 +676,15 @@ def run_ours(args, rank, world, local, dist):
         for idx in (0, 1, 2, 3):
             row = decode_row(args, idx, rank, world, local, dist)
             rows[row["workload"]] = row
-        pre = prefill_measure(args, rank, world, local, dist, tokens=8192, chunk=1024,
-                              steps=args.row_steps, load_seconds=args.row_load_seconds,
-                              cpu_seconds=args.row_cpu_seconds)
-        if pre is not None:
-            rows[pre["config"]["workload"]] = pre
+        # The chunked prefills: 8K tokens in 1K chunks, and 32K in 4K chunks
+        # (~7 ms a prefill: fewer timed steps, each still after an L2 flush).
+        for tokens, chunk, steps in ((8192, 1024, args.row_steps),
+                                     (32768, 4096, max(10, args.row_steps // 10))):
+            pre = prefill_measure(args, rank, world, local, dist, tokens=tokens, chunk=chunk,
+                                  steps=steps, load_seconds=args.row_load_seconds,
+                                  cpu_seconds=args.row_cpu_seconds)
+            if pre is not None:
+                rows[pre["config"]["workload"]] = pre
         if line is not None:
             line["rows"] = rows
     if line is not None:
